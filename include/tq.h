@@ -1,0 +1,232 @@
+/*
+ * tq.h -- C ABI of the rotated + quantized KV-cache library (GB300, sm_103a).
+ *
+ * The method (web pages on the subject, cited by page title and section):
+ *   - "turboquant-mlx" (TurboQuant-MLX v2.0 README), "Walsh-Hadamard Rotation":
+ *     each key/value head vector is rotated by the SRHT R = D H D / sqrt(d)
+ *     (D a seeded sign diagonal, H the Sylvester Hadamard matrix), O(d log d).
+ *   - "TurboMOQ" (turboMOQ README), "Architecture": keys are quantized on a
+ *     symmetric grid, values with a Gaussian Lloyd-Max codebook, 1-8 bits per
+ *     head, with an optional 1-bit QJL sign sketch of the key residual ("QJL
+ *     residual correction (sub-2-bit)"); "Progressive temporal tiering": token
+ *     ranges by age carry different bit widths (16 = kept in fp16).
+ *   - "turboquant-mlx", "FP16 Attention Sinks" and "Dynamic Chunk Buffering":
+ *     the first 128 tokens stay fp16; new tokens are compressed 64 at a time.
+ *   - "turboquant-mlx" skill note, "Optimisations Metal": attention runs on the
+ *     compressed cache with the inverse transform pulled out of the V sum.
+ *
+ * Conventions for every entry point:
+ *   - Return value: TQ_OK (0) or a negative tq_status.  Arguments are checked on
+ *     the host before anything is launched; nothing aborts or throws.
+ *   - Device pointers are caller-owned CUDA device memory; the library never
+ *     allocates or frees device memory.  Host pointers are caller-owned too.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Launches are asynchronous on it; errors of kernel execution surface at
+ *     the caller's next synchronisation.  TQ_ERR_CUDA reports a launch error
+ *     whose cudaError_t value tq_last_cuda_error() returns.
+ *   - fp16 data are IEEE binary16 bit patterns (uint16_t / __half).
+ *   - Device buffers must be 16-byte aligned (TQ_ERR_ALIGN otherwise).
+ *   - Kernels support head_dim = 128 and GQA group sizes 1, 2 and 4 (query
+ *     heads per KV head); other shapes return TQ_ERR_UNSUPPORTED.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_MAX_HEADS 16    /* KV heads per layer */
+#define TQ_MAX_SEGMENTS 8  /* segments per layer in one decode call */
+#define TQ_MAX_HEAD_DIM 1024
+
+typedef int tq_status;
+#define TQ_OK 0
+#define TQ_ERR_ARG (-1)         /* a NULL / out-of-range argument */
+#define TQ_ERR_UNSUPPORTED (-2) /* a valid shape the kernels do not implement */
+#define TQ_ERR_ALIGN (-3)       /* a device pointer or stride is not 16-byte aligned */
+#define TQ_ERR_SIZE (-4)        /* a buffer is too small (workspace, capacity) */
+#define TQ_ERR_CUDA (-5)        /* a CUDA runtime call failed; see tq_last_cuda_error */
+
+/* Human-readable name of a status.  Never NULL. */
+const char *tq_status_string(tq_status s);
+/* cudaError_t value of the last TQ_ERR_CUDA returned on this host thread. */
+int tq_last_cuda_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int tq_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Rotation ("turboquant-mlx", "Walsh-Hadamard Rotation":                      */
+/* WalshHadamardRotation(head_dim, seed)).                                     */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int head_dim;          /* d: a power of two, 16..1024 */
+    uint64_t seed;         /* layer l conventionally uses seed + l */
+    uint32_t sign_bits[TQ_MAX_HEAD_DIM / 32]; /* bit i set <=> D_i = -1 */
+} tq_rotation;
+
+/* Fill *rot (caller-owned, plain data) with the sign diagonal of
+ * R = D H D / sqrt(d): D_i = -1 iff the top bit of the i-th SplitMix64 output
+ * of `seed` is set.  R is symmetric and R R = I.  TQ_ERR_ARG on a NULL rot or a
+ * head_dim that is not a power of two in [16, 1024]. */
+tq_status tq_make_rotation(int head_dim, uint64_t seed, tq_rotation *rot);
+
+/* ------------------------------------------------------------------------ */
+/* Value codebook ("TurboMOQ", "Architecture": Lloyd-Max codebook -> grid      */
+/* quantize).  Gaussian N(0,1) Lloyd-Max quantizer with 2^bits levels, fitted  */
+/* in binary64 by Lloyd's iteration from the quantiles (k + 1/2)/2^bits until   */
+/* no level moves by more than 1e-13, then rounded to binary32.  Thresholds are  */
+/* midpoints of adjacent levels (the middle one is exactly 0).                 */
+/* ------------------------------------------------------------------------ */
+/* centroids: 2^bits floats (host); thresholds: 2^bits - 1 floats (host, may be
+ * NULL).  Results are cached per bit width after the first call (the 8-bit fit
+ * takes about a second).  TQ_ERR_ARG for bits outside 1..8 or NULL centroids. */
+tq_status tq_fit_codebook(int bits, float *centroids, float *thresholds);
+
+/* ------------------------------------------------------------------------ */
+/* QJL projection ("TurboMOQ", "QJL residual correction (sub-2-bit)":          */
+/* QJLConfig(head_dim, jl_dim); "turboquant-mlx", "RaBitQ vs QJL correction").  */
+/* ------------------------------------------------------------------------ */
+/* Fill S (host, jl_dim x head_dim floats, row-major) with N(0,1) entries:
+ * SplitMix64(seed) words in pairs -> u1 = ((w1>>11)+1) 2^-53, u2 = (w2>>11) 2^-53
+ * -> Box-Muller (binary64) -> binary32.  The caller copies S to device memory
+ * it owns and passes that copy to tq_compress / tq_decode_attention.
+ * jl_dim must be a multiple of 32 and at most 1024 (kernels: jl_dim == 128). */
+tq_status tq_make_qjl(int head_dim, int jl_dim, uint64_t seed, float *S);
+
+/* ------------------------------------------------------------------------ */
+/* Packed segment layout (one layer, one token range with fixed bit widths).   */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int batch;         /* B */
+    int n_heads;       /* H (KV heads), 1..TQ_MAX_HEADS */
+    int head_dim;      /* d */
+    int capacity;      /* tokens the buffers are laid out for */
+    int jl_dim;        /* QJL sketch length (bits per key); used if any qjl[h] */
+    uint8_t kbits[TQ_MAX_HEADS]; /* per head, 1..8 */
+    uint8_t vbits[TQ_MAX_HEADS]; /* per head, 1..8 */
+    uint8_t qjl[TQ_MAX_HEADS];   /* per head, 0/1: 1-bit residual sketch of keys */
+} tq_segment_layout;
+
+/* Byte layout (all offsets are multiples of 16 when the bases are aligned):
+ *   record sizes rk(h) = d*kbits[h]/8, rv(h) = d*vbits[h]/8 bytes;
+ *   kcodes byte offset of (b, h, t) = b*cap*sum_h rk + cap*sum_{h'<h} rk(h')
+ *                                     + t*rk(h)      (vcodes likewise with rv);
+ *   code i of a vector occupies bits [b*i, b*i+b) of its record (LSB first);
+ *   kscale / vscale (float) index (b*H + h)*cap + t  (key: max|y|, value: RMS);
+ *   QJL heads ranked q(h) = #{h' < h : qjl[h']}, nq of them: qjl_signs byte
+ *   offset ((b*nq + q(h))*cap + t)*jl/8 (bit j LSB-first = sign of (S r)_j >= 0),
+ *   qjl_norm (float, ||r||_2) index (b*nq + q(h))*cap + t. */
+typedef struct {
+    size_t kcode_bytes, vcode_bytes, kscale_bytes, vscale_bytes, qjl_sign_bytes, qjl_norm_bytes;
+} tq_packed_sizes;
+
+/* Sizes of the six device buffers of a packed segment.  TQ_ERR_ARG on an
+ * invalid layout (bits outside 1..8, H outside 1..16, capacity < 0, ...). */
+tq_status tq_packed_size(const tq_segment_layout *layout, tq_packed_sizes *sizes);
+
+typedef struct {
+    void *kcodes, *vcodes;   /* device, sizes from tq_packed_size */
+    float *kscale, *vscale;  /* device */
+    void *qjl_signs;         /* device, may be NULL when no head uses QJL */
+    float *qjl_norm;         /* device, may be NULL when no head uses QJL */
+} tq_packed_bufs;
+
+/* ------------------------------------------------------------------------ */
+/* Compression (rotation -> per-vector scale -> quantize -> pack [-> QJL]).     */
+/* ------------------------------------------------------------------------ */
+/* K, V: device fp16, element (b, h, t, i) at b*stride_b + h*stride_h +
+ * t*stride_t + i (strides in elements; stride_t*2 and every base must be
+ * 16-byte aligned).  Compresses n_tokens tokens into positions
+ * [t_begin, t_begin + n_tokens) of the packed segment (chunked compression
+ * appends with t_begin = tokens already stored).  qjl_S: device jl_dim x
+ * head_dim floats from tq_make_qjl, required iff some qjl[h] is set.
+ * All arithmetic is IEEE binary32 in a fixed order, so the codes are a pure
+ * function of the input:
+ *   y = binary32(1/sqrt(d)) * D (butterflies h = 1, 2, ..., d/2 of D x);
+ *   keys: m = max|y_i|, r = 1/m (0 if m = 0), code = clamp(floor((y r + 1) 2^(b-1)),
+ *         0, 2^b - 1);
+ *   values: sigma = sqrt(pairwise-tree sum of y_i^2 / d), r = 1/sigma (0 if 0),
+ *         code = #{k : thr_k < y r};
+ *   QJL: r_i = y_i - m*((code+1/2) 2^(1-b) - 1), sign bits of S r, ||r||_2.
+ * Returns TQ_ERR_SIZE if t_begin + n_tokens > capacity. */
+tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot,
+                      const float *qjl_S, const void *K, const void *V, int n_tokens,
+                      int64_t stride_b, int64_t stride_h, int64_t stride_t, int t_begin,
+                      const tq_packed_bufs *out, void *stream);
+
+/* Dequantize token positions [t_begin, t_begin + n_tokens) of a packed segment.
+ * k_rot / v_rot (device floats [B][H][n_tokens][d], either may be NULL): the
+ * rotated-space values binary32(m * level(code)) and binary32(sigma *
+ * centroid[code]).  k_orig / v_orig (may be NULL): the original-space vectors
+ * R applied to those (binary32; keys include no QJL term).  A debugging and
+ * parity aid: decode attention never materialises these. */
+tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *bufs,
+                        const tq_rotation *rot, int t_begin, int n_tokens, float *k_rot,
+                        float *v_rot, float *k_orig, float *v_orig, void *stream);
+
+/* Progressive tiers by token age ("TurboMOQ", "Progressive temporal tiering"):
+ * position p has age n_tokens-1-p; tier i holds ages [bound[i-1], bound[i])
+ * (bound[-1] = 0, bound[n_bounds] = infinity).  Writes tier i's position
+ * range [start[i], end[i]) for i = 0..n_bounds (empty tiers get start == end). */
+tq_status tq_age_tiers(int n_tokens, int n_bounds, const int *age_bounds, int *start,
+                       int *end);
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention over the compressed cache.                                 */
+/* ------------------------------------------------------------------------ */
+#define TQ_SEG_PACKED 0
+#define TQ_SEG_FP16 1
+
+typedef struct {
+    int kind;                  /* TQ_SEG_PACKED or TQ_SEG_FP16 */
+    int n_tokens;              /* tokens attended, 0..layout.capacity */
+    tq_segment_layout layout;  /* batch/n_heads/head_dim/capacity for both kinds;
+                                  bits and qjl for packed segments */
+    tq_packed_bufs packed;     /* TQ_SEG_PACKED */
+    const void *k16, *v16;     /* TQ_SEG_FP16: fp16 [B][H][capacity][d], unrotated */
+} tq_segment;
+
+typedef struct {
+    tq_rotation rot;           /* the layer's rotation (same D for K, V and q) */
+    int n_segments;            /* 0..TQ_MAX_SEGMENTS; order does not matter */
+    tq_segment seg[TQ_MAX_SEGMENTS];
+} tq_layer_view;
+
+/* Bytes of device workspace tq_decode_attention needs for these layers. */
+tq_status tq_decode_workspace_size(const tq_layer_view *layers, int n_layers, int batch,
+                                   int n_heads, int q_heads, int head_dim, size_t *bytes);
+
+/* out[l][b][j][:] = softmax_t(q_j . k_t / sqrt(d)) . v_t over every token of
+ * every segment of layer l, where query head j reads KV head j/(q_heads/n_heads)
+ * and, for packed tokens, k_t = R (yhat_k [+ rhat_QJL]) and v_t = R yhat_v.
+ * Computed without materialising k_t, v_t: q is rotated once, scores and the
+ * value sum run in the rotated space on the packed codes (split over token
+ * chunks with an online softmax), and one inverse rotation is applied to the
+ * merged value sum.  QJL heads add sqrt(pi/2)/jl * ||r|| * <S q', s> to q'.yhat.
+ * q: device fp16 [n_layers][batch][q_heads][d]; out: device float, same shape.
+ * qjl_S: device jl_dim x d floats, required iff a packed segment uses QJL.
+ * workspace: device, >= tq_decode_workspace_size bytes (TQ_ERR_SIZE otherwise).
+ * The call copies a small plan (host -> workspace) with cudaMemcpyAsync from
+ * pageable host memory, then launches four kernels on `stream`.  A layer with
+ * no tokens yields zeros. */
+tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int batch,
+                              int n_heads, int q_heads, int head_dim, const float *qjl_S,
+                              int jl_dim, const void *q, float *out, void *workspace,
+                              size_t ws_bytes, void *stream);
+
+/* Measurement hook: when both events are non-NULL, every later
+ * tq_decode_attention call on this host thread records `start` on its stream
+ * just before the split-K kernel over packed segments and `stop` just after it,
+ * so the caller can time that kernel alone with cudaEventElapsedTime.  Pass
+ * NULL, NULL to turn it off.  The events are cudaEvent_t handles owned by the
+ * caller; no effect on results. */
+tq_status tq_set_decode_kernel_events(void *start, void *stop);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

@@ -1,0 +1,614 @@
+// tq_host.cpp -- host side of the C ABI declared in include/tq.h: argument
+// checks, buffer layouts, the codebook fit, the QJL projection, the decode
+// planner and the kernel launches.  No device memory is allocated here.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "tq_internal.h"
+
+using namespace tqk;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+
+tq_status cuda_fail(cudaError_t e) {
+    g_last_cuda = static_cast<int>(e);
+    return TQ_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// SplitMix64 (Steele, Lea, Flood, OOPSLA 2014).
+struct SplitMix64 {
+    uint64_t state;
+    uint64_t next() {
+        state += 0x9E3779B97F4A7C15ull;
+        uint64_t z = state;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        return z ^ (z >> 31);
+    }
+};
+
+// ---------------------------------------------------------------- codebook fit
+// Gaussian Lloyd-Max quantizer ("TurboMOQ", "Architecture": values go through a
+// Lloyd-Max codebook), computed for N(0,1) in binary64.  The codebook is odd
+// symmetric, so the upper half is iterated: cell k of the upper half is
+// [b_k, b_{k+1}) with b at the midpoints of adjacent levels (b = 0 at the middle,
+// +inf at the top); its conditional mean is (phi(b_k) - phi(b_{k+1})) / (Q(b_k) -
+// Q(b_{k+1})) with Q the upper tail.  Start: the (k + 1/2)/n quantiles; stop
+// when the largest move is at most 1e-13.
+double upper_tail(double x) { return 0.5 * std::erfc(x * 0.70710678118654752440); }
+double density(double x) { return 0.39894228040143267794 * std::exp(-0.5 * x * x); }
+
+double tail_quantile(double p) {  // x with upper_tail(x) = p, by bisection
+    double lo = -40.0, hi = 40.0;
+    for (int i = 0; i < 200; ++i) {
+        const double mid = 0.5 * (lo + hi);
+        (upper_tail(mid) > p ? lo : hi) = mid;
+    }
+    return 0.5 * (lo + hi);
+}
+
+struct FittedCodebook {
+    bool ready = false;
+    std::vector<double> level, bound;  // full codebook, n levels and n-1 thresholds
+};
+
+std::mutex g_cb_mutex;
+FittedCodebook g_cb[9];
+
+const FittedCodebook &fit(int bits) {
+    std::lock_guard<std::mutex> lock(g_cb_mutex);
+    FittedCodebook &cb = g_cb[bits];
+    if (cb.ready) return cb;
+    const int n = 1 << bits, half = n / 2;
+    std::vector<double> up(half);  // levels half..n-1
+    for (int k = 0; k < half; ++k) up[k] = tail_quantile(1.0 - (half + k + 0.5) / n);
+    std::vector<double> edge(half + 1);
+    for (int sweep = 0; sweep < 1000000; ++sweep) {
+        edge[0] = 0.0;
+        for (int k = 1; k < half; ++k) edge[k] = 0.5 * (up[k - 1] + up[k]);
+        double move = 0.0;
+        for (int k = 0; k < half; ++k) {
+            const double a = edge[k];
+            double num, den;
+            if (k + 1 < half) {
+                const double b = edge[k + 1];
+                // phi(a) - phi(b) without cancellation for narrow cells
+                num = -density(a) * std::expm1(-0.5 * (b - a) * (b + a));
+                den = upper_tail(a) - upper_tail(b);
+            } else {
+                num = density(a);
+                den = upper_tail(a);
+            }
+            const double v = num / den;
+            move = std::fmax(move, std::fabs(v - up[k]));
+            up[k] = v;
+        }
+        if (move <= 1e-13) break;
+    }
+    cb.level.assign(n, 0.0);
+    for (int k = 0; k < half; ++k) {
+        cb.level[half + k] = up[k];
+        cb.level[half - 1 - k] = -up[k];
+    }
+    cb.bound.assign(n - 1, 0.0);
+    for (int k = 0; k + 1 < n; ++k) cb.bound[k] = 0.5 * (cb.level[k] + cb.level[k + 1]);
+    cb.bound[half - 1] = 0.0;
+    cb.ready = true;
+    return cb;
+}
+
+void fill_thresholds(float *flat, const uint8_t *bits, int H) {
+    for (int h = 0; h < H; ++h) {
+        const FittedCodebook &cb = fit(bits[h]);
+        for (int k = 0; k + 1 < (1 << bits[h]); ++k) flat[cb_off(bits[h]) + k] = static_cast<float>(cb.bound[k]);
+    }
+}
+
+void fill_centroids(float *flat, const uint8_t *bits, int H) {
+    for (int h = 0; h < H; ++h) {
+        const FittedCodebook &cb = fit(bits[h]);
+        for (int k = 0; k < (1 << bits[h]); ++k) flat[cb_off(bits[h]) + k] = static_cast<float>(cb.level[k]);
+    }
+}
+
+// ---------------------------------------------------------------- layouts
+tq_status check_layout(const tq_segment_layout *L, bool need_bits) {
+    if (!L) return TQ_ERR_ARG;
+    if (L->batch < 1 || L->n_heads < 1 || L->n_heads > TQ_MAX_HEADS || L->capacity < 0) return TQ_ERR_ARG;
+    if (!pow2(L->head_dim) || L->head_dim < 16 || L->head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
+    if (need_bits) {
+        bool any_qjl = false;
+        for (int h = 0; h < L->n_heads; ++h) {
+            if (L->kbits[h] < 1 || L->kbits[h] > 8 || L->vbits[h] < 1 || L->vbits[h] > 8) return TQ_ERR_ARG;
+            if (L->qjl[h] > 1) return TQ_ERR_ARG;
+            any_qjl |= L->qjl[h] != 0;
+        }
+        if (any_qjl && (L->jl_dim < 32 || L->jl_dim > 1024 || L->jl_dim % 32)) return TQ_ERR_ARG;
+    }
+    return TQ_OK;
+}
+
+struct Offsets {
+    uint32_t kblock = 0, vblock = 0;
+    uint32_t koff[TQ_MAX_HEADS] = {}, voff[TQ_MAX_HEADS] = {};
+    int8_t qrank[TQ_MAX_HEADS] = {};
+    int nq = 0;
+};
+
+Offsets offsets(const tq_segment_layout *L) {
+    Offsets o;
+    size_t k = 0, v = 0;
+    for (int h = 0; h < L->n_heads; ++h) {
+        o.koff[h] = static_cast<uint32_t>(k);
+        o.voff[h] = static_cast<uint32_t>(v);
+        k += static_cast<size_t>(L->capacity) * L->head_dim * L->kbits[h] / 8;
+        v += static_cast<size_t>(L->capacity) * L->head_dim * L->vbits[h] / 8;
+        o.qrank[h] = L->qjl[h] ? static_cast<int8_t>(o.nq++) : static_cast<int8_t>(-1);
+    }
+    o.kblock = static_cast<uint32_t>(k);
+    o.vblock = static_cast<uint32_t>(v);
+    return o;
+}
+
+bool fits_u32(const tq_segment_layout *L) {
+    size_t k = 0, v = 0;
+    for (int h = 0; h < L->n_heads; ++h) {
+        k += static_cast<size_t>(L->capacity) * L->head_dim * L->kbits[h] / 8;
+        v += static_cast<size_t>(L->capacity) * L->head_dim * L->vbits[h] / 8;
+    }
+    return k < (1ull << 32) && v < (1ull << 32);
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+float inv_sqrt_f32(int d) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))); }
+
+// ---------------------------------------------------------------- decode plan
+struct Plan {
+    std::vector<SegPlan> seg;     // packed segments first, then fp16 segments
+    std::vector<LayerPlan> layer;
+    DecodeDims dims{};
+    int n_packed_seg = 0;
+    int kb_max = 1, vb_max = 1;
+    bool any_qjl = false;
+    size_t off_layer = 0, off_qrot = 0, off_qorig = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, int Hq, int d,
+                     const float *S, int jl, Plan &P, bool check_ptrs) {
+    if (!layers || n_layers < 1 || B < 1 || H < 1 || H > TQ_MAX_HEADS || Hq < H || Hq % H) return TQ_ERR_ARG;
+    if (!pow2(d) || d < 16 || d > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
+    const int gqa = Hq / H;
+    if (d != kD || (gqa != 1 && gqa != 2 && gqa != 4)) return TQ_ERR_UNSUPPORTED;
+    // pass 1: validate, collect total bytes for the chunk size
+    double total_bytes = 0.0;
+    for (int l = 0; l < n_layers; ++l) {
+        const tq_layer_view &lv = layers[l];
+        if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
+        for (int s = 0; s < lv.n_segments; ++s) {
+            const tq_segment &sg = lv.seg[s];
+            const tq_segment_layout &L = sg.layout;
+            if (sg.kind != TQ_SEG_PACKED && sg.kind != TQ_SEG_FP16) return TQ_ERR_ARG;
+            tq_status st = check_layout(&L, sg.kind == TQ_SEG_PACKED);
+            if (st != TQ_OK) return st;
+            if (L.batch != B || L.n_heads != H || L.head_dim != d) return TQ_ERR_ARG;
+            if (sg.n_tokens < 0 || sg.n_tokens > L.capacity) return TQ_ERR_SIZE;
+            if (sg.kind == TQ_SEG_PACKED) {
+                if (L.capacity % 16) return TQ_ERR_ALIGN;
+                if (!fits_u32(&L)) return TQ_ERR_UNSUPPORTED;
+                bool q = false;
+                for (int h = 0; h < H; ++h) q |= L.qjl[h] != 0;
+                if (check_ptrs) {
+                    const tq_packed_bufs &pb = sg.packed;
+                    if (!pb.kcodes || !pb.vcodes || !pb.kscale || !pb.vscale) return TQ_ERR_ARG;
+                    if (!aligned16(pb.kcodes) || !aligned16(pb.vcodes) || !aligned16(pb.kscale) ||
+                        !aligned16(pb.vscale))
+                        return TQ_ERR_ALIGN;
+                    if (q) {
+                        if (!pb.qjl_signs || !pb.qjl_norm || !S) return TQ_ERR_ARG;
+                        if (!aligned16(pb.qjl_signs) || !aligned16(pb.qjl_norm) || !aligned16(S)) return TQ_ERR_ALIGN;
+                    }
+                }
+                if (q && (jl != kJl || L.jl_dim != kJl)) return TQ_ERR_UNSUPPORTED;
+                double per = 0;
+                for (int h = 0; h < H; ++h) per += 16.0 * (L.kbits[h] + L.vbits[h]) + 8 + (L.qjl[h] ? 20 : 0);
+                total_bytes += per * B * sg.n_tokens;
+            } else {
+                if (check_ptrs) {
+                    if (!sg.k16 || !sg.v16) return TQ_ERR_ARG;
+                    if (!aligned16(sg.k16) || !aligned16(sg.v16)) return TQ_ERR_ALIGN;
+                }
+                total_bytes += 4.0 * d * H * B * sg.n_tokens;
+            }
+        }
+    }
+    const double target = std::fmin(std::fmax(total_bytes / (sm_count() * 12.0), 8192.0), 262144.0);
+    // pass 2: chunking and the plan, packed segments first
+    P = Plan();
+    P.layer.resize(n_layers);
+    int cta_packed = 0;
+    for (int kind = 0; kind < 2; ++kind) {
+        for (int l = 0; l < n_layers; ++l) {
+            const tq_layer_view &lv = layers[l];
+            LayerPlan &lp = P.layer[l];
+            if (kind == 0) {
+                std::memcpy(lp.sign_bits, lv.rot.sign_bits, sizeof(lp.sign_bits));
+                lp.has_qjl = 0;
+                lp.seg_begin = static_cast<int>(P.seg.size());
+            } else {
+                lp.f16_begin = static_cast<int>(P.seg.size());
+            }
+            for (int s = 0; s < lv.n_segments; ++s) {
+                const tq_segment &sg = lv.seg[s];
+                if (sg.kind != (kind == 0 ? TQ_SEG_PACKED : TQ_SEG_FP16) || sg.n_tokens == 0) continue;
+                const tq_segment_layout &L = sg.layout;
+                SegPlan sp;
+                std::memset(&sp, 0, sizeof(sp));
+                sp.kind = sg.kind;
+                sp.layer = l;
+                sp.n_tokens = sg.n_tokens;
+                sp.capacity = L.capacity;
+                double bpt;
+                if (sg.kind == TQ_SEG_PACKED) {
+                    const Offsets o = offsets(&L);
+                    sp.kcodes = static_cast<const uint8_t *>(sg.packed.kcodes);
+                    sp.vcodes = static_cast<const uint8_t *>(sg.packed.vcodes);
+                    sp.kscale = sg.packed.kscale;
+                    sp.vscale = sg.packed.vscale;
+                    sp.qjl_signs = static_cast<const uint8_t *>(sg.packed.qjl_signs);
+                    sp.qjl_norm = sg.packed.qjl_norm;
+                    sp.nq = o.nq;
+                    sp.kblock = o.kblock;
+                    sp.vblock = o.vblock;
+                    double per = 0;
+                    for (int h = 0; h < H; ++h) {
+                        sp.koff[h] = o.koff[h];
+                        sp.voff[h] = o.voff[h];
+                        sp.kbits[h] = L.kbits[h];
+                        sp.vbits[h] = L.vbits[h];
+                        sp.qrank[h] = o.qrank[h];
+                        P.kb_max = std::max<int>(P.kb_max, L.kbits[h]);
+                        P.vb_max = std::max<int>(P.vb_max, L.vbits[h]);
+                        if (L.qjl[h]) { P.any_qjl = true; lp.has_qjl = 1; }
+                        per += 16.0 * (L.kbits[h] + L.vbits[h]) + 8 + (L.qjl[h] ? 20 : 0);
+                    }
+                    bpt = per / H;
+                } else {
+                    sp.kcodes = static_cast<const uint8_t *>(sg.k16);
+                    sp.vcodes = static_cast<const uint8_t *>(sg.v16);
+                    bpt = 4.0 * d;
+                }
+                int chunk = static_cast<int>(std::ceil(target / bpt));
+                chunk = ((chunk + kStageTokens - 1) / kStageTokens) * kStageTokens;
+                const int maxc = ((sg.n_tokens + kStageTokens - 1) / kStageTokens) * kStageTokens;
+                chunk = std::max(kStageTokens, std::min(chunk, maxc));
+                sp.chunk = chunk;
+                sp.n_chunks = (sg.n_tokens + chunk - 1) / chunk;
+                P.seg.push_back(sp);
+            }
+            if (kind == 0) lp.seg_end = static_cast<int>(P.seg.size());
+            else lp.f16_end = static_cast<int>(P.seg.size());
+        }
+        if (kind == 0) P.n_packed_seg = static_cast<int>(P.seg.size());
+    }
+    // CTA and partial numbering
+    int cta16 = 0, part = 0;
+    for (size_t i = 0; i < P.seg.size(); ++i) {
+        SegPlan &sp = P.seg[i];
+        const long long ctas = static_cast<long long>(B) * H * sp.n_chunks;
+        if (static_cast<int>(i) < P.n_packed_seg) {
+            sp.cta_begin = cta_packed;
+            cta_packed += static_cast<int>(ctas);
+        } else {
+            sp.cta_begin = cta16;
+            cta16 += static_cast<int>(ctas);
+        }
+        sp.part_begin = part;
+        part += static_cast<int>(ctas);
+        if (part < 0 || cta_packed < 0 || cta16 < 0) return TQ_ERR_UNSUPPORTED;
+    }
+    DecodeDims &D = P.dims;
+    D.L = n_layers;
+    D.B = B;
+    D.H = H;
+    D.Hq = Hq;
+    D.gqa = gqa;
+    D.n_seg = static_cast<int>(P.seg.size());
+    D.n_packed_ctas = cta_packed;
+    D.n_fp16_ctas = cta16;
+    D.n_parts = part;
+    D.inv_sqrt_d = inv_sqrt_f32(d);
+    D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
+    size_t off = align256(sizeof(SegPlan) * std::max<size_t>(P.seg.size(), 1));
+    P.off_layer = off;
+    off += align256(sizeof(LayerPlan) * n_layers);
+    P.off_qrot = off;
+    off += align256(nq * d * 4);
+    P.off_qorig = off;
+    off += align256(nq * d * 4);
+    P.off_qjlt = off;
+    off += align256(nq * d * 4);
+    P.off_qsum = off;
+    off += align256(nq * 16);
+    P.off_part = off;
+    off += align256(static_cast<size_t>(std::max(part, 1)) * kMaxGqa * (4 + kD) * 4);
+    P.total = off;
+    return TQ_OK;
+}
+
+}  // namespace
+
+// =============================================================== C ABI
+extern "C" {
+
+const char *tq_status_string(tq_status s) {
+    switch (s) {
+        case TQ_OK: return "TQ_OK";
+        case TQ_ERR_ARG: return "TQ_ERR_ARG: invalid argument";
+        case TQ_ERR_UNSUPPORTED: return "TQ_ERR_UNSUPPORTED: shape not implemented by the kernels";
+        case TQ_ERR_ALIGN: return "TQ_ERR_ALIGN: pointer, stride or capacity not 16-byte aligned";
+        case TQ_ERR_SIZE: return "TQ_ERR_SIZE: buffer or capacity too small";
+        case TQ_ERR_CUDA: return "TQ_ERR_CUDA: CUDA runtime error (see tq_last_cuda_error)";
+        default: return "unknown tq_status";
+    }
+}
+
+int tq_last_cuda_error(void) { return g_last_cuda; }
+
+int tq_version(void) { return 100; }
+
+tq_status tq_make_rotation(int head_dim, uint64_t seed, tq_rotation *rot) {
+    if (!rot || !pow2(head_dim) || head_dim < 16 || head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
+    std::memset(rot, 0, sizeof(*rot));
+    rot->head_dim = head_dim;
+    rot->seed = seed;
+    SplitMix64 g{seed};
+    for (int i = 0; i < head_dim; ++i)
+        if (g.next() >> 63) rot->sign_bits[i >> 5] |= 1u << (i & 31);
+    return TQ_OK;
+}
+
+tq_status tq_fit_codebook(int bits, float *centroids, float *thresholds) {
+    if (bits < 1 || bits > 8 || !centroids) return TQ_ERR_ARG;
+    const FittedCodebook &cb = fit(bits);
+    for (int k = 0; k < (1 << bits); ++k) centroids[k] = static_cast<float>(cb.level[k]);
+    if (thresholds)
+        for (int k = 0; k + 1 < (1 << bits); ++k) thresholds[k] = static_cast<float>(cb.bound[k]);
+    return TQ_OK;
+}
+
+tq_status tq_make_qjl(int head_dim, int jl_dim, uint64_t seed, float *S) {
+    if (!S || !pow2(head_dim) || head_dim < 16 || head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
+    if (jl_dim < 32 || jl_dim > 1024 || jl_dim % 32) return TQ_ERR_ARG;
+    SplitMix64 g{seed};
+    const int n = jl_dim * head_dim;
+    const double two_pi = 6.283185307179586476925;
+    for (int i = 0; i < n; i += 2) {
+        const double u1 = static_cast<double>((g.next() >> 11) + 1) * 0x1p-53;
+        const double u2 = static_cast<double>(g.next() >> 11) * 0x1p-53;
+        const double rad = std::sqrt(-2.0 * std::log(u1));
+        S[i] = static_cast<float>(rad * std::cos(two_pi * u2));
+        if (i + 1 < n) S[i + 1] = static_cast<float>(rad * std::sin(two_pi * u2));
+    }
+    return TQ_OK;
+}
+
+tq_status tq_packed_size(const tq_segment_layout *layout, tq_packed_sizes *sizes) {
+    tq_status st = check_layout(layout, true);
+    if (st != TQ_OK) return st;
+    if (!sizes) return TQ_ERR_ARG;
+    const Offsets o = offsets(layout);
+    const size_t B = layout->batch, cap = layout->capacity;
+    size_t k = 0, v = 0;
+    for (int h = 0; h < layout->n_heads; ++h) {
+        k += cap * layout->head_dim * layout->kbits[h] / 8;
+        v += cap * layout->head_dim * layout->vbits[h] / 8;
+    }
+    sizes->kcode_bytes = B * k;
+    sizes->vcode_bytes = B * v;
+    sizes->kscale_bytes = B * layout->n_heads * cap * 4;
+    sizes->vscale_bytes = sizes->kscale_bytes;
+    sizes->qjl_sign_bytes = B * o.nq * cap * (o.nq ? layout->jl_dim / 8 : 0);
+    sizes->qjl_norm_bytes = B * o.nq * cap * 4;
+    return TQ_OK;
+}
+
+tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, const float *qjl_S,
+                      const void *K, const void *V, int n_tokens, int64_t stride_b, int64_t stride_h,
+                      int64_t stride_t, int t_begin, const tq_packed_bufs *out, void *stream) {
+    tq_status st = check_layout(layout, true);
+    if (st != TQ_OK) return st;
+    if (!rot || !K || !V || !out || n_tokens < 0 || t_begin < 0) return TQ_ERR_ARG;
+    if (rot->head_dim != layout->head_dim) return TQ_ERR_ARG;
+    if (layout->head_dim != kD) return TQ_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(t_begin) + n_tokens > layout->capacity) return TQ_ERR_SIZE;
+    if (!out->kcodes || !out->vcodes || !out->kscale || !out->vscale) return TQ_ERR_ARG;
+    if (!fits_u32(layout)) return TQ_ERR_UNSUPPORTED;
+    const Offsets o = offsets(layout);
+    if (o.nq) {
+        if (!qjl_S || !out->qjl_signs || !out->qjl_norm) return TQ_ERR_ARG;
+        if (layout->jl_dim != kJl) return TQ_ERR_UNSUPPORTED;
+        if (!aligned16(qjl_S) || !aligned16(out->qjl_signs)) return TQ_ERR_ALIGN;
+    }
+    if (!aligned16(K) || !aligned16(V) || !aligned16(out->kcodes) || !aligned16(out->vcodes) ||
+        !aligned16(out->kscale) || !aligned16(out->vscale))
+        return TQ_ERR_ALIGN;
+    if (stride_t < kD || stride_h < 0 || stride_b < 0 || (stride_t % 8) || (stride_h % 8) || (stride_b % 8))
+        return TQ_ERR_ALIGN;
+    if (n_tokens == 0) return TQ_OK;
+    CompressParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.K = static_cast<const uint16_t *>(K);
+    p.V = static_cast<const uint16_t *>(V);
+    p.sb = stride_b;
+    p.sh = stride_h;
+    p.st = stride_t;
+    p.B = layout->batch;
+    p.H = layout->n_heads;
+    p.T = n_tokens;
+    p.t_begin = t_begin;
+    p.capacity = layout->capacity;
+    p.kcodes = static_cast<uint8_t *>(out->kcodes);
+    p.vcodes = static_cast<uint8_t *>(out->vcodes);
+    p.kscale = out->kscale;
+    p.vscale = out->vscale;
+    p.qjl_signs = static_cast<uint8_t *>(out->qjl_signs);
+    p.qjl_norm = out->qjl_norm;
+    p.S = qjl_S;
+    p.nq = o.nq;
+    p.kblock = o.kblock;
+    p.vblock = o.vblock;
+    for (int h = 0; h < p.H; ++h) {
+        p.koff[h] = o.koff[h];
+        p.voff[h] = o.voff[h];
+        p.kbits[h] = layout->kbits[h];
+        p.vbits[h] = layout->vbits[h];
+        p.qrank[h] = o.qrank[h];
+    }
+    std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
+    p.inv_sqrt_d = inv_sqrt_f32(kD);
+    fill_thresholds(p.thr, layout->vbits, p.H);
+    const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *bufs, const tq_rotation *rot,
+                        int t_begin, int n_tokens, float *k_rot, float *v_rot, float *k_orig, float *v_orig,
+                        void *stream) {
+    tq_status st = check_layout(layout, true);
+    if (st != TQ_OK) return st;
+    if (!bufs || !bufs->kcodes || !bufs->vcodes || !bufs->kscale || !bufs->vscale) return TQ_ERR_ARG;
+    if (t_begin < 0 || n_tokens < 0) return TQ_ERR_ARG;
+    if (static_cast<int64_t>(t_begin) + n_tokens > layout->capacity) return TQ_ERR_SIZE;
+    if ((k_orig || v_orig) && !rot) return TQ_ERR_ARG;
+    if (layout->head_dim != kD) return TQ_ERR_UNSUPPORTED;
+    if (rot && rot->head_dim != layout->head_dim) return TQ_ERR_ARG;
+    if (!fits_u32(layout)) return TQ_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return TQ_OK;
+    const Offsets o = offsets(layout);
+    DequantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = layout->batch;
+    p.H = layout->n_heads;
+    p.t_begin = t_begin;
+    p.n = n_tokens;
+    p.capacity = layout->capacity;
+    p.kcodes = static_cast<const uint8_t *>(bufs->kcodes);
+    p.vcodes = static_cast<const uint8_t *>(bufs->vcodes);
+    p.kscale = bufs->kscale;
+    p.vscale = bufs->vscale;
+    p.kblock = o.kblock;
+    p.vblock = o.vblock;
+    for (int h = 0; h < p.H; ++h) {
+        p.koff[h] = o.koff[h];
+        p.voff[h] = o.voff[h];
+        p.kbits[h] = layout->kbits[h];
+        p.vbits[h] = layout->vbits[h];
+    }
+    if (rot) std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
+    p.inv_sqrt_d = inv_sqrt_f32(kD);
+    p.k_rot = k_rot;
+    p.v_rot = v_rot;
+    p.k_orig = k_orig;
+    p.v_orig = v_orig;
+    fill_centroids(p.centroid, layout->vbits, p.H);
+    const cudaError_t e = launch_dequant(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_age_tiers(int n_tokens, int n_bounds, const int *age_bounds, int *start, int *end) {
+    if (n_tokens < 0 || n_bounds < 0 || !start || !end || (n_bounds > 0 && !age_bounds)) return TQ_ERR_ARG;
+    for (int i = 0; i < n_bounds; ++i)
+        if (age_bounds[i] < 0 || (i > 0 && age_bounds[i] < age_bounds[i - 1])) return TQ_ERR_ARG;
+    for (int tier = 0; tier <= n_bounds; ++tier) {
+        const long long lo_age = tier == 0 ? 0 : age_bounds[tier - 1];
+        // positions with lo_age <= n-1-p < hi_age  <=>  n-hi_age <= p <= n-1-lo_age
+        const long long e = std::max<long long>(0, n_tokens - lo_age);
+        long long s = 0;
+        if (tier < n_bounds) s = std::max<long long>(0, static_cast<long long>(n_tokens) - age_bounds[tier]);
+        start[tier] = static_cast<int>(std::min(s, e));
+        end[tier] = static_cast<int>(e);
+    }
+    return TQ_OK;
+}
+
+tq_status tq_decode_workspace_size(const tq_layer_view *layers, int n_layers, int batch, int n_heads,
+                                   int q_heads, int head_dim, size_t *bytes) {
+    if (!bytes) return TQ_ERR_ARG;
+    Plan P;
+    tq_status st = build_plan(layers, n_layers, batch, n_heads, q_heads, head_dim, nullptr, kJl, P, false);
+    if (st != TQ_OK) return st;
+    *bytes = P.total;
+    return TQ_OK;
+}
+
+tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int batch, int n_heads, int q_heads,
+                              int head_dim, const float *qjl_S, int jl_dim, const void *q, float *out,
+                              void *workspace, size_t ws_bytes, void *stream) {
+    if (!q || !out || !workspace) return TQ_ERR_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return TQ_ERR_ALIGN;
+    Plan P;
+    tq_status st = build_plan(layers, n_layers, batch, n_heads, q_heads, head_dim, qjl_S, jl_dim, P, true);
+    if (st != TQ_OK) return st;
+    if (ws_bytes < P.total) return TQ_ERR_SIZE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    // upload the plan (pageable source: staged before the call returns)
+    std::vector<uint8_t> host(P.off_qrot, 0);
+    if (!P.seg.empty()) std::memcpy(host.data(), P.seg.data(), sizeof(SegPlan) * P.seg.size());
+    std::memcpy(host.data() + P.off_layer, P.layer.data(), sizeof(LayerPlan) * P.layer.size());
+    cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DecodeWorkspace W;
+    W.seg = reinterpret_cast<SegPlan *>(ws);
+    W.layer = reinterpret_cast<LayerPlan *>(ws + P.off_layer);
+    W.qrot = reinterpret_cast<uint32_t *>(ws + P.off_qrot);
+    W.qorig = reinterpret_cast<uint32_t *>(ws + P.off_qorig);
+    W.qjlt = reinterpret_cast<uint32_t *>(ws + P.off_qjlt);
+    W.qsum = reinterpret_cast<float *>(ws + P.off_qsum);
+    W.part = reinterpret_cast<float *>(ws + P.off_part);
+    // fp16 codebook values of every width used by a packed segment
+    unsigned short cent_half[kCbTotal];
+    std::memset(cent_half, 0, sizeof(cent_half));
+    for (int i = 0; i < P.n_packed_seg; ++i) {
+        for (int h = 0; h < n_heads; ++h) {
+            const int vb = P.seg[i].vbits[h];
+            const FittedCodebook &cb = fit(vb);
+            for (int k = 0; k < (1 << vb); ++k)
+                cent_half[cb_off(vb) + k] = __half_as_ushort(__float2half_rn(static_cast<float>(cb.level[k])));
+        }
+    }
+    e = launch_decode_kernels(P.dims, W, P.n_packed_seg, P.kb_max, P.vb_max, P.any_qjl,
+                              static_cast<const uint16_t *>(q), qjl_S, cent_half, out, s, g_ev_start,
+                              g_ev_stop);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_set_decode_kernel_events(void *start, void *stop) {
+    if ((start == nullptr) != (stop == nullptr)) return TQ_ERR_ARG;
+    g_ev_start = static_cast<cudaEvent_t>(start);
+    g_ev_stop = static_cast<cudaEvent_t>(stop);
+    return TQ_OK;
+}
+
+}  // extern "C"

@@ -139,6 +139,13 @@ def queries(w: Workload, layer: int, batch: int, seed: int, device="cpu", step: 
     return torch.randn(batch, w.q_heads, w.head_dim, generator=g, device=device).to(torch.float16)
 
 
+def query_pool(w: Workload, steps: int, batch: int, seed: int, device="cpu"):
+    """fp16 decode queries for `steps` steps of every layer: [steps][layers][batch][q_heads][head_dim]."""
+    g = _gen(seed * 524_287 + 99, device)
+    return torch.randn(steps, w.layers, batch, w.q_heads, w.head_dim, generator=g, device=device).to(
+        torch.float16)
+
+
 def tier_bits(tier: int):
     """(kbits, vbits) of the age tiers: 0 fp16, 1 K4V4, 2 K3V2, 3 K2V1."""
     return [(16, 16), (4, 4), (3, 2), (2, 1)][tier]

@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Compression: codes bit-exact; scales bit-exact (the binary32 order is part of
+the format); QJL sign bits exact except where |(S r)_j| <= 1e-6 ||S_j|| rho
+(counted, < 1e-5 of all bits).  Dequantization: rotated values bit-exact,
+original-space values within 1e-5 max(1, |x|).  Attention: per query head,
+max|o - o_ref| / max|o_ref| <= 2e-3 against the binary64 oracle over the same
+packed cache (the oracle's own compression of the same input, uploaded)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from rotated_quantized_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from rotated_quantized_kv_gb300 import build
+    build.build()
+    from rotated_quantized_kv_gb300 import tq as T
+    return T
+
+
+def _kv(B, H, T, seed, law="outliers"):
+    w = W.Workload("t", layers=1, batch=B, context=T, kv_heads=H, law=law)
+    return W.kv_block(w, 0, B, T, seed)
+
+
+def _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin=0):
+    seg = O.PackedSegment(B, H, 128, cap, kb, vb, qjl, jl=128)
+    O.compress(seg, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S, t_begin=t_begin)
+    return seg
+
+
+def _upload(tq, oseg, layout, n_tokens):
+    g = tq.PackedSegment(layout, n_tokens=n_tokens)
+    g.kcodes.copy_(torch.from_numpy(oseg.kcodes))
+    g.vcodes.copy_(torch.from_numpy(oseg.vcodes))
+    g.kscale.copy_(torch.from_numpy(oseg.kscale))
+    g.vscale.copy_(torch.from_numpy(oseg.vscale))
+    if g.qjl_signs is not None:
+        g.qjl_signs.copy_(torch.from_numpy(oseg.qjl_signs))
+        g.qjl_norm.copy_(torch.from_numpy(oseg.qjl_norm))
+    return g
+
+
+def _qjl_window_ok(oseg, gseg_signs, K, sign, S, B, H, T, t_begin):
+    """Sign-bit mismatches must sit in the 1e-6 window around zero."""
+    got = gseg_signs.cpu().numpy()
+    bad = np.flatnonzero(got != oseg.qjl_signs)
+    if bad.size == 0:
+        return 0
+    Sd = S.astype(np.float64)
+    rown = np.linalg.norm(Sd, axis=1)
+    mism = 0
+    for byte in bad:
+        rec = byte // 16
+        pos = rec % oseg.capacity
+        bq = rec // oseg.capacity
+        b, q = divmod(bq, oseg.nq)
+        h = [hh for hh in range(H) if oseg.qjl[hh] and oseg.qjl_rank(hh) == q][0]
+        x = K[b, h, pos - t_begin].float().numpy()
+        y = O.rotate_f32(x, sign)
+        codes, m = O.quant_key(y, int(oseg.kbits[h]))
+        yh = (m * O.key_levels(int(oseg.kbits[h]))[codes]).astype(np.float32)
+        r = (y - yh).astype(np.float32)
+        p = Sd @ r.astype(np.float64)
+        rho = np.linalg.norm(r.astype(np.float64))
+        diff = got[byte] ^ oseg.qjl_signs[byte]
+        for bit in range(8):
+            if (diff >> bit) & 1:
+                j = (byte % 16) * 8 + bit
+                assert abs(p[j]) <= 1e-6 * rown[j] * rho, (b, h, pos, j, p[j])
+                mism += 1
+    return mism
+
+
+COMPRESS_CASES = [
+    # B, H, T, t_begin, kbits, vbits, qjl
+    (2, 8, 200, 0, [1, 2, 3, 4, 5, 6, 7, 8], [8, 7, 6, 5, 4, 3, 2, 1], None),
+    (1, 8, 64, 16, [4] * 8, [4] * 8, None),
+    (3, 4, 77, 32, [1, 2, 2, 3], [1, 3, 2, 4], [1, 1, 0, 0]),
+    (1, 8, 130, 0, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], [0, 0, 1, 1, 0, 0, 0, 1]),
+]
+
+
+@pytest.mark.parametrize("B,H,T,t_begin,kb,vb,qjl", COMPRESS_CASES)
+def test_compress_bit_exact(tq, B, H, T, t_begin, kb, vb, qjl):
+    K, V = _kv(B, H, T, seed=11 + T)
+    cap = ((t_begin + T + 15) // 16) * 16
+    sign = O.signs(128, 42)
+    S = O.qjl_matrix(128, 128, 42 + 1000) if qjl else None
+    oseg = _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin)
+    layout = tq.make_layout(B, H, 128, cap, kb, vb, qjl)
+    g = tq.PackedSegment(layout)
+    rot = tq.tq_make_rotation(128, 42)
+    Sd = torch.from_numpy(S).cuda() if qjl else None
+    tq.tq_compress(g, rot, K.cuda(), V.cuda(), t_begin=t_begin, qjl_S=Sd)
+    torch.cuda.synchronize()
+    assert np.array_equal(g.kcodes.cpu().numpy(), oseg.kcodes)
+    assert np.array_equal(g.vcodes.cpu().numpy(), oseg.vcodes)
+    assert np.array_equal(g.kscale.cpu().numpy().view(np.uint32), oseg.kscale.view(np.uint32))
+    assert np.array_equal(g.vscale.cpu().numpy().view(np.uint32), oseg.vscale.view(np.uint32))
+    if qjl:
+        n = _qjl_window_ok(oseg, g.qjl_signs, K, sign, S, B, H, T, t_begin)
+        assert n <= 1e-5 * oseg.qjl_signs.size * 8
+        assert np.allclose(g.qjl_norm.cpu().numpy(), oseg.qjl_norm, rtol=1e-5, atol=0)
+
+
+def test_compress_edge_vectors(tq):
+    # all-zero vectors, one-hot vectors (exact +-absmax), huge fp16 values
+    B, H, T = 1, 8, 70
+    K = torch.zeros(B, H, T, 128, dtype=torch.float16)
+    V = torch.zeros(B, H, T, 128, dtype=torch.float16)
+    K[0, :, 1, 5] = 1.0
+    V[0, :, 1, 5] = -2.0
+    K[0, :, 2] = 60000.0
+    V[0, :, 2, ::2] = -60000.0
+    K[0, :, 3:] = torch.randn(H, T - 3, 128).half()
+    V[0, :, 3:] = torch.randn(H, T - 3, 128).half()
+    kb = [1, 2, 3, 4, 5, 6, 7, 8]
+    sign = O.signs(128, 42 + 3)
+    oseg = _oracle_segment(B, H, 80, kb, kb[::-1], None, K, V, sign, None)
+    layout = tq.make_layout(B, H, 128, 80, kb, kb[::-1])
+    g = tq.PackedSegment(layout)
+    tq.tq_compress(g, tq.tq_make_rotation(128, 42 + 3), K.cuda(), V.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(g.kcodes.cpu().numpy(), oseg.kcodes)
+    assert np.array_equal(g.vcodes.cpu().numpy(), oseg.vcodes)
+    assert np.array_equal(g.kscale.cpu().numpy(), oseg.kscale)
+    assert np.array_equal(g.vscale.cpu().numpy(), oseg.vscale)
+
+
+def test_compress_chunked_equals_one_shot(tq):
+    # "Dynamic Chunk Buffering": compressing 64 tokens at a time gives the same bytes
+    B, H, T = 1, 8, 256
+    K, V = _kv(B, H, T, seed=5)
+    layout = tq.make_layout(B, H, 128, T, 8, 3)
+    rot = tq.tq_make_rotation(128, 42)
+    a, c = tq.PackedSegment(layout), tq.PackedSegment(layout)
+    Kc, Vc = K.cuda(), V.cuda()
+    tq.tq_compress(a, rot, Kc, Vc)
+    for t0 in range(0, T, 64):
+        tq.tq_compress(c, rot, Kc[:, :, t0:t0 + 64], Vc[:, :, t0:t0 + 64], t_begin=t0)
+    torch.cuda.synchronize()
+    for x, y in ((a.kcodes, c.kcodes), (a.vcodes, c.vcodes), (a.kscale, c.kscale), (a.vscale, c.vscale)):
+        assert torch.equal(x, y)
+
+
+def test_compress_strided_input(tq):
+    # K, V viewed from a [B][T][H][d] tensor (token-major layout)
+    B, H, T = 2, 8, 100
+    base = torch.randn(2, B, T, H, 128).half()
+    K = base[0].permute(0, 2, 1, 3)
+    V = base[1].permute(0, 2, 1, 3)
+    sign = O.signs(128, 42)
+    oseg = _oracle_segment(B, H, 112, [3] * 8, [3] * 8, None, K.contiguous(), V.contiguous(), sign, None)
+    g = tq.PackedSegment(tq.make_layout(B, H, 128, 112, 3, 3))
+    bc = base.cuda()
+    tq.tq_compress(g, tq.tq_make_rotation(128, 42), bc[0].permute(0, 2, 1, 3), bc[1].permute(0, 2, 1, 3))
+    torch.cuda.synchronize()
+    assert np.array_equal(g.kcodes.cpu().numpy(), oseg.kcodes)
+    assert np.array_equal(g.vcodes.cpu().numpy(), oseg.vcodes)
+
+
+def test_dequantize(tq):
+    B, H, T = 2, 8, 90
+    kb = [1, 2, 3, 4, 5, 6, 7, 8]
+    vb = [2, 3, 4, 5, 6, 7, 8, 1]
+    K, V = _kv(B, H, T, seed=3)
+    sign = O.signs(128, 42)
+    oseg = _oracle_segment(B, H, 96, kb, vb, None, K, V, sign, None)
+    layout = tq.make_layout(B, H, 128, 96, kb, vb)
+    g = _upload(tq, oseg, layout, T)
+    rot = tq.tq_make_rotation(128, 42)
+    kr, vr, ko, vo = tq.tq_dequantize(g, 5, T - 5, rot=rot, rotated=True, original=True)
+    torch.cuda.synchronize()
+    for b in range(B):
+        for h in range(H):
+            ok, ov = O.dequant(oseg, b, h, 5, T - 5)
+            assert np.array_equal(kr[b, h].cpu().numpy(), ok)
+            assert np.array_equal(vr[b, h].cpu().numpy(), ov)
+            for got, y in ((ko, ok), (vo, ov)):
+                x = O.rotate_f64(y.astype(np.float64), sign)
+                err = np.abs(got[b, h].cpu().numpy() - x)
+                assert np.all(err <= 1e-5 * np.maximum(1.0, np.abs(x)))
+
+
+def _max_rel(out, ref):
+    o = out.reshape(-1, out.shape[-1])
+    r = ref.reshape(-1, ref.shape[-1])
+    return (np.abs(o - r).max(axis=1) / np.maximum(np.abs(r).max(axis=1), 1e-30)).max()
+
+
+def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
+    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl)."""
+    rng = np.random.default_rng(seed)
+    S = O.qjl_matrix(128, 128, 42 + 1000) if qjl_any else None
+    Sd = torch.from_numpy(S).cuda() if qjl_any else None
+    views, oracle_layers, keep = [], [], []
+    for l in range(L):
+        sign = O.signs(128, 42 + l)
+        rot = tq.tq_make_rotation(128, 42 + l)
+        osegs, gsegs = [], []
+        for si, sp in enumerate(spec):
+            T = sp[1]
+            cap = max(16, ((T + 15) // 16) * 16)
+            K, V = _kv(B, H, max(T, 1), seed=seed * 100 + l * 10 + si)
+            if sp[0] == "fp16":
+                o = O.Fp16Segment(B, H, 128, cap, n_tokens=T)
+                kk = np.zeros((B, H, cap, 128), np.float16)
+                vv = np.zeros((B, H, cap, 128), np.float16)
+                kk[:, :, :T] = K.numpy()[:, :, :T]
+                vv[:, :, :T] = V.numpy()[:, :, :T]
+                o.k16[:] = kk.ravel().view(np.uint16)
+                o.v16[:] = vv.ravel().view(np.uint16)
+                g = tq.Fp16Segment(B, H, 128, cap, n_tokens=T, k=torch.from_numpy(kk).cuda(),
+                                   v=torch.from_numpy(vv).cuda())
+            else:
+                _, _, kb, vb, qj = sp
+                o = O.PackedSegment(B, H, 128, cap, kb, vb, qj, jl=128)
+                if T:
+                    O.compress(o, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S)
+                o.n_tokens = T
+                g = _upload(tq, o, tq.make_layout(B, H, 128, cap, kb, vb, qj), T)
+            osegs.append(o)
+            gsegs.append(g)
+        keep.append(gsegs)
+        views.append(tq.layer_view(rot, gsegs))
+        oracle_layers.append((osegs, sign))
+    q = torch.from_numpy(rng.standard_normal((L, B, Hq, 128)).astype(np.float16))
+    out = torch.empty(L, B, Hq, 128, device="cuda")
+    ws = torch.empty(tq.tq_decode_workspace_size(views, B, H, Hq, 128), dtype=torch.uint8, device="cuda")
+    tq.tq_decode_attention(views, q.cuda(), out, ws, H, qjl_S=Sd)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    worst = 0.0
+    for l in range(L):
+        osegs, sign = oracle_layers[l]
+        ref = O.decode_attention(osegs, q[l].numpy(), sign, H, S=S)
+        if all(s.n_tokens == 0 for s in osegs):
+            assert np.all(got[l] == 0)
+            continue
+        worst = max(worst, _max_rel(got[l], ref))
+    return worst
+
+
+ATTN_CASES = [
+    # L, B, H, Hq, segments
+    (1, 1, 8, 32, [("packed", 1024, [4] * 8, [4] * 8, None)]),
+    (2, 2, 2, 8, [("fp16", 10), ("packed", 300, [3, 5], [2, 8], None), ("fp16", 7)]),
+    (1, 2, 4, 8, [("packed", 200, [1, 2, 3, 4], [1, 2, 3, 4], None), ("packed", 129, [5, 6, 7, 8], [8, 7, 6, 5], None)]),
+    (1, 1, 8, 8, [("packed", 333, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], None)]),
+    (2, 1, 4, 16, [("fp16", 64), ("packed", 190, [2, 1, 4, 3], [3, 4, 1, 2], [1, 1, 0, 0])]),
+]
+
+
+@pytest.mark.parametrize("L,B,H,Hq,spec", ATTN_CASES)
+def test_decode_attention_matches_oracle(tq, L, B, H, Hq, spec):
+    qjl_any = any(s[0] == "packed" and s[4] for s in spec)
+    worst = _attention_case(tq, L, B, H, Hq, spec, seed=len(spec) * 7 + L, qjl_any=qjl_any)
+    assert worst <= ATTN_TOL, worst
+
+
+def test_decode_attention_empty_and_single_token(tq):
+    # a layer with no tokens gives zeros; a single token returns its value
+    assert _attention_case(tq, 1, 1, 2, 8, [("fp16", 0), ("packed", 0, [3, 3], [3, 3], None)], seed=1) == 0.0
+    w = _attention_case(tq, 1, 1, 2, 8, [("packed", 1, [4, 4], [4, 4], None)], seed=2)
+    assert w <= ATTN_TOL
+    w = _attention_case(tq, 1, 2, 2, 2, [("fp16", 1)], seed=3)
+    assert w <= ATTN_TOL
+
+
+def test_decode_attention_tiers(tq):
+    # progressive tiers on a short context: fp16 newest, then K4V4, K3V2, K2V1
+    T = 3000
+    tiers = tq.tq_age_tiers(T, [256, 1024, 2048])
+    spec = []
+    for tier, (s, e) in enumerate(tiers):
+        if e > s:
+            kb, vb = W.tier_bits(tier)
+            spec.append(("fp16", e - s) if kb == 16 else ("packed", e - s, [kb] * 8, [vb] * 8, None))
+    assert _attention_case(tq, 1, 1, 8, 32, spec, seed=9) <= ATTN_TOL
