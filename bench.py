@@ -221,6 +221,9 @@ def run_ours(args, rank, world):
         m.step(s)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:  # torch creates the CUDA event at its first record; the library re-records it
+        a.record()
+        b.record()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     total_bytes = 0
