@@ -226,6 +226,37 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
  * caller; no effect on results. */
 tq_status tq_set_decode_kernel_events(void *start, void *stop);
 
+/* ------------------------------------------------------------------------ */
+/* Decode attention without a caller-supplied workspace.  (No counterpart on   */
+/* the pages: this entry point exists for callers, not for the method.)        */
+/* ------------------------------------------------------------------------ */
+/* Bytes of the library's own scratch array, held on every GPU that loads the
+ * library until the process exits. */
+#define TQ_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/* Same result and same kernels as tq_decode_attention, for callers that may not
+ * allocate device memory while they run: serving loops that reserve all their
+ * device memory at start-up and forbid cudaMalloc afterwards (it can synchronize
+ * the device and fragment a budgeted pool), or hosts whose device memory is
+ * owned by another framework's allocator.  The scratch (plan, rotated queries,
+ * split-K partials) is a fixed array of TQ_STATIC_WORKSPACE_BYTES inside the
+ * library instead of a caller buffer; the caller still passes q and out.  The
+ * call allocates nothing.
+ *   - Set-up: the first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Limit: returns TQ_ERR_SIZE, before launching anything, when the call needs
+ *     more scratch than TQ_STATIC_WORKSPACE_BYTES (tq_decode_workspace_size tells
+ *     how much); split the layers over several calls or use tq_decode_attention.
+ *   - Sharing: every call uses the same array, which keeps the previous call's
+ *     contents; nothing in it needs to start at zero (each call writes all it
+ *     reads).  Calls that overlap on the GPU -- on different streams or from
+ *     different host threads -- race on the array: order them on one stream.
+ * Other arguments and errors as for tq_decode_attention. */
+tq_status tq_decode_attention_static(const tq_layer_view *layers, int n_layers, int batch,
+                                     int n_heads, int q_heads, int head_dim, const float *qjl_S,
+                                     int jl_dim, const void *q, float *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

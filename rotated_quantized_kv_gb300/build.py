@@ -20,7 +20,7 @@ OBJ = os.path.join(ROOT, "_build", "obj")
 LIB = os.path.join(PKG, "_lib", "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["tq_compress.cu", "tq_decode.cu"]
+CUDA_SOURCES = ["tq_compress.cu", "tq_decode.cu", "tq_static.cu"]
 HOST_SOURCES = ["tq_host.cpp"]
 
 

@@ -358,6 +358,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
 
 }  // namespace
 
+tq_status tqk::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 // =============================================================== C ABI
 extern "C" {
 

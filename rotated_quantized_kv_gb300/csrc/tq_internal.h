@@ -117,6 +117,9 @@ constexpr int kStages = 4;
 
 size_t packed_stage_bytes(int kb_max, int vb_max, bool qjl);
 
+// Records a CUDA error for tq_last_cuda_error() and returns TQ_ERR_CUDA.
+tq_status record_cuda_error(cudaError_t e);
+
 // Launchers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams &p, cudaStream_t s);

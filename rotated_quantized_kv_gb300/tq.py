@@ -41,7 +41,7 @@ STATUS = {0: "TQ_OK", -1: "TQ_ERR_ARG", -2: "TQ_ERR_UNSUPPORTED", -3: "TQ_ERR_AL
 EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rotation",
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
-            "tq_set_decode_kernel_events"]
+            "tq_set_decode_kernel_events", "tq_decode_attention_static"]
 
 
 class TQError(RuntimeError):
@@ -106,6 +106,9 @@ _lib.tq_decode_workspace_size.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I,
 _lib.tq_decode_attention.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, _I, _I, _P, _I, _P, _P,
                                      _P, ctypes.c_size_t, _P]
 _lib.tq_set_decode_kernel_events.argtypes = [_P, _P]
+_lib.tq_decode_attention_static.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, _I, _I, _P, _I, _P,
+                                            _P, _P]
+TQ_STATIC_WORKSPACE_BYTES = 16 << 20
 for _n in EXPORTED:
     if _n not in ("tq_status_string", "tq_last_cuda_error", "tq_version"):
         getattr(_lib, _n).restype = _I
@@ -309,6 +312,19 @@ def tq_set_decode_kernel_events(start=None, stop=None):
     sp = start.cuda_event if start is not None else None
     ep = stop.cuda_event if stop is not None else None
     _check(_lib.tq_set_decode_kernel_events(sp, ep), "tq_set_decode_kernel_events")
+
+
+def tq_decode_attention_static(layers, q: torch.Tensor, out: torch.Tensor, n_heads: int,
+                               qjl_S: torch.Tensor | None = None, jl_dim: int = 128, stream=None, views=None):
+    """tq_decode_attention without a workspace argument: the library's fixed
+    TQ_STATIC_WORKSPACE_BYTES device array is the scratch, so the call allocates
+    nothing (for callers that may not allocate device memory while running).
+    Calls share that array: keep them ordered on one stream."""
+    L, B, Hq, d = q.shape
+    arr = views if views is not None else _views(layers)
+    _check(_lib.tq_decode_attention_static(arr, L, B, n_heads, Hq, d, _ptr(qjl_S), jl_dim, _ptr(q), _ptr(out),
+                                           _stream(stream)), "tq_decode_attention_static")
+    return out
 
 
 def views_array(layers):

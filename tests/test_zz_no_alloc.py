@@ -1,0 +1,86 @@
+"""tq_decode_attention_static: decode attention for callers that may not allocate
+device memory while they run (serving loops that reserve all device memory at
+start-up, or hosts whose device memory belongs to another allocator).  Its
+scratch is the library's fixed device array instead of a caller workspace.
+
+Checked through the C ABI against tq_decode_attention (caller workspace) on two
+calls in a row: the array keeps the previous call's contents, so the second
+call must not depend on them.  Collected last on purpose; runs alone too."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from rotated_quantized_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3  # the attention tolerance used by the parity tests
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from rotated_quantized_kv_gb300 import build
+    build.build()
+    from rotated_quantized_kv_gb300 import tq as T
+    return T
+
+
+def _cache(tq, L, B, H, seed):
+    w = W.Workload("t", layers=L, batch=B, context=600, kv_heads=H, law="outliers")
+    keep, views = [], []
+    for l in range(L):
+        rot = tq.tq_make_rotation(128, 42 + l)
+        K, V = W.kv_block(w, l, B, 600, seed)
+        sink = tq.Fp16Segment(B, H, 128, 32, n_tokens=32, k=K[:, :, :32].contiguous().cuda(),
+                              v=V[:, :, :32].contiguous().cuda())
+        kb = [(3 + h + l) % 8 + 1 for h in range(H)]
+        vb = [(5 + 2 * h + l) % 8 + 1 for h in range(H)]
+        seg = tq.PackedSegment(tq.make_layout(B, H, 128, 576, kb, vb))
+        tq.tq_compress(seg, rot, K[:, :, 32:].cuda(), V[:, :, 32:].cuda())
+        keep.append((sink, seg))
+        views.append(tq.layer_view(rot, [sink, seg]))
+    return keep, views
+
+
+def _rel(a, b):
+    a = a.reshape(-1, a.shape[-1])
+    b = b.reshape(-1, b.shape[-1])
+    return (np.abs(a - b).max(axis=1) / np.abs(b).max(axis=1)).max()
+
+
+def test_static_workspace_matches_caller_workspace_twice(tq):
+    L, B, H, Hq = 3, 2, 4, 16
+    keep, views = _cache(tq, L, B, H, seed=31)
+    arr = tq.views_array(views)
+    ws = torch.empty(tq.tq_decode_workspace_size(views, B, H, Hq, 128), dtype=torch.uint8, device="cuda")
+    lib = ctypes.CDLL(tq.LIB_PATH)
+    lib.tq_decode_attention_static.restype = ctypes.c_int
+    lib.tq_decode_attention_static.argtypes = tq._lib.tq_decode_attention_static.argtypes
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        q = torch.randn(L, B, Hq, 128, generator=torch.Generator().manual_seed(call)).half().cuda()
+        ref = torch.empty(L, B, Hq, 128, device="cuda")
+        out = torch.full((L, B, Hq, 128), float("nan"), device="cuda")
+        tq.tq_decode_attention(None, q, ref, ws, H, views=arr)
+        st = lib.tq_decode_attention_static(arr, L, B, H, Hq, 128, None, 128, q.data_ptr(), out.data_ptr(),
+                                            stream)
+        assert st == 0, tq._lib.tq_status_string(st)
+        torch.cuda.synchronize()
+        r, o = ref.cpu().numpy(), out.cpu().numpy()
+        assert np.all(np.isfinite(o))
+        assert _rel(o, r) <= TOL
+
+
+def test_static_workspace_rejects_oversized_calls(tq):
+    # 512 sequences x 32 query heads need more scratch than the fixed array holds
+    B, H, Hq = 512, 8, 32
+    seg = tq.Fp16Segment(B, H, 128, 16, n_tokens=1)
+    views = [tq.layer_view(tq.tq_make_rotation(128, 42), [seg])]
+    assert tq.tq_decode_workspace_size(views, B, H, Hq, 128) > tq.TQ_STATIC_WORKSPACE_BYTES
+    q = torch.zeros(1, B, Hq, 128, dtype=torch.float16, device="cuda")
+    out = torch.zeros(1, B, Hq, 128, device="cuda")
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_attention_static(views, q, out, H)
+    assert e.value.status == -4
