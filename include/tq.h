@@ -218,6 +218,13 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
                               int jl_dim, const void *q, float *out, void *workspace,
                               size_t ws_bytes, void *stream);
 
+/* The kernels never spin without bound: a split-K CTA that waits too long for
+ * its own shared-memory copies (never expected) stops, leaves its part of the
+ * output unwritten and sets a flag at the start of the workspace.  This call
+ * synchronises `stream` and stores that flag (0 = no such event) in *flag.  The
+ * next tq_decode_attention call on the workspace clears it. */
+tq_status tq_decode_error_flag(const void *workspace, int *flag, void *stream);
+
 /* Measurement hook: when both events are non-NULL, every later
  * tq_decode_attention call on this host thread records `start` on its stream
  * just before the split-K kernel over packed segments and `stop` just after it,

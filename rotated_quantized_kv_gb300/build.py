@@ -20,7 +20,7 @@ OBJ = os.path.join(ROOT, "_build", "obj")
 LIB = os.path.join(PKG, "_lib", "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["tq_compress.cu", "tq_decode.cu", "tq_static.cu"]
+CUDA_SOURCES = ["tq_compress.cu", "tq_decode.cu", "tq_static.cu"] + [f"tq_decode_kb{k}.cu" for k in range(1, 9)]
 HOST_SOURCES = ["tq_host.cpp"]
 
 
@@ -33,7 +33,8 @@ def nvcc() -> str:
 
 def _sources():
     return [os.path.join(CSRC, s) for s in CUDA_SOURCES + HOST_SOURCES] + [
-        os.path.join(CSRC, "tq_internal.h"), os.path.join(ROOT, "include", "tq.h")]
+        os.path.join(CSRC, h) for h in ("tq_internal.h", "tq_decode_common.cuh", "tq_decode_packed.cuh")] + [
+        os.path.join(ROOT, "include", "tq.h")]
 
 
 def _stale() -> bool:
@@ -64,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
     os.makedirs(os.path.dirname(LIB), exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in CUDA_SOURCES + HOST_SOURCES]
-    with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]

@@ -1,0 +1,413 @@
+// tq_decode_common.cuh -- device helpers shared by the decode-attention
+// kernels (split-K over packed and fp16 segments, prep, combine).
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "tq_internal.h"
+
+namespace tqk {
+namespace dec {
+
+constexpr int kThreads = 128;                 // 4 warps per CTA
+constexpr int kPartStride = 4 + kD;           // m, l, pad, pad, acc[d]
+constexpr float kNegInf = -__builtin_huge_valf();
+
+__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, int src_bytes) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------ TMA bulk copies
+// One thread issues 1-D bulk copies global -> shared that complete on an
+// mbarrier (transaction bytes); consumers wait on the barrier's phase.
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// Orders this thread's earlier generic-proxy shared accesses before its later
+// async-proxy (bulk copy) writes.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for a barrier phase: gives up after 2^20 polls (each poll
+// may suspend in hardware for a while), so a copy that never completes cannot
+// hang the GPU.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
+    for (int i = 0; i < (1 << 20); i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+    return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+__device__ __forceinline__ float warp_max_g(float v) {  // over the 8 lanes sharing lane & 3
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+    return v;
+}
+__device__ __forceinline__ float warp_sum_g(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    return v;
+}
+
+// Running state of one warp: per thread, query head c = lane & 3 of the GQA
+// group; acc holds the P.V accumulator fragment (8 m-tiles x 4).
+struct WarpState {
+    float m, l;
+    float acc[8][4];
+};
+
+__device__ __forceinline__ void init_state(WarpState &st) {
+    st.m = kNegInf;
+    st.l = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+        for (int q = 0; q < 4; q++) st.acc[mt][q] = 0.f;
+}
+
+// Online-softmax update of one 16-token tile (scores s of tokens g and g+8 for
+// head c, already in base-2 logits) and the B fragment of P (times the value
+// scale vs) for the P.V MMA: column n = g holds head g/2, hi (g even) or lo
+// (g odd) fp16 part, rows = tokens 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1).
+__device__ __forceinline__ void softmax_tile(WarpState &st, float s0, float s1, bool v0ok, bool v1ok,
+                                             float vs0, float vs1, int g, int c, bool head_ok,
+                                             uint32_t &b0, uint32_t &b1) {
+    float t = fmaxf(v0ok ? s0 : kNegInf, v1ok ? s1 : kNegInf);
+    t = warp_max_g(t);
+    const float mnew = fmaxf(st.m, t);
+    float p0 = 0.f, p1 = 0.f;
+    if (mnew != kNegInf) {
+        p0 = v0ok ? ex2(s0 - mnew) : 0.f;
+        p1 = v1ok ? ex2(s1 - mnew) : 0.f;
+    }
+    // rescale only when some head's running max moved (rare after the first tiles)
+    if (__any_sync(0xffffffffu, mnew > st.m)) {
+        const float corr = (mnew == kNegInf) ? 1.f : ex2(st.m - mnew);
+        st.l *= corr;
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) st.acc[mt][q] *= corr;
+    }
+    st.m = mnew;
+    st.l += p0 + p1;
+    // selects, not products: value scales of masked tokens may be stale bytes
+    const float w0 = (head_ok && v0ok) ? p0 * vs0 : 0.f;
+    const float w1 = (head_ok && v1ok) ? p1 * vs1 : 0.f;
+    const int src0 = 8 * c + (g >> 1), src1 = src0 + 4;
+    const float x0 = __shfl_sync(0xffffffffu, w0, src0);
+    const float x1 = __shfl_sync(0xffffffffu, w0, src1);
+    const float x2 = __shfl_sync(0xffffffffu, w1, src0);
+    const float x3 = __shfl_sync(0xffffffffu, w1, src1);
+    // hi part for even columns, lo = x - hi for odd ones (branch-free: the
+    // columns alternate within a warp)
+    const __half2 h01 = __floats2half2_rn(x0, x1);
+    const __half2 h23 = __floats2half2_rn(x2, x3);
+    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+    const float m = (g & 1) ? 1.f : 0.f;  // subtract hi only for the lo columns
+    const __half2 p01 = __floats2half2_rn(x0 - m * f01.x, x1 - m * f01.y);
+    const __half2 p23 = __floats2half2_rn(x2 - m * f23.x, x3 - m * f23.y);
+    b0 = *reinterpret_cast<const uint32_t *>(&p01);
+    b1 = *reinterpret_cast<const uint32_t *>(&p23);
+}
+
+// Merge the four warps' states through shared memory and write the CTA's
+// partial record.  dim_of(mt, r) gives the head dimension of accumulator row r
+// (0: row g, 1: row g+8) of m-tile mt for this thread.
+template <typename DimOf>
+__device__ __forceinline__ void write_partial(WarpState &st, float *scratch, float *part, int gqa,
+                                              DimOf dim_of) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
+    float *wm = scratch;          // [4 warps][4 heads]
+    float *wl = scratch + 16;     // [4][4]
+    float *wacc = scratch + 32;   // [4 warps][4 heads][128]
+    const float l = warp_sum_g(st.l);
+    if ((lane >> 2) == 0) {
+        wm[warp * 4 + c] = st.m;
+        wl[warp * 4 + c] = l;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++) {
+        float *dst = wacc + (warp * 4 + c) * kD;
+        dst[dim_of(mt, 0)] = st.acc[mt][0] + st.acc[mt][1];
+        dst[dim_of(mt, 1)] = st.acc[mt][2] + st.acc[mt][3];
+    }
+    __syncthreads();
+    const int head = threadIdx.x >> 5;
+    if (head < gqa) {
+        float M = kNegInf;
+    #pragma unroll
+        for (int w = 0; w < kThreads / 32; w++) M = fmaxf(M, wm[w * 4 + head]);
+        float f[kThreads / 32];
+        float L = 0.f;
+    #pragma unroll
+        for (int w = 0; w < kThreads / 32; w++) {
+            f[w] = (M == kNegInf) ? 0.f : ex2(wm[w * 4 + head] - M);
+            L += f[w] * wl[w * 4 + head];
+        }
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    #pragma unroll
+        for (int w = 0; w < kThreads / 32; w++) {
+            const float4 v = *reinterpret_cast<const float4 *>(wacc + (w * 4 + head) * kD + 4 * lane);
+            a.x += f[w] * v.x;
+            a.y += f[w] * v.y;
+            a.z += f[w] * v.z;
+            a.w += f[w] * v.w;
+        }
+        float *rec = part + head * kPartStride;
+        if (lane == 0) {
+            rec[0] = M;
+            rec[1] = L;
+        }
+        *reinterpret_cast<float4 *>(rec + 4 + 4 * lane) = a;
+    }
+}
+
+// ------------------------------------------------------------ rotations
+// Walsh-Hadamard transform of a 128-vector held by one warp (lane owns dims
+// 4 lane .. 4 lane + 3): stages 1, 2 in registers, 4..64 by shuffles.
+__device__ __forceinline__ void warp_wht(float (&x)[4], int lane) {
+    const float t0 = x[0] + x[1], t1 = x[0] - x[1], t2 = x[2] + x[3], t3 = x[2] - x[3];
+    x[0] = t0 + t2;
+    x[2] = t0 - t2;
+    x[1] = t1 + t3;
+    x[3] = t1 - t3;
+#pragma unroll
+    for (int hl = 1; hl < 32; hl <<= 1) {
+        const bool upper = lane & hl;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[e], hl);
+            x[e] = upper ? (o - x[e]) : (x[e] + o);
+        }
+    }
+}
+
+__device__ __forceinline__ void apply_signs(float (&x)[4], const uint32_t *sign_bits, int lane) {
+    const uint32_t w = sign_bits[lane >> 3] >> ((4 * lane) & 31);
+#pragma unroll
+    for (int e = 0; e < 4; e++)
+        if ((w >> e) & 1u) x[e] = -x[e];
+}
+
+// y = R x for a warp-held vector: R = binary32(1/sqrt(d)) D H D.
+__device__ __forceinline__ void warp_rotate(float (&x)[4], const uint32_t *sign_bits, float inv_sqrt_d, int lane) {
+    apply_signs(x, sign_bits, lane);
+    warp_wht(x, lane);
+    apply_signs(x, sign_bits, lane);
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] *= inv_sqrt_d;
+}
+
+__device__ __forceinline__ void load_q4(const uint16_t *q, int lane, float (&x)[4]) {
+    const uint2 v = reinterpret_cast<const uint2 *>(q)[lane];
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    x[0] = f0.x;
+    x[1] = f0.y;
+    x[2] = f1.x;
+    x[3] = f1.y;
+}
+
+// fp16 hi and lo = x - hi of a warp-held vector as half2 words (dims 2i, 2i+1
+// in word i): dst[0..63] hi, dst[64..127] lo; returns sum(hi + lo) over the warp.
+__device__ __forceinline__ float store_hilo(uint32_t *dst, const float (&x)[4], int lane) {
+    __half hi[4], lo[4];
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        hi[e] = __float2half_rn(x[e]);
+        lo[e] = __float2half_rn(x[e] - __half2float(hi[e]));
+        s += __half2float(hi[e]) + __half2float(lo[e]);
+    }
+    dst[2 * lane] = pack_half2(hi[0], hi[1]);
+    dst[2 * lane + 1] = pack_half2(hi[2], hi[3]);
+    dst[64 + 2 * lane] = pack_half2(lo[0], lo[1]);
+    dst[64 + 2 * lane + 1] = pack_half2(lo[2], lo[3]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+// ------------------------------------------------------------ dependent launches
+// Let the next kernel of the call start launching CTAs into free SM slots.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the previous kernel of the call has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------ fused combine
+// After a CTA wrote its partial record(s) of (layer, batch b, KV head h): count
+// the CTA; the CTA that brings the count to the group's total merges every
+// partial record of the group (no CTA ever waits for another).  Warp w merges query head h*gqa + w:
+// max-rescale merge of the packed-space and fp16-space sums, one inverse
+// rotation of the packed sum (R is its own inverse), normalisation, store.
+// Called by all threads; returns with all threads synchronised.  `flag` is one
+// int of shared memory.
+__device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const DecodeWorkspace &ws, int layer,
+                                                   int b, int h, int *flag) {
+    __threadfence();
+    __syncthreads();
+    const size_t lbh = (static_cast<size_t>(layer) * dims.B + b) * dims.H + h;
+    if (threadIdx.x == 0) {
+        const int done = atomicAdd(ws.counter + lbh, 1);
+        *flag = (done == ws.lbh_total[lbh] - 1);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (*flag && warp < dims.gqa) {
+        __threadfence();
+        const LayerPlan &lp = ws.layer[layer];
+        const int n_items = lp.n_items[h];
+        const size_t rec_stride = kMaxGqa * kPartStride;
+        float M = kNegInf;
+        for (int ii = 0; ii < n_items; ii++) {
+            const size_t gr = static_cast<size_t>(lp.item[h][ii]) * dims.B + b;
+            const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
+            for (int c = lane; c < np; c += 32)
+                M = fmaxf(M, __ldcg(ws.part + (static_cast<size_t>(p0) + c) * rec_stride + warp * kPartStride));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        float ar[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
+        if (M != kNegInf) {
+            for (int ii = 0; ii < n_items; ii++) {
+                const int item = lp.item[h][ii];
+                const size_t gr = static_cast<size_t>(item) * dims.B + b;
+                const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
+                const bool rot = ws.items[item].kind == TQ_SEG_PACKED;
+                for (int c = 0; c < np; c++) {
+                    const float *rec = ws.part + (static_cast<size_t>(p0) + c) * rec_stride + warp * kPartStride;
+                    const float m = __ldcg(rec);
+                    if (m == kNegInf) continue;
+                    const float f = ex2(m - M);
+                    L += f * __ldcg(rec + 1);
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
+                    float *a = rot ? ar : ao;
+                    a[0] += f * v.x;
+                    a[1] += f * v.y;
+                    a[2] += f * v.z;
+                    a[3] += f * v.w;
+                }
+            }
+        }
+        warp_rotate(ar, lp.sign_bits, dims.inv_sqrt_d, lane);
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        float4 o;
+        o.x = (ar[0] + ao[0]) * inv;
+        o.y = (ar[1] + ao[1]) * inv;
+        o.z = (ar[2] + ao[2]) * inv;
+        o.w = (ar[3] + ao[3]) * inv;
+        const size_t row = ((static_cast<size_t>(layer) * dims.B + b) * dims.Hq + h * dims.gqa + warp) * kD;
+        reinterpret_cast<float4 *>(ws.out + row)[lane] = o;
+    }
+    __syncthreads();
+}
+
+// Largest i in [lo, hi) with items[i].cta_begin <= cta.
+__device__ __forceinline__ int find_item(const WorkItem *items, int lo, int hi, int cta) {
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (items[mid].cta_begin <= cta) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Write one warp's state as a partial record (no cross-warp merge): for each
+// query head c < gqa, m (base-2 units) and l, and the 128 accumulator dims;
+// dim_of(mt, r) is the head dimension of accumulator row r of m-tile mt.
+template <typename DimOf>
+__device__ __forceinline__ void write_warp_partial(WarpState &st, float *rec_base, int gqa, DimOf dim_of) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const float l = warp_sum_g(st.l);
+    if (c < gqa) {
+        float *rec = rec_base + c * kPartStride;
+        if (g == 0) {
+            rec[0] = st.m;
+            rec[1] = l;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) {
+            rec[4 + dim_of(mt, 0)] = st.acc[mt][0] + st.acc[mt][1];
+            rec[4 + dim_of(mt, 1)] = st.acc[mt][2] + st.acc[mt][3];
+        }
+    }
+}
+
+// Largest i in [lo, hi) with items[i].stage_begin <= s.
+__device__ __forceinline__ int find_stage_item(const WorkItem *items, int lo, int hi, long long s) {
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (items[mid].stage_begin <= s) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Equal contiguous ranges of S stages over G persistent CTAs: CTA i takes
+// [i S / G, (i+1) S / G); the CTA holding stage s is the last i with
+// i S / G <= s.
+__host__ __device__ __forceinline__ long long range_begin(long long i, long long S, long long G) { return i * S / G; }
+__host__ __device__ __forceinline__ long long cta_of_stage(long long s, long long S, long long G) {
+    return ((s + 1) * G + S - 1) / S - 1;
+}
+
+}  // namespace dec
+}  // namespace tqk

@@ -67,6 +67,11 @@ struct FittedCodebook {
 std::mutex g_cb_mutex;
 FittedCodebook g_cb[9];
 
+std::mutex &g_cb_mutex_tables() {
+    static std::mutex m;
+    return m;
+}
+
 const FittedCodebook &fit(int bits) {
     std::lock_guard<std::mutex> lock(g_cb_mutex);
     FittedCodebook &cb = g_cb[bits];
@@ -182,24 +187,35 @@ float inv_sqrt_f32(int d) { return static_cast<float>(1.0 / std::sqrt(static_cas
 
 // ---------------------------------------------------------------- decode plan
 struct Plan {
-    std::vector<SegPlan> seg;     // packed segments first, then fp16 segments
+    std::vector<WorkItem> items;      // sorted by class; fp16 items last
     std::vector<LayerPlan> layer;
+    std::vector<ClassLaunch> classes;
     DecodeDims dims{};
-    int n_packed_seg = 0;
-    int kb_max = 1, vb_max = 1;
     bool any_qjl = false;
-    size_t off_layer = 0, off_qrot = 0, off_qorig = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, total = 0;
+    int n_parts = 0;
+    std::vector<int> grp_part, grp_nparts, lbh_total;
+    size_t off_items = 0, off_layer = 0, off_grp_part = 0, off_grp_nparts = 0, off_lbh_total = 0, off_counter = 0;
+    size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The persistent CTA (of G sharing S stages in equal contiguous ranges
+// [i S / G, (i+1) S / G)) that holds stage s; same arithmetic as the kernels.
+long long dec_cta_of_stage(long long s, long long S, long long G) { return ((s + 1) * G + S - 1) / S - 1; }
+
+int class_key(const WorkItem &w) { return w.kind == TQ_SEG_FP16 ? 1 << 20 : (w.kb * 16 + w.vb) * 2 + w.qjl; }
+
+// Validate the views and lay out the work: one item per (layer, segment, KV
+// head) with tokens, split into chunks of `chunk` tokens (a multiple of 64)
+// sized so that each CTA reads a few hundred KB at most while the whole call
+// still spans many CTAs per SM.
 tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, int Hq, int d,
                      const float *S, int jl, Plan &P, bool check_ptrs) {
     if (!layers || n_layers < 1 || B < 1 || H < 1 || H > TQ_MAX_HEADS || Hq < H || Hq % H) return TQ_ERR_ARG;
     if (!pow2(d) || d < 16 || d > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     const int gqa = Hq / H;
     if (d != kD || (gqa != 1 && gqa != 2 && gqa != 4)) return TQ_ERR_UNSUPPORTED;
-    // pass 1: validate, collect total bytes for the chunk size
     double total_bytes = 0.0;
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
@@ -241,117 +257,159 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             }
         }
     }
-    const double target = std::fmin(std::fmax(total_bytes / (sm_count() * 12.0), 8192.0), 262144.0);
-    // pass 2: chunking and the plan, packed segments first
+    const double target = std::fmin(std::fmax(total_bytes / (sm_count() * 24.0), 8192.0), 262144.0);
     P = Plan();
-    P.layer.resize(n_layers);
-    int cta_packed = 0;
-    for (int kind = 0; kind < 2; ++kind) {
-        for (int l = 0; l < n_layers; ++l) {
-            const tq_layer_view &lv = layers[l];
-            LayerPlan &lp = P.layer[l];
-            if (kind == 0) {
-                std::memcpy(lp.sign_bits, lv.rot.sign_bits, sizeof(lp.sign_bits));
-                lp.has_qjl = 0;
-                lp.seg_begin = static_cast<int>(P.seg.size());
-            } else {
-                lp.f16_begin = static_cast<int>(P.seg.size());
-            }
-            for (int s = 0; s < lv.n_segments; ++s) {
-                const tq_segment &sg = lv.seg[s];
-                if (sg.kind != (kind == 0 ? TQ_SEG_PACKED : TQ_SEG_FP16) || sg.n_tokens == 0) continue;
-                const tq_segment_layout &L = sg.layout;
-                SegPlan sp;
-                std::memset(&sp, 0, sizeof(sp));
-                sp.kind = sg.kind;
-                sp.layer = l;
-                sp.n_tokens = sg.n_tokens;
-                sp.capacity = L.capacity;
+    P.layer.assign(n_layers, LayerPlan{});
+    for (int l = 0; l < n_layers; ++l) {
+        const tq_layer_view &lv = layers[l];
+        LayerPlan &lp = P.layer[l];
+        std::memcpy(lp.sign_bits, lv.rot.sign_bits, sizeof(lp.sign_bits));
+        for (int s = 0; s < lv.n_segments; ++s) {
+            const tq_segment &sg = lv.seg[s];
+            if (sg.n_tokens == 0) continue;
+            const tq_segment_layout &L = sg.layout;
+            const size_t cap = static_cast<size_t>(L.capacity);
+            const Offsets o = offsets(&L);
+            for (int h = 0; h < H; ++h) {
+                WorkItem w;
+                std::memset(&w, 0, sizeof(w));
+                w.kind = sg.kind;
+                w.layer = l;
+                w.head = h;
+                w.n_tokens = sg.n_tokens;
                 double bpt;
                 if (sg.kind == TQ_SEG_PACKED) {
-                    const Offsets o = offsets(&L);
-                    sp.kcodes = static_cast<const uint8_t *>(sg.packed.kcodes);
-                    sp.vcodes = static_cast<const uint8_t *>(sg.packed.vcodes);
-                    sp.kscale = sg.packed.kscale;
-                    sp.vscale = sg.packed.vscale;
-                    sp.qjl_signs = static_cast<const uint8_t *>(sg.packed.qjl_signs);
-                    sp.qjl_norm = sg.packed.qjl_norm;
-                    sp.nq = o.nq;
-                    sp.kblock = o.kblock;
-                    sp.vblock = o.vblock;
-                    double per = 0;
-                    for (int h = 0; h < H; ++h) {
-                        sp.koff[h] = o.koff[h];
-                        sp.voff[h] = o.voff[h];
-                        sp.kbits[h] = L.kbits[h];
-                        sp.vbits[h] = L.vbits[h];
-                        sp.qrank[h] = o.qrank[h];
-                        P.kb_max = std::max<int>(P.kb_max, L.kbits[h]);
-                        P.vb_max = std::max<int>(P.vb_max, L.vbits[h]);
-                        if (L.qjl[h]) { P.any_qjl = true; lp.has_qjl = 1; }
-                        per += 16.0 * (L.kbits[h] + L.vbits[h]) + 8 + (L.qjl[h] ? 20 : 0);
+                    w.kc = static_cast<const uint8_t *>(sg.packed.kcodes) + o.koff[h];
+                    w.vc = static_cast<const uint8_t *>(sg.packed.vcodes) + o.voff[h];
+                    w.ks = sg.packed.kscale + h * cap;
+                    w.vs = sg.packed.vscale + h * cap;
+                    w.kstride = o.kblock;
+                    w.vstride = o.vblock;
+                    w.sstride = static_cast<uint32_t>(H * cap);
+                    w.kb = L.kbits[h];
+                    w.vb = L.vbits[h];
+                    w.qjl = L.qjl[h] ? 1 : 0;
+                    if (w.qjl) {
+                        w.qs = static_cast<const uint8_t *>(sg.packed.qjl_signs) + o.qrank[h] * cap * (kJl / 8);
+                        w.qn = sg.packed.qjl_norm + o.qrank[h] * cap;
+                        w.qstride = static_cast<uint32_t>(o.nq * cap);
+                        P.any_qjl = true;
+                        lp.has_qjl = 1;
                     }
-                    bpt = per / H;
+                    bpt = 16.0 * (w.kb + w.vb) + 8 + (w.qjl ? 20 : 0);
                 } else {
-                    sp.kcodes = static_cast<const uint8_t *>(sg.k16);
-                    sp.vcodes = static_cast<const uint8_t *>(sg.v16);
+                    const size_t row = cap * d * 2;  // bytes of one (b, h) block
+                    w.kc = static_cast<const uint8_t *>(sg.k16) + h * row;
+                    w.vc = static_cast<const uint8_t *>(sg.v16) + h * row;
+                    w.kstride = w.vstride = H * row;
+                    w.kb = w.vb = 16;
                     bpt = 4.0 * d;
                 }
                 int chunk = static_cast<int>(std::ceil(target / bpt));
                 chunk = ((chunk + kStageTokens - 1) / kStageTokens) * kStageTokens;
                 const int maxc = ((sg.n_tokens + kStageTokens - 1) / kStageTokens) * kStageTokens;
-                chunk = std::max(kStageTokens, std::min(chunk, maxc));
-                sp.chunk = chunk;
-                sp.n_chunks = (sg.n_tokens + chunk - 1) / chunk;
-                P.seg.push_back(sp);
+                w.chunk = std::max(kStageTokens, std::min(chunk, maxc));
+                w.n_chunks = (sg.n_tokens + w.chunk - 1) / w.chunk;
+                P.items.push_back(w);
             }
-            if (kind == 0) lp.seg_end = static_cast<int>(P.seg.size());
-            else lp.f16_end = static_cast<int>(P.seg.size());
         }
-        if (kind == 0) P.n_packed_seg = static_cast<int>(P.seg.size());
     }
-    // CTA and partial numbering
-    int cta16 = 0, part = 0;
-    for (size_t i = 0; i < P.seg.size(); ++i) {
-        SegPlan &sp = P.seg[i];
-        const long long ctas = static_cast<long long>(B) * H * sp.n_chunks;
-        if (static_cast<int>(i) < P.n_packed_seg) {
-            sp.cta_begin = cta_packed;
-            cta_packed += static_cast<int>(ctas);
+    std::stable_sort(P.items.begin(), P.items.end(),
+                     [](const WorkItem &a, const WorkItem &b) { return class_key(a) < class_key(b); });
+    // classes: packed ones run persistent CTAs over their 64-token stages,
+    // fp16 runs one CTA per (item, batch element, chunk)
+    const int slots = sm_count() * kPackedCtasPerSm;
+    long long cta = 0, stages = 0;
+    for (size_t i = 0; i < P.items.size(); ++i) {
+        WorkItem &w = P.items[i];
+        if (i == 0 || class_key(w) != class_key(P.items[i - 1])) {
+            P.classes.push_back(ClassLaunch{w.kb, w.vb, w.qjl, static_cast<int>(i), static_cast<int>(i), 0, 0});
+            cta = 0;
+            stages = 0;
+        }
+        ClassLaunch &c = P.classes.back();
+        c.item_hi = static_cast<int>(i) + 1;
+        if (w.kind == TQ_SEG_PACKED) {
+            w.n_stages = (w.n_tokens + kStageTokens - 1) / kStageTokens;
+            w.stage_begin = stages;
+            stages += static_cast<long long>(B) * w.n_stages;
+            c.n_stages = stages;
+            c.n_ctas = static_cast<int>(std::min<long long>(stages, slots));
         } else {
-            sp.cta_begin = cta16;
-            cta16 += static_cast<int>(ctas);
+            w.cta_begin = static_cast<int>(cta);
+            cta += static_cast<long long>(B) * w.n_chunks;
+            if (cta > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
+            c.n_ctas = static_cast<int>(cta);
         }
-        sp.part_begin = part;
-        part += static_cast<int>(ctas);
-        if (part < 0 || cta_packed < 0 || cta16 < 0) return TQ_ERR_UNSUPPORTED;
     }
+    // partial records: one per (group, CTA touching it); per (layer, batch, KV
+    // head) the total the fused combine waits for
+    P.grp_part.assign(P.items.size() * B, 0);
+    P.grp_nparts.assign(P.items.size() * B, 0);
+    P.lbh_total.assign(static_cast<size_t>(n_layers) * B * H, 0);
+    long long part = 0;
+    int ci = 0;
+    for (size_t i = 0; i < P.items.size(); ++i) {
+        WorkItem &w = P.items[i];
+        while (static_cast<int>(i) >= P.classes[ci].item_hi) ++ci;
+        const ClassLaunch &c = P.classes[ci];
+        for (int b = 0; b < B; ++b) {
+            int np, portions;
+            if (w.kind == TQ_SEG_PACKED) {
+                // CTAs touching the group; each writes one record per warp
+                const long long gs = w.stage_begin + static_cast<long long>(b) * w.n_stages;
+                portions = static_cast<int>(dec_cta_of_stage(gs + w.n_stages - 1, c.n_stages, c.n_ctas) -
+                                            dec_cta_of_stage(gs, c.n_stages, c.n_ctas) + 1);
+                np = kDecodeWarps * portions;
+            } else {
+                portions = np = w.n_chunks;  // one CTA-merged record per chunk
+            }
+            P.grp_part[i * B + b] = static_cast<int>(part);
+            P.grp_nparts[i * B + b] = np;
+            P.lbh_total[(static_cast<size_t>(w.layer) * B + b) * H + w.head] += portions;
+            part += np;
+        }
+        if (part > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
+        LayerPlan &lp = P.layer[w.layer];
+        lp.item[w.head][lp.n_items[w.head]++] = static_cast<int>(i);
+    }
+    P.n_parts = static_cast<int>(part);
     DecodeDims &D = P.dims;
     D.L = n_layers;
     D.B = B;
     D.H = H;
     D.Hq = Hq;
     D.gqa = gqa;
-    D.n_seg = static_cast<int>(P.seg.size());
-    D.n_packed_ctas = cta_packed;
-    D.n_fp16_ctas = cta16;
-    D.n_parts = part;
+    D.any_qjl = P.any_qjl ? 1 : 0;
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
-    size_t off = align256(sizeof(SegPlan) * std::max<size_t>(P.seg.size(), 1));
+    // offset 0: the error flag (kept in its own 256 bytes so that it has a
+    // fixed place), then the work items
+    P.off_items = 256;
+    size_t off = P.off_items + align256(sizeof(WorkItem) * std::max<size_t>(P.items.size(), 1));
     P.off_layer = off;
     off += align256(sizeof(LayerPlan) * n_layers);
-    P.off_qrot = off;
-    off += align256(nq * d * 4);
-    P.off_qorig = off;
-    off += align256(nq * d * 4);
-    P.off_qjlt = off;
-    off += align256(nq * d * 4);
-    P.off_qsum = off;
-    off += align256(nq * 16);
+    P.off_grp_part = off;
+    off += align256(sizeof(int) * std::max<size_t>(P.grp_part.size(), 1));
+    P.off_grp_nparts = off;
+    off += align256(sizeof(int) * std::max<size_t>(P.grp_nparts.size(), 1));
+    P.off_lbh_total = off;
+    off += align256(static_cast<size_t>(n_layers) * B * H * sizeof(int));
+    P.off_counter = off;
+    off += align256(static_cast<size_t>(n_layers) * B * H * sizeof(int));
+    P.off_qrot = off;  // the uploaded plan ends here
+    if (P.any_qjl) {
+        off += align256(nq * d * 4);
+        P.off_qjlt = off;
+        off += align256(nq * d * 4);
+        P.off_qsum = off;
+        off += align256(nq * 16);
+    } else {
+        P.off_qjlt = P.off_qsum = off;
+    }
     P.off_part = off;
-    off += align256(static_cast<size_t>(std::max(part, 1)) * kMaxGqa * (4 + kD) * 4);
+    off += align256(static_cast<size_t>(std::max(P.n_parts, 1)) * kMaxGqa * (4 + kD) * 4);
     P.total = off;
     return TQ_OK;
 }
@@ -577,32 +635,64 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     // upload the plan (pageable source: staged before the call returns)
     std::vector<uint8_t> host(P.off_qrot, 0);
-    if (!P.seg.empty()) std::memcpy(host.data(), P.seg.data(), sizeof(SegPlan) * P.seg.size());
+    if (!P.items.empty())
+        std::memcpy(host.data() + P.off_items, P.items.data(), sizeof(WorkItem) * P.items.size());
     std::memcpy(host.data() + P.off_layer, P.layer.data(), sizeof(LayerPlan) * P.layer.size());
+    if (!P.grp_part.empty()) {
+        std::memcpy(host.data() + P.off_grp_part, P.grp_part.data(), sizeof(int) * P.grp_part.size());
+        std::memcpy(host.data() + P.off_grp_nparts, P.grp_nparts.data(), sizeof(int) * P.grp_nparts.size());
+    }
+    std::memcpy(host.data() + P.off_lbh_total, P.lbh_total.data(), sizeof(int) * P.lbh_total.size());
     cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
     DecodeWorkspace W;
-    W.seg = reinterpret_cast<SegPlan *>(ws);
+    W.items = reinterpret_cast<WorkItem *>(ws + P.off_items);
     W.layer = reinterpret_cast<LayerPlan *>(ws + P.off_layer);
+    W.grp_part = reinterpret_cast<int *>(ws + P.off_grp_part);
+    W.grp_nparts = reinterpret_cast<int *>(ws + P.off_grp_nparts);
+    W.lbh_total = reinterpret_cast<int *>(ws + P.off_lbh_total);
+    W.counter = reinterpret_cast<int *>(ws + P.off_counter);
+    W.error = reinterpret_cast<int *>(ws);
     W.qrot = reinterpret_cast<uint32_t *>(ws + P.off_qrot);
-    W.qorig = reinterpret_cast<uint32_t *>(ws + P.off_qorig);
     W.qjlt = reinterpret_cast<uint32_t *>(ws + P.off_qjlt);
     W.qsum = reinterpret_cast<float *>(ws + P.off_qsum);
     W.part = reinterpret_cast<float *>(ws + P.off_part);
-    // fp16 codebook values of every width used by a packed segment
-    unsigned short cent_half[kCbTotal];
-    std::memset(cent_half, 0, sizeof(cent_half));
-    for (int i = 0; i < P.n_packed_seg; ++i) {
-        for (int h = 0; h < n_heads; ++h) {
-            const int vb = P.seg[i].vbits[h];
-            const FittedCodebook &cb = fit(vb);
-            for (int k = 0; k < (1 << vb); ++k)
-                cent_half[cb_off(vb) + k] = __half_as_ushort(__float2half_rn(static_cast<float>(cb.level[k])));
+    W.q = static_cast<const uint16_t *>(q);
+    W.out = out;
+    // fp16 codebook values of every value width in use
+    static unsigned short value_half[9][256];
+    static bool value_ready[9] = {};
+    {
+        std::lock_guard<std::mutex> lock(g_cb_mutex_tables());
+        for (const ClassLaunch &c : P.classes) {
+            if (c.kb == 16 || value_ready[c.vb]) continue;
+            const FittedCodebook &cb = fit(c.vb);
+            for (int k = 0; k < 256; ++k)
+                value_half[c.vb][k] =
+                    k < (1 << c.vb) ? __half_as_ushort(__float2half_rn(static_cast<float>(cb.level[k]))) : 0;
+            value_ready[c.vb] = true;
         }
     }
-    e = launch_decode_kernels(P.dims, W, P.n_packed_seg, P.kb_max, P.vb_max, P.any_qjl,
-                              static_cast<const uint16_t *>(q), qjl_S, cent_half, out, s, g_ev_start,
-                              g_ev_stop);
+    // (layer, KV head) groups without any token are written by no CTA: their
+    // output is zero
+    bool empty_group = false;
+    for (int l = 0; l < n_layers; ++l)
+        for (int h = 0; h < n_heads; ++h) empty_group |= P.layer[l].n_items[h] == 0;
+    if (empty_group) {
+        e = cudaMemsetAsync(out, 0, static_cast<size_t>(n_layers) * batch * q_heads * head_dim * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (P.items.empty()) return TQ_OK;
+    e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S, value_half, s,
+                              g_ev_start, g_ev_stop);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_decode_error_flag(const void *workspace, int *flag, void *stream) {
+    if (!workspace || !flag) return TQ_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(flag, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 

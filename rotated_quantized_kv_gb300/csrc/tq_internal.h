@@ -62,60 +62,89 @@ struct DequantParams {
 };
 
 // ----------------------------------------------------------------- decode
-// One entry per (layer, segment) of a decode call, stored in the workspace.
-struct alignas(16) SegPlan {
-    const uint8_t *kcodes, *vcodes;  // packed codes, or fp16 K / V for fp16 segments
-    const float *kscale, *vscale;
-    const uint8_t *qjl_signs;
-    const float *qjl_norm;
-    int kind;          // TQ_SEG_PACKED / TQ_SEG_FP16
-    int layer;
+// One work item per (layer, segment, KV head) of a decode call; its CTAs are
+// (batch element, token chunk) pairs.  Stored in the workspace.
+struct alignas(16) WorkItem {
+    const uint8_t *kc, *vc;   // packed codes of (b=0, head, t=0); fp16 segments: K / V of (b=0, head, t=0)
+    const float *ks, *vs;     // scales of (b=0, head, t=0) (packed)
+    const uint8_t *qs;        // QJL sign records of (b=0, head's rank, t=0)
+    const float *qn;          // QJL norms
+    uint64_t kstride, vstride;  // bytes between batch elements
+    uint32_t sstride;         // floats between batch elements in the scale arrays (H * cap)
+    uint32_t qstride;         // records between batch elements in the QJL arrays (nq * cap)
+    long long stage_begin;    // packed: first 64-token stage of (this item, b = 0) within its class launch
+    int n_stages;             // packed: 64-token stages per batch element
+    int kind;                 // TQ_SEG_PACKED / TQ_SEG_FP16
+    int layer, head;
     int n_tokens;
-    int capacity;
-    int chunk;         // tokens per CTA (multiple of 64)
-    int n_chunks;
-    int cta_begin;     // first CTA of this segment within its kind's launch
-    int part_begin;    // first partial record of this segment
-    int nq;
-    uint32_t kblock, vblock;
-    uint32_t koff[kMaxH], voff[kMaxH];
-    uint8_t kbits[kMaxH], vbits[kMaxH];
-    int8_t qrank[kMaxH];
+    int chunk, n_chunks;      // fp16: tokens per CTA (multiple of 64) and CTAs per batch element
+    int cta_begin;            // fp16: first CTA within its launch
+    int kb, vb, qjl, pad;
 };
 
 struct LayerPlan {
-    int seg_begin, seg_end;          // this layer's packed segments in the SegPlan array
-    int f16_begin, f16_end;          // this layer's fp16 segments
-    int has_qjl;
     uint32_t sign_bits[kD / 32];
+    int has_qjl;
+    int n_items[kMaxH];                    // items of each KV head
+    int item[kMaxH][TQ_MAX_SEGMENTS];      // their indices in the WorkItem array
 };
 
 struct DecodeDims {
     int L, B, H, Hq, gqa;
-    int n_seg;
-    int n_packed_ctas, n_fp16_ctas;  // CTAs of the two split-K kernels
-    int n_parts;                      // partial records (one per CTA)
-    float qk_scale;                   // log2(e) / sqrt(d)
-    float inv_sqrt_d;                 // binary32(1/sqrt(d)) used by the rotations
+    int any_qjl;         // the prep kernel ran (QJL layers read S R q from it)
+    float qk_scale;      // log2(e) / sqrt(d)
+    float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
 };
 
-// Workspace: [SegPlan x n_seg][LayerPlan x L][q prep][partials] (16-aligned parts).
+// Workspace: [WorkItem x n][LayerPlan x L][group tables][counters][q prep]
+// [partials] (256-aligned parts; everything before the q prep is uploaded by
+// every call, counters as zeros).  A group is (item, batch element), index
+// item * B + b; its partial records are grp_part[g] .. grp_part[g] + grp_nparts[g] - 1.
 struct DecodeWorkspace {
-    SegPlan *seg;
+    WorkItem *items;
     LayerPlan *layer;
-    uint32_t *qrot;    // [L][B][Hq][2][d/2] half2 words: hi, lo of R q
-    uint32_t *qorig;   // [L][B][Hq][2][d/2] half2 words: hi, lo of q
-    uint32_t *qjlt;    // [L][B][Hq][2][d/2] half2 words: hi, lo of S R q
-    float *qsum;       // [L][B][Hq][4]: sum(R q), sum(S R q)
-    float *part;       // [n_parts][kMaxGqa][2 + d]: m (log2 units), l, acc
+    int *grp_part;     // [items * B]
+    int *grp_nparts;   // [items * B]
+    int *lbh_total;    // [L][B][H]: CTA portions of (layer, batch, KV head) over all its items
+    int *counter;      // [L][B][H]: CTA portions of (layer, batch, KV head) finished so far
+    int *error;        // set non-zero by a kernel that gave up waiting for its copies
+    uint32_t *qrot;    // [L][B][Hq][2][d/2] half2 words: hi, lo of R q (QJL calls only)
+    uint32_t *qjlt;    // [L][B][Hq][2][d/2] half2 words: hi, lo of S R q (QJL calls only)
+    float *qsum;       // [L][B][Hq][4]: sum(R q), sum(S R q) (QJL calls only)
+    float *part;       // [parts][kMaxGqa][4 + d]: m (log2 units), l, pad, pad, acc
+    const uint16_t *q; // the caller's queries, fp16 [L][B][Hq][d]
+    float *out;        // the caller's output, [L][B][Hq][d]
 };
 
-// Packed-kernel stage geometry: 64 tokens per stage, 16 per warp.
+// Stage geometry of the split-K kernels: 64 tokens per stage, 16 per warp.
 constexpr int kStageTokens = 64;
 constexpr int kDecodeWarps = 4;
 constexpr int kStages = 4;
 
-size_t packed_stage_bytes(int kb_max, int vb_max, bool qjl);
+// A launch of the split-K kernel of one class over items [item_lo, item_hi).
+// Packed classes run persistent CTAs over n_stages 64-token stages (n_ctas of
+// them, each taking an equal contiguous range); fp16 runs one CTA per chunk.
+struct ClassLaunch {
+    int kb, vb, qjl;   // kb == 16: fp16 segments
+    int item_lo, item_hi, n_ctas;
+    long long n_stages;
+};
+
+// Resident CTAs per SM of the packed split-K kernels (registers and shared
+// memory are sized for it).
+constexpr int kPackedCtasPerSm = 4;
+
+typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, int item_lo, int item_hi,
+                                      int n_ctas, long long n_stages, const unsigned short *value_half,
+                                      cudaStream_t s, bool pdl);
+PackedLauncher packed_launcher_kb1(int vb, bool qjl);
+PackedLauncher packed_launcher_kb2(int vb, bool qjl);
+PackedLauncher packed_launcher_kb3(int vb, bool qjl);
+PackedLauncher packed_launcher_kb4(int vb, bool qjl);
+PackedLauncher packed_launcher_kb5(int vb, bool qjl);
+PackedLauncher packed_launcher_kb6(int vb, bool qjl);
+PackedLauncher packed_launcher_kb7(int vb, bool qjl);
+PackedLauncher packed_launcher_kb8(int vb, bool qjl);
 
 // Records a CUDA error for tq_last_cuda_error() and returns TQ_ERR_CUDA.
 tq_status record_cuda_error(cudaError_t e);
@@ -123,9 +152,8 @@ tq_status record_cuda_error(cudaError_t e);
 // Launchers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams &p, cudaStream_t s);
-cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, int n_packed_seg,
-                                  int kb_max, int vb_max, bool any_qjl, const uint16_t *q,
-                                  const float *S, const unsigned short *centroid_half, float *out,
+cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,
+                                  int n_classes, const float *S, const unsigned short (*value_half)[256],
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace tqk

@@ -41,7 +41,7 @@ STATUS = {0: "TQ_OK", -1: "TQ_ERR_ARG", -2: "TQ_ERR_UNSUPPORTED", -3: "TQ_ERR_AL
 EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rotation",
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
-            "tq_set_decode_kernel_events", "tq_decode_attention_static"]
+            "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag"]
 
 
 class TQError(RuntimeError):
@@ -106,6 +106,7 @@ _lib.tq_decode_workspace_size.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I,
 _lib.tq_decode_attention.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, _I, _I, _P, _I, _P, _P,
                                      _P, ctypes.c_size_t, _P]
 _lib.tq_set_decode_kernel_events.argtypes = [_P, _P]
+_lib.tq_decode_error_flag.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
 _lib.tq_decode_attention_static.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, _I, _I, _P, _I, _P,
                                             _P, _P]
 TQ_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -325,6 +326,14 @@ def tq_decode_attention_static(layers, q: torch.Tensor, out: torch.Tensor, n_hea
     _check(_lib.tq_decode_attention_static(arr, L, B, n_heads, Hq, d, _ptr(qjl_S), jl_dim, _ptr(q), _ptr(out),
                                            _stream(stream)), "tq_decode_attention_static")
     return out
+
+
+def tq_decode_error_flag(workspace: torch.Tensor, stream=None) -> int:
+    """Non-zero if a decode call on this workspace stopped a CTA after a bounded
+    wait for its own copies (never expected); synchronises the stream."""
+    f = ctypes.c_int()
+    _check(_lib.tq_decode_error_flag(_ptr(workspace), ctypes.byref(f), _stream(stream)), "tq_decode_error_flag")
+    return f.value
 
 
 def views_array(layers):

@@ -239,6 +239,7 @@ def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
     out = torch.empty(L, B, Hq, 128, device="cuda")
     ws = torch.empty(tq.tq_decode_workspace_size(views, B, H, Hq, 128), dtype=torch.uint8, device="cuda")
     tq.tq_decode_attention(views, q.cuda(), out, ws, H, qjl_S=Sd)
+    assert tq.tq_decode_error_flag(ws) == 0
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     worst = 0.0

@@ -74,8 +74,9 @@ def test_static_workspace_matches_caller_workspace_twice(tq):
 
 
 def test_static_workspace_rejects_oversized_calls(tq):
-    # 512 sequences x 32 query heads need more scratch than the fixed array holds
-    B, H, Hq = 512, 8, 32
+    # 2048 sequences x 8 KV heads: one split-K partial each, more scratch than
+    # the fixed array holds
+    B, H, Hq = 2048, 8, 32
     seg = tq.Fp16Segment(B, H, 128, 16, n_tokens=1)
     views = [tq.layer_view(tq.tq_make_rotation(128, 42), [seg])]
     assert tq.tq_decode_workspace_size(views, B, H, Hq, 128) > tq.TQ_STATIC_WORKSPACE_BYTES
