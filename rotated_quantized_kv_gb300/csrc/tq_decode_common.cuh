@@ -167,6 +167,90 @@ __device__ __forceinline__ void softmax_tile(WarpState &st, float s0, float s1, 
     b1 = *reinterpret_cast<const uint32_t *>(&p23);
 }
 
+// Online softmax over two 16-token tiles with a lazy running max, for the
+// packed kernel.  Thread (g, c) holds the scores (base-2 logits) of tokens g
+// and g+8 of tile A (s[0], s[1]) and tile B (s[2], s[3]) for query head c.
+// Probabilities are taken relative to the head's reference max m; the
+// cross-lane max and the rescale run only when a score exceeds m by more than
+// 8 (so every probability stays <= 2^8, exact enough in fp16).  The P.V B
+// fragments are plain fp16 probabilities times the value scale: column n = g
+// holds head g (g < gqa; zero otherwise), rows = tokens 2c, 2c+1 (b0) and
+// 2c+8, 2c+9 (b1).  The P.V accumulator columns 2c, 2c+1 of lane (g, c) are
+// heads 2c, 2c+1, so a rescale fetches those heads' factors from their owners.
+__device__ __forceinline__ void softmax_pair(WarpState &st, const float (&s)[4], const bool (&ok)[4],
+                                             const float (&vs)[4], int g, int c, int gqa, uint32_t (&b)[4]) {
+    const int lane = threadIdx.x & 31;
+    float smax = kNegInf, vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        smax = fmaxf(smax, ok[i] ? s[i] : kNegInf);
+        vmax = fmaxf(vmax, ok[i] ? vs[i] : 0.f);
+    }
+    // The running max may lag the true one by up to 8 (log2 units), so that
+    // most tiles skip the rescale; weights then reach 2^8 * scale, which stays
+    // inside fp16 while scales are <= 255.  Larger scales rescale exactly
+    // (weights <= scale <= 65504, the fp16 range of the cached values).
+    if (__any_sync(0xffffffffu, smax > st.m + 8.0f || (smax > st.m && vmax > 255.0f))) {
+        const float mnew = fmaxf(st.m, warp_max_g(smax));
+        const float corr = (mnew == kNegInf) ? 1.f : ex2(st.m - mnew);
+        st.l *= corr;
+        const float c0 = __shfl_sync(0xffffffffu, corr, (lane & ~3) | ((2 * c) & 3));
+        const float c1 = __shfl_sync(0xffffffffu, corr, (lane & ~3) | ((2 * c + 1) & 3));
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) {
+            st.acc[mt][0] *= c0;
+            st.acc[mt][1] *= c1;
+            st.acc[mt][2] *= c0;
+            st.acc[mt][3] *= c1;
+        }
+        st.m = mnew;
+    }
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float p = ok[i] ? ex2(s[i] - st.m) : 0.f;
+        st.l += p;
+        w[i] = (ok[i] && c < gqa) ? p * vs[i] : 0.f;  // a select: masked scales may be stale bytes
+    }
+    // transpose: lane (g, c) needs head g's weights of tokens 2c, 2c+1, 2c+8, 2c+9
+    const int src0 = 8 * c + (g & 3), src1 = src0 + 4;
+    const bool col = g < 4;
+#pragma unroll
+    for (int t = 0; t < 2; t++) {
+        const float x0 = __shfl_sync(0xffffffffu, w[2 * t], src0);
+        const float x1 = __shfl_sync(0xffffffffu, w[2 * t], src1);
+        const float x2 = __shfl_sync(0xffffffffu, w[2 * t + 1], src0);
+        const float x3 = __shfl_sync(0xffffffffu, w[2 * t + 1], src1);
+        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+        b[2 * t] = col ? *reinterpret_cast<const uint32_t *>(&h01) : 0u;
+        b[2 * t + 1] = col ? *reinterpret_cast<const uint32_t *>(&h23) : 0u;
+    }
+}
+
+// Partial record of one warp of the packed kernel (accumulator columns 2c,
+// 2c+1 of lane (g, c) are heads 2c, 2c+1; lanes c = h own head h's m and l).
+template <typename DimOf>
+__device__ __forceinline__ void write_warp_partial_pair(WarpState &st, float *rec_base, int gqa, DimOf dim_of) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const float l = warp_sum_g(st.l);
+    if (c < gqa && g == 0) {
+        rec_base[c * kPartStride] = st.m;
+        rec_base[c * kPartStride + 1] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int h = 2 * c + e;
+        if (h < gqa) {
+            float *rec = rec_base + h * kPartStride + 4;
+#pragma unroll
+            for (int mt = 0; mt < 8; mt++) {
+                rec[dim_of(mt, 0)] = st.acc[mt][e];
+                rec[dim_of(mt, 1)] = st.acc[mt][2 + e];
+            }
+        }
+    }
+}
+
 // Merge the four warps' states through shared memory and write the CTA's
 // partial record.  dim_of(mt, r) gives the head dimension of accumulator row r
 // (0: row g, 1: row g+8) of m-tile mt for this thread.

@@ -6,11 +6,11 @@
 // scored in the rotated space q' . yhat with yhat = alpha*code + beta, values
 // summed in the rotated space and rotated back once by the combine kernel.
 //
-// Persistent CTAs of 4 warps share the class's 64-token stages (over all
+// Persistent CTAs of 4 warps share the class's 128-token stages (over all
 // (layer x segment x KV head, batch) groups) in equal contiguous ranges.  One
 // thread streams each CTA's stages into 2-4 shared buffers with TMA bulk copies
 // (cp.async.bulk, completion on an mbarrier per buffer); warp w owns tokens
-// [16w, 16w + 16) of each stage:
+// [32w, 32w + 32) of each stage, two 16-token tiles:
 //   Q.K  mma.m16n8k16: A = 16 tokens x 16 dims of raw key codes written as
 //        fp16 subnormals (code * 2^-24, exact), B = the GQA group's 4 query
 //        heads as fp16 hi/lo column pairs.  Thread (g, c) owns dims
@@ -18,7 +18,8 @@
 //        chosen per bit width so that one or two integer instructions extract
 //        them (KUnpack), and the B fragment is gathered with the same map.
 //   P.V  mma.m16n8k16: A = 16 dims x 16 tokens of fp16 codebook values, B =
-//        probabilities times the value scale (hi/lo columns).  Thread (g, c)
+//        probabilities (<= 2^8 with a lazy running max) times the value scale
+//        in fp16, one column per query head.  Thread (g, c)
 //        owns dims [16g, 16g + 16); codebook lookups are byte permutes (PRMT)
 //        on register-resident tables for 1-4 bits, shared-memory loads above.
 #pragma once
@@ -157,14 +158,14 @@ __device__ __forceinline__ void gather_b(const uint32_t (&q)[16], uint32_t (&b)[
 template <int VB>
 struct VWin {
     static constexpr int NW = (2 * VB + 3) / 4;
-    static __device__ __forceinline__ void load(const uint8_t *rec, int g, uint32_t (&x)[NW]) {
-        const int off = 2 * VB * g;
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(rec + (off & ~3));
+    // p: the record plus the thread's window offset rounded down to 4 bytes;
+    // sh: 8 * (window offset mod 4), 0 or 16
+    static __device__ __forceinline__ void load(const uint8_t *p8, int sh, uint32_t (&x)[NW]) {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(p8);
         if constexpr (VB % 2 == 0) {
 #pragma unroll
             for (int i = 0; i < NW; i++) x[i] = p[i];
         } else {
-            const int sh = (off & 3) * 8;  // 0 or 16
             uint32_t raw[NW];
 #pragma unroll
             for (int i = 0; i < NW; i++) raw[i] = p[i];
@@ -292,15 +293,17 @@ struct ValueTable {
     unsigned short half[256];  // fp16 codebook values of this class's value width
 };
 
+constexpr int kPT = kPackedStageTokens;  // 32 tokens per warp: two 16-token tiles
+
 template <int KB, int VB, bool QJL>
 struct PackedGeom {
     static constexpr int RK = 16 * KB, RV = 16 * VB;
-    static constexpr int offV = kStageTokens * RK;
-    static constexpr int offKS = offV + kStageTokens * RV;
-    static constexpr int offVS = offKS + kStageTokens * 4;
-    static constexpr int offQS = offVS + kStageTokens * 4;
-    static constexpr int offQN = offQS + kStageTokens * 16;
-    static constexpr int stage = QJL ? offQN + kStageTokens * 4 : offQS;
+    static constexpr int offV = kPT * RK;
+    static constexpr int offKS = offV + kPT * RV;
+    static constexpr int offVS = offKS + kPT * 4;
+    static constexpr int offQS = offVS + kPT * 4;
+    static constexpr int offQN = offQS + kPT * 16;
+    static constexpr int stage = QJL ? offQN + kPT * 4 : offQS;
     static constexpr int fixed = (VB >= 5 ? 512 : 0) + kMaxGqa * kD * 4 + 64;  // codebook, queries, flag, barriers
     // as many stages in flight (2..4) as fit with kPackedCtasPerSm CTAs per SM
     static constexpr int fit = (227 * 1024 / kPackedCtasPerSm - 1024 - fixed) / stage;
@@ -408,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
     auto load_next = [&](int k) {
         uint64_t *bar = &full[k % NS];
         uint8_t *dst = smem + (k % NS) * G::stage;
-        const int t0 = lc.st * kStageTokens;
-        const int n = min(kStageTokens, lc.n_tokens - t0);
+        const int t0 = lc.st * kPT;
+        const int n = min(kPT, lc.n_tokens - t0);
         // scale runs are rounded up to 16 bytes: rows hold a multiple of 16 tokens
         const unsigned nk = n * G::RK, nv = n * G::RV, ns = (n * 4 + 15) & ~15u;
         const unsigned total = nk + nv + 2 * ns + (QJL ? n * 16 + ns : 0);
@@ -445,6 +448,11 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
     constexpr float alpha = 16777216.0f * 2.0f / static_cast<float>(1 << KB);  // 2^(1-KB), times 2^24
     constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
     const float qk_scale = dims.qk_scale;
+    // per-thread byte offsets of the key window (codes [32c, 32c+32) of token
+    // row g) and of the value window (codes [16g, 16g+16) of token row 2c)
+    const int koff = g * G::RK + 4 * KB * c;
+    const int voff = 2 * c * G::RV + ((2 * VB * g) & ~3);
+    const int vsh = ((2 * VB * g) & 3) * 8;
 
     // each warp writes its own partial of the current group; then the group's
     // CTA-level count (and possibly the merge)
@@ -452,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
         const long long gr = static_cast<long long>(g_item) * B + g_b;
         const int slot = ws.grp_part[gr] +
                          kDecodeWarps * static_cast<int>(blockIdx.x - cta_of_stage(g_stage0, S, gridDim.x)) + warp;
-        write_warp_partial(st, ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride), gqa,
-                           [g](int mt, int r) { return 16 * g + VUnpack<VB>::dim(mt, r); });
+        write_warp_partial_pair(st, ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride), gqa,
+                                [g](int mt, int r) { return 16 * g + VUnpack<VB>::dim(mt, r); });
         finish_and_combine(dims, ws, g_layer, g_b, g_head, flag);
     };
     // a new group: its identity and the B fragments of its rotated queries
@@ -518,42 +526,56 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
             start_group();
         }
         const uint8_t *buf = smem + (k % NS) * G::stage;
-        const int n = min(kStageTokens, cc.n_tokens - cc.st * kStageTokens);
-        const int t0 = warp * 16;
+        const int n = min(kPT, cc.n_tokens - cc.st * kPT);
         new_group = cc.advance(ws.items, B, k + 1 < n_st);
-        if (t0 >= n) continue;
-        // ---- scores
-        float raw0, raw1;
-        qk_raw<KB>(buf + (t0 + g) * G::RK + 4 * KB * c, buf + (t0 + g + 8) * G::RK + 4 * KB * c, bq, raw0, raw1);
+        const int tA = warp * 32;  // this warp's tiles: tokens [tA, tA + 16) and [tA + 16, tA + 32)
+        if (tA >= n) continue;
+        const bool has_b = tA + 16 < n;
+        // ---- scores of both tiles
+        float sc[4];
         const float *kss = reinterpret_cast<const float *>(buf + G::offKS);
-        float s0 = kss[t0 + g] * (alpha * raw0 + beta * qsum);
-        float s1 = kss[t0 + g + 8] * (alpha * raw1 + beta * qsum);
-        if constexpr (QJL) {
-            float r0, r1;
-            qk_raw<1>(buf + G::offQS + (t0 + g) * 16 + 4 * c, buf + G::offQS + (t0 + g + 8) * 16 + 4 * c, bt, r0, r1);
-            const float *qns = reinterpret_cast<const float *>(buf + G::offQN);
-            constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
-            s0 += gam * qns[t0 + g] * (33554432.0f * r0 - tsum);
-            s1 += gam * qns[t0 + g + 8] * (33554432.0f * r1 - tsum);
-        }
-        s0 *= qk_scale;
-        s1 *= qk_scale;
-        const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
-        uint32_t b0, b1;
-        softmax_tile(st, s0, s1, t0 + g < n, t0 + g + 8 < n, vss[t0 + g], vss[t0 + g + 8], g, c, c < gqa, b0,
-                     b1);
-        // ---- values
-        const uint8_t *vst = buf + G::offV;
-        uint32_t x0[VWin<VB>::NW], x1[VWin<VB>::NW], x2[VWin<VB>::NW], x3[VWin<VB>::NW];
-        VWin<VB>::load(vst + (t0 + 2 * c) * G::RV, g, x0);
-        VWin<VB>::load(vst + (t0 + 2 * c + 1) * G::RV, g, x1);
-        VWin<VB>::load(vst + (t0 + 2 * c + 8) * G::RV, g, x2);
-        VWin<VB>::load(vst + (t0 + 2 * c + 9) * G::RV, g, x3);
-        uint32_t ra[8], rb[8], rc[8], rd[8];
-        VUnpack<VB>::run(x0, x1, ptab, ctab, ra, rb);
-        VUnpack<VB>::run(x2, x3, ptab, ctab, rc, rd);
+        const float *qns = reinterpret_cast<const float *>(buf + G::offQN);
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++) mma16816(st.acc[mt], ra[mt], rb[mt], rc[mt], rd[mt], b0, b1);
+        for (int t = 0; t < 2; t++) {
+            const int t0 = tA + 16 * t;
+            float raw0, raw1;
+            qk_raw<KB>(buf + t0 * G::RK + koff, buf + (t0 + 8) * G::RK + koff, bq, raw0, raw1);
+            float s0 = kss[t0 + g] * (alpha * raw0 + beta * qsum);
+            float s1 = kss[t0 + g + 8] * (alpha * raw1 + beta * qsum);
+            if constexpr (QJL) {
+                float r0, r1;
+                qk_raw<1>(buf + G::offQS + (t0 + g) * 16 + 4 * c, buf + G::offQS + (t0 + g + 8) * 16 + 4 * c, bt, r0,
+                          r1);
+                constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
+                s0 += gam * qns[t0 + g] * (33554432.0f * r0 - tsum);
+                s1 += gam * qns[t0 + g + 8] * (33554432.0f * r1 - tsum);
+            }
+            sc[2 * t] = s0 * qk_scale;
+            sc[2 * t + 1] = s1 * qk_scale;
+        }
+        const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
+        const bool okv[4] = {tA + g < n, tA + g + 8 < n, tA + 16 + g < n, tA + 24 + g < n};
+        const float vsv[4] = {vss[tA + g], vss[tA + g + 8], vss[tA + 16 + g], vss[tA + 24 + g]};
+        uint32_t bp[4];
+        softmax_pair(st, sc, okv, vsv, g, c, gqa, bp);
+        // ---- values of both tiles
+        const uint8_t *vst = buf + G::offV;
+#pragma unroll
+        for (int t = 0; t < 2; t++) {
+            if (t == 1 && !has_b) break;
+            const uint8_t *vb = vst + (tA + 16 * t) * G::RV;
+            uint32_t x0[VWin<VB>::NW], x1[VWin<VB>::NW], x2[VWin<VB>::NW], x3[VWin<VB>::NW];
+            VWin<VB>::load(vb + voff, vsh, x0);
+            VWin<VB>::load(vb + voff + G::RV, vsh, x1);
+            VWin<VB>::load(vb + voff + 8 * G::RV, vsh, x2);
+            VWin<VB>::load(vb + voff + 9 * G::RV, vsh, x3);
+            uint32_t ra[8], rb[8], rc[8], rd[8];
+            VUnpack<VB>::run(x0, x1, ptab, ctab, ra, rb);
+            VUnpack<VB>::run(x2, x3, ptab, ctab, rc, rd);
+#pragma unroll
+            for (int mt = 0; mt < 8; mt++)
+                mma16816(st.acc[mt], ra[mt], rb[mt], rc[mt], rd[mt], bp[2 * t], bp[2 * t + 1]);
+        }
     }
     // every thread waits for the previous grid of the call before its last
     // merge, so that this grid's completion implies that of all earlier ones

@@ -316,7 +316,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     }
     std::stable_sort(P.items.begin(), P.items.end(),
                      [](const WorkItem &a, const WorkItem &b) { return class_key(a) < class_key(b); });
-    // classes: packed ones run persistent CTAs over their 64-token stages,
+    // classes: packed ones run persistent CTAs over their 128-token stages,
     // fp16 runs one CTA per (item, batch element, chunk)
     const int slots = sm_count() * kPackedCtasPerSm;
     long long cta = 0, stages = 0;
@@ -330,7 +330,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         ClassLaunch &c = P.classes.back();
         c.item_hi = static_cast<int>(i) + 1;
         if (w.kind == TQ_SEG_PACKED) {
-            w.n_stages = (w.n_tokens + kStageTokens - 1) / kStageTokens;
+            w.n_stages = (w.n_tokens + kPackedStageTokens - 1) / kPackedStageTokens;
             w.stage_begin = stages;
             stages += static_cast<long long>(B) * w.n_stages;
             c.n_stages = stages;

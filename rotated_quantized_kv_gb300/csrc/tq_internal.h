@@ -116,13 +116,15 @@ struct DecodeWorkspace {
     float *out;        // the caller's output, [L][B][Hq][d]
 };
 
-// Stage geometry of the split-K kernels: 64 tokens per stage, 16 per warp.
+// Stage geometry of the split-K kernels: the fp16 kernel takes 64 tokens per
+// stage (16 per warp), the packed kernels 128 (32 per warp, two 16-token tiles).
 constexpr int kStageTokens = 64;
+constexpr int kPackedStageTokens = 128;
 constexpr int kDecodeWarps = 4;
 constexpr int kStages = 4;
 
 // A launch of the split-K kernel of one class over items [item_lo, item_hi).
-// Packed classes run persistent CTAs over n_stages 64-token stages (n_ctas of
+// Packed classes run persistent CTAs over n_stages 128-token stages (n_ctas of
 // them, each taking an equal contiguous range); fp16 runs one CTA per chunk.
 struct ClassLaunch {
     int kb, vb, qjl;   // kb == 16: fp16 segments
