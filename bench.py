@@ -15,7 +15,12 @@ reads ~0.8 GB, more than L2, so no flush is needed between steps.
 plus q and output bytes, per step) over all ranks; `compress` reports KV
 compression in Mtok/s (one token = K and V of all 8 heads of one layer).
 
-    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Other workloads (`--workload w1|w3|w4|w5`, with `--batch`/`--context` for the
+w5 sweep) time decode steps over a prompt compressed once: w3 the age tiers
+(fp16 / K4V4 / K3V2 / K2V1) at 131072 positions, w4 per-head widths with QJL
+at batch 16, w5 uniform K3V3 behind 128 sinks.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload wN]
 
 Under torchrun each rank runs an independent replica (weak scaling); the time
 is the max over ranks.  `--impl reference` times the CPU oracle instead on a
@@ -44,8 +49,7 @@ from rotated_quantized_kv_gb300 import workloads as W  # noqa: E402
 METRIC = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"] if os.path.exists(
     os.path.join(ROOT, "BASELINE.json")) else "decode-attn HBM GB/s over packed KV; KV compress Mtok/s"
 NOMINAL_HBM_GBS = 8000.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_packed_w2_traffic.json")
-DECODE_SRC = os.path.join(ROOT, "rotated_quantized_kv_gb300", "csrc", "tq_decode.cu")
+DECODE_SRCS = ("tq_decode_packed.cuh", "tq_decode_common.cuh", "tq_decode.cu", "tq_internal.h")
 
 
 def measured_peaks():
@@ -114,120 +118,36 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
 
 
-# --------------------------------------------------------------------- w2 model
-class W2:
-    """The w2 cache on one GPU: per layer an fp16 sink segment, a packed segment
-    (capacity for the prompt plus the decode steps) and an fp16 buffer segment
-    that views a pool of the decode tokens."""
-
-    def __init__(self, tq, steps_cap=256, device="cuda", seed=1002):
-        self.tq = tq
-        w = self.w = W.WORKLOADS["w2"]
-        self.L, self.B, self.H, self.Hq, self.d = w.layers, w.batch, w.kv_heads, w.q_heads, w.head_dim
-        self.T, self.sinks, self.chunk = w.context, w.sinks, w.chunk
-        self.steps_cap = steps_cap
-        self.n_prompt_packed = self.T - self.sinks
-        cap = ((self.n_prompt_packed + steps_cap + 15) // 16) * 16
-        self.rots, self.sink, self.packed = [], [], []
-        # decode tokens of every layer: [L][B][H][steps][d], one tensor so that a
-        # step's new token of all layers is one strided slice
-        self.pool_k_all = torch.empty(self.L, self.B, self.H, steps_cap, self.d, dtype=torch.float16, device=device)
-        self.pool_v_all = torch.empty_like(self.pool_k_all)
-        for l in range(self.L):
-            rot = tq.tq_make_rotation(self.d, W.ROTATION_SEED + l)
-            K, V = W.kv_block(w, l, self.B, self.T, seed, device=device)
-            s = tq.Fp16Segment(self.B, self.H, self.d, self.sinks, n_tokens=self.sinks,
-                               k=K[:, :, :self.sinks].contiguous(), v=V[:, :, :self.sinks].contiguous())
-            p = tq.PackedSegment(tq.make_layout(self.B, self.H, self.d, cap, w.kbits, w.vbits))
-            tq.tq_compress(p, rot, K[:, :, self.sinks:], V[:, :, self.sinks:], t_begin=0)
-            p.n_tokens = self.n_prompt_packed
-            pk, pv = W.kv_block(w, l, self.B, steps_cap, seed, device=device, token_offset=self.T)
-            self.pool_k_all[l].copy_(pk)
-            self.pool_v_all[l].copy_(pv)
-            self.rots.append(rot)
-            self.sink.append(s)
-            self.packed.append(p)
-            del K, V, pk, pv
-        self.pool_k = [self.pool_k_all[l] for l in range(self.L)]
-        self.pool_v = [self.pool_v_all[l] for l in range(self.L)]
-        self.qpool = W.query_pool(w, steps_cap, self.B, seed, device=device)  # [steps][L][B][Hq][d]
-        self.q = self.qpool[0]
-        self.buf = [tq.Fp16Segment(self.B, self.H, self.d, steps_cap, n_tokens=1, k=self.pool_k[l],
-                                   v=self.pool_v[l]) for l in range(self.L)]
-        self.views = [tq.layer_view(self.rots[l], [self.sink[l], self.packed[l], self.buf[l]])
-                      for l in range(self.L)]
-        self.arr = tq.views_array(self.views)
-        self.out = torch.empty(self.L, self.B, self.Hq, self.d, device=device)
-        self.ws = torch.empty(self.max_workspace(), dtype=torch.uint8, device=device)
-        torch.cuda.synchronize()
-
-    def max_workspace(self):
-        best = 0
-        for s in (0, self.steps_cap - 1):
-            self.set_step(s)
-            best = max(best, self.tq.tq_decode_workspace_size(list(self.arr), self.B, self.H, self.Hq, self.d))
-        return best + (1 << 20)
-
-    def set_step(self, s):
-        """Point the segment views at decode step s (0-based within the pool)."""
-        s %= self.steps_cap
-        w0 = (s // self.chunk) * self.chunk
-        esz = self.pool_k[0].element_size()
-        for l in range(self.L):
-            seg = self.arr[l].seg
-            seg[1].n_tokens = self.n_prompt_packed + w0
-            seg[2].n_tokens = s - w0 + 1
-            seg[2].k16 = self.pool_k[l].data_ptr() + w0 * self.d * esz
-            seg[2].v16 = self.pool_v[l].data_ptr() + w0 * self.d * esz
-        return w0
-
-    def compress_window(self, s):
-        """At the first step of a new 64-token window, compress the previous one."""
-        s %= self.steps_cap
-        if s == 0 or s % self.chunk:
-            return 0
-        w0 = s - self.chunk
-        for l in range(self.L):
-            self.tq.tq_compress(self.packed[l], self.rots[l], self.pool_k[l][:, :, w0:s],
-                                self.pool_v[l][:, :, w0:s], t_begin=self.n_prompt_packed + w0)
-        return self.L
-
-    def step(self, s, q=None):
-        launches = self.compress_window(s)
-        self.set_step(s)
-        qq = self.qpool[s % self.steps_cap] if q is None else q
-        self.tq.tq_decode_attention(None, qq, self.out, self.ws, self.H, views=self.arr)
-        return launches + 2  # split-K over fp16 segments, split-K over packed segments
-
-    def step_bytes(self, s):
-        s %= self.steps_cap
-        w0 = (s // self.chunk) * self.chunk
-        per_tok_packed = self.H * (16 * (self.w.kbits + self.w.vbits) + 8)
-        per_tok_fp16 = self.H * self.d * 2 * 2
-        packed = self.L * (self.n_prompt_packed + w0) * per_tok_packed * self.B
-        fp16 = self.L * (self.sinks + s - w0 + 1) * per_tok_fp16 * self.B
-        qo = self.L * self.B * self.Hq * self.d * (2 + 4)
-        return packed, fp16 + qo
+def traffic_for(workload: str):
+    """DRAM bytes per launch of the packed kernel from an ncu capture, if it was
+    taken on the current kernel sources (null otherwise)."""
+    path = os.path.join(ROOT, "profiles", f"decode_packed_{workload}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    t = json.load(open(path))
+    return t.get("traffic_bytes_per_launch") if t.get("source_sha256") == kernel_sha() else None
 
 
-def run_ours(args, rank, world):
-    from rotated_quantized_kv_gb300 import build
-    build.build()
-    from rotated_quantized_kv_gb300 import tq
-    dev = torch.cuda.current_device()
-    m = W2(tq)
-    K, Wm = args.steps, args.warmup
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SRCS:
+        h.update(open(os.path.join(ROOT, "rotated_quantized_kv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def timed_region(tq, step, nbytes, K, Wm, world, dev):
+    """Warm-up, then K timed steps between a barrier and a synchronize on both
+    sides; the packed kernels of each step are bracketed by their own events.
+    step(i) runs step i and returns its launches; nbytes(i) -> (packed, total)."""
     for s in range(Wm):
-        m.step(s)
+        step(s)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for a, b in ev:  # torch creates the CUDA event at its first record; the library re-records it
         a.record()
         b.record()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
-    total_bytes = 0
-    packed_bytes = []
+    launches, total_bytes, packed_bytes = 0, 0, []
     if world > 1:
         torch.distributed.barrier()
     with ClockSampler(dev) as clk:
@@ -236,32 +156,91 @@ def run_ours(args, rank, world):
         for i in range(K):
             s = Wm + i
             tq.tq_set_decode_kernel_events(*ev[i])
-            launches += m.step(s)
-            pb, ob = m.step_bytes(s)
+            launches += step(s)
+            pb, tb = nbytes(s)
             packed_bytes.append(pb)
-            total_bytes += pb + ob
+            total_bytes += tb
         stop.record()
         tq.tq_set_decode_kernel_events(None, None)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        # the timed region lasts milliseconds, shorter than the 200 ms sampling
-        # period: keep the same steps running for ~1.5 s so the clock samples
-        # see the GPU under this load
+        # a short timed region sees few 200 ms clock samples: keep the same
+        # steps running for ~1.5 s so the samples see the GPU under this load
         t_end = time.time() + 1.5
         s = Wm + K
         while time.time() < t_end:
-            for _ in range(20):
-                m.step(s)
+            for _ in range(4):
+                step(s)
                 s += 1
             torch.cuda.synchronize()
     ms = start.elapsed_time(stop)
     ms_all = torch.tensor([ms], device="cuda")
     if world > 1:
         torch.distributed.all_reduce(ms_all, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_all.item())
-    kern_ms = [a.elapsed_time(b) for a, b in ev]
-    clocks = clk.summary()
+    return {"ms": float(ms_all.item()), "kern_ms": [a.elapsed_time(b) for a, b in ev], "launches": launches,
+            "total_bytes": total_bytes, "packed_bytes": packed_bytes, "clocks": clk.summary()}
+
+
+def time_compress(tq, jobs, reps=3):
+    """Mean ms of one pass over `jobs` (callables that each launch one compress)."""
+    for j in jobs:
+        j()
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(reps):
+        for j in jobs:
+            j()
+    c1.record()
+    torch.cuda.synchronize()
+    return c0.elapsed_time(c1) / reps
+
+
+def result_line(args, world, m, t, e2e, comp, config, workload):
+    peak, peak_kind = measured_peaks()
+    K = args.steps
+    value = world * t["total_bytes"] / (t["ms"] * 1e-3) / 1e9
+    kern_avg_ms = float(np.mean(t["kern_ms"]))
+    achieved = float(np.mean(t["packed_bytes"])) / (kern_avg_ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(t["ms"] / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": config,
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "tokens_per_s": round(world * m.B * K / (t["ms"] * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_packed_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_for(workload), "bytes_per_launch": int(np.mean(t["packed_bytes"])),
+                     "avg_launch_ms": round(kern_avg_ms, 5)},
+        "compress": {"value": round(comp["mtok"], 1), "unit": "Mtok/s", "ms_per_layer": round(comp["ms"], 4),
+                     "tokens_per_layer": comp["tokens"],
+                     "achieved_gbs": round(comp["bytes"] / (comp["ms"] * 1e-3) / 1e9, 1),
+                     "frac_of_peak": round(comp["bytes"] / (comp["ms"] * 1e-3) / 1e9 / peak, 4)},
+        "e2e": {"value": round(world * e2e["bytes"] / (e2e["ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["bi"], "d2h_bytes_per_step": e2e["bo"]},
+        "gpu_launches": t["launches"],
+        "clocks": t["clocks"],
+    }
+
+
+def run_w2(args, rank, world, tq):
+    from rotated_quantized_kv_gb300.model_cache import ChunkedDecodeCache
+    dev = torch.cuda.current_device()
+    m = ChunkedDecodeCache()
+    K, Wm = args.steps, args.warmup
+    torch.cuda.synchronize()
+    t = timed_region(tq, m.step, lambda s: (lambda pb, ob: (pb, pb + ob))(*m.step_bytes(s)), K, Wm, world, dev)
 
     # ---- e2e: q and the new token's K/V from pinned host memory, output back to host
     qh = m.qpool.cpu().pin_memory()
@@ -272,11 +251,9 @@ def run_ours(args, rank, world):
     vstage = torch.empty_like(kstage)
     outh = torch.empty(m.out.shape, dtype=torch.float32).pin_memory()
     qdev = torch.empty_like(m.q)
-    bi = m.q.numel() * 2 + kstage.numel() * 2 * 2
-    bo = m.out.numel() * 4
+    e2e = {"bi": m.q.numel() * 2 + kstage.numel() * 2 * 2, "bo": m.out.numel() * 4, "bytes": 0}
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_bytes = 0
     e0.record()
     for i in range(K):
         s = (Wm + i) % m.steps_cap
@@ -288,134 +265,199 @@ def run_ours(args, rank, world):
         m.step(s, q=qdev)
         outh.copy_(m.out, non_blocking=True)
         pb, ob = m.step_bytes(s)
-        e2e_bytes += pb + ob
+        e2e["bytes"] += pb + ob
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e["ms"] = e0.elapsed_time(e1)
 
-    # ---- compress throughput: re-compress every layer's prompt (one step = 32 calls)
-    comp_tokens = m.n_prompt_packed * m.L * m.B
+    # ---- compress throughput: re-compress every layer's prompt (one pass = 32 calls)
     nsrc = 8  # distinct inputs cycled: 8 x 66 MB, more than L2
     src = [W.kv_block(m.w, l, m.B, m.n_prompt_packed, 1002, device="cuda", token_offset=777)
            for l in range(nsrc)]
     scratch = [tq.PackedSegment(m.packed[l].layout) for l in range(nsrc)]
-    for l in range(m.L):  # warm-up
-        tq.tq_compress(scratch[l % nsrc], m.rots[l], *src[l % nsrc])
-    torch.cuda.synchronize()
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    creps = 3
-    c0.record()
-    for _ in range(creps):
-        for l in range(m.L):
-            tq.tq_compress(scratch[l % nsrc], m.rots[l], *src[l % nsrc])
-    c1.record()
-    torch.cuda.synchronize()
-    cms = c0.elapsed_time(c1) / creps
-    c_mtok = comp_tokens / (cms * 1e-3) / 1e6
-    c_bytes = comp_tokens * m.H * (m.d * 2 * 2 + 16 * (m.w.kbits + m.w.vbits) + 8)
-    peak, peak_kind = measured_peaks()
+    jobs = [(lambda l=l: tq.tq_compress(scratch[l % nsrc], m.rots[l], *src[l % nsrc])) for l in range(m.L)]
+    ms = time_compress(tq, jobs) / m.L
+    tokens = m.n_prompt_packed * m.B
+    comp = {"ms": ms, "tokens": tokens, "mtok": tokens / (ms * 1e-3) / 1e6,
+            "bytes": tokens * m.H * (m.d * 2 * 2 + 16 * (m.w.kbits + m.w.vbits) + 8)}
+    config = {"workload": m.w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
+              "q_heads": m.Hq, "head_dim": m.d, "kbits": m.w.kbits, "vbits": m.w.vbits,
+              "sinks": m.sinks, "chunk": m.chunk, "l2": "inputs larger than L2 (~0.8 GB read per step)",
+              "parallelism": f"replicas x{world}"}
+    return result_line(args, world, m, t, e2e, comp, config, "w2")
 
-    value = world * total_bytes / (ms_max * 1e-3) / 1e9
-    kern_avg_ms = float(np.mean(kern_ms))
-    achieved = float(np.mean(packed_bytes)) / (kern_avg_ms * 1e-3) / 1e9
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        t = json.load(open(TRAFFIC_FILE))
-        h = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
-        if t.get("source_sha256") == h:
-            traffic = t.get("traffic_bytes_per_launch")
-    result = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": Wm,
-        "ms_per_step": round(ms_max / K, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": m.w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
-                   "q_heads": m.Hq, "head_dim": m.d, "kbits": m.w.kbits, "vbits": m.w.vbits,
-                   "sinks": m.sinks, "chunk": m.chunk, "l2": "inputs larger than L2 (~0.8 GB read per step)",
-                   "parallelism": f"replicas x{world}"},
-        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "tokens_per_s": round(world * m.B * K / (ms_max * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "decode_packed_kernel", "achieved": round(achieved, 1),
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "bytes_per_launch": int(np.mean(packed_bytes)),
-                     "avg_launch_ms": round(kern_avg_ms, 5)},
-        "compress": {"value": round(c_mtok, 1), "unit": "Mtok/s", "ms_per_model": round(cms, 4),
-                     "achieved_gbs": round(c_bytes / (cms * 1e-3) / 1e9, 1),
-                     "frac_of_peak": round(c_bytes / (cms * 1e-3) / 1e9 / peak, 4)},
-        "e2e": {"value": round(world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
-        "gpu_launches": launches,
-        "clocks": clocks,
-    }
+
+def run_static(args, rank, world, tq):
+    from rotated_quantized_kv_gb300.model_cache import StaticCache
+    dev = torch.cuda.current_device()
+    w = W.WORKLOADS[args.workload]
+    seed = 1000 + int(args.workload[1:])
+    m = StaticCache(w, batch=args.batch, context=args.context, seed=seed)
+    K, Wm = args.steps, args.warmup
+    nq = 4
+    qpool = W.query_pool(w, nq, m.B, seed, device="cuda")
+    pb, ob = m.step_bytes()
+    torch.cuda.synchronize()
+
+    # launches per step: the QJL query prep (if any), the fp16 kernel (if any
+    # fp16 segment), one persistent kernel per packed (kbits, vbits, QJL) class
+    n_launch = (1 if w.qjl_max_bits else 0) + int(any(not si.packed for segs in m.layers for si in segs)) + len(
+        {(si.kbits[h], si.vbits[h], si.qjl[h]) for segs in m.layers for si in segs if si.packed for h in range(m.H)})
+
+    def step(s):
+        m.decode(qpool[s % nq])
+        return n_launch
+    t = timed_region(tq, step, lambda s: (pb, pb + ob), K, Wm, world, dev)
+
+    # ---- e2e: queries from pinned host memory, output back to host
+    qh = qpool.cpu().pin_memory()
+    outh = torch.empty(m.out.shape, dtype=torch.float32).pin_memory()
+    qdev = torch.empty_like(qpool[0])
+    e2e = {"bi": qdev.numel() * 2, "bo": m.out.numel() * 4, "bytes": 0}
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        qdev.copy_(qh[i % nq], non_blocking=True)
+        m.decode(qdev)
+        outh.copy_(m.out, non_blocking=True)
+        e2e["bytes"] += pb + ob
+    e1.record()
+    torch.cuda.synchronize()
+    e2e["ms"] = e0.elapsed_time(e1)
+
+    # ---- compress throughput: each layer's packed segments from its fp16
+    # prompt, cycling distinct layers' inputs until they exceed 4x L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    layer_in = 2 * m.B * m.H * m.T * m.d * 2
+    nsrc = max(1, min(m.L, -(-4 * l2 // layer_in)))
+    if layer_in * nsrc > 24 * (1 << 30):
+        nsrc = 1
+    src = [W.kv_block(w, l, m.B, m.T, seed + 7, device="cuda") for l in range(nsrc)]
+    scr, calls = {}, []
+    for l in range(m.L):
+        Kx, Vx = src[l % nsrc]
+        for si in m.layers[l]:
+            if not si.packed:
+                continue
+            # one scratch segment per distinct layout (the layer's own widths)
+            lay = si.seg.layout
+            key = (si.pos0, tuple(lay.kbits), tuple(lay.vbits), tuple(lay.qjl))
+            if key not in scr:
+                scr[key] = tq.PackedSegment(si.seg.layout)
+            calls.append(lambda Kx=Kx, Vx=Vx, si=si, sg=scr[key], rot=m.rots[l]: tq.tq_compress(
+                sg, rot, Kx[:, :, si.pos0:si.pos0 + si.n], Vx[:, :, si.pos0:si.pos0 + si.n],
+                qjl_S=m.qjl_S if any(si.qjl) else None))
+    ms = time_compress(tq, calls) / m.L
+    tokens = m.packed_tokens() // m.L
+    cbytes = sum(m.B * si.n * (m.H * m.d * 4 + si.bytes_per_token(m.d)) for si in m.layers[0] if si.packed)
+    comp = {"ms": ms, "tokens": tokens, "mtok": tokens / (ms * 1e-3) / 1e6, "bytes": cbytes}
+    del src, scr, calls
+    plan = [(si.pos0, si.n, sorted(set(zip(si.kbits, si.vbits, si.qjl)))) for si in m.layers[0]]
+    config = {"workload": w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
+              "q_heads": m.Hq, "head_dim": m.d,
+              "segments_layer0": [{"pos0": p, "n": n, "k_v_qjl": [list(x) for x in kb]} for p, n, kb in plan],
+              "l2": f"inputs larger than L2 ({(pb + ob) / 1e9:.2f} GB read per step)",
+              "parallelism": f"replicas x{world}"}
+    return result_line(args, world, m, t, e2e, comp, config, args.workload)
+
+
+def run_ours(args, rank, world):
+    from rotated_quantized_kv_gb300 import build
+    build.build()
+    from rotated_quantized_kv_gb300 import tq
+    if args.workload == "w2":
+        res = run_w2(args, rank, world, tq)
+        wl = W.WORKLOADS["w2"]
+    else:
+        res = run_static(args, rank, world, tq)
+        wl = W.WORKLOADS[args.workload]
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
-    return result
+        res["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
+    return res
 
 
 # --------------------------------------------------------------------- oracle arm
-def oracle_sample(layers=1, packed_tokens=4096, seed=1002):
-    """A bounded sample of w2 for the CPU oracle: `layers` layers with the 128
-    sinks, the first `packed_tokens` packed tokens and a 1-token buffer.
-    Returns (list of (segments, sign), queries, algorithmic bytes)."""
+def oracle_plan(w, context):
+    """Layer 0's segments as (pos0, n, kbits[H], vbits[H], qjl[H]), planned on
+    the oracle side (its own tier ranges; the seeded bit-width draw)."""
     from oracle import oracle as O
-    w = W.WORKLOADS["w2"]
+    H = w.kv_heads
+    if w.tiers:
+        return [(s, e - s, [W.tier_bits(t)[0]] * H, [W.tier_bits(t)[1]] * H, [0] * H)
+                for t, s, e in O.tier_ranges(context)]
+    if w.per_head_bits:
+        kb = [int(b) for b in W.draw_head_bits(w.layers, H)[0]]
+        return [(0, context, kb, list(kb), [int(b <= w.qjl_max_bits) for b in kb])]
+    out = [(0, w.sinks, [16] * H, [16] * H, [0] * H)] if w.sinks else []
+    return out + [(w.sinks, context - w.sinks, [w.kbits] * H, [w.vbits] * H, [0] * H)]
+
+
+def oracle_sample(w, budget_tokens=4096, seed=1002):
+    """A bounded sample of a workload for the CPU oracle: layer 0, batch element
+    0, each segment of the layer's plan cut to its share of `budget_tokens`
+    positions (fp16 segments of <= 128 positions kept whole).  Returns
+    (segments, sign, q, S, algorithmic bytes, description)."""
+    from oracle import oracle as O
     H, d = w.kv_heads, w.head_dim
-    out, nbytes = [], 0
-    for l in range(layers):
-        K, V = W.kv_block(w, l, 1, w.sinks + packed_tokens, seed)
-        sign = O.signs(d, W.ROTATION_SEED + l)
-        sink = O.Fp16Segment(1, H, d, w.sinks, n_tokens=w.sinks)
-        sink.k16[:] = K[:, :, :w.sinks].numpy().view(np.uint16).ravel()
-        sink.v16[:] = V[:, :, :w.sinks].numpy().view(np.uint16).ravel()
-        cap = ((packed_tokens + 15) // 16) * 16
-        seg = O.PackedSegment(1, H, d, cap, [w.kbits] * H, [w.vbits] * H)
-        O.compress(seg, K[:, :, w.sinks:].numpy().view(np.uint16), V[:, :, w.sinks:].numpy().view(np.uint16),
-                   sign)
-        q = W.queries(w, l, 1, seed).numpy()
-        out.append(([sink, seg], sign, q))
-        nbytes += packed_tokens * H * (16 * (w.kbits + w.vbits) + 8) + w.sinks * H * d * 4 + w.q_heads * d * 6
-    return out, nbytes
+    plan = oracle_plan(w, w.context)
+    total = sum(n for _, n, *_ in plan)
+    cut = []
+    for pos0, n, kb, vb, qj in plan:
+        m = n if (kb[0] == 16 and n <= 128) else max(16, min(n, round(n * budget_tokens / total)))
+        cut.append((pos0, m, kb, vb, qj))
+    span = max(p + m for p, m, *_ in cut)
+    K, V = W.kv_block(w, 0, 1, span, seed)
+    sign = O.signs(d, W.ROTATION_SEED)
+    S = O.qjl_matrix(128, d, W.QJL_SEED) if w.qjl_max_bits else None
+    segs, nbytes = [], w.q_heads * d * 6
+    for pos0, m, kb, vb, qj in cut:
+        if kb[0] == 16:
+            sg = O.Fp16Segment(1, H, d, m, n_tokens=m)
+            sg.k16[:] = K[:, :, pos0:pos0 + m].numpy().view(np.uint16).ravel()
+            sg.v16[:] = V[:, :, pos0:pos0 + m].numpy().view(np.uint16).ravel()
+            nbytes += m * H * d * 4
+        else:
+            sg = O.PackedSegment(1, H, d, ((m + 15) // 16) * 16, kb, vb, qj)
+            O.compress(sg, K[:, :, pos0:pos0 + m].numpy().view(np.uint16),
+                       V[:, :, pos0:pos0 + m].numpy().view(np.uint16), sign, S)
+            sg.n_tokens = m
+            nbytes += m * sum(d // 8 * (a + b) + 8 + (20 if q else 0) for a, b, q in zip(kb, vb, qj))
+        segs.append(sg)
+    q = W.queries(w, 0, 1, seed).numpy()
+    desc = (f"{w.name} layer 0, batch element 0: " +
+            " + ".join(f"{m} {'fp16' if kb[0] == 16 else 'packed'}" for _, m, kb, _, _ in cut) +
+            f" tokens, {w.q_heads} query heads")
+    return segs, sign, q, S, nbytes, desc
 
 
-def cpu_baseline(seconds=10.0):
+def cpu_baseline(w, seconds=10.0):
     from oracle import oracle as O
-    sample, nbytes = oracle_sample(layers=1, packed_tokens=4096)
+    segs, sign, q, S, nbytes, desc = oracle_sample(w)
     reps, t = 0, 0.0
     while t < seconds or reps == 0:
         t0 = time.perf_counter()
-        for segs, sign, q in sample:
-            O.decode_attention(segs, q, sign, W.KV_HEADS)
+        O.decode_attention(segs, q, sign, w.kv_heads, S=S)
         t += time.perf_counter() - t0
         reps += 1
     return {"value": round(reps * nbytes / t / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"w2 layer 0: 128 fp16 sinks + 4096 packed K8/V3 tokens, 32 query heads; "
-                      f"{reps} repetitions, {t:.1f} s of single-threaded C"}
+            "sample": f"{desc}; {reps} repetitions, {t:.1f} s of single-threaded C"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
     from oracle import oracle as O
-    sample, nbytes = oracle_sample(layers=1, packed_tokens=1024)
+    w = W.WORKLOADS[args.workload]
+    segs, sign, q, S, nbytes, desc = oracle_sample(w, budget_tokens=1024)
     for _ in range(args.warmup):
-        for segs, sign, q in sample:
-            O.decode_attention(segs, q, sign, W.KV_HEADS)
+        O.decode_attention(segs, q, sign, w.kv_heads, S=S)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        for segs, sign, q in sample:
-            O.decode_attention(segs, q, sign, W.KV_HEADS)
+        O.decode_attention(segs, q, sign, w.kv_heads, S=S)
     dt = time.perf_counter() - t0
     v = args.steps * nbytes / dt / 1e9
-    w = W.WORKLOADS["w2"]
-    desc = "w2 layer 0: 128 fp16 sinks + 1024 packed K8/V3 tokens, 32 query heads (CPU oracle, 1 thread)"
+    desc += " (CPU oracle, 1 thread)"
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -435,6 +477,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="w2", choices=sorted(W.WORKLOADS),
+                    help="w2 (default): the chunked decode workload the metric is quoted on; "
+                         "w1, w3, w4, w5: decode steps over a prompt compressed once")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (w1, w3-w5)")
+    ap.add_argument("--context", type=int, default=None, help="override the workload's context (w1, w3-w5)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

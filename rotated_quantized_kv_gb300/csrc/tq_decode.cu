@@ -133,8 +133,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // -------------------------------------------------------------- prep kernel
 // Calls with QJL heads only: one warp per (layer, batch, query head) computes
-// q' = R q and t = S q' (fp16 hi/lo words and sums) for the QJL split-K
-// kernels, which read them after griddepcontrol.wait.
+// q' = R q (normalised by a power of two) and t = S q' (fp16 hi/lo words),
+// with sum q', sum t and the power of two, for the QJL split-K kernels, which
+// read them after griddepcontrol.wait.
 __global__ void __launch_bounds__(kThreads)
     decode_prep_kernel(const DecodeDims dims, const DecodeWorkspace ws, const float *S) {
     __shared__ float qsh[kThreads / 32][kD];
@@ -147,7 +148,13 @@ __global__ void __launch_bounds__(kThreads)
     float x[4];
     load_q4(ws.q + static_cast<size_t>(wid) * kD, lane, x);
     warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
-    const float qs = store_hilo(ws.qrot + static_cast<size_t>(wid) * kD, x, lane);
+    // q' / 2^e with its largest coordinate in [0.5, 1) (the packed kernels
+    // scale the B fragment up by powers of two); t = S q' from q' itself
+    const float f = warp_pow2_norm(x);
+    float xn[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) xn[e] = x[e] * f;
+    const float qs = store_hilo(ws.qrot + static_cast<size_t>(wid) * kD, xn, lane) / f;
     float ts = 0.f;
     if (lp.has_qjl) {
 #pragma unroll
@@ -166,6 +173,7 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) {
         ws.qsum[static_cast<size_t>(wid) * 4] = qs;
         ws.qsum[static_cast<size_t>(wid) * 4 + 1] = ts;
+        ws.qsum[static_cast<size_t>(wid) * 4 + 2] = 1.0f / f;
     }
 }
 

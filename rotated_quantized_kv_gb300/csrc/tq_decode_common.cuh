@@ -109,12 +109,14 @@ __device__ __forceinline__ float warp_sum_g(float v) {
 // group; acc holds the P.V accumulator fragment (8 m-tiles x 4).
 struct WarpState {
     float m, l;
+    float wsum;  // sum of the weights p * value scale (linear value decodes only)
     float acc[8][4];
 };
 
 __device__ __forceinline__ void init_state(WarpState &st) {
     st.m = kNegInf;
     st.l = 0.f;
+    st.wsum = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; mt++)
 #pragma unroll
@@ -174,17 +176,27 @@ __device__ __forceinline__ void softmax_tile(WarpState &st, float s0, float s1, 
 // cross-lane max and the rescale run only when a score exceeds m by more than
 // 8 (so every probability stays <= 2^8, exact enough in fp16).  The P.V B
 // fragments are plain fp16 probabilities times the value scale: column n = g
-// holds head g (g < gqa; zero otherwise), rows = tokens 2c, 2c+1 (b0) and
-// 2c+8, 2c+9 (b1).  The P.V accumulator columns 2c, 2c+1 of lane (g, c) are
-// heads 2c, 2c+1, so a rescale fetches those heads' factors from their owners.
+// holds head g (columns of heads >= gqa carry values nobody reads), rows =
+// tokens 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1).  The P.V accumulator columns 2c,
+// 2c+1 of lane (g, c) are heads 2c, 2c+1, so a rescale fetches those heads'
+// factors from their owners.  FULL: all 32 tokens valid (no masking).  WSUM:
+// also accumulate the weights (for value decodes that are affine in the code).
+template <bool FULL, bool WSUM>
 __device__ __forceinline__ void softmax_pair(WarpState &st, const float (&s)[4], const bool (&ok)[4],
-                                             const float (&vs)[4], int g, int c, int gqa, uint32_t (&b)[4]) {
+                                             const float (&vs)[4], int g, int c, uint32_t (&b)[4]) {
     const int lane = threadIdx.x & 31;
-    float smax = kNegInf, vmax = 0.f;
+    float smax, vmax;
+    if constexpr (FULL) {
+        smax = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+        vmax = fmaxf(fmaxf(vs[0], vs[1]), fmaxf(vs[2], vs[3]));
+    } else {
+        smax = kNegInf;
+        vmax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        smax = fmaxf(smax, ok[i] ? s[i] : kNegInf);
-        vmax = fmaxf(vmax, ok[i] ? vs[i] : 0.f);
+        for (int i = 0; i < 4; i++) {
+            smax = fmaxf(smax, ok[i] ? s[i] : kNegInf);
+            vmax = fmaxf(vmax, ok[i] ? vs[i] : 0.f);
+        }
     }
     // The running max may lag the true one by up to 8 (log2 units), so that
     // most tiles skip the rescale; weights then reach 2^8 * scale, which stays
@@ -194,6 +206,7 @@ __device__ __forceinline__ void softmax_pair(WarpState &st, const float (&s)[4],
         const float mnew = fmaxf(st.m, warp_max_g(smax));
         const float corr = (mnew == kNegInf) ? 1.f : ex2(st.m - mnew);
         st.l *= corr;
+        if constexpr (WSUM) st.wsum *= corr;
         const float c0 = __shfl_sync(0xffffffffu, corr, (lane & ~3) | ((2 * c) & 3));
         const float c1 = __shfl_sync(0xffffffffu, corr, (lane & ~3) | ((2 * c + 1) & 3));
 #pragma unroll
@@ -208,13 +221,19 @@ __device__ __forceinline__ void softmax_pair(WarpState &st, const float (&s)[4],
     float w[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const float p = ok[i] ? ex2(s[i] - st.m) : 0.f;
-        st.l += p;
-        w[i] = (ok[i] && c < gqa) ? p * vs[i] : 0.f;  // a select: masked scales may be stale bytes
+        if constexpr (FULL) {
+            const float p = ex2(s[i] - st.m);
+            st.l += p;
+            w[i] = p * vs[i];
+        } else {
+            const float p = ok[i] ? ex2(s[i] - st.m) : 0.f;
+            st.l += p;
+            w[i] = ok[i] ? p * vs[i] : 0.f;  // a select: masked scales may be stale bytes
+        }
     }
+    if constexpr (WSUM) st.wsum += (w[0] + w[1]) + (w[2] + w[3]);
     // transpose: lane (g, c) needs head g's weights of tokens 2c, 2c+1, 2c+8, 2c+9
     const int src0 = 8 * c + (g & 3), src1 = src0 + 4;
-    const bool col = g < 4;
 #pragma unroll
     for (int t = 0; t < 2; t++) {
         const float x0 = __shfl_sync(0xffffffffu, w[2 * t], src0);
@@ -222,17 +241,23 @@ __device__ __forceinline__ void softmax_pair(WarpState &st, const float (&s)[4],
         const float x2 = __shfl_sync(0xffffffffu, w[2 * t + 1], src0);
         const float x3 = __shfl_sync(0xffffffffu, w[2 * t + 1], src1);
         const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-        b[2 * t] = col ? *reinterpret_cast<const uint32_t *>(&h01) : 0u;
-        b[2 * t + 1] = col ? *reinterpret_cast<const uint32_t *>(&h23) : 0u;
+        b[2 * t] = *reinterpret_cast<const uint32_t *>(&h01);
+        b[2 * t + 1] = *reinterpret_cast<const uint32_t *>(&h23);
     }
 }
 
 // Partial record of one warp of the packed kernel (accumulator columns 2c,
 // 2c+1 of lane (g, c) are heads 2c, 2c+1; lanes c = h own head h's m and l).
-template <typename DimOf>
-__device__ __forceinline__ void write_warp_partial_pair(WarpState &st, float *rec_base, int gqa, DimOf dim_of) {
+// fin(mt, r, acc, W): the accumulator value of row r of m-tile mt as written
+// (W: the head's summed weights, for value decodes that are affine in the code).
+template <typename DimOf, typename Fin>
+__device__ __forceinline__ void write_warp_partial_pair(WarpState &st, float *rec_base, int gqa, DimOf dim_of,
+                                                        Fin fin) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const float l = warp_sum_g(st.l);
+    const float W = warp_sum_g(st.wsum);
+    const float W0 = __shfl_sync(0xffffffffu, W, (lane & ~3) | ((2 * c) & 3));
+    const float W1 = __shfl_sync(0xffffffffu, W, (lane & ~3) | ((2 * c + 1) & 3));
     if (c < gqa && g == 0) {
         rec_base[c * kPartStride] = st.m;
         rec_base[c * kPartStride + 1] = l;
@@ -240,12 +265,13 @@ __device__ __forceinline__ void write_warp_partial_pair(WarpState &st, float *re
 #pragma unroll
     for (int e = 0; e < 2; e++) {
         const int h = 2 * c + e;
+        const float Wh = e ? W1 : W0;
         if (h < gqa) {
             float *rec = rec_base + h * kPartStride + 4;
 #pragma unroll
             for (int mt = 0; mt < 8; mt++) {
-                rec[dim_of(mt, 0)] = st.acc[mt][e];
-                rec[dim_of(mt, 1)] = st.acc[mt][2 + e];
+                rec[dim_of(mt, 0)] = fin(mt, 0, st.acc[mt][e], Wh);
+                rec[dim_of(mt, 1)] = fin(mt, 1, st.acc[mt][2 + e], Wh);
             }
         }
     }
@@ -347,6 +373,18 @@ __device__ __forceinline__ void load_q4(const uint16_t *q, int lane, float (&x)[
     x[1] = f0.y;
     x[2] = f1.x;
     x[3] = f1.y;
+}
+
+// Power of two f such that f * max|x| over the warp lies in [0.5, 1) (1 for
+// an all-zero or non-finite vector): scaling by f is exact.
+__device__ __forceinline__ float warp_pow2_norm(const float (&x)[4]) {
+    float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (!(m > 0.f) || !(m < __builtin_huge_valf())) return 1.f;
+    int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 126;  // m in [2^(e-1), 2^e)
+    e = max(-100, min(100, e));
+    return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 }
 
 // fp16 hi and lo = x - hi of a warp-held vector as half2 words (dims 2i, 2i+1

@@ -11,31 +11,55 @@
 // thread streams each CTA's stages into 2-4 shared buffers with TMA bulk copies
 // (cp.async.bulk, completion on an mbarrier per buffer); warp w owns tokens
 // [32w, 32w + 32) of each stage, two 16-token tiles:
-//   Q.K  mma.m16n8k16: A = 16 tokens x 16 dims of raw key codes written as
-//        fp16 subnormals (code * 2^-24, exact), B = the GQA group's 4 query
-//        heads as fp16 hi/lo column pairs.  Thread (g, c) owns dims
+//   Q.K  mma.m16n8k16: A = 16 tokens x 16 dims of raw key codes left at their
+//        bit offset s inside an fp16 half (code * 2^(s-24), a subnormal, so one
+//        AND extracts two codes), B = the GQA group's 4 query heads as fp16
+//        hi/lo column pairs, each element scaled by 2^(kA-s), so that every
+//        product is q * code * 2^(kA-24).  Thread (g, c) owns dims
 //        [32c, 32c + 32) of a record; which two codes share an A register is
-//        chosen per bit width so that one or two integer instructions extract
-//        them (KUnpack), and the B fragment is gathered with the same map.
-//   P.V  mma.m16n8k16: A = 16 dims x 16 tokens of fp16 codebook values, B =
-//        probabilities (<= 2^8 with a lazy running max) times the value scale
-//        in fp16, one column per query head.  Thread (g, c)
-//        owns dims [16g, 16g + 16); codebook lookups are byte permutes (PRMT)
-//        on register-resident tables for 1-4 bits, shared-memory loads above.
+//        chosen per bit width (KUnpack) and the B fragment uses the same map.
+//   P.V  mma.m16n8k16: A = 16 dims x 16 tokens of values, B = probabilities
+//        (<= 2^8 with a lazy running max) times the value scale in fp16, one
+//        column per query head.  Thread (g, c) owns dims [16g, 16g + 16).  An A
+//        register pairs one dim of two tokens; its decoding depends on the
+//        value width (VDec):
+//          1 bit   the codebook is +-c1, affine in the code: A holds the code
+//                  bit as a subnormal and the record is finished as
+//                  c1 * (2 acc - sum of weights);
+//          2, 3    one shared-memory load per register from a table of fp16
+//                  pairs (c[x], c[y]) indexed by both tokens' codes, one
+//                  column of the table per lane (no bank conflicts);
+//          4       byte permutes (PRMT) on register-resident tables;
+//          5-8     per-code loads from a shared-memory codebook.
 #pragma once
+
+#include <type_traits>
 
 #include "tq_decode_common.cuh"
 
 namespace tqk {
 namespace dec {
 
+// bits of the fp16 power of two 2^k (0 <= k <= 15)
+__host__ __device__ constexpr uint32_t half_pow2_bits(int k) { return static_cast<uint32_t>(15 + k) << 10; }
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 // ------------------------------------------------------------------- keys
 // run(): 16 A registers from the thread's KB-word window (codes 0..31 of its
-// 32-dim slice); register r feeds k-step r/2 (r even: a0/a1 rows, r odd: a2/a3).
-// dim(r, half): the code index (0..31) in the low (0) / high (1) fp16 half.
+// 32-dim slice); register r feeds k-step r/2 (r even: a0/a1 rows, r odd:
+// a2/a3).  dim(r, half): the code index (0..31) in the low (0) / high (1) fp16
+// half; shift(r, half): its bit offset s inside the half (the half holds
+// code * 2^(s-24)).  kA: the largest shift; the B fragment holds q * 2^(kA-s).
 template <int KB>
-struct KUnpack {  // 3, 5, 6, 7 bits: pairs (j, j+16) from 16-bit slices
+struct KUnpack {  // 5, 6, 7 bits: pairs (j, j+16) from 16-bit slices, shifted down
+    static constexpr int kA = 0;
     static constexpr __host__ __device__ int dim(int r, int half) { return r + 16 * half; }
+    static constexpr __host__ __device__ int shift(int, int) { return 0; }
     static __device__ __forceinline__ void run(const uint32_t (&w)[KB], uint32_t (&a)[16]) {
         constexpr uint32_t M = (1u << KB) - 1u;
         constexpr uint32_t MM = M | (M << 16);
@@ -64,38 +88,83 @@ struct KUnpack {  // 3, 5, 6, 7 bits: pairs (j, j+16) from 16-bit slices
 };
 
 template <>
-struct KUnpack<1> {  // pairs (r, r+16) of one word
+struct KUnpack<1> {  // codes (r, r+16) at bit r (r < 10) or, after >> 10, bit r - 10
+    static constexpr int kA = 9;
     static constexpr __host__ __device__ int dim(int r, int half) { return r + 16 * half; }
+    static constexpr __host__ __device__ int shift(int r, int) { return r < 10 ? r : r - 10; }
     static __device__ __forceinline__ void run(const uint32_t (&w)[1], uint32_t (&a)[16]) {
+        const uint32_t t = w[0] >> 10;
 #pragma unroll
-        for (int r = 0; r < 16; r++) a[r] = (w[0] >> r) & 0x00010001u;
+        for (int r = 0; r < 16; r++) a[r] = (r < 10 ? w[0] : t) & (0x00010001u << shift(r, 0));
     }
 };
 
 template <>
-struct KUnpack<2> {  // word i, shift 2e: codes (16i + e, 16i + e + 8)
+struct KUnpack<2> {  // word i: codes (16i + e, 16i + 8 + e), e < 5 in place, e >= 5 after >> 10
+    static constexpr int kA = 8;
     static constexpr __host__ __device__ int dim(int r, int half) { return 16 * (r >> 3) + (r & 7) + 8 * half; }
+    static constexpr __host__ __device__ int shift(int r, int) { return (r & 7) < 5 ? 2 * (r & 7) : 2 * (r & 7) - 10; }
     static __device__ __forceinline__ void run(const uint32_t (&w)[2], uint32_t (&a)[16]) {
+        const uint32_t t[2] = {w[0] >> 10, w[1] >> 10};
 #pragma unroll
-        for (int r = 0; r < 16; r++) a[r] = (w[r >> 3] >> (2 * (r & 7))) & 0x00030003u;
+        for (int r = 0; r < 16; r++) a[r] = ((r & 7) < 5 ? w[r >> 3] : t[r >> 3]) & (0x00030003u << shift(r, 0));
     }
 };
 
 template <>
-struct KUnpack<4> {  // word i, shift 4e: codes (8i + e, 8i + e + 4)
+struct KUnpack<3> {  // byte-aligned sources from PRMT; code j sits at bit (3j mod 8) of its half
+    static constexpr int kA = 7;
+    static constexpr __host__ __device__ int dim(int r, int half) { return (r < 8 ? r : r + 8) + 8 * half; }
+    static constexpr __host__ __device__ int shift(int r, int half) { return (3 * dim(r, half)) & 7; }
+    static __device__ __forceinline__ void run(const uint32_t (&w)[3], uint32_t (&a)[16]) {
+        // sources (bytes of the 12-byte window in the low half | high half):
+        // S0 (0,1 | 3,4): codes 0-2 | 8-10; S1 (1,2 | 4,5): 3-5 | 11-13;
+        // S2 (2 | 5): 6-7 | 14-15; S3 (6,7 | 9,10): 16-18 | 24-26;
+        // S4 (7,8 | 10,11): 19-21 | 27-29; S5 (8 | 11): 22-23 | 30-31
+        const uint32_t S[6] = {prmt(w[0], w[1], 0x4310u), prmt(w[0], w[1], 0x5421u), prmt(w[0], w[1], 0x6532u),
+                               prmt(w[1], w[2], 0x6532u), prmt(w[1], w[2], 0x7643u), prmt(w[2], w[2], 0x3310u)};
+        constexpr int src[16] = {0, 0, 0, 1, 1, 1, 2, 2, 3, 3, 3, 4, 4, 4, 5, 5};
+#pragma unroll
+        for (int r = 0; r < 16; r++) a[r] = S[src[r]] & (0x00070007u << shift(r, 0));
+    }
+};
+
+template <>
+struct KUnpack<4> {  // word i: codes (8i + e, 8i + 4 + e); e = 0, 1 in place, e = 2, 3 after >> 8
+    static constexpr int kA = 4;
     static constexpr __host__ __device__ int dim(int r, int half) { return 8 * (r >> 2) + (r & 3) + 4 * half; }
+    static constexpr __host__ __device__ int shift(int r, int) { return (r & 1) ? 4 : 0; }
     static __device__ __forceinline__ void run(const uint32_t (&w)[4], uint32_t (&a)[16]) {
 #pragma unroll
-        for (int r = 0; r < 16; r++) a[r] = (w[r >> 2] >> (4 * (r & 3))) & 0x000F000Fu;
+        for (int i = 0; i < 4; i++) {
+            const uint32_t t = w[i] >> 8;
+            a[4 * i] = w[i] & 0x000F000Fu;
+            a[4 * i + 1] = w[i] & 0x00F000F0u;
+            a[4 * i + 2] = t & 0x000F000Fu;
+            a[4 * i + 3] = t & 0x00F000F0u;
+        }
     }
 };
 
 template <>
 struct KUnpack<8> {  // bytes (2e, 2e+1) of word i zero-extended: codes (4i + 2e, 4i + 2e + 1)
+    static constexpr int kA = 0;
     static constexpr __host__ __device__ int dim(int r, int half) { return 4 * (r >> 1) + 2 * (r & 1) + half; }
+    static constexpr __host__ __device__ int shift(int, int) { return 0; }
     static __device__ __forceinline__ void run(const uint32_t (&w)[8], uint32_t (&a)[16]) {
 #pragma unroll
         for (int r = 0; r < 16; r++) a[r] = prmt(w[r >> 1], 0u, (r & 1) ? 0x4342u : 0x4140u);
+    }
+};
+
+// QJL sign bits (1 bit per projection): pairs (r, r+16) shifted down to bit 0.
+struct SignUnpack {
+    static constexpr int kA = 0;
+    static constexpr __host__ __device__ int dim(int r, int half) { return r + 16 * half; }
+    static constexpr __host__ __device__ int shift(int, int) { return 0; }
+    static __device__ __forceinline__ void run(const uint32_t (&w)[1], uint32_t (&a)[16]) {
+#pragma unroll
+        for (int r = 0; r < 16; r++) a[r] = (w[0] >> r) & 0x00010001u;
     }
 };
 
@@ -119,15 +188,15 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[NW], const uint8_t *p) {
     }
 }
 
-// Raw Q.K (in units of 2^-24 code units) of tokens g and g+8 for head c.
-template <int KB>
+// Raw Q.K of tokens g and g+8 for head c (units of 2^(KU::kA - 24) code units).
+template <typename KU, int NW>
 __device__ __forceinline__ void qk_raw(const uint8_t *rec0, const uint8_t *rec1, const uint32_t (&bq)[16],
                                        float &raw0, float &raw1) {
-    uint32_t w0[KB], w1[KB], a0[16], a1[16];
+    uint32_t w0[NW], w1[NW], a0[16], a1[16];
     lds_words(w0, rec0);
     lds_words(w1, rec1);
-    KUnpack<KB>::run(w0, a0);
-    KUnpack<KB>::run(w1, a1);
+    KU::run(w0, a0);
+    KU::run(w1, a1);
     float e[4] = {0.f, 0.f, 0.f, 0.f}, o[4] = {0.f, 0.f, 0.f, 0.f};  // two chains for ILP
 #pragma unroll
     for (int kk = 0; kk < 8; kk += 2) {
@@ -141,7 +210,7 @@ __device__ __forceinline__ void qk_raw(const uint8_t *rec0, const uint8_t *rec1,
 
 // B fragment (16 registers) of a natural-order fp16 vector slice: words q[0..15]
 // hold dims 2i, 2i+1 of the thread's 32-dim slice; register r pairs dims
-// KU::dim(r, 0) and KU::dim(r, 1).
+// KU::dim(r, 0) and KU::dim(r, 1), each scaled by 2^(kA - shift) (exact).
 template <typename KU>
 __device__ __forceinline__ void gather_b(const uint32_t (&q)[16], uint32_t (&b)[16]) {
 #pragma unroll
@@ -149,12 +218,19 @@ __device__ __forceinline__ void gather_b(const uint32_t (&q)[16], uint32_t (&b)[
         const int d0 = KU::dim(r, 0), d1 = KU::dim(r, 1);
         const uint32_t sel = ((d0 & 1) ? 0x32u : 0x10u) | (((d1 & 1) ? 0x76u : 0x54u) << 8);
         b[r] = prmt(q[d0 >> 1], q[d1 >> 1], sel);
+        if constexpr (KU::kA > 0) {
+            const uint32_t f = half_pow2_bits(KU::kA - KU::shift(r, 0)) |
+                               (half_pow2_bits(KU::kA - KU::shift(r, 1)) << 16);
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&b[r]),
+                                      *reinterpret_cast<const __half2 *>(&f));
+            b[r] = *reinterpret_cast<const uint32_t *>(&v);
+        }
     }
 }
 
 // ------------------------------------------------------------------- values
 // Window of the thread's 16 value codes (bits [16g VB, 16g VB + 16 VB) of the
-// record) as little-endian words.
+// record) as little-endian words, for the 5- to 8-bit decoders.
 template <int VB>
 struct VWin {
     static constexpr int NW = (2 * VB + 3) / 4;
@@ -181,36 +257,30 @@ struct PrmtTable {
     uint32_t tl[4], th[4];
 };
 
-// 8 nibbles of eight 3-bit codes (bits 0..23 of v; higher bits ignored).
-__device__ __forceinline__ uint32_t spread3(uint32_t v) {
-    uint32_t t = (v & 0x00000FFFu) | ((v << 4) & 0x0FFF0000u);
-    t = (t & 0x003F003Fu) | ((t << 2) & 0x3F003F00u);
-    return (t & 0x07070707u) | ((t << 1) & 0x70707070u);
+// Per-thread constants of the value decoders.
+struct VCtx {
+    int off;                     // byte offset of the thread's window in token row 2c of a tile
+    int sh;                      // funnel shift (0/16) or PRMT selector of the window
+    uint32_t tab;                // shared address of this lane's column of the pair table
+    PrmtTable pt;                // 4-bit codebook bytes
+    const unsigned short *ctab;  // 5- to 8-bit codebook in shared memory
+};
+
+// Byte offset of pair-table entry F[POS .. POS + BITS) with entries 2^TS bytes
+// apart (a multiply or a high multiply, both off the integer-logic pipe).
+template <int POS, int BITS, int TS>
+__device__ __forceinline__ uint32_t pair_off(uint32_t F) {
+    const uint32_t f = F & (((1u << BITS) - 1u) << POS);
+    if constexpr (POS <= TS) return f * (1u << (TS - POS));
+    else return __umulhi(f, 1u << (32 - POS + TS));
 }
 
-// Lookup of 4 codes given as selector nibbles [x_j, x_j', y_j, y_j'] (3-bit
-// indices, bit 3 clear): returns half2(c[x_j], c[y_j]) and half2(c[x_j'], c[y_j']).
-template <int VB>
-__device__ __forceinline__ void lookup4(uint32_t sel, const PrmtTable &t, uint32_t &ra, uint32_t &rb) {
-    uint32_t pl, ph;
-    if constexpr (VB <= 3) {
-        pl = prmt(t.tl[0], t.tl[1], sel);
-        ph = prmt(t.th[0], t.th[1], sel);
-    } else {  // 4 bits: two 8-entry tables, chosen per byte by the nibble's bit 3
-        const uint32_t s7 = sel & 0x7777u;
-        const uint32_t hb = ((sel >> 1) & 0x4444u) | 0x3210u;
-        pl = prmt(prmt(t.tl[0], t.tl[1], s7), prmt(t.tl[2], t.tl[3], s7), hb);
-        ph = prmt(prmt(t.th[0], t.th[1], s7), prmt(t.th[2], t.th[3], s7), hb);
-    }
-    ra = prmt(pl, ph, 0x6240u);
-    rb = prmt(pl, ph, 0x7351u);
-}
-
-// dim(mt, r): the code index (0..15) of accumulator row r (0: row g, 1: row
-// g+8) of m-tile mt.  run(): the A registers of one token pair (x, y) for all
-// eight m-tiles: ra[mt] for row g, rb[mt] for row g+8.
-template <int VB>
-struct VUnpack {  // 5..8 bits: shared-memory table, codes (2mt, 2mt+1)
+// pair(): the A registers of one token pair (x = the row at p, y = the next
+// row) for all eight m-tiles: ra[mt] for accumulator row g (dim(mt, 0)),
+// rb[mt] for row g+8 (dim(mt, 1)); the low half of each register is token x.
+template <int VB, int TS>
+struct VDec {  // 5..8 bits: shared-memory codebook, codes (2mt, 2mt+1)
+    static constexpr bool kLinear = false;
     static constexpr __host__ __device__ int dim(int mt, int r) { return 2 * mt + r; }
     template <int NW>
     static __device__ __forceinline__ uint32_t code(const uint32_t (&x)[NW], int j) {
@@ -218,72 +288,132 @@ struct VUnpack {  // 5..8 bits: shared-memory table, codes (2mt, 2mt+1)
         const uint32_t v = (sh + VB <= 32) ? (x[wi] >> sh) : __funnelshift_r(x[wi], x[wi + 1], sh);
         return v & ((1u << VB) - 1u);
     }
-    static __device__ __forceinline__ void run(const uint32_t (&x)[VWin<VB>::NW], const uint32_t (&y)[VWin<VB>::NW],
-                                               const PrmtTable &, const unsigned short *ctab, uint32_t (&ra)[8],
-                                               uint32_t (&rb)[8]) {
+    static __device__ __forceinline__ void pair(const uint8_t *p, int RV, const VCtx &cx, uint32_t (&ra)[8],
+                                                uint32_t (&rb)[8]) {
+        uint32_t x[VWin<VB>::NW], y[VWin<VB>::NW];
+        VWin<VB>::load(p + cx.off, cx.sh, x);
+        VWin<VB>::load(p + cx.off + RV, cx.sh, y);
 #pragma unroll
         for (int mt = 0; mt < 8; mt++) {
-            ra[mt] = static_cast<uint32_t>(ctab[code(x, 2 * mt)]) | (static_cast<uint32_t>(ctab[code(y, 2 * mt)]) << 16);
-            rb[mt] = static_cast<uint32_t>(ctab[code(x, 2 * mt + 1)]) |
-                     (static_cast<uint32_t>(ctab[code(y, 2 * mt + 1)]) << 16);
+            ra[mt] = static_cast<uint32_t>(cx.ctab[code(x, 2 * mt)]) |
+                     (static_cast<uint32_t>(cx.ctab[code(y, 2 * mt)]) << 16);
+            rb[mt] = static_cast<uint32_t>(cx.ctab[code(x, 2 * mt + 1)]) |
+                     (static_cast<uint32_t>(cx.ctab[code(y, 2 * mt + 1)]) << 16);
         }
     }
 };
 
-template <>
-struct VUnpack<1> {  // nibble selectors (Z >> e) & 0x1111 with Z = bytes interleaved: codes (e, e+4)
-    static constexpr __host__ __device__ int dim(int mt, int r) { return 8 * (mt >> 2) + (mt & 3) + 4 * r; }
-    static __device__ __forceinline__ void run(const uint32_t (&x)[1], const uint32_t (&y)[1], const PrmtTable &t,
-                                               const unsigned short *, uint32_t (&ra)[8], uint32_t (&rb)[8]) {
-        const uint32_t Z = prmt(x[0], y[0], 0x5140u);  // [x.b0, y.b0, x.b1, y.b1]
+template <int TS>
+struct VDec<1, TS> {  // code j at bit j (j < 10) or, after >> 10, bit j - 10: dims (mt, mt + 8)
+    static constexpr bool kLinear = true;
+    static constexpr __host__ __device__ int dim(int mt, int r) { return mt + 8 * r; }
+    static constexpr __host__ __device__ int shift(int j) { return j < 10 ? j : j - 10; }
+    static __device__ __forceinline__ void pair(const uint8_t *p, int RV, const VCtx &cx, uint32_t (&ra)[8],
+                                                uint32_t (&rb)[8]) {
+        const uint32_t wx = *reinterpret_cast<const uint32_t *>(p + cx.off);
+        const uint32_t wy = *reinterpret_cast<const uint32_t *>(p + cx.off + RV);
+        const uint32_t Z = prmt(wx, wy, static_cast<uint32_t>(cx.sh));  // x's 16 codes | y's 16 codes
+        const uint32_t Z2 = Z >> 10;
 #pragma unroll
         for (int mt = 0; mt < 8; mt++) {
-            const int sh = (mt >> 2) * 16 + (mt & 3);
-            lookup4<1>((Z >> sh) & 0x1111u, t, ra[mt], rb[mt]);
+            ra[mt] = Z & (0x00010001u << mt);
+            rb[mt] = (mt < 2 ? Z : Z2) & (0x00010001u << shift(mt + 8));
         }
+    }
+    // 2^(24 - s): the accumulator of code j holds the weighted bit sum times 2^(s - 24)
+    static __device__ __forceinline__ float unscale(int mt, int r) {
+        return __uint_as_float(static_cast<uint32_t>(127 + 24 - shift(dim(mt, r))) << 23);
     }
 };
 
-template <>
-struct VUnpack<2> {  // byte k of both tokens, shift 2e: codes (4k + e, 4k + e + 2)
-    static constexpr __host__ __device__ int dim(int mt, int r) { return 4 * (mt >> 1) + (mt & 1) + 2 * r; }
-    static __device__ __forceinline__ void run(const uint32_t (&x)[1], const uint32_t (&y)[1], const PrmtTable &t,
-                                               const unsigned short *, uint32_t (&ra)[8], uint32_t (&rb)[8]) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t Z = prmt(x[0], y[0], static_cast<uint32_t>(k | ((k + 4) << 4)));
-            lookup4<2>(Z & 0x3333u, t, ra[2 * k], rb[2 * k]);
-            lookup4<2>((Z >> 2) & 0x3333u, t, ra[2 * k + 1], rb[2 * k + 1]);
-        }
-    }
-};
-
-template <>
-struct VUnpack<3> {  // codes spread to nibbles; selector = byte k of both tokens: codes (2mt, 2mt+1)
+template <int TS>
+struct VDec<2, TS> {  // pair table of 16 entries; E/O fields of 4 bits: dims (2mt, 2mt+1)
+    static constexpr bool kLinear = false;
     static constexpr __host__ __device__ int dim(int mt, int r) { return 2 * mt + r; }
-    static __device__ __forceinline__ void run(const uint32_t (&x)[2], const uint32_t (&y)[2], const PrmtTable &t,
-                                               const unsigned short *, uint32_t (&ra)[8], uint32_t (&rb)[8]) {
-        const uint32_t sx[2] = {spread3(x[0]), spread3(__funnelshift_r(x[0], x[1], 24))};
-        const uint32_t sy[2] = {spread3(y[0]), spread3(__funnelshift_r(y[0], y[1], 24))};
+    static __device__ __forceinline__ uint32_t field(uint32_t F, int j) {
+        switch (j) {
+            case 0: return pair_off<0, 4, TS>(F);
+            case 1: return pair_off<4, 4, TS>(F);
+            case 2: return pair_off<8, 4, TS>(F);
+            case 3: return pair_off<12, 4, TS>(F);
+            case 4: return pair_off<16, 4, TS>(F);
+            case 5: return pair_off<20, 4, TS>(F);
+            case 6: return pair_off<24, 4, TS>(F);
+            default: return pair_off<28, 4, TS>(F);
+        }
+    }
+    static __device__ __forceinline__ void pair(const uint8_t *p, int RV, const VCtx &cx, uint32_t (&ra)[8],
+                                                uint32_t (&rb)[8]) {
+        const uint32_t wx = *reinterpret_cast<const uint32_t *>(p + cx.off);
+        const uint32_t wy = *reinterpret_cast<const uint32_t *>(p + cx.off + RV);
+        constexpr uint32_t M = 0x33333333u;
+        const uint32_t E = (wx & M) | ((wy << 2) & ~M);  // field j: x_{2j} | y_{2j} << 2
+        const uint32_t O = ((wx >> 2) & M) | (wy & ~M);  // field j: x_{2j+1} | y_{2j+1} << 2
 #pragma unroll
         for (int mt = 0; mt < 8; mt++) {
-            const int h = mt >> 2, k = mt & 3;
-            const uint32_t sel = prmt(sx[h], sy[h], static_cast<uint32_t>(k | ((k + 4) << 4)));
-            lookup4<3>(sel, t, ra[mt], rb[mt]);
+            ra[mt] = lds32(cx.tab + field(E, mt));
+            rb[mt] = lds32(cx.tab + field(O, mt));
         }
     }
 };
 
-template <>
-struct VUnpack<4> {  // nibbles already; selector = byte k of both tokens: codes (2mt, 2mt+1)
+template <int TS>
+struct VDec<3, TS> {  // pair table of 64 entries; E/O fields of 6 bits: dims (2mt, 2mt+1)
+    static constexpr bool kLinear = false;
     static constexpr __host__ __device__ int dim(int mt, int r) { return 2 * mt + r; }
-    static __device__ __forceinline__ void run(const uint32_t (&x)[2], const uint32_t (&y)[2], const PrmtTable &t,
-                                               const unsigned short *, uint32_t (&ra)[8], uint32_t (&rb)[8]) {
+    static __device__ __forceinline__ uint32_t field(uint32_t F, int j) {
+        switch (j) {
+            case 0: return pair_off<0, 6, TS>(F);
+            case 1: return pair_off<6, 6, TS>(F);
+            case 2: return pair_off<12, 6, TS>(F);
+            case 3: return pair_off<18, 6, TS>(F);
+            default: return pair_off<24, 6, TS>(F);
+        }
+    }
+    static __device__ __forceinline__ void pair(const uint8_t *p, int RV, const VCtx &cx, uint32_t (&ra)[8],
+                                                uint32_t (&rb)[8]) {
+        // the 48-bit window starts cx.sh bits into the word at p + cx.off
+        const uint32_t *px = reinterpret_cast<const uint32_t *>(p + cx.off);
+        const uint32_t *py = reinterpret_cast<const uint32_t *>(p + cx.off + RV);
+        const uint32_t x0 = __funnelshift_r(px[0], px[1], cx.sh), y0 = __funnelshift_r(py[0], py[1], cx.sh);
+        const uint32_t x1 = __funnelshift_r(x0, px[1] >> cx.sh, 30);  // codes 10..15
+        const uint32_t y1 = __funnelshift_r(y0, py[1] >> cx.sh, 30);
+        constexpr uint32_t M = 0x071C71C7u;  // 3-bit fields at 6j
+        const uint32_t E0 = (x0 & M) | ((y0 << 3) & ~M), O0 = ((x0 >> 3) & M) | (y0 & ~M);
+        const uint32_t E1 = (x1 & M) | ((y1 << 3) & ~M), O1 = ((x1 >> 3) & M) | (y1 & ~M);
 #pragma unroll
         for (int mt = 0; mt < 8; mt++) {
-            const int h = mt >> 2, k = mt & 3;
-            const uint32_t sel = prmt(x[h], y[h], static_cast<uint32_t>(k | ((k + 4) << 4)));
-            lookup4<4>(sel, t, ra[mt], rb[mt]);
+            ra[mt] = lds32(cx.tab + (mt < 5 ? field(E0, mt) : field(E1, mt - 5)));
+            rb[mt] = lds32(cx.tab + (mt < 5 ? field(O0, mt) : field(O1, mt - 5)));
+        }
+    }
+};
+
+// Lookup of 4 codes given as selector nibbles [x_j, x_j', y_j, y_j'] (4-bit
+// indices): half2(c[x_j], c[y_j]) and half2(c[x_j'], c[y_j']); two 8-entry
+// tables chosen per byte by the nibble's bit 3.
+__device__ __forceinline__ void lookup4(uint32_t sel, const PrmtTable &t, uint32_t &ra, uint32_t &rb) {
+    const uint32_t s7 = sel & 0x7777u;
+    const uint32_t hb = ((sel >> 1) & 0x4444u) | 0x3210u;
+    const uint32_t pl = prmt(prmt(t.tl[0], t.tl[1], s7), prmt(t.tl[2], t.tl[3], s7), hb);
+    const uint32_t ph = prmt(prmt(t.th[0], t.th[1], s7), prmt(t.th[2], t.th[3], s7), hb);
+    ra = prmt(pl, ph, 0x6240u);
+    rb = prmt(pl, ph, 0x7351u);
+}
+
+template <int TS>
+struct VDec<4, TS> {  // nibbles; selector = byte k of both tokens: codes (2mt, 2mt+1)
+    static constexpr bool kLinear = false;
+    static constexpr __host__ __device__ int dim(int mt, int r) { return 2 * mt + r; }
+    static __device__ __forceinline__ void pair(const uint8_t *p, int RV, const VCtx &cx, uint32_t (&ra)[8],
+                                                uint32_t (&rb)[8]) {
+        const uint2 x = *reinterpret_cast<const uint2 *>(p + cx.off);
+        const uint2 y = *reinterpret_cast<const uint2 *>(p + cx.off + RV);
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) {
+            const int k = mt & 3;
+            const uint32_t sel = prmt(mt < 4 ? x.x : x.y, mt < 4 ? y.x : y.y, static_cast<uint32_t>(k | ((k + 4) << 4)));
+            lookup4(sel, cx.pt, ra[mt], rb[mt]);
         }
     }
 };
@@ -304,14 +434,24 @@ struct PackedGeom {
     static constexpr int offQS = offVS + kPT * 4;
     static constexpr int offQN = offQS + kPT * 16;
     static constexpr int stage = QJL ? offQN + kPT * 4 : offQS;
-    static constexpr int fixed = (VB >= 5 ? 512 : 0) + kMaxGqa * kD * 4 + 64;  // codebook, queries, flag, barriers
-    // as many stages in flight (2..4) as fit with kPackedCtasPerSm CTAs per SM
-    static constexpr int fit = (227 * 1024 / kPackedCtasPerSm - 1024 - fixed) / stage;
+    static constexpr int budget = 227 * 1024 / packed_ctas_per_sm(QJL) - 1024;
+    static constexpr int qbytes = kMaxGqa * kD * 4 + 32 + 16 + 64;  // queries, sums, scales, flag, barriers
+    static constexpr int pair_entries = (VB == 2 || VB == 3) ? (1 << (2 * VB)) : 0;
+    // pair table: one column per lane (32 copies) if that still leaves 3
+    // stages in flight at the class's CTAs per SM, else 16 (2-way conflicts)
+    static constexpr int fit32 = (budget - qbytes - pair_entries * 128) / stage;
+    static constexpr int copies = (pair_entries == 0 || fit32 >= 3) ? 32 : 16;
+    static constexpr int tab_bytes = pair_entries * copies * 4;
+    static constexpr int TS = copies == 32 ? 7 : 6;  // log2 of the table's entry stride
+    static constexpr int fixed = (VB >= 5 ? 512 : 0) + tab_bytes + qbytes;
+    // as many stages in flight (2..4) as fit with the class's CTAs per SM
+    static constexpr int fit = (budget - fixed) / stage;
     static constexpr int stages = fit > 4 ? 4 : (fit < 2 ? 2 : fit);
-    static constexpr int ctab = stages * stage;                  // fp16 codebook (5-8 bits)
-    static constexpr int qoff = ctab + (VB >= 5 ? 512 : 0);      // rotated queries [4][128] words, sums [4]
-    static constexpr int flag = qoff + kMaxGqa * kD * 4 + 16;
-    static constexpr int bar = flag + 16;                        // one mbarrier per stage buffer
+    static constexpr int ctab = stages * stage;               // fp16 codebook (5-8 bits)
+    static constexpr int ptab = ctab + (VB >= 5 ? 512 : 0);   // pair table (2, 3 bits)
+    static constexpr int qoff = ptab + tab_bytes;             // rotated queries [4][128] words, sums [4], scales [4]
+    static constexpr int flag = qoff + kMaxGqa * kD * 4 + 32;
+    static constexpr int bar = flag + 16;                     // one mbarrier per stage buffer
     static constexpr int smem = bar + 8 * stages;
 };
 
@@ -358,15 +498,17 @@ struct StageCursor {
 };
 
 // Persistent split-K kernel of one class: gridDim.x CTAs share the class's S
-// stages in equal contiguous ranges and stream them through one cp.async
-// pipeline that never drains at group boundaries.  Each CTA writes one partial
-// per (item, batch) group it touches; the CTA completing a (layer, batch, KV
-// head) merges its partials (finish_and_combine).
+// stages in equal contiguous ranges and stream them through one bulk-copy
+// pipeline that never drains at group boundaries.  Each warp writes one
+// partial per (item, batch) group its CTA touches; the CTA completing a
+// (layer, batch, KV head) merges the partials (finish_and_combine).
 template <int KB, int VB, bool QJL>
-__global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
+__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     decode_packed_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int item_lo, const int item_hi,
                          const long long S, const __grid_constant__ ValueTable vt) {
     using G = PackedGeom<KB, VB, QJL>;
+    using KU = KUnpack<KB>;
+    using VD = VDec<VB, G::TS>;
     constexpr int NS = G::stages;
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
@@ -375,24 +517,44 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
     const int n_st = static_cast<int>(range_begin(blockIdx.x + 1, S, gridDim.x) - s_begin);
     pdl_launch_dependents();
 
-    unsigned short *ctab = reinterpret_cast<unsigned short *>(smem + G::ctab);
-    if constexpr (VB >= 5) {
-        for (int i = threadIdx.x; i < (1 << VB); i += kThreads) ctab[i] = vt.half[i];
+    // ---- value decoder constants and tables
+    VCtx vx;
+    vx.ctab = reinterpret_cast<const unsigned short *>(smem + G::ctab);
+    vx.tab = smem_u32(smem + G::ptab) + 4 * (lane & (G::copies - 1));
+    if constexpr (VB == 1) {
+        vx.off = 2 * c * G::RV + 4 * (g >> 1);
+        vx.sh = (g & 1) ? 0x7632 : 0x5410;  // PRMT: x's halfword g | y's halfword g
+    } else if constexpr (VB == 3) {
+        vx.off = 2 * c * G::RV + 4 * ((3 * g) >> 1);
+        vx.sh = (g & 1) * 16;
+    } else {
+        vx.off = 2 * c * G::RV + ((2 * VB * g) & ~3);
+        vx.sh = ((2 * VB * g) & 3) * 8;
     }
-    PrmtTable ptab;
-    if constexpr (VB <= 4) {
+    if constexpr (VB >= 5) {
+        unsigned short *ct = reinterpret_cast<unsigned short *>(smem + G::ctab);
+        for (int i = threadIdx.x; i < (1 << VB); i += kThreads) ct[i] = vt.half[i];
+    }
+    if constexpr (G::pair_entries > 0) {
+        uint32_t *pt = reinterpret_cast<uint32_t *>(smem + G::ptab);
+        for (int i = threadIdx.x; i < G::pair_entries * G::copies; i += kThreads) {
+            const int e = i / G::copies;
+            pt[i] = static_cast<uint32_t>(vt.half[e & ((1 << VB) - 1)]) |
+                    (static_cast<uint32_t>(vt.half[e >> VB]) << 16);
+        }
+    }
+    if constexpr (VB == 4) {
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             uint32_t lo = 0, hi = 0;
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                const int k = 4 * i + e;
-                const uint32_t v = k < (1 << VB) ? vt.half[k] : 0u;
+                const uint32_t v = vt.half[4 * i + e];
                 lo |= (v & 0xFFu) << (8 * e);
                 hi |= (v >> 8) << (8 * e);
             }
-            ptab.tl[i] = lo;
-            ptab.th[i] = hi;
+            vx.pt.tl[i] = lo;
+            vx.pt.th[i] = hi;
         }
     }
 
@@ -440,19 +602,19 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
     int g_layer = 0, g_head = 0, g_b = 0, g_item = 0;
     long long g_stage0 = 0;  // class stage index of the group's first stage
     uint32_t bq[16], bt[16];
-    float qsum = 0.f, tsum = 0.f;
+    float qsum = 0.f, tsum = 0.f, aq = 0.f;
     WarpState st;
     uint32_t *qsh = reinterpret_cast<uint32_t *>(smem + G::qoff);
     float *qs_sum = reinterpret_cast<float *>(qsh + kMaxGqa * kD);
+    float *qs_scale = qs_sum + kMaxGqa;
     int *flag = reinterpret_cast<int *>(smem + G::flag);
-    constexpr float alpha = 16777216.0f * 2.0f / static_cast<float>(1 << KB);  // 2^(1-KB), times 2^24
+    // raw = (q / 2^e) . code * 2^(kA - 24) and q . yhat = m (alpha q.code + beta sum q)
+    constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
     constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
     const float qk_scale = dims.qk_scale;
-    // per-thread byte offsets of the key window (codes [32c, 32c+32) of token
-    // row g) and of the value window (codes [16g, 16g+16) of token row 2c)
+    const float c1 = dims.value_c1;
+    // byte offset of the thread's key window: codes [32c, 32c+32) of token row g
     const int koff = g * G::RK + 4 * KB * c;
-    const int voff = 2 * c * G::RV + ((2 * VB * g) & ~3);
-    const int vsh = ((2 * VB * g) & 3) * 8;
 
     // each warp writes its own partial of the current group; then the group's
     // CTA-level count (and possibly the merge)
@@ -460,12 +622,18 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
         const long long gr = static_cast<long long>(g_item) * B + g_b;
         const int slot = ws.grp_part[gr] +
                          kDecodeWarps * static_cast<int>(blockIdx.x - cta_of_stage(g_stage0, S, gridDim.x)) + warp;
-        write_warp_partial_pair(st, ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride), gqa,
-                                [g](int mt, int r) { return 16 * g + VUnpack<VB>::dim(mt, r); });
+        write_warp_partial_pair(
+            st, ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride), gqa,
+            [g](int mt, int r) { return 16 * g + VD::dim(mt, r); },
+            [c1](int mt, int r, float acc, float W) {
+                if constexpr (VD::kLinear) return c1 * (2.0f * acc * VDec<1, 7>::unscale(mt, r) - W);
+                else return acc;
+            });
         finish_and_combine(dims, ws, g_layer, g_b, g_head, flag);
     };
     // a new group: its identity and the B fragments of its rotated queries
-    // (column g: head g/2, part g&1)
+    // (column g: head g/2, part g&1), each head divided by a power of two 2^e
+    // that brings its largest coordinate into [0.5, 1)
     auto start_group = [&]() {
         const WorkItem &it = ws.items[cc.item];
         g_item = cc.item;
@@ -481,30 +649,90 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
             const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
 #pragma unroll
             for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
-            gather_b<KUnpack<KB>>(q, bq);
+            gather_b<KU>(q, bq);
             const uint32_t *tw = ws.qjlt + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
 #pragma unroll
             for (int i = 0; i < 16; i++) q[i] = head < gqa ? tw[i] : 0u;
-            gather_b<KUnpack<1>>(q, bt);
+            gather_b<SignUnpack>(q, bt);
             qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
+            aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
         } else {
             if (warp < gqa) {  // warp w rotates query head w of the group
                 float x[4];
                 load_q4(ws.q + (qbase + warp) * kD, lane, x);
                 warp_rotate(x, ws.layer[g_layer].sign_bits, dims.inv_sqrt_d, lane);
+                const float f = warp_pow2_norm(x);
+#pragma unroll
+                for (int e = 0; e < 4; e++) x[e] *= f;
                 const float sm = store_hilo(qsh + warp * kD, x, lane);
-                if (lane == 0) qs_sum[warp] = sm;
+                if (lane == 0) {
+                    qs_sum[warp] = sm / f;
+                    qs_scale[warp] = 1.0f / f;
+                }
             }
             __syncthreads();
             const uint32_t *qw = qsh + head * kD + part * (kD / 2) + 16 * c;
 #pragma unroll
             for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
-            gather_b<KUnpack<KB>>(q, bq);
+            gather_b<KU>(q, bq);
             qsum = c < gqa ? qs_sum[c] : 0.f;
+            aq = c < gqa ? alphaA * qs_scale[c] : 0.f;
             __syncthreads();
         }
     };
+    // the warp's two 16-token tiles: tokens [tA, tA + 32) of the stage buffer
+    auto tiles = [&](const uint8_t *buf, int tA, int n, auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        float sc[4];
+        const float *kss = reinterpret_cast<const float *>(buf + G::offKS);
+#pragma unroll
+        for (int t = 0; t < 2; t++) {
+            const int t0 = tA + 16 * t;
+            float raw0, raw1;
+            qk_raw<KU, KB>(buf + t0 * G::RK + koff, buf + (t0 + 8) * G::RK + koff, bq, raw0, raw1);
+            float s0 = kss[t0 + g] * (aq * raw0 + beta * qsum);
+            float s1 = kss[t0 + g + 8] * (aq * raw1 + beta * qsum);
+            if constexpr (QJL) {
+                const float *qns = reinterpret_cast<const float *>(buf + G::offQN);
+                float r0, r1;
+                qk_raw<SignUnpack, 1>(buf + G::offQS + (t0 + g) * 16 + 4 * c,
+                                      buf + G::offQS + (t0 + g + 8) * 16 + 4 * c, bt, r0, r1);
+                constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
+                s0 += gam * qns[t0 + g] * (33554432.0f * r0 - tsum);
+                s1 += gam * qns[t0 + g + 8] * (33554432.0f * r1 - tsum);
+            }
+            sc[2 * t] = s0 * qk_scale;
+            sc[2 * t + 1] = s1 * qk_scale;
+        }
+        const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
+        bool okv[4];
+        if constexpr (FULL) {
+            okv[0] = okv[1] = okv[2] = okv[3] = true;
+        } else {
+            okv[0] = tA + g < n;
+            okv[1] = tA + g + 8 < n;
+            okv[2] = tA + 16 + g < n;
+            okv[3] = tA + 24 + g < n;
+        }
+        const float vsv[4] = {vss[tA + g], vss[tA + g + 8], vss[tA + 16 + g], vss[tA + 24 + g]};
+        uint32_t bp[4];
+        softmax_pair<FULL, VD::kLinear>(st, sc, okv, vsv, g, c, bp);
+        // ---- values of both tiles
+        const uint8_t *vst = buf + G::offV;
+#pragma unroll
+        for (int t = 0; t < 2; t++) {
+            if (!FULL && t == 1 && tA + 16 >= n) break;
+            const uint8_t *vrow = vst + (tA + 16 * t) * G::RV;
+            uint32_t ra[8], rb[8], rc[8], rd[8];
+            VD::pair(vrow, G::RV, vx, ra, rb);              // tokens 2c, 2c+1
+            VD::pair(vrow + 8 * G::RV, G::RV, vx, rc, rd);  // tokens 2c+8, 2c+9
+#pragma unroll
+            for (int mt = 0; mt < 8; mt++)
+                mma16816(st.acc[mt], ra[mt], rb[mt], rc[mt], rd[mt], bp[2 * t], bp[2 * t + 1]);
+        }
+    };
+    __syncthreads();  // codebook and pair table written
     start_group();
     bool new_group = false;
 
@@ -528,54 +756,10 @@ __global__ void __launch_bounds__(kThreads, kPackedCtasPerSm)
         const uint8_t *buf = smem + (k % NS) * G::stage;
         const int n = min(kPT, cc.n_tokens - cc.st * kPT);
         new_group = cc.advance(ws.items, B, k + 1 < n_st);
-        const int tA = warp * 32;  // this warp's tiles: tokens [tA, tA + 16) and [tA + 16, tA + 32)
+        const int tA = warp * 32;
         if (tA >= n) continue;
-        const bool has_b = tA + 16 < n;
-        // ---- scores of both tiles
-        float sc[4];
-        const float *kss = reinterpret_cast<const float *>(buf + G::offKS);
-        const float *qns = reinterpret_cast<const float *>(buf + G::offQN);
-#pragma unroll
-        for (int t = 0; t < 2; t++) {
-            const int t0 = tA + 16 * t;
-            float raw0, raw1;
-            qk_raw<KB>(buf + t0 * G::RK + koff, buf + (t0 + 8) * G::RK + koff, bq, raw0, raw1);
-            float s0 = kss[t0 + g] * (alpha * raw0 + beta * qsum);
-            float s1 = kss[t0 + g + 8] * (alpha * raw1 + beta * qsum);
-            if constexpr (QJL) {
-                float r0, r1;
-                qk_raw<1>(buf + G::offQS + (t0 + g) * 16 + 4 * c, buf + G::offQS + (t0 + g + 8) * 16 + 4 * c, bt, r0,
-                          r1);
-                constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
-                s0 += gam * qns[t0 + g] * (33554432.0f * r0 - tsum);
-                s1 += gam * qns[t0 + g + 8] * (33554432.0f * r1 - tsum);
-            }
-            sc[2 * t] = s0 * qk_scale;
-            sc[2 * t + 1] = s1 * qk_scale;
-        }
-        const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
-        const bool okv[4] = {tA + g < n, tA + g + 8 < n, tA + 16 + g < n, tA + 24 + g < n};
-        const float vsv[4] = {vss[tA + g], vss[tA + g + 8], vss[tA + 16 + g], vss[tA + 24 + g]};
-        uint32_t bp[4];
-        softmax_pair(st, sc, okv, vsv, g, c, gqa, bp);
-        // ---- values of both tiles
-        const uint8_t *vst = buf + G::offV;
-#pragma unroll
-        for (int t = 0; t < 2; t++) {
-            if (t == 1 && !has_b) break;
-            const uint8_t *vb = vst + (tA + 16 * t) * G::RV;
-            uint32_t x0[VWin<VB>::NW], x1[VWin<VB>::NW], x2[VWin<VB>::NW], x3[VWin<VB>::NW];
-            VWin<VB>::load(vb + voff, vsh, x0);
-            VWin<VB>::load(vb + voff + G::RV, vsh, x1);
-            VWin<VB>::load(vb + voff + 8 * G::RV, vsh, x2);
-            VWin<VB>::load(vb + voff + 9 * G::RV, vsh, x3);
-            uint32_t ra[8], rb[8], rc[8], rd[8];
-            VUnpack<VB>::run(x0, x1, ptab, ctab, ra, rb);
-            VUnpack<VB>::run(x2, x3, ptab, ctab, rc, rd);
-#pragma unroll
-            for (int mt = 0; mt < 8; mt++)
-                mma16816(st.acc[mt], ra[mt], rb[mt], rc[mt], rd[mt], bp[2 * t], bp[2 * t + 1]);
-        }
+        if (tA + 32 <= n) tiles(buf, tA, n, std::true_type{});
+        else tiles(buf, tA, n, std::false_type{});
     }
     // every thread waits for the previous grid of the call before its last
     // merge, so that this grid's completion implies that of all earlier ones

@@ -318,7 +318,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                      [](const WorkItem &a, const WorkItem &b) { return class_key(a) < class_key(b); });
     // classes: packed ones run persistent CTAs over their 128-token stages,
     // fp16 runs one CTA per (item, batch element, chunk)
-    const int slots = sm_count() * kPackedCtasPerSm;
+    const int sms = sm_count();
     long long cta = 0, stages = 0;
     for (size_t i = 0; i < P.items.size(); ++i) {
         WorkItem &w = P.items[i];
@@ -334,7 +334,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             w.stage_begin = stages;
             stages += static_cast<long long>(B) * w.n_stages;
             c.n_stages = stages;
-            c.n_ctas = static_cast<int>(std::min<long long>(stages, slots));
+            c.n_ctas = static_cast<int>(std::min<long long>(stages, static_cast<long long>(sms) *
+                                                                         packed_ctas_per_sm(w.qjl != 0)));
         } else {
             w.cta_begin = static_cast<int>(cta);
             cta += static_cast<long long>(B) * w.n_chunks;
@@ -383,6 +384,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.any_qjl = P.any_qjl ? 1 : 0;
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    D.value_c1 = 0.f;
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
     // offset 0: the error flag (kept in its own 256 bytes so that it has a
     // fixed place), then the work items
@@ -672,6 +674,9 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
                     k < (1 << c.vb) ? __half_as_ushort(__float2half_rn(static_cast<float>(cb.level[k]))) : 0;
             value_ready[c.vb] = true;
         }
+        // 1-bit values decode as c1 * (2 code - 1) (the codebook is symmetric)
+        for (const ClassLaunch &c : P.classes)
+            if (c.kb != 16 && c.vb == 1) P.dims.value_c1 = static_cast<float>(fit(1).level[1]);
     }
     // (layer, KV head) groups without any token are written by no CTA: their
     // output is zero

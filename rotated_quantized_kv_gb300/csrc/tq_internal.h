@@ -94,6 +94,7 @@ struct DecodeDims {
     int any_qjl;         // the prep kernel ran (QJL layers read S R q from it)
     float qk_scale;      // log2(e) / sqrt(d)
     float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
+    float value_c1;      // binary32 centroid 1 of the 1-bit value codebook (= -centroid 0)
 };
 
 // Workspace: [WorkItem x n][LayerPlan x L][group tables][counters][q prep]
@@ -110,7 +111,7 @@ struct DecodeWorkspace {
     int *error;        // set non-zero by a kernel that gave up waiting for its copies
     uint32_t *qrot;    // [L][B][Hq][2][d/2] half2 words: hi, lo of R q (QJL calls only)
     uint32_t *qjlt;    // [L][B][Hq][2][d/2] half2 words: hi, lo of S R q (QJL calls only)
-    float *qsum;       // [L][B][Hq][4]: sum(R q), sum(S R q) (QJL calls only)
+    float *qsum;       // [L][B][Hq][4]: sum(R q), sum(S R q), 2^e of the stored R q / 2^e (QJL calls only)
     float *part;       // [parts][kMaxGqa][4 + d]: m (log2 units), l, pad, pad, acc
     const uint16_t *q; // the caller's queries, fp16 [L][B][Hq][d]
     float *out;        // the caller's output, [L][B][Hq][d]
@@ -135,6 +136,9 @@ struct ClassLaunch {
 // Resident CTAs per SM of the packed split-K kernels (registers and shared
 // memory are sized for it).
 constexpr int kPackedCtasPerSm = 4;
+// QJL classes carry the sketch operands too: 3 CTAs per SM (more registers each)
+constexpr int kPackedCtasPerSmQjl = 3;
+__host__ __device__ constexpr int packed_ctas_per_sm(bool qjl) { return qjl ? kPackedCtasPerSmQjl : kPackedCtasPerSm; }
 
 typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, int item_lo, int item_hi,
                                       int n_ctas, long long n_stages, const unsigned short *value_half,

@@ -1,0 +1,246 @@
+"""Parity at the full sizes of the five workloads, in the launch configuration
+the benchmark times.
+
+The CUDA path builds each workload's whole cache with the same code the
+benchmark runs (model_cache) and makes the same decode call over all layers.
+The oracle cannot redo a whole workload in seconds, so it checks samples:
+
+  compression  the records and scales of sampled positions of sampled (layer,
+               batch element), all heads, are bit-exact against the oracle
+               compressing the same fp16 input vectors; QJL signs may differ
+               only inside the stated boundary window.
+  decode       the outputs of sampled (layer, batch element, KV head) groups
+               (the head's 4 query heads) agree within 2e-3 max relative error
+               with the oracle's fp64 attention over that group's packed and
+               fp16 segments copied back from the device.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from rotated_quantized_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rotated_quantized_kv_gb300 import build
+    build.build()
+    from rotated_quantized_kv_gb300 import model_cache as MC
+    from rotated_quantized_kv_gb300 import tq as T
+    return T, MC
+
+
+def _cap16(n):
+    return max(16, ((n + 15) // 16) * 16)
+
+
+def _u16(t):
+    return t.contiguous().cpu().numpy().view(np.uint16)
+
+
+def _head_segments(si_list, b, h, buf_kv=None):
+    """Oracle segments (batch 1, one KV head) holding (b, h) of each device segment."""
+    out = []
+    for si in si_list:
+        if not si.packed:
+            if si.seg is None:  # the fp16 decode buffer, passed in directly
+                k, v = buf_kv
+            else:
+                k, v = si.seg.k[b, h, :si.n], si.seg.v[b, h, :si.n]
+            o = O.Fp16Segment(1, 1, 128, max(si.n, 1), n_tokens=si.n)
+            o.k16[:si.n * 128] = _u16(k).ravel()
+            o.v16[:si.n * 128] = _u16(v).ravel()
+            out.append(o)
+            continue
+        g = si.seg
+        L = g.layout
+        H, cap = L.n_heads, L.capacity
+        rk = [128 * L.kbits[i] // 8 for i in range(H)]
+        rv = [128 * L.vbits[i] // 8 for i in range(H)]
+        qj = [L.qjl[i] for i in range(H)]
+        o = O.PackedSegment(1, 1, 128, cap, [L.kbits[h]], [L.vbits[h]], [qj[h]], jl=128, n_tokens=si.n)
+        k0 = b * cap * sum(rk) + cap * sum(rk[:h])
+        v0 = b * cap * sum(rv) + cap * sum(rv[:h])
+        o.kcodes[:] = g.kcodes[k0:k0 + cap * rk[h]].cpu().numpy()
+        o.vcodes[:] = g.vcodes[v0:v0 + cap * rv[h]].cpu().numpy()
+        o.kscale[:] = g.kscale[(b * H + h) * cap:(b * H + h + 1) * cap].cpu().numpy()
+        o.vscale[:] = g.vscale[(b * H + h) * cap:(b * H + h + 1) * cap].cpu().numpy()
+        if qj[h]:
+            nq, r = sum(qj), sum(qj[:h])
+            base = (b * nq + r) * cap
+            o.qjl_signs[:] = g.qjl_signs[base * 16:(base + cap) * 16].cpu().numpy()
+            o.qjl_norm[:] = g.qjl_norm[base:base + cap].cpu().numpy()
+        out.append(o)
+    return out
+
+
+def _check_decode(out, q, groups, segs_of, sign_of, S):
+    worst = 0.0
+    got = out.cpu().numpy()
+    qn = q.cpu().numpy()
+    for l, b, h in groups:
+        osegs = segs_of(l, b, h)
+        ref = O.decode_attention(osegs, qn[l, b:b + 1, 4 * h:4 * h + 4], sign_of(l), 1, S=S)
+        g = got[l, b, 4 * h:4 * h + 4]
+        r = ref.reshape(4, 128)
+        rel = (np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)).max()
+        worst = max(worst, rel)
+    assert worst <= ATTN_TOL, worst
+    return worst
+
+
+def _check_records(si, b, pos, kin, vin, sign, S):
+    """Records of positions `pos` (segment-relative) of batch element b against
+    the oracle compressing kin/vin ([H][n][d] fp16 numpy, the same vectors)."""
+    g = si.seg
+    L = g.layout
+    H, cap = L.n_heads, L.capacity
+    n = len(pos)
+    kb = [L.kbits[i] for i in range(H)]
+    vb = [L.vbits[i] for i in range(H)]
+    qj = [L.qjl[i] for i in range(H)]
+    o = O.PackedSegment(1, H, 128, _cap16(n), kb, vb, qj, jl=128)
+    O.compress(o, kin[None].view(np.uint16), vin[None].view(np.uint16), sign, S)
+    rk = [16 * x for x in kb]
+    rv = [16 * x for x in vb]
+    pos = np.asarray(pos, np.int64)
+    near = 0
+    for h in range(H):
+        for which, r, codes, ocodes in (("k", rk, g.kcodes, o.kcodes), ("v", rv, g.vcodes, o.vcodes)):
+            base = b * cap * sum(r) + cap * sum(r[:h])
+            idx = torch.from_numpy((base + pos[:, None] * r[h] + np.arange(r[h])[None]).ravel()).to(codes.device)
+            dev = codes[idx].cpu().numpy().reshape(n, r[h])
+            ref = ocodes[_cap16(n) * sum(r[:h]):_cap16(n) * sum(r[:h]) + n * r[h]].reshape(n, r[h])
+            assert np.array_equal(dev, ref), (which, b, h)
+        for sc, osc in ((g.kscale, o.kscale), (g.vscale, o.vscale)):
+            dev = sc[torch.from_numpy((b * H + h) * cap + pos).to(sc.device)].cpu().numpy()
+            ref = osc[h * _cap16(n):h * _cap16(n) + n]
+            assert np.array_equal(dev.view(np.uint32), ref.view(np.uint32)), (b, h)
+        if qj[h]:
+            nq, rr = sum(qj), sum(qj[:h])
+            base = (b * nq + rr) * cap
+            idx = torch.from_numpy(((base + pos)[:, None] * 16 + np.arange(16)[None]).ravel()).to(g.qjl_signs.device)
+            dev = g.qjl_signs[idx].cpu().numpy().reshape(n, 16)
+            ref = o.qjl_signs[rr * _cap16(n) * 16:(rr * _cap16(n) + n) * 16].reshape(n, 16)
+            diff = np.unpackbits(dev ^ ref, axis=1, bitorder="little")
+            if diff.any():  # allowed only where |(S r)_j| is within 1e-6 ||S_j|| ||r||
+                Sd = S.astype(np.float64)
+                rown = np.linalg.norm(Sd, axis=1)
+                for t_i, j in zip(*np.nonzero(diff)):
+                    x = kin[h, t_i].astype(np.float32)
+                    y = O.rotate_f32(x, sign)
+                    codes_, m = O.quant_key(y, kb[h])
+                    yh = (m * O.key_levels(kb[h])[codes_]).astype(np.float32)
+                    rv_ = (y - yh).astype(np.float64)
+                    p = Sd[j] @ rv_
+                    assert abs(p) <= 1e-6 * rown[j] * np.linalg.norm(rv_)
+                    near += 1
+            dn = g.qjl_norm[torch.from_numpy(base + pos).to(g.qjl_norm.device)].cpu().numpy()
+            assert np.allclose(dn, o.qjl_norm[rr * _cap16(n):rr * _cap16(n) + n], rtol=1e-5, atol=0)
+    return near
+
+
+def _sample_positions(n, k=48, seed=0):
+    rng = np.random.default_rng(seed)
+    p = set(rng.choice(n, size=min(n, k), replace=False).tolist())
+    p.update({0, n - 1})
+    return np.array(sorted(p), np.int64)
+
+
+def _groups(L, B, H):
+    g = {(0, 0, 0), (L - 1, B - 1, H - 1), (L // 2, B // 2, H // 2), (L - 1, 0, 1 % H)}
+    return sorted(g)
+
+
+@pytest.mark.parametrize("name,batch,context", [
+    ("w1", None, None),
+    ("w3", None, None),
+    ("w4", None, None),
+    ("w5", 32, 65536),
+    ("w5", 1, 4096),
+])
+def test_static_workload_full_size(lib, name, batch, context):
+    T, MC = lib
+    w = W.WORKLOADS[name]
+    seed = 1000 + int(name[1:])
+    B = batch or w.batch
+    L = w.layers
+    check_layers = {0, L - 1}
+    check_b = sorted({0, B - 1})
+    samples = {}
+
+    def keep(l, K, V):
+        if l in check_layers:
+            samples[l] = {b: (K[b].cpu(), V[b].cpu()) for b in check_b}
+
+    m = MC.StaticCache(w, batch=batch, context=context, seed=seed, sample_inputs=keep)
+    q = W.query_pool(w, 4, m.B, seed, device="cuda")[0]
+    m.decode(q)
+    assert T.tq_decode_error_flag(m.ws) == 0
+    torch.cuda.synchronize()
+    S = O.qjl_matrix(128, 128, W.QJL_SEED) if w.qjl_max_bits else None
+
+    # compression of sampled positions, every packed segment of the checked layers
+    near = total = 0
+    for l in sorted(check_layers):
+        sign = O.signs(128, W.ROTATION_SEED + l)
+        for b in check_b:
+            K, V = samples[l][b]
+            for i, si in enumerate(m.layers[l]):
+                if not si.packed:
+                    kk = si.seg.k[b].cpu()
+                    assert torch.equal(kk, K[:, si.pos0:si.pos0 + si.n])
+                    continue
+                pos = _sample_positions(si.n, seed=l * 131 + b * 7 + i)
+                tp = torch.from_numpy(si.pos0 + pos)
+                kin = K[:, tp].numpy()
+                vin = V[:, tp].numpy()
+                near += _check_records(si, b, pos, kin, vin, sign, S)
+                total += len(pos) * m.H * 128
+    assert near <= 1e-5 * total
+
+    # decode outputs of sampled groups
+    _check_decode(m.out, q, _groups(L, m.B, m.H),
+                  lambda l, b, h: _head_segments(m.layers[l], b, h),
+                  lambda l: O.signs(128, W.ROTATION_SEED + l), S)
+    del m, samples
+    torch.cuda.empty_cache()
+
+
+def test_chunked_workload_full_size(lib):
+    """Workload 2 through 66 decode steps: step 64 compresses the first 64
+    buffered tokens of every layer into the packed segment; step 65 attends to
+    the sinks, the packed prompt + window and the 2 newest buffered tokens."""
+    T, MC = lib
+    m = MC.ChunkedDecodeCache()
+    for s in range(66):
+        m.step(s)
+    assert T.tq_decode_error_flag(m.ws) == 0
+    torch.cuda.synchronize()
+    w = m.w
+    # compression: sampled prompt positions and the whole compressed window
+    for l in (0, m.L - 1):
+        sign = O.signs(128, W.ROTATION_SEED + l)
+        K, V = W.kv_block(w, l, m.B, m.T, 1002, device="cuda")
+        si = m.layer_segments(l, 65)[1]
+        pos = _sample_positions(m.n_prompt_packed, seed=l)
+        tp = torch.from_numpy(m.sinks + pos).cuda()
+        _check_records(si, 0, pos, K[0][:, tp].cpu().numpy(), V[0][:, tp].cpu().numpy(), sign, None)
+        win = np.arange(m.n_prompt_packed, m.n_prompt_packed + 64)
+        _check_records(si, 0, win, m.pool_k_all[l, 0, :, :64].cpu().numpy(),
+                       m.pool_v_all[l, 0, :, :64].cpu().numpy(), sign, None)
+        del K, V
+
+    def segs_of(l, b, h):
+        buf = (m.pool_k_all[l, b, h, 64:66], m.pool_v_all[l, b, h, 64:66])
+        return _head_segments(m.layer_segments(l, 65), b, h, buf_kv=buf)
+
+    _check_decode(m.out, m.qpool[65], _groups(m.L, m.B, m.H), segs_of,
+                  lambda l: O.signs(128, W.ROTATION_SEED + l), None)
+    del m
+    torch.cuda.empty_cache()
