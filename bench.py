@@ -118,14 +118,21 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
 
 
-def traffic_for(workload: str):
-    """DRAM bytes per launch of the packed kernel from an ncu capture, if it was
-    taken on the current kernel sources (null otherwise)."""
+def traffic_for(workload: str, packed_bytes: int):
+    """DRAM bytes per launch of the packed kernel from an ncu capture taken on
+    the current kernel sources (null otherwise): the captured bytes when the
+    capture had this launch's size, else the captured traffic per algorithmic
+    byte times this launch's algorithmic bytes (captures of the large
+    workloads are taken at a smaller batch)."""
     path = os.path.join(ROOT, "profiles", f"decode_packed_{workload}_traffic.json")
     if not os.path.exists(path):
         return None
     t = json.load(open(path))
-    return t.get("traffic_bytes_per_launch") if t.get("source_sha256") == kernel_sha() else None
+    if t.get("source_sha256") != kernel_sha():
+        return None
+    if t.get("algorithmic_bytes_per_launch") == packed_bytes and "traffic_bytes_per_launch" in t:
+        return t["traffic_bytes_per_launch"]
+    return int(round(t["traffic_ratio"] * packed_bytes)) if "traffic_ratio" in t else None
 
 
 def kernel_sha() -> str:
@@ -133,6 +140,20 @@ def kernel_sha() -> str:
     for f in DECODE_SRCS:
         h.update(open(os.path.join(ROOT, "rotated_quantized_kv_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank's timed region covers the same
+    per-rank work, so the job finishes when the slowest replica does."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, bytes_per_rank: int, ms_max: float) -> float:
+    """Weak scaling: all replicas' bytes over the slowest replica's time."""
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e9
 
 
 def timed_region(tq, step, nbytes, K, Wm, world, dev):
@@ -174,11 +195,8 @@ def timed_region(tq, step, nbytes, K, Wm, world, dev):
                 step(s)
                 s += 1
             torch.cuda.synchronize()
-    ms = start.elapsed_time(stop)
-    ms_all = torch.tensor([ms], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(ms_all, op=torch.distributed.ReduceOp.MAX)
-    return {"ms": float(ms_all.item()), "kern_ms": [a.elapsed_time(b) for a, b in ev], "launches": launches,
+    return {"ms": max_over_ranks(start.elapsed_time(stop), world, "cuda"),
+            "kern_ms": [a.elapsed_time(b) for a, b in ev], "launches": launches,
             "total_bytes": total_bytes, "packed_bytes": packed_bytes, "clocks": clk.summary()}
 
 
@@ -200,7 +218,7 @@ def time_compress(tq, jobs, reps=3):
 def result_line(args, world, m, t, e2e, comp, config, workload):
     peak, peak_kind = measured_peaks()
     K = args.steps
-    value = world * t["total_bytes"] / (t["ms"] * 1e-3) / 1e9
+    value = whole_job_gbs(world, t["total_bytes"], t["ms"])
     kern_avg_ms = float(np.mean(t["kern_ms"]))
     achieved = float(np.mean(t["packed_bytes"])) / (kern_avg_ms * 1e-3) / 1e9
     return {
@@ -221,7 +239,8 @@ def result_line(args, world, m, t, e2e, comp, config, workload):
         "tokens_per_s": round(world * m.B * K / (t["ms"] * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": "decode_packed_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic_for(workload), "bytes_per_launch": int(np.mean(t["packed_bytes"])),
+                     "traffic": traffic_for(workload, int(np.mean(t["packed_bytes"]))),
+                     "bytes_per_launch": int(np.mean(t["packed_bytes"])),
                      "avg_launch_ms": round(kern_avg_ms, 5)},
         "compress": {"value": round(comp["mtok"], 1), "unit": "Mtok/s", "ms_per_layer": round(comp["ms"], 4),
                      "tokens_per_layer": comp["tokens"],
