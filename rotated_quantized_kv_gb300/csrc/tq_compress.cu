@@ -7,14 +7,22 @@
 // keys only); "TurboMOQ", "Architecture" (keys: symmetric quantize, values:
 // Lloyd-Max grid quantize, per-head 1-8 bits) and "QJL residual correction".
 //
-// Design (GB300): one CTA per (batch, head, 64-token block); warps 0-1 take the
-// 64 key vectors, warps 2-3 the 64 value vectors, one vector per thread so the
-// whole Walsh-Hadamard transform stays in registers with no shuffles.  The
-// block is staged with coalesced 16-byte cp.async copies into shared rows padded
-// to 272 bytes, which makes each thread's 16-byte row reads bank-conflict free.
-// Every rounding step is an explicit IEEE binary32 intrinsic (__fadd_rn,
-// __fmul_rn, __frcp_rn, __fsqrt_rn): no contraction into FMA, so the codes are
-// the same bits the fixed-order format defines.
+// Design (GB300): two threads per vector, each holding 64 of its coordinates
+// in registers: butterfly stages h = 1..32 stay in registers, stage h = 64 is
+// one exchange of the 64 values with the partner lane, and every later
+// reduction (absmax, the pairwise sum of squares) finishes with one more
+// exchange in the same fixed order.  A CTA of 8 warps takes a 64-token block of
+// one (batch, head): warps 0-3 its 64 key vectors, warps 4-7 its 64 value
+// vectors.  CTAs are persistent (two per SM) and double-buffer their blocks:
+// the next block is staged with coalesced 16-byte cp.async copies while the
+// current one is computed.  Shared rows are laid out [64 coordinates | 16 B |
+// 64 coordinates | 16 B] so that the two halves of a vector, read by two
+// neighbouring lanes, fall in different banks.  Every rounding step is an
+// explicit IEEE binary32 intrinsic (__fadd_rn, __fmul_rn, __frcp_rn,
+// __fsqrt_rn): no contraction into FMA, so the codes are the same bits the
+// fixed-order format defines.
+#include <algorithm>
+
 #include <cuda_fp16.h>
 
 #include "tq_internal.h"
@@ -22,28 +30,34 @@
 namespace tqk {
 namespace {
 
-constexpr int kTok = 64;         // tokens per CTA
-constexpr int kRow = 272;        // padded shared row: 256 B of fp16 + 16 B
-constexpr int kThreads = 128;
+constexpr int kTok = 64;         // tokens per block
+constexpr int kRow = 288;        // shared row: 128 B | 16 B pad | 128 B | 16 B pad
+constexpr int kHalfOff = 144;    // byte offset of coordinates 64..127 in a row
+constexpr int kThreads = 256;    // 8 warps: 64 key and 64 value vectors, two lanes each
+constexpr int kHalf = kD / 2;
+constexpr int kBuf = 2 * kTok * kRow;  // one staged block (keys then values)
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// y = R x for one 128-vector: input sign flip applied to the fp16 bits, the
-// seven butterfly stages h = 1..64 in ascending order, then one rounded
-// multiply by +-binary32(1/sqrt(d)) (the output sign folded into the factor).
-__device__ __forceinline__ void load_rotate(const uint8_t *row, const uint32_t *in_mask,
-                                            const float *out_scale, float (&a)[kD]) {
+// y = R x for one 128-vector held by a lane pair: this lane's coordinates
+// [64 half, 64 half + 64) in a[0..63].  Input sign flip on the fp16 bits, the
+// seven butterfly stages h = 1..64 in ascending order (h = 64 across the pair:
+// the low lane keeps a_i + a_{i+64}, the high lane a_i - a_{i+64}), then one
+// rounded multiply by +-binary32(1/sqrt(d)) (the output sign folded in).
+__device__ __forceinline__ void load_rotate(const uint8_t *half_row, const uint32_t *in_mask,
+                                            const float *out_scale, int half, float (&a)[kHalf]) {
 #pragma unroll
-    for (int c = 0; c < 16; c++) {
-        uint4 v = *reinterpret_cast<const uint4 *>(row + c * 16);
-        const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + c * 4);
+    for (int c = 0; c < 8; c++) {
+        uint4 v = *reinterpret_cast<const uint4 *>(half_row + c * 16);
+        const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + half * 32 + c * 4);
         v.x ^= mk.x; v.y ^= mk.y; v.z ^= mk.z; v.w ^= mk.w;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -54,9 +68,9 @@ __device__ __forceinline__ void load_rotate(const uint8_t *row, const uint32_t *
         }
     }
 #pragma unroll
-    for (int h = 1; h < kD; h <<= 1) {
+    for (int h = 1; h < kHalf; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < kD; i++) {
+        for (int i = 0; i < kHalf; i++) {
             if ((i & h) == 0) {
                 const float u = a[i], v = a[i + h];
                 a[i] = __fadd_rn(u, v);
@@ -65,8 +79,13 @@ __device__ __forceinline__ void load_rotate(const uint8_t *row, const uint32_t *
         }
     }
 #pragma unroll
-    for (int c = 0; c < kD / 4; c++) {
-        const float4 s = *reinterpret_cast<const float4 *>(out_scale + 4 * c);
+    for (int i = 0; i < kHalf; i++) {
+        const float o = __shfl_xor_sync(0xffffffffu, a[i], 1);
+        a[i] = half ? __fsub_rn(o, a[i]) : __fadd_rn(a[i], o);
+    }
+#pragma unroll
+    for (int c = 0; c < kHalf / 4; c++) {
+        const float4 s = *reinterpret_cast<const float4 *>(out_scale + half * kHalf + 4 * c);
         a[4 * c] = __fmul_rn(a[4 * c], s.x);
         a[4 * c + 1] = __fmul_rn(a[4 * c + 1], s.y);
         a[4 * c + 2] = __fmul_rn(a[4 * c + 2], s.z);
@@ -74,19 +93,19 @@ __device__ __forceinline__ void load_rotate(const uint8_t *row, const uint32_t *
     }
 }
 
-// Code i occupies bits [B*i, B*i + B) of the record (LSB first).
+// Code i of this lane's 64 occupies bits [B*i, B*i + B) of its half record
+// (the record's bytes [8 B half, 8 B half + 8 B)), LSB first.
 template <int B>
-__device__ __forceinline__ void put_code(uint32_t (&w)[4 * B], int i, uint32_t k) {
+__device__ __forceinline__ void put_code(uint32_t (&w)[2 * B], int i, uint32_t k) {
     const int bit = i * B, wi = bit >> 5, sh = bit & 31;
     w[wi] |= k << sh;
     if (sh + B > 32) w[wi + 1] |= k >> (32 - sh);
 }
 
 template <int B>
-__device__ __forceinline__ void store_record(uint8_t *dst, const uint32_t (&w)[4 * B]) {
+__device__ __forceinline__ void store_half_record(uint8_t *dst, const uint32_t (&w)[2 * B]) {
 #pragma unroll
-    for (int j = 0; j < B; j++)
-        reinterpret_cast<uint4 *>(dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    for (int j = 0; j < B; j++) reinterpret_cast<uint2 *>(dst)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
 }
 
 // Select t[k*STRIDE] for a runtime k < N from a register-resident table (a
@@ -126,23 +145,25 @@ __device__ __forceinline__ uint32_t search_smem(float u, const float *t) {
     return k;
 }
 
+// One key vector (lane pair); `store` is false for rows past the block's end
+// (the pair still runs so that its exchanges stay warp-uniform).
 template <int KB, bool QJL>
-__device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *row,
-                                        const uint32_t *in_mask, const float *out_scale, int b,
-                                        int h, int pos) {
-    float y[kD];
-    load_rotate(row, in_mask, out_scale, y);
+__device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *half_row, const uint32_t *in_mask,
+                                        const float *out_scale, int half, int b, int h, int pos, bool store) {
+    float y[kHalf];
+    load_rotate(half_row, in_mask, out_scale, half, y);
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kD; i++) m = fmaxf(m, fabsf(y[i]));
+    for (int i = 0; i < kHalf; i++) m = fmaxf(m, fabsf(y[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     const float r = m > 0.0f ? __frcp_rn(m) : 0.0f;
     constexpr float half_cells = static_cast<float>(1 << (KB - 1));
     constexpr float top = static_cast<float>((1 << KB) - 1);
-    uint32_t w[4 * KB];
+    uint32_t w[2 * KB];
 #pragma unroll
-    for (int j = 0; j < 4 * KB; j++) w[j] = 0;
+    for (int j = 0; j < 2 * KB; j++) w[j] = 0;
 #pragma unroll
-    for (int i = 0; i < kD; i++) {
+    for (int i = 0; i < kHalf; i++) {
         const float v = __fmul_rn(y[i], r);
         const float t = __fadd_rn(v, 1.0f);
         float u = __fmul_rn(t, half_cells);  // exact: power of two
@@ -157,104 +178,123 @@ __device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *
             y[i] = __fsub_rn(y[i], __fmul_rn(m, lev));
         }
     }
-    const size_t sidx = (static_cast<size_t>(b) * p.H + h) * p.capacity + pos;
-    store_record<KB>(p.kcodes + static_cast<size_t>(b) * p.kblock + p.koff[h] +
-                         static_cast<size_t>(pos) * (16 * KB), w);
-    p.kscale[sidx] = m;
+    if (store) {
+        store_half_record<KB>(p.kcodes + static_cast<size_t>(b) * p.kblock + p.koff[h] +
+                                  static_cast<size_t>(pos) * (16 * KB) + half * (8 * KB), w);
+        if (!half) p.kscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = m;
+    }
     if constexpr (QJL) {
         // p_j = sum_i S[j][i] r_i in binary32 (any order: the only decision is the
-        // sign); bit j = (p_j >= 0).  rho = ||r||_2.
+        // sign); bit j = (p_j >= 0).  rho = ||r||_2.  Each lane forms partial sums
+        // over its 64 coordinates for 32 projections at a time; the pair adds them
+        // and each lane keeps the signs of its own 64 projections.
         float ss = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kD; i++) ss = fmaf(y[i], y[i], ss);
-        uint32_t sb[4];
-#pragma unroll
-        for (int jw = 0; jw < 4; jw++) {
+        for (int i = 0; i < kHalf; i++) ss = fmaf(y[i], y[i], ss);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        uint32_t sb[2] = {0u, 0u};
+#pragma unroll 1
+        for (int jc = 0; jc < 4; jc++) {  // projections 32 jc .. 32 jc + 31
             uint32_t word = 0;
             for (int jj = 0; jj < 32; jj++) {
-                const float4 *Sj = reinterpret_cast<const float4 *>(p.S + (jw * 32 + jj) * kD);
+                const float4 *Sj = reinterpret_cast<const float4 *>(p.S + (32 * jc + jj) * kD + half * kHalf);
                 float acc = 0.0f;
 #pragma unroll
-                for (int i4 = 0; i4 < kD / 4; i4++) {
+                for (int i4 = 0; i4 < kHalf / 4; i4++) {
                     const float4 s = __ldg(Sj + i4);
                     acc = fmaf(s.x, y[4 * i4], acc);
                     acc = fmaf(s.y, y[4 * i4 + 1], acc);
                     acc = fmaf(s.z, y[4 * i4 + 2], acc);
                     acc = fmaf(s.w, y[4 * i4 + 3], acc);
                 }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
                 word |= (acc >= 0.0f ? 1u : 0u) << jj;
             }
-            sb[jw] = word;
+            if ((jc >> 1) == half) sb[jc & 1] = word;
         }
-        const size_t q = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
-        *reinterpret_cast<uint4 *>(p.qjl_signs + q * (kJl / 8)) = make_uint4(sb[0], sb[1], sb[2], sb[3]);
-        p.qjl_norm[q] = sqrtf(ss);
+        if (store) {
+            const size_t q = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
+            *reinterpret_cast<uint2 *>(p.qjl_signs + q * (kJl / 8) + half * 8) = make_uint2(sb[0], sb[1]);
+            if (!half) p.qjl_norm[q] = sqrtf(ss);
+        }
     }
 }
 
 template <int VB>
-__device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *row,
-                                          const uint32_t *in_mask, const float *out_scale,
-                                          const float *thr_smem, int b, int h, int pos) {
-    float y[kD];
-    load_rotate(row, in_mask, out_scale, y);
-    // pairwise tree of squares in index order
-    float s[kD / 2];
+__device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *half_row, const uint32_t *in_mask,
+                                          const float *out_scale, const float *thr_smem, int half, int b, int h,
+                                          int pos, bool store) {
+    float y[kHalf];
+    load_rotate(half_row, in_mask, out_scale, half, y);
+    // pairwise tree of squares in index order: this lane's 64 give one of the
+    // two subtrees under the root, which adds (low half) + (high half)
+    float s[kHalf / 2];
 #pragma unroll
-    for (int j = 0; j < kD / 2; j++)
+    for (int j = 0; j < kHalf / 2; j++)
         s[j] = __fadd_rn(__fmul_rn(y[2 * j], y[2 * j]), __fmul_rn(y[2 * j + 1], y[2 * j + 1]));
 #pragma unroll
-    for (int len = kD / 2; len > 1; len >>= 1) {
+    for (int len = kHalf / 2; len > 1; len >>= 1) {
 #pragma unroll
         for (int j = 0; j < len / 2; j++) s[j] = __fadd_rn(s[2 * j], s[2 * j + 1]);
     }
-    const float sigma = __fsqrt_rn(__fmul_rn(s[0], 1.0f / kD));  // /d exact (power of two)
+    const float other = __shfl_xor_sync(0xffffffffu, s[0], 1);
+    const float total = half ? __fadd_rn(other, s[0]) : __fadd_rn(s[0], other);
+    const float sigma = __fsqrt_rn(__fmul_rn(total, 1.0f / kD));  // /d exact (power of two)
     const float r = sigma > 0.0f ? __frcp_rn(sigma) : 0.0f;
-    uint32_t w[4 * VB];
+    uint32_t w[2 * VB];
 #pragma unroll
-    for (int j = 0; j < 4 * VB; j++) w[j] = 0;
+    for (int j = 0; j < 2 * VB; j++) w[j] = 0;
     if constexpr (VB <= 4) {
         float t[(1 << VB) - 1];
 #pragma unroll
-        for (int j = 0; j < (1 << VB) - 1; j++) t[j] = p.thr[cb_off(VB) + j];
+        for (int j = 0; j < (1 << VB) - 1; j++) t[j] = thr_smem[j];
 #pragma unroll
-        for (int i = 0; i < kD; i++) {
+        for (int i = 0; i < kHalf; i++) {
             const float u = __fmul_rn(y[i], r);
             put_code<VB>(w, i, search_reg<VB>(u, t, 0u));
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kD; i++) {
+        for (int i = 0; i < kHalf; i++) {
             const float u = __fmul_rn(y[i], r);
             put_code<VB>(w, i, search_smem<VB>(u, thr_smem));
         }
     }
-    const size_t sidx = (static_cast<size_t>(b) * p.H + h) * p.capacity + pos;
-    store_record<VB>(p.vcodes + static_cast<size_t>(b) * p.vblock + p.voff[h] +
-                         static_cast<size_t>(pos) * (16 * VB), w);
-    p.vscale[sidx] = sigma;
+    if (store) {
+        store_half_record<VB>(p.vcodes + static_cast<size_t>(b) * p.vblock + p.voff[h] +
+                                  static_cast<size_t>(pos) * (16 * VB) + half * (8 * VB), w);
+        if (!half) p.vscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = sigma;
+    }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    compress_kernel(const __grid_constant__ CompressParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *rows = smem;                                            // [2][64][272]
-    uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + 2 * kTok * kRow);  // [64]
-    float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);             // [128]
-    float *thr = out_scale + kD;                                                 // [255]
-
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int t0 = blockIdx.x * kTok;
-    const int nt = min(kTok, p.T - t0);
+// Stage block `blk` (t-block fastest, then head, then batch) into buffer `dst`.
+__device__ __forceinline__ void stage_block(const CompressParams &p, int n_tblk, int blk, uint8_t *dst) {
+    const int tb = blk % n_tblk, rest = blk / n_tblk;
+    const int h = rest % p.H, b = rest / p.H;
+    const int t0 = tb * kTok, nt = min(kTok, p.T - t0);
     const uint16_t *srcK = p.K + b * p.sb + h * p.sh;
     const uint16_t *srcV = p.V + b * p.sb + h * p.sh;
     for (int idx = threadIdx.x; idx < 2 * kTok * 16; idx += kThreads) {
         const int which = idx / (kTok * 16), r = (idx >> 4) % kTok, ch = idx & 15;
         if (r < nt) {
             const uint16_t *src = (which ? srcV : srcK) + static_cast<int64_t>(t0 + r) * p.st + ch * 8;
-            cp_async16(rows + (which * kTok + r) * kRow + ch * 16, src);
+            cp_async16(dst + (which * kTok + r) * kRow + (ch < 8 ? ch * 16 : kHalfOff + (ch - 8) * 16), src);
         }
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    compress_kernel(const __grid_constant__ CompressParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t *bufs = smem;                                                   // [2][2][64][288]
+    uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + 2 * kBuf);      // [64]
+    float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);         // [128]
+    float *thr = out_scale + kD;                                            // [kCbTotal]
+
+    const int n_tblk = (p.T + kTok - 1) / kTok;
+    const int n_blk = n_tblk * p.H * p.B;
+    int blk = blockIdx.x;
+    if (blk < n_blk) stage_block(p, n_tblk, blk, bufs);
     cp_async_commit();
     if (threadIdx.x < kD / 2) {
         const int i = 2 * threadIdx.x;
@@ -262,48 +302,58 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t s1 = (p.sign_bits[(i + 1) >> 5] >> ((i + 1) & 31)) & 1u;
         in_mask[threadIdx.x] = (s0 << 15) | (s1 << 31);
     }
-    {
+    if (threadIdx.x < kD) {
         const int i = threadIdx.x;
         const uint32_t s = (p.sign_bits[i >> 5] >> (i & 31)) & 1u;
         out_scale[i] = s ? -p.inv_sqrt_d : p.inv_sqrt_d;
     }
-    const int vb = p.vbits[h];
-    for (int j = threadIdx.x; j < (1 << vb) - 1; j += kThreads) thr[j] = p.thr[cb_off(vb) + j];
-    cp_async_wait_all();
-    __syncthreads();
+    for (int j = threadIdx.x; j < kCbTotal; j += kThreads) thr[j] = p.thr[j];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = (warp & 1) * 32 + lane;
-    if (r >= nt) return;  // no barrier follows
-    const int pos = p.t_begin + t0 + r;
-    if (warp < 2) {
-        const uint8_t *row = rows + r * kRow;
-        const bool q = p.qrank[h] >= 0;
-        switch (p.kbits[h] * 2 + (q ? 1 : 0)) {
-#define TQ_KEY_CASE(KB)                                                                     \
-    case 2 * KB: key_vector<KB, false>(p, row, in_mask, out_scale, b, h, pos); break;      \
-    case 2 * KB + 1: key_vector<KB, true>(p, row, in_mask, out_scale, b, h, pos); break;
-            TQ_KEY_CASE(1) TQ_KEY_CASE(2) TQ_KEY_CASE(3) TQ_KEY_CASE(4)
-            TQ_KEY_CASE(5) TQ_KEY_CASE(6) TQ_KEY_CASE(7) TQ_KEY_CASE(8)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane & 1;
+    const int r = (warp & 3) * 16 + (lane >> 1);  // this pair's row in the block
+    for (int it = 0; blk < n_blk; blk += gridDim.x, it++) {
+        const int next = blk + gridDim.x;
+        if (next < n_blk) stage_block(p, n_tblk, next, bufs + ((it + 1) & 1) * kBuf);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();  // block `blk` staged and visible
+
+        const int tb = blk % n_tblk, rest = blk / n_tblk;
+        const int h = rest % p.H, b = rest / p.H;
+        const int t0 = tb * kTok, nt = min(kTok, p.T - t0);
+        const bool store = r < nt;
+        const int pos = p.t_begin + t0 + r;
+        const uint8_t *buf = bufs + (it & 1) * kBuf;
+        if (warp < 4) {
+            const uint8_t *hrow = buf + r * kRow + half * kHalfOff;
+            const bool q = p.qrank[h] >= 0;
+            switch (p.kbits[h] * 2 + (q ? 1 : 0)) {
+#define TQ_KEY_CASE(KB)                                                                                  \
+    case 2 * KB: key_vector<KB, false>(p, hrow, in_mask, out_scale, half, b, h, pos, store); break;     \
+    case 2 * KB + 1: key_vector<KB, true>(p, hrow, in_mask, out_scale, half, b, h, pos, store); break;
+                TQ_KEY_CASE(1) TQ_KEY_CASE(2) TQ_KEY_CASE(3) TQ_KEY_CASE(4)
+                TQ_KEY_CASE(5) TQ_KEY_CASE(6) TQ_KEY_CASE(7) TQ_KEY_CASE(8)
 #undef TQ_KEY_CASE
-            default: break;
-        }
-    } else {
-        const uint8_t *row = rows + (kTok + r) * kRow;
-        switch (vb) {
+                default: break;
+            }
+        } else {
+            const uint8_t *hrow = buf + (kTok + r) * kRow + half * kHalfOff;
+            const int vb = p.vbits[h];
+            const float *t = thr + cb_off(vb);
+            switch (vb) {
 #define TQ_VAL_CASE(VB) \
-    case VB: value_vector<VB>(p, row, in_mask, out_scale, thr, b, h, pos); break;
-            TQ_VAL_CASE(1) TQ_VAL_CASE(2) TQ_VAL_CASE(3) TQ_VAL_CASE(4)
-            TQ_VAL_CASE(5) TQ_VAL_CASE(6) TQ_VAL_CASE(7) TQ_VAL_CASE(8)
+    case VB: value_vector<VB>(p, hrow, in_mask, out_scale, t, half, b, h, pos, store); break;
+                TQ_VAL_CASE(1) TQ_VAL_CASE(2) TQ_VAL_CASE(3) TQ_VAL_CASE(4)
+                TQ_VAL_CASE(5) TQ_VAL_CASE(6) TQ_VAL_CASE(7) TQ_VAL_CASE(8)
 #undef TQ_VAL_CASE
-            default: break;
+                default: break;
+            }
         }
+        __syncthreads();  // every lane is done with this buffer before it is restaged
     }
 }
 
-constexpr size_t compress_smem() {
-    return 2 * kTok * kRow + (kD / 2) * 4 + kD * 4 + 256 * 4;
-}
+constexpr size_t compress_smem() { return 2 * kBuf + (kD / 2) * 4 + kD * 4 + kCbTotal * 4; }
 
 // ------------------------------------------------------------------ dequant
 // One thread per (b, h, token, K|V) vector: unpack, scale in binary32 and
@@ -383,7 +433,14 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const dim3 grid((p.T + kTok - 1) / kTok, p.H, p.B);
+    // persistent: two CTAs per SM, each looping over 64-token blocks
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long n_blk = static_cast<long long>((p.T + kTok - 1) / kTok) * p.H * p.B;
+    if (n_blk == 0) return cudaSuccess;
+    const int grid = static_cast<int>(std::min<long long>(n_blk, 2LL * sms));
     compress_kernel<<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
