@@ -7,17 +7,18 @@
 // keys only); "TurboMOQ", "Architecture" (keys: symmetric quantize, values:
 // Lloyd-Max grid quantize, per-head 1-8 bits) and "QJL residual correction".
 //
-// Design (GB300): two threads per vector, each holding 64 of its coordinates
-// in registers: butterfly stages h = 1..32 stay in registers, stage h = 64 is
-// one exchange of the 64 values with the partner lane, and every later
-// reduction (absmax, the pairwise sum of squares) finishes with one more
-// exchange in the same fixed order.  A CTA of 8 warps takes a 64-token block of
-// one (batch, head): warps 0-3 its 64 key vectors, warps 4-7 its 64 value
-// vectors.  CTAs are persistent (two per SM) and double-buffer their blocks:
-// the next block is staged with coalesced 16-byte cp.async copies while the
-// current one is computed.  Shared rows are laid out [64 coordinates | 16 B |
-// 64 coordinates | 16 B] so that the two halves of a vector, read by two
-// neighbouring lanes, fall in different banks.  Every rounding step is an
+// Design (GB300): four lanes per vector, each holding 32 of its coordinates in
+// registers: butterfly stages h = 1..16 stay in registers, stages h = 32 and
+// h = 64 are exchanges with the partner lanes (xor 1, xor 2), and every later
+// reduction (absmax, the pairwise sum of squares) finishes with exchanges in the
+// same fixed order.  A CTA of 8 warps runs two independent groups: warps 0-3
+// compress key vectors, warps 4-7 value vectors, 32 vectors per pass.  Each
+// group loops over 32-token blocks of (batch, head) on its own (persistent
+// CTAs, three per SM), double-buffers its rows with coalesced 16-byte cp.async
+// copies and synchronises on its own named barrier, so the lighter key path
+// never waits for the value path.  Shared rows are laid out as four 80-byte
+// quarters (64 B of coordinates + 16 B pad) so that the eight 16-byte reads of
+// a load phase fall in eight different bank groups.  Every rounding step is an
 // explicit IEEE binary32 intrinsic (__fadd_rn, __fmul_rn, __frcp_rn,
 // __fsqrt_rn): no contraction into FMA, so the codes are the same bits the
 // fixed-order format defines.
@@ -30,12 +31,12 @@
 namespace tqk {
 namespace {
 
-constexpr int kTok = 64;         // tokens per block
-constexpr int kRow = 288;        // shared row: 128 B | 16 B pad | 128 B | 16 B pad
-constexpr int kHalfOff = 144;    // byte offset of coordinates 64..127 in a row
-constexpr int kThreads = 256;    // 8 warps: 64 key and 64 value vectors, two lanes each
-constexpr int kHalf = kD / 2;
-constexpr int kBuf = 2 * kTok * kRow;  // one staged block (keys then values)
+constexpr int kTok = 32;          // tokens per block
+constexpr int kQuarter = 80;      // 64 B of coordinates + 16 B pad
+constexpr int kRow = 4 * kQuarter;
+constexpr int kThreads = 256;     // two groups of 4 warps (keys, values); 4 lanes per vector
+constexpr int kQ = kD / 4;        // coordinates per lane
+constexpr int kGroupBuf = kTok * kRow;  // one staged block of one group
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -46,18 +47,24 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+// barrier of one 128-thread group (ids 1, 2; 0 is __syncthreads)
+__device__ __forceinline__ void group_sync(int group) {
+    if (group == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+    else asm volatile("bar.sync 2, 128;" ::: "memory");
+}
 
-// y = R x for one 128-vector held by a lane pair: this lane's coordinates
-// [64 half, 64 half + 64) in a[0..63].  Input sign flip on the fp16 bits, the
-// seven butterfly stages h = 1..64 in ascending order (h = 64 across the pair:
-// the low lane keeps a_i + a_{i+64}, the high lane a_i - a_{i+64}), then one
-// rounded multiply by +-binary32(1/sqrt(d)) (the output sign folded in).
-__device__ __forceinline__ void load_rotate(const uint8_t *half_row, const uint32_t *in_mask,
-                                            const float *out_scale, int half, float (&a)[kHalf]) {
+// y = R x for one 128-vector held by four lanes: this lane's coordinates
+// [32 q, 32 q + 32) in a[0..31].  Input sign flip on the fp16 bits, the seven
+// butterfly stages h = 1..64 in ascending order (h = 32: lanes q, q^1; h = 64:
+// lanes q, q^2; the lower lane keeps a_i + a_{i+h}, the upper one
+// a_i - a_{i+h}), then one rounded multiply by +-binary32(1/sqrt(d)) (the
+// output sign folded in).
+__device__ __forceinline__ void load_rotate(const uint8_t *qrow, const uint32_t *in_mask, const float *out_scale,
+                                            int q, float (&a)[kQ]) {
 #pragma unroll
-    for (int c = 0; c < 8; c++) {
-        uint4 v = *reinterpret_cast<const uint4 *>(half_row + c * 16);
-        const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + half * 32 + c * 4);
+    for (int c = 0; c < 4; c++) {
+        uint4 v = *reinterpret_cast<const uint4 *>(qrow + c * 16);
+        const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + q * 16 + c * 4);
         v.x ^= mk.x; v.y ^= mk.y; v.z ^= mk.z; v.w ^= mk.w;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -68,9 +75,9 @@ __device__ __forceinline__ void load_rotate(const uint8_t *half_row, const uint3
         }
     }
 #pragma unroll
-    for (int h = 1; h < kHalf; h <<= 1) {
+    for (int h = 1; h < kQ; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < kHalf; i++) {
+        for (int i = 0; i < kQ; i++) {
             if ((i & h) == 0) {
                 const float u = a[i], v = a[i + h];
                 a[i] = __fadd_rn(u, v);
@@ -79,13 +86,17 @@ __device__ __forceinline__ void load_rotate(const uint8_t *half_row, const uint3
         }
     }
 #pragma unroll
-    for (int i = 0; i < kHalf; i++) {
-        const float o = __shfl_xor_sync(0xffffffffu, a[i], 1);
-        a[i] = half ? __fsub_rn(o, a[i]) : __fadd_rn(a[i], o);
+    for (int x = 1; x <= 2; x <<= 1) {
+        const bool upper = (q & x) != 0;
+#pragma unroll
+        for (int i = 0; i < kQ; i++) {
+            const float o = __shfl_xor_sync(0xffffffffu, a[i], x);
+            a[i] = upper ? __fsub_rn(o, a[i]) : __fadd_rn(a[i], o);
+        }
     }
 #pragma unroll
-    for (int c = 0; c < kHalf / 4; c++) {
-        const float4 s = *reinterpret_cast<const float4 *>(out_scale + half * kHalf + 4 * c);
+    for (int c = 0; c < kQ / 4; c++) {
+        const float4 s = *reinterpret_cast<const float4 *>(out_scale + q * kQ + 4 * c);
         a[4 * c] = __fmul_rn(a[4 * c], s.x);
         a[4 * c + 1] = __fmul_rn(a[4 * c + 1], s.y);
         a[4 * c + 2] = __fmul_rn(a[4 * c + 2], s.z);
@@ -93,19 +104,19 @@ __device__ __forceinline__ void load_rotate(const uint8_t *half_row, const uint3
     }
 }
 
-// Code i of this lane's 64 occupies bits [B*i, B*i + B) of its half record
-// (the record's bytes [8 B half, 8 B half + 8 B)), LSB first.
+// Code i of this lane's 32 occupies bits [B*i, B*i + B) of its quarter record
+// (the record's bytes [4 B q, 4 B q + 4 B)), LSB first.
 template <int B>
-__device__ __forceinline__ void put_code(uint32_t (&w)[2 * B], int i, uint32_t k) {
+__device__ __forceinline__ void put_code(uint32_t (&w)[B], int i, uint32_t k) {
     const int bit = i * B, wi = bit >> 5, sh = bit & 31;
     w[wi] |= k << sh;
     if (sh + B > 32) w[wi + 1] |= k >> (32 - sh);
 }
 
 template <int B>
-__device__ __forceinline__ void store_half_record(uint8_t *dst, const uint32_t (&w)[2 * B]) {
+__device__ __forceinline__ void store_quarter_record(uint8_t *dst, const uint32_t (&w)[B]) {
 #pragma unroll
-    for (int j = 0; j < B; j++) reinterpret_cast<uint2 *>(dst)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
+    for (int j = 0; j < B; j++) reinterpret_cast<uint32_t *>(dst)[j] = w[j];
 }
 
 // Select t[k*STRIDE] for a runtime k < N from a register-resident table (a
@@ -145,25 +156,26 @@ __device__ __forceinline__ uint32_t search_smem(float u, const float *t) {
     return k;
 }
 
-// One key vector (lane pair); `store` is false for rows past the block's end
-// (the pair still runs so that its exchanges stay warp-uniform).
+// One key vector (four lanes); `store` is false for rows past the block's end
+// (the lanes still run so that their exchanges stay warp-uniform).
 template <int KB, bool QJL>
-__device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *half_row, const uint32_t *in_mask,
-                                        const float *out_scale, int half, int b, int h, int pos, bool store) {
-    float y[kHalf];
-    load_rotate(half_row, in_mask, out_scale, half, y);
+__device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
+                                        const float *out_scale, int q, int b, int h, int pos, bool store) {
+    float y[kQ];
+    load_rotate(qrow, in_mask, out_scale, q, y);
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kHalf; i++) m = fmaxf(m, fabsf(y[i]));
+    for (int i = 0; i < kQ; i++) m = fmaxf(m, fabsf(y[i]));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     const float r = m > 0.0f ? __frcp_rn(m) : 0.0f;
     constexpr float half_cells = static_cast<float>(1 << (KB - 1));
     constexpr float top = static_cast<float>((1 << KB) - 1);
-    uint32_t w[2 * KB];
+    uint32_t w[KB];
 #pragma unroll
-    for (int j = 0; j < 2 * KB; j++) w[j] = 0;
+    for (int j = 0; j < KB; j++) w[j] = 0;
 #pragma unroll
-    for (int i = 0; i < kHalf; i++) {
+    for (int i = 0; i < kQ; i++) {
         const float v = __fmul_rn(y[i], r);
         const float t = __fadd_rn(v, 1.0f);
         float u = __fmul_rn(t, half_cells);  // exact: power of two
@@ -179,122 +191,143 @@ __device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *
         }
     }
     if (store) {
-        store_half_record<KB>(p.kcodes + static_cast<size_t>(b) * p.kblock + p.koff[h] +
-                                  static_cast<size_t>(pos) * (16 * KB) + half * (8 * KB), w);
-        if (!half) p.kscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = m;
+        store_quarter_record<KB>(p.kcodes + static_cast<size_t>(b) * p.kblock + p.koff[h] +
+                                     static_cast<size_t>(pos) * (16 * KB) + q * (4 * KB), w);
+        if (q == 0) p.kscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = m;
     }
     if constexpr (QJL) {
         // p_j = sum_i S[j][i] r_i in binary32 (any order: the only decision is the
-        // sign); bit j = (p_j >= 0).  rho = ||r||_2.  Each lane forms partial sums
-        // over its 64 coordinates for 32 projections at a time; the pair adds them
-        // and each lane keeps the signs of its own 64 projections.
+        // sign); bit j = (p_j >= 0).  rho = ||r||_2.  Each lane forms the partial
+        // sum over its 32 coordinates, the four lanes add them, and lane q keeps
+        // the signs of projections [32 q, 32 q + 32).
         float ss = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kHalf; i++) ss = fmaf(y[i], y[i], ss);
+        for (int i = 0; i < kQ; i++) ss = fmaf(y[i], y[i], ss);
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        uint32_t sb[2] = {0u, 0u};
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        uint32_t mine = 0;
 #pragma unroll 1
         for (int jc = 0; jc < 4; jc++) {  // projections 32 jc .. 32 jc + 31
             uint32_t word = 0;
-            for (int jj = 0; jj < 32; jj++) {
-                const float4 *Sj = reinterpret_cast<const float4 *>(p.S + (32 * jc + jj) * kD + half * kHalf);
-                float acc = 0.0f;
+#pragma unroll 1
+            for (int jj = 0; jj < 32; jj += 2) {  // two projections, four partial sums each
+                const float4 *S0 = reinterpret_cast<const float4 *>(p.S + (32 * jc + jj) * kD + q * kQ);
+                const float4 *S1 = S0 + kD / 4;
+                float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i4 = 0; i4 < kHalf / 4; i4++) {
-                    const float4 s = __ldg(Sj + i4);
-                    acc = fmaf(s.x, y[4 * i4], acc);
-                    acc = fmaf(s.y, y[4 * i4 + 1], acc);
-                    acc = fmaf(s.z, y[4 * i4 + 2], acc);
-                    acc = fmaf(s.w, y[4 * i4 + 3], acc);
+                for (int i4 = 0; i4 < kQ / 4; i4++) {
+                    const float4 s = __ldg(S0 + i4), t = __ldg(S1 + i4);
+                    const int e = i4 & 3;
+                    a0[e] = fmaf(s.x, y[4 * i4], a0[e]);
+                    a0[e] = fmaf(s.y, y[4 * i4 + 1], a0[e]);
+                    a0[e] = fmaf(s.z, y[4 * i4 + 2], a0[e]);
+                    a0[e] = fmaf(s.w, y[4 * i4 + 3], a0[e]);
+                    a1[e] = fmaf(t.x, y[4 * i4], a1[e]);
+                    a1[e] = fmaf(t.y, y[4 * i4 + 1], a1[e]);
+                    a1[e] = fmaf(t.z, y[4 * i4 + 2], a1[e]);
+                    a1[e] = fmaf(t.w, y[4 * i4 + 3], a1[e]);
                 }
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                word |= (acc >= 0.0f ? 1u : 0u) << jj;
+                float p0 = (a0[0] + a0[1]) + (a0[2] + a0[3]), p1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+                p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+                p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+                word |= ((p0 >= 0.0f ? 1u : 0u) << jj) | ((p1 >= 0.0f ? 1u : 0u) << (jj + 1));
             }
-            if ((jc >> 1) == half) sb[jc & 1] = word;
+            if (jc == q) mine = word;
         }
         if (store) {
-            const size_t q = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
-            *reinterpret_cast<uint2 *>(p.qjl_signs + q * (kJl / 8) + half * 8) = make_uint2(sb[0], sb[1]);
-            if (!half) p.qjl_norm[q] = sqrtf(ss);
+            const size_t qi = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
+            reinterpret_cast<uint32_t *>(p.qjl_signs + qi * (kJl / 8))[q] = mine;
+            if (q == 0) p.qjl_norm[qi] = sqrtf(ss);
         }
     }
 }
 
 template <int VB>
-__device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *half_row, const uint32_t *in_mask,
-                                          const float *out_scale, const float *thr_smem, int half, int b, int h,
+__device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
+                                          const float *out_scale, const float *thr_smem, int q, int b, int h,
                                           int pos, bool store) {
-    float y[kHalf];
-    load_rotate(half_row, in_mask, out_scale, half, y);
-    // pairwise tree of squares in index order: this lane's 64 give one of the
-    // two subtrees under the root, which adds (low half) + (high half)
-    float s[kHalf / 2];
+    float y[kQ];
+    load_rotate(qrow, in_mask, out_scale, q, y);
+    // pairwise tree of squares in index order: this lane's 32 give one of the
+    // four subtrees two levels under the root; the root adds
+    // (q0 + q1) + (q2 + q3)
+    float s[kQ / 2];
 #pragma unroll
-    for (int j = 0; j < kHalf / 2; j++)
+    for (int j = 0; j < kQ / 2; j++)
         s[j] = __fadd_rn(__fmul_rn(y[2 * j], y[2 * j]), __fmul_rn(y[2 * j + 1], y[2 * j + 1]));
 #pragma unroll
-    for (int len = kHalf / 2; len > 1; len >>= 1) {
+    for (int len = kQ / 2; len > 1; len >>= 1) {
 #pragma unroll
         for (int j = 0; j < len / 2; j++) s[j] = __fadd_rn(s[2 * j], s[2 * j + 1]);
     }
-    const float other = __shfl_xor_sync(0xffffffffu, s[0], 1);
-    const float total = half ? __fadd_rn(other, s[0]) : __fadd_rn(s[0], other);
-    const float sigma = __fsqrt_rn(__fmul_rn(total, 1.0f / kD));  // /d exact (power of two)
+    float t = s[0];
+#pragma unroll
+    for (int x = 1; x <= 2; x <<= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, t, x);
+        t = (q & x) ? __fadd_rn(o, t) : __fadd_rn(t, o);
+    }
+    const float sigma = __fsqrt_rn(__fmul_rn(t, 1.0f / kD));  // /d exact (power of two)
     const float r = sigma > 0.0f ? __frcp_rn(sigma) : 0.0f;
-    uint32_t w[2 * VB];
+    uint32_t w[VB];
 #pragma unroll
-    for (int j = 0; j < 2 * VB; j++) w[j] = 0;
+    for (int j = 0; j < VB; j++) w[j] = 0;
     if constexpr (VB <= 4) {
-        float t[(1 << VB) - 1];
+        float th[(1 << VB) - 1];
 #pragma unroll
-        for (int j = 0; j < (1 << VB) - 1; j++) t[j] = thr_smem[j];
+        for (int j = 0; j < (1 << VB) - 1; j++) th[j] = thr_smem[j];
 #pragma unroll
-        for (int i = 0; i < kHalf; i++) {
+        for (int i = 0; i < kQ; i++) {
             const float u = __fmul_rn(y[i], r);
-            put_code<VB>(w, i, search_reg<VB>(u, t, 0u));
+            put_code<VB>(w, i, search_reg<VB>(u, th, 0u));
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kHalf; i++) {
+        for (int i = 0; i < kQ; i++) {
             const float u = __fmul_rn(y[i], r);
             put_code<VB>(w, i, search_smem<VB>(u, thr_smem));
         }
     }
     if (store) {
-        store_half_record<VB>(p.vcodes + static_cast<size_t>(b) * p.vblock + p.voff[h] +
-                                  static_cast<size_t>(pos) * (16 * VB) + half * (8 * VB), w);
-        if (!half) p.vscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = sigma;
+        store_quarter_record<VB>(p.vcodes + static_cast<size_t>(b) * p.vblock + p.voff[h] +
+                                     static_cast<size_t>(pos) * (16 * VB) + q * (4 * VB), w);
+        if (q == 0) p.vscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = sigma;
     }
 }
 
-// Stage block `blk` (t-block fastest, then head, then batch) into buffer `dst`.
-__device__ __forceinline__ void stage_block(const CompressParams &p, int n_tblk, int blk, uint8_t *dst) {
+// Stage the rows of block `blk` (t-block fastest, then head, then batch) of
+// one group (0: K, 1: V) into `dst`, by the group's 128 threads.
+__device__ __forceinline__ void stage_block(const CompressParams &p, int n_tblk, int blk, int group, int gtid,
+                                            uint8_t *dst) {
     const int tb = blk % n_tblk, rest = blk / n_tblk;
     const int h = rest % p.H, b = rest / p.H;
     const int t0 = tb * kTok, nt = min(kTok, p.T - t0);
-    const uint16_t *srcK = p.K + b * p.sb + h * p.sh;
-    const uint16_t *srcV = p.V + b * p.sb + h * p.sh;
-    for (int idx = threadIdx.x; idx < 2 * kTok * 16; idx += kThreads) {
-        const int which = idx / (kTok * 16), r = (idx >> 4) % kTok, ch = idx & 15;
-        if (r < nt) {
-            const uint16_t *src = (which ? srcV : srcK) + static_cast<int64_t>(t0 + r) * p.st + ch * 8;
-            cp_async16(dst + (which * kTok + r) * kRow + (ch < 8 ? ch * 16 : kHalfOff + (ch - 8) * 16), src);
-        }
+    const uint16_t *src = (group ? p.V : p.K) + b * p.sb + h * p.sh;
+#pragma unroll
+    for (int i = 0; i < kTok * 16 / 128; i++) {
+        const int idx = gtid + 128 * i, r = idx >> 4, ch = idx & 15;
+        if (r < nt)
+            cp_async16(dst + r * kRow + (ch >> 2) * kQuarter + (ch & 3) * 16,
+                       src + static_cast<int64_t>(t0 + r) * p.st + ch * 8);
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     compress_kernel(const __grid_constant__ CompressParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *bufs = smem;                                                   // [2][2][64][288]
-    uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + 2 * kBuf);      // [64]
-    float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);         // [128]
-    float *thr = out_scale + kD;                                            // [kCbTotal]
+    uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + 4 * kGroupBuf);  // [64]
+    float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);          // [128]
+    float *thr = out_scale + kD;                                             // [kCbTotal]
 
     const int n_tblk = (p.T + kTok - 1) / kTok;
     const int n_blk = n_tblk * p.H * p.B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = warp >> 2, gtid = threadIdx.x & 127, q = lane & 3;
+    const int r = (warp & 3) * 8 + (lane >> 2);  // this vector's row in the block
+    uint8_t *bufs = smem + group * 2 * kGroupBuf;
     int blk = blockIdx.x;
-    if (blk < n_blk) stage_block(p, n_tblk, blk, bufs);
+    if (blk < n_blk) stage_block(p, n_tblk, blk, group, gtid, bufs);
     cp_async_commit();
     if (threadIdx.x < kD / 2) {
         const int i = 2 * threadIdx.x;
@@ -308,52 +341,49 @@ __global__ void __launch_bounds__(kThreads, 2)
         out_scale[i] = s ? -p.inv_sqrt_d : p.inv_sqrt_d;
     }
     for (int j = threadIdx.x; j < kCbTotal; j += kThreads) thr[j] = p.thr[j];
+    __syncthreads();  // tables written
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane & 1;
-    const int r = (warp & 3) * 16 + (lane >> 1);  // this pair's row in the block
     for (int it = 0; blk < n_blk; blk += gridDim.x, it++) {
         const int next = blk + gridDim.x;
-        if (next < n_blk) stage_block(p, n_tblk, next, bufs + ((it + 1) & 1) * kBuf);
+        if (next < n_blk) stage_block(p, n_tblk, next, group, gtid, bufs + ((it + 1) & 1) * kGroupBuf);
         cp_async_commit();
         cp_async_wait<1>();
-        __syncthreads();  // block `blk` staged and visible
+        group_sync(group);  // block `blk` staged and visible to the group
 
         const int tb = blk % n_tblk, rest = blk / n_tblk;
         const int h = rest % p.H, b = rest / p.H;
         const int t0 = tb * kTok, nt = min(kTok, p.T - t0);
         const bool store = r < nt;
         const int pos = p.t_begin + t0 + r;
-        const uint8_t *buf = bufs + (it & 1) * kBuf;
-        if (warp < 4) {
-            const uint8_t *hrow = buf + r * kRow + half * kHalfOff;
-            const bool q = p.qrank[h] >= 0;
-            switch (p.kbits[h] * 2 + (q ? 1 : 0)) {
-#define TQ_KEY_CASE(KB)                                                                                  \
-    case 2 * KB: key_vector<KB, false>(p, hrow, in_mask, out_scale, half, b, h, pos, store); break;     \
-    case 2 * KB + 1: key_vector<KB, true>(p, hrow, in_mask, out_scale, half, b, h, pos, store); break;
+        const uint8_t *qrow = bufs + (it & 1) * kGroupBuf + r * kRow + q * kQuarter;
+        if (group == 0) {
+            const bool qj = p.qrank[h] >= 0;
+            switch (p.kbits[h] * 2 + (qj ? 1 : 0)) {
+#define TQ_KEY_CASE(KB)                                                                                 \
+    case 2 * KB: key_vector<KB, false>(p, qrow, in_mask, out_scale, q, b, h, pos, store); break;       \
+    case 2 * KB + 1: key_vector<KB, true>(p, qrow, in_mask, out_scale, q, b, h, pos, store); break;
                 TQ_KEY_CASE(1) TQ_KEY_CASE(2) TQ_KEY_CASE(3) TQ_KEY_CASE(4)
                 TQ_KEY_CASE(5) TQ_KEY_CASE(6) TQ_KEY_CASE(7) TQ_KEY_CASE(8)
 #undef TQ_KEY_CASE
                 default: break;
             }
         } else {
-            const uint8_t *hrow = buf + (kTok + r) * kRow + half * kHalfOff;
             const int vb = p.vbits[h];
             const float *t = thr + cb_off(vb);
             switch (vb) {
 #define TQ_VAL_CASE(VB) \
-    case VB: value_vector<VB>(p, hrow, in_mask, out_scale, t, half, b, h, pos, store); break;
+    case VB: value_vector<VB>(p, qrow, in_mask, out_scale, t, q, b, h, pos, store); break;
                 TQ_VAL_CASE(1) TQ_VAL_CASE(2) TQ_VAL_CASE(3) TQ_VAL_CASE(4)
                 TQ_VAL_CASE(5) TQ_VAL_CASE(6) TQ_VAL_CASE(7) TQ_VAL_CASE(8)
 #undef TQ_VAL_CASE
                 default: break;
             }
         }
-        __syncthreads();  // every lane is done with this buffer before it is restaged
+        group_sync(group);  // the group is done with this buffer before it is restaged
     }
 }
 
-constexpr size_t compress_smem() { return 2 * kBuf + (kD / 2) * 4 + kD * 4 + kCbTotal * 4; }
+constexpr size_t compress_smem() { return 4 * kGroupBuf + (kD / 2) * 4 + kD * 4 + kCbTotal * 4; }
 
 // ------------------------------------------------------------------ dequant
 // One thread per (b, h, token, K|V) vector: unpack, scale in binary32 and
@@ -433,14 +463,14 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    // persistent: two CTAs per SM, each looping over 64-token blocks
+    // persistent: three CTAs per SM, each group looping over 32-token blocks
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const long long n_blk = static_cast<long long>((p.T + kTok - 1) / kTok) * p.H * p.B;
     if (n_blk == 0) return cudaSuccess;
-    const int grid = static_cast<int>(std::min<long long>(n_blk, 2LL * sms));
+    const int grid = static_cast<int>(std::min<long long>(n_blk, 3LL * sms));
     compress_kernel<<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
