@@ -20,6 +20,9 @@
  *     the host before anything is launched; nothing aborts or throws.
  *   - Device pointers are caller-owned CUDA device memory; the library never
  *     allocates or frees device memory.  Host pointers are caller-owned too.
+ *     The one exception on the host: decode calls keep eight pinned host
+ *     staging buffers for their plan upload (allocated by the first calls,
+ *     grown when a larger plan needs it, kept until the process exits).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Launches are asynchronous on it; errors of kernel execution surface at
  *     the caller's next synchronisation.  TQ_ERR_CUDA reports a launch error
@@ -211,8 +214,12 @@ tq_status tq_decode_workspace_size(const tq_layer_view *layers, int n_layers, in
  * qjl_S: device jl_dim x d floats, required iff a packed segment uses QJL.
  * workspace: device, >= tq_decode_workspace_size bytes (TQ_ERR_SIZE otherwise).
  * The call copies a small plan (host -> workspace) with cudaMemcpyAsync from
- * pageable host memory, then launches four kernels on `stream`.  A layer with
- * no tokens yields zeros. */
+ * one of the library's pinned staging buffers (so the host does not wait for
+ * the stream), then launches its kernels on `stream`: the QJL query prep (if
+ * any QJL segment), the fp16-segment split-K kernel (if any fp16 segment) and
+ * one persistent split-K kernel per (key bits, value bits, QJL) class of the
+ * packed segments, each merging the partials of the (layer, batch, KV head)
+ * it completes.  A layer with no tokens yields zeros. */
 tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int batch,
                               int n_heads, int q_heads, int head_dim, const float *qjl_S,
                               int jl_dim, const void *q, float *out, void *workspace,
@@ -248,7 +255,8 @@ tq_status tq_set_decode_kernel_events(void *start, void *stop);
  * owned by another framework's allocator.  The scratch (plan, rotated queries,
  * split-K partials) is a fixed array of TQ_STATIC_WORKSPACE_BYTES inside the
  * library instead of a caller buffer; the caller still passes q and out.  The
- * call allocates nothing.
+ * call allocates no device memory (its plan upload uses the library's pinned
+ * host staging buffers, allocated by the first decode calls of the process).
  *   - Set-up: the first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and caches it; make that
  *     first call before any stream capture.

@@ -22,8 +22,7 @@ namespace {
 
 // -------------------------------------------------------------- fp16 kernel
 constexpr int kRow16 = 272;  // padded row of 128 fp16 (conflict-free ldmatrix)
-constexpr int kStages16 = 3;
-constexpr int kStage16Bytes = 2 * kStageTokens * kRow16;
+constexpr int kStage16Bytes = 2 * kStageTokens * kRow16;  // one 64-token chunk of K and V
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(p));
@@ -40,8 +39,10 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *
 
 // Tokens kept in fp16 (sinks, newest tier, chunk buffer), attended in the
 // original space with the unrotated query: ldmatrix gives K rows as the A
-// fragment of Q.K and V rows transposed as the A fragment of P.V.
-__global__ void __launch_bounds__(kThreads, 2)
+// fragment of Q.K and V rows transposed as the A fragment of P.V.  One CTA per
+// (item, batch element, 64-token chunk): a single staged chunk, so that many
+// small CTAs (six per SM) cover the memory latency together.
+__global__ void __launch_bounds__(kThreads, 6)
     decode_fp16_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int item_lo, const int item_hi) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int idx = find_item(ws.items, item_lo, item_hi, blockIdx.x);
@@ -49,22 +50,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int local = blockIdx.x - it.cta_begin;
     const int b = local / it.n_chunks, chunk = local - b * it.n_chunks;
     const int tok0 = chunk * it.chunk;
-    const int ntok = min(it.chunk, it.n_tokens - tok0);
+    const int ntok = min(it.chunk, it.n_tokens - tok0);  // <= kStageTokens
     const uint8_t *K = it.kc + b * it.kstride + static_cast<size_t>(tok0) * (kD * 2);
     const uint8_t *V = it.vc + b * it.vstride + static_cast<size_t>(tok0) * (kD * 2);
-    const int n_st = (ntok + kStageTokens - 1) / kStageTokens;
-
-    auto load_stage = [&](int s) {
-        uint8_t *dst = smem + (s % kStages16) * kStage16Bytes;
-        const int t0 = s * kStageTokens;
-        const int n = min(kStageTokens, ntok - t0);
-        for (int i = threadIdx.x; i < 2 * kStageTokens * 16; i += kThreads) {
-            const int which = i / (kStageTokens * 16), r = (i >> 4) % kStageTokens, ch = i & 15;
-            const uint8_t *src = (which ? V : K) + static_cast<size_t>(t0 + r) * (kD * 2) + ch * 16;
-            const bool ok = r < n;
-            cp_async16_zfill(dst + (which * kStageTokens + r) * kRow16 + ch * 16, ok ? src : K, ok ? 16 : 0);
-        }
-    };
+    for (int i = threadIdx.x; i < 2 * kStageTokens * 16; i += kThreads) {
+        const int which = i / (kStageTokens * 16), r = (i >> 4) % kStageTokens, ch = i & 15;
+        const uint8_t *src = (which ? V : K) + static_cast<size_t>(r) * (kD * 2) + ch * 16;
+        const bool ok = r < ntok;
+        cp_async16_zfill(smem + (which * kStageTokens + r) * kRow16 + ch * 16, ok ? src : K, ok ? 16 : 0);
+    }
+    cp_async_commit();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int gqa = dims.gqa;
@@ -86,21 +81,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     WarpState st;
     init_state(st);
-#pragma unroll
-    for (int s = 0; s < kStages16 - 1; s++) {
-        if (s < n_st) load_stage(s);
-        cp_async_commit();
-    }
-    for (int s = 0; s < n_st; s++) {
-        cp_async_wait<kStages16 - 2>();
-        __syncthreads();
-        if (s + kStages16 - 1 < n_st) load_stage(s + kStages16 - 1);
-        cp_async_commit();
-        const uint8_t *buf = smem + (s % kStages16) * kStage16Bytes;
-        const int n = min(kStageTokens, ntok - s * kStageTokens);
-        const int tile0 = warp * 16;
-        if (tile0 >= n) continue;
-        const uint8_t *Ks = buf, *Vs = buf + kStageTokens * kRow16;
+    cp_async_wait<0>();
+    __syncthreads();
+    const int tile0 = warp * 16;
+    if (tile0 < ntok) {
+        const uint8_t *Ks = smem, *Vs = smem + kStageTokens * kRow16;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
@@ -110,8 +95,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             mma16816(acc, a[0], a[1], a[2], a[3], bq[kk][0], bq[kk][1]);
         }
         uint32_t b0, b1;
-        softmax_tile(st, (acc[0] + acc[1]) * dims.qk_scale, (acc[2] + acc[3]) * dims.qk_scale, tile0 + g < n,
-                     tile0 + g + 8 < n, 1.f, 1.f, g, c, c < gqa, b0, b1);
+        softmax_tile(st, (acc[0] + acc[1]) * dims.qk_scale, (acc[2] + acc[3]) * dims.qk_scale, tile0 + g < ntok,
+                     tile0 + g + 8 < ntok, 1.f, 1.f, g, c, c < gqa, b0, b1);
 #pragma unroll
         for (int mt = 0; mt < 8; mt++) {
             uint32_t a[4];
@@ -121,14 +106,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             mma16816(st.acc[mt], a[0], a[1], a[2], a[3], b0, b1);
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    __syncthreads();  // the staged chunk is dead: its space becomes the merge scratch
     const int slot = ws.grp_part[static_cast<size_t>(idx) * dims.B + b] + chunk;
     float *part = ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride);
     write_partial(st, reinterpret_cast<float *>(smem), part, gqa,
                   [g](int mt, int r) { return 16 * mt + g + 8 * r; });
     pdl_wait();  // this grid's completion implies the completion of the earlier ones
-    finish_and_combine(dims, ws, it.layer, b, it.head, reinterpret_cast<int *>(smem + kStages16 * kStage16Bytes));
+    finish_and_combine(dims, ws, it.layer, b, it.head, reinterpret_cast<int *>(smem + kStage16Bytes));
 }
 
 // -------------------------------------------------------------- prep kernel
@@ -198,7 +182,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
                                   int n_classes, const float *S, const unsigned short (*value_half)[256],
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
     static bool configured = false;
-    const size_t smem16 = static_cast<size_t>(dec::kStages16) * dec::kStage16Bytes + 16;
+    const size_t smem16 = static_cast<size_t>(dec::kStage16Bytes) + 16;
     if (!configured) {
         const cudaError_t e = cudaFuncSetAttribute(dec::decode_fp16_kernel,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -206,10 +190,13 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    // Order: [prep] -> fp16 segments -> packed classes.  Every kernel after the
-    // first may start early (programmatic dependent launch): the split-K grids
-    // are independent of each other; the QJL ones wait for prep before reading
-    // its outputs, and each grid waits for its predecessor before exiting.
+    // Order: [prep] -> packed classes -> fp16 segments.  Every kernel after the
+    // first may start early (programmatic dependent launch); each grid waits
+    // for its predecessor before its final merges, the QJL classes also wait
+    // for prep before reading its outputs.  The persistent packed grids come
+    // first so that all their CTAs start together (their stage ranges are fixed:
+    // a CTA that starts late finishes late); the many small fp16 CTAs come last
+    // and fill the SMs the packed grid frees at its end.
     bool first = true;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -217,20 +204,6 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
     if (dims.any_qjl) {
         const int n_warps = dims.L * dims.B * dims.Hq;
         dec::decode_prep_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
-        first = false;
-    }
-    for (int i = 0; i < n_classes; i++) {
-        const ClassLaunch &c = classes[i];
-        if (c.n_ctas <= 0 || c.kb != 16) continue;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(c.n_ctas);
-        cfg.blockDim = dim3(dec::kThreads);
-        cfg.dynamicSmemBytes = smem16;
-        cfg.stream = s;
-        cfg.attrs = attr;
-        cfg.numAttrs = first ? 0 : 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel, dims, ws, c.item_lo, c.item_hi);
-        if (e != cudaSuccess) return e;
         first = false;
     }
     bool any_packed = false;
@@ -248,7 +221,24 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         if (e != cudaSuccess) return e;
         first = false;
     }
-    if (ev_stop && any_packed) cudaEventRecord(ev_stop, s);
+    if (ev_stop && any_packed) {
+        cudaEventRecord(ev_stop, s);
+        first = true;
+    }
+    for (int i = 0; i < n_classes; i++) {
+        const ClassLaunch &c = classes[i];
+        if (c.n_ctas <= 0 || c.kb != 16) continue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c.n_ctas);
+        cfg.blockDim = dim3(dec::kThreads);
+        cfg.dynamicSmemBytes = smem16;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = first ? 0 : 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel, dims, ws, c.item_lo, c.item_hi);
+        if (e != cudaSuccess) return e;
+        first = false;
+    }
     return cudaGetLastError();
 }
 

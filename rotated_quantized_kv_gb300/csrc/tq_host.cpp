@@ -216,7 +216,6 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     if (!pow2(d) || d < 16 || d > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     const int gqa = Hq / H;
     if (d != kD || (gqa != 1 && gqa != 2 && gqa != 4)) return TQ_ERR_UNSUPPORTED;
-    double total_bytes = 0.0;
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
         if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
@@ -245,21 +244,21 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                     }
                 }
                 if (q && (jl != kJl || L.jl_dim != kJl)) return TQ_ERR_UNSUPPORTED;
-                double per = 0;
-                for (int h = 0; h < H; ++h) per += 16.0 * (L.kbits[h] + L.vbits[h]) + 8 + (L.qjl[h] ? 20 : 0);
-                total_bytes += per * B * sg.n_tokens;
             } else {
                 if (check_ptrs) {
                     if (!sg.k16 || !sg.v16) return TQ_ERR_ARG;
                     if (!aligned16(sg.k16) || !aligned16(sg.v16)) return TQ_ERR_ALIGN;
                 }
-                total_bytes += 4.0 * d * H * B * sg.n_tokens;
             }
         }
     }
-    const double target = std::fmin(std::fmax(total_bytes / (sm_count() * 24.0), 8192.0), 262144.0);
     P = Plan();
     P.layer.assign(n_layers, LayerPlan{});
+    {
+        size_t n = 0;
+        for (int l = 0; l < n_layers; ++l) n += static_cast<size_t>(layers[l].n_segments) * H;
+        P.items.reserve(n);
+    }
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
         LayerPlan &lp = P.layer[l];
@@ -277,7 +276,6 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                 w.layer = l;
                 w.head = h;
                 w.n_tokens = sg.n_tokens;
-                double bpt;
                 if (sg.kind == TQ_SEG_PACKED) {
                     w.kc = static_cast<const uint8_t *>(sg.packed.kcodes) + o.koff[h];
                     w.vc = static_cast<const uint8_t *>(sg.packed.vcodes) + o.voff[h];
@@ -296,26 +294,44 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                         P.any_qjl = true;
                         lp.has_qjl = 1;
                     }
-                    bpt = 16.0 * (w.kb + w.vb) + 8 + (w.qjl ? 20 : 0);
                 } else {
                     const size_t row = cap * d * 2;  // bytes of one (b, h) block
                     w.kc = static_cast<const uint8_t *>(sg.k16) + h * row;
                     w.vc = static_cast<const uint8_t *>(sg.v16) + h * row;
                     w.kstride = w.vstride = H * row;
                     w.kb = w.vb = 16;
-                    bpt = 4.0 * d;
                 }
-                int chunk = static_cast<int>(std::ceil(target / bpt));
-                chunk = ((chunk + kStageTokens - 1) / kStageTokens) * kStageTokens;
-                const int maxc = ((sg.n_tokens + kStageTokens - 1) / kStageTokens) * kStageTokens;
-                w.chunk = std::max(kStageTokens, std::min(chunk, maxc));
+                // fp16 segments: one CTA per 64-token chunk (packed segments
+                // ignore the chunk: their persistent CTAs split the stages)
+                w.chunk = kStageTokens;
                 w.n_chunks = (sg.n_tokens + w.chunk - 1) / w.chunk;
                 P.items.push_back(w);
             }
         }
     }
-    std::stable_sort(P.items.begin(), P.items.end(),
-                     [](const WorkItem &a, const WorkItem &b) { return class_key(a) < class_key(b); });
+    {  // stable bucket sort by class (at most 2 * 8 * 8 packed classes, fp16 last)
+        std::vector<int> key(P.items.size());
+        int nkeys = 0;
+        int slot_of[2 * 16 * 16 + 2];
+        std::fill(std::begin(slot_of), std::end(slot_of), -1);
+        int keys[2 * 16 * 16 + 2];
+        for (size_t i = 0; i < P.items.size(); ++i) {
+            const int k = P.items[i].kind == TQ_SEG_FP16 ? 2 * 16 * 16 + 1 : class_key(P.items[i]);
+            if (slot_of[k] < 0) {
+                slot_of[k] = 0;
+                keys[nkeys++] = k;
+            }
+            key[i] = k;
+        }
+        std::sort(keys, keys + nkeys);
+        std::vector<int> start(nkeys + 1, 0);
+        for (int j = 0; j < nkeys; ++j) slot_of[keys[j]] = j;
+        for (size_t i = 0; i < P.items.size(); ++i) start[slot_of[key[i]] + 1]++;
+        for (int j = 0; j < nkeys; ++j) start[j + 1] += start[j];
+        std::vector<WorkItem> sorted(P.items.size());
+        for (size_t i = 0; i < P.items.size(); ++i) sorted[start[slot_of[key[i]]]++] = P.items[i];
+        P.items.swap(sorted);
+    }
     // classes: packed ones run persistent CTAs over their 128-token stages,
     // fp16 runs one CTA per (item, batch element, chunk)
     const int sms = sm_count();
@@ -624,6 +640,27 @@ tq_status tq_decode_workspace_size(const tq_layer_view *layers, int n_layers, in
     return TQ_OK;
 }
 
+// Pinned host staging of the per-call plan.  A copy from pageable memory
+// synchronises the stream before it starts, which would keep the caller's host
+// thread from running ahead of the GPU; slots of pinned memory are reused
+// round-robin, each guarded by an event recorded after its copy.
+struct PlanStaging {
+    static constexpr int kSlots = 8;
+    struct Slot {
+        void *p = nullptr;
+        size_t cap = 0;
+        cudaEvent_t ev = nullptr;
+        int dev = -1;
+    };
+    std::mutex mu;
+    Slot slot[kSlots];
+    int next = 0;
+};
+PlanStaging &plan_staging() {
+    static PlanStaging s;
+    return s;
+}
+
 tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int batch, int n_heads, int q_heads,
                               int head_dim, const float *qjl_S, int jl_dim, const void *q, float *out,
                               void *workspace, size_t ws_bytes, void *stream) {
@@ -635,18 +672,51 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     if (ws_bytes < P.total) return TQ_ERR_SIZE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    // upload the plan (pageable source: staged before the call returns)
-    std::vector<uint8_t> host(P.off_qrot, 0);
-    if (!P.items.empty())
-        std::memcpy(host.data() + P.off_items, P.items.data(), sizeof(WorkItem) * P.items.size());
-    std::memcpy(host.data() + P.off_layer, P.layer.data(), sizeof(LayerPlan) * P.layer.size());
-    if (!P.grp_part.empty()) {
-        std::memcpy(host.data() + P.off_grp_part, P.grp_part.data(), sizeof(int) * P.grp_part.size());
-        std::memcpy(host.data() + P.off_grp_nparts, P.grp_nparts.data(), sizeof(int) * P.grp_nparts.size());
+    // upload the plan (error flag, items, tables, zeroed counters) from a pinned slot
+    cudaError_t e;
+    {
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        PlanStaging &ring = plan_staging();
+        std::lock_guard<std::mutex> lock(ring.mu);
+        PlanStaging::Slot &sl = ring.slot[ring.next];
+        ring.next = (ring.next + 1) % PlanStaging::kSlots;
+        if (sl.ev) {  // the slot's previous copy (kSlots calls ago) has normally long finished
+            e = cudaEventSynchronize(sl.ev);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        if (sl.cap < P.off_qrot) {
+            if (sl.p) cudaFreeHost(sl.p);
+            sl.p = nullptr;
+            sl.cap = 0;
+            const size_t cap = std::max<size_t>(P.off_qrot, 64 * 1024);
+            e = cudaHostAlloc(&sl.p, cap, cudaHostAllocPortable);
+            if (e != cudaSuccess) return cuda_fail(e);
+            sl.cap = cap;
+        }
+        if (sl.ev == nullptr || sl.dev != dev) {
+            if (sl.ev) cudaEventDestroy(sl.ev);
+            sl.ev = nullptr;
+            e = cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e);
+            sl.dev = dev;
+        }
+        uint8_t *host = static_cast<uint8_t *>(sl.p);
+        std::memset(host, 0, P.off_qrot);
+        if (!P.items.empty())
+            std::memcpy(host + P.off_items, P.items.data(), sizeof(WorkItem) * P.items.size());
+        std::memcpy(host + P.off_layer, P.layer.data(), sizeof(LayerPlan) * P.layer.size());
+        if (!P.grp_part.empty()) {
+            std::memcpy(host + P.off_grp_part, P.grp_part.data(), sizeof(int) * P.grp_part.size());
+            std::memcpy(host + P.off_grp_nparts, P.grp_nparts.data(), sizeof(int) * P.grp_nparts.size());
+        }
+        std::memcpy(host + P.off_lbh_total, P.lbh_total.data(), sizeof(int) * P.lbh_total.size());
+        e = cudaMemcpyAsync(ws, host, P.off_qrot, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaEventRecord(sl.ev, s);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
-    std::memcpy(host.data() + P.off_lbh_total, P.lbh_total.data(), sizeof(int) * P.lbh_total.size());
-    cudaError_t e = cudaMemcpyAsync(ws, host.data(), host.size(), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e);
     DecodeWorkspace W;
     W.items = reinterpret_cast<WorkItem *>(ws + P.off_items);
     W.layer = reinterpret_cast<LayerPlan *>(ws + P.off_layer);
