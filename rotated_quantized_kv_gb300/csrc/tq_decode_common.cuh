@@ -449,23 +449,42 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
         float L = 0.f;
         float ar[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
         if (M != kNegInf) {
+            // records four at a time: their loads are independent, so they are
+            // all in flight before the first is used (records of warps without
+            // tokens have m = -inf and contribute nothing)
             for (int ii = 0; ii < n_items; ii++) {
                 const int item = lp.item[h][ii];
                 const size_t gr = static_cast<size_t>(item) * dims.B + b;
                 const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
-                const bool rot = ws.items[item].kind == TQ_SEG_PACKED;
-                for (int c = 0; c < np; c++) {
-                    const float *rec = ws.part + (static_cast<size_t>(p0) + c) * rec_stride + warp * kPartStride;
-                    const float m = __ldcg(rec);
-                    if (m == kNegInf) continue;
-                    const float f = ex2(m - M);
-                    L += f * __ldcg(rec + 1);
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
-                    float *a = rot ? ar : ao;
-                    a[0] += f * v.x;
-                    a[1] += f * v.y;
-                    a[2] += f * v.z;
-                    a[3] += f * v.w;
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+                const float *base = ws.part + static_cast<size_t>(p0) * rec_stride + warp * kPartStride;
+                for (int c0 = 0; c0 < np; c0 += 4) {
+                    float m[4], l[4];
+                    float4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        const int c = min(c0 + u, np - 1);
+                        const float *rec = base + static_cast<size_t>(c) * rec_stride;
+                        m[u] = c0 + u < np ? __ldcg(rec) : kNegInf;
+                        l[u] = __ldcg(rec + 1);
+                        v[u] = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        if (m[u] == kNegInf) continue;
+                        const float f = ex2(m[u] - M);
+                        L += f * l[u];
+                        a[0] += f * v[u].x;
+                        a[1] += f * v[u].y;
+                        a[2] += f * v[u].z;
+                        a[3] += f * v[u].w;
+                    }
+                }
+                const bool rot = ws.items[item].kind == TQ_SEG_PACKED;  // rotated-space sums
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    ar[e] += rot ? a[e] : 0.f;
+                    ao[e] += rot ? 0.f : a[e];
                 }
             }
         }
