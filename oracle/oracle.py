@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
     L.tqo_dequant.argtypes = [_I, _I, ctypes.POINTER(_Segment), _I, _I, _I, _I, _P, _P, _P]
     L.tqo_decode_attention.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_Segment), _P, _P,
                                        _P, _I, _P, _P]
+    L.tqo_requantize.argtypes = [_I, _I, _I, ctypes.POINTER(_Segment), _I, _I, _P, _P,
+                                 ctypes.POINTER(_Segment), _I]
     return L
 
 
@@ -166,7 +168,11 @@ def codebook_f32(bits: int):
     return c.astype(np.float32), t.astype(np.float32)
 
 
+@functools.lru_cache(maxsize=None)
 def _cent_thr_tables():
+    """binary32 centroid and threshold tables of widths 1..8 and C pointer
+    arrays to them (cached: the arrays must outlive every call that uses the
+    pointers)."""
     cents = [np.zeros(1, np.float32)] + [codebook_f32(b)[0] for b in range(1, 9)]
     thrs = [np.zeros(1, np.float32)] + [codebook_f32(b)[1] for b in range(1, 9)]
     cp = (ctypes.c_void_p * 9)(*[c.ctypes.data for c in cents])
@@ -338,6 +344,18 @@ def dequant(seg: PackedSegment, b: int, h: int, t0: int, n: int):
     cs = seg.c_struct()
     lib().tqo_dequant(seg.H, seg.d, ctypes.byref(cs), b, h, t0, n, cp, _ptr(kh), _ptr(vh))
     return kh, vh
+
+
+def requantize(src: PackedSegment, src_t0: int, n: int, dst: PackedSegment, dst_t0: int) -> None:
+    """Tier demotion: tokens [src_t0, src_t0 + n) of src, dequantized in the
+    rotated space, compressed again with dst's widths into [dst_t0, dst_t0 + n)
+    of dst (no QJL on dst)."""
+    assert (src.B, src.H, src.d) == (dst.B, dst.H, dst.d)
+    assert src_t0 + n <= src.capacity and dst_t0 + n <= dst.capacity and not dst.qjl.any()
+    _, _, cp, tp = _cent_thr_tables()
+    ss, ds = src.c_struct(), dst.c_struct()
+    lib().tqo_requantize(src.B, src.H, src.d, ctypes.byref(ss), src_t0, n, cp, tp, ctypes.byref(ds), dst_t0)
+    dst.n_tokens = max(dst.n_tokens, dst_t0 + n)
 
 
 def decode_attention(segments, q: np.ndarray, sign: np.ndarray, H: int,

@@ -413,6 +413,35 @@ void tqo_dequant(int H, int d, const tqo_segment *seg, int b, int h, int t0, int
     }
 }
 
+/* Tier demotion ("TurboMOQ", "Progressive temporal tiering": tokens move to
+ * tiers with fewer bits as they age; "Attention-Weighted Demotion").  Reading:
+ * the rotated-space reconstruction of a packed token (keys m*level(code),
+ * values sigma*c[code], exactly as tqo_dequant) is compressed again with the
+ * destination segment's widths by the same per-vector quantizers, in the
+ * rotated space (no rotation either way).  Tokens [src_t0, src_t0 + n) of src
+ * go to [dst_t0, dst_t0 + n) of dst; destination heads carry no QJL sketch. */
+void tqo_requantize(int B, int H, int d, const tqo_segment *src, int src_t0, int n,
+                    const float *const *cent, const float *const *thr, const tqo_segment *dst,
+                    int dst_t0) {
+    float kh[TQO_MAX_D], vh[TQO_MAX_D];
+    uint8_t code[TQO_MAX_D];
+    for (int b = 0; b < B; b++)
+        for (int h = 0; h < H; h++)
+            for (int t = 0; t < n; t++) {
+                tqo_dequant(H, d, src, b, h, src_t0 + t, 1, cent, kh, vh);
+                const int pos = dst_t0 + t;
+                const size_t sidx = ((size_t)b * H + h) * dst->capacity + pos;
+                const int kb = dst->kbits[h], vb = dst->vbits[h];
+                float m, sg;
+                tqo_quant_key(d, kb, kh, code, &m);
+                tqo_pack(d, kb, code, dst->kcodes + off_codes(dst->kbits, H, d, dst->capacity, b, h, pos));
+                dst->kscale[sidx] = m;
+                tqo_quant_value(d, vb, vh, thr[vb], code, &sg);
+                tqo_pack(d, vb, code, dst->vcodes + off_codes(dst->vbits, H, d, dst->capacity, b, h, pos));
+                dst->vscale[sidx] = sg;
+            }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention over one layer's cache, in binary64.                       */
 /*   packed tokens: khat = R (m*level(code) [+ rhat]), vhat = R (sigma*c[code]),  */
