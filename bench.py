@@ -381,13 +381,32 @@ def run_static(args, rank, world, tq):
     cbytes = sum(m.B * si.n * (m.H * m.d * 4 + si.bytes_per_token(m.d)) for si in m.layers[0] if si.packed)
     comp = {"ms": ms, "tokens": tokens, "mtok": tokens / (ms * 1e-3) / 1e6, "bytes": cbytes}
     del src, scr, calls
+    rq = None
+    if w.tiers:
+        # tier demotion: every layer's K4V4 (warm) tier re-quantised to K3V2 (cold)
+        warm = [[si for si in segs if si.packed and si.kbits[0] == 4][0] for segs in m.layers]
+        n = warm[0].n
+        dst = [tq.PackedSegment(tq.make_layout(m.B, m.H, m.d, warm[0].seg.layout.capacity, 3, 2))
+               for _ in range(2)]
+        rcalls = [(lambda l=l: tq.tq_requantize(warm[l].seg, 0, n, dst[l % 2], 0)) for l in range(m.L)]
+        rms = time_compress(tq, rcalls) / m.L
+        rbytes = m.B * m.H * n * ((16 * 8 + 8) + (16 * 5 + 8))
+        peak, _ = measured_peaks()
+        rq = {"from": "K4V4", "to": "K3V2", "tokens_per_layer": n * m.B, "ms_per_layer": round(rms, 4),
+              "value": round(rbytes / (rms * 1e-3) / 1e9, 1), "unit": "GB/s",
+              "frac_of_peak": round(rbytes / (rms * 1e-3) / 1e9 / peak, 4),
+              "mtok_per_s": round(n * m.B / (rms * 1e-3) / 1e6, 1)}
+        del dst, rcalls
     plan = [(si.pos0, si.n, sorted(set(zip(si.kbits, si.vbits, si.qjl)))) for si in m.layers[0]]
     config = {"workload": w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
               "q_heads": m.Hq, "head_dim": m.d,
               "segments_layer0": [{"pos0": p, "n": n, "k_v_qjl": [list(x) for x in kb]} for p, n, kb in plan],
               "l2": f"inputs larger than L2 ({(pb + ob) / 1e9:.2f} GB read per step)",
               "parallelism": f"replicas x{world}"}
-    return result_line(args, world, m, t, e2e, comp, config, args.workload)
+    res = result_line(args, world, m, t, e2e, comp, config, args.workload)
+    if rq is not None:
+        res["requantize"] = rq
+    return res
 
 
 def run_ours(args, rank, world):

@@ -171,6 +171,21 @@ tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *b
                         const tq_rotation *rot, int t_begin, int n_tokens, float *k_rot,
                         float *v_rot, float *k_orig, float *v_orig, void *stream);
 
+/* Tier demotion ("TurboMOQ", "Progressive temporal tiering": tokens move to
+ * tiers with fewer bits as they age).  Tokens [src_t_begin, src_t_begin + n)
+ * of a packed segment are dequantized in the rotated space (keys m*level(code),
+ * values sigma*centroid[code], binary32) and compressed again with the widths
+ * of `dst` into its positions [dst_t_begin, dst_t_begin + n): the same
+ * per-vector scales and quantizers as tq_compress, applied to the
+ * reconstruction, with no rotation either way.  Both segments must have the
+ * same batch, heads and head_dim; dst must carry no QJL heads
+ * (TQ_ERR_UNSUPPORTED); the two segments' buffers must not overlap.  Any
+ * widths 1..8 are accepted (demotion normally lowers them).  TQ_ERR_SIZE if a
+ * range exceeds its capacity. */
+tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_bufs, int src_t_begin,
+                        const tq_segment_layout *dst, const tq_packed_bufs *dst_bufs, int dst_t_begin,
+                        int n_tokens, void *stream);
+
 /* Progressive tiers by token age ("TurboMOQ", "Progressive temporal tiering"):
  * position p has age n_tokens-1-p; tier i holds ages [bound[i-1], bound[i])
  * (bound[-1] = 0, bound[n_bounds] = infinity).  Writes tier i's position

@@ -156,13 +156,12 @@ __device__ __forceinline__ uint32_t search_smem(float u, const float *t) {
     return k;
 }
 
-// One key vector (four lanes); `store` is false for rows past the block's end
-// (the lanes still run so that their exchanges stay warp-uniform).
+// Quantize and store one key vector held by four lanes (this lane's rotated
+// coordinates [32 q, 32 q + 32) in y); `store` is false for rows past the
+// block's end (the lanes still run so that their exchanges stay warp-uniform).
 template <int KB, bool QJL>
-__device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
-                                        const float *out_scale, int q, int b, int h, int pos, bool store) {
-    float y[kQ];
-    load_rotate(qrow, in_mask, out_scale, q, y);
+__device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ], int q, int b, int h, int pos,
+                                         bool store) {
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < kQ; i++) m = fmaxf(m, fabsf(y[i]));
@@ -244,12 +243,10 @@ __device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *
     }
 }
 
+// Quantize and store one value vector held by four lanes (as key_tail).
 template <int VB>
-__device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
-                                          const float *out_scale, const float *thr_smem, int q, int b, int h,
-                                          int pos, bool store) {
-    float y[kQ];
-    load_rotate(qrow, in_mask, out_scale, q, y);
+__device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[kQ], const float *thr_smem, int q,
+                                           int b, int h, int pos, bool store) {
     // pairwise tree of squares in index order: this lane's 32 give one of the
     // four subtrees two levels under the root; the root adds
     // (q0 + q1) + (q2 + q3)
@@ -294,6 +291,24 @@ __device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t
                                      static_cast<size_t>(pos) * (16 * VB) + q * (4 * VB), w);
         if (q == 0) p.vscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = sigma;
     }
+}
+
+// One key vector of the compress path: rotate, then quantize.
+template <int KB, bool QJL>
+__device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
+                                        const float *out_scale, int q, int b, int h, int pos, bool store) {
+    float y[kQ];
+    load_rotate(qrow, in_mask, out_scale, q, y);
+    key_tail<KB, QJL>(p, y, q, b, h, pos, store);
+}
+
+template <int VB>
+__device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
+                                          const float *out_scale, const float *thr_smem, int q, int b, int h,
+                                          int pos, bool store) {
+    float y[kQ];
+    load_rotate(qrow, in_mask, out_scale, q, y);
+    value_tail<VB>(p, y, thr_smem, q, b, h, pos, store);
 }
 
 // Stage the rows of block `blk` (t-block fastest, then head, then batch) of
@@ -380,6 +395,92 @@ __global__ void __launch_bounds__(kThreads, 3)
             }
         }
         group_sync(group);  // the group is done with this buffer before it is restaged
+    }
+}
+
+// ------------------------------------------------------------------ requantize
+// Code i (0..31) of a lane's quarter record, runtime width: byte loads so that
+// nothing past the quarter is read.
+__device__ __forceinline__ uint32_t quarter_code(const uint8_t *rec, int i, int bits) {
+    const int bit = i * bits, by = bit >> 3, sh = bit & 7;
+    uint32_t v = __ldg(rec + by);
+    if (sh + bits > 8) v |= static_cast<uint32_t>(__ldg(rec + by + 1)) << 8;
+    return (v >> sh) & ((1u << bits) - 1u);
+}
+
+// One demoted key vector (four lanes): the source record's reconstruction
+// m * level(code) in binary32 (level = (2 code + 1) 2^-b - 1, exact), then the
+// destination width's quantizer.
+template <int KB>
+__device__ __noinline__ void key_requant(const RequantParams &p, int q, int b, int h, int sp, int dp, bool store) {
+    const int sb = p.skbits[h];
+    const uint8_t *rec = p.skcodes + static_cast<size_t>(b) * p.skblock + p.skoff[h] +
+                         static_cast<size_t>(sp) * (16 * sb) + q * (4 * sb);
+    const float m = __ldg(p.skscale + (static_cast<size_t>(b) * p.dst.H + h) * p.scapacity + sp);
+    const float inv_cells = __uint_as_float(static_cast<uint32_t>(127 - sb) << 23);  // 2^-b
+    float y[kQ];
+#pragma unroll
+    for (int i = 0; i < kQ; i++) {
+        const float lev = __fadd_rn(__fmul_rn(static_cast<float>(2 * quarter_code(rec, i, sb) + 1), inv_cells), -1.0f);
+        y[i] = __fmul_rn(m, lev);
+    }
+    key_tail<KB, false>(p.dst, y, q, b, h, dp, store);
+}
+
+// One demoted value vector: sigma * centroid[code] in binary32, then the
+// destination width's quantizer.
+template <int VB>
+__device__ __noinline__ void value_requant(const RequantParams &p, const float *cent, const float *thr_smem, int q,
+                                           int b, int h, int sp, int dp, bool store) {
+    const int sb = p.svbits[h];
+    const uint8_t *rec = p.svcodes + static_cast<size_t>(b) * p.svblock + p.svoff[h] +
+                         static_cast<size_t>(sp) * (16 * sb) + q * (4 * sb);
+    const float sg = __ldg(p.svscale + (static_cast<size_t>(b) * p.dst.H + h) * p.scapacity + sp);
+    const float *c = cent + cb_off(sb);
+    float y[kQ];
+#pragma unroll
+    for (int i = 0; i < kQ; i++) y[i] = __fmul_rn(sg, c[quarter_code(rec, i, sb)]);
+    value_tail<VB>(p.dst, y, thr_smem, q, b, h, dp, store);
+}
+
+// One CTA per 32-token block of (batch, head): warps 0-3 keys, 4-7 values,
+// four lanes per vector (the compress kernel's layout and quantizers).
+__global__ void __launch_bounds__(kThreads) requantize_kernel(const __grid_constant__ RequantParams p) {
+    __shared__ float cent[kCbTotal], thr[kCbTotal];
+    for (int j = threadIdx.x; j < kCbTotal; j += kThreads) {
+        cent[j] = p.centroid[j];
+        thr[j] = p.dst.thr[j];
+    }
+    __syncthreads();
+    const int n_tblk = (p.dst.T + kTok - 1) / kTok;
+    const int blk = blockIdx.x;
+    const int tb = blk % n_tblk, rest = blk / n_tblk;
+    const int h = rest % p.dst.H, b = rest / p.dst.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = warp >> 2, q = lane & 3;
+    const int r = (warp & 3) * 8 + (lane >> 2);
+    const int t = tb * kTok + r;
+    const bool store = t < p.dst.T;
+    const int sp = p.s_t0 + min(t, p.dst.T - 1);  // rows past the end re-read the last token
+    const int dp = p.dst.t_begin + t;
+    if (group == 0) {
+        switch (p.dst.kbits[h]) {
+#define TQ_RQ_KEY(KB) \
+    case KB: key_requant<KB>(p, q, b, h, sp, dp, store); break;
+            TQ_RQ_KEY(1) TQ_RQ_KEY(2) TQ_RQ_KEY(3) TQ_RQ_KEY(4) TQ_RQ_KEY(5) TQ_RQ_KEY(6) TQ_RQ_KEY(7) TQ_RQ_KEY(8)
+#undef TQ_RQ_KEY
+            default: break;
+        }
+    } else {
+        const int vb = p.dst.vbits[h];
+        const float *tv = thr + cb_off(vb);
+        switch (vb) {
+#define TQ_RQ_VAL(VB) \
+    case VB: value_requant<VB>(p, cent, tv, q, b, h, sp, dp, store); break;
+            TQ_RQ_VAL(1) TQ_RQ_VAL(2) TQ_RQ_VAL(3) TQ_RQ_VAL(4) TQ_RQ_VAL(5) TQ_RQ_VAL(6) TQ_RQ_VAL(7) TQ_RQ_VAL(8)
+#undef TQ_RQ_VAL
+            default: break;
+        }
     }
 }
 
@@ -472,6 +573,14 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t s) {
     if (n_blk == 0) return cudaSuccess;
     const int grid = static_cast<int>(std::min<long long>(n_blk, 3LL * sms));
     compress_kernel<<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requantize(const RequantParams &p, cudaStream_t s) {
+    const long long n_blk = static_cast<long long>((p.dst.T + kTok - 1) / kTok) * p.dst.H * p.dst.B;
+    if (n_blk == 0) return cudaSuccess;
+    if (n_blk > 0x7fffffffLL) return cudaErrorInvalidValue;
+    requantize_kernel<<<static_cast<unsigned>(n_blk), kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -614,6 +614,71 @@ tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *b
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
+tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_bufs, int src_t_begin,
+                        const tq_segment_layout *dst, const tq_packed_bufs *dst_bufs, int dst_t_begin,
+                        int n_tokens, void *stream) {
+    tq_status st = check_layout(src, true);
+    if (st != TQ_OK) return st;
+    st = check_layout(dst, true);
+    if (st != TQ_OK) return st;
+    if (!src_bufs || !dst_bufs || n_tokens < 0 || src_t_begin < 0 || dst_t_begin < 0) return TQ_ERR_ARG;
+    if (src->batch != dst->batch || src->n_heads != dst->n_heads || src->head_dim != dst->head_dim)
+        return TQ_ERR_ARG;
+    if (src->head_dim != kD) return TQ_ERR_UNSUPPORTED;
+    for (int h = 0; h < dst->n_heads; ++h)
+        if (dst->qjl[h]) return TQ_ERR_UNSUPPORTED;  // demoted tokens carry no sketch
+    if (static_cast<int64_t>(src_t_begin) + n_tokens > src->capacity ||
+        static_cast<int64_t>(dst_t_begin) + n_tokens > dst->capacity)
+        return TQ_ERR_SIZE;
+    if (!src_bufs->kcodes || !src_bufs->vcodes || !src_bufs->kscale || !src_bufs->vscale || !dst_bufs->kcodes ||
+        !dst_bufs->vcodes || !dst_bufs->kscale || !dst_bufs->vscale)
+        return TQ_ERR_ARG;
+    if (!aligned16(src_bufs->kcodes) || !aligned16(src_bufs->vcodes) || !aligned16(dst_bufs->kcodes) ||
+        !aligned16(dst_bufs->vcodes) || !aligned16(src_bufs->kscale) || !aligned16(src_bufs->vscale) ||
+        !aligned16(dst_bufs->kscale) || !aligned16(dst_bufs->vscale))
+        return TQ_ERR_ALIGN;
+    if (!fits_u32(src) || !fits_u32(dst)) return TQ_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return TQ_OK;
+    const Offsets so = offsets(src), d_o = offsets(dst);
+    RequantParams p;
+    std::memset(&p, 0, sizeof(p));
+    CompressParams &q = p.dst;
+    q.B = dst->batch;
+    q.H = dst->n_heads;
+    q.T = n_tokens;
+    q.t_begin = dst_t_begin;
+    q.capacity = dst->capacity;
+    q.kcodes = static_cast<uint8_t *>(dst_bufs->kcodes);
+    q.vcodes = static_cast<uint8_t *>(dst_bufs->vcodes);
+    q.kscale = dst_bufs->kscale;
+    q.vscale = dst_bufs->vscale;
+    q.kblock = d_o.kblock;
+    q.vblock = d_o.vblock;
+    for (int h = 0; h < q.H; ++h) {
+        q.koff[h] = d_o.koff[h];
+        q.voff[h] = d_o.voff[h];
+        q.kbits[h] = dst->kbits[h];
+        q.vbits[h] = dst->vbits[h];
+        q.qrank[h] = -1;
+        p.skoff[h] = so.koff[h];
+        p.svoff[h] = so.voff[h];
+        p.skbits[h] = src->kbits[h];
+        p.svbits[h] = src->vbits[h];
+    }
+    fill_thresholds(q.thr, dst->vbits, q.H);
+    p.skcodes = static_cast<const uint8_t *>(src_bufs->kcodes);
+    p.svcodes = static_cast<const uint8_t *>(src_bufs->vcodes);
+    p.skscale = src_bufs->kscale;
+    p.svscale = src_bufs->vscale;
+    p.skblock = so.kblock;
+    p.svblock = so.vblock;
+    p.scapacity = src->capacity;
+    p.s_t0 = src_t_begin;
+    fill_centroids(p.centroid, src->vbits, src->n_heads);
+    const cudaError_t e = launch_requantize(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
 tq_status tq_age_tiers(int n_tokens, int n_bounds, const int *age_bounds, int *start, int *end) {
     if (n_tokens < 0 || n_bounds < 0 || !start || !end || (n_bounds > 0 && !age_bounds)) return TQ_ERR_ARG;
     for (int i = 0; i < n_bounds; ++i)

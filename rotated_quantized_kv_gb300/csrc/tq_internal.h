@@ -61,6 +61,22 @@ struct DequantParams {
     float centroid[kCbTotal];
 };
 
+// ----------------------------------------------------------------- requantize
+// Tier demotion: tokens [s_t0, s_t0 + dst.T) of a source packed segment,
+// dequantized in the rotated space and compressed again into positions
+// [dst.t_begin, dst.t_begin + dst.T) of the destination segment `dst` (whose K
+// and V pointers are unused).
+struct RequantParams {
+    CompressParams dst;
+    const uint8_t *skcodes, *svcodes;
+    const float *skscale, *svscale;
+    uint32_t skblock, svblock;
+    uint32_t skoff[kMaxH], svoff[kMaxH];
+    uint8_t skbits[kMaxH], svbits[kMaxH];
+    int scapacity, s_t0;
+    float centroid[kCbTotal];    // value centroids, flat by bit width
+};
+
 // ----------------------------------------------------------------- decode
 // One work item per (layer, segment, KV head) of a decode call; its CTAs are
 // (batch element, token chunk) pairs.  Stored in the workspace.
@@ -158,6 +174,7 @@ tq_status record_cuda_error(cudaError_t e);
 // Launchers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams &p, cudaStream_t s);
+cudaError_t launch_requantize(const RequantParams &p, cudaStream_t s);
 cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,
                                   int n_classes, const float *S, const unsigned short (*value_half)[256],
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop);

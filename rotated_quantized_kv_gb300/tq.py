@@ -41,7 +41,8 @@ STATUS = {0: "TQ_OK", -1: "TQ_ERR_ARG", -2: "TQ_ERR_UNSUPPORTED", -3: "TQ_ERR_AL
 EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rotation",
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
-            "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag"]
+            "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag",
+            "tq_requantize"]
 
 
 class TQError(RuntimeError):
@@ -100,6 +101,8 @@ _lib.tq_compress.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(t
                              ctypes.POINTER(tq_packed_bufs), _P]
 _lib.tq_dequantize.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_packed_bufs),
                                ctypes.POINTER(tq_rotation), _I, _I, _P, _P, _P, _P, _P]
+_lib.tq_requantize.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_packed_bufs), _I,
+                               ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_packed_bufs), _I, _I, _P]
 _lib.tq_age_tiers.argtypes = [_I, _I, _P, _P, _P]
 _lib.tq_decode_workspace_size.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, _I, _I,
                                           ctypes.POINTER(ctypes.c_size_t)]
@@ -263,6 +266,16 @@ def tq_compress(seg: PackedSegment, rot: tq_rotation, K: torch.Tensor, V: torch.
     _check(_lib.tq_compress(ctypes.byref(seg.layout), ctypes.byref(rot), _ptr(qjl_S), _ptr(K), _ptr(V), T,
                             sb, sh, st, t_begin, ctypes.byref(seg.bufs()), _stream(stream)), "tq_compress")
     seg.n_tokens = max(seg.n_tokens, t_begin + T)
+
+
+def tq_requantize(src: PackedSegment, src_t_begin: int, n_tokens: int, dst: PackedSegment, dst_t_begin: int,
+                  stream=None):
+    """Tier demotion: tokens [src_t_begin, src_t_begin + n) of src re-quantised
+    in the rotated space with dst's widths into [dst_t_begin, dst_t_begin + n)."""
+    _check(_lib.tq_requantize(ctypes.byref(src.layout), ctypes.byref(src.bufs()), src_t_begin,
+                              ctypes.byref(dst.layout), ctypes.byref(dst.bufs()), dst_t_begin, n_tokens,
+                              _stream(stream)), "tq_requantize")
+    dst.n_tokens = max(dst.n_tokens, dst_t_begin + n_tokens)
 
 
 def tq_dequantize(seg: PackedSegment, t_begin: int, n_tokens: int, rot: tq_rotation | None = None,

@@ -128,6 +128,27 @@ def test_host_side_argument_errors(tq):
         tq.tq_age_tiers(10, [5, 3])
 
 
+def test_requantize_argument_errors(tq):
+    lib = tq._lib
+    fake = tq.tq_packed_bufs(16, 16, 16, 16, None, None)
+    src = tq.make_layout(2, 4, 128, 64, 4, 4)
+
+    def call(dst_layout, s0=0, d0=0, n=8, src_layout=src):
+        return lib.tq_requantize(ctypes.byref(src_layout), ctypes.byref(fake), s0, ctypes.byref(dst_layout),
+                                 ctypes.byref(fake), d0, n, None)
+    assert call(tq.make_layout(2, 2, 128, 64, 3, 2)) == -1           # head counts differ
+    assert call(tq.make_layout(1, 4, 128, 64, 3, 2)) == -1           # batch differs
+    assert call(tq.make_layout(2, 4, 128, 64, 2, 2, qjl=[1, 0, 0, 0])) == -2  # QJL on the destination
+    assert call(tq.make_layout(2, 4, 128, 32, 3, 2), d0=30) == -4    # destination range past capacity
+    assert call(tq.make_layout(2, 4, 128, 64, 3, 2), s0=60) == -4    # source range past capacity
+    assert call(tq.make_layout(2, 4, 128, 64, 9, 2)) == -1           # width outside 1..8
+    assert call(tq.make_layout(2, 4, 128, 64, 3, 2), n=0) == 0       # nothing to do
+    odd = tq.tq_packed_bufs(18, 16, 16, 16, None, None)
+    assert lib.tq_requantize(ctypes.byref(src), ctypes.byref(odd), 0,
+                             ctypes.byref(tq.make_layout(2, 4, 128, 64, 3, 2)), ctypes.byref(fake), 0, 8,
+                             None) == -3                                # misaligned buffer
+
+
 def test_product_binding_has_no_fallback():
     # the binding refuses to import without the library rather than falling back
     src = open(os.path.join(ROOT, "rotated_quantized_kv_gb300", "tq.py")).read()

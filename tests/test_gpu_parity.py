@@ -289,3 +289,32 @@ def test_decode_attention_tiers(tq):
             kb, vb = W.tier_bits(tier)
             spec.append(("fp16", e - s) if kb == 16 else ("packed", e - s, [kb] * 8, [vb] * 8, None))
     assert _attention_case(tq, 1, 1, 8, 32, spec, seed=9) <= ATTN_TOL
+
+
+REQUANT_CASES = [
+    # B, H, T, src kbits, src vbits, dst kbits, dst vbits
+    (2, 4, 70, [4, 4, 4, 4], [4, 4, 4, 4], [3, 3, 3, 3], [2, 2, 2, 2]),   # warm -> cold tier
+    (1, 8, 45, [3] * 8, [2] * 8, [2] * 8, [1] * 8),                       # cold -> archive tier
+    (1, 8, 33, [8, 7, 6, 5, 4, 3, 2, 1], [1, 2, 3, 4, 5, 6, 7, 8], [1, 2, 3, 4, 5, 6, 7, 8],
+     [8, 7, 6, 5, 4, 3, 2, 1]),                                            # every width pair shape
+    (2, 2, 16, [5, 5], [5, 5], [5, 5], [5, 5]),                            # same widths
+]
+
+
+@pytest.mark.parametrize("B,H,T,skb,svb,dkb,dvb", REQUANT_CASES)
+def test_requantize_bit_exact(tq, B, H, T, skb, svb, dkb, dvb):
+    K, V = _kv(B, H, T, seed=300 + T)
+    sign = O.signs(128, 42)
+    scap = ((T + 20 + 15) // 16) * 16
+    osrc = _oracle_segment(B, H, scap, skb, svb, None, K, V, sign, None, 20)
+    gsrc = _upload(tq, osrc, tq.make_layout(B, H, 128, scap, skb, svb), 20 + T)
+    dcap = ((T + 7 + 15) // 16) * 16
+    odst = O.PackedSegment(B, H, 128, dcap, dkb, dvb)
+    O.requantize(osrc, 20, T, odst, 7)
+    gdst = tq.PackedSegment(tq.make_layout(B, H, 128, dcap, dkb, dvb))
+    tq.tq_requantize(gsrc, 20, T, gdst, 7)
+    torch.cuda.synchronize()
+    assert np.array_equal(gdst.kcodes.cpu().numpy()[:odst.kcodes.size], odst.kcodes)
+    assert np.array_equal(gdst.vcodes.cpu().numpy()[:odst.vcodes.size], odst.vcodes)
+    assert np.array_equal(gdst.kscale.cpu().numpy()[:odst.kscale.size].view(np.uint32), odst.kscale.view(np.uint32))
+    assert np.array_equal(gdst.vscale.cpu().numpy()[:odst.vscale.size].view(np.uint32), odst.vscale.view(np.uint32))
