@@ -59,7 +59,7 @@ class _Segment(ctypes.Structure):
         ("kind", _I), ("n_tokens", _I), ("capacity", _I),
         ("kbits", _P), ("vbits", _P), ("qjl", _P),
         ("kcodes", _P), ("vcodes", _P), ("kscale", _P), ("vscale", _P),
-        ("qjl_signs", _P), ("qjl_norm", _P), ("k16", _P), ("v16", _P),
+        ("qjl_signs", _P), ("qjl_norm", _P), ("k16", _P), ("v16", _P), ("value_law", _I),
     ]
 
 
@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
     L.tqo_rotate_f64.argtypes = [_I, _P, _P, _P]
     L.tqo_lloyd_max.argtypes = [_I, _P, _P, _I]
     L.tqo_lloyd_max.restype = _I
+    L.tqo_lloyd_max_sphere.argtypes = [_I, _I, _P, _P, _I]
+    L.tqo_lloyd_max_sphere.restype = _I
     L.tqo_quant_key.argtypes = [_I, _I, _P, _P, _P]
     L.tqo_key_level.argtypes = [_I, _I]
     L.tqo_key_level.restype = ctypes.c_double
@@ -162,21 +164,43 @@ def lloyd_max(bits: int, max_iter: int = 1_000_000):
     return c, t[: n - 1], it
 
 
+@functools.lru_cache(maxsize=None)
+def lloyd_max_sphere(bits: int, d: int = 128, max_iter: int = 1_000_000):
+    """binary64 (centroids, thresholds, sweeps) of the Lloyd-Max quantizer for
+    sqrt(d) times a coordinate of a uniform unit d-vector (the sphere-coordinate
+    value codebook)."""
+    n = 1 << bits
+    c = np.zeros(n)
+    t = np.zeros(max(n - 1, 1))
+    it = lib().tqo_lloyd_max_sphere(bits, d, _ptr(c), _ptr(t), max_iter)
+    assert it > 0
+    return c, t[: n - 1], it
+
+
 def codebook_f32(bits: int):
     """The binary32 centroids and thresholds the format stores."""
     c, t, _ = lloyd_max(bits)
     return c.astype(np.float32), t.astype(np.float32)
 
 
+def codebook_sphere_f32(bits: int, d: int = 128):
+    """The binary32 centroids and thresholds of the sphere-coordinate codebook."""
+    c, t, _ = lloyd_max_sphere(bits, d)
+    return c.astype(np.float32), t.astype(np.float32)
+
+
 @functools.lru_cache(maxsize=None)
 def _cent_thr_tables():
-    """binary32 centroid and threshold tables of widths 1..8 and C pointer
-    arrays to them (cached: the arrays must outlive every call that uses the
-    pointers)."""
-    cents = [np.zeros(1, np.float32)] + [codebook_f32(b)[0] for b in range(1, 9)]
-    thrs = [np.zeros(1, np.float32)] + [codebook_f32(b)[1] for b in range(1, 9)]
-    cp = (ctypes.c_void_p * 9)(*[c.ctypes.data for c in cents])
-    tp = (ctypes.c_void_p * 9)(*[t.ctypes.data for t in thrs])
+    """binary32 centroid and threshold tables of widths 1..8 for both value
+    codebook laws (index law * 9 + bits; law 0 Gaussian, 1 sphere coordinate
+    for d = 128) and C pointer arrays to them (cached: the arrays must outlive
+    every call that uses the pointers)."""
+    cents = ([np.zeros(1, np.float32)] + [codebook_f32(b)[0] for b in range(1, 9)] +
+             [np.zeros(1, np.float32)] + [codebook_sphere_f32(b)[0] for b in range(1, 9)])
+    thrs = ([np.zeros(1, np.float32)] + [codebook_f32(b)[1] for b in range(1, 9)] +
+            [np.zeros(1, np.float32)] + [codebook_sphere_f32(b)[1] for b in range(1, 9)])
+    cp = (ctypes.c_void_p * 18)(*[c.ctypes.data for c in cents])
+    tp = (ctypes.c_void_p * 18)(*[t.ctypes.data for t in thrs])
     return cents, thrs, cp, tp
 
 
@@ -266,8 +290,10 @@ class PackedSegment:
 
     kind = 0
 
-    def __init__(self, B, H, d, capacity, kbits, vbits, qjl=None, jl=128, n_tokens=0):
+    def __init__(self, B, H, d, capacity, kbits, vbits, qjl=None, jl=128, n_tokens=0, law=0):
         self.B, self.H, self.d, self.capacity, self.jl = B, H, d, capacity, jl
+        self.law = law  # value codebook: 0 Gaussian, 1 sphere coordinate (d = 128)
+        assert law in (0, 1) and (law == 0 or d == 128)
         self.kbits = _c(kbits, np.uint8)
         self.vbits = _c(vbits, np.uint8)
         self.qjl = _c(np.zeros(H) if qjl is None else qjl, np.uint8)
@@ -299,6 +325,7 @@ class PackedSegment:
         s.kscale, s.vscale = _ptr(self.kscale), _ptr(self.vscale)
         s.qjl_signs, s.qjl_norm = _ptr(self.qjl_signs), _ptr(self.qjl_norm)
         s.k16 = s.v16 = None
+        s.value_law = self.law
         return s
 
 

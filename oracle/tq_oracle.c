@@ -184,6 +184,112 @@ int tqo_lloyd_max(int bits, double *centroid, double *threshold, int max_iter) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* Sphere-coordinate Lloyd-Max codebook ("TurboMOQ", "Head-to-Head Comparison":  */
+/* a Beta-CDF codebook beside the Lloyd-Max one; "Project Structure": Beta-    */
+/* distribution codebooks).  Reading: after a random rotation a coordinate of   */
+/* a d-vector, divided by the vector's RMS, is sqrt(d) times a coordinate of a  */
+/* uniform unit vector, whose density is proportional to (1 - u^2/d)^((d-3)/2) */
+/* on |u| < sqrt(d) (a scaled symmetric Beta((d-1)/2, (d-1)/2) law).  Same     */
+/* Lloyd iteration as the Gaussian codebook, with this law.                    */
+/* ------------------------------------------------------------------------ */
+
+/* Gauss-Legendre nodes and weights on [-1, 1] (n points), by Newton's method
+ * on the Legendre recurrence. */
+static void gauss_legendre(int n, double *x, double *w) {
+    for (int i = 0; i < (n + 1) / 2; i++) {
+        double z = cos(TQO_PI * (i + 0.75) / (n + 0.5)), dp = 1.0;
+        for (int it = 0; it < 100; it++) {
+            double p0 = 1.0, p1 = 0.0;
+            for (int j = 1; j <= n; j++) {
+                const double p2 = p1;
+                p1 = p0;
+                p0 = ((2.0 * j - 1.0) * z * p1 - (j - 1.0) * p2) / j;
+            }
+            dp = n * (z * p0 - p1) / (z * z - 1.0);
+            const double dz = p0 / dp;
+            z -= dz;
+            if (fabs(dz) < 1e-16) break;
+        }
+        x[i] = -z;
+        x[n - 1 - i] = z;
+        w[i] = w[n - 1 - i] = 2.0 / ((1.0 - z * z) * dp * dp);
+    }
+}
+
+/* integral of (1 - s^2)^a over [s0, s1] within [0, 1]: composite 20-point
+ * Gauss-Legendre on `panels` equal panels. */
+static double sphere_mass(double a, double s0, double s1, int panels) {
+    static double gx[20], gw[20];
+    static int ready = 0;
+    if (!ready) {
+        gauss_legendre(20, gx, gw);
+        ready = 1;
+    }
+    double sum = 0.0;
+    const double h = (s1 - s0) / panels;
+    for (int p = 0; p < panels; p++) {
+        const double lo = s0 + p * h, mid = lo + 0.5 * h;
+        for (int i = 0; i < 20; i++) {
+            const double s = mid + 0.5 * h * gx[i];
+            sum += gw[i] * exp(a * log1p(-s * s));
+        }
+    }
+    return 0.5 * h * sum;
+}
+
+int tqo_lloyd_max_sphere(int bits, int d, double *centroid, double *threshold, int max_iter) {
+    if (bits < 1 || bits > 8 || d < 4) return -1;
+    const int n = 1 << bits, half = n / 2;
+    const double a = 0.5 * (d - 3), rd = sqrt((double)d);
+    /* upper tail P(U > x) up to the normalisation, as a mass in s = u / sqrt(d) */
+    const double total = sphere_mass(a, 0.0, 1.0, 256);  /* half the full mass */
+    double c[256], t[257];
+    for (int k = half; k < n; k++) {
+        /* initial centroid: the quantile (k + 1/2)/n, by bisection on the tail */
+        const double p = 1.0 - (k + 0.5) / n;  /* upper tail probability, < 1/2 */
+        double lo = 0.0, hi = 1.0;
+        for (int it = 0; it < 80; it++) {
+            const double mid = 0.5 * (lo + hi);
+            if (sphere_mass(a, mid, 1.0, 32) / (2.0 * total) > p) lo = mid; else hi = mid;
+        }
+        c[k] = rd * 0.5 * (lo + hi);
+    }
+    int it;
+    for (it = 1; it <= max_iter; it++) {
+        t[half] = 0.0;
+        for (int k = half + 1; k < n; k++) t[k] = 0.5 * (c[k - 1] + c[k]);
+        double delta = 0.0;
+        for (int k = half; k < n; k++) {
+            /* centroid of [x0, x1]: int u f / int f with f = (1 - u^2/d)^a; the
+             * numerator is d/(2(a+1)) ((1 - x0^2/d)^(a+1) - (1 - x1^2/d)^(a+1)),
+             * written with expm1 for narrow cells */
+            const double x0 = t[k], x1 = k + 1 < n ? t[k + 1] : rd;
+            const double l0 = log1p(-x0 * x0 / d);
+            double num;
+            if (k + 1 < n) {
+                const double l1 = log1p(-x1 * x1 / d);
+                num = -exp((a + 1.0) * l0) * expm1((a + 1.0) * (l1 - l0));
+            } else {
+                num = exp((a + 1.0) * l0);
+            }
+            num *= d / (2.0 * (a + 1.0));
+            const int panels = k + 1 < n ? 2 : 64;
+            const double den = rd * sphere_mass(a, x0 / rd, x1 / rd, panels);
+            const double nc = num / den;
+            const double dd = fabs(nc - c[k]);
+            if (dd > delta) delta = dd;
+            c[k] = nc;
+        }
+        if (delta <= 1e-13) break;
+    }
+    for (int k = half; k < n; k++) c[n - 1 - k] = -c[k];
+    for (int k = 0; k < n; k++) centroid[k] = c[k];
+    for (int k = 0; k + 1 < n; k++) threshold[k] = 0.5 * (c[k] + c[k + 1]);
+    threshold[half - 1] = 0.0;
+    return it;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Scalar quantizers (binary32 order is part of the format).                  */
 /* ------------------------------------------------------------------------ */
 
@@ -336,6 +442,7 @@ typedef struct {
     uint8_t *qjl_signs;
     float *qjl_norm;
     uint16_t *k16, *v16;
+    int value_law; /* value codebook: 0 Gaussian, 1 sphere coordinate (tables [law * 9 + bits]) */
 } tqo_segment;
 
 static size_t off_codes(const uint8_t *bits, int H, int d, int cap, int b, int h, int t) {
@@ -356,7 +463,8 @@ static int qjl_rank(const uint8_t *qjl, int h) {
 
 /* Compress T tokens of K and V (fp16 bit patterns, element strides sb, sh, st,
  * unit stride along d) into token positions [t_begin, t_begin + T) of a packed
- * segment.  thr[b] points at the 2^b - 1 binary32 value thresholds for b bits.
+ * segment.  thr[law * 9 + b] points at the 2^b - 1 binary32 value thresholds for
+ * b bits of codebook law `law` (0 Gaussian, 1 sphere coordinate).
  * S is the QJL matrix (jl x d) or NULL when no head uses QJL. */
 void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t *V,
                   long long sb, long long sh, long long st, const int8_t *sign,
@@ -389,7 +497,7 @@ void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t 
                 for (int i = 0; i < d; i++) x[i] = (float)tqo_half_to_double(V[src + i]);
                 tqo_rotate_f32(d, sign, x, y);
                 float sg;
-                tqo_quant_value(d, vb, y, thr[vb], code, &sg);
+                tqo_quant_value(d, vb, y, thr[seg->value_law * 9 + vb], code, &sg);
                 tqo_pack(d, vb, code, seg->vcodes + off_codes(seg->vbits, H, d, seg->capacity, b, h, pos));
                 seg->vscale[sidx] = sg;
             }
@@ -397,7 +505,7 @@ void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t 
 
 /* Dequantize token positions [t0, t0 + n) of one (b, h) of a packed segment into
  * the rotated space with the binary32 products the format defines:
- * keys m * level(code), values sigma * centroid[code] (cent[b] are binary32
+ * keys m * level(code), values sigma * centroid[code] (cent[law * 9 + b] are binary32
  * centroids).  Outputs are [n][d] floats. */
 void tqo_dequant(int H, int d, const tqo_segment *seg, int b, int h, int t0, int n,
                  const float *const *cent, float *khat, float *vhat) {
@@ -409,7 +517,8 @@ void tqo_dequant(int H, int d, const tqo_segment *seg, int b, int h, int t0, int
         tqo_unpack(d, kb, seg->kcodes + off_codes(seg->kbits, H, d, seg->capacity, b, h, pos), code);
         for (int i = 0; i < d; i++) khat[(size_t)t * d + i] = seg->kscale[sidx] * (float)tqo_key_level(kb, code[i]);
         tqo_unpack(d, vb, seg->vcodes + off_codes(seg->vbits, H, d, seg->capacity, b, h, pos), code);
-        for (int i = 0; i < d; i++) vhat[(size_t)t * d + i] = seg->vscale[sidx] * cent[vb][code[i]];
+        for (int i = 0; i < d; i++)
+            vhat[(size_t)t * d + i] = seg->vscale[sidx] * cent[seg->value_law * 9 + vb][code[i]];
     }
 }
 
@@ -436,7 +545,7 @@ void tqo_requantize(int B, int H, int d, const tqo_segment *src, int src_t0, int
                 tqo_quant_key(d, kb, kh, code, &m);
                 tqo_pack(d, kb, code, dst->kcodes + off_codes(dst->kbits, H, d, dst->capacity, b, h, pos));
                 dst->kscale[sidx] = m;
-                tqo_quant_value(d, vb, vh, thr[vb], code, &sg);
+                tqo_quant_value(d, vb, vh, thr[dst->value_law * 9 + vb], code, &sg);
                 tqo_pack(d, vb, code, dst->vcodes + off_codes(dst->vbits, H, d, dst->capacity, b, h, pos));
                 dst->vscale[sidx] = sg;
             }
@@ -494,7 +603,8 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
                         }
                         tqo_rotate_f64(d, sign, yk, kh);
                         tqo_unpack(d, vb, sg->vcodes + off_codes(sg->vbits, H, d, sg->capacity, b, h, t), code);
-                        for (int i = 0; i < d; i++) yv[i] = (double)sg->vscale[sidx] * (double)cent[vb][code[i]];
+                        for (int i = 0; i < d; i++)
+                            yv[i] = (double)sg->vscale[sidx] * (double)cent[sg->value_law * 9 + vb][code[i]];
                         tqo_rotate_f64(d, sign, yv, v);
                     }
                     double dot = 0.0;
