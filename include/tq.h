@@ -89,6 +89,13 @@ tq_status tq_make_rotation(int head_dim, uint64_t seed, tq_rotation *rot);
  * takes about a second).  TQ_ERR_ARG for bits outside 1..8 or NULL centroids. */
 tq_status tq_fit_codebook(int bits, float *centroids, float *thresholds);
 
+/* The sphere-coordinate codebook (TQ_VALUE_LAW_SPHERE) of `bits` for vectors
+ * of head_dim coordinates (4..1024): the same Lloyd iteration in binary64
+ * rounded to binary32, centroids (2^bits) and thresholds (2^bits - 1, may be
+ * NULL).  The first fit of a width takes up to ~20 s of host time at 8 bits
+ * (head_dim 128 fits are kept for the process). */
+tq_status tq_fit_codebook_sphere(int bits, int head_dim, float *centroids, float *thresholds);
+
 /* ------------------------------------------------------------------------ */
 /* QJL projection ("TurboMOQ", "QJL residual correction (sub-2-bit)":          */
 /* QJLConfig(head_dim, jl_dim); "turboquant-mlx", "RaBitQ vs QJL correction").  */
@@ -112,7 +119,19 @@ typedef struct {
     uint8_t kbits[TQ_MAX_HEADS]; /* per head, 1..8 */
     uint8_t vbits[TQ_MAX_HEADS]; /* per head, 1..8 */
     uint8_t qjl[TQ_MAX_HEADS];   /* per head, 0/1: 1-bit residual sketch of keys */
+    uint8_t value_law;           /* value codebook: TQ_VALUE_LAW_GAUSS or TQ_VALUE_LAW_SPHERE
+                                  * (the latter fitted for d = 128); anything else is
+                                  * TQ_ERR_ARG */
 } tq_segment_layout;
+
+/* Value codebook laws (the Lloyd-Max quantizer of u = y / RMS(y)):
+ *   TQ_VALUE_LAW_GAUSS   N(0,1) ("TurboMOQ", "Architecture": Lloyd-Max codebook)
+ *   TQ_VALUE_LAW_SPHERE  sqrt(d) times a coordinate of a uniform unit d-vector,
+ *                        density ~ (1 - u^2/d)^((d-3)/2): the exact law of a
+ *                        rotated coordinate ("TurboMOQ", "Head-to-Head
+ *                        Comparison": Beta-CDF codebook). */
+#define TQ_VALUE_LAW_GAUSS 0
+#define TQ_VALUE_LAW_SPHERE 1
 
 /* Byte layout (all offsets are multiples of 16 when the bases are aligned):
  *   record sizes rk(h) = d*kbits[h]/8, rv(h) = d*vbits[h]/8 bytes;

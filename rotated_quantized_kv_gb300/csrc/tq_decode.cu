@@ -179,7 +179,8 @@ PackedLauncher packed_launcher(int kb, int vb, bool qjl) {
 }  // namespace dec
 
 cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,
-                                  int n_classes, const float *S, const unsigned short (*value_half)[256],
+                                  int n_classes, const float *S, const unsigned short *const *value_half,
+                                  const float *value_c1,
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
     static bool configured = false;
     const size_t smem16 = static_cast<size_t>(dec::kStage16Bytes) + 16;
@@ -217,7 +218,8 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         if (c.n_ctas <= 0 || c.kb == 16) continue;
         const PackedLauncher fn = dec::packed_launcher(c.kb, c.vb, c.qjl != 0);
         if (!fn) return cudaErrorInvalidValue;
-        const cudaError_t e = fn(dims, ws, c.item_lo, c.item_hi, c.n_ctas, c.n_stages, value_half[c.vb], s, !first);
+        const cudaError_t e =
+            fn(dims, ws, c.item_lo, c.item_hi, c.n_ctas, c.n_stages, value_half[i], value_c1[i], s, !first);
         if (e != cudaSuccess) return e;
         first = false;
     }

@@ -420,7 +420,8 @@ struct VDec<4, TS> {  // nibbles; selector = byte k of both tokens: codes (2mt, 
 
 // ------------------------------------------------------------------- kernel
 struct ValueTable {
-    unsigned short half[256];  // fp16 codebook values of this class's value width
+    unsigned short half[256];  // fp16 codebook values of this class's value width and law
+    float c1;                  // binary32 centroid 1 of a 1-bit codebook (= -centroid 0)
 };
 
 constexpr int kPT = kPackedStageTokens;  // 32 tokens per warp: two 16-token tiles
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
     constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
     const float qk_scale = dims.qk_scale;
-    const float c1 = dims.value_c1;
+    const float c1 = vt.c1;
     // byte offset of the thread's key window: codes [32c, 32c+32) of token row g
     const int koff = g * G::RK + 4 * KB * c;
 
@@ -769,7 +770,8 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
 
 template <int KB, int VB, bool QJL>
 cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int item_lo, int item_hi, int n_ctas,
-                          long long n_stages, const unsigned short *value_half, cudaStream_t s, bool pdl) {
+                          long long n_stages, const unsigned short *value_half, float value_c1, cudaStream_t s,
+                          bool pdl) {
     using G = PackedGeom<KB, VB, QJL>;
     static bool configured = false;
     if (!configured) {
@@ -782,6 +784,7 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int
     }
     ValueTable vt;
     for (int i = 0; i < 256; i++) vt.half[i] = i < (1 << VB) ? value_half[i] : 0;
+    vt.c1 = value_c1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_ctas);
     cfg.blockDim = dim3(kThreads);

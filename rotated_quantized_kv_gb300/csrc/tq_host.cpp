@@ -114,16 +114,121 @@ const FittedCodebook &fit(int bits) {
     return cb;
 }
 
-void fill_thresholds(float *flat, const uint8_t *bits, int H) {
+// ------------------------------------------- sphere-coordinate codebook
+// The law of sqrt(d) times a coordinate of a uniform unit d-vector (what a
+// rotated coordinate divided by its vector's RMS follows): density
+// proportional to (1 - u^2/d)^((d-3)/2) on |u| < sqrt(d).  Lloyd's iteration
+// as for the Gaussian law: first moments of a cell in closed form, cell masses
+// by composite Gauss-Legendre quadrature in s = u / sqrt(d).
+struct GaussRule {
+    double x[24], w[24];
+    GaussRule() {
+        const int n = 24;
+        for (int i = 0; i < n / 2; ++i) {
+            double z = std::cos(3.14159265358979323846 * (i + 0.75) / (n + 0.5)), d = 1.0;
+            for (int it = 0; it < 100; ++it) {
+                double p = 1.0, q = 0.0;
+                for (int j = 1; j <= n; ++j) {
+                    const double r = q;
+                    q = p;
+                    p = ((2 * j - 1) * z * q - (j - 1) * r) / j;
+                }
+                d = n * (z * p - q) / (z * z - 1.0);
+                const double step = p / d;
+                z -= step;
+                if (std::fabs(step) < 1e-16) break;
+            }
+            x[i] = z;
+            x[n - 1 - i] = -z;
+            w[i] = w[n - 1 - i] = 2.0 / ((1.0 - z * z) * d * d);
+        }
+    }
+};
+
+// mass of (1 - s^2)^e over [s0, s1] (0 <= s0 <= s1 <= 1) on `panels` panels
+double sphere_cell_mass(double e, double s0, double s1, int panels) {
+    static const GaussRule rule;
+    const double h = (s1 - s0) / panels;
+    double acc = 0.0;
+    for (int p = 0; p < panels; ++p) {
+        const double c = s0 + (p + 0.5) * h;
+        for (int i = 0; i < 24; ++i) {
+            const double s = c + 0.5 * h * rule.x[i];
+            acc += rule.w[i] * std::exp(e * std::log1p(-s * s));
+        }
+    }
+    return 0.5 * h * acc;
+}
+
+void fit_sphere(int bits, int d, FittedCodebook &cb) {
+    const int n = 1 << bits, half = n / 2;
+    const double e = 0.5 * (d - 3), sd = std::sqrt(static_cast<double>(d));
+    const double half_mass = sphere_cell_mass(e, 0.0, 1.0, 256);
+    std::vector<double> up(half);
+    for (int k = 0; k < half; ++k) {  // start at the (k + 1/2)/n quantiles
+        const double p = 1.0 - (half + k + 0.5) / n;
+        double lo = 0.0, hi = 1.0;
+        for (int it = 0; it < 80; ++it) {
+            const double mid = 0.5 * (lo + hi);
+            (sphere_cell_mass(e, mid, 1.0, 32) / (2.0 * half_mass) > p ? lo : hi) = mid;
+        }
+        up[k] = sd * 0.5 * (lo + hi);
+    }
+    std::vector<double> edge(half + 1);
+    for (int sweep = 0; sweep < 1000000; ++sweep) {
+        edge[0] = 0.0;
+        for (int k = 1; k < half; ++k) edge[k] = 0.5 * (up[k - 1] + up[k]);
+        double move = 0.0;
+        for (int k = 0; k < half; ++k) {
+            const double a = edge[k], la = std::log1p(-a * a / d);
+            double num, b;
+            if (k + 1 < half) {
+                b = edge[k + 1];
+                num = -std::exp((e + 1.0) * la) * std::expm1((e + 1.0) * (std::log1p(-b * b / d) - la));
+            } else {
+                b = sd;
+                num = std::exp((e + 1.0) * la);
+            }
+            num *= 0.5 * d / (e + 1.0);
+            const double den = sd * sphere_cell_mass(e, a / sd, b / sd, k + 1 < half ? 2 : 64);
+            const double v = num / den;
+            move = std::fmax(move, std::fabs(v - up[k]));
+            up[k] = v;
+        }
+        if (move <= 1e-13) break;
+    }
+    cb.level.assign(n, 0.0);
+    for (int k = 0; k < half; ++k) {
+        cb.level[half + k] = up[k];
+        cb.level[half - 1 - k] = -up[k];
+    }
+    cb.bound.assign(n - 1, 0.0);
+    for (int k = 0; k + 1 < n; ++k) cb.bound[k] = 0.5 * (cb.level[k] + cb.level[k + 1]);
+    cb.bound[half - 1] = 0.0;
+    cb.ready = true;
+}
+
+FittedCodebook g_cb_sphere[9];  // d = kD
+
+// The value codebook of a law: TQ_VALUE_LAW_GAUSS or TQ_VALUE_LAW_SPHERE (d = 128).
+const FittedCodebook &fit(int bits, int law) {
+    if (law == TQ_VALUE_LAW_GAUSS) return fit(bits);
+    std::lock_guard<std::mutex> lock(g_cb_mutex);
+    FittedCodebook &cb = g_cb_sphere[bits];
+    if (!cb.ready) fit_sphere(bits, kD, cb);
+    return cb;
+}
+
+void fill_thresholds(float *flat, const uint8_t *bits, int H, int law) {
     for (int h = 0; h < H; ++h) {
-        const FittedCodebook &cb = fit(bits[h]);
+        const FittedCodebook &cb = fit(bits[h], law);
         for (int k = 0; k + 1 < (1 << bits[h]); ++k) flat[cb_off(bits[h]) + k] = static_cast<float>(cb.bound[k]);
     }
 }
 
-void fill_centroids(float *flat, const uint8_t *bits, int H) {
+void fill_centroids(float *flat, const uint8_t *bits, int H, int law) {
     for (int h = 0; h < H; ++h) {
-        const FittedCodebook &cb = fit(bits[h]);
+        const FittedCodebook &cb = fit(bits[h], law);
         for (int k = 0; k < (1 << bits[h]); ++k) flat[cb_off(bits[h]) + k] = static_cast<float>(cb.level[k]);
     }
 }
@@ -141,6 +246,7 @@ tq_status check_layout(const tq_segment_layout *L, bool need_bits) {
             any_qjl |= L->qjl[h] != 0;
         }
         if (any_qjl && (L->jl_dim < 32 || L->jl_dim > 1024 || L->jl_dim % 32)) return TQ_ERR_ARG;
+        if (L->value_law != TQ_VALUE_LAW_GAUSS && L->value_law != TQ_VALUE_LAW_SPHERE) return TQ_ERR_ARG;
     }
     return TQ_OK;
 }
@@ -204,7 +310,12 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // [i S / G, (i+1) S / G)) that holds stage s; same arithmetic as the kernels.
 long long dec_cta_of_stage(long long s, long long S, long long G) { return ((s + 1) * G + S - 1) / S - 1; }
 
-int class_key(const WorkItem &w) { return w.kind == TQ_SEG_FP16 ? 1 << 20 : (w.kb * 16 + w.vb) * 2 + w.qjl; }
+// Decode class of an item: one kernel instantiation and one value table each
+// (fp16 items form one class after all packed ones).
+constexpr int kFp16ClassKey = 1100;
+int class_key(const WorkItem &w) {
+    return w.kind == TQ_SEG_FP16 ? kFp16ClassKey : ((w.kb * 16 + w.vb) * 2 + w.qjl) * 2 + w.vlaw;
+}
 
 // Validate the views and lay out the work: one item per (layer, segment, KV
 // head) with tokens, split into chunks of `chunk` tokens (a multiple of 64)
@@ -287,6 +398,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                     w.kb = L.kbits[h];
                     w.vb = L.vbits[h];
                     w.qjl = L.qjl[h] ? 1 : 0;
+                    w.vlaw = L.value_law;
                     if (w.qjl) {
                         w.qs = static_cast<const uint8_t *>(sg.packed.qjl_signs) + o.qrank[h] * cap * (kJl / 8);
                         w.qn = sg.packed.qjl_norm + o.qrank[h] * cap;
@@ -312,11 +424,11 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     {  // stable bucket sort by class (at most 2 * 8 * 8 packed classes, fp16 last)
         std::vector<int> key(P.items.size());
         int nkeys = 0;
-        int slot_of[2 * 16 * 16 + 2];
+        int slot_of[kFp16ClassKey + 1];
         std::fill(std::begin(slot_of), std::end(slot_of), -1);
-        int keys[2 * 16 * 16 + 2];
+        int keys[kFp16ClassKey + 1];
         for (size_t i = 0; i < P.items.size(); ++i) {
-            const int k = P.items[i].kind == TQ_SEG_FP16 ? 2 * 16 * 16 + 1 : class_key(P.items[i]);
+            const int k = class_key(P.items[i]);
             if (slot_of[k] < 0) {
                 slot_of[k] = 0;
                 keys[nkeys++] = k;
@@ -339,7 +451,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     for (size_t i = 0; i < P.items.size(); ++i) {
         WorkItem &w = P.items[i];
         if (i == 0 || class_key(w) != class_key(P.items[i - 1])) {
-            P.classes.push_back(ClassLaunch{w.kb, w.vb, w.qjl, static_cast<int>(i), static_cast<int>(i), 0, 0});
+            P.classes.push_back(ClassLaunch{w.kb, w.vb, w.qjl, w.vlaw, static_cast<int>(i), static_cast<int>(i), 0, 0});
             cta = 0;
             stages = 0;
         }
@@ -400,7 +512,6 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.any_qjl = P.any_qjl ? 1 : 0;
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-    D.value_c1 = 0.f;
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
     // offset 0: the error flag (kept in its own 256 bytes so that it has a
     // fixed place), then the work items
@@ -472,6 +583,18 @@ tq_status tq_fit_codebook(int bits, float *centroids, float *thresholds) {
     for (int k = 0; k < (1 << bits); ++k) centroids[k] = static_cast<float>(cb.level[k]);
     if (thresholds)
         for (int k = 0; k + 1 < (1 << bits); ++k) thresholds[k] = static_cast<float>(cb.bound[k]);
+    return TQ_OK;
+}
+
+tq_status tq_fit_codebook_sphere(int bits, int head_dim, float *centroids, float *thresholds) {
+    if (bits < 1 || bits > 8 || !centroids || head_dim < 4 || head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
+    FittedCodebook local;
+    const FittedCodebook *cb = &local;
+    if (head_dim == kD) cb = &fit(bits, TQ_VALUE_LAW_SPHERE);
+    else fit_sphere(bits, head_dim, local);
+    for (int k = 0; k < (1 << bits); ++k) centroids[k] = static_cast<float>(cb->level[k]);
+    if (thresholds)
+        for (int k = 0; k + 1 < (1 << bits); ++k) thresholds[k] = static_cast<float>(cb->bound[k]);
     return TQ_OK;
 }
 
@@ -565,7 +688,7 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
     }
     std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
     p.inv_sqrt_d = inv_sqrt_f32(kD);
-    fill_thresholds(p.thr, layout->vbits, p.H);
+    fill_thresholds(p.thr, layout->vbits, p.H, layout->value_law);
     const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -609,7 +732,7 @@ tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *b
     p.v_rot = v_rot;
     p.k_orig = k_orig;
     p.v_orig = v_orig;
-    fill_centroids(p.centroid, layout->vbits, p.H);
+    fill_centroids(p.centroid, layout->vbits, p.H, layout->value_law);
     const cudaError_t e = launch_dequant(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -665,7 +788,7 @@ tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_
         p.skbits[h] = src->kbits[h];
         p.svbits[h] = src->vbits[h];
     }
-    fill_thresholds(q.thr, dst->vbits, q.H);
+    fill_thresholds(q.thr, dst->vbits, q.H, dst->value_law);
     p.skcodes = static_cast<const uint8_t *>(src_bufs->kcodes);
     p.svcodes = static_cast<const uint8_t *>(src_bufs->vcodes);
     p.skscale = src_bufs->kscale;
@@ -674,7 +797,7 @@ tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_
     p.svblock = so.vblock;
     p.scapacity = src->capacity;
     p.s_t0 = src_t_begin;
-    fill_centroids(p.centroid, src->vbits, src->n_heads);
+    fill_centroids(p.centroid, src->vbits, src->n_heads, src->value_law);
     const cudaError_t e = launch_requantize(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -796,22 +919,27 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     W.part = reinterpret_cast<float *>(ws + P.off_part);
     W.q = static_cast<const uint16_t *>(q);
     W.out = out;
-    // fp16 codebook values of every value width in use
-    static unsigned short value_half[9][256];
-    static bool value_ready[9] = {};
+    // fp16 codebook values (and the 1-bit centroid) of every decode class;
+    // 1-bit values decode as c1 * (2 code - 1) since the codebooks are symmetric
+    static unsigned short value_half[2][9][256];
+    static bool value_ready[2][9] = {};
+    std::vector<const unsigned short *> class_half(P.classes.size(), nullptr);
+    std::vector<float> class_c1(P.classes.size(), 0.f);
     {
         std::lock_guard<std::mutex> lock(g_cb_mutex_tables());
-        for (const ClassLaunch &c : P.classes) {
-            if (c.kb == 16 || value_ready[c.vb]) continue;
-            const FittedCodebook &cb = fit(c.vb);
-            for (int k = 0; k < 256; ++k)
-                value_half[c.vb][k] =
-                    k < (1 << c.vb) ? __half_as_ushort(__float2half_rn(static_cast<float>(cb.level[k]))) : 0;
-            value_ready[c.vb] = true;
+        for (size_t i = 0; i < P.classes.size(); ++i) {
+            const ClassLaunch &c = P.classes[i];
+            if (c.kb == 16) continue;
+            const FittedCodebook &cb = fit(c.vb, c.law);
+            if (!value_ready[c.law][c.vb]) {
+                for (int k = 0; k < 256; ++k)
+                    value_half[c.law][c.vb][k] =
+                        k < (1 << c.vb) ? __half_as_ushort(__float2half_rn(static_cast<float>(cb.level[k]))) : 0;
+                value_ready[c.law][c.vb] = true;
+            }
+            class_half[i] = value_half[c.law][c.vb];
+            class_c1[i] = c.vb == 1 ? static_cast<float>(cb.level[1]) : 0.f;
         }
-        // 1-bit values decode as c1 * (2 code - 1) (the codebook is symmetric)
-        for (const ClassLaunch &c : P.classes)
-            if (c.kb != 16 && c.vb == 1) P.dims.value_c1 = static_cast<float>(fit(1).level[1]);
     }
     // (layer, KV head) groups without any token are written by no CTA: their
     // output is zero
@@ -823,8 +951,8 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (P.items.empty()) return TQ_OK;
-    e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S, value_half, s,
-                              g_ev_start, g_ev_stop);
+    e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S,
+                              class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 

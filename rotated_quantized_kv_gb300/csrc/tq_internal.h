@@ -95,7 +95,7 @@ struct alignas(16) WorkItem {
     int n_tokens;
     int chunk, n_chunks;      // fp16: tokens per CTA (multiple of 64) and CTAs per batch element
     int cta_begin;            // fp16: first CTA within its launch
-    int kb, vb, qjl, pad;
+    int kb, vb, qjl, vlaw;  // vlaw: value codebook law (host side only)
 };
 
 struct LayerPlan {
@@ -110,7 +110,6 @@ struct DecodeDims {
     int any_qjl;         // the prep kernel ran (QJL layers read S R q from it)
     float qk_scale;      // log2(e) / sqrt(d)
     float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
-    float value_c1;      // binary32 centroid 1 of the 1-bit value codebook (= -centroid 0)
 };
 
 // Workspace: [WorkItem x n][LayerPlan x L][group tables][counters][q prep]
@@ -145,6 +144,7 @@ constexpr int kStages = 4;
 // them, each taking an equal contiguous range); fp16 runs one CTA per chunk.
 struct ClassLaunch {
     int kb, vb, qjl;   // kb == 16: fp16 segments
+    int law;           // value codebook law
     int item_lo, item_hi, n_ctas;
     long long n_stages;
 };
@@ -158,6 +158,7 @@ __host__ __device__ constexpr int packed_ctas_per_sm(bool qjl) { return qjl ? kP
 
 typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, int item_lo, int item_hi,
                                       int n_ctas, long long n_stages, const unsigned short *value_half,
+                                      float value_c1,
                                       cudaStream_t s, bool pdl);
 PackedLauncher packed_launcher_kb1(int vb, bool qjl);
 PackedLauncher packed_launcher_kb2(int vb, bool qjl);
@@ -176,7 +177,8 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams &p, cudaStream_t s);
 cudaError_t launch_requantize(const RequantParams &p, cudaStream_t s);
 cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,
-                                  int n_classes, const float *S, const unsigned short (*value_half)[256],
+                                  int n_classes, const float *S, const unsigned short *const *value_half,
+                                  const float *value_c1,
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace tqk

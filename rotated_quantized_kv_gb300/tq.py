@@ -34,6 +34,8 @@ TQ_MAX_SEGMENTS = 8
 TQ_MAX_HEAD_DIM = 1024
 TQ_SEG_PACKED = 0
 TQ_SEG_FP16 = 1
+TQ_VALUE_LAW_GAUSS = 0
+TQ_VALUE_LAW_SPHERE = 1
 
 STATUS = {0: "TQ_OK", -1: "TQ_ERR_ARG", -2: "TQ_ERR_UNSUPPORTED", -3: "TQ_ERR_ALIGN",
           -4: "TQ_ERR_SIZE", -5: "TQ_ERR_CUDA"}
@@ -42,7 +44,7 @@ EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rot
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
             "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag",
-            "tq_requantize"]
+            "tq_requantize", "tq_fit_codebook_sphere"]
 
 
 class TQError(RuntimeError):
@@ -63,7 +65,7 @@ class tq_segment_layout(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("capacity", ctypes.c_int), ("jl_dim", ctypes.c_int),
                 ("kbits", ctypes.c_uint8 * TQ_MAX_HEADS), ("vbits", ctypes.c_uint8 * TQ_MAX_HEADS),
-                ("qjl", ctypes.c_uint8 * TQ_MAX_HEADS)]
+                ("qjl", ctypes.c_uint8 * TQ_MAX_HEADS), ("value_law", ctypes.c_uint8)]
 
 
 class tq_packed_sizes(ctypes.Structure):
@@ -94,6 +96,7 @@ _lib.tq_last_cuda_error.restype = _I
 _lib.tq_version.restype = _I
 _lib.tq_make_rotation.argtypes = [_I, ctypes.c_uint64, ctypes.POINTER(tq_rotation)]
 _lib.tq_fit_codebook.argtypes = [_I, _P, _P]
+_lib.tq_fit_codebook_sphere.argtypes = [_I, _I, _P, _P]
 _lib.tq_make_qjl.argtypes = [_I, _I, ctypes.c_uint64, _P]
 _lib.tq_packed_size.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_packed_sizes)]
 _lib.tq_compress.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_rotation), _P, _P, _P,
@@ -156,6 +159,14 @@ def tq_fit_codebook(bits: int):
     return c, t[: (1 << bits) - 1]
 
 
+def tq_fit_codebook_sphere(bits: int, head_dim: int = 128):
+    """(centroids, thresholds) of the sphere-coordinate law, float32 CPU tensors."""
+    c = torch.zeros(1 << bits, dtype=torch.float32)
+    t = torch.zeros(max((1 << bits) - 1, 1), dtype=torch.float32)
+    _check(_lib.tq_fit_codebook_sphere(bits, head_dim, c.data_ptr(), t.data_ptr()), "tq_fit_codebook_sphere")
+    return c, t[: (1 << bits) - 1]
+
+
 def tq_make_qjl(head_dim: int, jl_dim: int, seed: int) -> torch.Tensor:
     """QJL projection S (float32 CPU tensor [jl_dim][head_dim])."""
     S = torch.zeros(jl_dim, head_dim, dtype=torch.float32)
@@ -163,9 +174,10 @@ def tq_make_qjl(head_dim: int, jl_dim: int, seed: int) -> torch.Tensor:
     return S
 
 
-def make_layout(batch, n_heads, head_dim, capacity, kbits, vbits, qjl=None, jl_dim=128):
+def make_layout(batch, n_heads, head_dim, capacity, kbits, vbits, qjl=None, jl_dim=128, value_law=0):
     L = tq_segment_layout()
     L.batch, L.n_heads, L.head_dim, L.capacity, L.jl_dim = batch, n_heads, head_dim, capacity, jl_dim
+    L.value_law = value_law
     kb = [int(kbits)] * n_heads if isinstance(kbits, int) else [int(x) for x in kbits]
     vb = [int(vbits)] * n_heads if isinstance(vbits, int) else [int(x) for x in vbits]
     qj = [0] * n_heads if qjl is None else [int(bool(x)) for x in qjl]

@@ -49,6 +49,16 @@ def test_codebook_matches_oracle(tq, bits):
     assert np.array_equal(t.numpy(), ot)
 
 
+@pytest.mark.parametrize("bits", range(1, 8))
+def test_sphere_codebook_matches_oracle(tq, bits):
+    # the host fit and the oracle's are separate programs of the same iteration;
+    # the 8-bit fit (~15 s on each side) is covered by the GPU parity tests
+    c, t = tq.tq_fit_codebook_sphere(bits, 128)
+    oc, ot = O.codebook_sphere_f32(bits)
+    assert np.array_equal(c.numpy().view(np.uint32), np.asarray(oc, np.float32).view(np.uint32))
+    assert np.array_equal(t.numpy().view(np.uint32), np.asarray(ot, np.float32).view(np.uint32))
+
+
 def test_qjl_matrix_matches_oracle(tq):
     S = tq.tq_make_qjl(128, 128, 1042).numpy()
     assert np.array_equal(S, O.qjl_matrix(128, 128, 1042))
@@ -85,6 +95,11 @@ def test_host_side_argument_errors(tq):
     with pytest.raises(tq.TQError) as e:
         tq.tq_packed_size(bad)
     assert e.value.status == -1
+    with pytest.raises(tq.TQError) as e:  # value codebook law outside {0, 1}
+        tq.tq_packed_size(tq.make_layout(1, 8, 128, 64, 3, 3, value_law=2))
+    assert e.value.status == -1
+    with pytest.raises(tq.TQError):
+        tq.tq_fit_codebook_sphere(0, 128)
     L = tq.make_layout(1, 8, 128, 64, 3, 3)
     b = tq.tq_packed_bufs()
     rot = tq.tq_make_rotation(128, 42)

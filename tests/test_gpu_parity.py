@@ -33,8 +33,8 @@ def _kv(B, H, T, seed, law="outliers"):
     return W.kv_block(w, 0, B, T, seed)
 
 
-def _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin=0):
-    seg = O.PackedSegment(B, H, 128, cap, kb, vb, qjl, jl=128)
+def _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin=0, law=0):
+    seg = O.PackedSegment(B, H, 128, cap, kb, vb, qjl, jl=128, law=law)
     O.compress(seg, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S, t_begin=t_begin)
     return seg
 
@@ -83,22 +83,23 @@ def _qjl_window_ok(oseg, gseg_signs, K, sign, S, B, H, T, t_begin):
 
 
 COMPRESS_CASES = [
-    # B, H, T, t_begin, kbits, vbits, qjl
-    (2, 8, 200, 0, [1, 2, 3, 4, 5, 6, 7, 8], [8, 7, 6, 5, 4, 3, 2, 1], None),
-    (1, 8, 64, 16, [4] * 8, [4] * 8, None),
-    (3, 4, 77, 32, [1, 2, 2, 3], [1, 3, 2, 4], [1, 1, 0, 0]),
-    (1, 8, 130, 0, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], [0, 0, 1, 1, 0, 0, 0, 1]),
+    # B, H, T, t_begin, kbits, vbits, qjl, value codebook law
+    (2, 8, 200, 0, [1, 2, 3, 4, 5, 6, 7, 8], [8, 7, 6, 5, 4, 3, 2, 1], None, 0),
+    (1, 8, 64, 16, [4] * 8, [4] * 8, None, 0),
+    (3, 4, 77, 32, [1, 2, 2, 3], [1, 3, 2, 4], [1, 1, 0, 0], 0),
+    (1, 8, 130, 0, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], [0, 0, 1, 1, 0, 0, 0, 1], 0),
+    (2, 8, 150, 16, [4, 4, 3, 3, 2, 2, 1, 8], [1, 2, 3, 4, 5, 6, 7, 8], [0, 0, 0, 0, 1, 0, 0, 0], 1),
 ]
 
 
-@pytest.mark.parametrize("B,H,T,t_begin,kb,vb,qjl", COMPRESS_CASES)
-def test_compress_bit_exact(tq, B, H, T, t_begin, kb, vb, qjl):
+@pytest.mark.parametrize("B,H,T,t_begin,kb,vb,qjl,law", COMPRESS_CASES)
+def test_compress_bit_exact(tq, B, H, T, t_begin, kb, vb, qjl, law):
     K, V = _kv(B, H, T, seed=11 + T)
     cap = ((t_begin + T + 15) // 16) * 16
     sign = O.signs(128, 42)
     S = O.qjl_matrix(128, 128, 42 + 1000) if qjl else None
-    oseg = _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin)
-    layout = tq.make_layout(B, H, 128, cap, kb, vb, qjl)
+    oseg = _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin, law=law)
+    layout = tq.make_layout(B, H, 128, cap, kb, vb, qjl, value_law=law)
     g = tq.PackedSegment(layout)
     rot = tq.tq_make_rotation(128, 42)
     Sd = torch.from_numpy(S).cuda() if qjl else None
@@ -170,14 +171,15 @@ def test_compress_strided_input(tq):
     assert np.array_equal(g.vcodes.cpu().numpy(), oseg.vcodes)
 
 
-def test_dequantize(tq):
+@pytest.mark.parametrize("law", [0, 1])
+def test_dequantize(tq, law):
     B, H, T = 2, 8, 90
     kb = [1, 2, 3, 4, 5, 6, 7, 8]
     vb = [2, 3, 4, 5, 6, 7, 8, 1]
     K, V = _kv(B, H, T, seed=3)
     sign = O.signs(128, 42)
-    oseg = _oracle_segment(B, H, 96, kb, vb, None, K, V, sign, None)
-    layout = tq.make_layout(B, H, 128, 96, kb, vb)
+    oseg = _oracle_segment(B, H, 96, kb, vb, None, K, V, sign, None, law=law)
+    layout = tq.make_layout(B, H, 128, 96, kb, vb, value_law=law)
     g = _upload(tq, oseg, layout, T)
     rot = tq.tq_make_rotation(128, 42)
     kr, vr, ko, vo = tq.tq_dequantize(g, 5, T - 5, rot=rot, rotated=True, original=True)
@@ -200,7 +202,7 @@ def _max_rel(out, ref):
 
 
 def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
-    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl)."""
+    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl[, law])."""
     rng = np.random.default_rng(seed)
     S = O.qjl_matrix(128, 128, 42 + 1000) if qjl_any else None
     Sd = torch.from_numpy(S).cuda() if qjl_any else None
@@ -224,12 +226,13 @@ def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
                 g = tq.Fp16Segment(B, H, 128, cap, n_tokens=T, k=torch.from_numpy(kk).cuda(),
                                    v=torch.from_numpy(vv).cuda())
             else:
-                _, _, kb, vb, qj = sp
-                o = O.PackedSegment(B, H, 128, cap, kb, vb, qj, jl=128)
+                kb, vb, qj = sp[2:5]
+                law = sp[5] if len(sp) > 5 else 0
+                o = O.PackedSegment(B, H, 128, cap, kb, vb, qj, jl=128, law=law)
                 if T:
                     O.compress(o, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S)
                 o.n_tokens = T
-                g = _upload(tq, o, tq.make_layout(B, H, 128, cap, kb, vb, qj), T)
+                g = _upload(tq, o, tq.make_layout(B, H, 128, cap, kb, vb, qj, value_law=law), T)
             osegs.append(o)
             gsegs.append(g)
         keep.append(gsegs)
@@ -260,12 +263,16 @@ ATTN_CASES = [
     (1, 2, 4, 8, [("packed", 200, [1, 2, 3, 4], [1, 2, 3, 4], None), ("packed", 129, [5, 6, 7, 8], [8, 7, 6, 5], None)]),
     (1, 1, 8, 8, [("packed", 333, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], None)]),
     (2, 1, 4, 16, [("fp16", 64), ("packed", 190, [2, 1, 4, 3], [3, 4, 1, 2], [1, 1, 0, 0])]),
+    # both value codebook laws in one call: same widths, separate decode classes
+    (1, 2, 4, 8, [("packed", 260, [4, 3, 2, 8], [1, 2, 3, 4], None, 1),
+                  ("packed", 140, [4, 3, 2, 8], [1, 2, 3, 4], None, 0), ("fp16", 5)]),
+    (1, 1, 8, 32, [("packed", 500, [3] * 8, [1, 3, 5, 6, 7, 8, 2, 4], [1, 0, 0, 0, 0, 0, 0, 1], 1)]),
 ]
 
 
 @pytest.mark.parametrize("L,B,H,Hq,spec", ATTN_CASES)
 def test_decode_attention_matches_oracle(tq, L, B, H, Hq, spec):
-    qjl_any = any(s[0] == "packed" and s[4] for s in spec)
+    qjl_any = any(s[0] == "packed" and s[4] and any(s[4]) for s in spec)
     worst = _attention_case(tq, L, B, H, Hq, spec, seed=len(spec) * 7 + L, qjl_any=qjl_any)
     assert worst <= ATTN_TOL, worst
 
@@ -300,6 +307,13 @@ REQUANT_CASES = [
     (2, 2, 16, [5, 5], [5, 5], [5, 5], [5, 5]),                            # same widths
 ]
 
+REQUANT_LAW_CASES = [
+    # B, H, T, src kbits, src vbits, dst kbits, dst vbits, src law, dst law
+    (2, 4, 70, [4] * 4, [4] * 4, [3] * 4, [2] * 4, 1, 1),
+    (1, 4, 40, [4, 3, 2, 8], [4, 6, 1, 8], [2, 2, 1, 5], [3, 1, 1, 7], 0, 1),
+    (1, 4, 40, [4, 3, 2, 8], [4, 6, 1, 8], [2, 2, 1, 5], [3, 1, 1, 7], 1, 0),
+]
+
 
 @pytest.mark.parametrize("B,H,T,skb,svb,dkb,dvb", REQUANT_CASES)
 def test_requantize_bit_exact(tq, B, H, T, skb, svb, dkb, dvb):
@@ -318,3 +332,22 @@ def test_requantize_bit_exact(tq, B, H, T, skb, svb, dkb, dvb):
     assert np.array_equal(gdst.vcodes.cpu().numpy()[:odst.vcodes.size], odst.vcodes)
     assert np.array_equal(gdst.kscale.cpu().numpy()[:odst.kscale.size].view(np.uint32), odst.kscale.view(np.uint32))
     assert np.array_equal(gdst.vscale.cpu().numpy()[:odst.vscale.size].view(np.uint32), odst.vscale.view(np.uint32))
+
+
+@pytest.mark.parametrize("B,H,T,skb,svb,dkb,dvb,slaw,dlaw", REQUANT_LAW_CASES)
+def test_requantize_across_codebook_laws(tq, B, H, T, skb, svb, dkb, dvb, slaw, dlaw):
+    K, V = _kv(B, H, T, seed=500 + T + slaw)
+    sign = O.signs(128, 42)
+    scap = ((T + 3 + 15) // 16) * 16
+    osrc = _oracle_segment(B, H, scap, skb, svb, None, K, V, sign, None, 3, law=slaw)
+    gsrc = _upload(tq, osrc, tq.make_layout(B, H, 128, scap, skb, svb, value_law=slaw), 3 + T)
+    dcap = ((T + 15) // 16) * 16
+    odst = O.PackedSegment(B, H, 128, dcap, dkb, dvb, law=dlaw)
+    O.requantize(osrc, 3, T, odst, 0)
+    gdst = tq.PackedSegment(tq.make_layout(B, H, 128, dcap, dkb, dvb, value_law=dlaw))
+    tq.tq_requantize(gsrc, 3, T, gdst, 0)
+    torch.cuda.synchronize()
+    for got, ref in ((gdst.kcodes, odst.kcodes), (gdst.vcodes, odst.vcodes)):
+        assert np.array_equal(got.cpu().numpy()[:ref.size], ref)
+    for got, ref in ((gdst.kscale, odst.kscale), (gdst.vscale, odst.vscale)):
+        assert np.array_equal(got.cpu().numpy()[:ref.size].view(np.uint32), ref.view(np.uint32))
