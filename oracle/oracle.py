@@ -89,7 +89,7 @@ def lib() -> ctypes.CDLL:
                                ctypes.POINTER(_Segment), _I]
     L.tqo_dequant.argtypes = [_I, _I, ctypes.POINTER(_Segment), _I, _I, _I, _I, _P, _P, _P]
     L.tqo_decode_attention.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_Segment), _P, _P,
-                                       _P, _I, _P, _P]
+                                       _P, _I, _I, _P, _P, _P]
     L.tqo_requantize.argtypes = [_I, _I, _I, ctypes.POINTER(_Segment), _I, _I, _P, _P,
                                  ctypes.POINTER(_Segment), _I]
     return L
@@ -386,8 +386,15 @@ def requantize(src: PackedSegment, src_t0: int, n: int, dst: PackedSegment, dst_
 
 
 def decode_attention(segments, q: np.ndarray, sign: np.ndarray, H: int,
-                     S: np.ndarray | None = None, jl: int = 128) -> np.ndarray:
-    """Binary64 attention of q ([B][Hq][d], fp16) over a layer's segments."""
+                     S: np.ndarray | None = None, jl: int = 128, estimator: int = 0,
+                     with_mass: bool = False):
+    """Binary64 attention of q ([B][Hq][d], fp16) over a layer's segments.
+
+    estimator: 0 = QJL residual estimate added to the key ("QJL residual
+    correction (sub-2-bit)"); 1 = sign-pair estimate added to the score ("RaBitQ
+    vs QJL correction").  with_mass: also return, per segment, the attention
+    mass [B][H][n_tokens] of each token: its softmax weight averaged over the
+    query heads of its KV head."""
     qb = _c(np.asarray(q).view(np.uint16) if np.asarray(q).dtype == np.float16 else q, np.uint16)
     B, Hq, d = qb.shape
     cents, _, cp, _ = _cent_thr_tables()
@@ -395,9 +402,17 @@ def decode_attention(segments, q: np.ndarray, sign: np.ndarray, H: int,
     out = np.zeros((B, Hq, d), np.float64)
     s = _c(sign, np.int8)
     Sm = None if S is None else _c(S, np.float32)
-    lib().tqo_decode_attention(B, H, Hq, d, len(segments), arr, _ptr(s), cp, _ptr(Sm), jl,
-                               _ptr(qb), _ptr(out))
-    return out
+    total = sum(int(sg.n_tokens) for sg in segments)
+    mass = np.zeros((B, H, max(total, 1)), np.float64) if with_mass else None
+    lib().tqo_decode_attention(B, H, Hq, d, len(segments), arr, _ptr(s), cp, _ptr(Sm), jl, estimator,
+                               _ptr(qb), _ptr(out), _ptr(mass))
+    if not with_mass:
+        return out
+    per_seg, n = [], 0
+    for sg in segments:
+        per_seg.append(mass[:, :, n:n + int(sg.n_tokens)].copy())
+        n += int(sg.n_tokens)
+    return out, per_seg
 
 
 # --------------------------------------------------------------------------- #

@@ -561,26 +561,54 @@ void tqo_requantize(int B, int H, int d, const tqo_segment *src, int src_t0, int
 /* q: fp16 bit patterns [B][Hq][d]; out: [B][Hq][d] binary64.  An empty cache     */
 /* gives a zero output.                                                         */
 /* ------------------------------------------------------------------------ */
+/* Decode attention in binary64 over a layer's segments.
+ *
+ * QJL heads: estimator 0 adds the residual estimate sqrt(pi/2)/jl * rho * S^T s
+ * to the key ("QJL residual correction (sub-2-bit)", the unbiased estimator);
+ * estimator 1 adds instead, to the score, (pi/2)/jl * ||q'|| * rho *
+ * <sign(S q'), s> with q' = R q (the sign-pair estimator of "RaBitQ vs QJL
+ * correction": pi/2 times the two scales times the mean sign agreement; the
+ * query's sign follows the key side's convention, sign(0) = +1).
+ *
+ * mass (may be NULL): for each (b, KV head h, token n of the segments taken in
+ * order), the softmax weight of the token averaged over the g query heads that
+ * read h, at mass[(b * H + h) * total + n] (total = the tokens of all segments).
+ */
 void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segment *segs,
                           const int8_t *sign, const float *const *cent, const float *S,
-                          int jl, const uint16_t *q, double *out) {
+                          int jl, int estimator, const uint16_t *q, double *out, double *mass) {
     const int g = Hq / H;
     int total = 0;
     for (int s = 0; s < n_seg; s++) total += segs[s].n_tokens;
     double *score = (double *)malloc(sizeof(double) * (total > 0 ? total : 1));
     double *vals = (double *)malloc(sizeof(double) * (size_t)(total > 0 ? total : 1) * d);
-    double yk[TQO_MAX_D], yv[TQO_MAX_D], kh[TQO_MAX_D], qq[TQO_MAX_D];
+    double yk[TQO_MAX_D], yv[TQO_MAX_D], kh[TQO_MAX_D], qq[TQO_MAX_D], qr[TQO_MAX_D];
+    double qsgn[1024];
     uint8_t code[TQO_MAX_D];
+    if (mass)
+        for (size_t i = 0; i < (size_t)B * H * total; i++) mass[i] = 0.0;
     for (int b = 0; b < B; b++)
         for (int j = 0; j < Hq; j++) {
             const int h = j / g;
             for (int i = 0; i < d; i++) qq[i] = tqo_half_to_double(q[((size_t)b * Hq + j) * d + i]);
+            double qnorm = 0.0;
+            if (estimator == 1 && S) {
+                tqo_rotate_f64(d, sign, qq, qr);
+                for (int i = 0; i < d; i++) qnorm += qr[i] * qr[i];
+                qnorm = sqrt(qnorm);
+                for (int jj = 0; jj < jl; jj++) {
+                    double t = 0.0;
+                    for (int i = 0; i < d; i++) t += (double)S[(size_t)jj * d + i] * qr[i];
+                    qsgn[jj] = t >= 0.0 ? 1.0 : -1.0;
+                }
+            }
             int n = 0;
             for (int s = 0; s < n_seg; s++) {
                 const tqo_segment *sg = &segs[s];
                 const int nq = sg->kind == 0 ? qjl_rank(sg->qjl, H) : 0;
                 for (int t = 0; t < sg->n_tokens; t++, n++) {
                     double *v = vals + (size_t)n * d;
+                    double corr = 0.0;  /* sign-pair QJL term of the score */
                     if (sg->kind == 1) {
                         const size_t o = (((size_t)b * H + h) * sg->capacity + t) * d;
                         for (int i = 0; i < d; i++) {
@@ -595,11 +623,17 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
                         if (sg->qjl[h]) {
                             const size_t qi = ((size_t)b * nq + qjl_rank(sg->qjl, h)) * sg->capacity + t;
                             const uint8_t *sb = sg->qjl_signs + qi * (jl / 8);
-                            const double coef = sqrt(TQO_PI / 2.0) / jl * (double)sg->qjl_norm[qi];
+                            const double rho = (double)sg->qjl_norm[qi];
                             for (int jj = 0; jj < jl; jj++) {
                                 const double sj = ((sb[jj >> 3] >> (jj & 7)) & 1) ? 1.0 : -1.0;
-                                for (int i = 0; i < d; i++) yk[i] += coef * sj * (double)S[(size_t)jj * d + i];
+                                if (estimator == 1) {
+                                    corr += qsgn[jj] * sj;
+                                } else {
+                                    const double coef = sqrt(TQO_PI / 2.0) / jl * rho;
+                                    for (int i = 0; i < d; i++) yk[i] += coef * sj * (double)S[(size_t)jj * d + i];
+                                }
                             }
+                            corr *= TQO_PI / 2.0 / jl * qnorm * rho;
                         }
                         tqo_rotate_f64(d, sign, yk, kh);
                         tqo_unpack(d, vb, sg->vcodes + off_codes(sg->vbits, H, d, sg->capacity, b, h, t), code);
@@ -609,6 +643,7 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
                     }
                     double dot = 0.0;
                     for (int i = 0; i < d; i++) dot += qq[i] * kh[i];
+                    dot += corr;
                     score[n] = dot / sqrt((double)d);
                 }
             }
@@ -625,6 +660,7 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
             for (int t = 0; t < total; t++) {
                 const double p = score[t] / l;
                 for (int i = 0; i < d; i++) o[i] += p * vals[(size_t)t * d + i];
+                if (mass) mass[((size_t)b * H + h) * total + t] += p / g;
             }
         }
     free(score);
