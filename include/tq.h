@@ -225,12 +225,29 @@ typedef struct {
                                   bits and qjl for packed segments */
     tq_packed_bufs packed;     /* TQ_SEG_PACKED */
     const void *k16, *v16;     /* TQ_SEG_FP16: fp16 [B][H][capacity][d], unrotated */
+    float *attn_mass;          /* optional (NULL: none), device float [B][H][capacity],
+                                  16-byte aligned, caller-owned: tq_decode_attention
+                                  writes entry (b, h, t), t < n_tokens, with the
+                                  attention mass of token t (below) */
 } tq_segment;
+
+/* Score estimators for QJL heads (the sketch s = sign(S r), rho = ||r|| is the
+ * same for both; q' = R q):
+ *   TQ_QJL_UNBIASED   q'.yhat + sqrt(pi/2)/jl * rho * <S q', s>  ("TurboMOQ",
+ *                     "QJL residual correction (sub-2-bit)"; unbiased)
+ *   TQ_QJL_SIGN_PAIR  q'.yhat + (pi/2)/jl * ||q'|| * rho * <sign(S q'), s>
+ *                     ("turboquant-mlx", "RaBitQ vs QJL correction": pi/2 times
+ *                     both scales times the sign agreement; sign(0) = +1).  Its
+ *                     mean is ||q'|| rho (pi/2 - theta), theta the angle of q'
+ *                     and r (Sheppard): unbiased only to first order in cos theta. */
+#define TQ_QJL_UNBIASED 0
+#define TQ_QJL_SIGN_PAIR 1
 
 typedef struct {
     tq_rotation rot;           /* the layer's rotation (same D for K, V and q) */
     int n_segments;            /* 0..TQ_MAX_SEGMENTS; order does not matter */
     tq_segment seg[TQ_MAX_SEGMENTS];
+    int qjl_estimator;         /* TQ_QJL_UNBIASED or TQ_QJL_SIGN_PAIR (else TQ_ERR_ARG) */
 } tq_layer_view;
 
 /* Bytes of device workspace tq_decode_attention needs for these layers. */
@@ -243,7 +260,7 @@ tq_status tq_decode_workspace_size(const tq_layer_view *layers, int n_layers, in
  * Computed without materialising k_t, v_t: q is rotated once, scores and the
  * value sum run in the rotated space on the packed codes (split over token
  * chunks with an online softmax), and one inverse rotation is applied to the
- * merged value sum.  QJL heads add sqrt(pi/2)/jl * ||r|| * <S q', s> to q'.yhat.
+ * merged value sum.  QJL heads add the layer's qjl_estimator term to q'.yhat.
  * q: device fp16 [n_layers][batch][q_heads][d]; out: device float, same shape.
  * qjl_S: device jl_dim x d floats, required iff a packed segment uses QJL.
  * workspace: device, >= tq_decode_workspace_size bytes (TQ_ERR_SIZE otherwise).
@@ -253,7 +270,15 @@ tq_status tq_decode_workspace_size(const tq_layer_view *layers, int n_layers, in
  * any QJL segment), the fp16-segment split-K kernel (if any fp16 segment) and
  * one persistent split-K kernel per (key bits, value bits, QJL) class of the
  * packed segments, each merging the partials of the (layer, batch, KV head)
- * it completes.  A layer with no tokens yields zeros. */
+ * it completes.  A layer with no tokens yields zeros.
+ * Attention mass (the per-token signal of attention-weighted tier demotion,
+ * "TurboMOQ", "Attention-weighted tier demotion"): for every segment with
+ * attn_mass set, one more kernel after the merges writes
+ *   attn_mass[b][h][t] = (1/g) sum_{j : j/g = h} p_j(t),
+ * p_j(t) the softmax weight of token t for query head j (g = q_heads/n_heads),
+ * so that over all segments of a layer sum_t attn_mass[b][h][t] = 1; scores are
+ * recomputed from the codes in binary32 and normalised by the merged max and
+ * sum. */
 tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int batch,
                               int n_heads, int q_heads, int head_dim, const float *qjl_S,
                               int jl_dim, const void *q, float *out, void *workspace,

@@ -495,8 +495,12 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
         o.y = (ar[1] + ao[1]) * inv;
         o.z = (ar[2] + ao[2]) * inv;
         o.w = (ar[3] + ao[3]) * inv;
-        const size_t row = ((static_cast<size_t>(layer) * dims.B + b) * dims.Hq + h * dims.gqa + warp) * kD;
-        reinterpret_cast<float4 *>(ws.out + row)[lane] = o;
+        const size_t qrow = (static_cast<size_t>(layer) * dims.B + b) * dims.Hq + h * dims.gqa + warp;
+        reinterpret_cast<float4 *>(ws.out + qrow * kD)[lane] = o;
+        if (ws.ml && lane == 0) {  // for the attention-mass kernel
+            ws.ml[qrow * 2] = M;
+            ws.ml[qrow * 2 + 1] = L;
+        }
     }
     __syncthreads();
 }

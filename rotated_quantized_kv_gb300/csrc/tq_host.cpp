@@ -299,9 +299,10 @@ struct Plan {
     DecodeDims dims{};
     bool any_qjl = false;
     int n_parts = 0;
+    int mass_ctas = 0;  // CTAs of the attention-mass launch (0: no segment asked for mass)
     std::vector<int> grp_part, grp_nparts, lbh_total;
     size_t off_items = 0, off_layer = 0, off_grp_part = 0, off_grp_nparts = 0, off_lbh_total = 0, off_counter = 0;
-    size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, total = 0;
+    size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, off_ml = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -330,10 +331,12 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
         if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
+        if (lv.qjl_estimator != TQ_QJL_UNBIASED && lv.qjl_estimator != TQ_QJL_SIGN_PAIR) return TQ_ERR_ARG;
         for (int s = 0; s < lv.n_segments; ++s) {
             const tq_segment &sg = lv.seg[s];
             const tq_segment_layout &L = sg.layout;
             if (sg.kind != TQ_SEG_PACKED && sg.kind != TQ_SEG_FP16) return TQ_ERR_ARG;
+            if (check_ptrs && sg.attn_mass && !aligned16(sg.attn_mass)) return TQ_ERR_ALIGN;
             tq_status st = check_layout(&L, sg.kind == TQ_SEG_PACKED);
             if (st != TQ_OK) return st;
             if (L.batch != B || L.n_heads != H || L.head_dim != d) return TQ_ERR_ARG;
@@ -374,6 +377,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         const tq_layer_view &lv = layers[l];
         LayerPlan &lp = P.layer[l];
         std::memcpy(lp.sign_bits, lv.rot.sign_bits, sizeof(lp.sign_bits));
+        lp.qjl_mode = lv.qjl_estimator;
         for (int s = 0; s < lv.n_segments; ++s) {
             const tq_segment &sg = lv.seg[s];
             if (sg.n_tokens == 0) continue;
@@ -387,6 +391,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                 w.layer = l;
                 w.head = h;
                 w.n_tokens = sg.n_tokens;
+                w.mass = sg.attn_mass ? sg.attn_mass + h * cap : nullptr;
+                w.sstride = static_cast<uint32_t>(H * cap);
                 if (sg.kind == TQ_SEG_PACKED) {
                     w.kc = static_cast<const uint8_t *>(sg.packed.kcodes) + o.koff[h];
                     w.vc = static_cast<const uint8_t *>(sg.packed.vcodes) + o.voff[h];
@@ -394,7 +400,6 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                     w.vs = sg.packed.vscale + h * cap;
                     w.kstride = o.kblock;
                     w.vstride = o.vblock;
-                    w.sstride = static_cast<uint32_t>(H * cap);
                     w.kb = L.kbits[h];
                     w.vb = L.vbits[h];
                     w.qjl = L.qjl[h] ? 1 : 0;
@@ -503,6 +508,17 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         lp.item[w.head][lp.n_items[w.head]++] = static_cast<int>(i);
     }
     P.n_parts = static_cast<int>(part);
+    // attention mass: one CTA per (item with a mass buffer, batch element,
+    // kMassTokens tokens); items without one start where the next one does
+    {
+        long long mc = 0;
+        for (WorkItem &w : P.items) {
+            w.mass_cta_begin = static_cast<int>(mc);
+            if (w.mass) mc += static_cast<long long>(B) * ((w.n_tokens + kMassTokens - 1) / kMassTokens);
+            if (mc > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
+        }
+        P.mass_ctas = static_cast<int>(mc);
+    }
     DecodeDims &D = P.dims;
     D.L = n_layers;
     D.B = B;
@@ -539,6 +555,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     }
     P.off_part = off;
     off += align256(static_cast<size_t>(std::max(P.n_parts, 1)) * kMaxGqa * (4 + kD) * 4);
+    P.off_ml = off;
+    if (P.mass_ctas > 0) off += align256(nq * 2 * sizeof(float));
     P.total = off;
     return TQ_OK;
 }
@@ -917,6 +935,7 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     W.qjlt = reinterpret_cast<uint32_t *>(ws + P.off_qjlt);
     W.qsum = reinterpret_cast<float *>(ws + P.off_qsum);
     W.part = reinterpret_cast<float *>(ws + P.off_part);
+    W.ml = P.mass_ctas > 0 ? reinterpret_cast<float *>(ws + P.off_ml) : nullptr;
     W.q = static_cast<const uint16_t *>(q);
     W.out = out;
     // fp16 codebook values (and the 1-bit centroid) of every decode class;
@@ -953,6 +972,8 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     if (P.items.empty()) return TQ_OK;
     e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S,
                               class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop);
+    if (e == cudaSuccess && P.mass_ctas > 0)
+        e = launch_attention_mass(P.dims, W, static_cast<int>(P.items.size()), P.mass_ctas, s);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 

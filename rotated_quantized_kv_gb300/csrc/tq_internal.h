@@ -96,11 +96,14 @@ struct alignas(16) WorkItem {
     int chunk, n_chunks;      // fp16: tokens per CTA (multiple of 64) and CTAs per batch element
     int cta_begin;            // fp16: first CTA within its launch
     int kb, vb, qjl, vlaw;  // vlaw: value codebook law (host side only)
+    float *mass;              // attention mass of (b=0, head, t=0), batch stride sstride; null: none
+    int mass_cta_begin;       // first CTA of the item in the attention-mass launch
 };
 
 struct LayerPlan {
     uint32_t sign_bits[kD / 32];
     int has_qjl;
+    int qjl_mode;                          // TQ_QJL_UNBIASED / TQ_QJL_SIGN_PAIR
     int n_items[kMaxH];                    // items of each KV head
     int item[kMaxH][TQ_MAX_SEGMENTS];      // their indices in the WorkItem array
 };
@@ -128,6 +131,7 @@ struct DecodeWorkspace {
     uint32_t *qjlt;    // [L][B][Hq][2][d/2] half2 words: hi, lo of S R q (QJL calls only)
     float *qsum;       // [L][B][Hq][4]: sum(R q), sum(S R q), 2^e of the stored R q / 2^e (QJL calls only)
     float *part;       // [parts][kMaxGqa][4 + d]: m (log2 units), l, pad, pad, acc
+    float *ml;         // [L][B][Hq][2]: merged max (log2 units) and sum, or null (no mass wanted)
     const uint16_t *q; // the caller's queries, fp16 [L][B][Hq][d]
     float *out;        // the caller's output, [L][B][Hq][d]
 };
@@ -137,6 +141,7 @@ struct DecodeWorkspace {
 constexpr int kStageTokens = 64;
 constexpr int kPackedStageTokens = 128;
 constexpr int kDecodeWarps = 4;
+constexpr int kMassTokens = 128;  // tokens per CTA of the attention-mass kernel (one thread each)
 constexpr int kStages = 4;
 
 // A launch of the split-K kernel of one class over items [item_lo, item_hi).
@@ -180,5 +185,9 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
                                   int n_classes, const float *S, const unsigned short *const *value_half,
                                   const float *value_c1,
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop);
+// Attention mass of every item with a mass pointer (items [0, n_items) of the
+// plan, n_ctas CTAs in all), after the decode kernels of the call.
+cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
+                                  cudaStream_t s);
 
 }  // namespace tqk

@@ -36,6 +36,8 @@ TQ_SEG_PACKED = 0
 TQ_SEG_FP16 = 1
 TQ_VALUE_LAW_GAUSS = 0
 TQ_VALUE_LAW_SPHERE = 1
+TQ_QJL_UNBIASED = 0
+TQ_QJL_SIGN_PAIR = 1
 
 STATUS = {0: "TQ_OK", -1: "TQ_ERR_ARG", -2: "TQ_ERR_UNSUPPORTED", -3: "TQ_ERR_ALIGN",
           -4: "TQ_ERR_SIZE", -5: "TQ_ERR_CUDA"}
@@ -80,12 +82,13 @@ class tq_packed_bufs(ctypes.Structure):
 
 class tq_segment(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("n_tokens", ctypes.c_int), ("layout", tq_segment_layout),
-                ("packed", tq_packed_bufs), ("k16", ctypes.c_void_p), ("v16", ctypes.c_void_p)]
+                ("packed", tq_packed_bufs), ("k16", ctypes.c_void_p), ("v16", ctypes.c_void_p),
+                ("attn_mass", ctypes.c_void_p)]
 
 
 class tq_layer_view(ctypes.Structure):
     _fields_ = [("rot", tq_rotation), ("n_segments", ctypes.c_int),
-                ("seg", tq_segment * TQ_MAX_SEGMENTS)]
+                ("seg", tq_segment * TQ_MAX_SEGMENTS), ("qjl_estimator", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -206,6 +209,7 @@ class PackedSegment:
     tq_packed_size reports."""
 
     kind = TQ_SEG_PACKED
+    attn_mass = None  # optional float tensor [B][H][capacity]: written by tq_decode_attention
 
     def __init__(self, layout: tq_segment_layout, device="cuda", n_tokens: int = 0):
         self.layout = layout
@@ -230,6 +234,7 @@ class PackedSegment:
     def segment(self) -> tq_segment:
         s = tq_segment()
         s.kind, s.n_tokens, s.layout, s.packed = TQ_SEG_PACKED, self.n_tokens, self.layout, self.bufs()
+        s.attn_mass = _ptr(self.attn_mass)
         return s
 
     def nbytes(self) -> int:
@@ -242,6 +247,7 @@ class Fp16Segment:
     """Tokens kept verbatim in fp16: [B][H][capacity][d] K and V."""
 
     kind = TQ_SEG_FP16
+    attn_mass = None  # optional float tensor [B][H][capacity]: written by tq_decode_attention
 
     def __init__(self, batch, n_heads, head_dim, capacity, device="cuda", n_tokens=0, k=None, v=None):
         self.layout = make_layout(batch, n_heads, head_dim, capacity, 1, 1)
@@ -254,12 +260,16 @@ class Fp16Segment:
         s = tq_segment()
         s.kind, s.n_tokens, s.layout = TQ_SEG_FP16, self.n_tokens, self.layout
         s.k16, s.v16 = _ptr(self.k), _ptr(self.v)
+        s.attn_mass = _ptr(self.attn_mass)
         return s
 
 
-def layer_view(rot: tq_rotation, segments) -> tq_layer_view:
+def layer_view(rot: tq_rotation, segments, qjl_estimator: int = TQ_QJL_UNBIASED) -> tq_layer_view:
+    """A layer's segments; a segment's attn_mass tensor (if set) receives the
+    attention mass of its tokens at the next decode call."""
     lv = tq_layer_view()
     lv.rot = rot
+    lv.qjl_estimator = qjl_estimator
     lv.n_segments = len(segments)
     for i, s in enumerate(segments):
         lv.seg[i] = s.segment()

@@ -134,6 +134,14 @@ def test_host_side_argument_errors(tq):
         tq.tq_decode_workspace_size([lv], 1, 2, 3, 128)
     assert e.value.status == -1
     assert tq.tq_decode_workspace_size([lv], 1, 2, 8, 128) > 0
+    with pytest.raises(tq.TQError) as e:  # unknown QJL estimator
+        tq.tq_decode_workspace_size([tq.layer_view(rot, [seg], qjl_estimator=2)], 1, 2, 8, 128)
+    assert e.value.status == -1
+    # an attention-mass buffer adds the merged (max, sum) table to the workspace
+    seg.attn_mass = torch.zeros(1, 2, 16)
+    assert tq.tq_decode_workspace_size([tq.layer_view(rot, [seg])], 1, 2, 8, 128) >= \
+        tq.tq_decode_workspace_size([lv], 1, 2, 8, 128)
+    seg.attn_mass = None
     # packed capacity must keep scale rows 16-byte aligned
     P = tq.PackedSegment(tq.make_layout(1, 2, 128, 40, 3, 3), device="cpu", n_tokens=10)
     with pytest.raises(tq.TQError) as e:

@@ -201,8 +201,12 @@ def _max_rel(out, ref):
     return (np.abs(o - r).max(axis=1) / np.maximum(np.abs(r).max(axis=1), 1e-30)).max()
 
 
-def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
-    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl[, law])."""
+MASS_RTOL = 1e-4  # binary32 scores: |ds| ~ 1e-5 in log units at these magnitudes
+
+
+def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False, estimator=0, mass=False):
+    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl[, law]).
+    mass: every segment gets an attention-mass buffer, checked against the oracle's."""
     rng = np.random.default_rng(seed)
     S = O.qjl_matrix(128, 128, 42 + 1000) if qjl_any else None
     Sd = torch.from_numpy(S).cuda() if qjl_any else None
@@ -233,10 +237,12 @@ def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
                     O.compress(o, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S)
                 o.n_tokens = T
                 g = _upload(tq, o, tq.make_layout(B, H, 128, cap, kb, vb, qj, value_law=law), T)
+            if mass:  # -1 marks entries the call must leave alone
+                g.attn_mass = torch.full((B, H, cap), -1.0, device="cuda")
             osegs.append(o)
             gsegs.append(g)
         keep.append(gsegs)
-        views.append(tq.layer_view(rot, gsegs))
+        views.append(tq.layer_view(rot, gsegs, qjl_estimator=estimator))
         oracle_layers.append((osegs, sign))
     q = torch.from_numpy(rng.standard_normal((L, B, Hq, 128)).astype(np.float16))
     out = torch.empty(L, B, Hq, 128, device="cuda")
@@ -248,7 +254,24 @@ def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False):
     worst = 0.0
     for l in range(L):
         osegs, sign = oracle_layers[l]
-        ref = O.decode_attention(osegs, q[l].numpy(), sign, H, S=S)
+        if estimator == 1 and S is not None:
+            # the query's sign decisions must be unique: no |(S q')_j| inside the
+            # binary32 error bound of the kernels' q' and S q' (~(7 + 128) 2^-24
+            # relative) around zero; the seed is chosen so that none is
+            Sd = S.astype(np.float64)
+            qr = np.stack([O.rotate_f64(x.astype(np.float64), sign) for x in q[l].numpy().reshape(-1, 128)])
+            t = qr @ Sd.T
+            rel = np.abs(t) / np.linalg.norm(Sd, axis=1)[None] / np.linalg.norm(qr, axis=1)[:, None]
+            assert rel.min() > 1e-5, rel.min()
+        ref = O.decode_attention(osegs, q[l].numpy(), sign, H, S=S, estimator=estimator, with_mass=mass)
+        if mass:
+            ref, ref_mass = ref
+            for g, rm in zip(keep[l], ref_mass):
+                gm = g.attn_mass.cpu().numpy()
+                n = g.n_tokens
+                assert np.all(gm[:, :, n:] == -1.0)
+                err = np.abs(gm[:, :, :n] - rm)
+                assert np.all(err <= MASS_RTOL * rm + 1e-30), (err / np.maximum(rm, 1e-30)).max()
         if all(s.n_tokens == 0 for s in osegs):
             assert np.all(got[l] == 0)
             continue
@@ -275,6 +298,33 @@ def test_decode_attention_matches_oracle(tq, L, B, H, Hq, spec):
     qjl_any = any(s[0] == "packed" and s[4] and any(s[4]) for s in spec)
     worst = _attention_case(tq, L, B, H, Hq, spec, seed=len(spec) * 7 + L, qjl_any=qjl_any)
     assert worst <= ATTN_TOL, worst
+
+
+MASS_CASES = [
+    # L, B, H, Hq, segments
+    (2, 2, 2, 8, [("fp16", 10), ("packed", 300, [3, 5], [2, 8], None), ("fp16", 7)]),
+    (1, 3, 4, 8, [("packed", 200, [1, 2, 3, 4], [1, 2, 3, 4], [1, 1, 0, 0]),
+                  ("packed", 129, [5, 6, 7, 8], [8, 7, 6, 5], None), ("fp16", 0)]),
+    (1, 1, 8, 8, [("packed", 333, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], None, 1)]),
+    (1, 2, 8, 16, [("fp16", 128), ("packed", 1000, [3] * 8, [3] * 8, None), ("fp16", 37)]),
+]
+
+
+@pytest.mark.parametrize("L,B,H,Hq,spec", MASS_CASES)
+def test_attention_mass_matches_oracle(tq, L, B, H, Hq, spec):
+    qjl_any = any(s[0] == "packed" and s[4] and any(s[4]) for s in spec)
+    worst = _attention_case(tq, L, B, H, Hq, spec, seed=40 + len(spec), qjl_any=qjl_any, mass=True)
+    assert worst <= ATTN_TOL, worst
+
+
+@pytest.mark.parametrize("spec", [
+    [("packed", 190, [2, 1, 4, 3], [3, 4, 1, 2], [1, 1, 0, 0]), ("fp16", 20)],
+    [("packed", 260, [1] * 4, [2] * 4, [1] * 4), ("packed", 70, [2] * 4, [1] * 4, [1, 0, 1, 0])],
+])
+def test_decode_attention_sign_pair_estimator(tq, spec):
+    # same sketch, the sign-pair score term; the mass kernel follows it too
+    w = _attention_case(tq, 1, 2, 4, 16, spec, seed=67, qjl_any=True, estimator=1, mass=True)
+    assert w <= ATTN_TOL, w
 
 
 def test_decode_attention_empty_and_single_token(tq):
