@@ -86,10 +86,11 @@ def lib() -> ctypes.CDLL:
     L.tqo_qjl_project.argtypes = [_I, _I, _P, _P, _P]
     L.tqo_qjl_sketch.argtypes = [_I, _I, _P, _P, _P, _P, _P]
     L.tqo_compress.argtypes = [_I, _I, _I, _I, _P, _P, _LL, _LL, _LL, _P, _P, _P, _I,
-                               ctypes.POINTER(_Segment), _I]
+                               ctypes.POINTER(_Segment), _I, _P]
+    L.tqo_rotate_dense_f32.argtypes = [_I, _P, _P, _P]
     L.tqo_dequant.argtypes = [_I, _I, ctypes.POINTER(_Segment), _I, _I, _I, _I, _P, _P, _P]
     L.tqo_decode_attention.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_Segment), _P, _P,
-                                       _P, _I, _I, _P, _P, _P]
+                                       _P, _I, _I, _P, _P, _P, _P]
     L.tqo_requantize.argtypes = [_I, _I, _I, ctypes.POINTER(_Segment), _I, _I, _P, _P,
                                  ctypes.POINTER(_Segment), _I]
     return L
@@ -151,6 +152,27 @@ def rotate_f64(x: np.ndarray, sign: np.ndarray) -> np.ndarray:
 
 
 @functools.lru_cache(maxsize=None)
+def haar_rotation(d: int, seed: int) -> np.ndarray:
+    """Dense Haar-random rotation ("TurboMOQ", "Stable QR Rotation": QR of a
+    Gaussian matrix through LAPACK).  G = the N(0,1) matrix of qjl_matrix(d, d,
+    seed) (Box-Muller on SplitMix64, binary32); G = Q R by numpy.linalg.qr in
+    binary64, the columns of Q multiplied by the signs of diag(R) so that R has a
+    positive diagonal (Q is then Haar-distributed, Mezzadri 2007); Q rounded to
+    binary32.  y = Q x is the rotation."""
+    G = qjl_matrix(d, d, seed).astype(np.float64)
+    Qm, R = np.linalg.qr(G)
+    sgn = np.where(np.diag(R) < 0, -1.0, 1.0)
+    return (Qm * sgn[None, :]).astype(np.float32)
+
+
+def rotate_dense_f32(x: np.ndarray, Q: np.ndarray) -> np.ndarray:
+    """Binary32 rotated vector y = Q x (the exact product rounded once)."""
+    xx = _c(np.asarray(x, np.float32), np.float32)
+    y = np.zeros(Q.shape[0], np.float32)
+    lib().tqo_rotate_dense_f32(Q.shape[0], _ptr(_c(Q, np.float32)), _ptr(xx), _ptr(y))
+    return y
+
+
 def lloyd_max(bits: int, max_iter: int = 1_000_000):
     """Gaussian Lloyd-Max codebook in binary64: (centroids, thresholds, sweeps)."""
     n = 1 << bits
@@ -347,9 +369,10 @@ class Fp16Segment:
 
 
 def compress(seg: PackedSegment, K: np.ndarray, V: np.ndarray, sign: np.ndarray,
-             S: np.ndarray | None = None, t_begin: int = 0) -> None:
+             S: np.ndarray | None = None, t_begin: int = 0, Q: np.ndarray | None = None) -> None:
     """Compress fp16 K, V ([B][H][T][d] arrays of fp16 values or uint16 bit
-    patterns) into positions [t_begin, t_begin + T) of ``seg``."""
+    patterns) into positions [t_begin, t_begin + T) of ``seg``; Q (binary32
+    d x d) replaces the SRHT of ``sign`` by the dense rotation y = Q x."""
     Kb = _c(np.asarray(K).view(np.uint16) if np.asarray(K).dtype == np.float16 else K, np.uint16)
     Vb = _c(np.asarray(V).view(np.uint16) if np.asarray(V).dtype == np.float16 else V, np.uint16)
     B, H, T, d = Kb.shape
@@ -358,8 +381,9 @@ def compress(seg: PackedSegment, K: np.ndarray, V: np.ndarray, sign: np.ndarray,
     s = _c(sign, np.int8)
     Sm = None if S is None else _c(S, np.float32)
     cs = seg.c_struct()
+    Qm = None if Q is None else _c(Q, np.float32)
     lib().tqo_compress(B, H, d, T, _ptr(Kb), _ptr(Vb), H * T * d, T * d, d, _ptr(s), tp,
-                       _ptr(Sm), seg.jl, ctypes.byref(cs), t_begin)
+                       _ptr(Sm), seg.jl, ctypes.byref(cs), t_begin, _ptr(Qm))
     seg.n_tokens = max(seg.n_tokens, t_begin + T)
 
 
@@ -387,14 +411,15 @@ def requantize(src: PackedSegment, src_t0: int, n: int, dst: PackedSegment, dst_
 
 def decode_attention(segments, q: np.ndarray, sign: np.ndarray, H: int,
                      S: np.ndarray | None = None, jl: int = 128, estimator: int = 0,
-                     with_mass: bool = False):
+                     with_mass: bool = False, Q: np.ndarray | None = None):
     """Binary64 attention of q ([B][Hq][d], fp16) over a layer's segments.
 
     estimator: 0 = QJL residual estimate added to the key ("QJL residual
     correction (sub-2-bit)"); 1 = sign-pair estimate added to the score ("RaBitQ
     vs QJL correction").  with_mass: also return, per segment, the attention
     mass [B][H][n_tokens] of each token: its softmax weight averaged over the
-    query heads of its KV head."""
+    query heads of its KV head.  Q: the layer's dense rotation (binary32 d x d)
+    instead of the SRHT of ``sign``."""
     qb = _c(np.asarray(q).view(np.uint16) if np.asarray(q).dtype == np.float16 else q, np.uint16)
     B, Hq, d = qb.shape
     cents, _, cp, _ = _cent_thr_tables()
@@ -404,8 +429,9 @@ def decode_attention(segments, q: np.ndarray, sign: np.ndarray, H: int,
     Sm = None if S is None else _c(S, np.float32)
     total = sum(int(sg.n_tokens) for sg in segments)
     mass = np.zeros((B, H, max(total, 1)), np.float64) if with_mass else None
+    Qm = None if Q is None else _c(Q, np.float32)
     lib().tqo_decode_attention(B, H, Hq, d, len(segments), arr, _ptr(s), cp, _ptr(Sm), jl, estimator,
-                               _ptr(qb), _ptr(out), _ptr(mass))
+                               _ptr(qb), _ptr(out), _ptr(mass), _ptr(Qm))
     if not with_mass:
         return out
     per_seg, n = [], 0

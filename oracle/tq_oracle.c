@@ -125,6 +125,28 @@ void tqo_rotate_f64(int d, const int8_t *sign, const double *x, double *y) {
 /* Gaussian Lloyd-Max codebook ([MOQ] "Architecture": values use a Lloyd-Max  */
 /* codebook; fitted here in closed form for the N(0,1) law, not on data).     */
 /* ------------------------------------------------------------------------ */
+/* Dense rotation ("TurboMOQ", "Stable QR Rotation": a Haar-random orthogonal
+ * matrix from a QR factorisation): y = Q x with Q a d x d binary32 matrix,
+ * row-major.  The binary32 form takes the exact product (binary64 sums of
+ * binary32 x binary16 terms, ~1e-16 relative) rounded once to binary32. */
+void tqo_rotate_dense_f32(int d, const float *Q, const float *x, float *y) {
+    for (int i = 0; i < d; i++) {
+        double acc = 0.0;
+        for (int j = 0; j < d; j++) acc += (double)Q[(size_t)i * d + j] * (double)x[j];
+        y[i] = (float)acc;
+    }
+}
+
+/* y = Q x (transpose = 0) or y = Q^T x (transpose = 1) in binary64. */
+void tqo_rotate_dense_f64(int d, const float *Q, int transpose, const double *x, double *y) {
+    for (int i = 0; i < d; i++) {
+        double acc = 0.0;
+        for (int j = 0; j < d; j++)
+            acc += (double)(transpose ? Q[(size_t)j * d + i] : Q[(size_t)i * d + j]) * x[j];
+        y[i] = acc;
+    }
+}
+
 static double std_pdf(double x) { return exp(-0.5 * x * x) / sqrt(2.0 * TQO_PI); }
 /* Upper tail Q(x) = P(X > x) = erfc(x / sqrt 2) / 2, accurate for large x. */
 static double std_tail(double x) { return 0.5 * erfc(x / sqrt(2.0)); }
@@ -465,11 +487,12 @@ static int qjl_rank(const uint8_t *qjl, int h) {
  * unit stride along d) into token positions [t_begin, t_begin + T) of a packed
  * segment.  thr[law * 9 + b] points at the 2^b - 1 binary32 value thresholds for
  * b bits of codebook law `law` (0 Gaussian, 1 sphere coordinate).
- * S is the QJL matrix (jl x d) or NULL when no head uses QJL. */
+ * S is the QJL matrix (jl x d) or NULL when no head uses QJL.
+ * Q: NULL for the SRHT of `sign`, else the dense rotation (d x d, y = Q x). */
 void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t *V,
                   long long sb, long long sh, long long st, const int8_t *sign,
                   const float *const *thr, const float *S, int jl,
-                  const tqo_segment *seg, int t_begin) {
+                  const tqo_segment *seg, int t_begin, const float *Q) {
     float x[TQO_MAX_D], y[TQO_MAX_D], yhat[TQO_MAX_D];
     uint8_t code[TQO_MAX_D];
     const int nq = qjl_rank(seg->qjl, H);
@@ -482,7 +505,8 @@ void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t 
                 /* keys */
                 const int kb = seg->kbits[h];
                 for (int i = 0; i < d; i++) x[i] = (float)tqo_half_to_double(K[src + i]);
-                tqo_rotate_f32(d, sign, x, y);
+                if (Q) tqo_rotate_dense_f32(d, Q, x, y);
+                else tqo_rotate_f32(d, sign, x, y);
                 float m;
                 tqo_quant_key(d, kb, y, code, &m);
                 tqo_pack(d, kb, code, seg->kcodes + off_codes(seg->kbits, H, d, seg->capacity, b, h, pos));
@@ -495,7 +519,8 @@ void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t 
                 /* values */
                 const int vb = seg->vbits[h];
                 for (int i = 0; i < d; i++) x[i] = (float)tqo_half_to_double(V[src + i]);
-                tqo_rotate_f32(d, sign, x, y);
+                if (Q) tqo_rotate_dense_f32(d, Q, x, y);
+                else tqo_rotate_f32(d, sign, x, y);
                 float sg;
                 tqo_quant_value(d, vb, y, thr[seg->value_law * 9 + vb], code, &sg);
                 tqo_pack(d, vb, code, seg->vcodes + off_codes(seg->vbits, H, d, seg->capacity, b, h, pos));
@@ -573,10 +598,14 @@ void tqo_requantize(int B, int H, int d, const tqo_segment *src, int src_t0, int
  * mass (may be NULL): for each (b, KV head h, token n of the segments taken in
  * order), the softmax weight of the token averaged over the g query heads that
  * read h, at mass[(b * H + h) * total + n] (total = the tokens of all segments).
+ *
+ * Q: NULL for the layer's SRHT (sign), else its dense rotation: packed keys and
+ * values return to the original space as Q^T yhat.
  */
 void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segment *segs,
                           const int8_t *sign, const float *const *cent, const float *S,
-                          int jl, int estimator, const uint16_t *q, double *out, double *mass) {
+                          int jl, int estimator, const uint16_t *q, double *out, double *mass,
+                          const float *Q) {
     const int g = Hq / H;
     int total = 0;
     for (int s = 0; s < n_seg; s++) total += segs[s].n_tokens;
@@ -593,7 +622,8 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
             for (int i = 0; i < d; i++) qq[i] = tqo_half_to_double(q[((size_t)b * Hq + j) * d + i]);
             double qnorm = 0.0;
             if (estimator == 1 && S) {
-                tqo_rotate_f64(d, sign, qq, qr);
+                if (Q) tqo_rotate_dense_f64(d, Q, 0, qq, qr);
+                else tqo_rotate_f64(d, sign, qq, qr);
                 for (int i = 0; i < d; i++) qnorm += qr[i] * qr[i];
                 qnorm = sqrt(qnorm);
                 for (int jj = 0; jj < jl; jj++) {
@@ -635,11 +665,13 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
                             }
                             corr *= TQO_PI / 2.0 / jl * qnorm * rho;
                         }
-                        tqo_rotate_f64(d, sign, yk, kh);
+                        if (Q) tqo_rotate_dense_f64(d, Q, 1, yk, kh);
+                        else tqo_rotate_f64(d, sign, yk, kh);
                         tqo_unpack(d, vb, sg->vcodes + off_codes(sg->vbits, H, d, sg->capacity, b, h, t), code);
                         for (int i = 0; i < d; i++)
                             yv[i] = (double)sg->vscale[sidx] * (double)cent[sg->value_law * 9 + vb][code[i]];
-                        tqo_rotate_f64(d, sign, yv, v);
+                        if (Q) tqo_rotate_dense_f64(d, Q, 1, yv, v);
+                        else tqo_rotate_f64(d, sign, yv, v);
                     }
                     double dot = 0.0;
                     for (int i = 0; i < d; i++) dot += qq[i] * kh[i];
