@@ -69,6 +69,12 @@ typedef struct {
     int head_dim;          /* d: a power of two, 16..1024 */
     uint64_t seed;         /* layer l conventionally uses seed + l */
     uint32_t sign_bits[TQ_MAX_HEAD_DIM / 32]; /* bit i set <=> D_i = -1 */
+    const float *dense;    /* NULL: the SRHT above.  Else a dense rotation
+                              ("TurboMOQ", "Stable QR Rotation"): device d x d
+                              floats, row-major, orthogonal, y = Q x (caller-owned,
+                              16-byte aligned; see tq_make_haar_rotation).  Used
+                              by tq_compress (tensor-core kernel, no QJL heads),
+                              tq_dequantize and tq_decode_attention. */
 } tq_rotation;
 
 /* Fill *rot (caller-owned, plain data) with the sign diagonal of
@@ -76,6 +82,15 @@ typedef struct {
  * of `seed` is set.  R is symmetric and R R = I.  TQ_ERR_ARG on a NULL rot or a
  * head_dim that is not a power of two in [16, 1024]. */
 tq_status tq_make_rotation(int head_dim, uint64_t seed, tq_rotation *rot);
+
+/* Haar-random rotation ("TurboMOQ", "Stable QR Rotation": QR factorisation of
+ * a Gaussian matrix): G = the N(0,1) matrix tq_make_qjl(head_dim, head_dim,
+ * seed) writes, factored G = Q R by Householder reflections in binary64, the
+ * columns of Q multiplied by the signs of diag(R) (so that Q is Haar
+ * distributed), rounded to binary32.  Q: host, head_dim^2 floats, row-major.
+ * Copy it to the device and set tq_rotation.dense to use it.  TQ_ERR_ARG on a
+ * NULL Q or a head_dim that is not a power of two in [16, 1024]. */
+tq_status tq_make_haar_rotation(int head_dim, uint64_t seed, float *Q);
 
 /* ------------------------------------------------------------------------ */
 /* Value codebook ("TurboMOQ", "Architecture": Lloyd-Max codebook -> grid      */
@@ -174,11 +189,22 @@ typedef struct {
  *   values: sigma = sqrt(pairwise-tree sum of y_i^2 / d), r = 1/sigma (0 if 0),
  *         code = #{k : thr_k < y r};
  *   QJL: r_i = y_i - m*((code+1/2) 2^(1-b) - 1), sign bits of S r, ||r||_2.
+ * With a dense rotation (rot->dense) y = Q x runs on the tensor cores: x fp16
+ * times Q carried as two fp16 parts (~2^-22), binary32 accumulation in an order
+ * the hardware chooses, so a code can differ from the exact product's where y
+ * lies within ~1e-6 of a decision boundary; the scales and quantizers are the
+ * ones above.  Dense rotation with QJL heads, or strides TMA cannot describe,
+ * return TQ_ERR_UNSUPPORTED.
  * Returns TQ_ERR_SIZE if t_begin + n_tokens > capacity. */
 tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot,
                       const float *qjl_S, const void *K, const void *V, int n_tokens,
                       int64_t stride_b, int64_t stride_h, int64_t stride_t, int t_begin,
                       const tq_packed_bufs *out, void *stream);
+
+/* The dense-rotation compress kernel bounds every wait for its own copies and
+ * tensor-core work; one that gave up sets a flag (process-wide, per device).
+ * *flag = that flag (waits for the device); reset != 0 clears it. */
+tq_status tq_compress_error_flag(int *flag, int reset);
 
 /* Dequantize token positions [t_begin, t_begin + n_tokens) of a packed segment.
  * k_rot / v_rot (device floats [B][H][n_tokens][d], either may be NULL): the

@@ -530,7 +530,14 @@ __global__ void dequant_kernel(const __grid_constant__ DequantParams p) {
         for (int i = 0; i < kD; i++) rot[o + i] = y[i];
     }
     float *orig = which ? p.v_orig : p.k_orig;
-    if (orig) {
+    if (orig && p.Q) {  // x = Q^T y, binary32 products in index order
+        for (int j = 0; j < kD; j++) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < kD; i++) acc = fmaf(__ldg(p.Q + static_cast<size_t>(i) * kD + j), y[i], acc);
+            orig[o + j] = acc;
+        }
+    } else if (orig) {
 #pragma unroll
         for (int i = 0; i < kD; i++)
             if ((p.sign_bits[i >> 5] >> (i & 31)) & 1u) y[i] = -y[i];

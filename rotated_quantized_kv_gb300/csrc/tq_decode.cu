@@ -116,10 +116,11 @@ __global__ void __launch_bounds__(kThreads, 6)
 }
 
 // -------------------------------------------------------------- prep kernel
-// Calls with QJL heads only: one warp per (layer, batch, query head) computes
-// q' = R q (normalised by a power of two) and t = S q' (fp16 hi/lo words),
-// with sum q', sum t and the power of two, for the QJL split-K kernels, which
-// read them after griddepcontrol.wait.
+// Calls with QJL heads or dense-rotation layers: one warp per (layer, batch,
+// query head) computes q' = R q (normalised by a power of two; R the layer's
+// SRHT or dense Q) and, for QJL layers, t = S q' (fp16 hi/lo words), with
+// sum q', sum t and the power of two, for the split-K kernels, which read them
+// after griddepcontrol.wait.
 __global__ void __launch_bounds__(kThreads)
     decode_prep_kernel(const DecodeDims dims, const DecodeWorkspace ws, const float *S) {
     __shared__ float qsh[kThreads / 32][kD];
@@ -131,7 +132,8 @@ __global__ void __launch_bounds__(kThreads)
     const LayerPlan &lp = ws.layer[l];
     float x[4];
     load_q4(ws.q + static_cast<size_t>(wid) * kD, lane, x);
-    warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
+    if (lp.dense) warp_rotate_dense(x, lp.dense, false, lane);
+    else warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
     // q' / 2^e with its largest coordinate in [0.5, 1) (the packed kernels
     // scale the B fragment up by powers of two); t = S q' from q' itself
     const float f = warp_pow2_norm(x);
@@ -255,7 +257,18 @@ __global__ void __launch_bounds__(kThreads)
         float tv[4] = {0.f, 0.f, 0.f, 0.f};
         if (warp < gqa) {
             load_q4(ws.q + qrow * kD, lane, x);
-            if (packed) warp_rotate(x, ws.layer[it.layer].sign_bits, dims.inv_sqrt_d, lane);
+            if (packed) {
+                const LayerPlan &lp = ws.layer[it.layer];
+                if (lp.dense) {  // the prep kernel's q' / 2^e (hi + lo) times 2^e
+                    const __half *qh = reinterpret_cast<const __half *>(ws.qrot + qrow * kD);
+                    const float f = ws.qsum[qrow * 4 + 2];
+#pragma unroll
+                    for (int e = 0; e < 4; e++)
+                        x[e] = (__half2float(qh[4 * lane + e]) + __half2float(qh[kD + 4 * lane + e])) * f;
+                } else {
+                    warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
+                }
+            }
             if (packed && it.qjl) {
                 const __half *th = reinterpret_cast<const __half *>(ws.qjlt + qrow * kD);
 #pragma unroll
@@ -368,7 +381,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    if (dims.any_qjl) {
+    if (dims.any_prep) {
         const int n_warps = dims.L * dims.B * dims.Hq;
         dec::decode_prep_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
         first = false;

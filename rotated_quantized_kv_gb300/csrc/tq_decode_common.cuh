@@ -365,6 +365,35 @@ __device__ __forceinline__ void warp_rotate(float (&x)[4], const uint32_t *sign_
     for (int e = 0; e < 4; e++) x[e] *= inv_sqrt_d;
 }
 
+// Dense rotation of a warp-held vector (lane holds coordinates 4 lane + e):
+// y = Q x (transpose = false) or y = Q^T x, Q row-major d x d.  Each step
+// reads one row of Q with one coalesced 16-byte load per lane.
+__device__ __forceinline__ void warp_rotate_dense(float (&x)[4], const float *Q, bool transpose, int lane) {
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    if (transpose) {  // y_j = sum_i Q[i][j] x_i
+#pragma unroll 4
+        for (int i = 0; i < kD; i++) {
+            const float xi = __shfl_sync(0xffffffffu, x[i & 3], i >> 2);
+            const float4 r = __ldg(reinterpret_cast<const float4 *>(Q + static_cast<size_t>(i) * kD) + lane);
+            y[0] = fmaf(r.x, xi, y[0]);
+            y[1] = fmaf(r.y, xi, y[1]);
+            y[2] = fmaf(r.z, xi, y[2]);
+            y[3] = fmaf(r.w, xi, y[3]);
+        }
+    } else {  // y_j = sum_i Q[j][i] x_i: a warp sum per row
+#pragma unroll 4
+        for (int j = 0; j < kD; j++) {
+            const float4 r = __ldg(reinterpret_cast<const float4 *>(Q + static_cast<size_t>(j) * kD) + lane);
+            float s = fmaf(r.x, x[0], fmaf(r.y, x[1], fmaf(r.z, x[2], r.w * x[3])));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if ((j >> 2) == lane) y[j & 3] = s;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] = y[e];
+}
+
 __device__ __forceinline__ void load_q4(const uint16_t *q, int lane, float (&x)[4]) {
     const uint2 v = reinterpret_cast<const uint2 *>(q)[lane];
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
@@ -488,7 +517,8 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
                 }
             }
         }
-        warp_rotate(ar, lp.sign_bits, dims.inv_sqrt_d, lane);
+        if (lp.dense) warp_rotate_dense(ar, lp.dense, true, lane);
+        else warp_rotate(ar, lp.sign_bits, dims.inv_sqrt_d, lane);
         const float inv = L > 0.f ? 1.0f / L : 0.f;
         float4 o;
         o.x = (ar[0] + ao[0]) * inv;

@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     if (threadIdx.x == 0) {
         for (int k = 0; k < NS - 1 && k < n_st; k++) load_next(k);
     }
-    if constexpr (QJL) pdl_wait();  // the prep kernel's outputs
+    if (QJL || dims.any_prep) pdl_wait();  // the prep kernel's outputs
 
     // ---- consumer
     StageCursor<QJL, false> cc;
@@ -657,6 +657,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
             gather_b<SignUnpack>(q, bt);
             qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
+            aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
+        } else if (ws.layer[g_layer].dense) {  // the prep kernel rotated the queries
+            const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
+#pragma unroll
+            for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
+            gather_b<KU>(q, bq);
+            qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
         } else {
             if (warp < gqa) {  // warp w rotates query head w of the group

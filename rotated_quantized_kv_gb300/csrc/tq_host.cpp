@@ -39,6 +39,19 @@ struct SplitMix64 {
     }
 };
 
+// n N(0,1) binary32 values: Box-Muller pairs on SplitMix64 words
+void fill_gaussian(uint64_t seed, int n, float *S) {
+    SplitMix64 g{seed};
+    const double two_pi = 6.283185307179586476925;
+    for (int i = 0; i < n; i += 2) {
+        const double u1 = static_cast<double>((g.next() >> 11) + 1) * 0x1p-53;
+        const double u2 = static_cast<double>(g.next() >> 11) * 0x1p-53;
+        const double rad = std::sqrt(-2.0 * std::log(u1));
+        S[i] = static_cast<float>(rad * std::cos(two_pi * u2));
+        if (i + 1 < n) S[i + 1] = static_cast<float>(rad * std::sin(two_pi * u2));
+    }
+}
+
 // ---------------------------------------------------------------- codebook fit
 // Gaussian Lloyd-Max quantizer ("TurboMOQ", "Architecture": values go through a
 // Lloyd-Max codebook), computed for N(0,1) in binary64.  The codebook is odd
@@ -332,6 +345,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         const tq_layer_view &lv = layers[l];
         if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
         if (lv.qjl_estimator != TQ_QJL_UNBIASED && lv.qjl_estimator != TQ_QJL_SIGN_PAIR) return TQ_ERR_ARG;
+        if (check_ptrs && lv.rot.dense && !aligned16(lv.rot.dense)) return TQ_ERR_ALIGN;
         for (int s = 0; s < lv.n_segments; ++s) {
             const tq_segment &sg = lv.seg[s];
             const tq_segment_layout &L = sg.layout;
@@ -368,6 +382,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     }
     P = Plan();
     P.layer.assign(n_layers, LayerPlan{});
+    bool any_dense = false;
     {
         size_t n = 0;
         for (int l = 0; l < n_layers; ++l) n += static_cast<size_t>(layers[l].n_segments) * H;
@@ -378,6 +393,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         LayerPlan &lp = P.layer[l];
         std::memcpy(lp.sign_bits, lv.rot.sign_bits, sizeof(lp.sign_bits));
         lp.qjl_mode = lv.qjl_estimator;
+        lp.dense = lv.rot.dense;
+        any_dense |= lv.rot.dense != nullptr;
         for (int s = 0; s < lv.n_segments; ++s) {
             const tq_segment &sg = lv.seg[s];
             if (sg.n_tokens == 0) continue;
@@ -526,6 +543,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.Hq = Hq;
     D.gqa = gqa;
     D.any_qjl = P.any_qjl ? 1 : 0;
+    D.any_prep = P.any_qjl || any_dense ? 1 : 0;
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
@@ -544,7 +562,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     P.off_counter = off;
     off += align256(static_cast<size_t>(n_layers) * B * H * sizeof(int));
     P.off_qrot = off;  // the uploaded plan ends here
-    if (P.any_qjl) {
+    if (D.any_prep) {
         off += align256(nq * d * 4);
         P.off_qjlt = off;
         off += align256(nq * d * 4);
@@ -616,19 +634,64 @@ tq_status tq_fit_codebook_sphere(int bits, int head_dim, float *centroids, float
     return TQ_OK;
 }
 
+tq_status tq_make_haar_rotation(int head_dim, uint64_t seed, float *Q) {
+    if (!Q || !pow2(head_dim) || head_dim < 16 || head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
+    const int d = head_dim;
+    std::vector<float> g(static_cast<size_t>(d) * d);
+    fill_gaussian(seed, d * d, g.data());  // the matrix tq_make_qjl(d, d, seed) writes
+    // Householder QR in binary64: A = G; reflector k maps A[k:, k] onto
+    // alpha_k e_1 with alpha_k = -sign(A_kk) ||A[k:, k]||, so R_kk = alpha_k.
+    std::vector<double> A(g.begin(), g.end()), V(static_cast<size_t>(d) * d, 0.0), alpha(d);
+    auto a = [&](int r, int c) -> double & { return A[static_cast<size_t>(r) * d + c]; };
+    for (int k = 0; k < d; ++k) {
+        double norm = 0.0;
+        for (int r = k; r < d; ++r) norm += a(r, k) * a(r, k);
+        norm = std::sqrt(norm);
+        alpha[k] = a(k, k) >= 0.0 ? -norm : norm;
+        double *v = &V[static_cast<size_t>(k) * d];
+        for (int r = k; r < d; ++r) v[r] = a(r, k);
+        v[k] -= alpha[k];
+        double vn = 0.0;
+        for (int r = k; r < d; ++r) vn += v[r] * v[r];
+        vn = std::sqrt(vn);
+        if (vn == 0.0) continue;  // column already alpha e_1
+        for (int r = k; r < d; ++r) v[r] /= vn;
+        for (int c = k; c < d; ++c) {
+            double dot = 0.0;
+            for (int r = k; r < d; ++r) dot += v[r] * a(r, c);
+            for (int r = k; r < d; ++r) a(r, c) -= 2.0 * v[r] * dot;
+        }
+    }
+    // Q = H_0 H_1 ... H_{d-1} (applied to I from the last reflector), then
+    // column j times sign(R_jj) so that R has a positive diagonal
+    std::vector<double> M(static_cast<size_t>(d) * d, 0.0);
+    for (int i = 0; i < d; ++i) M[static_cast<size_t>(i) * d + i] = 1.0;
+    for (int k = d - 1; k >= 0; --k) {
+        const double *v = &V[static_cast<size_t>(k) * d];
+        for (int c = 0; c < d; ++c) {
+            double dot = 0.0;
+            for (int r = k; r < d; ++r) dot += v[r] * M[static_cast<size_t>(r) * d + c];
+            for (int r = k; r < d; ++r) M[static_cast<size_t>(r) * d + c] -= 2.0 * v[r] * dot;
+        }
+    }
+    for (int r = 0; r < d; ++r)
+        for (int c = 0; c < d; ++c)
+            Q[static_cast<size_t>(r) * d + c] =
+                static_cast<float>(alpha[c] < 0.0 ? -M[static_cast<size_t>(r) * d + c] : M[static_cast<size_t>(r) * d + c]);
+    return TQ_OK;
+}
+
+tq_status tq_compress_error_flag(int *flag, int reset) {
+    if (!flag) return TQ_ERR_ARG;
+    cudaError_t e = read_compress_dense_error(flag);
+    if (e == cudaSuccess && reset) e = clear_compress_dense_error();
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
 tq_status tq_make_qjl(int head_dim, int jl_dim, uint64_t seed, float *S) {
     if (!S || !pow2(head_dim) || head_dim < 16 || head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     if (jl_dim < 32 || jl_dim > 1024 || jl_dim % 32) return TQ_ERR_ARG;
-    SplitMix64 g{seed};
-    const int n = jl_dim * head_dim;
-    const double two_pi = 6.283185307179586476925;
-    for (int i = 0; i < n; i += 2) {
-        const double u1 = static_cast<double>((g.next() >> 11) + 1) * 0x1p-53;
-        const double u2 = static_cast<double>(g.next() >> 11) * 0x1p-53;
-        const double rad = std::sqrt(-2.0 * std::log(u1));
-        S[i] = static_cast<float>(rad * std::cos(two_pi * u2));
-        if (i + 1 < n) S[i + 1] = static_cast<float>(rad * std::sin(two_pi * u2));
-    }
+    fill_gaussian(seed, jl_dim * head_dim, S);
     return TQ_OK;
 }
 
@@ -706,7 +769,18 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
     }
     std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
     p.inv_sqrt_d = inv_sqrt_f32(kD);
+    p.Q = rot->dense;
     fill_thresholds(p.thr, layout->vbits, p.H, layout->value_law);
+    if (p.Q) {  // dense rotation: the tensor-core kernel (no QJL heads)
+        if (o.nq) return TQ_ERR_UNSUPPORTED;
+        if (!aligned16(p.Q)) return TQ_ERR_ALIGN;
+        const cudaError_t e = launch_compress_dense(p, static_cast<cudaStream_t>(stream));
+        if (e == cudaErrorInvalidValue) {
+            cudaGetLastError();
+            return TQ_ERR_UNSUPPORTED;  // strides TMA cannot describe
+        }
+        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    }
     const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -745,6 +819,8 @@ tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *b
         p.vbits[h] = layout->vbits[h];
     }
     if (rot) std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
+    p.Q = rot ? rot->dense : nullptr;
+    if (p.Q && !aligned16(p.Q)) return TQ_ERR_ALIGN;
     p.inv_sqrt_d = inv_sqrt_f32(kD);
     p.k_rot = k_rot;
     p.v_rot = v_rot;

@@ -44,6 +44,7 @@ struct CompressParams {
     int8_t qrank[kMaxH];         // -1: no QJL
     uint32_t sign_bits[kD / 32];
     float inv_sqrt_d;            // binary32(1/sqrt(d))
+    const float *Q;              // dense rotation (d x d, device, y = Q x) or nullptr: the SRHT of sign_bits
     float thr[kCbTotal];         // value thresholds, flat by bit width
 };
 
@@ -57,6 +58,7 @@ struct DequantParams {
     uint8_t kbits[kMaxH], vbits[kMaxH];
     uint32_t sign_bits[kD / 32];
     float inv_sqrt_d;
+    const float *Q;              // dense rotation or nullptr (SRHT)
     float *k_rot, *v_rot, *k_orig, *v_orig;
     float centroid[kCbTotal];
 };
@@ -102,6 +104,7 @@ struct alignas(16) WorkItem {
 
 struct LayerPlan {
     uint32_t sign_bits[kD / 32];
+    const float *dense;                    // dense rotation (d x d, y = Q x) or nullptr: the SRHT
     int has_qjl;
     int qjl_mode;                          // TQ_QJL_UNBIASED / TQ_QJL_SIGN_PAIR
     int n_items[kMaxH];                    // items of each KV head
@@ -110,7 +113,8 @@ struct LayerPlan {
 
 struct DecodeDims {
     int L, B, H, Hq, gqa;
-    int any_qjl;         // the prep kernel ran (QJL layers read S R q from it)
+    int any_qjl;         // QJL layers: the prep kernel writes S R q
+    int any_prep;        // the prep kernel ran (QJL or dense-rotation layers read R q from it)
     float qk_scale;      // log2(e) / sqrt(d)
     float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
 };
@@ -179,6 +183,11 @@ tq_status record_cuda_error(cudaError_t e);
 
 // Launchers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);
+// Dense rotation (p.Q set, no QJL heads): the tensor-core kernel.  Returns
+// cudaErrorInvalidValue when the input strides cannot be described to TMA.
+cudaError_t launch_compress_dense(const CompressParams &p, cudaStream_t s);
+cudaError_t read_compress_dense_error(int *flag);
+cudaError_t clear_compress_dense_error();
 cudaError_t launch_dequant(const DequantParams &p, cudaStream_t s);
 cudaError_t launch_requantize(const RequantParams &p, cudaStream_t s);
 cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,

@@ -46,7 +46,7 @@ EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rot
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
             "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag",
-            "tq_requantize", "tq_fit_codebook_sphere"]
+            "tq_requantize", "tq_fit_codebook_sphere", "tq_make_haar_rotation", "tq_compress_error_flag"]
 
 
 class TQError(RuntimeError):
@@ -60,7 +60,7 @@ class TQError(RuntimeError):
 
 class tq_rotation(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int), ("seed", ctypes.c_uint64),
-                ("sign_bits", ctypes.c_uint32 * (TQ_MAX_HEAD_DIM // 32))]
+                ("sign_bits", ctypes.c_uint32 * (TQ_MAX_HEAD_DIM // 32)), ("dense", ctypes.c_void_p)]
 
 
 class tq_segment_layout(ctypes.Structure):
@@ -100,6 +100,8 @@ _lib.tq_version.restype = _I
 _lib.tq_make_rotation.argtypes = [_I, ctypes.c_uint64, ctypes.POINTER(tq_rotation)]
 _lib.tq_fit_codebook.argtypes = [_I, _P, _P]
 _lib.tq_fit_codebook_sphere.argtypes = [_I, _I, _P, _P]
+_lib.tq_make_haar_rotation.argtypes = [_I, ctypes.c_uint64, _P]
+_lib.tq_compress_error_flag.argtypes = [ctypes.POINTER(ctypes.c_int), _I]
 _lib.tq_make_qjl.argtypes = [_I, _I, ctypes.c_uint64, _P]
 _lib.tq_packed_size.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_packed_sizes)]
 _lib.tq_compress.argtypes = [ctypes.POINTER(tq_segment_layout), ctypes.POINTER(tq_rotation), _P, _P, _P,
@@ -168,6 +170,29 @@ def tq_fit_codebook_sphere(bits: int, head_dim: int = 128):
     t = torch.zeros(max((1 << bits) - 1, 1), dtype=torch.float32)
     _check(_lib.tq_fit_codebook_sphere(bits, head_dim, c.data_ptr(), t.data_ptr()), "tq_fit_codebook_sphere")
     return c, t[: (1 << bits) - 1]
+
+
+def tq_make_haar_rotation(head_dim: int, seed: int) -> torch.Tensor:
+    """Haar-random rotation Q (float32 CPU tensor [d][d], y = Q x)."""
+    Q = torch.zeros(head_dim, head_dim, dtype=torch.float32)
+    _check(_lib.tq_make_haar_rotation(head_dim, seed, Q.data_ptr()), "tq_make_haar_rotation")
+    return Q
+
+
+def dense_rotation(rot: tq_rotation, Q: torch.Tensor) -> tq_rotation:
+    """A copy of ``rot`` that rotates with the dense matrix Q (a float32 CUDA
+    tensor [d][d] the caller keeps alive) instead of the SRHT."""
+    r = tq_rotation()
+    ctypes.pointer(r)[0] = rot
+    assert Q.dtype == torch.float32 and Q.is_contiguous() and tuple(Q.shape) == (rot.head_dim, rot.head_dim)
+    r.dense = Q.data_ptr()
+    return r
+
+
+def tq_compress_error_flag(reset: bool = False) -> int:
+    f = ctypes.c_int(0)
+    _check(_lib.tq_compress_error_flag(ctypes.byref(f), int(reset)), "tq_compress_error_flag")
+    return f.value
 
 
 def tq_make_qjl(head_dim: int, jl_dim: int, seed: int) -> torch.Tensor:

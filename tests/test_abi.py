@@ -59,6 +59,17 @@ def test_sphere_codebook_matches_oracle(tq, bits):
     assert np.array_equal(t.numpy().view(np.uint32), np.asarray(ot, np.float32).view(np.uint32))
 
 
+@pytest.mark.parametrize("d,seed", [(16, 3), (64, 7), (128, 42), (128, 1043)])
+def test_haar_rotation_matches_oracle(tq, d, seed):
+    # Householder QR here, LAPACK's through numpy in the oracle: both round the
+    # binary64 factor to binary32; allow one ulp where the two land on either
+    # side of a rounding boundary
+    Q = tq.tq_make_haar_rotation(d, seed).numpy()
+    Qo = O.haar_rotation(d, seed)
+    ulps = np.abs(Q.astype(np.float64) - Qo) / np.spacing(np.abs(Qo))
+    assert ulps.max() <= 1 and (ulps > 0).sum() <= 2
+
+
 def test_qjl_matrix_matches_oracle(tq):
     S = tq.tq_make_qjl(128, 128, 1042).numpy()
     assert np.array_equal(S, O.qjl_matrix(128, 128, 1042))
