@@ -52,6 +52,20 @@ NOMINAL_HBM_GBS = 8000.0
 DECODE_SRCS = ("tq_decode_packed.cuh", "tq_decode_common.cuh", "tq_decode.cu", "tq_internal.h")
 
 
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor peak in TFLOP/s: the measured cuBLAS bf16 burst
+    figure (fp16 runs at the same nominal rate), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        for k in ("bf16_tflops", "bf16_dense_tflops"):
+            if k in d and d[k]:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return 1900.0, "fallback"
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -254,7 +268,8 @@ def result_line(args, world, m, t, e2e, comp, config, workload):
         "compress": {"value": round(comp["mtok"], 1), "unit": "Mtok/s", "ms_per_layer": round(comp["ms"], 4),
                      "tokens_per_layer": comp["tokens"],
                      "achieved_gbs": round(comp["bytes"] / (comp["ms"] * 1e-3) / 1e9, 1),
-                     "frac_of_peak": round(comp["bytes"] / (comp["ms"] * 1e-3) / 1e9 / peak, 4)},
+                     "frac_of_peak": round(comp["bytes"] / (comp["ms"] * 1e-3) / 1e9 / peak, 4),
+                     **({"dense_rotation": comp["dense"]} if "dense" in comp else {})},
         "e2e": {"value": round(world * e2e["bytes"] / (e2e["ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["bi"], "d2h_bytes_per_step": e2e["bo"]},
         "gpu_launches": t["launches"],
@@ -308,6 +323,26 @@ def run_w2(args, rank, world, tq):
     tokens = m.n_prompt_packed * m.B
     comp = {"ms": ms, "tokens": tokens, "mtok": tokens / (ms * 1e-3) / 1e6,
             "bytes": tokens * m.H * (m.d * 2 * 2 + 16 * (m.w.kbits + m.w.vbits) + 8)}
+    # ---- the same compression with a dense Haar rotation per layer (tensor cores)
+    qd = [tq.tq_make_haar_rotation(m.d, 42 + l).cuda() for l in range(m.L)]
+    drot = [tq.dense_rotation(m.rots[l], qd[l]) for l in range(m.L)]
+    djobs = [(lambda l=l: tq.tq_compress(scratch[l % nsrc], drot[l], *src[l % nsrc])) for l in range(m.L)]
+    tq.tq_compress_error_flag(reset=True)
+    dms = time_compress(tq, djobs) / m.L
+    assert tq.tq_compress_error_flag() == 0
+    peak, _ = measured_peaks()
+    tpeak, tkind = measured_tensor_peak()
+    vec = tokens * m.H * 2                      # K and V vectors per layer
+    dflops = vec * 2 * m.d * m.d                # y = Q x: 2 d^2 per vector (the kernel issues twice that: hi + lo)
+    comp["dense"] = {"value": round(tokens / (dms * 1e-3) / 1e6, 1), "unit": "Mtok/s", "ms_per_layer": round(dms, 4),
+                     "achieved_gbs": round(comp["bytes"] / (dms * 1e-3) / 1e9, 1),
+                     "frac_of_peak": round(comp["bytes"] / (dms * 1e-3) / 1e9 / peak, 4),
+                     "tensor_tflops": round(dflops / (dms * 1e-3) / 1e12, 1),
+                     "tensor_issued_tflops": round(2 * dflops / (dms * 1e-3) / 1e12, 1),
+                     "tensor_peak": tpeak, "tensor_peak_kind": tkind,
+                     "tensor_frac_issued": round(2 * dflops / (dms * 1e-3) / 1e12 / tpeak, 4),
+                     "rotation": "Haar (QR) per layer, fp16 hi + lo on tcgen05"}
+    del qd, drot, djobs
     config = {"workload": m.w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
               "q_heads": m.Hq, "head_dim": m.d, "kbits": m.w.kbits, "vbits": m.w.vbits,
               "sinks": m.sinks, "chunk": m.chunk, "l2": "inputs larger than L2 (~0.8 GB read per step)",
@@ -397,6 +432,51 @@ def run_static(args, rank, world, tq):
               "frac_of_peak": round(rbytes / (rms * 1e-3) / 1e9 / peak, 4),
               "mtok_per_s": round(n * m.B / (rms * 1e-3) / 1e6, 1)}
         del dst, rcalls
+    mass = None
+    if w.tiers:
+        # attention mass of every cached token (the demotion signal): the same
+        # decode with a mass buffer on every segment; the difference is the
+        # mass kernel (it runs after the merges)
+        views, bufs = [], []
+        for l, segs in enumerate(m.layers):
+            for si in segs:
+                si.seg.attn_mass = torch.empty(m.B, m.H, si.seg.layout.capacity, device="cuda")
+                bufs.append(si.seg.attn_mass)
+            views.append(tq.layer_view(m.rots[l], [si.seg for si in segs]))
+            for si in segs:
+                si.seg.attn_mass = None
+        arr = tq.views_array(views)
+        ws2 = torch.empty(tq.tq_decode_workspace_size(views, m.B, m.H, m.Hq, m.d), dtype=torch.uint8, device="cuda")
+        out2 = torch.empty_like(m.out)
+        call = (lambda s: tq.tq_decode_attention(None, qpool[s % nq], out2, ws2, m.H, qjl_S=m.qjl_S, views=arr))
+        for s in range(3):
+            call(s)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for s in range(K):
+            call(s)
+        a1.record()
+        torch.cuda.synchronize()
+        ms_mass = a0.elapsed_time(a1) / K
+        ms_plain = t["ms"] / K
+        # bytes the mass kernel reads and writes: key records + scales, fp16 keys, one float out
+        mbytes = 0
+        for segs in m.layers:
+            for si in segs:
+                if si.packed:  # key record + scale (+ QJL signs and norm) + the mass
+                    mbytes += m.B * si.n * sum(16 * si.kbits[h] + 4 + (20 if si.qjl[h] else 0) + 4
+                                               for h in range(m.H))
+                else:  # fp16 key + the mass
+                    mbytes += m.B * si.n * m.H * (2 * m.d + 4)
+        peak, _ = measured_peaks()
+        extra = max(ms_mass - ms_plain, 1e-6)
+        mass = {"ms_per_step_with_mass": round(ms_mass, 4), "ms_per_step_without": round(ms_plain, 4),
+                "extra_ms": round(extra, 4), "bytes": int(mbytes),
+                "kernel_gbs_est": round(mbytes / (extra * 1e-3) / 1e9, 1),
+                "frac_of_peak_est": round(mbytes / (extra * 1e-3) / 1e9 / peak, 4),
+                "timing": "difference of two decode-call timings (CUDA events, K steps each)"}
+        del views, bufs, arr, ws2, out2
     plan = [(si.pos0, si.n, sorted(set(zip(si.kbits, si.vbits, si.qjl)))) for si in m.layers[0]]
     config = {"workload": w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
               "q_heads": m.Hq, "head_dim": m.d,
@@ -406,6 +486,8 @@ def run_static(args, rank, world, tq):
     res = result_line(args, world, m, t, e2e, comp, config, args.workload)
     if rq is not None:
         res["requantize"] = rq
+    if mass is not None:
+        res["attention_mass"] = mass
     return res
 
 
