@@ -21,6 +21,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -185,8 +187,28 @@ class ChunkedDecodeCache:
         self.views = [T.layer_view(self.rots[l], [self.sink[l], self.packed[l], self.buf[l]])
                       for l in range(self.L)]
         self.arr = T.views_array(self.views)
+        self._bind_step_fields()
         self.out = torch.empty(self.L, self.B, self.Hq, self.d, device=device)
         self.ws = torch.empty(self.max_workspace(), dtype=torch.uint8, device=device)
+
+    def _bind_step_fields(self):
+        """numpy views of the four per-step fields of every layer's view (packed
+        n_tokens, buffer n_tokens, buffer K and V pointers) inside the ctypes
+        array, so that a step updates all layers with four array stores."""
+        lv, sg = T.tq_layer_view, T.tq_segment
+        base = ctypes.addressof(self.arr)
+        raw = (ctypes.c_char * (ctypes.sizeof(lv) * self.L)).from_address(base)
+
+        def field(seg_i, fld, dtype):
+            off = lv.seg.offset + seg_i * ctypes.sizeof(sg) + getattr(sg, fld).offset
+            return np.ndarray((self.L,), dtype=dtype, buffer=raw, offset=off, strides=(ctypes.sizeof(lv),))
+        self._n_packed = field(1, "n_tokens", np.int32)
+        self._n_buf = field(2, "n_tokens", np.int32)
+        self._k_buf = field(2, "k16", np.uint64)
+        self._v_buf = field(2, "v16", np.uint64)
+        self._k_base = np.array([self.pool_k[l].data_ptr() for l in range(self.L)], np.uint64)
+        self._v_base = np.array([self.pool_v[l].data_ptr() for l in range(self.L)], np.uint64)
+        self._tok_bytes = self.d * self.pool_k[0].element_size()
 
     def max_workspace(self):
         best = 0
@@ -199,13 +221,10 @@ class ChunkedDecodeCache:
         """Point the segment views at decode step s (0-based within the pool)."""
         s %= self.steps_cap
         w0 = (s // self.chunk) * self.chunk
-        esz = self.pool_k[0].element_size()
-        for l in range(self.L):
-            seg = self.arr[l].seg
-            seg[1].n_tokens = self.n_prompt_packed + w0
-            seg[2].n_tokens = s - w0 + 1
-            seg[2].k16 = self.pool_k[l].data_ptr() + w0 * self.d * esz
-            seg[2].v16 = self.pool_v[l].data_ptr() + w0 * self.d * esz
+        self._n_packed[:] = self.n_prompt_packed + w0
+        self._n_buf[:] = s - w0 + 1
+        self._k_buf[:] = self._k_base + np.uint64(w0 * self._tok_bytes)
+        self._v_buf[:] = self._v_base + np.uint64(w0 * self._tok_bytes)
         return w0
 
     def compress_window(self, s):
