@@ -17,11 +17,11 @@
 // path.  The accumulation order of the tensor cores is not the oracle's, so a
 // code can differ where y lies within ~1e-6 of a decision boundary.
 //
-// Roles (320 threads, one CTA per SM, persistent over tiles):
-//   warps 0-7  two epilogue warpgroups; warpgroup e takes the CTA's tiles
-//              e, e + 2, ... and TMEM accumulator e
-//   warp 8     TMA producer: 3 stages of 32 KB (two 64-column boxes per tile)
-//   warp 9     TMEM allocation (256 columns) and the MMA issue
+// Roles (576 threads, one CTA per SM, persistent over tiles):
+//   warps 0-15 four epilogue warpgroups; warpgroup e takes the CTA's tiles
+//              e, e + 4, ... and TMEM accumulator e
+//   warp 16    TMA producer: 3 stages of 32 KB (two 64-column boxes per tile)
+//   warp 17    TMEM allocation (all 512 columns) and the MMA issue
 // Every wait is bounded; on a timeout the kernel sets the compress error flag,
 // lets its own copies and MMAs finish (bounded again), frees TMEM and returns.
 #include <cuda.h>
@@ -39,17 +39,19 @@ namespace {
 
 constexpr int kTile = 128;                    // tokens per tile (MMA M)
 constexpr int kStagesA = 3;
-constexpr int kEpiWarps = 8;
+constexpr int kGroups = 4;                    // epilogue warpgroups = TMEM accumulators
+constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kWarpTma = kEpiWarps, kWarpMma = kEpiWarps + 1;
 constexpr int kThreadsDense = 32 * (kEpiWarps + 2);
 constexpr int kBoxBytes = kTile * 64 * 2;     // one 64-column box: 16 KB
 constexpr int kTileBytes = 2 * kBoxBytes;     // 32 KB
 constexpr int kBBytes = 2 * 2 * kBoxBytes;    // hi and lo, two K halves each: 64 KB
-constexpr int kTmemCols = 256;                // two 128-column fp32 accumulators
+constexpr int kTmemCols = 128 * kGroups;      // one 128-column fp32 accumulator per warpgroup
 constexpr int kOffA = kBBytes;
 constexpr int kOffThr = kOffA + kStagesA * kTileBytes;
 constexpr int kOffBar = kOffThr + kCbTotal * 4 + 8;  // 8-byte aligned
 constexpr int kSmemBytes = kOffBar + 16 * 8 + 16 + 1024;  // + alignment slack
+static_assert(2 * kStagesA + 2 * kGroups <= 16, "barrier slots");
 // instruction descriptor of kind::f16: D f32 (bits 4-5 = 1), A = B = f16,
 // both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(128 >> 3) << 17) |
@@ -277,11 +279,11 @@ __global__ void __launch_bounds__(kThreadsDense, 1)
     const unsigned sB = sbase, sA = sbase + kOffA;
     float *thr = reinterpret_cast<float *>(smem + kOffThr);
     const unsigned bars = sbase + kOffBar;
-    // barriers: full[3], empty[3], tfull[2], tempty[2]
+    // barriers: full[stages], empty[stages], tfull[groups], tempty[groups]
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (kStagesA + s); };
     auto tfull = [&](int a) { return bars + 8u * (2 * kStagesA + a); };
-    auto tempty = [&](int a) { return bars + 8u * (2 * kStagesA + 2 + a); };
+    auto tempty = [&](int a) { return bars + 8u * (2 * kStagesA + kGroups + a); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + 16 * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreadsDense, 1)
             bar_init(full(s), 1);
             bar_init(empty(s), 1);
         }
-        for (int a = 0; a < 2; a++) {
+        for (int a = 0; a < kGroups; a++) {
             bar_init(tfull(a), 1);
             bar_init(tempty(a), 4 * 32);
         }
@@ -354,9 +356,9 @@ __global__ void __launch_bounds__(kThreadsDense, 1)
             long long i = 0;
             bool ok = true;
             for (; i < n_local; i++) {
-                const int s = static_cast<int>(i % kStagesA), acc = static_cast<int>(i & 1);
+                const int s = static_cast<int>(i % kStagesA), acc = static_cast<int>(i % kGroups);
                 if (!bar_wait(full(s), static_cast<unsigned>((i / kStagesA) & 1)) ||
-                    !bar_wait(tempty(acc), static_cast<unsigned>(((i >> 1) & 1) ^ 1))) {
+                    !bar_wait(tempty(acc), static_cast<unsigned>(((i / kGroups) & 1) ^ 1))) {
                     ok = false;
                     break;
                 }
@@ -379,16 +381,16 @@ __global__ void __launch_bounds__(kThreadsDense, 1)
             if (!ok) atomicExch(&g_error, 1);
             if (i > 0) {  // the last tile's MMAs have completed (a commit covers all earlier MMAs)
                 const long long j = i - 1;
-                bar_wait(tfull(static_cast<int>(j & 1)), static_cast<unsigned>((j >> 1) & 1));
+                bar_wait(tfull(static_cast<int>(j % kGroups)), static_cast<unsigned>((j / kGroups) & 1));
             }
         }
     } else {
         // ----------------------------------------------------------- epilogue
         const int e = warp >> 2, quarter = warp & 3;
         const int row = 32 * quarter + lane;
-        for (long long i = e; i < n_local; i += 2) {
+        for (long long i = e; i < n_local; i += kGroups) {
             // warp-uniform outcome: tcgen05.ld below needs the whole warp
-            if (!__all_sync(0xffffffffu, bar_wait(tfull(e), static_cast<unsigned>((i >> 1) & 1)))) {
+            if (!__all_sync(0xffffffffu, bar_wait(tfull(e), static_cast<unsigned>((i / kGroups) & 1)))) {
                 if (lane == 0) atomicExch(&g_error, 1);
                 break;
             }
