@@ -175,171 +175,6 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// ------------------------------------------------------ attention mass kernel
-// One thread per token of an item with a mass buffer: the scores of the
-// group's query heads are recomputed from the token's key record in binary32
-// (packed: the rotated query against the affine key levels, plus the QJL term
-// from the prep kernel's t = S q' words; fp16: the query against the key) and
-// normalised by the merged max and sum the decode kernels left in ws.ml.
-static_assert(kMassTokens == kThreads, "one thread per token");
-
-// largest i in [0, n) with items[i].mass_cta_begin <= cta
-__device__ __forceinline__ int find_mass_item(const WorkItem *items, int n, int cta) {
-    int lo = 0, hi = n;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (items[mid].mass_cta_begin <= cta) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
-
-// sum_i q[j][i] * code_i for the 4 query slots, codes of a KB-bit record
-template <int KB>
-__device__ __forceinline__ void mass_code_dots(const uint8_t *rec, const float (*qf)[kD], float (&dot)[kMaxGqa]) {
-    uint32_t w[4 * KB + 1];
-#pragma unroll
-    for (int i = 0; i < KB; i++) {
-        const uint4 v = reinterpret_cast<const uint4 *>(rec)[i];
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
-    }
-    w[4 * KB] = 0u;
-#pragma unroll
-    for (int i4 = 0; i4 < kD / 4; i4++) {
-        float c[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const int bit = KB * (4 * i4 + e);
-            const uint64_t win = (static_cast<uint64_t>(w[(bit >> 5) + 1]) << 32) | w[bit >> 5];
-            c[e] = static_cast<float>(static_cast<uint32_t>(win >> (bit & 31)) & ((1u << KB) - 1u));
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxGqa; j++) {
-            const float4 q = reinterpret_cast<const float4 *>(qf[j])[i4];
-            dot[j] = fmaf(q.x, c[0], fmaf(q.y, c[1], fmaf(q.z, c[2], fmaf(q.w, c[3], dot[j]))));
-        }
-    }
-}
-
-template <int KB>
-__device__ __forceinline__ void mass_packed_scores(const WorkItem &it, int b, int t, const float (*qf)[kD],
-                                                   const float *qs, float (&sc)[kMaxGqa]) {
-    float dot[kMaxGqa] = {0.f, 0.f, 0.f, 0.f};
-    mass_code_dots<KB>(it.kc + b * it.kstride + static_cast<size_t>(t) * (16 * KB), qf, dot);
-    // level(c) = c * 2^(1-KB) + 2^(-KB) - 1
-    const float m = it.ks[static_cast<size_t>(b) * it.sstride + t];
-    constexpr float alpha = 2.0f / static_cast<float>(1 << KB);
-    constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxGqa; j++) sc[j] = m * fmaf(alpha, dot[j], beta * qs[j]);
-}
-
-__global__ void __launch_bounds__(kThreads)
-    attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items) {
-    __shared__ __align__(16) float qf[kMaxGqa][kD];
-    __shared__ __align__(16) float tf[kMaxGqa][kD];
-    __shared__ float qs[kMaxGqa], ts[kMaxGqa], mx[kMaxGqa], inv_l[kMaxGqa];
-    const int idx = find_mass_item(ws.items, n_items, blockIdx.x);
-    const WorkItem &it = ws.items[idx];
-    const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;
-    const int local = blockIdx.x - it.mass_cta_begin;
-    const int b = local / nch;
-    const int t = (local - b * nch) * kMassTokens + threadIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gqa = dims.gqa;
-    const bool packed = it.kind == TQ_SEG_PACKED;
-    const size_t qrow = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + it.head * gqa + warp;
-    if (warp < kMaxGqa) {
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        float tv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (warp < gqa) {
-            load_q4(ws.q + qrow * kD, lane, x);
-            if (packed) {
-                const LayerPlan &lp = ws.layer[it.layer];
-                if (lp.dense) {  // the prep kernel's q' / 2^e (hi + lo) times 2^e
-                    const __half *qh = reinterpret_cast<const __half *>(ws.qrot + qrow * kD);
-                    const float f = ws.qsum[qrow * 4 + 2];
-#pragma unroll
-                    for (int e = 0; e < 4; e++)
-                        x[e] = (__half2float(qh[4 * lane + e]) + __half2float(qh[kD + 4 * lane + e])) * f;
-                } else {
-                    warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
-                }
-            }
-            if (packed && it.qjl) {
-                const __half *th = reinterpret_cast<const __half *>(ws.qjlt + qrow * kD);
-#pragma unroll
-                for (int e = 0; e < 4; e++)
-                    tv[e] = __half2float(th[4 * lane + e]) + __half2float(th[kD + 4 * lane + e]);
-            }
-        }
-        float sum = x[0] + x[1] + x[2] + x[3];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            qf[warp][4 * lane + e] = x[e];
-            tf[warp][4 * lane + e] = tv[e];
-        }
-        if (lane == 0) {
-            qs[warp] = sum;
-            const bool on = warp < gqa;
-            ts[warp] = on && packed && it.qjl ? ws.qsum[qrow * 4 + 1] : 0.f;
-            mx[warp] = on ? ws.ml[qrow * 2] : 0.f;
-            const float l = on ? ws.ml[qrow * 2 + 1] : 0.f;
-            inv_l[warp] = l > 0.f ? 1.0f / l : 0.f;
-        }
-    }
-    __syncthreads();
-    if (t >= it.n_tokens) return;
-    float sc[kMaxGqa] = {0.f, 0.f, 0.f, 0.f};
-    if (packed) {
-        switch (it.kb) {
-            case 1: mass_packed_scores<1>(it, b, t, qf, qs, sc); break;
-            case 2: mass_packed_scores<2>(it, b, t, qf, qs, sc); break;
-            case 3: mass_packed_scores<3>(it, b, t, qf, qs, sc); break;
-            case 4: mass_packed_scores<4>(it, b, t, qf, qs, sc); break;
-            case 5: mass_packed_scores<5>(it, b, t, qf, qs, sc); break;
-            case 6: mass_packed_scores<6>(it, b, t, qf, qs, sc); break;
-            case 7: mass_packed_scores<7>(it, b, t, qf, qs, sc); break;
-            default: mass_packed_scores<8>(it, b, t, qf, qs, sc); break;
-        }
-        if (it.qjl) {  // + sqrt(pi/2)/jl * rho * (2 sum_{bit set} t_i - sum t)
-            const size_t rq = static_cast<size_t>(b) * it.qstride + t;
-            float dot[kMaxGqa] = {0.f, 0.f, 0.f, 0.f};
-            mass_code_dots<1>(it.qs + rq * (kJl / 8), tf, dot);
-            const float g = 1.2533141373155003f / kJl * it.qn[rq];
-#pragma unroll
-            for (int j = 0; j < kMaxGqa; j++) sc[j] = fmaf(g, 2.0f * dot[j] - ts[j], sc[j]);
-        }
-    } else {
-        const uint4 *k = reinterpret_cast<const uint4 *>(it.kc + b * it.kstride + static_cast<size_t>(t) * (kD * 2));
-        float dot[kMaxGqa] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int i8 = 0; i8 < kD / 8; i8++) {
-            const uint4 v = k[i8];
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
-#pragma unroll
-                for (int j = 0; j < kMaxGqa; j++)
-                    dot[j] = fmaf(qf[j][8 * i8 + 2 * e], f.x, fmaf(qf[j][8 * i8 + 2 * e + 1], f.y, dot[j]));
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxGqa; j++) sc[j] = dot[j];
-    }
-    float mass = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxGqa; j++)
-        if (j < gqa) mass += ex2(fmaf(sc[j], dims.qk_scale, -mx[j])) * inv_l[j];
-    it.mass[static_cast<size_t>(b) * it.sstride + t] = mass / static_cast<float>(gqa);
-}
-
 PackedLauncher packed_launcher(int kb, int vb, bool qjl) {
     switch (kb) {
         case 1: return packed_launcher_kb1(vb, qjl);
@@ -420,12 +255,6 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         if (e != cudaSuccess) return e;
         first = false;
     }
-    return cudaGetLastError();
-}
-
-cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                                  cudaStream_t s) {
-    dec::attention_mass_kernel<<<n_ctas, dec::kThreads, 0, s>>>(dims, ws, n_items);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,210 @@
+// tq_mass.cu -- per-token attention mass after a decode call: the signal of
+// attention-weighted tier demotion ("TurboMOQ", "Attention-weighted tier
+// demotion": tiers follow the attention weights of each decode step).
+//
+// mass[b][h][t] = (1/g) sum over the g query heads j of KV head h of
+// 2^(s_j(t) - M_j) / L_j, with s_j(t) the base-2 score of token t and (M_j, L_j)
+// the merged running max and sum the decode kernels left in the workspace.
+//
+// Packed tokens: the scores are recomputed on the tensor cores exactly as the
+// split-K kernel computes them (key codes left at their bit offsets as fp16
+// subnormals times the fp16 hi/lo query, mma.m16n8k16, the affine key levels
+// and the QJL term applied to the raw products), so only the key records,
+// scales and sketches are read.  One CTA of 4 warps takes 128 tokens of one
+// (item, batch element); a warp takes two 16-token tiles; lane (g, c) scores
+// tokens g and g + 8 for query head c and the four heads are summed across
+// the lane quad.  fp16 tokens (sinks, newest tier, chunk buffer) are scored
+// one token per thread on the CUDA cores against the unrotated query.
+#include "tq_decode_packed.cuh"
+
+namespace tqk {
+namespace dec {
+namespace {
+
+static_assert(kMassTokens % (16 * (kThreads / 32)) == 0, "whole 16-token tiles per warp");
+constexpr int kWarpTokens = kMassTokens / (kThreads / 32);  // packed tokens per warp
+
+// largest i in [0, n) with items[i].mass_cta_begin <= cta
+__device__ __forceinline__ int find_mass_item(const WorkItem *items, int n, int cta) {
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (items[mid].mass_cta_begin <= cta) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+struct MassShared {
+    uint32_t qsh[kMaxGqa][kD];   // rotated queries / 2^e as fp16 hi, lo words (SRHT layers)
+    float qf[kMaxGqa][kD];       // unrotated queries (fp16 items)
+    float qs_sum[kMaxGqa], qs_scale[kMaxGqa], mx[kMaxGqa], inv_l[kMaxGqa];
+};
+
+// A warp's packed tokens [t0, t0 + kWarpTokens) of batch element b in
+// 16-token tiles, four per unrolled step (their loads are independent and
+// issue together, which keeps enough bytes in flight per SM).
+template <int KB, bool QJL>
+__device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const DecodeWorkspace &ws,
+                                                 const WorkItem &it, int b, int t0, size_t qbase,
+                                                 const MassShared &sh) {
+    using KU = KUnpack<KB>;
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int gqa = dims.gqa, head = g >> 1, part = g & 1;
+    // raw = (q / 2^e) . code * 2^(kA - 24); q . yhat = m (alpha q.code + beta sum q)
+    constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
+    constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
+    const bool prepared = QJL || ws.layer[it.layer].dense != nullptr;  // the prep kernel rotated q
+    uint32_t q[16], bq[16];
+    const uint32_t *qw = prepared ? ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c
+                                  : &sh.qsh[head < kMaxGqa ? head : 0][part * (kD / 2) + 16 * c];
+#pragma unroll
+    for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
+    gather_b<KU>(q, bq);
+    const float qsum = c < gqa ? (prepared ? ws.qsum[(qbase + c) * 4] : sh.qs_sum[c]) : 0.f;
+    const float aq = c < gqa ? alphaA * (prepared ? ws.qsum[(qbase + c) * 4 + 2] : sh.qs_scale[c]) : 0.f;
+    uint32_t bt[16];
+    float tsum = 0.f;
+    if constexpr (QJL) {
+        const uint32_t *tw = ws.qjlt + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
+#pragma unroll
+        for (int i = 0; i < 16; i++) q[i] = head < gqa ? tw[i] : 0u;
+        gather_b<SignUnpack>(q, bt);
+        tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
+    }
+    const float m_c = c < gqa ? sh.mx[c] : 0.f, il_c = c < gqa ? sh.inv_l[c] : 0.f;
+    const float inv_g = 1.0f / static_cast<float>(gqa);
+    const int n = it.n_tokens;
+    const uint8_t *kc = it.kc + b * it.kstride;
+    const float *ks = it.ks + static_cast<size_t>(b) * it.sstride;
+    float *mass = it.mass + static_cast<size_t>(b) * it.sstride;
+    const int t_end = min(t0 + kWarpTokens, n);
+#pragma unroll 4
+    for (int tile = t0; tile < t_end; tile += 16) {  // warp-uniform; rows up to the next multiple of 16 exist
+        const int ta = tile + g, tb = ta + 8;
+        float raw0, raw1;
+        qk_raw<KU, KB>(kc + static_cast<size_t>(ta) * (16 * KB) + 4 * KB * c,
+                       kc + static_cast<size_t>(tb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
+        float s0 = (ta < n ? ks[ta] : 0.f) * (aq * raw0 + beta * qsum);
+        float s1 = (tb < n ? ks[tb] : 0.f) * (aq * raw1 + beta * qsum);
+        if constexpr (QJL) {
+            const size_t r0 = static_cast<size_t>(b) * it.qstride;
+            float q0, q1;
+            qk_raw<SignUnpack, 1>(it.qs + (r0 + ta) * (kJl / 8) + 4 * c, it.qs + (r0 + tb) * (kJl / 8) + 4 * c, bt,
+                                  q0, q1);
+            constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
+            s0 += gam * (ta < n ? it.qn[r0 + ta] : 0.f) * (33554432.0f * q0 - tsum);
+            s1 += gam * (tb < n ? it.qn[r0 + tb] : 0.f) * (33554432.0f * q1 - tsum);
+        }
+        float p0 = c < gqa ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c : 0.f;
+        float p1 = c < gqa ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c : 0.f;
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+        if (c == 0) {
+            if (ta < n) mass[ta] = p0 * inv_g;
+            if (tb < n) mass[tb] = p1 * inv_g;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items) {
+    __shared__ __align__(16) MassShared sh;
+    const int idx = find_mass_item(ws.items, n_items, blockIdx.x);
+    const WorkItem &it = ws.items[idx];
+    const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;  // CTAs per batch element
+    const int local = blockIdx.x - it.mass_cta_begin;
+    const int b = local / nch;
+    const int tok0 = (local - b * nch) * kMassTokens;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gqa = dims.gqa;
+    const bool packed = it.kind == TQ_SEG_PACKED;
+    const size_t qbase = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + static_cast<size_t>(it.head) * gqa;
+    const LayerPlan &lp = ws.layer[it.layer];
+    if (warp < kMaxGqa) {
+        const bool on = warp < gqa;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (on) load_q4(ws.q + (qbase + warp) * kD, lane, x);
+        if (packed && !it.qjl && !lp.dense) {  // SRHT layers rotate here, as the split-K kernel does
+            warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
+            const float f = warp_pow2_norm(x);
+#pragma unroll
+            for (int e = 0; e < 4; e++) x[e] *= f;
+            const float sm = store_hilo(sh.qsh[warp], x, lane);
+            if (lane == 0) {
+                sh.qs_sum[warp] = sm / f;
+                sh.qs_scale[warp] = 1.0f / f;
+            }
+        } else if (!packed) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) sh.qf[warp][4 * lane + e] = x[e];
+        }
+        if (lane == 0) {
+            sh.mx[warp] = on ? ws.ml[(qbase + warp) * 2] : 0.f;
+            const float l = on ? ws.ml[(qbase + warp) * 2 + 1] : 0.f;
+            sh.inv_l[warp] = l > 0.f ? 1.0f / l : 0.f;
+        }
+    }
+    __syncthreads();
+    if (packed) {
+        const int t0 = tok0 + kWarpTokens * warp;
+        if (t0 >= it.n_tokens) return;
+        const bool qj = it.qjl != 0;
+#define TQ_MASS_CASE(K)                                                                \
+    case K:                                                                            \
+        if (qj) mass_packed_warp<K, true>(dims, ws, it, b, t0, qbase, sh);             \
+        else mass_packed_warp<K, false>(dims, ws, it, b, t0, qbase, sh);               \
+        break;
+        switch (it.kb) {
+            TQ_MASS_CASE(1)
+            TQ_MASS_CASE(2)
+            TQ_MASS_CASE(3)
+            TQ_MASS_CASE(4)
+            TQ_MASS_CASE(5)
+            TQ_MASS_CASE(6)
+            TQ_MASS_CASE(7)
+            default:
+                if (qj) mass_packed_warp<8, true>(dims, ws, it, b, t0, qbase, sh);
+                else mass_packed_warp<8, false>(dims, ws, it, b, t0, qbase, sh);
+                break;
+        }
+#undef TQ_MASS_CASE
+        return;
+    }
+    // fp16 tokens: one thread per token against the unrotated query
+    const int t_stop = min(tok0 + kMassTokens, it.n_tokens);
+    for (int t = tok0 + threadIdx.x; t < t_stop; t += kThreads) {
+    const uint4 *k = reinterpret_cast<const uint4 *>(it.kc + b * it.kstride + static_cast<size_t>(t) * (kD * 2));
+    float dot[kMaxGqa] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int i8 = 0; i8 < kD / 8; i8++) {
+        const uint4 v = k[i8];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
+#pragma unroll
+            for (int j = 0; j < kMaxGqa; j++)
+                dot[j] = fmaf(sh.qf[j][8 * i8 + 2 * e], f.x, fmaf(sh.qf[j][8 * i8 + 2 * e + 1], f.y, dot[j]));
+        }
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxGqa; j++)
+        if (j < gqa) m += ex2(fmaf(dot[j], dims.qk_scale, -sh.mx[j])) * sh.inv_l[j];
+    it.mass[static_cast<size_t>(b) * it.sstride + t] = m / static_cast<float>(gqa);
+    }
+}
+
+}  // namespace
+}  // namespace dec
+
+cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
+                                  cudaStream_t s) {
+    dec::attention_mass_kernel<<<n_ctas, dec::kThreads, 0, s>>>(dims, ws, n_items);
+    return cudaGetLastError();
+}
+
+}  // namespace tqk

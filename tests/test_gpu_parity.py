@@ -306,7 +306,7 @@ MASS_CASES = [
     (1, 3, 4, 8, [("packed", 200, [1, 2, 3, 4], [1, 2, 3, 4], [1, 1, 0, 0]),
                   ("packed", 129, [5, 6, 7, 8], [8, 7, 6, 5], None), ("fp16", 0)]),
     (1, 1, 8, 8, [("packed", 333, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], None, 1)]),
-    (1, 2, 8, 16, [("fp16", 128), ("packed", 1000, [3] * 8, [3] * 8, None), ("fp16", 37)]),
+    (1, 2, 8, 16, [("fp16", 1100), ("packed", 2100, [3] * 8, [3] * 8, None), ("fp16", 37)]),
 ]
 
 
