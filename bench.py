@@ -362,14 +362,9 @@ def run_static(args, rank, world, tq):
     pb, ob = m.step_bytes()
     torch.cuda.synchronize()
 
-    # launches per step: the QJL query prep (if any), the fp16 kernel (if any
-    # fp16 segment), one persistent kernel per packed (kbits, vbits, QJL) class
-    n_launch = (1 if w.qjl_max_bits else 0) + int(any(not si.packed for segs in m.layers for si in segs)) + len(
-        {(si.kbits[h], si.vbits[h], si.qjl[h]) for segs in m.layers for si in segs if si.packed for h in range(m.H)})
-
-    def step(s):
+    def step(s):  # returns the kernel launches the library reports for the call
         m.decode(qpool[s % nq])
-        return n_launch
+        return tq.tq_decode_last_launches()
     t = timed_region(tq, step, lambda s: (pb, pb + ob), K, Wm, world, dev)
 
     # ---- e2e: queries from pinned host memory, output back to host

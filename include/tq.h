@@ -325,6 +325,10 @@ tq_status tq_decode_error_flag(const void *workspace, int *flag, void *stream);
  * caller; no effect on results. */
 tq_status tq_set_decode_kernel_events(void *start, void *stop);
 
+/* Kernel launches the calling thread's last decode call made (query prep,
+ * split-K grids, attention mass), for callers that account for them. */
+int tq_decode_last_launches(void);
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention without a caller-supplied workspace.  (No counterpart on   */
 /* the pages: this entry point exists for callers, not for the method.)        */

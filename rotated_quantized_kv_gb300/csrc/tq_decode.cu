@@ -195,7 +195,8 @@ PackedLauncher packed_launcher(int kb, int vb, bool qjl) {
 cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,
                                   int n_classes, const float *S, const unsigned short *const *value_half,
                                   const float *value_c1,
-                                  cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+                                  cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop, int *n_launched) {
+    *n_launched = 0;
     static bool configured = false;
     const size_t smem16 = static_cast<size_t>(dec::kStage16Bytes) + 16;
     if (!configured) {
@@ -220,6 +221,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         const int n_warps = dims.L * dims.B * dims.Hq;
         dec::decode_prep_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
         first = false;
+        ++*n_launched;
     }
     bool any_packed = false;
     for (int i = 0; i < n_classes; i++) any_packed |= classes[i].kb != 16 && classes[i].n_ctas > 0;
@@ -236,6 +238,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
             fn(dims, ws, c.item_lo, c.item_hi, c.n_ctas, c.n_stages, value_half[i], value_c1[i], s, !first);
         if (e != cudaSuccess) return e;
         first = false;
+        ++*n_launched;
     }
     if (ev_stop && any_packed) {
         cudaEventRecord(ev_stop, s);
@@ -253,6 +256,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         cfg.numAttrs = first ? 0 : 1;
         const cudaError_t e = cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel, dims, ws, c.item_lo, c.item_hi);
         if (e != cudaSuccess) return e;
+        ++*n_launched;
         first = false;
     }
     return cudaGetLastError();

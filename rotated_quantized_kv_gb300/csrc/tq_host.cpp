@@ -18,6 +18,10 @@ namespace {
 
 thread_local int g_last_cuda = 0;
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+thread_local int g_last_launches_v = 0;
+struct LaunchCounter {
+    void store(int v) { g_last_launches_v = v; }
+} g_last_launches;
 
 tq_status cuda_fail(cudaError_t e) {
     g_last_cuda = static_cast<int>(e);
@@ -1046,10 +1050,14 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (P.items.empty()) return TQ_OK;
+    int launched = 0;
     e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S,
-                              class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop);
-    if (e == cudaSuccess && P.mass_ctas > 0)
+                              class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop, &launched);
+    if (e == cudaSuccess && P.mass_ctas > 0) {
         e = launch_attention_mass(P.dims, W, static_cast<int>(P.items.size()), P.mass_ctas, s);
+        ++launched;
+    }
+    g_last_launches.store(launched);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
@@ -1060,6 +1068,8 @@ tq_status tq_decode_error_flag(const void *workspace, int *flag, void *stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
+
+int tq_decode_last_launches(void) { return g_last_launches_v; }
 
 tq_status tq_set_decode_kernel_events(void *start, void *stop) {
     if ((start == nullptr) != (stop == nullptr)) return TQ_ERR_ARG;

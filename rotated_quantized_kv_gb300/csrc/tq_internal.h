@@ -193,7 +193,7 @@ cudaError_t launch_requantize(const RequantParams &p, cudaStream_t s);
 cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace &ws, const ClassLaunch *classes,
                                   int n_classes, const float *S, const unsigned short *const *value_half,
                                   const float *value_c1,
-                                  cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop);
+                                  cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop, int *n_launched);
 // Attention mass of every item with a mass pointer (items [0, n_items) of the
 // plan, n_ctas CTAs in all), after the decode kernels of the call.
 cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,

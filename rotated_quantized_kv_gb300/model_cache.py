@@ -244,7 +244,7 @@ class ChunkedDecodeCache:
         self.set_step(s)
         qq = self.qpool[s % self.steps_cap] if q is None else q
         T.tq_decode_attention(None, qq, self.out, self.ws, self.H, views=self.arr)
-        return launches + 2  # split-K over fp16 segments, split-K over packed segments
+        return launches + T.tq_decode_last_launches()
 
     def step_bytes(self, s):
         s %= self.steps_cap

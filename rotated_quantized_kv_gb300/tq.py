@@ -46,7 +46,7 @@ EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rot
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
             "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag",
-            "tq_requantize", "tq_fit_codebook_sphere", "tq_make_haar_rotation", "tq_compress_error_flag"]
+            "tq_requantize", "tq_fit_codebook_sphere", "tq_make_haar_rotation", "tq_compress_error_flag", "tq_decode_last_launches"]
 
 
 class TQError(RuntimeError):
@@ -97,6 +97,8 @@ _lib.tq_status_string.restype = ctypes.c_char_p
 _lib.tq_status_string.argtypes = [_I]
 _lib.tq_last_cuda_error.restype = _I
 _lib.tq_version.restype = _I
+_lib.tq_decode_last_launches.restype = _I
+_lib.tq_decode_last_launches.argtypes = []
 _lib.tq_make_rotation.argtypes = [_I, ctypes.c_uint64, ctypes.POINTER(tq_rotation)]
 _lib.tq_fit_codebook.argtypes = [_I, _P, _P]
 _lib.tq_fit_codebook_sphere.argtypes = [_I, _I, _P, _P]
@@ -122,7 +124,7 @@ _lib.tq_decode_attention_static.argtypes = [ctypes.POINTER(tq_layer_view), _I, _
                                             _P, _P]
 TQ_STATIC_WORKSPACE_BYTES = 16 << 20
 for _n in EXPORTED:
-    if _n not in ("tq_status_string", "tq_last_cuda_error", "tq_version"):
+    if _n not in ("tq_status_string", "tq_last_cuda_error", "tq_version", "tq_decode_last_launches"):
         getattr(_lib, _n).restype = _I
 
 
@@ -365,6 +367,11 @@ def tq_decode_attention(layers, q: torch.Tensor, out: torch.Tensor, workspace: t
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "tq_decode_attention")
     return out
+
+
+def tq_decode_last_launches() -> int:
+    """Kernel launches this thread's last decode call made."""
+    return _lib.tq_decode_last_launches()
 
 
 def tq_set_decode_kernel_events(start=None, stop=None):
