@@ -355,7 +355,7 @@ def run_static(args, rank, world, tq):
     dev = torch.cuda.current_device()
     w = W.WORKLOADS[args.workload]
     seed = 1000 + int(args.workload[1:])
-    m = StaticCache(w, batch=args.batch, context=args.context, seed=seed)
+    m = StaticCache(w, batch=args.batch, context=args.context, seed=seed, rotation=args.rotation)
     K, Wm = args.steps, args.warmup
     nq = 4
     qpool = W.query_pool(w, nq, m.B, seed, device="cuda")
@@ -476,6 +476,7 @@ def run_static(args, rank, world, tq):
     config = {"workload": w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
               "q_heads": m.Hq, "head_dim": m.d,
               "segments_layer0": [{"pos0": p, "n": n, "k_v_qjl": [list(x) for x in kb]} for p, n, kb in plan],
+              "rotation": args.rotation,
               "l2": f"inputs larger than L2 ({(pb + ob) / 1e9:.2f} GB read per step)",
               "parallelism": f"replicas x{world}"}
     res = result_line(args, world, m, t, e2e, comp, config, args.workload)
@@ -491,6 +492,8 @@ def run_ours(args, rank, world):
     build.build()
     from rotated_quantized_kv_gb300 import tq
     if args.workload == "w2":
+        if args.rotation != "srht":
+            raise SystemExit("--rotation haar applies to the static workloads (w1, w3, w5)")
         res = run_w2(args, rank, world, tq)
         wl = W.WORKLOADS["w2"]
     else:
@@ -605,6 +608,8 @@ def main():
                     help="w2 (default): the chunked decode workload the metric is quoted on; "
                          "w1, w3, w4, w5: decode steps over a prompt compressed once")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (w1, w3-w5)")
+    ap.add_argument("--rotation", default="srht", choices=["srht", "haar"],
+                    help="haar: a dense Haar rotation per layer (tensor-core compressor; w1, w3, w5)")
     ap.add_argument("--context", type=int, default=None, help="override the workload's context (w1, w3-w5)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -88,18 +88,26 @@ class StaticCache:
     """A prompt of `context` positions compressed once per layer (workloads 1, 3, 4, 5)."""
 
     def __init__(self, w: W.Workload, batch: int | None = None, context: int | None = None, seed: int = 1000,
-                 device="cuda", sample_inputs=None):
+                 device="cuda", sample_inputs=None, rotation: str = "srht"):
         """sample_inputs(layer, K, V), if given, sees each layer's fp16 inputs
-        ([B][H][T][d] CUDA tensors) before they are dropped."""
+        ([B][H][T][d] CUDA tensors) before they are dropped.  rotation: "srht"
+        (D H D / sqrt(d)) or "haar" (a dense Haar matrix per layer, seed + l;
+        no QJL heads)."""
+        assert rotation in ("srht", "haar")
+        if rotation == "haar" and w.qjl_max_bits:
+            raise ValueError("the dense-rotation compressor takes no QJL heads")
         self.w = w
         self.L, self.H, self.Hq, self.d = w.layers, w.kv_heads, w.q_heads, w.head_dim
         self.B = batch or w.batch
         self.T = context or w.context
         self.seed = seed
         self.qjl_S = T.tq_make_qjl(self.d, 128, W.QJL_SEED).to(device) if w.qjl_max_bits else None
-        self.rots, self.layers, self.views = [], [], []
+        self.rots, self.layers, self.views, self.dense_q = [], [], [], []
         for l in range(self.L):
             rot = T.tq_make_rotation(self.d, W.ROTATION_SEED + l)
+            if rotation == "haar":
+                self.dense_q.append(T.tq_make_haar_rotation(self.d, W.ROTATION_SEED + l).to(device))
+                rot = T.dense_rotation(rot, self.dense_q[-1])
             K, V = W.kv_block(w, l, self.B, self.T, seed, device=device)
             segs = []
             for pos0, n, kb, vb, qj in plan_segments(w, self.T, l):
