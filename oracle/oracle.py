@@ -60,6 +60,7 @@ class _Segment(ctypes.Structure):
         ("kbits", _P), ("vbits", _P), ("qjl", _P),
         ("kcodes", _P), ("vcodes", _P), ("kscale", _P), ("vscale", _P),
         ("qjl_signs", _P), ("qjl_norm", _P), ("k16", _P), ("v16", _P), ("value_law", _I),
+        ("qjl_v", _P), ("vqjl_signs", _P), ("vqjl_norm", _P),
     ]
 
 
@@ -86,7 +87,7 @@ def lib() -> ctypes.CDLL:
     L.tqo_qjl_project.argtypes = [_I, _I, _P, _P, _P]
     L.tqo_qjl_sketch.argtypes = [_I, _I, _P, _P, _P, _P, _P]
     L.tqo_compress.argtypes = [_I, _I, _I, _I, _P, _P, _LL, _LL, _LL, _P, _P, _P, _I,
-                               ctypes.POINTER(_Segment), _I, _P]
+                               ctypes.POINTER(_Segment), _I, _P, _P]
     L.tqo_rotate_dense_f32.argtypes = [_I, _P, _P, _P]
     L.tqo_dequant.argtypes = [_I, _I, ctypes.POINTER(_Segment), _I, _I, _I, _I, _P, _P, _P]
     L.tqo_decode_attention.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_Segment), _P, _P,
@@ -312,7 +313,7 @@ class PackedSegment:
 
     kind = 0
 
-    def __init__(self, B, H, d, capacity, kbits, vbits, qjl=None, jl=128, n_tokens=0, law=0):
+    def __init__(self, B, H, d, capacity, kbits, vbits, qjl=None, jl=128, n_tokens=0, law=0, qjl_v=None):
         self.B, self.H, self.d, self.capacity, self.jl = B, H, d, capacity, jl
         self.law = law  # value codebook: 0 Gaussian, 1 sphere coordinate (d = 128)
         assert law in (0, 1) and (law == 0 or d == 128)
@@ -330,6 +331,12 @@ class PackedSegment:
         self.vscale = np.zeros(B * H * capacity, np.float32)
         self.qjl_signs = np.zeros(max(B * nq * capacity * (jl // 8), 1), np.uint8)
         self.qjl_norm = np.zeros(max(B * nq * capacity, 1), np.float32)
+        # QJL on values: the value residual's sketch, heads ranked like the keys'
+        self.qjl_v = _c(np.zeros(H) if qjl_v is None else qjl_v, np.uint8)
+        nv = int(self.qjl_v.astype(bool).sum())
+        self.nv = nv
+        self.vqjl_signs = np.zeros(max(B * nv * capacity * (jl // 8), 1), np.uint8)
+        self.vqjl_norm = np.zeros(max(B * nv * capacity, 1), np.float32)
 
     def code_offset(self, which: str, b: int, h: int, t: int) -> int:
         bits = self.kbits if which == "k" else self.vbits
@@ -338,6 +345,9 @@ class PackedSegment:
 
     def qjl_rank(self, h: int) -> int:
         return int(self.qjl[:h].astype(bool).sum())
+
+    def vqjl_rank(self, h: int) -> int:
+        return int(self.qjl_v[:h].astype(bool).sum())
 
     def c_struct(self) -> _Segment:
         s = _Segment()
@@ -348,6 +358,7 @@ class PackedSegment:
         s.qjl_signs, s.qjl_norm = _ptr(self.qjl_signs), _ptr(self.qjl_norm)
         s.k16 = s.v16 = None
         s.value_law = self.law
+        s.qjl_v, s.vqjl_signs, s.vqjl_norm = _ptr(self.qjl_v), _ptr(self.vqjl_signs), _ptr(self.vqjl_norm)
         return s
 
 
@@ -377,13 +388,13 @@ def compress(seg: PackedSegment, K: np.ndarray, V: np.ndarray, sign: np.ndarray,
     Vb = _c(np.asarray(V).view(np.uint16) if np.asarray(V).dtype == np.float16 else V, np.uint16)
     B, H, T, d = Kb.shape
     assert (B, H, d) == (seg.B, seg.H, seg.d) and t_begin + T <= seg.capacity
-    _, _, _, tp = _cent_thr_tables()
+    _, _, cp, tp = _cent_thr_tables()
     s = _c(sign, np.int8)
     Sm = None if S is None else _c(S, np.float32)
     cs = seg.c_struct()
     Qm = None if Q is None else _c(Q, np.float32)
     lib().tqo_compress(B, H, d, T, _ptr(Kb), _ptr(Vb), H * T * d, T * d, d, _ptr(s), tp,
-                       _ptr(Sm), seg.jl, ctypes.byref(cs), t_begin, _ptr(Qm))
+                       _ptr(Sm), seg.jl, ctypes.byref(cs), t_begin, _ptr(Qm), cp)
     seg.n_tokens = max(seg.n_tokens, t_begin + T)
 
 
@@ -402,7 +413,7 @@ def requantize(src: PackedSegment, src_t0: int, n: int, dst: PackedSegment, dst_
     rotated space, compressed again with dst's widths into [dst_t0, dst_t0 + n)
     of dst (no QJL on dst)."""
     assert (src.B, src.H, src.d) == (dst.B, dst.H, dst.d)
-    assert src_t0 + n <= src.capacity and dst_t0 + n <= dst.capacity and not dst.qjl.any()
+    assert src_t0 + n <= src.capacity and dst_t0 + n <= dst.capacity and not dst.qjl.any() and not dst.qjl_v.any()
     _, _, cp, tp = _cent_thr_tables()
     ss, ds = src.c_struct(), dst.c_struct()
     lib().tqo_requantize(src.B, src.H, src.d, ctypes.byref(ss), src_t0, n, cp, tp, ctypes.byref(ds), dst_t0)

@@ -465,6 +465,13 @@ typedef struct {
     float *qjl_norm;
     uint16_t *k16, *v16;
     int value_law; /* value codebook: 0 Gaussian, 1 sphere coordinate (tables [law * 9 + bits]) */
+    /* QJL on values: heads with qjl_v[h] != 0 also sketch the value residual,
+     * ranked v(h) = #{h' < h : qjl_v[h']}, nv of them, records at
+     * vqjl_signs byte offset ((b*nv + v(h))*cap + t) * jl/8 and norms at
+     * vqjl_norm index (b*nv + v(h))*cap + t (NULL qjl_v: none) */
+    const uint8_t *qjl_v;
+    uint8_t *vqjl_signs;
+    float *vqjl_norm;
 } tqo_segment;
 
 static size_t off_codes(const uint8_t *bits, int H, int d, int cap, int b, int h, int t) {
@@ -483,16 +490,24 @@ static int qjl_rank(const uint8_t *qjl, int h) {
     return r;
 }
 
+static int vqjl_rank(const tqo_segment *seg, int h) {
+    int r = 0;
+    for (int i = 0; i < h; i++) r += seg->qjl_v && seg->qjl_v[i] ? 1 : 0;
+    return r;
+}
+
 /* Compress T tokens of K and V (fp16 bit patterns, element strides sb, sh, st,
  * unit stride along d) into token positions [t_begin, t_begin + T) of a packed
  * segment.  thr[law * 9 + b] points at the 2^b - 1 binary32 value thresholds for
  * b bits of codebook law `law` (0 Gaussian, 1 sphere coordinate).
  * S is the QJL matrix (jl x d) or NULL when no head uses QJL.
- * Q: NULL for the SRHT of `sign`, else the dense rotation (d x d, y = Q x). */
+ * Q: NULL for the SRHT of `sign`, else the dense rotation (d x d, y = Q x).
+ * Value heads with qjl_v set sketch r = y - sigma*cent[code] (binary32 product
+ * and difference, cent[law * 9 + b] the binary32 centroids) like the keys. */
 void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t *V,
                   long long sb, long long sh, long long st, const int8_t *sign,
                   const float *const *thr, const float *S, int jl,
-                  const tqo_segment *seg, int t_begin, const float *Q) {
+                  const tqo_segment *seg, int t_begin, const float *Q, const float *const *cent) {
     float x[TQO_MAX_D], y[TQO_MAX_D], yhat[TQO_MAX_D];
     uint8_t code[TQO_MAX_D];
     const int nq = qjl_rank(seg->qjl, H);
@@ -525,6 +540,14 @@ void tqo_compress(int B, int H, int d, int T, const uint16_t *K, const uint16_t 
                 tqo_quant_value(d, vb, y, thr[seg->value_law * 9 + vb], code, &sg);
                 tqo_pack(d, vb, code, seg->vcodes + off_codes(seg->vbits, H, d, seg->capacity, b, h, pos));
                 seg->vscale[sidx] = sg;
+                if (seg->qjl_v && seg->qjl_v[h]) {
+                    const float *c = cent[seg->value_law * 9 + vb];
+                    for (int i = 0; i < d; i++) yhat[i] = sg * c[code[i]];
+                    int nv = 0;
+                    for (int i = 0; i < H; i++) nv += seg->qjl_v[i] ? 1 : 0;
+                    const size_t q = ((size_t)b * nv + vqjl_rank(seg, h)) * seg->capacity + pos;
+                    tqo_qjl_sketch(jl, d, S, y, yhat, seg->vqjl_signs + q * (jl / 8), &seg->vqjl_norm[q]);
+                }
             }
 }
 
@@ -670,6 +693,17 @@ void tqo_decode_attention(int B, int H, int Hq, int d, int n_seg, const tqo_segm
                         tqo_unpack(d, vb, sg->vcodes + off_codes(sg->vbits, H, d, sg->capacity, b, h, t), code);
                         for (int i = 0; i < d; i++)
                             yv[i] = (double)sg->vscale[sidx] * (double)cent[sg->value_law * 9 + vb][code[i]];
+                        if (sg->qjl_v && sg->qjl_v[h]) {  /* + sqrt(pi/2)/jl rho S^T s (the unbiased estimate of r) */
+                            int nv = 0;
+                            for (int i = 0; i < H; i++) nv += sg->qjl_v[i] ? 1 : 0;
+                            const size_t qi = ((size_t)b * nv + vqjl_rank(sg, h)) * sg->capacity + t;
+                            const uint8_t *sb = sg->vqjl_signs + qi * (jl / 8);
+                            const double coef = sqrt(TQO_PI / 2.0) / jl * (double)sg->vqjl_norm[qi];
+                            for (int jj = 0; jj < jl; jj++) {
+                                const double sj = ((sb[jj >> 3] >> (jj & 7)) & 1) ? 1.0 : -1.0;
+                                for (int i = 0; i < d; i++) yv[i] += coef * sj * (double)S[(size_t)jj * d + i];
+                            }
+                        }
                         if (Q) tqo_rotate_dense_f64(d, Q, 1, yv, v);
                         else tqo_rotate_f64(d, sign, yv, v);
                     }
