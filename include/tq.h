@@ -137,6 +137,9 @@ typedef struct {
     uint8_t value_law;           /* value codebook: TQ_VALUE_LAW_GAUSS or TQ_VALUE_LAW_SPHERE
                                   * (the latter fitted for d = 128); anything else is
                                   * TQ_ERR_ARG */
+    uint8_t qjl_v[TQ_MAX_HEADS]; /* per head, 0/1: 1-bit sketch of the value residual
+                                  * y - sigma c[code] (same S and jl_dim as the keys);
+                                  * decode adds sqrt(pi/2)/jl ||r|| S^T s to the value */
 } tq_segment_layout;
 
 /* Value codebook laws (the Lloyd-Max quantizer of u = y / RMS(y)):
@@ -156,12 +159,16 @@ typedef struct {
  *   kscale / vscale (float) index (b*H + h)*cap + t  (key: max|y|, value: RMS);
  *   QJL heads ranked q(h) = #{h' < h : qjl[h']}, nq of them: qjl_signs byte
  *   offset ((b*nq + q(h))*cap + t)*jl/8 (bit j LSB-first = sign of (S r)_j >= 0),
- *   qjl_norm (float, ||r||_2) index (b*nq + q(h))*cap + t. */
+ *   qjl_norm (float, ||r||_2) index (b*nq + q(h))*cap + t;
+ *   value sketches likewise with v(h) = #{h' < h : qjl_v[h']}, nv of them:
+ *   vqjl_signs byte offset ((b*nv + v(h))*cap + t)*jl/8, vqjl_norm index
+ *   (b*nv + v(h))*cap + t. */
 typedef struct {
     size_t kcode_bytes, vcode_bytes, kscale_bytes, vscale_bytes, qjl_sign_bytes, qjl_norm_bytes;
+    size_t vqjl_sign_bytes, vqjl_norm_bytes;
 } tq_packed_sizes;
 
-/* Sizes of the six device buffers of a packed segment.  TQ_ERR_ARG on an
+/* Sizes of the device buffers of a packed segment.  TQ_ERR_ARG on an
  * invalid layout (bits outside 1..8, H outside 1..16, capacity < 0, ...). */
 tq_status tq_packed_size(const tq_segment_layout *layout, tq_packed_sizes *sizes);
 
@@ -170,6 +177,8 @@ typedef struct {
     float *kscale, *vscale;  /* device */
     void *qjl_signs;         /* device, may be NULL when no head uses QJL */
     float *qjl_norm;         /* device, may be NULL when no head uses QJL */
+    void *vqjl_signs;        /* device, may be NULL when no head sketches its values */
+    float *vqjl_norm;        /* device, may be NULL when no head sketches its values */
 } tq_packed_bufs;
 
 /* ------------------------------------------------------------------------ */
@@ -180,7 +189,7 @@ typedef struct {
  * 16-byte aligned).  Compresses n_tokens tokens into positions
  * [t_begin, t_begin + n_tokens) of the packed segment (chunked compression
  * appends with t_begin = tokens already stored).  qjl_S: device jl_dim x
- * head_dim floats from tq_make_qjl, required iff some qjl[h] is set.
+ * head_dim floats from tq_make_qjl, required iff some qjl[h] or qjl_v[h] is set.
  * All arithmetic is IEEE binary32 in a fixed order, so the codes are a pure
  * function of the input:
  *   y = binary32(1/sqrt(d)) * D (butterflies h = 1, 2, ..., d/2 of D x);
@@ -188,13 +197,15 @@ typedef struct {
  *         0, 2^b - 1);
  *   values: sigma = sqrt(pairwise-tree sum of y_i^2 / d), r = 1/sigma (0 if 0),
  *         code = #{k : thr_k < y r};
- *   QJL: r_i = y_i - m*((code+1/2) 2^(1-b) - 1), sign bits of S r, ||r||_2.
+ *   QJL: r_i = y_i - m*((code+1/2) 2^(1-b) - 1), sign bits of S r, ||r||_2;
+ *   value QJL: r_i = y_i - sigma*c[code] (binary32 product and difference, c
+ *         the binary32 centroids), sign bits of S r, ||r||_2.
  * With a dense rotation (rot->dense) y = Q x runs on the tensor cores: x fp16
  * times Q carried as two fp16 parts (~2^-22), binary32 accumulation in an order
  * the hardware chooses, so a code can differ from the exact product's where y
  * lies within ~1e-6 of a decision boundary; the scales and quantizers are the
- * ones above.  Dense rotation with QJL heads, or strides TMA cannot describe,
- * return TQ_ERR_UNSUPPORTED.
+ * ones above.  Dense rotation with QJL (key or value) heads, or strides TMA
+ * cannot describe, return TQ_ERR_UNSUPPORTED.
  * Returns TQ_ERR_SIZE if t_begin + n_tokens > capacity. */
 tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot,
                       const float *qjl_S, const void *K, const void *V, int n_tokens,
@@ -210,8 +221,8 @@ tq_status tq_compress_error_flag(int *flag, int reset);
  * k_rot / v_rot (device floats [B][H][n_tokens][d], either may be NULL): the
  * rotated-space values binary32(m * level(code)) and binary32(sigma *
  * centroid[code]).  k_orig / v_orig (may be NULL): the original-space vectors
- * R applied to those (binary32; keys include no QJL term).  A debugging and
- * parity aid: decode attention never materialises these. */
+ * R applied to those (binary32; neither includes a QJL term).  A debugging
+ * and parity aid: decode attention never materialises these. */
 tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *bufs,
                         const tq_rotation *rot, int t_begin, int n_tokens, float *k_rot,
                         float *v_rot, float *k_orig, float *v_orig, void *stream);
@@ -223,8 +234,8 @@ tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *b
  * of `dst` into its positions [dst_t_begin, dst_t_begin + n): the same
  * per-vector scales and quantizers as tq_compress, applied to the
  * reconstruction, with no rotation either way.  Both segments must have the
- * same batch, heads and head_dim; dst must carry no QJL heads
- * (TQ_ERR_UNSUPPORTED); the two segments' buffers must not overlap.  Any
+ * same batch, heads and head_dim; dst must carry no QJL heads, key or value
+ * (TQ_ERR_UNSUPPORTED; a source's sketches are not carried over); the two segments' buffers must not overlap.  Any
  * widths 1..8 are accepted (demotion normally lowers them).  TQ_ERR_SIZE if a
  * range exceeds its capacity. */
 tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_bufs, int src_t_begin,

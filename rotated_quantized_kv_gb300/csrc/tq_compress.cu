@@ -156,6 +156,57 @@ __device__ __forceinline__ uint32_t search_smem(float u, const float *t) {
     return k;
 }
 
+// Sketch of a residual held by four lanes (this lane's coordinates [32 q,
+// 32 q + 32) in r): p_j = sum_i S[j][i] r_i in binary32 (any order: the only
+// decision is the sign); bit j = (p_j >= 0); rho = ||r||_2.  Each lane forms
+// the partial sum over its 32 coordinates, the four lanes add them, and lane q
+// keeps the signs of projections [32 q, 32 q + 32).
+__device__ __forceinline__ void qjl_sketch(const float *S, const float (&y)[kQ], int q, bool store, uint8_t *rec,
+                                           float *norm) {
+    {
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kQ; i++) ss = fmaf(y[i], y[i], ss);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        uint32_t mine = 0;
+#pragma unroll 1
+        for (int jc = 0; jc < 4; jc++) {  // projections 32 jc .. 32 jc + 31
+            uint32_t word = 0;
+#pragma unroll 1
+            for (int jj = 0; jj < 32; jj += 2) {  // two projections, four partial sums each
+                const float4 *S0 = reinterpret_cast<const float4 *>(S + (32 * jc + jj) * kD + q * kQ);
+                const float4 *S1 = S0 + kD / 4;
+                float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i4 = 0; i4 < kQ / 4; i4++) {
+                    const float4 s = __ldg(S0 + i4), t = __ldg(S1 + i4);
+                    const int e = i4 & 3;
+                    a0[e] = fmaf(s.x, y[4 * i4], a0[e]);
+                    a0[e] = fmaf(s.y, y[4 * i4 + 1], a0[e]);
+                    a0[e] = fmaf(s.z, y[4 * i4 + 2], a0[e]);
+                    a0[e] = fmaf(s.w, y[4 * i4 + 3], a0[e]);
+                    a1[e] = fmaf(t.x, y[4 * i4], a1[e]);
+                    a1[e] = fmaf(t.y, y[4 * i4 + 1], a1[e]);
+                    a1[e] = fmaf(t.z, y[4 * i4 + 2], a1[e]);
+                    a1[e] = fmaf(t.w, y[4 * i4 + 3], a1[e]);
+                }
+                float p0 = (a0[0] + a0[1]) + (a0[2] + a0[3]), p1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+                p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+                p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+                word |= ((p0 >= 0.0f ? 1u : 0u) << jj) | ((p1 >= 0.0f ? 1u : 0u) << (jj + 1));
+            }
+            if (jc == q) mine = word;
+        }
+        if (store) {
+            reinterpret_cast<uint32_t *>(rec)[q] = mine;
+            if (q == 0) *norm = sqrtf(ss);
+        }
+    }
+}
+
 // Quantize and store one key vector held by four lanes (this lane's rotated
 // coordinates [32 q, 32 q + 32) in y); `store` is false for rows past the
 // block's end (the lanes still run so that their exchanges stay warp-uniform).
@@ -195,58 +246,21 @@ __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ]
         if (q == 0) p.kscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = m;
     }
     if constexpr (QJL) {
-        // p_j = sum_i S[j][i] r_i in binary32 (any order: the only decision is the
-        // sign); bit j = (p_j >= 0).  rho = ||r||_2.  Each lane forms the partial
-        // sum over its 32 coordinates, the four lanes add them, and lane q keeps
-        // the signs of projections [32 q, 32 q + 32).
-        float ss = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kQ; i++) ss = fmaf(y[i], y[i], ss);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        uint32_t mine = 0;
-#pragma unroll 1
-        for (int jc = 0; jc < 4; jc++) {  // projections 32 jc .. 32 jc + 31
-            uint32_t word = 0;
-#pragma unroll 1
-            for (int jj = 0; jj < 32; jj += 2) {  // two projections, four partial sums each
-                const float4 *S0 = reinterpret_cast<const float4 *>(p.S + (32 * jc + jj) * kD + q * kQ);
-                const float4 *S1 = S0 + kD / 4;
-                float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int i4 = 0; i4 < kQ / 4; i4++) {
-                    const float4 s = __ldg(S0 + i4), t = __ldg(S1 + i4);
-                    const int e = i4 & 3;
-                    a0[e] = fmaf(s.x, y[4 * i4], a0[e]);
-                    a0[e] = fmaf(s.y, y[4 * i4 + 1], a0[e]);
-                    a0[e] = fmaf(s.z, y[4 * i4 + 2], a0[e]);
-                    a0[e] = fmaf(s.w, y[4 * i4 + 3], a0[e]);
-                    a1[e] = fmaf(t.x, y[4 * i4], a1[e]);
-                    a1[e] = fmaf(t.y, y[4 * i4 + 1], a1[e]);
-                    a1[e] = fmaf(t.z, y[4 * i4 + 2], a1[e]);
-                    a1[e] = fmaf(t.w, y[4 * i4 + 3], a1[e]);
-                }
-                float p0 = (a0[0] + a0[1]) + (a0[2] + a0[3]), p1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
-                p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-                p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-                p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-                word |= ((p0 >= 0.0f ? 1u : 0u) << jj) | ((p1 >= 0.0f ? 1u : 0u) << (jj + 1));
-            }
-            if (jc == q) mine = word;
-        }
         if (store) {
             const size_t qi = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
-            reinterpret_cast<uint32_t *>(p.qjl_signs + qi * (kJl / 8))[q] = mine;
-            if (q == 0) p.qjl_norm[qi] = sqrtf(ss);
+            qjl_sketch(p.S, y, q, true, p.qjl_signs + qi * (kJl / 8), p.qjl_norm + qi);
+        } else {
+            qjl_sketch(p.S, y, q, false, nullptr, nullptr);
         }
     }
 }
 
-// Quantize and store one value vector held by four lanes (as key_tail).
-template <int VB>
+// Quantize and store one value vector held by four lanes (as key_tail); with
+// QJLV also the sketch of the residual y - sigma c[code] (binary32 product and
+// difference, c the centroids in cent_smem).
+template <int VB, bool QJLV = false>
 __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[kQ], const float *thr_smem, int q,
-                                           int b, int h, int pos, bool store) {
+                                           int b, int h, int pos, bool store, const float *cent_smem = nullptr) {
     // pairwise tree of squares in index order: this lane's 32 give one of the
     // four subtrees two levels under the root; the root adds
     // (q0 + q1) + (q2 + q3)
@@ -277,19 +291,31 @@ __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[k
 #pragma unroll
         for (int i = 0; i < kQ; i++) {
             const float u = __fmul_rn(y[i], r);
-            put_code<VB>(w, i, search_reg<VB>(u, th, 0u));
+            const uint32_t k = search_reg<VB>(u, th, 0u);
+            put_code<VB>(w, i, k);
+            if constexpr (QJLV) y[i] = __fsub_rn(y[i], __fmul_rn(sigma, cent_smem[k]));
         }
     } else {
 #pragma unroll
         for (int i = 0; i < kQ; i++) {
             const float u = __fmul_rn(y[i], r);
-            put_code<VB>(w, i, search_smem<VB>(u, thr_smem));
+            const uint32_t k = search_smem<VB>(u, thr_smem);
+            put_code<VB>(w, i, k);
+            if constexpr (QJLV) y[i] = __fsub_rn(y[i], __fmul_rn(sigma, cent_smem[k]));
         }
     }
     if (store) {
         store_quarter_record<VB>(p.vcodes + static_cast<size_t>(b) * p.vblock + p.voff[h] +
                                      static_cast<size_t>(pos) * (16 * VB) + q * (4 * VB), w);
         if (q == 0) p.vscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = sigma;
+    }
+    if constexpr (QJLV) {
+        if (store) {
+            const size_t qi = (static_cast<size_t>(b) * p.nv + p.vrank[h]) * p.capacity + pos;
+            qjl_sketch(p.S, y, q, true, p.vqjl_signs + qi * (kJl / 8), p.vqjl_norm + qi);
+        } else {
+            qjl_sketch(p.S, y, q, false, nullptr, nullptr);
+        }
     }
 }
 
@@ -302,13 +328,13 @@ __device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *
     key_tail<KB, QJL>(p, y, q, b, h, pos, store);
 }
 
-template <int VB>
+template <int VB, bool QJLV>
 __device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
-                                          const float *out_scale, const float *thr_smem, int q, int b, int h,
-                                          int pos, bool store) {
+                                          const float *out_scale, const float *thr_smem, const float *cent_smem,
+                                          int q, int b, int h, int pos, bool store) {
     float y[kQ];
     load_rotate(qrow, in_mask, out_scale, q, y);
-    value_tail<VB>(p, y, thr_smem, q, b, h, pos, store);
+    value_tail<VB, QJLV>(p, y, thr_smem, q, b, h, pos, store, cent_smem);
 }
 
 // Stage the rows of block `blk` (t-block fastest, then head, then batch) of
@@ -334,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + 4 * kGroupBuf);  // [64]
     float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);          // [128]
     float *thr = out_scale + kD;                                             // [kCbTotal]
+    float *cent = thr + kCbTotal;                                            // [kCbTotal]
 
     const int n_tblk = (p.T + kTok - 1) / kTok;
     const int n_blk = n_tblk * p.H * p.B;
@@ -355,7 +382,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint32_t s = (p.sign_bits[i >> 5] >> (i & 31)) & 1u;
         out_scale[i] = s ? -p.inv_sqrt_d : p.inv_sqrt_d;
     }
-    for (int j = threadIdx.x; j < kCbTotal; j += kThreads) thr[j] = p.thr[j];
+    for (int j = threadIdx.x; j < kCbTotal; j += kThreads) {
+        thr[j] = p.thr[j];
+        cent[j] = p.cent[j];
+    }
     __syncthreads();  // tables written
 
     for (int it = 0; blk < n_blk; blk += gridDim.x, it++) {
@@ -384,10 +414,12 @@ __global__ void __launch_bounds__(kThreads, 3)
             }
         } else {
             const int vb = p.vbits[h];
-            const float *t = thr + cb_off(vb);
-            switch (vb) {
-#define TQ_VAL_CASE(VB) \
-    case VB: value_vector<VB>(p, qrow, in_mask, out_scale, t, q, b, h, pos, store); break;
+            const float *t = thr + cb_off(vb), *c = cent + cb_off(vb);
+            const bool qv = p.vrank[h] >= 0;
+            switch (vb * 2 + (qv ? 1 : 0)) {
+#define TQ_VAL_CASE(VB)                                                                                         \
+    case 2 * VB: value_vector<VB, false>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store); break;       \
+    case 2 * VB + 1: value_vector<VB, true>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store); break;
                 TQ_VAL_CASE(1) TQ_VAL_CASE(2) TQ_VAL_CASE(3) TQ_VAL_CASE(4)
                 TQ_VAL_CASE(5) TQ_VAL_CASE(6) TQ_VAL_CASE(7) TQ_VAL_CASE(8)
 #undef TQ_VAL_CASE
@@ -484,7 +516,7 @@ __global__ void __launch_bounds__(kThreads) requantize_kernel(const __grid_const
     }
 }
 
-constexpr size_t compress_smem() { return 4 * kGroupBuf + (kD / 2) * 4 + kD * 4 + kCbTotal * 4; }
+constexpr size_t compress_smem() { return 4 * kGroupBuf + (kD / 2) * 4 + kD * 4 + 2 * kCbTotal * 4; }
 
 // ------------------------------------------------------------------ dequant
 // One thread per (b, h, token, K|V) vector: unpack, scale in binary32 and

@@ -259,8 +259,8 @@ tq_status check_layout(const tq_segment_layout *L, bool need_bits) {
         bool any_qjl = false;
         for (int h = 0; h < L->n_heads; ++h) {
             if (L->kbits[h] < 1 || L->kbits[h] > 8 || L->vbits[h] < 1 || L->vbits[h] > 8) return TQ_ERR_ARG;
-            if (L->qjl[h] > 1) return TQ_ERR_ARG;
-            any_qjl |= L->qjl[h] != 0;
+            if (L->qjl[h] > 1 || L->qjl_v[h] > 1) return TQ_ERR_ARG;
+            any_qjl |= L->qjl[h] != 0 || L->qjl_v[h] != 0;
         }
         if (any_qjl && (L->jl_dim < 32 || L->jl_dim > 1024 || L->jl_dim % 32)) return TQ_ERR_ARG;
         if (L->value_law != TQ_VALUE_LAW_GAUSS && L->value_law != TQ_VALUE_LAW_SPHERE) return TQ_ERR_ARG;
@@ -273,6 +273,8 @@ struct Offsets {
     uint32_t koff[TQ_MAX_HEADS] = {}, voff[TQ_MAX_HEADS] = {};
     int8_t qrank[TQ_MAX_HEADS] = {};
     int nq = 0;
+    int8_t vrank[TQ_MAX_HEADS] = {};  // value sketches
+    int nv = 0;
 };
 
 Offsets offsets(const tq_segment_layout *L) {
@@ -284,6 +286,7 @@ Offsets offsets(const tq_segment_layout *L) {
         k += static_cast<size_t>(L->capacity) * L->head_dim * L->kbits[h] / 8;
         v += static_cast<size_t>(L->capacity) * L->head_dim * L->vbits[h] / 8;
         o.qrank[h] = L->qjl[h] ? static_cast<int8_t>(o.nq++) : static_cast<int8_t>(-1);
+        o.vrank[h] = L->qjl_v[h] ? static_cast<int8_t>(o.nv++) : static_cast<int8_t>(-1);
     }
     o.kblock = static_cast<uint32_t>(k);
     o.vblock = static_cast<uint32_t>(v);
@@ -317,9 +320,10 @@ struct Plan {
     bool any_qjl = false;
     int n_parts = 0;
     int mass_ctas = 0;  // CTAs of the attention-mass launch (0: no segment asked for mass)
+    int vqjl_ctas = 0;  // CTAs of the value-sketch launch (0: no value sketch)
     std::vector<int> grp_part, grp_nparts, lbh_total;
     size_t off_items = 0, off_layer = 0, off_grp_part = 0, off_grp_nparts = 0, off_lbh_total = 0, off_counter = 0;
-    size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, off_ml = 0, total = 0;
+    size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, off_ml = 0, off_z = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -362,8 +366,11 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             if (sg.kind == TQ_SEG_PACKED) {
                 if (L.capacity % 16) return TQ_ERR_ALIGN;
                 if (!fits_u32(&L)) return TQ_ERR_UNSUPPORTED;
-                bool q = false;
-                for (int h = 0; h < H; ++h) q |= L.qjl[h] != 0;
+                bool q = false, qv = false;
+                for (int h = 0; h < H; ++h) {
+                    q |= L.qjl[h] != 0;
+                    qv |= L.qjl_v[h] != 0;
+                }
                 if (check_ptrs) {
                     const tq_packed_bufs &pb = sg.packed;
                     if (!pb.kcodes || !pb.vcodes || !pb.kscale || !pb.vscale) return TQ_ERR_ARG;
@@ -374,8 +381,12 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                         if (!pb.qjl_signs || !pb.qjl_norm || !S) return TQ_ERR_ARG;
                         if (!aligned16(pb.qjl_signs) || !aligned16(pb.qjl_norm) || !aligned16(S)) return TQ_ERR_ALIGN;
                     }
+                    if (qv) {
+                        if (!pb.vqjl_signs || !pb.vqjl_norm || !S) return TQ_ERR_ARG;
+                        if (!aligned16(pb.vqjl_signs) || !aligned16(pb.vqjl_norm) || !aligned16(S)) return TQ_ERR_ALIGN;
+                    }
                 }
-                if (q && (jl != kJl || L.jl_dim != kJl)) return TQ_ERR_UNSUPPORTED;
+                if ((q || qv) && (jl != kJl || L.jl_dim != kJl)) return TQ_ERR_UNSUPPORTED;
             } else {
                 if (check_ptrs) {
                     if (!sg.k16 || !sg.v16) return TQ_ERR_ARG;
@@ -425,6 +436,12 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                     w.vb = L.vbits[h];
                     w.qjl = L.qjl[h] ? 1 : 0;
                     w.vlaw = L.value_law;
+                    if (L.qjl_v[h]) {
+                        w.vqs = static_cast<const uint8_t *>(sg.packed.vqjl_signs) + o.vrank[h] * cap * (kJl / 8);
+                        w.vqn = sg.packed.vqjl_norm + o.vrank[h] * cap;
+                        w.vqstride = static_cast<uint32_t>(o.nv * cap);
+                        lp.has_vqjl = 1;
+                    }
                     if (w.qjl) {
                         w.qs = static_cast<const uint8_t *>(sg.packed.qjl_signs) + o.qrank[h] * cap * (kJl / 8);
                         w.qn = sg.packed.qjl_norm + o.qrank[h] * cap;
@@ -539,6 +556,13 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             if (mc > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
         }
         P.mass_ctas = static_cast<int>(mc);
+        long long vc = 0;  // value sketches: the same split as the mass
+        for (WorkItem &w : P.items) {
+            w.vqjl_cta_begin = static_cast<int>(vc);
+            if (w.vqs) vc += static_cast<long long>(B) * ((w.n_tokens + kMassTokens - 1) / kMassTokens);
+            if (vc > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
+        }
+        P.vqjl_ctas = static_cast<int>(vc);
     }
     DecodeDims &D = P.dims;
     D.L = n_layers;
@@ -578,7 +602,9 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     P.off_part = off;
     off += align256(static_cast<size_t>(std::max(P.n_parts, 1)) * kMaxGqa * (4 + kD) * 4);
     P.off_ml = off;
-    if (P.mass_ctas > 0) off += align256(nq * 2 * sizeof(float));
+    if (P.mass_ctas > 0 || P.vqjl_ctas > 0) off += align256(nq * 2 * sizeof(float));
+    P.off_z = off;
+    if (P.vqjl_ctas > 0) off += align256(nq * kD * sizeof(float));
     P.total = off;
     return TQ_OK;
 }
@@ -716,6 +742,8 @@ tq_status tq_packed_size(const tq_segment_layout *layout, tq_packed_sizes *sizes
     sizes->vscale_bytes = sizes->kscale_bytes;
     sizes->qjl_sign_bytes = B * o.nq * cap * (o.nq ? layout->jl_dim / 8 : 0);
     sizes->qjl_norm_bytes = B * o.nq * cap * 4;
+    sizes->vqjl_sign_bytes = B * o.nv * cap * (o.nv ? layout->jl_dim / 8 : 0);
+    sizes->vqjl_norm_bytes = B * o.nv * cap * 4;
     return TQ_OK;
 }
 
@@ -735,6 +763,11 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
         if (!qjl_S || !out->qjl_signs || !out->qjl_norm) return TQ_ERR_ARG;
         if (layout->jl_dim != kJl) return TQ_ERR_UNSUPPORTED;
         if (!aligned16(qjl_S) || !aligned16(out->qjl_signs)) return TQ_ERR_ALIGN;
+    }
+    if (o.nv) {
+        if (!qjl_S || !out->vqjl_signs || !out->vqjl_norm) return TQ_ERR_ARG;
+        if (layout->jl_dim != kJl) return TQ_ERR_UNSUPPORTED;
+        if (!aligned16(qjl_S) || !aligned16(out->vqjl_signs)) return TQ_ERR_ALIGN;
     }
     if (!aligned16(K) || !aligned16(V) || !aligned16(out->kcodes) || !aligned16(out->vcodes) ||
         !aligned16(out->kscale) || !aligned16(out->vscale))
@@ -762,6 +795,9 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
     p.qjl_norm = out->qjl_norm;
     p.S = qjl_S;
     p.nq = o.nq;
+    p.vqjl_signs = static_cast<uint8_t *>(out->vqjl_signs);
+    p.vqjl_norm = out->vqjl_norm;
+    p.nv = o.nv;
     p.kblock = o.kblock;
     p.vblock = o.vblock;
     for (int h = 0; h < p.H; ++h) {
@@ -770,13 +806,15 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
         p.kbits[h] = layout->kbits[h];
         p.vbits[h] = layout->vbits[h];
         p.qrank[h] = o.qrank[h];
+        p.vrank[h] = o.vrank[h];
     }
     std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
     p.inv_sqrt_d = inv_sqrt_f32(kD);
     p.Q = rot->dense;
     fill_thresholds(p.thr, layout->vbits, p.H, layout->value_law);
+    if (o.nv) fill_centroids(p.cent, layout->vbits, p.H, layout->value_law);
     if (p.Q) {  // dense rotation: the tensor-core kernel (no QJL heads)
-        if (o.nq) return TQ_ERR_UNSUPPORTED;
+        if (o.nq || o.nv) return TQ_ERR_UNSUPPORTED;
         if (!aligned16(p.Q)) return TQ_ERR_ALIGN;
         const cudaError_t e = launch_compress_dense(p, static_cast<cudaStream_t>(stream));
         if (e == cudaErrorInvalidValue) {
@@ -847,7 +885,7 @@ tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_
         return TQ_ERR_ARG;
     if (src->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     for (int h = 0; h < dst->n_heads; ++h)
-        if (dst->qjl[h]) return TQ_ERR_UNSUPPORTED;  // demoted tokens carry no sketch
+        if (dst->qjl[h] || dst->qjl_v[h]) return TQ_ERR_UNSUPPORTED;  // demoted tokens carry no sketch
     if (static_cast<int64_t>(src_t_begin) + n_tokens > src->capacity ||
         static_cast<int64_t>(dst_t_begin) + n_tokens > dst->capacity)
         return TQ_ERR_SIZE;
@@ -881,6 +919,7 @@ tq_status tq_requantize(const tq_segment_layout *src, const tq_packed_bufs *src_
         q.kbits[h] = dst->kbits[h];
         q.vbits[h] = dst->vbits[h];
         q.qrank[h] = -1;
+        q.vrank[h] = -1;
         p.skoff[h] = so.koff[h];
         p.svoff[h] = so.voff[h];
         p.skbits[h] = src->kbits[h];
@@ -1015,7 +1054,8 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     W.qjlt = reinterpret_cast<uint32_t *>(ws + P.off_qjlt);
     W.qsum = reinterpret_cast<float *>(ws + P.off_qsum);
     W.part = reinterpret_cast<float *>(ws + P.off_part);
-    W.ml = P.mass_ctas > 0 ? reinterpret_cast<float *>(ws + P.off_ml) : nullptr;
+    W.ml = P.mass_ctas > 0 || P.vqjl_ctas > 0 ? reinterpret_cast<float *>(ws + P.off_ml) : nullptr;
+    W.z = P.vqjl_ctas > 0 ? reinterpret_cast<float *>(ws + P.off_z) : nullptr;
     W.q = static_cast<const uint16_t *>(q);
     W.out = out;
     // fp16 codebook values (and the 1-bit centroid) of every decode class;
@@ -1051,11 +1091,19 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     }
     if (P.items.empty()) return TQ_OK;
     int launched = 0;
+    if (P.vqjl_ctas > 0) {  // the value-sketch sums accumulate into z
+        e = cudaMemsetAsync(W.z, 0, static_cast<size_t>(n_layers) * batch * q_heads * kD * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S,
                               class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop, &launched);
     if (e == cudaSuccess && P.mass_ctas > 0) {
         e = launch_attention_mass(P.dims, W, static_cast<int>(P.items.size()), P.mass_ctas, s);
         ++launched;
+    }
+    if (e == cudaSuccess && P.vqjl_ctas > 0) {
+        e = launch_value_qjl(P.dims, W, static_cast<int>(P.items.size()), P.vqjl_ctas, qjl_S, s);
+        launched += 2;
     }
     g_last_launches.store(launched);
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);

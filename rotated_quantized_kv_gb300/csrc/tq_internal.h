@@ -45,7 +45,12 @@ struct CompressParams {
     uint32_t sign_bits[kD / 32];
     float inv_sqrt_d;            // binary32(1/sqrt(d))
     const float *Q;              // dense rotation (d x d, device, y = Q x) or nullptr: the SRHT of sign_bits
+    uint8_t *vqjl_signs;         // value-residual sketches (heads with vrank >= 0)
+    float *vqjl_norm;
+    int nv;
+    int8_t vrank[kMaxH];         // -1: no value sketch
     float thr[kCbTotal];         // value thresholds, flat by bit width
+    float cent[kCbTotal];        // value centroids, flat by bit width (value sketches)
 };
 
 // ----------------------------------------------------------------- dequantize
@@ -100,12 +105,17 @@ struct alignas(16) WorkItem {
     int kb, vb, qjl, vlaw;  // vlaw: value codebook law (host side only)
     float *mass;              // attention mass of (b=0, head, t=0), batch stride sstride; null: none
     int mass_cta_begin;       // first CTA of the item in the attention-mass launch
+    const uint8_t *vqs;       // value-residual sketches of (b=0, head's rank, t=0); null: none
+    const float *vqn;         // their norms
+    uint32_t vqstride;        // records between batch elements (nv * cap)
+    int vqjl_cta_begin;       // first CTA of the item in the value-sketch launch
 };
 
 struct LayerPlan {
     uint32_t sign_bits[kD / 32];
     const float *dense;                    // dense rotation (d x d, y = Q x) or nullptr: the SRHT
     int has_qjl;
+    int has_vqjl;                          // some packed item of the layer sketches its values
     int qjl_mode;                          // TQ_QJL_UNBIASED / TQ_QJL_SIGN_PAIR
     int n_items[kMaxH];                    // items of each KV head
     int item[kMaxH][TQ_MAX_SEGMENTS];      // their indices in the WorkItem array
@@ -135,7 +145,8 @@ struct DecodeWorkspace {
     uint32_t *qjlt;    // [L][B][Hq][2][d/2] half2 words: hi, lo of S R q (QJL calls only)
     float *qsum;       // [L][B][Hq][4]: sum(R q), sum(S R q), 2^e of the stored R q / 2^e (QJL calls only)
     float *part;       // [parts][kMaxGqa][4 + d]: m (log2 units), l, pad, pad, acc
-    float *ml;         // [L][B][Hq][2]: merged max (log2 units) and sum, or null (no mass wanted)
+    float *ml;         // [L][B][Hq][2]: merged max (log2 units) and sum, or null (no mass, no value sketch)
+    float *z;          // [L][B][Hq][d]: sum_t p_t rho_t s_t of the value sketches (null: none)
     const uint16_t *q; // the caller's queries, fp16 [L][B][Hq][d]
     float *out;        // the caller's output, [L][B][Hq][d]
 };
@@ -198,5 +209,9 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
 // plan, n_ctas CTAs in all), after the decode kernels of the call.
 cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
                                   cudaStream_t s);
+// QJL on values: z of every item with a value sketch (n_ctas CTAs), then
+// out += R (sqrt(pi/2)/jl S^T z) for the query heads of layers that have one.
+cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
+                             const float *S, cudaStream_t s);
 
 }  // namespace tqk

@@ -1,4 +1,7 @@
-// tq_mass.cu -- per-token attention mass after a decode call: the signal of
+// tq_mass.cu -- passes after a decode call that rescore the packed tokens:
+// the per-token attention mass and the QJL correction of sketched values.
+//
+// Attention mass: the signal of
 // attention-weighted tier demotion ("TurboMOQ", "Attention-weighted tier
 // demotion": tiers follow the attention weights of each decode step).
 //
@@ -198,8 +201,221 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// ------------------------------------------------------------ QJL on values
+// z[l][b][j][i] = sum_t p_j(t) rho(t) s_i(t) over the packed tokens whose values
+// carry a residual sketch (s = 2 bit - 1 the signs of S r, rho = ||r||), with
+// p the final attention weights (rescored as above and normalised by the merged
+// max and sum).  A warp's tiles: the scores give lane (g, c) the weights of
+// tokens g, g + 8 for head c; shuffles turn w = p rho into the B fragment of an
+// mma.m16n8k16 whose A fragment holds the sign bits as fp16 subnormals (the
+// 1-bit value decoder), so the accumulator holds sum_t w bit 2^(s - 24) and
+// sum_t w s = 2 sum_t w bit - sum_t w.  The CTA's warps add into shared memory,
+// the CTA into z with one atomic per (head, coordinate).
+__device__ __forceinline__ int find_vqjl_item(const WorkItem *items, int n, int cta) {
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (items[mid].vqjl_cta_begin <= cta) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <int KB, bool QJL>
+__device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWorkspace &ws, const WorkItem &it,
+                                          int b, int t0, size_t qbase, const MassShared &sh, float (*zsh)[kD]) {
+    using KU = KUnpack<KB>;
+    using VS = VDec<1, 7>;  // sign records decode as 1-bit codes
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int gqa = dims.gqa, head = g >> 1, part = g & 1;
+    constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
+    constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
+    const bool prepared = QJL || ws.layer[it.layer].dense != nullptr;
+    uint32_t q[16], bq[16];
+    const uint32_t *qw = prepared ? ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c
+                                  : &sh.qsh[head][part * (kD / 2) + 16 * c];
+#pragma unroll
+    for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
+    gather_b<KU>(q, bq);
+    const float qsum = c < gqa ? (prepared ? ws.qsum[(qbase + c) * 4] : sh.qs_sum[c]) : 0.f;
+    const float aq = c < gqa ? alphaA * (prepared ? ws.qsum[(qbase + c) * 4 + 2] : sh.qs_scale[c]) : 0.f;
+    uint32_t bt[16];
+    float tsum = 0.f;
+    if constexpr (QJL) {
+        const uint32_t *tw = ws.qjlt + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
+#pragma unroll
+        for (int i = 0; i < 16; i++) q[i] = head < gqa ? tw[i] : 0u;
+        gather_b<SignUnpack>(q, bt);
+        tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
+    }
+    const float m_c = c < gqa ? sh.mx[c] : 0.f, il_c = c < gqa ? sh.inv_l[c] : 0.f;
+    const int n = it.n_tokens;
+    const uint8_t *kc = it.kc + b * it.kstride;
+    const float *ks = it.ks + static_cast<size_t>(b) * it.sstride;
+    const uint8_t *vs = it.vqs + static_cast<size_t>(b) * it.vqstride * (kJl / 8);
+    const float *vn = it.vqn + static_cast<size_t>(b) * it.vqstride;
+    VCtx vx;
+    vx.off = 2 * c * 16 + 4 * (g >> 1);
+    vx.sh = (g & 1) ? 0x7632 : 0x5410;
+    float z[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++) z[mt][0] = z[mt][1] = z[mt][2] = z[mt][3] = 0.f;
+    float wsum = 0.f;  // this lane's B-fragment weights: head g
+    const int t_end = min(t0 + kWarpTokens, n);
+    for (int tile = t0; tile < t_end; tile += 16) {  // warp-uniform
+        const int ta = tile + g, tb = ta + 8;
+        float raw0, raw1;
+        qk_raw<KU, KB>(kc + static_cast<size_t>(ta) * (16 * KB) + 4 * KB * c,
+                       kc + static_cast<size_t>(tb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
+        float s0 = (ta < n ? ks[ta] : 0.f) * (aq * raw0 + beta * qsum);
+        float s1 = (tb < n ? ks[tb] : 0.f) * (aq * raw1 + beta * qsum);
+        if constexpr (QJL) {
+            const size_t r0 = static_cast<size_t>(b) * it.qstride;
+            float q0, q1;
+            qk_raw<SignUnpack, 1>(it.qs + (r0 + ta) * (kJl / 8) + 4 * c, it.qs + (r0 + tb) * (kJl / 8) + 4 * c, bt,
+                                  q0, q1);
+            constexpr float gam = 1.2533141373155003f / kJl;
+            s0 += gam * (ta < n ? it.qn[r0 + ta] : 0.f) * (33554432.0f * q0 - tsum);
+            s1 += gam * (tb < n ? it.qn[r0 + tb] : 0.f) * (33554432.0f * q1 - tsum);
+        }
+        // weights of (token g, head c) and (token g + 8, head c), times the sketch norm
+        const float w0 = c < gqa && ta < n ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c * vn[ta] : 0.f;
+        const float w1 = c < gqa && tb < n ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c * vn[tb] : 0.f;
+        // B fragment of head g: tokens 2c, 2c + 1 (rows 0-7) and 2c + 8, 2c + 9
+        const int src = 8 * c + (g & 3);
+        float v0 = __shfl_sync(0xffffffffu, w0, src), v1 = __shfl_sync(0xffffffffu, w0, src + 4);
+        float v2 = __shfl_sync(0xffffffffu, w1, src), v3 = __shfl_sync(0xffffffffu, w1, src + 4);
+        if (g >= gqa) v0 = v1 = v2 = v3 = 0.f;
+        wsum += (v0 + v1) + (v2 + v3);
+        const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
+        const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&h01), b1 = *reinterpret_cast<const uint32_t *>(&h23);
+        uint32_t ra[8], rb[8], rc[8], rd[8];
+        const uint8_t *vrow = vs + static_cast<size_t>(tile) * (kJl / 8);
+        VS::pair(vrow, kJl / 8, vx, ra, rb);                  // tokens 2c, 2c + 1
+        VS::pair(vrow + 8 * (kJl / 8), kJl / 8, vx, rc, rd);  // tokens 2c + 8, 2c + 9
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) mma16816(z[mt], ra[mt], rb[mt], rc[mt], rd[mt], b0, b1);
+    }
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // W of head g
+    const float W0 = __shfl_sync(0xffffffffu, wsum, 8 * c), W1 = __shfl_sync(0xffffffffu, wsum, 8 * c + 4);
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int r = e >> 1, hq = 2 * c + (e & 1);
+            if (hq < gqa) {
+                const float v = 2.0f * z[mt][e] * VS::unscale(mt, r) - ((e & 1) ? W1 : W0);
+                atomicAdd(&zsh[hq][16 * g + VS::dim(mt, r)], v);
+            }
+        }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    value_qjl_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items) {
+    __shared__ __align__(16) MassShared sh;
+    __shared__ float zsh[kMaxGqa][kD];
+    const int idx = find_vqjl_item(ws.items, n_items, blockIdx.x);
+    const WorkItem &it = ws.items[idx];
+    const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;
+    const int local = blockIdx.x - it.vqjl_cta_begin;
+    const int b = local / nch;
+    const int tok0 = (local - b * nch) * kMassTokens;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gqa = dims.gqa;
+    const size_t qbase = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + static_cast<size_t>(it.head) * gqa;
+    const LayerPlan &lp = ws.layer[it.layer];
+    for (int i = threadIdx.x; i < kMaxGqa * kD; i += kThreads) zsh[i / kD][i % kD] = 0.f;
+    if (warp < kMaxGqa) {
+        const bool on = warp < gqa;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (on) load_q4(ws.q + (qbase + warp) * kD, lane, x);
+        if (!it.qjl && !lp.dense) {
+            warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
+            const float f = warp_pow2_norm(x);
+#pragma unroll
+            for (int e = 0; e < 4; e++) x[e] *= f;
+            const float sm = store_hilo(sh.qsh[warp], x, lane);
+            if (lane == 0) {
+                sh.qs_sum[warp] = sm / f;
+                sh.qs_scale[warp] = 1.0f / f;
+            }
+        }
+        if (lane == 0) {
+            sh.mx[warp] = on ? ws.ml[(qbase + warp) * 2] : 0.f;
+            const float l = on ? ws.ml[(qbase + warp) * 2 + 1] : 0.f;
+            sh.inv_l[warp] = l > 0.f ? 1.0f / l : 0.f;
+        }
+    }
+    __syncthreads();
+    const int t0 = tok0 + kWarpTokens * warp;
+    if (t0 < it.n_tokens) {
+        const bool qj = it.qjl != 0;
+#define TQ_VQJL_CASE(K)                                                            \
+    case K:                                                                        \
+        if (qj) vqjl_warp<K, true>(dims, ws, it, b, t0, qbase, sh, zsh);           \
+        else vqjl_warp<K, false>(dims, ws, it, b, t0, qbase, sh, zsh);             \
+        break;
+        switch (it.kb) {
+            TQ_VQJL_CASE(1)
+            TQ_VQJL_CASE(2)
+            TQ_VQJL_CASE(3)
+            TQ_VQJL_CASE(4)
+            TQ_VQJL_CASE(5)
+            TQ_VQJL_CASE(6)
+            TQ_VQJL_CASE(7)
+            default:
+                if (qj) vqjl_warp<8, true>(dims, ws, it, b, t0, qbase, sh, zsh);
+                else vqjl_warp<8, false>(dims, ws, it, b, t0, qbase, sh, zsh);
+                break;
+        }
+#undef TQ_VQJL_CASE
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < gqa * kD; i += kThreads)
+        atomicAdd(ws.z + (qbase + i / kD) * kD + (i % kD), zsh[i / kD][i % kD]);
+}
+
+// out[l][b][j] += R (sqrt(pi/2)/jl S^T z[l][b][j]) (R^T = R for the SRHT; Q^T
+// for a dense rotation), one warp per query head of a layer with value sketches.
+__global__ void __launch_bounds__(kThreads)
+    value_qjl_apply_kernel(const DecodeDims dims, const DecodeWorkspace ws, const float *S) {
+    const int wid = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (wid >= dims.L * dims.B * dims.Hq) return;
+    const int l = wid / (dims.B * dims.Hq);
+    const LayerPlan &lp = ws.layer[l];
+    if (!lp.has_vqjl) return;
+    float x[4];
+    const float4 zv = reinterpret_cast<const float4 *>(ws.z + static_cast<size_t>(wid) * kD)[lane];
+    x[0] = zv.x;
+    x[1] = zv.y;
+    x[2] = zv.z;
+    x[3] = zv.w;
+    warp_rotate_dense(x, S, true, lane);  // S^T z
+    constexpr float coef = 1.2533141373155003f / kJl;
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] *= coef;
+    if (lp.dense) warp_rotate_dense(x, lp.dense, true, lane);
+    else warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
+    float4 *o = reinterpret_cast<float4 *>(ws.out + static_cast<size_t>(wid) * kD) + lane;
+    float4 ov = *o;
+    ov.x += x[0];
+    ov.y += x[1];
+    ov.z += x[2];
+    ov.w += x[3];
+    *o = ov;
+}
+
 }  // namespace
 }  // namespace dec
+
+cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
+                             const float *S, cudaStream_t s) {
+    dec::value_qjl_kernel<<<n_ctas, dec::kThreads, 0, s>>>(dims, ws, n_items);
+    const int n_warps = dims.L * dims.B * dims.Hq;
+    dec::value_qjl_apply_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
                                   cudaStream_t s) {

@@ -67,17 +67,19 @@ class tq_segment_layout(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("capacity", ctypes.c_int), ("jl_dim", ctypes.c_int),
                 ("kbits", ctypes.c_uint8 * TQ_MAX_HEADS), ("vbits", ctypes.c_uint8 * TQ_MAX_HEADS),
-                ("qjl", ctypes.c_uint8 * TQ_MAX_HEADS), ("value_law", ctypes.c_uint8)]
+                ("qjl", ctypes.c_uint8 * TQ_MAX_HEADS), ("value_law", ctypes.c_uint8),
+                ("qjl_v", ctypes.c_uint8 * TQ_MAX_HEADS)]
 
 
 class tq_packed_sizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("kcode_bytes", "vcode_bytes", "kscale_bytes",
-                                                "vscale_bytes", "qjl_sign_bytes", "qjl_norm_bytes")]
+                                                "vscale_bytes", "qjl_sign_bytes", "qjl_norm_bytes",
+                                                "vqjl_sign_bytes", "vqjl_norm_bytes")]
 
 
 class tq_packed_bufs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("kcodes", "vcodes", "kscale", "vscale",
-                                                "qjl_signs", "qjl_norm")]
+                                                "qjl_signs", "qjl_norm", "vqjl_signs", "vqjl_norm")]
 
 
 class tq_segment(ctypes.Structure):
@@ -204,15 +206,16 @@ def tq_make_qjl(head_dim: int, jl_dim: int, seed: int) -> torch.Tensor:
     return S
 
 
-def make_layout(batch, n_heads, head_dim, capacity, kbits, vbits, qjl=None, jl_dim=128, value_law=0):
+def make_layout(batch, n_heads, head_dim, capacity, kbits, vbits, qjl=None, jl_dim=128, value_law=0, qjl_v=None):
     L = tq_segment_layout()
     L.batch, L.n_heads, L.head_dim, L.capacity, L.jl_dim = batch, n_heads, head_dim, capacity, jl_dim
     L.value_law = value_law
     kb = [int(kbits)] * n_heads if isinstance(kbits, int) else [int(x) for x in kbits]
     vb = [int(vbits)] * n_heads if isinstance(vbits, int) else [int(x) for x in vbits]
     qj = [0] * n_heads if qjl is None else [int(bool(x)) for x in qjl]
+    qv = [0] * n_heads if qjl_v is None else [int(bool(x)) for x in qjl_v]
     for h in range(n_heads):
-        L.kbits[h], L.vbits[h], L.qjl[h] = kb[h], vb[h], qj[h]
+        L.kbits[h], L.vbits[h], L.qjl[h], L.qjl_v[h] = kb[h], vb[h], qj[h], qv[h]
     return L
 
 
@@ -250,12 +253,15 @@ class PackedSegment:
         self.vscale = torch.zeros(max(s.vscale_bytes // 4, 4), **f32)
         self.qjl_signs = torch.zeros(max(s.qjl_sign_bytes, 16), **u8) if s.qjl_sign_bytes else None
         self.qjl_norm = torch.zeros(max(s.qjl_norm_bytes // 4, 4), **f32) if s.qjl_norm_bytes else None
+        self.vqjl_signs = torch.zeros(max(s.vqjl_sign_bytes, 16), **u8) if s.vqjl_sign_bytes else None
+        self.vqjl_norm = torch.zeros(max(s.vqjl_norm_bytes // 4, 4), **f32) if s.vqjl_norm_bytes else None
 
     def bufs(self) -> tq_packed_bufs:
         b = tq_packed_bufs()
         b.kcodes, b.vcodes = _ptr(self.kcodes), _ptr(self.vcodes)
         b.kscale, b.vscale = _ptr(self.kscale), _ptr(self.vscale)
         b.qjl_signs, b.qjl_norm = _ptr(self.qjl_signs), _ptr(self.qjl_norm)
+        b.vqjl_signs, b.vqjl_norm = _ptr(self.vqjl_signs), _ptr(self.vqjl_norm)
         return b
 
     def segment(self) -> tq_segment:
@@ -266,7 +272,8 @@ class PackedSegment:
 
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in
-                   (self.kcodes, self.vcodes, self.kscale, self.vscale, self.qjl_signs, self.qjl_norm)
+                   (self.kcodes, self.vcodes, self.kscale, self.vscale, self.qjl_signs, self.qjl_norm,
+                    self.vqjl_signs, self.vqjl_norm)
                    if t is not None)
 
 

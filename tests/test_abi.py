@@ -85,6 +85,15 @@ def test_packed_sizes_match_layout(tq):
     assert s.kcode_bytes == seg.kcodes.nbytes and s.vcode_bytes == seg.vcodes.nbytes
     assert s.kscale_bytes == seg.kscale.nbytes and s.vscale_bytes == seg.vscale.nbytes
     assert s.qjl_sign_bytes == seg.qjl_signs.nbytes and s.qjl_norm_bytes == seg.qjl_norm.nbytes
+    assert s.vqjl_sign_bytes == 0 and s.vqjl_norm_bytes == 0
+    qv = [0, 1, 1, 0, 0, 0, 0, 1]
+    sv = tq.tq_packed_size(tq.make_layout(3, 8, 128, 96, kb, vb, qj, qjl_v=qv))
+    segv = O.PackedSegment(3, 8, 128, 96, kb, vb, qj, qjl_v=qv)
+    assert sv.vqjl_sign_bytes == segv.vqjl_signs.nbytes and sv.vqjl_norm_bytes == segv.vqjl_norm.nbytes
+    bad_v = tq.make_layout(1, 8, 128, 16, 3, 3)
+    bad_v.qjl_v[0] = 2
+    with pytest.raises(tq.TQError):  # flags are 0/1
+        tq.tq_packed_size(bad_v)
     # 3 bits: codes are 3/16 of the fp16 bytes (1024 MB -> 192 MB)
     s3 = tq.tq_packed_size(tq.make_layout(1, 8, 128, 65536, 3, 3))
     assert (s3.kcode_bytes + s3.vcode_bytes) * 16 == 65536 * 8 * 128 * 2 * 2 * 3

@@ -33,8 +33,8 @@ def _kv(B, H, T, seed, law="outliers"):
     return W.kv_block(w, 0, B, T, seed)
 
 
-def _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin=0, law=0):
-    seg = O.PackedSegment(B, H, 128, cap, kb, vb, qjl, jl=128, law=law)
+def _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin=0, law=0, qjl_v=None):
+    seg = O.PackedSegment(B, H, 128, cap, kb, vb, qjl, jl=128, law=law, qjl_v=qjl_v)
     O.compress(seg, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S, t_begin=t_begin)
     return seg
 
@@ -48,6 +48,9 @@ def _upload(tq, oseg, layout, n_tokens):
     if g.qjl_signs is not None:
         g.qjl_signs.copy_(torch.from_numpy(oseg.qjl_signs))
         g.qjl_norm.copy_(torch.from_numpy(oseg.qjl_norm))
+    if g.vqjl_signs is not None:
+        g.vqjl_signs.copy_(torch.from_numpy(oseg.vqjl_signs))
+        g.vqjl_norm.copy_(torch.from_numpy(oseg.vqjl_norm))
     return g
 
 
@@ -113,6 +116,57 @@ def test_compress_bit_exact(tq, B, H, T, t_begin, kb, vb, qjl, law):
         n = _qjl_window_ok(oseg, g.qjl_signs, K, sign, S, B, H, T, t_begin)
         assert n <= 1e-5 * oseg.qjl_signs.size * 8
         assert np.allclose(g.qjl_norm.cpu().numpy(), oseg.qjl_norm, rtol=1e-5, atol=0)
+
+
+VALUE_SKETCH_CASES = [
+    # B, H, T, t_begin, kbits, vbits, key qjl, value qjl
+    (2, 4, 90, 16, [2, 1, 3, 2], [1, 2, 1, 3], [1, 0, 0, 1], [1, 1, 0, 1]),
+    (1, 8, 130, 0, [1] * 8, [1, 2, 3, 4, 5, 6, 7, 8], None, [1, 0, 1, 0, 1, 0, 1, 1]),
+]
+
+
+def _value_window_ok(oseg, gsigns, V, sign, S, B, H, t_begin):
+    """Value-sketch sign mismatches must sit in the 1e-6 window around zero."""
+    got = gsigns.cpu().numpy()
+    bad = np.flatnonzero(got != oseg.vqjl_signs)
+    Sd = S.astype(np.float64)
+    rown = np.linalg.norm(Sd, axis=1)
+    n = 0
+    for byte in bad:
+        rec = byte // 16
+        pos = rec % oseg.capacity
+        b, v = divmod(rec // oseg.capacity, oseg.nv)
+        h = [hh for hh in range(H) if oseg.qjl_v[hh] and oseg.vqjl_rank(hh) == v][0]
+        y = O.rotate_f32(V[b, h, pos - t_begin].float().numpy(), sign)
+        codes, sg = O.quant_value(y[None], int(oseg.vbits[h]))
+        c32, _ = O.codebook_f32(int(oseg.vbits[h]))
+        r = (y - (np.float32(sg[0]) * c32[codes[0]]).astype(np.float32)).astype(np.float64)
+        p = Sd @ r
+        diff = got[byte] ^ oseg.vqjl_signs[byte]
+        for bit in range(8):
+            if (diff >> bit) & 1:
+                j = (byte % 16) * 8 + bit
+                assert abs(p[j]) <= 1e-6 * rown[j] * np.linalg.norm(r), (b, h, pos, j)
+                n += 1
+    return n
+
+
+@pytest.mark.parametrize("B,H,T,t_begin,kb,vb,qjl,qjl_v", VALUE_SKETCH_CASES)
+def test_compress_value_sketch(tq, B, H, T, t_begin, kb, vb, qjl, qjl_v):
+    K, V = _kv(B, H, T, seed=70 + T)
+    cap = ((t_begin + T + 15) // 16) * 16
+    sign = O.signs(128, 42)
+    S = O.qjl_matrix(128, 128, 42 + 1000)
+    oseg = _oracle_segment(B, H, cap, kb, vb, qjl, K, V, sign, S, t_begin, qjl_v=qjl_v)
+    g = tq.PackedSegment(tq.make_layout(B, H, 128, cap, kb, vb, qjl, qjl_v=qjl_v))
+    tq.tq_compress(g, tq.tq_make_rotation(128, 42), K.cuda(), V.cuda(), t_begin=t_begin,
+                   qjl_S=torch.from_numpy(S).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(g.vcodes.cpu().numpy(), oseg.vcodes)
+    assert np.array_equal(g.vscale.cpu().numpy().view(np.uint32), oseg.vscale.view(np.uint32))
+    n = _value_window_ok(oseg, g.vqjl_signs, V, sign, S, B, H, t_begin)
+    assert n <= 1e-5 * oseg.vqjl_signs.size * 8
+    assert np.allclose(g.vqjl_norm.cpu().numpy(), oseg.vqjl_norm, rtol=1e-5, atol=0)
 
 
 def test_compress_edge_vectors(tq):
@@ -205,7 +259,7 @@ MASS_RTOL = 1e-4  # binary32 scores: |ds| ~ 1e-5 in log units at these magnitude
 
 
 def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False, estimator=0, mass=False):
-    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl[, law]).
+    """spec: list of segments per layer: ('fp16', T) or ('packed', T, kb, vb, qjl[, law[, qjl_v]]).
     mass: every segment gets an attention-mass buffer, checked against the oracle's."""
     rng = np.random.default_rng(seed)
     S = O.qjl_matrix(128, 128, 42 + 1000) if qjl_any else None
@@ -232,11 +286,12 @@ def _attention_case(tq, L, B, H, Hq, spec, seed, qjl_any=False, estimator=0, mas
             else:
                 kb, vb, qj = sp[2:5]
                 law = sp[5] if len(sp) > 5 else 0
-                o = O.PackedSegment(B, H, 128, cap, kb, vb, qj, jl=128, law=law)
+                qv = sp[6] if len(sp) > 6 else None
+                o = O.PackedSegment(B, H, 128, cap, kb, vb, qj, jl=128, law=law, qjl_v=qv)
                 if T:
                     O.compress(o, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, S)
                 o.n_tokens = T
-                g = _upload(tq, o, tq.make_layout(B, H, 128, cap, kb, vb, qj, value_law=law), T)
+                g = _upload(tq, o, tq.make_layout(B, H, 128, cap, kb, vb, qj, value_law=law, qjl_v=qv), T)
             if mass:  # -1 marks entries the call must leave alone
                 g.attn_mass = torch.full((B, H, cap), -1.0, device="cuda")
             osegs.append(o)
@@ -324,6 +379,17 @@ def test_attention_mass_matches_oracle(tq, L, B, H, Hq, spec):
 def test_decode_attention_sign_pair_estimator(tq, spec):
     # same sketch, the sign-pair score term; the mass kernel follows it too
     w = _attention_case(tq, 1, 2, 4, 16, spec, seed=67, qjl_any=True, estimator=1, mass=True)
+    assert w <= ATTN_TOL, w
+
+
+@pytest.mark.parametrize("L,B,H,Hq,spec", [
+    (1, 2, 4, 16, [("packed", 300, [2, 1, 2, 1], [1, 1, 2, 1], [1, 1, 0, 0], 0, [1, 1, 1, 0]), ("fp16", 9)]),
+    (2, 1, 8, 32, [("packed", 1500, [1] * 8, [1] * 8, [1] * 8, 0, [1] * 8),
+                   ("packed", 200, [3] * 8, [2] * 8, None, 1, [0, 1, 0, 1, 0, 1, 0, 1])]),
+])
+def test_decode_attention_value_sketch(tq, L, B, H, Hq, spec):
+    # QJL on values: the correction pass adds R (sqrt(pi/2)/jl S^T z) to the output
+    w = _attention_case(tq, L, B, H, Hq, spec, seed=90 + L, qjl_any=True, mass=True)
     assert w <= ATTN_TOL, w
 
 
