@@ -472,6 +472,29 @@ def run_static(args, rank, world, tq):
                 "frac_of_peak_est": round(mbytes / (extra * 1e-3) / 1e9 / peak, 4),
                 "timing": "difference of two decode-call timings (CUDA events, K steps each)"}
         del views, bufs, arr, ws2, out2
+    vq = None
+    if w.qjl_max_bits and args.rotation == "srht":
+        # QJL on values: the same cache with the key-sketched heads also sketching
+        # their values; the decode call adds the correction pass
+        m2 = StaticCache(w, batch=args.batch, context=args.context, seed=seed, value_qjl=True)
+        for s in range(3):
+            m2.decode(qpool[s % nq])
+        torch.cuda.synchronize()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record()
+        for s in range(K):
+            m2.decode(qpool[s % nq])
+        v1.record()
+        torch.cuda.synchronize()
+        ms_v = v0.elapsed_time(v1) / K
+        sk = sum(m2.B * si.n * 20 for segs in m2.layers for si in segs if si.packed for h in range(m2.H)
+                 if si.qjl[h])
+        vq = {"ms_per_step": round(ms_v, 4), "ms_per_step_without": round(t["ms"] / K, 4),
+              "extra_ms": round(ms_v - t["ms"] / K, 4), "sketch_bytes": int(sk),
+              "heads": "every head with a key sketch (widths <= 2) also sketches its values",
+              "launches_per_step": tq.tq_decode_last_launches()}
+        del m2
+        torch.cuda.empty_cache()
     plan = [(si.pos0, si.n, sorted(set(zip(si.kbits, si.vbits, si.qjl)))) for si in m.layers[0]]
     config = {"workload": w.name, "layers": m.L, "batch": m.B, "context": m.T, "kv_heads": m.H,
               "q_heads": m.Hq, "head_dim": m.d,
@@ -484,6 +507,8 @@ def run_static(args, rank, world, tq):
         res["requantize"] = rq
     if mass is not None:
         res["attention_mass"] = mass
+    if vq is not None:
+        res["value_qjl"] = vq
     return res
 
 

@@ -88,11 +88,12 @@ class StaticCache:
     """A prompt of `context` positions compressed once per layer (workloads 1, 3, 4, 5)."""
 
     def __init__(self, w: W.Workload, batch: int | None = None, context: int | None = None, seed: int = 1000,
-                 device="cuda", sample_inputs=None, rotation: str = "srht"):
+                 device="cuda", sample_inputs=None, rotation: str = "srht", value_qjl: bool = False):
         """sample_inputs(layer, K, V), if given, sees each layer's fp16 inputs
         ([B][H][T][d] CUDA tensors) before they are dropped.  rotation: "srht"
         (D H D / sqrt(d)) or "haar" (a dense Haar matrix per layer, seed + l;
-        no QJL heads)."""
+        no QJL heads).  value_qjl: the heads with a key sketch also sketch
+        their value residuals."""
         assert rotation in ("srht", "haar")
         if rotation == "haar" and w.qjl_max_bits:
             raise ValueError("the dense-rotation compressor takes no QJL heads")
@@ -115,7 +116,8 @@ class StaticCache:
                     s = T.Fp16Segment(self.B, self.H, self.d, n, n_tokens=n,
                                       k=K[:, :, pos0:pos0 + n].contiguous(), v=V[:, :, pos0:pos0 + n].contiguous())
                 else:
-                    s = T.PackedSegment(T.make_layout(self.B, self.H, self.d, _cap16(n), kb, vb, qj), device=device)
+                    s = T.PackedSegment(T.make_layout(self.B, self.H, self.d, _cap16(n), kb, vb, qj,
+                                                      qjl_v=qj if value_qjl else None), device=device)
                     T.tq_compress(s, rot, K[:, :, pos0:pos0 + n], V[:, :, pos0:pos0 + n], t_begin=0,
                                   qjl_S=self.qjl_S if any(qj) else None)
                 segs.append(SegInfo(s, pos0, n, kb, vb, qj))
