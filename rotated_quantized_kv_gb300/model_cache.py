@@ -248,12 +248,13 @@ class ChunkedDecodeCache:
                           self.pool_v[l][:, :, w0:s], t_begin=self.n_prompt_packed + w0)
         return self.L
 
-    def step(self, s, q=None):
-        """Decode step s; returns the number of kernel launches it made."""
+    def step(self, s, q=None, out=None):
+        """Decode step s (into `out`, default self.out); returns the number of
+        kernel launches it made."""
         launches = self.compress_window(s)
         self.set_step(s)
         qq = self.qpool[s % self.steps_cap] if q is None else q
-        T.tq_decode_attention(None, qq, self.out, self.ws, self.H, views=self.arr)
+        T.tq_decode_attention(None, qq, self.out if out is None else out, self.ws, self.H, views=self.arr)
         return launches + T.tq_decode_last_launches()
 
     def step_bytes(self, s):
