@@ -244,3 +244,31 @@ def test_chunked_workload_full_size(lib):
                   lambda l: O.signs(128, W.ROTATION_SEED + l), None)
     del m
     torch.cuda.empty_cache()
+
+
+def test_dense_rotation_workload(lib):
+    """w5 (K3V3) with a Haar rotation per layer at batch 2 x 16384, built by the
+    tensor-core compressor as the benchmark's --rotation haar does: the decode
+    outputs of sampled groups against the oracle's attention over the packed
+    records copied back, with the same per-layer Q."""
+    T, MC = lib
+    w = W.WORKLOADS["w5"]
+    m = MC.StaticCache(w, batch=2, context=16384, seed=1005, rotation="haar")
+    assert T.tq_compress_error_flag() == 0
+    q = W.query_pool(w, 2, m.B, 1005, device="cuda")[1]
+    m.decode(q)
+    assert T.tq_decode_error_flag(m.ws) == 0
+    torch.cuda.synchronize()
+    Qs = [Qd.cpu().numpy() for Qd in m.dense_q]
+    got = m.out.cpu().numpy()
+    qn = q.cpu().numpy()
+    worst = 0.0
+    for l, b, h in _groups(m.L, m.B, m.H):
+        osegs = _head_segments(m.layers[l], b, h)
+        ref = O.decode_attention(osegs, qn[l, b:b + 1, 4 * h:4 * h + 4], O.signs(128, W.ROTATION_SEED + l), 1,
+                                 Q=Qs[l]).reshape(4, 128)
+        g = got[l, b, 4 * h:4 * h + 4]
+        worst = max(worst, (np.abs(g - ref).max(axis=1) / np.abs(ref).max(axis=1)).max())
+    assert worst <= ATTN_TOL, worst
+    del m
+    torch.cuda.empty_cache()
