@@ -148,22 +148,35 @@ __device__ __forceinline__ float tree_sumsq(const float (&y)[32]) {
     else return __fadd_rn(tree_sumsq<N / 2, OFF>(y), tree_sumsq<N / 2, OFF + N / 2>(y));
 }
 
-// codes of coordinates [32 j, 32 j + 32) into LSB-first words
-template <int BITS, int J, typename CodeOf>
-__device__ __forceinline__ void pack_chunk(uint32_t (&w)[4 * BITS], CodeOf code_of) {
+// Codes of coordinates [32 j, 32 j + 32) as BITS LSB-first words (the record's
+// bytes [4 BITS j, 4 BITS (j + 1))), stored at once: the four chunks of a
+// record run as a loop, so each width's code is one 32-code body (a quarter
+// of the instructions to cache, and BITS words live instead of 4 BITS).
+template <int BITS, typename CodeOf>
+__device__ __forceinline__ void pack_store_chunk(uint8_t *rec, int j, bool store, CodeOf code_of) {
+    uint32_t w[BITS];
+#pragma unroll
+    for (int i = 0; i < BITS; i++) w[i] = 0u;
 #pragma unroll
     for (int i = 0; i < 32; i++) {
         const uint32_t c = code_of(i);
-        const int bit = BITS * (32 * J + i);
+        const int bit = BITS * i;
         w[bit >> 5] |= c << (bit & 31);
         if ((bit & 31) + BITS > 32) w[(bit >> 5) + 1] |= c >> (32 - (bit & 31));
     }
-}
-template <int BITS>
-__device__ __forceinline__ void store_record(uint8_t *rec, const uint32_t (&w)[4 * BITS]) {
+    if (!store) return;
+    uint8_t *dst = rec + 4 * BITS * j;
+    if constexpr (BITS % 4 == 0) {
 #pragma unroll
-    for (int i = 0; i < BITS; i++)
-        reinterpret_cast<uint4 *>(rec)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < BITS / 4; i++)
+            reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else if constexpr (BITS % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < BITS / 2; i++) reinterpret_cast<uint2 *>(dst)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < BITS; i++) reinterpret_cast<uint32_t *>(dst)[i] = w[i];
+    }
 }
 
 // keys: m = max |y|, code = clamp(floor((y * fl(1/m) + 1) * 2^(b-1)))
@@ -179,26 +192,17 @@ __device__ __forceinline__ void key_epilogue(unsigned taddr, uint8_t *rec, float
     }
     const float r = m > 0.f ? __frcp_rn(m) : 0.f;
     constexpr float half_cells = static_cast<float>(1 << (KB - 1));
-    uint32_t w[4 * KB];
-#pragma unroll
-    for (int i = 0; i < 4 * KB; i++) w[i] = 0u;
     auto code = [&](int i) {
         const float u = __fmul_rn(__fadd_rn(__fmul_rn(v[i], r), 1.0f), half_cells);
         const int k = static_cast<int>(floorf(u));
         return static_cast<uint32_t>(min(max(k, 0), (1 << KB) - 1));
     };
-    tmem_ld32(taddr, v);
-    pack_chunk<KB, 0>(w, code);
-    tmem_ld32(taddr + 32, v);
-    pack_chunk<KB, 1>(w, code);
-    tmem_ld32(taddr + 64, v);
-    pack_chunk<KB, 2>(w, code);
-    tmem_ld32(taddr + 96, v);
-    pack_chunk<KB, 3>(w, code);
-    if (store) {
-        store_record<KB>(rec, w);
-        *scale = m;
+#pragma unroll 1
+    for (int j = 0; j < 4; j++) {
+        tmem_ld32(taddr + 32 * j, v);
+        pack_store_chunk<KB>(rec, j, store, code);
     }
+    if (store) *scale = m;
 }
 
 // values: sigma = sqrt(tree(y^2) / d), code = #{thresholds < y * fl(1/sigma)}
@@ -215,9 +219,6 @@ __device__ __forceinline__ void value_epilogue(unsigned taddr, const float *thr,
     const float ss = __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
     const float sigma = __fsqrt_rn(__fdiv_rn(ss, static_cast<float>(kD)));
     const float r = sigma > 0.f ? __frcp_rn(sigma) : 0.f;
-    uint32_t w[4 * VB];
-#pragma unroll
-    for (int i = 0; i < 4 * VB; i++) w[i] = 0u;
     // up to 4 bits: count the thresholds below u from registers; wider codes:
     // binary search with volatile shared loads (one dependent load per step;
     // plain loads get if-converted into loads of every threshold)
@@ -242,18 +243,12 @@ __device__ __forceinline__ void value_epilogue(unsigned taddr, const float *thr,
         }
         return static_cast<uint32_t>(k);
     };
-    tmem_ld32(taddr, v);
-    pack_chunk<VB, 0>(w, code);
-    tmem_ld32(taddr + 32, v);
-    pack_chunk<VB, 1>(w, code);
-    tmem_ld32(taddr + 64, v);
-    pack_chunk<VB, 2>(w, code);
-    tmem_ld32(taddr + 96, v);
-    pack_chunk<VB, 3>(w, code);
-    if (store) {
-        store_record<VB>(rec, w);
-        *scale = sigma;
+#pragma unroll 1
+    for (int j = 0; j < 4; j++) {
+        tmem_ld32(taddr + 32 * j, v);
+        pack_store_chunk<VB>(rec, j, store, code);
     }
+    if (store) *scale = sigma;
 }
 
 struct TileId {
