@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "tq_internal.h"
+#include "tq_mass.h"
 
 using namespace tqk;
 

@@ -156,7 +156,6 @@ struct DecodeWorkspace {
 constexpr int kStageTokens = 64;
 constexpr int kPackedStageTokens = 128;
 constexpr int kDecodeWarps = 4;
-constexpr int kMassTokens = 1024;  // tokens per CTA of the attention-mass kernel
 constexpr int kStages = 4;
 
 // A launch of the split-K kernel of one class over items [item_lo, item_hi).

@@ -19,6 +19,7 @@
 // the lane quad.  fp16 tokens (sinks, newest tier, chunk buffer) are scored
 // one token per thread on the CUDA cores against the unrotated query.
 #include "tq_decode_packed.cuh"
+#include "tq_mass.h"
 
 namespace tqk {
 namespace dec {
@@ -82,22 +83,28 @@ __device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const D
     const float *ks = it.ks + static_cast<size_t>(b) * it.sstride;
     float *mass = it.mass + static_cast<size_t>(b) * it.sstride;
     const int t_end = min(t0 + kWarpTokens, n);
-#pragma unroll 4
-    for (int tile = t0; tile < t_end; tile += 16) {  // warp-uniform; rows up to the next multiple of 16 exist
+    const int last = ((n + 15) & ~15) - 1;  // records exist up to the next multiple of 16
+    // four tiles per step with every row clamped into the segment, so that all
+    // their loads are unconditional and issue together (masked by t < n after)
+    for (int t4 = t0; t4 < t_end; t4 += 64) {
+#pragma unroll
+    for (int tt = 0; tt < 4; tt++) {
+        const int tile = t4 + 16 * tt;
         const int ta = tile + g, tb = ta + 8;
+        const int ra = min(ta, last), rb = min(tb, last);
         float raw0, raw1;
-        qk_raw<KU, KB>(kc + static_cast<size_t>(ta) * (16 * KB) + 4 * KB * c,
-                       kc + static_cast<size_t>(tb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
-        float s0 = (ta < n ? ks[ta] : 0.f) * (aq * raw0 + beta * qsum);
-        float s1 = (tb < n ? ks[tb] : 0.f) * (aq * raw1 + beta * qsum);
+        qk_raw<KU, KB>(kc + static_cast<size_t>(ra) * (16 * KB) + 4 * KB * c,
+                       kc + static_cast<size_t>(rb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
+        float s0 = (ta < n ? ks[ra] : 0.f) * (aq * raw0 + beta * qsum);
+        float s1 = (tb < n ? ks[rb] : 0.f) * (aq * raw1 + beta * qsum);
         if constexpr (QJL) {
             const size_t r0 = static_cast<size_t>(b) * it.qstride;
             float q0, q1;
-            qk_raw<SignUnpack, 1>(it.qs + (r0 + ta) * (kJl / 8) + 4 * c, it.qs + (r0 + tb) * (kJl / 8) + 4 * c, bt,
+            qk_raw<SignUnpack, 1>(it.qs + (r0 + ra) * (kJl / 8) + 4 * c, it.qs + (r0 + rb) * (kJl / 8) + 4 * c, bt,
                                   q0, q1);
             constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
-            s0 += gam * (ta < n ? it.qn[r0 + ta] : 0.f) * (33554432.0f * q0 - tsum);
-            s1 += gam * (tb < n ? it.qn[r0 + tb] : 0.f) * (33554432.0f * q1 - tsum);
+            s0 += gam * (ta < n ? it.qn[r0 + ra] : 0.f) * (33554432.0f * q0 - tsum);
+            s1 += gam * (tb < n ? it.qn[r0 + rb] : 0.f) * (33554432.0f * q1 - tsum);
         }
         float p0 = c < gqa ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c : 0.f;
         float p1 = c < gqa ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c : 0.f;
@@ -110,9 +117,10 @@ __device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const D
             if (tb < n) mass[tb] = p1 * inv_g;
         }
     }
+    }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items) {
     __shared__ __align__(16) MassShared sh;
     const int idx = find_mass_item(ws.items, n_items, blockIdx.x);
@@ -262,25 +270,30 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
     for (int mt = 0; mt < 8; mt++) z[mt][0] = z[mt][1] = z[mt][2] = z[mt][3] = 0.f;
     float wsum = 0.f;  // this lane's B-fragment weights: head g
     const int t_end = min(t0 + kWarpTokens, n);
-    for (int tile = t0; tile < t_end; tile += 16) {  // warp-uniform
+    const int last = ((n + 15) & ~15) - 1;  // records exist up to the next multiple of 16
+    for (int t2 = t0; t2 < t_end; t2 += 32) {  // two tiles per step, rows clamped (as the mass pass)
+#pragma unroll
+    for (int tt = 0; tt < 2; tt++) {
+        const int tile = t2 + 16 * tt;
         const int ta = tile + g, tb = ta + 8;
+        const int ra = min(ta, last), rb = min(tb, last);
         float raw0, raw1;
-        qk_raw<KU, KB>(kc + static_cast<size_t>(ta) * (16 * KB) + 4 * KB * c,
-                       kc + static_cast<size_t>(tb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
-        float s0 = (ta < n ? ks[ta] : 0.f) * (aq * raw0 + beta * qsum);
-        float s1 = (tb < n ? ks[tb] : 0.f) * (aq * raw1 + beta * qsum);
+        qk_raw<KU, KB>(kc + static_cast<size_t>(ra) * (16 * KB) + 4 * KB * c,
+                       kc + static_cast<size_t>(rb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
+        float s0 = (ta < n ? ks[ra] : 0.f) * (aq * raw0 + beta * qsum);
+        float s1 = (tb < n ? ks[rb] : 0.f) * (aq * raw1 + beta * qsum);
         if constexpr (QJL) {
             const size_t r0 = static_cast<size_t>(b) * it.qstride;
             float q0, q1;
-            qk_raw<SignUnpack, 1>(it.qs + (r0 + ta) * (kJl / 8) + 4 * c, it.qs + (r0 + tb) * (kJl / 8) + 4 * c, bt,
+            qk_raw<SignUnpack, 1>(it.qs + (r0 + ra) * (kJl / 8) + 4 * c, it.qs + (r0 + rb) * (kJl / 8) + 4 * c, bt,
                                   q0, q1);
             constexpr float gam = 1.2533141373155003f / kJl;
-            s0 += gam * (ta < n ? it.qn[r0 + ta] : 0.f) * (33554432.0f * q0 - tsum);
-            s1 += gam * (tb < n ? it.qn[r0 + tb] : 0.f) * (33554432.0f * q1 - tsum);
+            s0 += gam * (ta < n ? it.qn[r0 + ra] : 0.f) * (33554432.0f * q0 - tsum);
+            s1 += gam * (tb < n ? it.qn[r0 + rb] : 0.f) * (33554432.0f * q1 - tsum);
         }
         // weights of (token g, head c) and (token g + 8, head c), times the sketch norm
-        const float w0 = c < gqa && ta < n ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c * vn[ta] : 0.f;
-        const float w1 = c < gqa && tb < n ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c * vn[tb] : 0.f;
+        const float w0 = c < gqa && ta < n ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c * vn[ra] : 0.f;
+        const float w1 = c < gqa && tb < n ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c * vn[rb] : 0.f;
         // B fragment of head g: tokens 2c, 2c + 1 (rows 0-7) and 2c + 8, 2c + 9
         const int src = 8 * c + (g & 3);
         float v0 = __shfl_sync(0xffffffffu, w0, src), v1 = __shfl_sync(0xffffffffu, w0, src + 4);
@@ -289,12 +302,14 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
         wsum += (v0 + v1) + (v2 + v3);
         const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
         const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&h01), b1 = *reinterpret_cast<const uint32_t *>(&h23);
-        uint32_t ra[8], rb[8], rc[8], rd[8];
-        const uint8_t *vrow = vs + static_cast<size_t>(tile) * (kJl / 8);
-        VS::pair(vrow, kJl / 8, vx, ra, rb);                  // tokens 2c, 2c + 1
-        VS::pair(vrow + 8 * (kJl / 8), kJl / 8, vx, rc, rd);  // tokens 2c + 8, 2c + 9
+        uint32_t fa[8], fb[8], fc[8], fd[8];
+        // a tile past the end reads the last whole tile (its weights are 0)
+        const uint8_t *vrow = vs + static_cast<size_t>(min(tile, last - 15)) * (kJl / 8);
+        VS::pair(vrow, kJl / 8, vx, fa, fb);                  // tokens 2c, 2c + 1
+        VS::pair(vrow + 8 * (kJl / 8), kJl / 8, vx, fc, fd);  // tokens 2c + 8, 2c + 9
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++) mma16816(z[mt], ra[mt], rb[mt], rc[mt], rd[mt], b0, b1);
+        for (int mt = 0; mt < 8; mt++) mma16816(z[mt], fa[mt], fb[mt], fc[mt], fd[mt], b0, b1);
+    }
     }
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // W of head g
