@@ -436,12 +436,14 @@ struct PackedGeom {
     static constexpr int offQN = offQS + kPT * 16;
     static constexpr int stage = QJL ? offQN + kPT * 4 : offQS;
     static constexpr int budget = 227 * 1024 / packed_ctas_per_sm(QJL) - 1024;
-    static constexpr int qbytes = kMaxGqa * kD * 4 + 32 + 16 + 64;  // queries, sums, scales, flag, barriers
+    static constexpr int qbytes = 16 + 64;  // flag, barriers (the rotated queries come from the prep kernel)
     static constexpr int pair_entries = (VB == 2 || VB == 3) ? (1 << (2 * VB)) : 0;
     // pair table: one column per lane (32 copies) if that still leaves 3
-    // stages in flight at the class's CTAs per SM, else 16 (2-way conflicts)
+    // stages in flight at the class's CTAs per SM, or as many as 16 copies
+    // would; else 16 (2-way bank conflicts)
     static constexpr int fit32 = (budget - qbytes - pair_entries * 128) / stage;
-    static constexpr int copies = (pair_entries == 0 || fit32 >= 3) ? 32 : 16;
+    static constexpr int fit16 = (budget - qbytes - pair_entries * 64) / stage;
+    static constexpr int copies = (pair_entries == 0 || fit32 >= 3 || fit32 >= fit16) ? 32 : 16;
     static constexpr int tab_bytes = pair_entries * copies * 4;
     static constexpr int TS = copies == 32 ? 7 : 6;  // log2 of the table's entry stride
     static constexpr int fixed = (VB >= 5 ? 512 : 0) + tab_bytes + qbytes;
@@ -450,8 +452,8 @@ struct PackedGeom {
     static constexpr int stages = fit > 4 ? 4 : (fit < 2 ? 2 : fit);
     static constexpr int ctab = stages * stage;               // fp16 codebook (5-8 bits)
     static constexpr int ptab = ctab + (VB >= 5 ? 512 : 0);   // pair table (2, 3 bits)
-    static constexpr int qoff = ptab + tab_bytes;             // rotated queries [4][128] words, sums [4], scales [4]
-    static constexpr int flag = qoff + kMaxGqa * kD * 4 + 32;
+    static constexpr int qoff = ptab + tab_bytes;             // end of the tables
+    static constexpr int flag = qoff;
     static constexpr int bar = flag + 16;                     // one mbarrier per stage buffer
     static constexpr int smem = bar + 8 * stages;
 };
@@ -595,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     if (threadIdx.x == 0) {
         for (int k = 0; k < NS - 1 && k < n_st; k++) load_next(k);
     }
-    if (QJL || dims.any_prep) pdl_wait();  // the prep kernel's outputs
+    pdl_wait();  // the prep kernel's rotated queries (its grid precedes every packed class)
 
     // ---- consumer
     StageCursor<QJL, false> cc;
@@ -605,9 +607,6 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     uint32_t bq[16], bt[16];
     float qsum = 0.f, tsum = 0.f, aq = 0.f;
     WarpState st;
-    uint32_t *qsh = reinterpret_cast<uint32_t *>(smem + G::qoff);
-    float *qs_sum = reinterpret_cast<float *>(qsh + kMaxGqa * kD);
-    float *qs_scale = qs_sum + kMaxGqa;
     int *flag = reinterpret_cast<int *>(smem + G::flag);
     // raw = (q / 2^e) . code * 2^(kA - 24) and q . yhat = m (alpha q.code + beta sum q)
     constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
@@ -658,35 +657,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
             qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
             aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
-        } else if (ws.layer[g_layer].dense) {  // the prep kernel rotated the queries
+        } else {  // the prep kernel rotated the queries
             const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
 #pragma unroll
             for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
             gather_b<KU>(q, bq);
             qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
-        } else {
-            if (warp < gqa) {  // warp w rotates query head w of the group
-                float x[4];
-                load_q4(ws.q + (qbase + warp) * kD, lane, x);
-                warp_rotate(x, ws.layer[g_layer].sign_bits, dims.inv_sqrt_d, lane);
-                const float f = warp_pow2_norm(x);
-#pragma unroll
-                for (int e = 0; e < 4; e++) x[e] *= f;
-                const float sm = store_hilo(qsh + warp * kD, x, lane);
-                if (lane == 0) {
-                    qs_sum[warp] = sm / f;
-                    qs_scale[warp] = 1.0f / f;
-                }
-            }
-            __syncthreads();
-            const uint32_t *qw = qsh + head * kD + part * (kD / 2) + 16 * c;
-#pragma unroll
-            for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
-            gather_b<KU>(q, bq);
-            qsum = c < gqa ? qs_sum[c] : 0.f;
-            aq = c < gqa ? alphaA * qs_scale[c] : 0.f;
-            __syncthreads();
         }
     };
     // the warp's two 16-token tiles: tokens [tA, tA + 32) of the stage buffer

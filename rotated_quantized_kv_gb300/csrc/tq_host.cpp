@@ -572,7 +572,11 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.Hq = Hq;
     D.gqa = gqa;
     D.any_qjl = P.any_qjl ? 1 : 0;
-    D.any_prep = P.any_qjl || any_dense ? 1 : 0;
+    // the prep kernel rotates every query once (the packed classes read its
+    // output); calls with fp16 segments only skip it
+    bool any_packed = false;
+    for (const WorkItem &w : P.items) any_packed |= w.kind == TQ_SEG_PACKED;
+    D.any_prep = any_packed || P.any_qjl || any_dense ? 1 : 0;
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
