@@ -1,9 +1,9 @@
 // tq_mass.cu -- passes after a decode call that rescore the packed tokens:
 // the per-token attention mass and the QJL correction of sketched values.
 //
-// Attention mass: the signal of
-// attention-weighted tier demotion ("TurboMOQ", "Attention-weighted tier
-// demotion": tiers follow the attention weights of each decode step).
+// Attention mass: the signal of attention-weighted tier demotion ("TurboMOQ",
+// "Attention-weighted tier demotion": tiers follow the attention weights of
+// each decode step).
 //
 // mass[b][h][t] = (1/g) sum over the g query heads j of KV head h of
 // 2^(s_j(t) - M_j) / L_j, with s_j(t) the base-2 score of token t and (M_j, L_j)
@@ -11,13 +11,14 @@
 //
 // Packed tokens: the scores are recomputed on the tensor cores exactly as the
 // split-K kernel computes them (key codes left at their bit offsets as fp16
-// subnormals times the fp16 hi/lo query, mma.m16n8k16, the affine key levels
-// and the QJL term applied to the raw products), so only the key records,
-// scales and sketches are read.  One CTA of 4 warps takes 128 tokens of one
-// (item, batch element); a warp takes two 16-token tiles; lane (g, c) scores
-// tokens g and g + 8 for query head c and the four heads are summed across
-// the lane quad.  fp16 tokens (sinks, newest tier, chunk buffer) are scored
-// one token per thread on the CUDA cores against the unrotated query.
+// subnormals times the prep kernel's fp16 hi/lo rotated query, mma.m16n8k16,
+// the affine key levels and the QJL term applied to the raw products), so
+// only the key records, scales and sketches are read.  One CTA of 4 warps
+// takes kMassTokens tokens of one (item, batch element); a warp takes its
+// quarter in 16-token tiles, four per step; lane (g, c) scores tokens g and
+// g + 8 for query head c and the four heads are summed across the lane quad.
+// fp16 tokens (sinks, newest tier, chunk buffer) are scored one token per
+// thread on the CUDA cores against the unrotated query.
 #include "tq_decode_packed.cuh"
 #include "tq_mass.h"
 
@@ -40,9 +41,8 @@ __device__ __forceinline__ int find_mass_item(const WorkItem *items, int n, int 
 }
 
 struct MassShared {
-    uint32_t qsh[kMaxGqa][kD];   // rotated queries / 2^e as fp16 hi, lo words (SRHT layers)
     float qf[kMaxGqa][kD];       // unrotated queries (fp16 items)
-    float qs_sum[kMaxGqa], qs_scale[kMaxGqa], mx[kMaxGqa], inv_l[kMaxGqa];
+    float mx[kMaxGqa], inv_l[kMaxGqa];
 };
 
 // A warp's packed tokens [t0, t0 + kWarpTokens) of batch element b in
@@ -58,15 +58,14 @@ __device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const D
     // raw = (q / 2^e) . code * 2^(kA - 24); q . yhat = m (alpha q.code + beta sum q)
     constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
     constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
-    const bool prepared = QJL || ws.layer[it.layer].dense != nullptr;  // the prep kernel rotated q
+    // the prep kernel rotated every query of a call with packed segments
     uint32_t q[16], bq[16];
-    const uint32_t *qw = prepared ? ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c
-                                  : &sh.qsh[head < kMaxGqa ? head : 0][part * (kD / 2) + 16 * c];
+    const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
 #pragma unroll
     for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
     gather_b<KU>(q, bq);
-    const float qsum = c < gqa ? (prepared ? ws.qsum[(qbase + c) * 4] : sh.qs_sum[c]) : 0.f;
-    const float aq = c < gqa ? alphaA * (prepared ? ws.qsum[(qbase + c) * 4 + 2] : sh.qs_scale[c]) : 0.f;
+    const float qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
+    const float aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
     uint32_t bt[16];
     float tsum = 0.f;
     if constexpr (QJL) {
@@ -133,22 +132,11 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int gqa = dims.gqa;
     const bool packed = it.kind == TQ_SEG_PACKED;
     const size_t qbase = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + static_cast<size_t>(it.head) * gqa;
-    const LayerPlan &lp = ws.layer[it.layer];
     if (warp < kMaxGqa) {
         const bool on = warp < gqa;
         float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (on) load_q4(ws.q + (qbase + warp) * kD, lane, x);
-        if (packed && !it.qjl && !lp.dense) {  // SRHT layers rotate here, as the split-K kernel does
-            warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
-            const float f = warp_pow2_norm(x);
-#pragma unroll
-            for (int e = 0; e < 4; e++) x[e] *= f;
-            const float sm = store_hilo(sh.qsh[warp], x, lane);
-            if (lane == 0) {
-                sh.qs_sum[warp] = sm / f;
-                sh.qs_scale[warp] = 1.0f / f;
-            }
-        } else if (!packed) {
+        if (!packed) {  // fp16 tokens: the unrotated query
+            if (on) load_q4(ws.q + (qbase + warp) * kD, lane, x);
 #pragma unroll
             for (int e = 0; e < 4; e++) sh.qf[warp][4 * lane + e] = x[e];
         }
@@ -238,15 +226,13 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
     const int gqa = dims.gqa, head = g >> 1, part = g & 1;
     constexpr float alphaA = static_cast<float>(1 << (24 - KU::kA)) * 2.0f / static_cast<float>(1 << KB);
     constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
-    const bool prepared = QJL || ws.layer[it.layer].dense != nullptr;
     uint32_t q[16], bq[16];
-    const uint32_t *qw = prepared ? ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c
-                                  : &sh.qsh[head][part * (kD / 2) + 16 * c];
+    const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
 #pragma unroll
     for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
     gather_b<KU>(q, bq);
-    const float qsum = c < gqa ? (prepared ? ws.qsum[(qbase + c) * 4] : sh.qs_sum[c]) : 0.f;
-    const float aq = c < gqa ? alphaA * (prepared ? ws.qsum[(qbase + c) * 4 + 2] : sh.qs_scale[c]) : 0.f;
+    const float qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
+    const float aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
     uint32_t bt[16];
     float tsum = 0.f;
     if constexpr (QJL) {
@@ -339,23 +325,9 @@ __global__ void __launch_bounds__(kThreads)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gqa = dims.gqa;
     const size_t qbase = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + static_cast<size_t>(it.head) * gqa;
-    const LayerPlan &lp = ws.layer[it.layer];
     for (int i = threadIdx.x; i < kMaxGqa * kD; i += kThreads) zsh[i / kD][i % kD] = 0.f;
     if (warp < kMaxGqa) {
         const bool on = warp < gqa;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (on) load_q4(ws.q + (qbase + warp) * kD, lane, x);
-        if (!it.qjl && !lp.dense) {
-            warp_rotate(x, lp.sign_bits, dims.inv_sqrt_d, lane);
-            const float f = warp_pow2_norm(x);
-#pragma unroll
-            for (int e = 0; e < 4; e++) x[e] *= f;
-            const float sm = store_hilo(sh.qsh[warp], x, lane);
-            if (lane == 0) {
-                sh.qs_sum[warp] = sm / f;
-                sh.qs_scale[warp] = 1.0f / f;
-            }
-        }
         if (lane == 0) {
             sh.mx[warp] = on ? ws.ml[(qbase + warp) * 2] : 0.f;
             const float l = on ? ws.ml[(qbase + warp) * 2 + 1] : 0.f;
