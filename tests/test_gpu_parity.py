@@ -467,3 +467,29 @@ def test_requantize_across_codebook_laws(tq, B, H, T, skb, svb, dkb, dvb, slaw, 
         assert np.array_equal(got.cpu().numpy()[:ref.size], ref)
     for got, ref in ((gdst.kscale, odst.kscale), (gdst.vscale, odst.vscale)):
         assert np.array_equal(got.cpu().numpy()[:ref.size].view(np.uint32), ref.view(np.uint32))
+
+
+def test_decode_reports_its_launches(tq):
+    # query prep + one grid per packed class + the fp16 kernel (+ mass pass)
+    B, H, Hq = 1, 2, 8
+    rot = tq.tq_make_rotation(128, 42)
+    K, V = _kv(B, H, 70, seed=5)
+    segs = []
+    for kb, vb in ((3, 3), (4, 2)):
+        o = _oracle_segment(B, H, 80, [kb] * H, [vb] * H, None, K, V, O.signs(128, 42), None)
+        o.n_tokens = 70
+        segs.append(_upload(tq, o, tq.make_layout(B, H, 128, 80, [kb] * H, [vb] * H), 70))
+    f16 = tq.Fp16Segment(B, H, 128, 16, n_tokens=9, k=torch.zeros(B, H, 16, 128, dtype=torch.float16, device="cuda"),
+                         v=torch.zeros(B, H, 16, 128, dtype=torch.float16, device="cuda"))
+    q = torch.randn(1, B, Hq, 128, device="cuda").half()
+    out = torch.empty(1, B, Hq, 128, device="cuda")
+    views = [tq.layer_view(rot, segs + [f16])]
+    ws = torch.empty(tq.tq_decode_workspace_size(views, B, H, Hq, 128), dtype=torch.uint8, device="cuda")
+    tq.tq_decode_attention(views, q, out, ws, H)
+    assert tq.tq_decode_last_launches() == 1 + 2 + 1
+    f16.attn_mass = torch.zeros(B, H, 16, device="cuda")
+    views = [tq.layer_view(rot, segs + [f16])]
+    ws = torch.empty(tq.tq_decode_workspace_size(views, B, H, Hq, 128), dtype=torch.uint8, device="cuda")
+    tq.tq_decode_attention(views, q, out, ws, H)
+    assert tq.tq_decode_last_launches() == 1 + 2 + 1 + 1
+    torch.cuda.synchronize()
