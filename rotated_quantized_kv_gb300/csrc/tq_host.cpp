@@ -322,6 +322,7 @@ struct Plan {
     int n_parts = 0;
     int mass_ctas = 0;  // CTAs of the attention-mass launch (0: no segment asked for mass)
     int vqjl_ctas = 0;  // CTAs of the value-sketch launch (0: no value sketch)
+    int mass_stage = 0, vqjl_stage = 0;  // bytes of one step buffer of each rescoring launch
     std::vector<int> grp_part, grp_nparts, lbh_total;
     size_t off_items = 0, off_layer = 0, off_grp_part = 0, off_grp_nparts = 0, off_lbh_total = 0, off_counter = 0;
     size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, off_ml = 0, off_z = 0, total = 0;
@@ -551,19 +552,31 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     // kMassTokens tokens); items without one start where the next one does
     {
         long long mc = 0;
+        int mkb = 1, vkb = 1;
+        bool mq = false, vq = false;
         for (WorkItem &w : P.items) {
             w.mass_cta_begin = static_cast<int>(mc);
             if (w.mass) mc += static_cast<long long>(B) * ((w.n_tokens + kMassTokens - 1) / kMassTokens);
             if (mc > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
+            if (w.mass && w.kind == TQ_SEG_PACKED) {
+                mkb = std::max(mkb, static_cast<int>(w.kb));
+                mq |= w.qjl != 0;
+            }
         }
         P.mass_ctas = static_cast<int>(mc);
+        P.mass_stage = mass_stage_bytes(mkb, mq, false);
         long long vc = 0;  // value sketches: the same split as the mass
         for (WorkItem &w : P.items) {
             w.vqjl_cta_begin = static_cast<int>(vc);
-            if (w.vqs) vc += static_cast<long long>(B) * ((w.n_tokens + kMassTokens - 1) / kMassTokens);
+            if (w.vqs) {
+                vc += static_cast<long long>(B) * ((w.n_tokens + kMassTokens - 1) / kMassTokens);
+                vkb = std::max(vkb, static_cast<int>(w.kb));
+                vq |= w.qjl != 0;
+            }
             if (vc > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
         }
         P.vqjl_ctas = static_cast<int>(vc);
+        P.vqjl_stage = mass_stage_bytes(vkb, vq, true);
     }
     DecodeDims &D = P.dims;
     D.L = n_layers;
@@ -1103,11 +1116,11 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S,
                               class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop, &launched);
     if (e == cudaSuccess && P.mass_ctas > 0) {
-        e = launch_attention_mass(P.dims, W, static_cast<int>(P.items.size()), P.mass_ctas, s);
+        e = launch_attention_mass(P.dims, W, static_cast<int>(P.items.size()), P.mass_ctas, P.mass_stage, s);
         ++launched;
     }
     if (e == cudaSuccess && P.vqjl_ctas > 0) {
-        e = launch_value_qjl(P.dims, W, static_cast<int>(P.items.size()), P.vqjl_ctas, qjl_S, s);
+        e = launch_value_qjl(P.dims, W, static_cast<int>(P.items.size()), P.vqjl_ctas, P.vqjl_stage, qjl_S, s);
         launched += 2;
     }
     g_last_launches.store(launched);

@@ -204,13 +204,5 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
                                   int n_classes, const float *S, const unsigned short *const *value_half,
                                   const float *value_c1,
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop, int *n_launched);
-// Attention mass of every item with a mass pointer (items [0, n_items) of the
-// plan, n_ctas CTAs in all), after the decode kernels of the call.
-cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                                  cudaStream_t s);
-// QJL on values: z of every item with a value sketch (n_ctas CTAs), then
-// out += R (sqrt(pi/2)/jl S^T z) for the query heads of layers that have one.
-cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                             const float *S, cudaStream_t s);
 
 }  // namespace tqk

@@ -45,13 +45,68 @@ struct MassShared {
     float mx[kMaxGqa], inv_l[kMaxGqa];
 };
 
+// One 64-token step of a warp's records into a shared buffer, by cp.async
+// (16-byte chunks spread over the lanes; rows past the segment's records read
+// as zeros): key records (16 KB bytes a row), scales, and for QJL / value-
+// sketch items their sign records (16 bytes) and norms.  Layout of a buffer:
+// [keys][scales][key signs][key norms][value signs][value norms].
+struct StepSrc {
+    const uint8_t *kc;   // key records of row 0 (the batch element's)
+    const float *ks;     // scales of row 0
+    const uint8_t *qs;   // key sign records of row 0 (or null)
+    const float *qn;
+    const uint8_t *vs;   // value sign records of row 0 (or null)
+    const float *vn;
+};
+
+template <int KB>
+__device__ __forceinline__ void stage_step(uint8_t *buf, const StepSrc &src, int t, int last, int lane) {
+    constexpr int RK = 16 * KB;
+    const int rows_ok = min(kMassStep, last + 1 - t);  // whole rows of this step that exist
+    // keys: kMassStep * RK / 16 chunks
+    for (int i = lane; i < kMassStep * RK / 16; i += 32) {
+        const int row = (i * 16) / RK;
+        const bool ok = row < rows_ok;
+        cp_async16_zfill(buf + i * 16, ok ? src.kc + static_cast<size_t>(t) * RK + i * 16 : src.kc, ok ? 16 : 0);
+    }
+    uint8_t *p = buf + kMassStep * RK;
+    if (lane < kMassStep / 4) {  // scales: 4 per chunk
+        const bool ok = 4 * lane < rows_ok;
+        cp_async16_zfill(p + lane * 16, ok ? src.ks + t + 4 * lane : src.ks, ok ? 16 : 0);
+    }
+    p += kMassStep * 4;
+    if (src.qs) {
+        for (int i = lane; i < kMassStep; i += 32) {
+            const bool ok = i < rows_ok;
+            cp_async16_zfill(p + i * 16, ok ? src.qs + static_cast<size_t>(t + i) * 16 : src.qs, ok ? 16 : 0);
+        }
+        p += kMassStep * 16;
+        if (lane < kMassStep / 4) {
+            const bool ok = 4 * lane < rows_ok;
+            cp_async16_zfill(p + lane * 16, ok ? src.qn + t + 4 * lane : src.qn, ok ? 16 : 0);
+        }
+        p += kMassStep * 4;
+    }
+    if (src.vs) {
+        for (int i = lane; i < kMassStep; i += 32) {
+            const bool ok = i < rows_ok;
+            cp_async16_zfill(p + i * 16, ok ? src.vs + static_cast<size_t>(t + i) * 16 : src.vs, ok ? 16 : 0);
+        }
+        p += kMassStep * 16;
+        if (lane < kMassStep / 4) {
+            const bool ok = 4 * lane < rows_ok;
+            cp_async16_zfill(p + lane * 16, ok ? src.vn + t + 4 * lane : src.vn, ok ? 16 : 0);
+        }
+    }
+}
+
 // A warp's packed tokens [t0, t0 + kWarpTokens) of batch element b in
-// 16-token tiles, four per unrolled step (their loads are independent and
-// issue together, which keeps enough bytes in flight per SM).
+// 64-token steps staged through two shared buffers (the next step's copies in
+// flight while this one is scored), 16-token tiles within a step.
 template <int KB, bool QJL>
 __device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const DecodeWorkspace &ws,
                                                  const WorkItem &it, int b, int t0, size_t qbase,
-                                                 const MassShared &sh) {
+                                                 const MassShared &sh, uint8_t *buf0, int stage_bytes) {
     using KU = KUnpack<KB>;
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int gqa = dims.gqa, head = g >> 1, part = g & 1;
@@ -78,50 +133,65 @@ __device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const D
     const float m_c = c < gqa ? sh.mx[c] : 0.f, il_c = c < gqa ? sh.inv_l[c] : 0.f;
     const float inv_g = 1.0f / static_cast<float>(gqa);
     const int n = it.n_tokens;
-    const uint8_t *kc = it.kc + b * it.kstride;
-    const float *ks = it.ks + static_cast<size_t>(b) * it.sstride;
     float *mass = it.mass + static_cast<size_t>(b) * it.sstride;
     const int t_end = min(t0 + kWarpTokens, n);
     const int last = ((n + 15) & ~15) - 1;  // records exist up to the next multiple of 16
-    // four tiles per step with every row clamped into the segment, so that all
-    // their loads are unconditional and issue together (masked by t < n after)
-    for (int t4 = t0; t4 < t_end; t4 += 64) {
+    StepSrc src;
+    src.kc = it.kc + b * it.kstride;
+    src.ks = it.ks + static_cast<size_t>(b) * it.sstride;
+    src.qs = QJL ? it.qs + static_cast<size_t>(b) * it.qstride * (kJl / 8) : nullptr;
+    src.qn = QJL ? it.qn + static_cast<size_t>(b) * it.qstride : nullptr;
+    src.vs = nullptr;
+    src.vn = nullptr;
+    constexpr int RK = 16 * KB;
+    const int steps = (t_end - t0 + kMassStep - 1) / kMassStep;
+    stage_step<KB>(buf0, src, t0, last, lane);
+    cp_async_commit();
+    for (int st = 0; st < steps; st++) {
+        if (st + 1 < steps) stage_step<KB>(buf0 + ((st + 1) & 1) * stage_bytes, src, t0 + (st + 1) * kMassStep, last, lane);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncwarp();
+        const uint8_t *buf = buf0 + (st & 1) * stage_bytes;
+        const float *kss = reinterpret_cast<const float *>(buf + kMassStep * RK);
+        const uint8_t *qsb = buf + kMassStep * (RK + 4);
+        const float *qnb = reinterpret_cast<const float *>(qsb + kMassStep * 16);
+        const int ts = t0 + st * kMassStep;
 #pragma unroll
-    for (int tt = 0; tt < 4; tt++) {
-        const int tile = t4 + 16 * tt;
-        const int ta = tile + g, tb = ta + 8;
-        const int ra = min(ta, last), rb = min(tb, last);
-        float raw0, raw1;
-        qk_raw<KU, KB>(kc + static_cast<size_t>(ra) * (16 * KB) + 4 * KB * c,
-                       kc + static_cast<size_t>(rb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
-        float s0 = (ta < n ? ks[ra] : 0.f) * (aq * raw0 + beta * qsum);
-        float s1 = (tb < n ? ks[rb] : 0.f) * (aq * raw1 + beta * qsum);
-        if constexpr (QJL) {
-            const size_t r0 = static_cast<size_t>(b) * it.qstride;
-            float q0, q1;
-            qk_raw<SignUnpack, 1>(it.qs + (r0 + ra) * (kJl / 8) + 4 * c, it.qs + (r0 + rb) * (kJl / 8) + 4 * c, bt,
-                                  q0, q1);
-            constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
-            s0 += gam * (ta < n ? it.qn[r0 + ra] : 0.f) * (33554432.0f * q0 - tsum);
-            s1 += gam * (tb < n ? it.qn[r0 + rb] : 0.f) * (33554432.0f * q1 - tsum);
+        for (int tt = 0; tt < kMassStep / 16; tt++) {
+            const int la = 16 * tt + g, lb = la + 8;  // rows within the step
+            const int ta = ts + la, tb = ts + lb;
+            float raw0, raw1;
+            qk_raw<KU, KB>(buf + la * RK + 4 * KB * c, buf + lb * RK + 4 * KB * c, bq, raw0, raw1);
+            float s0 = (ta < n ? kss[la] : 0.f) * (aq * raw0 + beta * qsum);
+            float s1 = (tb < n ? kss[lb] : 0.f) * (aq * raw1 + beta * qsum);
+            if constexpr (QJL) {
+                float q0, q1;
+                qk_raw<SignUnpack, 1>(qsb + la * 16 + 4 * c, qsb + lb * 16 + 4 * c, bt, q0, q1);
+                constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
+                s0 += gam * (ta < n ? qnb[la] : 0.f) * (33554432.0f * q0 - tsum);
+                s1 += gam * (tb < n ? qnb[lb] : 0.f) * (33554432.0f * q1 - tsum);
+            }
+            float p0 = c < gqa ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c : 0.f;
+            float p1 = c < gqa ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c : 0.f;
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+            p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+            if (c == 0) {
+                if (ta < n) mass[ta] = p0 * inv_g;
+                if (tb < n) mass[tb] = p1 * inv_g;
+            }
         }
-        float p0 = c < gqa ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c : 0.f;
-        float p1 = c < gqa ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c : 0.f;
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-        p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-        if (c == 0) {
-            if (ta < n) mass[ta] = p0 * inv_g;
-            if (tb < n) mass[tb] = p1 * inv_g;
-        }
+        __syncwarp();  // the buffer is refilled two steps on
     }
-    }
+    cp_async_wait<0>();
 }
 
 __global__ void __launch_bounds__(kThreads, 4)
-    attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items) {
+    attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items, const int stage_bytes) {
     __shared__ __align__(16) MassShared sh;
+    extern __shared__ __align__(16) uint8_t dyn[];
     const int idx = find_mass_item(ws.items, n_items, blockIdx.x);
     const WorkItem &it = ws.items[idx];
     const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;  // CTAs per batch element
@@ -151,10 +221,11 @@ __global__ void __launch_bounds__(kThreads, 4)
         const int t0 = tok0 + kWarpTokens * warp;
         if (t0 >= it.n_tokens) return;
         const bool qj = it.qjl != 0;
+        uint8_t *buf0 = dyn + 2 * warp * stage_bytes;  // the warp's two step buffers
 #define TQ_MASS_CASE(K)                                                                \
     case K:                                                                            \
-        if (qj) mass_packed_warp<K, true>(dims, ws, it, b, t0, qbase, sh);             \
-        else mass_packed_warp<K, false>(dims, ws, it, b, t0, qbase, sh);               \
+        if (qj) mass_packed_warp<K, true>(dims, ws, it, b, t0, qbase, sh, buf0, stage_bytes);       \
+        else mass_packed_warp<K, false>(dims, ws, it, b, t0, qbase, sh, buf0, stage_bytes);         \
         break;
         switch (it.kb) {
             TQ_MASS_CASE(1)
@@ -165,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 4)
             TQ_MASS_CASE(6)
             TQ_MASS_CASE(7)
             default:
-                if (qj) mass_packed_warp<8, true>(dims, ws, it, b, t0, qbase, sh);
-                else mass_packed_warp<8, false>(dims, ws, it, b, t0, qbase, sh);
+                if (qj) mass_packed_warp<8, true>(dims, ws, it, b, t0, qbase, sh, buf0, stage_bytes);
+                else mass_packed_warp<8, false>(dims, ws, it, b, t0, qbase, sh, buf0, stage_bytes);
                 break;
         }
 #undef TQ_MASS_CASE
@@ -219,7 +290,8 @@ __device__ __forceinline__ int find_vqjl_item(const WorkItem *items, int n, int 
 
 template <int KB, bool QJL>
 __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWorkspace &ws, const WorkItem &it,
-                                          int b, int t0, size_t qbase, const MassShared &sh, float (*zsh)[kD]) {
+                                          int b, int t0, size_t qbase, const MassShared &sh, float (*zsh)[kD],
+                                          uint8_t *buf0, int stage_bytes) {
     using KU = KUnpack<KB>;
     using VS = VDec<1, 7>;  // sign records decode as 1-bit codes
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
@@ -244,10 +316,13 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
     }
     const float m_c = c < gqa ? sh.mx[c] : 0.f, il_c = c < gqa ? sh.inv_l[c] : 0.f;
     const int n = it.n_tokens;
-    const uint8_t *kc = it.kc + b * it.kstride;
-    const float *ks = it.ks + static_cast<size_t>(b) * it.sstride;
-    const uint8_t *vs = it.vqs + static_cast<size_t>(b) * it.vqstride * (kJl / 8);
-    const float *vn = it.vqn + static_cast<size_t>(b) * it.vqstride;
+    StepSrc src;
+    src.kc = it.kc + b * it.kstride;
+    src.ks = it.ks + static_cast<size_t>(b) * it.sstride;
+    src.qs = QJL ? it.qs + static_cast<size_t>(b) * it.qstride * (kJl / 8) : nullptr;
+    src.qn = QJL ? it.qn + static_cast<size_t>(b) * it.qstride : nullptr;
+    src.vs = it.vqs + static_cast<size_t>(b) * it.vqstride * (kJl / 8);
+    src.vn = it.vqn + static_cast<size_t>(b) * it.vqstride;
     VCtx vx;
     vx.off = 2 * c * 16 + 4 * (g >> 1);
     vx.sh = (g & 1) ? 0x7632 : 0x5410;
@@ -257,46 +332,60 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
     float wsum = 0.f;  // this lane's B-fragment weights: head g
     const int t_end = min(t0 + kWarpTokens, n);
     const int last = ((n + 15) & ~15) - 1;  // records exist up to the next multiple of 16
-    for (int t2 = t0; t2 < t_end; t2 += 32) {  // two tiles per step, rows clamped (as the mass pass)
+    constexpr int RK = 16 * KB;
+    constexpr int kSignOff = kMassStep * (RK + 4 + (QJL ? 20 : 0));  // value signs within a buffer
+    const int steps = (t_end - t0 + kMassStep - 1) / kMassStep;
+    stage_step<KB>(buf0, src, t0, last, lane);
+    cp_async_commit();
+    for (int st = 0; st < steps; st++) {
+        if (st + 1 < steps) stage_step<KB>(buf0 + ((st + 1) & 1) * stage_bytes, src, t0 + (st + 1) * kMassStep, last, lane);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncwarp();
+        const uint8_t *buf = buf0 + (st & 1) * stage_bytes;
+        const float *kss = reinterpret_cast<const float *>(buf + kMassStep * RK);
+        const uint8_t *qsb = buf + kMassStep * (RK + 4);
+        const float *qnb = reinterpret_cast<const float *>(qsb + kMassStep * 16);
+        const uint8_t *vsb = buf + kSignOff;
+        const float *vnb = reinterpret_cast<const float *>(vsb + kMassStep * 16);
+        const int ts = t0 + st * kMassStep;
+#pragma unroll 2
+        for (int tt = 0; tt < kMassStep / 16; tt++) {
+            const int la = 16 * tt + g, lb = la + 8;  // rows within the step
+            const int ta = ts + la, tb = ts + lb;
+            float raw0, raw1;
+            qk_raw<KU, KB>(buf + la * RK + 4 * KB * c, buf + lb * RK + 4 * KB * c, bq, raw0, raw1);
+            float s0 = (ta < n ? kss[la] : 0.f) * (aq * raw0 + beta * qsum);
+            float s1 = (tb < n ? kss[lb] : 0.f) * (aq * raw1 + beta * qsum);
+            if constexpr (QJL) {
+                float q0, q1;
+                qk_raw<SignUnpack, 1>(qsb + la * 16 + 4 * c, qsb + lb * 16 + 4 * c, bt, q0, q1);
+                constexpr float gam = 1.2533141373155003f / kJl;
+                s0 += gam * (ta < n ? qnb[la] : 0.f) * (33554432.0f * q0 - tsum);
+                s1 += gam * (tb < n ? qnb[lb] : 0.f) * (33554432.0f * q1 - tsum);
+            }
+            // weights of (token g, head c) and (token g + 8, head c), times the sketch norm
+            const float w0 = c < gqa && ta < n ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c * vnb[la] : 0.f;
+            const float w1 = c < gqa && tb < n ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c * vnb[lb] : 0.f;
+            // B fragment of head g: tokens 2c, 2c + 1 (rows 0-7) and 2c + 8, 2c + 9
+            const int sl = 8 * c + (g & 3);
+            float v0 = __shfl_sync(0xffffffffu, w0, sl), v1 = __shfl_sync(0xffffffffu, w0, sl + 4);
+            float v2 = __shfl_sync(0xffffffffu, w1, sl), v3 = __shfl_sync(0xffffffffu, w1, sl + 4);
+            if (g >= gqa) v0 = v1 = v2 = v3 = 0.f;
+            wsum += (v0 + v1) + (v2 + v3);
+            const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
+            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&h01), b1 = *reinterpret_cast<const uint32_t *>(&h23);
+            uint32_t fa[8], fb[8], fc[8], fd[8];
+            // rows past the records are zeros in the buffer (and their weights 0)
+            const uint8_t *vrow = vsb + 16 * tt * (kJl / 8);
+            VS::pair(vrow, kJl / 8, vx, fa, fb);                  // tokens 2c, 2c + 1
+            VS::pair(vrow + 8 * (kJl / 8), kJl / 8, vx, fc, fd);  // tokens 2c + 8, 2c + 9
 #pragma unroll
-    for (int tt = 0; tt < 2; tt++) {
-        const int tile = t2 + 16 * tt;
-        const int ta = tile + g, tb = ta + 8;
-        const int ra = min(ta, last), rb = min(tb, last);
-        float raw0, raw1;
-        qk_raw<KU, KB>(kc + static_cast<size_t>(ra) * (16 * KB) + 4 * KB * c,
-                       kc + static_cast<size_t>(rb) * (16 * KB) + 4 * KB * c, bq, raw0, raw1);
-        float s0 = (ta < n ? ks[ra] : 0.f) * (aq * raw0 + beta * qsum);
-        float s1 = (tb < n ? ks[rb] : 0.f) * (aq * raw1 + beta * qsum);
-        if constexpr (QJL) {
-            const size_t r0 = static_cast<size_t>(b) * it.qstride;
-            float q0, q1;
-            qk_raw<SignUnpack, 1>(it.qs + (r0 + ra) * (kJl / 8) + 4 * c, it.qs + (r0 + rb) * (kJl / 8) + 4 * c, bt,
-                                  q0, q1);
-            constexpr float gam = 1.2533141373155003f / kJl;
-            s0 += gam * (ta < n ? it.qn[r0 + ra] : 0.f) * (33554432.0f * q0 - tsum);
-            s1 += gam * (tb < n ? it.qn[r0 + rb] : 0.f) * (33554432.0f * q1 - tsum);
+            for (int mt = 0; mt < 8; mt++) mma16816(z[mt], fa[mt], fb[mt], fc[mt], fd[mt], b0, b1);
         }
-        // weights of (token g, head c) and (token g + 8, head c), times the sketch norm
-        const float w0 = c < gqa && ta < n ? ex2(fmaf(s0, dims.qk_scale, -m_c)) * il_c * vn[ra] : 0.f;
-        const float w1 = c < gqa && tb < n ? ex2(fmaf(s1, dims.qk_scale, -m_c)) * il_c * vn[rb] : 0.f;
-        // B fragment of head g: tokens 2c, 2c + 1 (rows 0-7) and 2c + 8, 2c + 9
-        const int src = 8 * c + (g & 3);
-        float v0 = __shfl_sync(0xffffffffu, w0, src), v1 = __shfl_sync(0xffffffffu, w0, src + 4);
-        float v2 = __shfl_sync(0xffffffffu, w1, src), v3 = __shfl_sync(0xffffffffu, w1, src + 4);
-        if (g >= gqa) v0 = v1 = v2 = v3 = 0.f;
-        wsum += (v0 + v1) + (v2 + v3);
-        const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
-        const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&h01), b1 = *reinterpret_cast<const uint32_t *>(&h23);
-        uint32_t fa[8], fb[8], fc[8], fd[8];
-        // a tile past the end reads the last whole tile (its weights are 0)
-        const uint8_t *vrow = vs + static_cast<size_t>(min(tile, last - 15)) * (kJl / 8);
-        VS::pair(vrow, kJl / 8, vx, fa, fb);                  // tokens 2c, 2c + 1
-        VS::pair(vrow + 8 * (kJl / 8), kJl / 8, vx, fc, fd);  // tokens 2c + 8, 2c + 9
-#pragma unroll
-        for (int mt = 0; mt < 8; mt++) mma16816(z[mt], fa[mt], fb[mt], fc[mt], fd[mt], b0, b1);
+        __syncwarp();  // the buffer is refilled two steps on
     }
-    }
+    cp_async_wait<0>();
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // W of head g
     const float W0 = __shfl_sync(0xffffffffu, wsum, 8 * c), W1 = __shfl_sync(0xffffffffu, wsum, 8 * c + 4);
@@ -313,9 +402,10 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
 }
 
 __global__ void __launch_bounds__(kThreads)
-    value_qjl_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items) {
+    value_qjl_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items, const int stage_bytes) {
     __shared__ __align__(16) MassShared sh;
     __shared__ float zsh[kMaxGqa][kD];
+    extern __shared__ __align__(16) uint8_t dyn[];
     const int idx = find_vqjl_item(ws.items, n_items, blockIdx.x);
     const WorkItem &it = ws.items[idx];
     const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;
@@ -338,10 +428,11 @@ __global__ void __launch_bounds__(kThreads)
     const int t0 = tok0 + kWarpTokens * warp;
     if (t0 < it.n_tokens) {
         const bool qj = it.qjl != 0;
+        uint8_t *buf0 = dyn + 2 * warp * stage_bytes;  // the warp's two step buffers
 #define TQ_VQJL_CASE(K)                                                            \
     case K:                                                                        \
-        if (qj) vqjl_warp<K, true>(dims, ws, it, b, t0, qbase, sh, zsh);           \
-        else vqjl_warp<K, false>(dims, ws, it, b, t0, qbase, sh, zsh);             \
+        if (qj) vqjl_warp<K, true>(dims, ws, it, b, t0, qbase, sh, zsh, buf0, stage_bytes);     \
+        else vqjl_warp<K, false>(dims, ws, it, b, t0, qbase, sh, zsh, buf0, stage_bytes);       \
         break;
         switch (it.kb) {
             TQ_VQJL_CASE(1)
@@ -352,8 +443,8 @@ __global__ void __launch_bounds__(kThreads)
             TQ_VQJL_CASE(6)
             TQ_VQJL_CASE(7)
             default:
-                if (qj) vqjl_warp<8, true>(dims, ws, it, b, t0, qbase, sh, zsh);
-                else vqjl_warp<8, false>(dims, ws, it, b, t0, qbase, sh, zsh);
+                if (qj) vqjl_warp<8, true>(dims, ws, it, b, t0, qbase, sh, zsh, buf0, stage_bytes);
+                else vqjl_warp<8, false>(dims, ws, it, b, t0, qbase, sh, zsh, buf0, stage_bytes);
                 break;
         }
 #undef TQ_VQJL_CASE
@@ -397,16 +488,23 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace dec
 
 cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                             const float *S, cudaStream_t s) {
-    dec::value_qjl_kernel<<<n_ctas, dec::kThreads, 0, s>>>(dims, ws, n_items);
+                             int stage_bytes, const float *S, cudaStream_t s) {
+    const int dyn = 2 * (dec::kThreads / 32) * stage_bytes;
+    cudaError_t e = cudaFuncSetAttribute(dec::value_qjl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return e;
+    dec::value_qjl_kernel<<<n_ctas, dec::kThreads, dyn, s>>>(dims, ws, n_items, stage_bytes);
     const int n_warps = dims.L * dims.B * dims.Hq;
     dec::value_qjl_apply_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                                  cudaStream_t s) {
-    dec::attention_mass_kernel<<<n_ctas, dec::kThreads, 0, s>>>(dims, ws, n_items);
+                                  int stage_bytes, cudaStream_t s) {
+    const int dyn = 2 * (dec::kThreads / 32) * stage_bytes;
+    cudaError_t e =
+        cudaFuncSetAttribute(dec::attention_mass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return e;
+    dec::attention_mass_kernel<<<n_ctas, dec::kThreads, dyn, s>>>(dims, ws, n_items, stage_bytes);
     return cudaGetLastError();
 }
 
