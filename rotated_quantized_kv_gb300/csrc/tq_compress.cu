@@ -156,12 +156,32 @@ __device__ __forceinline__ uint32_t search_smem(float u, const float *t) {
     return k;
 }
 
+// The projection matrix S (jl x d binary32) in shared memory: row j holds
+// 32 16-byte chunks, quarter qq's chunk i4 (coordinates 32 qq + 4 i4 ..) at
+// chunk 8 qq + (i4 ^ qq), so that the four quarters a warp reads together
+// (same row and i4, one per lane q) fall in four different bank groups.
+constexpr int kSketchSmem = kJl * kD * 4;
+
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void stage_sketch_matrix(const float *S, uint8_t *dst) {
+    for (int idx = threadIdx.x; idx < kJl * kD / 4; idx += blockDim.x) {
+        const int j = idx >> 5, c = idx & 31, qq = c >> 3, i4 = c & 7;
+        reinterpret_cast<float4 *>(dst)[j * 32 + qq * 8 + (i4 ^ qq)] = __ldg(reinterpret_cast<const float4 *>(S) + idx);
+    }
+}
+
 // Sketch of a residual held by four lanes (this lane's coordinates [32 q,
 // 32 q + 32) in r): p_j = sum_i S[j][i] r_i in binary32 (any order: the only
 // decision is the sign); bit j = (p_j >= 0); rho = ||r||_2.  Each lane forms
 // the partial sum over its 32 coordinates, the four lanes add them, and lane q
-// keeps the signs of projections [32 q, 32 q + 32).
-__device__ __forceinline__ void qjl_sketch(const float *S, const float (&y)[kQ], int q, bool store, uint8_t *rec,
+// keeps the signs of projections [32 q, 32 q + 32).  S_sm: the shared address
+// of the staged matrix.
+__device__ __forceinline__ void qjl_sketch(uint32_t S_sm, const float (&y)[kQ], int q, bool store, uint8_t *rec,
                                            float *norm) {
     {
         float ss = 0.0f;
@@ -175,12 +195,12 @@ __device__ __forceinline__ void qjl_sketch(const float *S, const float (&y)[kQ],
             uint32_t word = 0;
 #pragma unroll 1
             for (int jj = 0; jj < 32; jj += 2) {  // two projections, four partial sums each
-                const float4 *S0 = reinterpret_cast<const float4 *>(S + (32 * jc + jj) * kD + q * kQ);
-                const float4 *S1 = S0 + kD / 4;
+                const uint32_t S0 = S_sm + static_cast<uint32_t>((32 * jc + jj) * kD * 4 + q * kQ * 4);
                 float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i4 = 0; i4 < kQ / 4; i4++) {
-                    const float4 s = __ldg(S0 + i4), t = __ldg(S1 + i4);
+                    const uint32_t o = static_cast<uint32_t>((i4 ^ q) * 16);
+                    const float4 s = lds128(S0 + o), t = lds128(S0 + kD * 4 + o);
                     const int e = i4 & 3;
                     a0[e] = fmaf(s.x, y[4 * i4], a0[e]);
                     a0[e] = fmaf(s.y, y[4 * i4 + 1], a0[e]);
@@ -212,7 +232,7 @@ __device__ __forceinline__ void qjl_sketch(const float *S, const float (&y)[kQ],
 // block's end (the lanes still run so that their exchanges stay warp-uniform).
 template <int KB, bool QJL>
 __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ], int q, int b, int h, int pos,
-                                         bool store) {
+                                         bool store, uint32_t S_sm = 0) {
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < kQ; i++) m = fmaxf(m, fabsf(y[i]));
@@ -248,9 +268,9 @@ __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ]
     if constexpr (QJL) {
         if (store) {
             const size_t qi = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
-            qjl_sketch(p.S, y, q, true, p.qjl_signs + qi * (kJl / 8), p.qjl_norm + qi);
+            qjl_sketch(S_sm, y, q, true, p.qjl_signs + qi * (kJl / 8), p.qjl_norm + qi);
         } else {
-            qjl_sketch(p.S, y, q, false, nullptr, nullptr);
+            qjl_sketch(S_sm, y, q, false, nullptr, nullptr);
         }
     }
 }
@@ -260,7 +280,8 @@ __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ]
 // difference, c the centroids in cent_smem).
 template <int VB, bool QJLV = false>
 __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[kQ], const float *thr_smem, int q,
-                                           int b, int h, int pos, bool store, const float *cent_smem = nullptr) {
+                                           int b, int h, int pos, bool store, const float *cent_smem = nullptr,
+                                           uint32_t S_sm = 0) {
     // pairwise tree of squares in index order: this lane's 32 give one of the
     // four subtrees two levels under the root; the root adds
     // (q0 + q1) + (q2 + q3)
@@ -312,9 +333,9 @@ __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[k
     if constexpr (QJLV) {
         if (store) {
             const size_t qi = (static_cast<size_t>(b) * p.nv + p.vrank[h]) * p.capacity + pos;
-            qjl_sketch(p.S, y, q, true, p.vqjl_signs + qi * (kJl / 8), p.vqjl_norm + qi);
+            qjl_sketch(S_sm, y, q, true, p.vqjl_signs + qi * (kJl / 8), p.vqjl_norm + qi);
         } else {
-            qjl_sketch(p.S, y, q, false, nullptr, nullptr);
+            qjl_sketch(S_sm, y, q, false, nullptr, nullptr);
         }
     }
 }
@@ -322,19 +343,20 @@ __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[k
 // One key vector of the compress path: rotate, then quantize.
 template <int KB, bool QJL>
 __device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
-                                        const float *out_scale, int q, int b, int h, int pos, bool store) {
+                                        const float *out_scale, int q, int b, int h, int pos, bool store,
+                                        uint32_t S_sm) {
     float y[kQ];
     load_rotate(qrow, in_mask, out_scale, q, y);
-    key_tail<KB, QJL>(p, y, q, b, h, pos, store);
+    key_tail<KB, QJL>(p, y, q, b, h, pos, store, S_sm);
 }
 
 template <int VB, bool QJLV>
 __device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
                                           const float *out_scale, const float *thr_smem, const float *cent_smem,
-                                          int q, int b, int h, int pos, bool store) {
+                                          int q, int b, int h, int pos, bool store, uint32_t S_sm) {
     float y[kQ];
     load_rotate(qrow, in_mask, out_scale, q, y);
-    value_tail<VB, QJLV>(p, y, thr_smem, q, b, h, pos, store, cent_smem);
+    value_tail<VB, QJLV>(p, y, thr_smem, q, b, h, pos, store, cent_smem, S_sm);
 }
 
 // Stage the rows of block `blk` (t-block fastest, then head, then batch) of
@@ -361,6 +383,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);          // [128]
     float *thr = out_scale + kD;                                             // [kCbTotal]
     float *cent = thr + kCbTotal;                                            // [kCbTotal]
+    uint8_t *S_stage = reinterpret_cast<uint8_t *>(cent + kCbTotal);         // [jl][d] when sketching
+    const uint32_t S_sm = static_cast<uint32_t>(__cvta_generic_to_shared(S_stage));
 
     const int n_tblk = (p.T + kTok - 1) / kTok;
     const int n_blk = n_tblk * p.H * p.B;
@@ -386,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         thr[j] = p.thr[j];
         cent[j] = p.cent[j];
     }
+    if (p.nq > 0 || p.nv > 0) stage_sketch_matrix(p.S, S_stage);
     __syncthreads();  // tables written
 
     for (int it = 0; blk < n_blk; blk += gridDim.x, it++) {
@@ -405,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             const bool qj = p.qrank[h] >= 0;
             switch (p.kbits[h] * 2 + (qj ? 1 : 0)) {
 #define TQ_KEY_CASE(KB)                                                                                 \
-    case 2 * KB: key_vector<KB, false>(p, qrow, in_mask, out_scale, q, b, h, pos, store); break;       \
-    case 2 * KB + 1: key_vector<KB, true>(p, qrow, in_mask, out_scale, q, b, h, pos, store); break;
+    case 2 * KB: key_vector<KB, false>(p, qrow, in_mask, out_scale, q, b, h, pos, store, S_sm); break;   \
+    case 2 * KB + 1: key_vector<KB, true>(p, qrow, in_mask, out_scale, q, b, h, pos, store, S_sm); break;
                 TQ_KEY_CASE(1) TQ_KEY_CASE(2) TQ_KEY_CASE(3) TQ_KEY_CASE(4)
                 TQ_KEY_CASE(5) TQ_KEY_CASE(6) TQ_KEY_CASE(7) TQ_KEY_CASE(8)
 #undef TQ_KEY_CASE
@@ -418,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             const bool qv = p.vrank[h] >= 0;
             switch (vb * 2 + (qv ? 1 : 0)) {
 #define TQ_VAL_CASE(VB)                                                                                         \
-    case 2 * VB: value_vector<VB, false>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store); break;       \
-    case 2 * VB + 1: value_vector<VB, true>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store); break;
+    case 2 * VB: value_vector<VB, false>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store, S_sm); break;   \
+    case 2 * VB + 1: value_vector<VB, true>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store, S_sm); break;
                 TQ_VAL_CASE(1) TQ_VAL_CASE(2) TQ_VAL_CASE(3) TQ_VAL_CASE(4)
                 TQ_VAL_CASE(5) TQ_VAL_CASE(6) TQ_VAL_CASE(7) TQ_VAL_CASE(8)
 #undef TQ_VAL_CASE
@@ -596,21 +621,23 @@ __global__ void dequant_kernel(const __grid_constant__ DequantParams p) {
 
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s) {
     static bool configured = false;
-    const size_t smem = compress_smem();
+    // launches with sketched heads also stage S (two CTAs per SM instead of three)
+    const bool sketch = p.nq > 0 || p.nv > 0;
+    const size_t smem = compress_smem() + (sketch ? kSketchSmem : 0);
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+                                             static_cast<int>(compress_smem() + kSketchSmem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    // persistent: three CTAs per SM, each group looping over 32-token blocks
+    // persistent: three (two) CTAs per SM, each group looping over 32-token blocks
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const long long n_blk = static_cast<long long>((p.T + kTok - 1) / kTok) * p.H * p.B;
     if (n_blk == 0) return cudaSuccess;
-    const int grid = static_cast<int>(std::min<long long>(n_blk, 3LL * sms));
+    const int grid = static_cast<int>(std::min<long long>(n_blk, (sketch ? 2LL : 3LL) * sms));
     compress_kernel<<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
