@@ -85,13 +85,16 @@ __device__ __forceinline__ void load_rotate(const uint8_t *qrow, const uint32_t 
             }
         }
     }
+    // the upper lane's o - a is fma(-1, a, o) and the lower lane's a + o is
+    // fma(1, a, o): one rounding of an exact product, the same bits (signed
+    // zeros included) as the subtraction or addition
 #pragma unroll
     for (int x = 1; x <= 2; x <<= 1) {
-        const bool upper = (q & x) != 0;
+        const float sgn = (q & x) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < kQ; i++) {
             const float o = __shfl_xor_sync(0xffffffffu, a[i], x);
-            a[i] = upper ? __fsub_rn(o, a[i]) : __fadd_rn(a[i], o);
+            a[i] = __fmaf_rn(sgn, a[i], o);
         }
     }
 #pragma unroll
@@ -247,8 +250,9 @@ __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ]
 #pragma unroll
     for (int i = 0; i < kQ; i++) {
         const float v = __fmul_rn(y[i], r);
-        const float t = __fadd_rn(v, 1.0f);
-        float u = __fmul_rn(t, half_cells);  // exact: power of two
+        // round(v + 1) 2^(KB-1) = round(v 2^(KB-1) + 2^(KB-1)): scaling by a
+        // power of two commutes with the rounding (v + 1 is never subnormal)
+        float u = __fmaf_rn(v, half_cells, half_cells);
         u = fminf(fmaxf(u, 0.0f), top);
         // floor(u) for u in [0, 255]: 2^23 + u rounded toward -inf is 2^23 + floor(u)
         const uint32_t k = __float_as_uint(__fadd_rd(u, 8388608.0f)) & 0xFFu;
