@@ -64,7 +64,7 @@ __device__ __forceinline__ void load_rotate(const uint8_t *qrow, const uint32_t 
 #pragma unroll
     for (int c = 0; c < 4; c++) {
         uint4 v = *reinterpret_cast<const uint4 *>(qrow + c * 16);
-        const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + q * 16 + c * 4);
+        const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + (c * 4 + q) * 4);
         v.x ^= mk.x; v.y ^= mk.y; v.z ^= mk.z; v.w ^= mk.w;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -99,7 +99,7 @@ __device__ __forceinline__ void load_rotate(const uint8_t *qrow, const uint32_t 
     }
 #pragma unroll
     for (int c = 0; c < kQ / 4; c++) {
-        const float4 s = *reinterpret_cast<const float4 *>(out_scale + q * kQ + 4 * c);
+        const float4 s = *reinterpret_cast<const float4 *>(out_scale + (c * 4 + q) * 4);
         a[4 * c] = __fmul_rn(a[4 * c], s.x);
         a[4 * c + 1] = __fmul_rn(a[4 * c + 1], s.y);
         a[4 * c + 2] = __fmul_rn(a[4 * c + 2], s.z);
@@ -383,6 +383,8 @@ __device__ __forceinline__ void stage_block(const CompressParams &p, int n_tblk,
 __global__ void __launch_bounds__(kThreads, 3)
     compress_kernel(const __grid_constant__ CompressParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
+    // sign masks and output scales, 16-byte chunk c of quarter q at chunk
+    // 4 c + q: the four quarters a warp reads together sit in four bank groups
     uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + 4 * kGroupBuf);  // [64]
     float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);          // [128]
     float *thr = out_scale + kD;                                             // [kCbTotal]
@@ -403,12 +405,13 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int i = 2 * threadIdx.x;
         const uint32_t s0 = (p.sign_bits[i >> 5] >> (i & 31)) & 1u;
         const uint32_t s1 = (p.sign_bits[(i + 1) >> 5] >> ((i + 1) & 31)) & 1u;
-        in_mask[threadIdx.x] = (s0 << 15) | (s1 << 31);
+        const int t = threadIdx.x;  // coordinates 2t, 2t + 1: quarter t / 16, chunk (t / 4) % 4
+        in_mask[((((t >> 2) & 3) * 4) + (t >> 4)) * 4 + (t & 3)] = (s0 << 15) | (s1 << 31);
     }
     if (threadIdx.x < kD) {
         const int i = threadIdx.x;
         const uint32_t s = (p.sign_bits[i >> 5] >> (i & 31)) & 1u;
-        out_scale[i] = s ? -p.inv_sqrt_d : p.inv_sqrt_d;
+        out_scale[((((i >> 2) & 7) * 4) + (i >> 5)) * 4 + (i & 3)] = s ? -p.inv_sqrt_d : p.inv_sqrt_d;
     }
     for (int j = threadIdx.x; j < kCbTotal; j += kThreads) {
         thr[j] = p.thr[j];
