@@ -196,7 +196,7 @@ __device__ __forceinline__ void qjl_sketch(uint32_t S_sm, const float (&y)[kQ], 
 #pragma unroll 1
         for (int jc = 0; jc < 4; jc++) {  // projections 32 jc .. 32 jc + 31
             uint32_t word = 0;
-#pragma unroll 1
+#pragma unroll 4  // eight projections' shared loads in flight
             for (int jj = 0; jj < 32; jj += 2) {  // two projections, four partial sums each
                 const uint32_t S0 = S_sm + static_cast<uint32_t>((32 * jc + jj) * kD * 4 + q * kQ * 4);
                 float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
