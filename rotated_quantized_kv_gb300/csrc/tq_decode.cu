@@ -43,9 +43,9 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *
 // (item, batch element, 64-token chunk): a single staged chunk, so that many
 // small CTAs (six per SM) cover the memory latency together.
 __global__ void __launch_bounds__(kThreads, 6)
-    decode_fp16_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int item_lo, const int item_hi) {
+    decode_fp16_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int idx = find_item(ws.items, item_lo, item_hi, blockIdx.x);
+    const int idx = cta_item[blockIdx.x];
     const WorkItem &it = ws.items[idx];
     const int local = blockIdx.x - it.cta_begin;
     const int b = local / it.n_chunks, chunk = local - b * it.n_chunks;
@@ -235,7 +235,8 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         const PackedLauncher fn = dec::packed_launcher(c.kb, c.vb, c.qjl != 0);
         if (!fn) return cudaErrorInvalidValue;
         const cudaError_t e =
-            fn(dims, ws, c.item_lo, c.item_hi, c.n_ctas, c.n_stages, value_half[i], value_c1[i], s, !first);
+            fn(dims, ws, c.item_lo, c.item_hi, ws.cta_item + c.cta_off, c.n_ctas, c.n_stages, value_half[i],
+               value_c1[i], s, !first);
         if (e != cudaSuccess) return e;
         first = false;
         ++*n_launched;
@@ -254,7 +255,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = first ? 0 : 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel, dims, ws, c.item_lo, c.item_hi);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel, dims, ws, ws.cta_item + c.cta_off);
         if (e != cudaSuccess) return e;
         ++*n_launched;
         first = false;

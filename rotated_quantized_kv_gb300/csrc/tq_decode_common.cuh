@@ -535,16 +535,6 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
     __syncthreads();
 }
 
-// Largest i in [lo, hi) with items[i].cta_begin <= cta.
-__device__ __forceinline__ int find_item(const WorkItem *items, int lo, int hi, int cta) {
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (items[mid].cta_begin <= cta) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
-
 // Write one warp's state as a partial record (no cross-warp merge): for each
 // query head c < gqa, m (base-2 units) and l, and the 128 accumulator dims;
 // dim_of(mt, r) is the head dimension of accumulator row r of m-tile mt.
@@ -564,16 +554,6 @@ __device__ __forceinline__ void write_warp_partial(WarpState &st, float *rec_bas
             rec[4 + dim_of(mt, 1)] = st.acc[mt][2] + st.acc[mt][3];
         }
     }
-}
-
-// Largest i in [lo, hi) with items[i].stage_begin <= s.
-__device__ __forceinline__ int find_stage_item(const WorkItem *items, int lo, int hi, long long s) {
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (items[mid].stage_begin <= s) lo = mid;
-        else hi = mid;
-    }
-    return lo;
 }
 
 // Equal contiguous ranges of S stages over G persistent CTAs: CTA i takes

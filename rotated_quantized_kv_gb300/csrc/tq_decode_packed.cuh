@@ -479,8 +479,9 @@ struct StageCursor {
             qn = it.qn + static_cast<size_t>(b) * it.qstride;
         }
     }
-    __device__ __forceinline__ void locate(const WorkItem *items, int lo, int hi, long long s) {
-        item = find_stage_item(items, lo, hi, s);
+    // stage s of the launch, in item `it` (the host's per-CTA table)
+    __device__ __forceinline__ void locate(const WorkItem *items, int it, long long s) {
+        item = it;
         const long long r = s - items[item].stage_begin;
         const int ns = items[item].n_stages;
         b = static_cast<int>(r / ns);
@@ -507,7 +508,7 @@ struct StageCursor {
 // (layer, batch, KV head) merges the partials (finish_and_combine).
 template <int KB, int VB, bool QJL>
 __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
-    decode_packed_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int item_lo, const int item_hi,
+    decode_packed_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item,
                          const long long S, const __grid_constant__ ValueTable vt) {
     using G = PackedGeom<KB, VB, QJL>;
     using KU = KUnpack<KB>;
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + G::bar);
     StageCursor<QJL, true> lc;
     if (threadIdx.x == 0) {
-        lc.locate(ws.items, item_lo, item_hi, s_begin);
+        lc.locate(ws.items, cta_item[blockIdx.x], s_begin);
 #pragma unroll
         for (int i = 0; i < NS; i++) mbar_init(&full[i], 1);
         mbar_init_fence();
@@ -601,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
 
     // ---- consumer
     StageCursor<QJL, false> cc;
-    cc.locate(ws.items, item_lo, item_hi, s_begin);
+    cc.locate(ws.items, cta_item[blockIdx.x], s_begin);
     int g_layer = 0, g_head = 0, g_b = 0, g_item = 0;
     long long g_stage0 = 0;  // class stage index of the group's first stage
     uint32_t bq[16], bt[16];
@@ -753,9 +754,9 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
 }
 
 template <int KB, int VB, bool QJL>
-cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int item_lo, int item_hi, int n_ctas,
-                          long long n_stages, const unsigned short *value_half, float value_c1, cudaStream_t s,
-                          bool pdl) {
+cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int item_lo, int item_hi,
+                          const int *cta_item, int n_ctas, long long n_stages, const unsigned short *value_half,
+                          float value_c1, cudaStream_t s, bool pdl) {
     using G = PackedGeom<KB, VB, QJL>;
     static bool configured = false;
     if (!configured) {
@@ -779,7 +780,9 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL>, dims, ws, item_lo, item_hi, n_stages, vt);
+    (void)item_lo;
+    (void)item_hi;
+    return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL>, dims, ws, cta_item, n_stages, vt);
 }
 
 }  // namespace dec

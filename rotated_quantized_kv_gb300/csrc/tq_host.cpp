@@ -323,8 +323,13 @@ struct Plan {
     int mass_ctas = 0;  // CTAs of the attention-mass launch (0: no segment asked for mass)
     int vqjl_ctas = 0;  // CTAs of the value-sketch launch (0: no value sketch)
     int mass_stage = 0, vqjl_stage = 0;  // bytes of one step buffer of each rescoring launch
+    // work item of every CTA: the class launches' tables (ClassLaunch::cta_off),
+    // then the attention-mass launch's (mass_cta_off), then the value-sketch one's
+    std::vector<int> cta_item;
+    int mass_cta_off = 0, vqjl_cta_off = 0;
     std::vector<int> grp_part, grp_nparts, lbh_total;
     size_t off_items = 0, off_layer = 0, off_grp_part = 0, off_grp_nparts = 0, off_lbh_total = 0, off_counter = 0;
+    size_t off_cta_item = 0;
     size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, off_ml = 0, off_z = 0, total = 0;
 };
 
@@ -333,6 +338,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // The persistent CTA (of G sharing S stages in equal contiguous ranges
 // [i S / G, (i+1) S / G)) that holds stage s; same arithmetic as the kernels.
 long long dec_cta_of_stage(long long s, long long S, long long G) { return ((s + 1) * G + S - 1) / S - 1; }
+// first stage of CTA i of a packed launch (the kernels' range_begin)
+long long dec_range_begin(long long i, long long S, long long G) { return i * S / G; }
 
 // Decode class of an item: one kernel instantiation and one value table each
 // (fp16 items form one class after all packed ones).
@@ -578,6 +585,38 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         P.vqjl_ctas = static_cast<int>(vc);
         P.vqjl_stage = mass_stage_bytes(vkb, vq, true);
     }
+    {  // per-CTA work items: stage range_begin(i) of a packed launch, chunk CTA i
+       // of the fp16 launch, the CTAs of each mass / value-sketch item
+        size_t total = static_cast<size_t>(P.mass_ctas) + P.vqjl_ctas;
+        for (const ClassLaunch &c : P.classes) total += c.n_ctas;
+        P.cta_item.clear();
+        P.cta_item.reserve(total);
+        for (ClassLaunch &c : P.classes) {
+            c.cta_off = static_cast<int>(P.cta_item.size());
+            int it = c.item_lo;
+            for (int i = 0; i < c.n_ctas; ++i) {
+                if (c.kb != 16) {
+                    const long long s0 = dec_range_begin(i, c.n_stages, c.n_ctas);
+                    while (it + 1 < c.item_hi && P.items[it + 1].stage_begin <= s0) ++it;
+                } else {
+                    while (it + 1 < c.item_hi && P.items[it + 1].cta_begin <= i) ++it;
+                }
+                P.cta_item.push_back(it);
+            }
+        }
+        P.mass_cta_off = static_cast<int>(P.cta_item.size());
+        for (size_t i = 0; i < P.items.size(); ++i)
+            if (P.items[i].mass) {
+                const long long n = static_cast<long long>(B) * ((P.items[i].n_tokens + kMassTokens - 1) / kMassTokens);
+                P.cta_item.insert(P.cta_item.end(), static_cast<size_t>(n), static_cast<int>(i));
+            }
+        P.vqjl_cta_off = static_cast<int>(P.cta_item.size());
+        for (size_t i = 0; i < P.items.size(); ++i)
+            if (P.items[i].vqs) {
+                const long long n = static_cast<long long>(B) * ((P.items[i].n_tokens + kMassTokens - 1) / kMassTokens);
+                P.cta_item.insert(P.cta_item.end(), static_cast<size_t>(n), static_cast<int>(i));
+            }
+    }
     DecodeDims &D = P.dims;
     D.L = n_layers;
     D.B = B;
@@ -605,6 +644,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     off += align256(sizeof(int) * std::max<size_t>(P.grp_nparts.size(), 1));
     P.off_lbh_total = off;
     off += align256(static_cast<size_t>(n_layers) * B * H * sizeof(int));
+    P.off_cta_item = off;
+    off += align256(sizeof(int) * std::max<size_t>(P.cta_item.size(), 1));
     P.off_counter = off;
     off += align256(static_cast<size_t>(n_layers) * B * H * sizeof(int));
     P.off_qrot = off;  // the uploaded plan ends here
@@ -1055,6 +1096,8 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
             std::memcpy(host + P.off_grp_nparts, P.grp_nparts.data(), sizeof(int) * P.grp_nparts.size());
         }
         std::memcpy(host + P.off_lbh_total, P.lbh_total.data(), sizeof(int) * P.lbh_total.size());
+        if (!P.cta_item.empty())
+            std::memcpy(host + P.off_cta_item, P.cta_item.data(), sizeof(int) * P.cta_item.size());
         e = cudaMemcpyAsync(ws, host, P.off_qrot, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e);
         e = cudaEventRecord(sl.ev, s);
@@ -1067,6 +1110,9 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     W.grp_nparts = reinterpret_cast<int *>(ws + P.off_grp_nparts);
     W.lbh_total = reinterpret_cast<int *>(ws + P.off_lbh_total);
     W.counter = reinterpret_cast<int *>(ws + P.off_counter);
+    W.cta_item = reinterpret_cast<const int *>(ws + P.off_cta_item);
+    W.mass_cta_item = W.cta_item + P.mass_cta_off;
+    W.vqjl_cta_item = W.cta_item + P.vqjl_cta_off;
     W.error = reinterpret_cast<int *>(ws);
     W.qrot = reinterpret_cast<uint32_t *>(ws + P.off_qrot);
     W.qjlt = reinterpret_cast<uint32_t *>(ws + P.off_qjlt);
@@ -1116,11 +1162,11 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
     e = launch_decode_kernels(P.dims, W, P.classes.data(), static_cast<int>(P.classes.size()), qjl_S,
                               class_half.data(), class_c1.data(), s, g_ev_start, g_ev_stop, &launched);
     if (e == cudaSuccess && P.mass_ctas > 0) {
-        e = launch_attention_mass(P.dims, W, static_cast<int>(P.items.size()), P.mass_ctas, P.mass_stage, s);
+        e = launch_attention_mass(P.dims, W, P.mass_ctas, P.mass_stage, s);
         ++launched;
     }
     if (e == cudaSuccess && P.vqjl_ctas > 0) {
-        e = launch_value_qjl(P.dims, W, static_cast<int>(P.items.size()), P.vqjl_ctas, P.vqjl_stage, qjl_S, s);
+        e = launch_value_qjl(P.dims, W, P.vqjl_ctas, P.vqjl_stage, qjl_S, s);
         launched += 2;
     }
     g_last_launches.store(launched);

@@ -149,6 +149,12 @@ struct DecodeWorkspace {
     float *z;          // [L][B][Hq][d]: sum_t p_t rho_t s_t of the value sketches (null: none)
     const uint16_t *q; // the caller's queries, fp16 [L][B][Hq][d]
     float *out;        // the caller's output, [L][B][Hq][d]
+    // per-CTA work item of each launch (host-computed, one load instead of a
+    // search): the split-K classes' tables (each launch gets its own offset),
+    // the attention-mass and the value-sketch launches'
+    const int *cta_item;
+    const int *mass_cta_item;
+    const int *vqjl_cta_item;
 };
 
 // Stage geometry of the split-K kernels: the fp16 kernel takes 64 tokens per
@@ -166,6 +172,7 @@ struct ClassLaunch {
     int law;           // value codebook law
     int item_lo, item_hi, n_ctas;
     long long n_stages;
+    int cta_off;       // this launch's per-CTA item table within DecodeWorkspace::cta_item
 };
 
 // Resident CTAs per SM of the packed split-K kernels (registers and shared
@@ -176,7 +183,8 @@ constexpr int kPackedCtasPerSmQjl = 3;
 __host__ __device__ constexpr int packed_ctas_per_sm(bool qjl) { return qjl ? kPackedCtasPerSmQjl : kPackedCtasPerSm; }
 
 typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, int item_lo, int item_hi,
-                                      int n_ctas, long long n_stages, const unsigned short *value_half,
+                                      const int *cta_item, int n_ctas, long long n_stages,
+                                      const unsigned short *value_half,
                                       float value_c1,
                                       cudaStream_t s, bool pdl);
 PackedLauncher packed_launcher_kb1(int vb, bool qjl);

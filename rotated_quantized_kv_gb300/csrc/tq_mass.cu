@@ -29,16 +29,6 @@ namespace {
 static_assert(kMassTokens % (16 * (kThreads / 32)) == 0, "whole 16-token tiles per warp");
 constexpr int kWarpTokens = kMassTokens / (kThreads / 32);  // packed tokens per warp
 
-// largest i in [0, n) with items[i].mass_cta_begin <= cta
-__device__ __forceinline__ int find_mass_item(const WorkItem *items, int n, int cta) {
-    int lo = 0, hi = n;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (items[mid].mass_cta_begin <= cta) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
 
 struct MassShared {
     float qf[kMaxGqa][kD];       // unrotated queries (fp16 items)
@@ -189,10 +179,10 @@ __device__ __forceinline__ void mass_packed_warp(const DecodeDims &dims, const D
 }
 
 __global__ void __launch_bounds__(kThreads, 4)
-    attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items, const int stage_bytes) {
+    attention_mass_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int stage_bytes) {
     __shared__ __align__(16) MassShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
-    const int idx = find_mass_item(ws.items, n_items, blockIdx.x);
+    const int idx = ws.mass_cta_item[blockIdx.x];
     const WorkItem &it = ws.items[idx];
     const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;  // CTAs per batch element
     const int local = blockIdx.x - it.mass_cta_begin;
@@ -278,15 +268,6 @@ __global__ void __launch_bounds__(kThreads, 4)
 // 1-bit value decoder), so the accumulator holds sum_t w bit 2^(s - 24) and
 // sum_t w s = 2 sum_t w bit - sum_t w.  The CTA's warps add into shared memory,
 // the CTA into z with one atomic per (head, coordinate).
-__device__ __forceinline__ int find_vqjl_item(const WorkItem *items, int n, int cta) {
-    int lo = 0, hi = n;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (items[mid].vqjl_cta_begin <= cta) lo = mid;
-        else hi = mid;
-    }
-    return lo;
-}
 
 template <int KB, bool QJL>
 __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWorkspace &ws, const WorkItem &it,
@@ -402,11 +383,11 @@ __device__ __forceinline__ void vqjl_warp(const DecodeDims &dims, const DecodeWo
 }
 
 __global__ void __launch_bounds__(kThreads)
-    value_qjl_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int n_items, const int stage_bytes) {
+    value_qjl_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int stage_bytes) {
     __shared__ __align__(16) MassShared sh;
     __shared__ float zsh[kMaxGqa][kD];
     extern __shared__ __align__(16) uint8_t dyn[];
-    const int idx = find_vqjl_item(ws.items, n_items, blockIdx.x);
+    const int idx = ws.vqjl_cta_item[blockIdx.x];
     const WorkItem &it = ws.items[idx];
     const int nch = (it.n_tokens + kMassTokens - 1) / kMassTokens;
     const int local = blockIdx.x - it.vqjl_cta_begin;
@@ -487,24 +468,24 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 }  // namespace dec
 
-cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
+cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_ctas,
                              int stage_bytes, const float *S, cudaStream_t s) {
     const int dyn = 2 * (dec::kThreads / 32) * stage_bytes;
     cudaError_t e = cudaFuncSetAttribute(dec::value_qjl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return e;
-    dec::value_qjl_kernel<<<n_ctas, dec::kThreads, dyn, s>>>(dims, ws, n_items, stage_bytes);
+    dec::value_qjl_kernel<<<n_ctas, dec::kThreads, dyn, s>>>(dims, ws, stage_bytes);
     const int n_warps = dims.L * dims.B * dims.Hq;
     dec::value_qjl_apply_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
+cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_ctas,
                                   int stage_bytes, cudaStream_t s) {
     const int dyn = 2 * (dec::kThreads / 32) * stage_bytes;
     cudaError_t e =
         cudaFuncSetAttribute(dec::attention_mass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return e;
-    dec::attention_mass_kernel<<<n_ctas, dec::kThreads, dyn, s>>>(dims, ws, n_items, stage_bytes);
+    dec::attention_mass_kernel<<<n_ctas, dec::kThreads, dyn, s>>>(dims, ws, stage_bytes);
     return cudaGetLastError();
 }
 

@@ -22,14 +22,14 @@ constexpr int mass_stage_bytes(int max_kb, bool key_sketch, bool value_sketch) {
 struct DecodeDims;
 struct DecodeWorkspace;
 
-// Attention mass of every item with a mass pointer (items [0, n_items) of the
-// plan, n_ctas CTAs in all), after the decode kernels of the call; stage_bytes
-// from mass_stage_bytes for the launch's items.
-cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                                  int stage_bytes, cudaStream_t s);
+// Attention mass of every item with a mass pointer (n_ctas CTAs in all, each
+// finding its item in the workspace's per-CTA table), after the decode kernels
+// of the call; stage_bytes from mass_stage_bytes for the launch's items.
+cudaError_t launch_attention_mass(const DecodeDims &dims, const DecodeWorkspace &ws, int n_ctas, int stage_bytes,
+                                  cudaStream_t s);
 // QJL on values: z of every item with a value sketch (n_ctas CTAs), then
 // out += R (sqrt(pi/2)/jl S^T z) for the query heads of layers that have one.
-cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_items, int n_ctas,
-                             int stage_bytes, const float *S, cudaStream_t s);
+cudaError_t launch_value_qjl(const DecodeDims &dims, const DecodeWorkspace &ws, int n_ctas, int stage_bytes,
+                             const float *S, cudaStream_t s);
 
 }  // namespace tqk
