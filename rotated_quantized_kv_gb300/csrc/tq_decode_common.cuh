@@ -466,50 +466,52 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
         const LayerPlan &lp = ws.layer[layer];
         const int n_items = lp.n_items[h];
         const size_t rec_stride = kMaxGqa * kPartStride;
-        float M = kNegInf;
-        for (int ii = 0; ii < n_items; ii++) {
-            const size_t gr = static_cast<size_t>(lp.item[h][ii]) * dims.B + b;
-            const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
-            for (int c = lane; c < np; c += 32)
-                M = fmaxf(M, __ldcg(ws.part + (static_cast<size_t>(p0) + c) * rec_stride + warp * kPartStride));
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float L = 0.f;
+        // one pass over the records with an online max: eight records'
+        // loads in flight at a time (records of warps without tokens have
+        // m = -inf and contribute nothing)
+        float M = kNegInf, L = 0.f;
         float ar[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
-        if (M != kNegInf) {
-            // records four at a time: their loads are independent, so they are
-            // all in flight before the first is used (records of warps without
-            // tokens have m = -inf and contribute nothing)
-            for (int ii = 0; ii < n_items; ii++) {
-                const int item = lp.item[h][ii];
-                const size_t gr = static_cast<size_t>(item) * dims.B + b;
-                const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
-                float a[4] = {0.f, 0.f, 0.f, 0.f};
-                const float *base = ws.part + static_cast<size_t>(p0) * rec_stride + warp * kPartStride;
-                for (int c0 = 0; c0 < np; c0 += 4) {
-                    float m[4], l[4];
-                    float4 v[4];
+        for (int ii = 0; ii < n_items; ii++) {
+            const int item = lp.item[h][ii];
+            const size_t gr = static_cast<size_t>(item) * dims.B + b;
+            const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
+            const bool rot = ws.items[item].kind == TQ_SEG_PACKED;  // rotated-space sums
+            const float *base = ws.part + static_cast<size_t>(p0) * rec_stride + warp * kPartStride;
+            for (int c0 = 0; c0 < np; c0 += 8) {
+                float m[8], l[8];
+                float4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const int c = min(c0 + u, np - 1);
-                        const float *rec = base + static_cast<size_t>(c) * rec_stride;
-                        m[u] = c0 + u < np ? __ldcg(rec) : kNegInf;
-                        l[u] = __ldcg(rec + 1);
-                        v[u] = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        if (m[u] == kNegInf) continue;
-                        const float f = ex2(m[u] - M);
-                        L += f * l[u];
-                        a[0] += f * v[u].x;
-                        a[1] += f * v[u].y;
-                        a[2] += f * v[u].z;
-                        a[3] += f * v[u].w;
-                    }
+                for (int u = 0; u < 8; u++) {
+                    const int c = min(c0 + u, np - 1);
+                    const float *rec = base + static_cast<size_t>(c) * rec_stride;
+                    m[u] = c0 + u < np ? __ldcg(rec) : kNegInf;
+                    l[u] = __ldcg(rec + 1);
+                    v[u] = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
                 }
-                const bool rot = ws.items[item].kind == TQ_SEG_PACKED;  // rotated-space sums
+                float mc = m[0];
+#pragma unroll
+                for (int u = 1; u < 8; u++) mc = fmaxf(mc, m[u]);
+                if (mc > M) {  // a new running max: rescale what is summed so far
+                    const float sc = ex2(M - mc);
+                    L *= sc;
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        ar[e] *= sc;
+                        ao[e] *= sc;
+                    }
+                    M = mc;
+                }
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u = 0; u < 8; u++) {
+                    if (m[u] == kNegInf) continue;
+                    const float f = ex2(m[u] - M);
+                    L += f * l[u];
+                    a[0] += f * v[u].x;
+                    a[1] += f * v[u].y;
+                    a[2] += f * v[u].z;
+                    a[3] += f * v[u].w;
+                }
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     ar[e] += rot ? a[e] : 0.f;
