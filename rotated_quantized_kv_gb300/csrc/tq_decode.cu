@@ -235,8 +235,7 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         const PackedLauncher fn = dec::packed_launcher(c.kb, c.vb, c.qjl != 0);
         if (!fn) return cudaErrorInvalidValue;
         const cudaError_t e =
-            fn(dims, ws, c.item_lo, c.item_hi, ws.cta_item + c.cta_off, c.n_ctas, c.n_stages, value_half[i],
-               value_c1[i], s, !first);
+            fn(dims, ws, ws.cta_item + c.cta_off, c.n_ctas, c.n_stages, value_half[i], value_c1[i], s, !first);
         if (e != cudaSuccess) return e;
         first = false;
         ++*n_launched;

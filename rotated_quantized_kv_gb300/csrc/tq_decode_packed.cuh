@@ -754,9 +754,9 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
 }
 
 template <int KB, int VB, bool QJL>
-cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int item_lo, int item_hi,
-                          const int *cta_item, int n_ctas, long long n_stages, const unsigned short *value_half,
-                          float value_c1, cudaStream_t s, bool pdl) {
+cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, const int *cta_item, int n_ctas,
+                          long long n_stages, const unsigned short *value_half, float value_c1, cudaStream_t s,
+                          bool pdl) {
     using G = PackedGeom<KB, VB, QJL>;
     static bool configured = false;
     if (!configured) {
@@ -780,8 +780,6 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    (void)item_lo;
-    (void)item_hi;
     return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL>, dims, ws, cta_item, n_stages, vt);
 }
 

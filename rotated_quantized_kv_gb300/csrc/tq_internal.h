@@ -182,9 +182,8 @@ constexpr int kPackedCtasPerSm = 4;
 constexpr int kPackedCtasPerSmQjl = 3;
 __host__ __device__ constexpr int packed_ctas_per_sm(bool qjl) { return qjl ? kPackedCtasPerSmQjl : kPackedCtasPerSm; }
 
-typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, int item_lo, int item_hi,
-                                      const int *cta_item, int n_ctas, long long n_stages,
-                                      const unsigned short *value_half,
+typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, const int *cta_item,
+                                      int n_ctas, long long n_stages, const unsigned short *value_half,
                                       float value_c1,
                                       cudaStream_t s, bool pdl);
 PackedLauncher packed_launcher_kb1(int vb, bool qjl);

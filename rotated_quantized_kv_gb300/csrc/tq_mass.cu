@@ -15,8 +15,10 @@
 // the affine key levels and the QJL term applied to the raw products), so
 // only the key records, scales and sketches are read.  One CTA of 4 warps
 // takes kMassTokens tokens of one (item, batch element); a warp takes its
-// quarter in 16-token tiles, four per step; lane (g, c) scores tokens g and
-// g + 8 for query head c and the four heads are summed across the lane quad.
+// quarter in 64-token steps staged through two shared buffers by cp.async
+// (the next step in flight while one is scored), 16-token tiles within a
+// step; lane (g, c) scores tokens g and g + 8 for query head c and the four
+// heads are summed across the lane quad.
 // fp16 tokens (sinks, newest tier, chunk buffer) are scored one token per
 // thread on the CUDA cores against the unrotated query.
 #include "tq_decode_packed.cuh"
