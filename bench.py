@@ -1,30 +1,32 @@
 #!/usr/bin/env python
 """Benchmark: decode attention over the packed KV cache, and KV compression.
 
-Default workload (w2): Llama-3-8B-shaped KV cache, 32 layers x 8 KV heads x 128,
-32 query heads, batch 1, context 16384; keys 8-bit, values 3-bit; 128 fp16 sink
-tokens; new tokens buffered in fp16 and compressed 64 at a time.  One step is
-one decode step of the whole model: the query of every layer attends to its
-sinks, its packed tokens and its fp16 buffer (prep, split-K and combine kernels
-over all 32 layers), and every 64th step the 64 buffered tokens of each layer
-are compressed into the packed segment.  Inputs are synthetic (seeded N(0,1)
-with per-channel log-normal scales), resident in HBM before timing; each step
-reads ~0.8 GB, more than L2, so no flush is needed between steps.
+Default workload (w5 at batch 32 x context 65536, 2.1M cached tokens per layer):
+Mistral-Nemo-12B-shaped KV cache, 40 layers x 8 KV heads x 128, 32 query heads,
+keys 3-bit (symmetric grid) and values 3-bit (Gaussian Lloyd-Max), 128 fp16
+sink tokens per sequence.  One step is one decode step of the whole model: the
+query of every layer attends to its sinks and its packed tokens (prep, split-K
+and combine kernels over all 40 layers, 70.3 GB of cache read per step, far
+more than L2, so no flush is needed between steps).  Inputs are synthetic
+(seeded N(0,1) with 4 outlier channels per head x10), compressed once by the
+library and resident in HBM before timing.
 
 `value` is decode-attention throughput in algorithmic GB/s (cache bytes read
 plus q and output bytes, per step) over all ranks; `compress` reports KV
-compression in Mtok/s (one token = K and V of all 8 heads of one layer).
-
-Other workloads (`--workload w1|w3|w4|w5`, with `--batch`/`--context` for the
-w5 sweep) time decode steps over a prompt compressed once: w3 the age tiers
-(fp16 / K4V4 / K3V2 / K2V1) at 131072 positions, w4 per-head widths with QJL
-at batch 16, w5 uniform K3V3 behind 128 sinks.
+compression in Mtok/s (one token = K and V of all 8 heads of one layer);
+`roofline` is the packed split-K kernel alone.  `also` holds the decode figures
+of the other large workloads (unless --no-extra): w2 (Llama-3-8B shape, K8V3,
+sinks and 64-token chunks), w3 at batch 8 (age tiers fp16 / K4V4 / K3V2 / K2V1
+over 131072 positions, 1.05M tokens) and w4 at batch 32 (per-head widths 1-8
+with QJL sketches, 1.05M tokens).
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload wN]
 
-Under torchrun each rank runs an independent replica (weak scaling); the time
-is the max over ranks.  `--impl reference` times the CPU oracle instead on a
-bounded sample of the same workload (rank 0 only).
+Other workloads (`--workload w1|w2|w3|w4|w5`, with `--batch`/`--context` for the
+w5 sweep) make the main line instead.  Under torchrun each rank runs an
+independent replica (weak scaling); the time is the max over ranks.
+`--impl reference` times the CPU oracle instead on a bounded sample of the same
+workload (rank 0 only).
 """
 from __future__ import annotations
 
@@ -46,8 +48,7 @@ sys.path.insert(0, ROOT)
 
 from rotated_quantized_kv_gb300 import workloads as W  # noqa: E402
 
-METRIC = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"] if os.path.exists(
-    os.path.join(ROOT, "BASELINE.json")) else "decode-attn HBM GB/s over packed KV; KV compress Mtok/s"
+METRIC = "decode-attn HBM GB/s (% of ~8 TB/s) over packed KV; KV compress Mtok/s"
 NOMINAL_HBM_GBS = 8000.0
 DECODE_SRCS = ("tq_decode_packed.cuh", "tq_decode_common.cuh", "tq_decode.cu", "tq_internal.h")
 
@@ -170,7 +171,7 @@ def whole_job_gbs(world: int, bytes_per_rank: int, ms_max: float) -> float:
     return world * bytes_per_rank / (ms_max * 1e-3) / 1e9
 
 
-def timed_region(tq, step, nbytes, K, Wm, world, dev):
+def timed_region(tq, step, nbytes, K, Wm, world, dev, sample_clocks=True):
     """Warm-up, then K timed steps between a barrier and a synchronize on both
     sides (the whole-job value).  Then K more steps with the packed split-K
     launches of each step bracketed by their own CUDA events on the launching
@@ -210,7 +211,7 @@ def timed_region(tq, step, nbytes, K, Wm, world, dev):
         torch.cuda.synchronize()
         # a short timed region sees few 200 ms clock samples: keep the same
         # steps running for ~1.5 s so the samples see the GPU under this load
-        t_end = time.time() + 1.5
+        t_end = time.time() + (1.5 if sample_clocks else 0.0)
         s = Wm + 2 * K
         while time.time() < t_end:
             for _ in range(4):
@@ -285,24 +286,27 @@ def run_w2(args, rank, world, tq):
     torch.cuda.synchronize()
     t = timed_region(tq, m.step, lambda s: (lambda pb, ob: (pb, pb + ob))(*m.step_bytes(s)), K, Wm, world, dev)
 
-    # ---- e2e: q and the new token's K/V from pinned host memory, output back to host
-    qh = m.qpool.cpu().pin_memory()
+    # ---- e2e: each step's q and new-token K/V as one pinned host block (one
+    # host-to-device copy), the output back to host (one copy)
+    steps = m.steps_cap
+    qh = m.qpool.cpu().reshape(steps, -1)
     # the new token's K and V of every layer, [steps][L][B][H][d] on the host
-    newk = m.pool_k_all.permute(3, 0, 1, 2, 4).contiguous().cpu().pin_memory()
-    newv = m.pool_v_all.permute(3, 0, 1, 2, 4).contiguous().cpu().pin_memory()
-    kstage = torch.empty(newk.shape[1:], dtype=torch.float16, device="cuda")
-    vstage = torch.empty_like(kstage)
+    newk = m.pool_k_all.permute(3, 0, 1, 2, 4).contiguous().cpu().reshape(steps, -1)
+    newv = m.pool_v_all.permute(3, 0, 1, 2, 4).contiguous().cpu().reshape(steps, -1)
+    nq, nk = qh.shape[1], newk.shape[1]
+    blk_h = torch.cat([qh, newk, newv], dim=1).pin_memory()   # [steps][q | k | v] fp16
+    blk_d = torch.empty(blk_h.shape[1], dtype=torch.float16, device="cuda")
+    qdev = blk_d[:nq].view(m.q.shape)
+    kstage = blk_d[nq:nq + nk].view(m.pool_k_all[:, :, :, 0].shape)
+    vstage = blk_d[nq + nk:].view(m.pool_v_all[:, :, :, 0].shape)
     outh = torch.empty(m.out.shape, dtype=torch.float32).pin_memory()
-    qdev = torch.empty_like(m.q)
-    e2e = {"bi": m.q.numel() * 2 + kstage.numel() * 2 * 2, "bo": m.out.numel() * 4, "bytes": 0}
+    e2e = {"bi": blk_d.numel() * 2, "bo": m.out.numel() * 4, "bytes": 0}
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(K):
         s = (Wm + i) % m.steps_cap
-        qdev.copy_(qh[s], non_blocking=True)
-        kstage.copy_(newk[s], non_blocking=True)
-        vstage.copy_(newv[s], non_blocking=True)
+        blk_d.copy_(blk_h[s], non_blocking=True)
         m.pool_k_all[:, :, :, s].copy_(kstage)
         m.pool_v_all[:, :, :, s].copy_(vstage)
         m.step(s, q=qdev)
@@ -512,6 +516,48 @@ def run_static(args, rank, world, tq):
     return res
 
 
+EXTRA_POINTS = (("w2", None, None), ("w3", 8, None), ("w4", 32, None))
+
+
+def decode_point(tq, name, batch, context, K, Wm, world, dev):
+    """Decode figures of one more workload (compact): whole-step GB/s over K
+    steps and the packed split-K kernel alone (CUDA events on its stream)."""
+    from rotated_quantized_kv_gb300.model_cache import ChunkedDecodeCache, StaticCache
+    w = W.WORKLOADS[name]
+    if name == "w2":
+        m = ChunkedDecodeCache()
+        step = m.step
+        nbytes = lambda s: (lambda pb, ob: (pb, pb + ob))(*m.step_bytes(s))  # noqa: E731
+        B, T = m.B, m.T
+    else:
+        seed = 1000 + int(name[1:])
+        m = StaticCache(w, batch=batch, context=context, seed=seed)
+        qpool = W.query_pool(w, 4, m.B, seed, device="cuda")
+        pb, ob = m.step_bytes()
+
+        def step(s):
+            m.decode(qpool[s % 4])
+            return tq.tq_decode_last_launches()
+        nbytes = lambda s: (pb, pb + ob)  # noqa: E731
+        B, T = m.B, m.T
+    torch.cuda.synchronize()
+    t = timed_region(tq, step, nbytes, K, Wm, world, dev, sample_clocks=False)
+    peak, peak_kind = measured_peaks()
+    value = whole_job_gbs(world, t["total_bytes"], t["ms"])
+    kern_ms = float(np.mean(t["kern_ms"]))
+    achieved = float(np.mean(t["packed_bytes"])) / (kern_ms * 1e-3) / 1e9
+    res = {"workload": w.name, "batch": B, "context": T, "tokens": B * T, "layers": w.layers,
+           "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(t["ms"] / K, 5),
+           "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+           "kernel_gbs": round(achieved, 1), "kernel_frac": round(achieved / peak, 4), "peak": peak,
+           "peak_kind": peak_kind, "kernel_ms": round(kern_ms, 5),
+           "bytes_per_step": int(t["total_bytes"] / K), "gpu_launches": t["launches"]}
+    del m
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world):
     from rotated_quantized_kv_gb300 import build
     build.build()
@@ -524,6 +570,12 @@ def run_ours(args, rank, world):
     else:
         res = run_static(args, rank, world, tq)
         wl = W.WORKLOADS[args.workload]
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if not args.no_extra and args.workload == "w5" and args.batch is None and args.context is None:
+        dev = torch.cuda.current_device()
+        res["also"] = [decode_point(tq, n, b, c, args.steps, args.warmup, world, dev)
+                       for n, b, c in EXTRA_POINTS]
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
     return res
@@ -545,11 +597,11 @@ def oracle_plan(w, context):
     return out + [(w.sinks, context - w.sinks, [w.kbits] * H, [w.vbits] * H, [0] * H)]
 
 
-def oracle_sample(w, budget_tokens=4096, seed=1002):
-    """A bounded sample of a workload for the CPU oracle: layer 0, batch element
-    0, each segment of the layer's plan cut to its share of `budget_tokens`
-    positions (fp16 segments of <= 128 positions kept whole).  Returns
-    (segments, sign, q, S, algorithmic bytes, description)."""
+def oracle_sample(w, budget_tokens=4096, seed=1002, layer=0):
+    """A bounded sample of a workload for the CPU oracle: one layer (default 0),
+    batch element 0, each segment of the layer's plan cut to its share of
+    `budget_tokens` positions (fp16 segments of <= 128 positions kept whole).
+    Returns (segments, sign, q, S, algorithmic bytes, description)."""
     from oracle import oracle as O
     H, d = w.kv_heads, w.head_dim
     plan = oracle_plan(w, w.context)
@@ -559,8 +611,8 @@ def oracle_sample(w, budget_tokens=4096, seed=1002):
         m = n if (kb[0] == 16 and n <= 128) else max(16, min(n, round(n * budget_tokens / total)))
         cut.append((pos0, m, kb, vb, qj))
     span = max(p + m for p, m, *_ in cut)
-    K, V = W.kv_block(w, 0, 1, span, seed)
-    sign = O.signs(d, W.ROTATION_SEED)
+    K, V = W.kv_block(w, layer, 1, span, seed)
+    sign = O.signs(d, W.ROTATION_SEED + layer)
     S = O.qjl_matrix(128, d, W.QJL_SEED) if w.qjl_max_bits else None
     segs, nbytes = [], w.q_heads * d * 6
     for pos0, m, kb, vb, qj in cut:
@@ -576,40 +628,82 @@ def oracle_sample(w, budget_tokens=4096, seed=1002):
             sg.n_tokens = m
             nbytes += m * sum(d // 8 * (a + b) + 8 + (20 if q else 0) for a, b, q in zip(kb, vb, qj))
         segs.append(sg)
-    q = W.queries(w, 0, 1, seed).numpy()
-    desc = (f"{w.name} layer 0, batch element 0: " +
+    q = W.queries(w, layer, 1, seed).numpy()
+    desc = (f"{w.name} layer {layer}, batch element 0: " +
             " + ".join(f"{m} {'fp16' if kb[0] == 16 else 'packed'}" for _, m, kb, _, _ in cut) +
             f" tokens, {w.q_heads} query heads")
     return segs, sign, q, S, nbytes, desc
 
 
 def cpu_baseline(w, seconds=10.0):
+    """The oracle as it stands, timed on the host cores: one thread on one
+    layer's sample, then one thread per allowed core, each on its own layer's
+    sample (the oracle's C call releases the GIL, so the threads run in
+    parallel over independent (layer) units).  The all-core figure is the
+    line's value; the single-thread one is kept beside it."""
+    import concurrent.futures as cf
     from oracle import oracle as O
     segs, sign, q, S, nbytes, desc = oracle_sample(w)
     reps, t = 0, 0.0
-    while t < seconds or reps == 0:
+    while t < seconds / 2 or reps == 0:
         t0 = time.perf_counter()
         O.decode_attention(segs, q, sign, w.kv_heads, S=S)
         t += time.perf_counter() - t0
         reps += 1
-    return {"value": round(reps * nbytes / t / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{desc}; {reps} repetitions, {t:.1f} s of single-threaded C"}
+    single = reps * nbytes / t / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    samples = [(segs, sign, q, S, nbytes)] + [oracle_sample(w, layer=l % w.layers)[:5] for l in range(1, cores)]
+    done = [0] * cores
+    t_stop = [0.0]
+
+    def worker(i):
+        sg, sn, qq, SS, _ = samples[i]
+        while True:
+            O.decode_attention(sg, qq, sn, w.kv_heads, S=SS)
+            done[i] += 1
+            if time.perf_counter() >= t_stop[0]:
+                return
+
+    t0 = time.perf_counter()
+    t_stop[0] = t0 + seconds / 2
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(worker, range(cores)))
+    dt = time.perf_counter() - t0
+    allb = sum(done[i] * samples[i][4] for i in range(cores))
+    return {"value": round(allb / dt / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_thread": {"value": round(single, 6), "unit": "GB/s", "cores": 1, "repetitions": reps,
+                              "seconds": round(t, 2)},
+            "sample": f"{desc}; all-core run: {cores} threads, thread i on layer i's sample of the same "
+                      f"shape, {sum(done)} calls in {dt:.1f} s; single thread: {reps} calls in {t:.1f} s "
+                      f"(plain scalar C)"}
 
 
 def run_reference(args, rank, world):
+    """The oracle as it stands on the host cores: one thread per allowed core,
+    thread i on layer i's bounded sample; a step is one call on every thread."""
     if rank != 0:
         return None
+    import concurrent.futures as cf
     from oracle import oracle as O
     w = W.WORKLOADS[args.workload]
-    segs, sign, q, S, nbytes, desc = oracle_sample(w, budget_tokens=1024)
-    for _ in range(args.warmup):
-        O.decode_attention(segs, q, sign, w.kv_heads, S=S)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        O.decode_attention(segs, q, sign, w.kv_heads, S=S)
-    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    samples = [oracle_sample(w, budget_tokens=1024, layer=l % w.layers) for l in range(cores)]
+    desc = samples[0][5]
+    nbytes = sum(smp[4] for smp in samples)
+
+    def one(i):
+        sg, sn, qq, SS = samples[i][:4]
+        O.decode_attention(sg, qq, sn, w.kv_heads, S=SS)
+
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        for _ in range(args.warmup):
+            list(ex.map(one, range(cores)))
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            list(ex.map(one, range(cores)))
+        dt = time.perf_counter() - t0
     v = args.steps * nbytes / dt / 1e9
-    desc += " (CPU oracle, 1 thread)"
+    desc += f" (CPU oracle, {cores} threads, thread i on layer i's sample of the same shape)"
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -617,7 +711,8 @@ def run_reference(args, rank, world):
             "config": {"workload": w.name, "layers": w.layers, "batch": w.batch, "context": w.context,
                        "kv_heads": w.kv_heads, "q_heads": w.q_heads, "head_dim": w.head_dim, "kbits": w.kbits,
                        "vbits": w.vbits, "sinks": w.sinks, "chunk": w.chunk, "sample": desc},
-            "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
             "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -629,9 +724,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="w2", choices=sorted(W.WORKLOADS),
-                    help="w2 (default): the chunked decode workload the metric is quoted on; "
-                         "w1, w3, w4, w5: decode steps over a prompt compressed once")
+    ap.add_argument("--workload", default="w5", choices=sorted(W.WORKLOADS),
+                    help="w5 (default, batch 32 x 65536): the largest single-GPU workload; "
+                         "w2: chunked decode with sinks; w1, w3, w4: decode steps over a prompt "
+                         "compressed once")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decode figures of w2, w3 (batch 8) and w4 (batch 32)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (w1, w3-w5)")
     ap.add_argument("--rotation", default="srht", choices=["srht", "haar"],
                     help="haar: a dense Haar rotation per layer (tensor-core compressor; w1, w3, w5)")

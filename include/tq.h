@@ -53,6 +53,9 @@ typedef int tq_status;
 #define TQ_ERR_ALIGN (-3)       /* a device pointer or stride is not 16-byte aligned */
 #define TQ_ERR_SIZE (-4)        /* a buffer is too small (workspace, capacity) */
 #define TQ_ERR_CUDA (-5)        /* a CUDA runtime call failed; see tq_last_cuda_error */
+#define TQ_ERR_TIMEOUT (-6)     /* a kernel gave up a bounded wait for its own copies
+                                   (tq_decode_error_flag, tq_compress_error_flag):
+                                   the output of that call is incomplete */
 
 /* Human-readable name of a status.  Never NULL. */
 const char *tq_status_string(tq_status s);
@@ -214,7 +217,8 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot,
 
 /* The dense-rotation compress kernel bounds every wait for its own copies and
  * tensor-core work; one that gave up sets a flag (process-wide, per device).
- * *flag = that flag (waits for the device); reset != 0 clears it. */
+ * *flag = that flag (waits for the device); reset != 0 clears it.  Returns
+ * TQ_ERR_TIMEOUT when the flag was set (before any reset), TQ_OK when not. */
 tq_status tq_compress_error_flag(int *flag, int reset);
 
 /* Dequantize token positions [t_begin, t_begin + n_tokens) of a packed segment.
@@ -322,11 +326,23 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
                               size_t ws_bytes, void *stream);
 
 /* The kernels never spin without bound: a split-K CTA that waits too long for
- * its own shared-memory copies (never expected) stops, leaves its part of the
- * output unwritten and sets a flag at the start of the workspace.  This call
- * synchronises `stream` and stores that flag (0 = no such event) in *flag.  The
- * next tq_decode_attention call on the workspace clears it. */
+ * its own shared-memory copies (never expected) stops, lets the copies it
+ * issued land, leaves its part of the output unwritten (no merge completes for
+ * the (layer, batch, KV head) groups it touched) and sets a flag at the start
+ * of the workspace.  This call synchronises `stream` and stores that flag
+ * (0 = no such event) in *flag; it returns TQ_ERR_TIMEOUT when the flag is set
+ * and TQ_OK when not.  workspace = NULL reads the flag of this device's static
+ * scratch array (the one tq_decode_attention_static uses).  The next decode
+ * call on the same workspace clears it. */
 tq_status tq_decode_error_flag(const void *workspace, int *flag, void *stream);
+
+/* Failure-path hook, for tests of the timeout handling: the number of polls a
+ * split-K CTA makes while waiting for a stage of its own copies before it gives
+ * up (default and maximum 2^20; 0 makes every such wait give up at once, while
+ * the drain of the copies already issued keeps the full bound, so that no copy
+ * outlives its CTA).  Applies to later tq_decode_attention calls of the
+ * process.  TQ_ERR_ARG outside [0, 2^20]. */
+tq_status tq_set_decode_wait_polls(int polls);
 
 /* Measurement hook: when both events are non-NULL, every later
  * tq_decode_attention call on this host thread records `start` on its stream
@@ -344,8 +360,10 @@ int tq_decode_last_launches(void);
 /* Decode attention without a caller-supplied workspace.  (No counterpart on   */
 /* the pages: this entry point exists for callers, not for the method.)        */
 /* ------------------------------------------------------------------------ */
-/* Bytes of the library's own scratch array, held on every GPU that loads the
- * library until the process exits. */
+/* Bytes of the library's own scratch array.  A device commits it when the
+ * array's module is loaded there -- with the CUDA runtime's default lazy
+ * loading, at the first tq_decode_attention_static call (or static flag read)
+ * on that device -- and holds it until the process exits. */
 #define TQ_STATIC_WORKSPACE_BYTES (16u << 20)
 
 /* Same result and same kernels as tq_decode_attention, for callers that may not
@@ -357,12 +375,16 @@ int tq_decode_last_launches(void);
  * library instead of a caller buffer; the caller still passes q and out.  The
  * call allocates no device memory (its plan upload uses the library's pinned
  * host staging buffers, allocated by the first decode calls of the process).
- *   - Set-up: the first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.
+ *   - Set-up: the first call on a device, with that device current, loads the
+ *     array (committing its TQ_STATIC_WORKSPACE_BYTES of device memory), looks up
+ *     its device address (cudaGetSymbolAddress) and caches it.  Make that first
+ *     call (a warm-up on a small cache) during start-up, before reserving the
+ *     rest of the device memory for a pool and before any stream capture.
  *   - Limit: returns TQ_ERR_SIZE, before launching anything, when the call needs
  *     more scratch than TQ_STATIC_WORKSPACE_BYTES (tq_decode_workspace_size tells
  *     how much); split the layers over several calls or use tq_decode_attention.
+ *     Argument and alignment errors come first, as for tq_decode_attention.
+ *   - Timeouts: tq_decode_error_flag(NULL, ...) reads the array's flag.
  *   - Sharing: every call uses the same array, which keeps the previous call's
  *     contents; nothing in it needs to start at zero (each call writes all it
  *     reads).  Calls that overlap on the GPU -- on different streams or from

@@ -20,7 +20,7 @@
  *   [SKL]  "turboquant-mlx" skill note: "Standalone Benchmark" (per-layer seed 42 + i),
  *          "Optimisations Metal" (inverse transform pulled out of V-attention).
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - PRNG: SplitMix64 (Steele, Lea, Flood 2014).
  *   - D @ H @ D uses ONE sign diagonal on both sides, so R = D H D / sqrt(d) is
  *     symmetric and R R = I; its inverse is R itself.

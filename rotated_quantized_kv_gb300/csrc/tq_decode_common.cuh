@@ -66,11 +66,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for a barrier phase: gives up after 2^20 polls (each poll
-// may suspend in hardware for a while), so a copy that never completes cannot
-// hang the GPU.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
-    for (int i = 0; i < (1 << 20); i++)
+// Bounded wait for a barrier phase: gives up after `polls` polls (default
+// 2^20; each poll may suspend in hardware for a while), so a copy that never
+// completes cannot hang the GPU.  Returns false on timeout.
+constexpr int kWaitPolls = 1 << 20;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, int polls = kWaitPolls) {
+    for (int i = 0; i < polls; i++)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }

@@ -723,12 +723,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
     bool new_group = false;
 
     for (int k = 0; k < n_st; k++) {
-        const bool arrived = mbar_wait(&full[k % NS], (k / NS) & 1);
+        const bool arrived = mbar_wait(&full[k % NS], (k / NS) & 1, dims.wait_polls);
         // all warps are past stage k-1 (its buffer is free) and agree on errors
         if (__syncthreads_or(!arrived)) {
             if (threadIdx.x == 0) {
                 atomicExch(ws.error, 1);
-                // let the copies still in flight land before the CTA's shared memory goes away
+                // let the copies still in flight land before the CTA's shared
+                // memory goes away (always with the full bound)
                 for (int j = k; j < n_st && j < k + NS - 1; j++) mbar_wait(&full[j % NS], (j / NS) & 1);
             }
             __syncthreads();

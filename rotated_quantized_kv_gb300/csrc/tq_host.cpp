@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -20,6 +21,8 @@ namespace {
 thread_local int g_last_cuda = 0;
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 thread_local int g_last_launches_v = 0;
+// polls of a split-K CTA's wait for its own copies (tq_set_decode_wait_polls)
+std::atomic<int> g_wait_polls{1 << 20};
 struct LaunchCounter {
     void store(int v) { g_last_launches_v = v; }
 } g_last_launches;
@@ -631,6 +634,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.any_prep = any_packed || P.any_qjl || any_dense ? 1 : 0;
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    D.wait_polls = g_wait_polls.load();
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
     // offset 0: the error flag (kept in its own 256 bytes so that it has a
     // fixed place), then the work items
@@ -683,6 +687,7 @@ const char *tq_status_string(tq_status s) {
         case TQ_ERR_ALIGN: return "TQ_ERR_ALIGN: pointer, stride or capacity not 16-byte aligned";
         case TQ_ERR_SIZE: return "TQ_ERR_SIZE: buffer or capacity too small";
         case TQ_ERR_CUDA: return "TQ_ERR_CUDA: CUDA runtime error (see tq_last_cuda_error)";
+        case TQ_ERR_TIMEOUT: return "TQ_ERR_TIMEOUT: a kernel gave up waiting for its own copies; its output is incomplete";
         default: return "unknown tq_status";
     }
 }
@@ -774,7 +779,8 @@ tq_status tq_compress_error_flag(int *flag, int reset) {
     if (!flag) return TQ_ERR_ARG;
     cudaError_t e = read_compress_dense_error(flag);
     if (e == cudaSuccess && reset) e = clear_compress_dense_error();
-    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return *flag ? TQ_ERR_TIMEOUT : TQ_OK;
 }
 
 tq_status tq_make_qjl(int head_dim, int jl_dim, uint64_t seed, float *S) {
@@ -1174,11 +1180,24 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
 }
 
 tq_status tq_decode_error_flag(const void *workspace, int *flag, void *stream) {
-    if (!workspace || !flag) return TQ_ERR_ARG;
+    if (!flag) return TQ_ERR_ARG;
+    if (!workspace) {  // the static scratch array of this device (tq_decode_attention_static)
+        void *ws = nullptr;
+        const tq_status st = static_workspace(&ws);
+        if (st != TQ_OK) return st;
+        workspace = ws;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(flag, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return *flag ? TQ_ERR_TIMEOUT : TQ_OK;
+}
+
+tq_status tq_set_decode_wait_polls(int polls) {
+    if (polls < 0 || polls > (1 << 20)) return TQ_ERR_ARG;
+    g_wait_polls.store(polls);
+    return TQ_OK;
 }
 
 int tq_decode_last_launches(void) { return g_last_launches_v; }

@@ -127,6 +127,7 @@ struct DecodeDims {
     int any_prep;        // the prep kernel ran (QJL or dense-rotation layers read R q from it)
     float qk_scale;      // log2(e) / sqrt(d)
     float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
+    int wait_polls;      // polls of a split-K CTA's wait for its own copies before it gives up
 };
 
 // Workspace: [WorkItem x n][LayerPlan x L][group tables][counters][q prep]
@@ -197,6 +198,10 @@ PackedLauncher packed_launcher_kb8(int vb, bool qjl);
 
 // Records a CUDA error for tq_last_cuda_error() and returns TQ_ERR_CUDA.
 tq_status record_cuda_error(cudaError_t e);
+
+// Device address of the static decode scratch array on the current device
+// (tq_static.cu); looked up on the first use per device.
+tq_status static_workspace(void **out);
 
 // Launchers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s);

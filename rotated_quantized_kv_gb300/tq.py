@@ -38,15 +38,18 @@ TQ_VALUE_LAW_GAUSS = 0
 TQ_VALUE_LAW_SPHERE = 1
 TQ_QJL_UNBIASED = 0
 TQ_QJL_SIGN_PAIR = 1
+TQ_ERR_TIMEOUT = -6
+TQ_WAIT_POLLS_DEFAULT = 1 << 20
 
 STATUS = {0: "TQ_OK", -1: "TQ_ERR_ARG", -2: "TQ_ERR_UNSUPPORTED", -3: "TQ_ERR_ALIGN",
-          -4: "TQ_ERR_SIZE", -5: "TQ_ERR_CUDA"}
+          -4: "TQ_ERR_SIZE", -5: "TQ_ERR_CUDA", -6: "TQ_ERR_TIMEOUT"}
 
 EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rotation",
             "tq_fit_codebook", "tq_make_qjl", "tq_packed_size", "tq_compress", "tq_dequantize",
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
             "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag",
-            "tq_requantize", "tq_fit_codebook_sphere", "tq_make_haar_rotation", "tq_compress_error_flag", "tq_decode_last_launches"]
+            "tq_requantize", "tq_fit_codebook_sphere", "tq_make_haar_rotation", "tq_compress_error_flag", "tq_decode_last_launches",
+            "tq_set_decode_wait_polls"]
 
 
 class TQError(RuntimeError):
@@ -122,6 +125,7 @@ _lib.tq_decode_attention.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, 
                                      _P, ctypes.c_size_t, _P]
 _lib.tq_set_decode_kernel_events.argtypes = [_P, _P]
 _lib.tq_decode_error_flag.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
+_lib.tq_set_decode_wait_polls.argtypes = [_I]
 _lib.tq_decode_attention_static.argtypes = [ctypes.POINTER(tq_layer_view), _I, _I, _I, _I, _I, _P, _I, _P,
                                             _P, _P]
 TQ_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -194,8 +198,12 @@ def dense_rotation(rot: tq_rotation, Q: torch.Tensor) -> tq_rotation:
 
 
 def tq_compress_error_flag(reset: bool = False) -> int:
+    """The dense compressor's timeout flag (0: none); the call's TQ_ERR_TIMEOUT
+    status is returned as the flag, not raised."""
     f = ctypes.c_int(0)
-    _check(_lib.tq_compress_error_flag(ctypes.byref(f), int(reset)), "tq_compress_error_flag")
+    st = _lib.tq_compress_error_flag(ctypes.byref(f), int(reset))
+    if st != TQ_ERR_TIMEOUT:
+        _check(st, "tq_compress_error_flag")
     return f.value
 
 
@@ -402,12 +410,22 @@ def tq_decode_attention_static(layers, q: torch.Tensor, out: torch.Tensor, n_hea
     return out
 
 
-def tq_decode_error_flag(workspace: torch.Tensor, stream=None) -> int:
+def tq_decode_error_flag(workspace: torch.Tensor | None, stream=None) -> int:
     """Non-zero if a decode call on this workspace stopped a CTA after a bounded
-    wait for its own copies (never expected); synchronises the stream."""
+    wait for its own copies (never expected); synchronises the stream.  None:
+    the static scratch array of tq_decode_attention_static.  The call's
+    TQ_ERR_TIMEOUT status is returned as the flag, not raised."""
     f = ctypes.c_int()
-    _check(_lib.tq_decode_error_flag(_ptr(workspace), ctypes.byref(f), _stream(stream)), "tq_decode_error_flag")
+    st = _lib.tq_decode_error_flag(_ptr(workspace), ctypes.byref(f), _stream(stream))
+    if st != TQ_ERR_TIMEOUT:
+        _check(st, "tq_decode_error_flag")
     return f.value
+
+
+def tq_set_decode_wait_polls(polls: int):
+    """Failure-path hook for tests: polls of a split-K CTA's wait for its own
+    copies before it gives up (default 2^20; 0 = give up at once)."""
+    _check(_lib.tq_set_decode_wait_polls(polls), "tq_set_decode_wait_polls")
 
 
 def views_array(layers):
