@@ -29,8 +29,14 @@
  *     whose cudaError_t value tq_last_cuda_error() returns.
  *   - fp16 data are IEEE binary16 bit patterns (uint16_t / __half).
  *   - Device buffers must be 16-byte aligned (TQ_ERR_ALIGN otherwise).
- *   - Kernels support head_dim = 128 and GQA group sizes 1, 2 and 4 (query
- *     heads per KV head); other shapes return TQ_ERR_UNSUPPORTED.
+ *   - head_dim is any power of two from 16 to 1024 ("turboquant-mlx",
+ *     "Walsh-Hadamard Rotation": WalshHadamardRotation(head_dim, seed)).  At
+ *     head_dim = 128 every call and option below is available (decode with GQA
+ *     group sizes 1, 2 and 4, query heads per KV head).  Other head dims take
+ *     tq_compress, tq_dequantize and tq_decode_attention (GQA 1 to 4) with the
+ *     SRHT rotation and the Gaussian value codebook; QJL sketches (keys or
+ *     values), dense rotations, the sphere codebook, attention-mass outputs
+ *     and tq_requantize return TQ_ERR_UNSUPPORTED there.
  */
 #ifndef TQ_H
 #define TQ_H

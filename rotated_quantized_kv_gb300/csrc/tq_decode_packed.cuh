@@ -424,18 +424,18 @@ struct ValueTable {
     float c1;                  // binary32 centroid 1 of a 1-bit codebook (= -centroid 0)
 };
 
-constexpr int kPT = kPackedStageTokens;  // 32 tokens per warp: two 16-token tiles
-
 template <int KB, int VB, bool QJL>
 struct PackedGeom {
+    static constexpr int PT = packed_stage_tokens(KB, VB, QJL);  // tokens per stage, a multiple of 128
+    static constexpr int CTAS = packed_ctas_per_sm(KB, VB, QJL);
     static constexpr int RK = 16 * KB, RV = 16 * VB;
-    static constexpr int offV = kPT * RK;
-    static constexpr int offKS = offV + kPT * RV;
-    static constexpr int offVS = offKS + kPT * 4;
-    static constexpr int offQS = offVS + kPT * 4;
-    static constexpr int offQN = offQS + kPT * 16;
-    static constexpr int stage = QJL ? offQN + kPT * 4 : offQS;
-    static constexpr int budget = 227 * 1024 / packed_ctas_per_sm(QJL) - 1024;
+    static constexpr int offV = PT * RK;
+    static constexpr int offKS = offV + PT * RV;
+    static constexpr int offVS = offKS + PT * 4;
+    static constexpr int offQS = offVS + PT * 4;
+    static constexpr int offQN = offQS + PT * 16;
+    static constexpr int stage = QJL ? offQN + PT * 4 : offQS;
+    static constexpr int budget = 227 * 1024 / CTAS - 1024;
     static constexpr int qbytes = 16 + 64;  // flag, barriers (the rotated queries come from the prep kernel)
     static constexpr int pair_entries = (VB == 2 || VB == 3) ? (1 << (2 * VB)) : 0;
     // pair table: one column per lane (32 copies) if that still leaves 3
@@ -507,13 +507,14 @@ struct StageCursor {
 // partial per (item, batch) group its CTA touches; the CTA completing a
 // (layer, batch, KV head) merges the partials (finish_and_combine).
 template <int KB, int VB, bool QJL>
-__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
+__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
     decode_packed_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item,
                          const long long S, const __grid_constant__ ValueTable vt) {
     using G = PackedGeom<KB, VB, QJL>;
     using KU = KUnpack<KB>;
     using VD = VDec<VB, G::TS>;
     constexpr int NS = G::stages;
+    constexpr int kPT = G::PT;
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int gqa = dims.gqa, B = dims.B;
@@ -743,10 +744,11 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(QJL))
         const uint8_t *buf = smem + (k % NS) * G::stage;
         const int n = min(kPT, cc.n_tokens - cc.st * kPT);
         new_group = cc.advance(ws.items, B, k + 1 < n_st);
-        const int tA = warp * 32;
-        if (tA >= n) continue;
-        if (tA + 32 <= n) tiles(buf, tA, n, std::true_type{});
-        else tiles(buf, tA, n, std::false_type{});
+        // warp w takes tokens [32 w, 32 w + 32) of every 128 of the stage
+        for (int tA = warp * 32; tA < n; tA += 32 * kDecodeWarps) {
+            if (tA + 32 <= n) tiles(buf, tA, n, std::true_type{});
+            else tiles(buf, tA, n, std::false_type{});
+        }
     }
     // every thread waits for the previous grid of the call before its last
     // merge, so that this grid's completion implies that of all earlier ones

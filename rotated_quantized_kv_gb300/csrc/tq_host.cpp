@@ -315,6 +315,129 @@ int sm_count() {
 
 float inv_sqrt_f32(int d) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))); }
 
+// Launches of the one-thread-per-vector kernels for a compression without
+// sketches: the keys of each distinct key width, then the values of each
+// distinct value width (one launch each; uniform layouts take two).
+cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout, cudaStream_t s) {
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.sb = c.sb;
+    p.sh = c.sh;
+    p.st = c.st;
+    p.B = c.B;
+    p.H = c.H;
+    p.T = c.T;
+    p.t_begin = c.t_begin;
+    p.capacity = c.capacity;
+    for (int i = 0; i < kD / 2; ++i) {
+        const uint32_t s0 = (c.sign_bits[(2 * i) >> 5] >> ((2 * i) & 31)) & 1u;
+        const uint32_t s1 = (c.sign_bits[(2 * i + 1) >> 5] >> ((2 * i + 1) & 31)) & 1u;
+        p.in_mask[i] = (s0 << 15) | (s1 << 31);
+    }
+    for (int i = 0; i < kD; ++i)
+        p.out_scale[i] = ((c.sign_bits[i >> 5] >> (i & 31)) & 1u) ? -c.inv_sqrt_d : c.inv_sqrt_d;
+    for (int values = 0; values < 2; ++values) {
+        p.X = values ? c.V : c.K;
+        p.codes = values ? c.vcodes : c.kcodes;
+        p.scale = values ? c.vscale : c.kscale;
+        p.block = values ? c.vblock : c.kblock;
+        for (int h = 0; h < c.H; ++h) p.off[h] = values ? c.voff[h] : c.koff[h];
+        for (int bits = 1; bits <= 8; ++bits) {
+            p.n_heads = 0;
+            for (int h = 0; h < c.H; ++h)
+                if ((values ? c.vbits[h] : c.kbits[h]) == bits) p.head[p.n_heads++] = static_cast<uint8_t>(h);
+            if (p.n_heads == 0) continue;
+            if (values) {
+                const FittedCodebook &cb = fit(bits, layout->value_law);
+                for (int k = 0; k + 1 < (1 << bits); ++k) p.thr[k] = static_cast<float>(cb.bound[k]);
+            }
+            const cudaError_t e = launch_compress_rows(p, bits, values != 0, s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- other head dims
+// Compression for head dimensions other than kD (tq_generic.cu): SRHT only,
+// no QJL sketches, Gaussian value codebook.
+tq_status compress_other_dims(const tq_segment_layout *layout, const tq_rotation *rot, const Offsets &o,
+                              const void *K, const void *V, int n_tokens, int64_t stride_b, int64_t stride_h,
+                              int64_t stride_t, int t_begin, const tq_packed_bufs *out, cudaStream_t s) {
+    const int d = layout->head_dim;
+    if (o.nq || o.nv || rot->dense || layout->value_law != TQ_VALUE_LAW_GAUSS) return TQ_ERR_UNSUPPORTED;
+    if (!aligned16(K) || !aligned16(V) || !aligned16(out->kcodes) || !aligned16(out->vcodes) ||
+        !aligned16(out->kscale) || !aligned16(out->vscale))
+        return TQ_ERR_ALIGN;
+    if (stride_t < d || stride_h < 0 || stride_b < 0 || (stride_t % 8) || (stride_h % 8) || (stride_b % 8))
+        return TQ_ERR_ALIGN;
+    if (n_tokens == 0) return TQ_OK;
+    GenCompressParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.K = static_cast<const uint16_t *>(K);
+    p.V = static_cast<const uint16_t *>(V);
+    p.sb = stride_b;
+    p.sh = stride_h;
+    p.st = stride_t;
+    p.B = layout->batch;
+    p.H = layout->n_heads;
+    p.T = n_tokens;
+    p.t_begin = t_begin;
+    p.capacity = layout->capacity;
+    p.kcodes = static_cast<uint8_t *>(out->kcodes);
+    p.vcodes = static_cast<uint8_t *>(out->vcodes);
+    p.kscale = out->kscale;
+    p.vscale = out->vscale;
+    p.kblock = o.kblock;
+    p.vblock = o.vblock;
+    for (int h = 0; h < p.H; ++h) {
+        p.koff[h] = o.koff[h];
+        p.voff[h] = o.voff[h];
+        p.kbits[h] = layout->kbits[h];
+        p.vbits[h] = layout->vbits[h];
+    }
+    std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
+    p.inv_sqrt_d = inv_sqrt_f32(d);
+    fill_thresholds(p.thr, layout->vbits, p.H, layout->value_law);
+    const cudaError_t e = launch_gen_compress(p, d, s);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status dequantize_other_dims(const tq_segment_layout *layout, const tq_packed_bufs *bufs, const tq_rotation *rot,
+                                const Offsets &o, int t_begin, int n_tokens, float *k_rot, float *v_rot,
+                                float *k_orig, float *v_orig, cudaStream_t s) {
+    if (rot && rot->dense) return TQ_ERR_UNSUPPORTED;
+    if (layout->value_law != TQ_VALUE_LAW_GAUSS) return TQ_ERR_UNSUPPORTED;
+    GenDequantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = layout->batch;
+    p.H = layout->n_heads;
+    p.t_begin = t_begin;
+    p.n = n_tokens;
+    p.capacity = layout->capacity;
+    p.kcodes = static_cast<const uint8_t *>(bufs->kcodes);
+    p.vcodes = static_cast<const uint8_t *>(bufs->vcodes);
+    p.kscale = bufs->kscale;
+    p.vscale = bufs->vscale;
+    p.kblock = o.kblock;
+    p.vblock = o.vblock;
+    for (int h = 0; h < p.H; ++h) {
+        p.koff[h] = o.koff[h];
+        p.voff[h] = o.voff[h];
+        p.kbits[h] = layout->kbits[h];
+        p.vbits[h] = layout->vbits[h];
+    }
+    if (rot) std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
+    p.inv_sqrt_d = inv_sqrt_f32(layout->head_dim);
+    p.k_rot = k_rot;
+    p.v_rot = v_rot;
+    p.k_orig = k_orig;
+    p.v_orig = v_orig;
+    fill_centroids(p.centroid, layout->vbits, p.H, layout->value_law);
+    const cudaError_t e = launch_gen_dequant(p, layout->head_dim, s);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
 // ---------------------------------------------------------------- decode plan
 struct Plan {
     std::vector<WorkItem> items;      // sorted by class; fp16 items last
@@ -334,6 +457,11 @@ struct Plan {
     size_t off_items = 0, off_layer = 0, off_grp_part = 0, off_grp_nparts = 0, off_lbh_total = 0, off_counter = 0;
     size_t off_cta_item = 0;
     size_t off_qrot = 0, off_qjlt = 0, off_qsum = 0, off_part = 0, off_ml = 0, off_z = 0, total = 0;
+    // head dimensions other than kD: one CTA per (layer, batch, KV head) over
+    // the layer's items, the rotations' sign bits per layer
+    bool generic = false;
+    std::vector<uint32_t> signs;
+    size_t off_signs = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -360,12 +488,15 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     if (!layers || n_layers < 1 || B < 1 || H < 1 || H > TQ_MAX_HEADS || Hq < H || Hq % H) return TQ_ERR_ARG;
     if (!pow2(d) || d < 16 || d > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     const int gqa = Hq / H;
-    if (d != kD || (gqa != 1 && gqa != 2 && gqa != 4)) return TQ_ERR_UNSUPPORTED;
+    const bool generic = d != kD;  // other head dims: the generic kernel (GQA up to 4, no QJL, SRHT)
+    if (!generic && gqa != 1 && gqa != 2 && gqa != 4) return TQ_ERR_UNSUPPORTED;
+    if (generic && gqa > kMaxGqa) return TQ_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
         if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
         if (lv.qjl_estimator != TQ_QJL_UNBIASED && lv.qjl_estimator != TQ_QJL_SIGN_PAIR) return TQ_ERR_ARG;
         if (check_ptrs && lv.rot.dense && !aligned16(lv.rot.dense)) return TQ_ERR_ALIGN;
+        if (generic && lv.rot.dense) return TQ_ERR_UNSUPPORTED;
         for (int s = 0; s < lv.n_segments; ++s) {
             const tq_segment &sg = lv.seg[s];
             const tq_segment_layout &L = sg.layout;
@@ -375,6 +506,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             if (st != TQ_OK) return st;
             if (L.batch != B || L.n_heads != H || L.head_dim != d) return TQ_ERR_ARG;
             if (sg.n_tokens < 0 || sg.n_tokens > L.capacity) return TQ_ERR_SIZE;
+            if (generic && sg.attn_mass) return TQ_ERR_UNSUPPORTED;
             if (sg.kind == TQ_SEG_PACKED) {
                 if (L.capacity % 16) return TQ_ERR_ALIGN;
                 if (!fits_u32(&L)) return TQ_ERR_UNSUPPORTED;
@@ -399,6 +531,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                     }
                 }
                 if ((q || qv) && (jl != kJl || L.jl_dim != kJl)) return TQ_ERR_UNSUPPORTED;
+                if (generic && (q || qv || L.value_law != TQ_VALUE_LAW_GAUSS)) return TQ_ERR_UNSUPPORTED;
             } else {
                 if (check_ptrs) {
                     if (!sg.k16 || !sg.v16) return TQ_ERR_ARG;
@@ -476,6 +609,34 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             }
         }
     }
+    if (generic) {  // each (layer, KV head)'s items, the sign bits, the offsets
+        P.generic = true;
+        for (size_t i = 0; i < P.items.size(); ++i) {
+            LayerPlan &lp = P.layer[P.items[i].layer];
+            lp.item[P.items[i].head][lp.n_items[P.items[i].head]++] = static_cast<int>(i);
+        }
+        P.signs.assign(static_cast<size_t>(n_layers) * (kMaxD / 32), 0u);
+        for (int l = 0; l < n_layers; ++l)
+            std::memcpy(P.signs.data() + static_cast<size_t>(l) * (kMaxD / 32), layers[l].rot.sign_bits,
+                        sizeof(uint32_t) * (kMaxD / 32));
+        DecodeDims &D = P.dims;
+        D.L = n_layers;
+        D.B = B;
+        D.H = H;
+        D.Hq = Hq;
+        D.gqa = gqa;
+        D.inv_sqrt_d = inv_sqrt_f32(d);
+        D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+        P.off_items = 256;
+        size_t off = P.off_items + align256(sizeof(WorkItem) * std::max<size_t>(P.items.size(), 1));
+        P.off_layer = off;
+        off += align256(sizeof(LayerPlan) * n_layers);
+        P.off_signs = off;
+        off += align256(sizeof(uint32_t) * P.signs.size());
+        P.off_qrot = off;  // the uploaded plan ends here
+        P.total = off;
+        return TQ_OK;
+    }
     {  // stable bucket sort by class (at most 2 * 8 * 8 packed classes, fp16 last)
         std::vector<int> key(P.items.size());
         int nkeys = 0;
@@ -513,12 +674,13 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         ClassLaunch &c = P.classes.back();
         c.item_hi = static_cast<int>(i) + 1;
         if (w.kind == TQ_SEG_PACKED) {
-            w.n_stages = (w.n_tokens + kPackedStageTokens - 1) / kPackedStageTokens;
+            const int pt = packed_stage_tokens(w.kb, w.vb, w.qjl != 0);
+            w.n_stages = (w.n_tokens + pt - 1) / pt;
             w.stage_begin = stages;
             stages += static_cast<long long>(B) * w.n_stages;
             c.n_stages = stages;
             c.n_ctas = static_cast<int>(std::min<long long>(stages, static_cast<long long>(sms) *
-                                                                         packed_ctas_per_sm(w.qjl != 0)));
+                                                                         packed_ctas_per_sm(w.kb, w.vb, w.qjl != 0)));
         } else {
             w.cta_begin = static_cast<int>(cta);
             cta += static_cast<long long>(B) * w.n_chunks;
@@ -819,11 +981,13 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
     if (st != TQ_OK) return st;
     if (!rot || !K || !V || !out || n_tokens < 0 || t_begin < 0) return TQ_ERR_ARG;
     if (rot->head_dim != layout->head_dim) return TQ_ERR_ARG;
-    if (layout->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(t_begin) + n_tokens > layout->capacity) return TQ_ERR_SIZE;
     if (!out->kcodes || !out->vcodes || !out->kscale || !out->vscale) return TQ_ERR_ARG;
     if (!fits_u32(layout)) return TQ_ERR_UNSUPPORTED;
     const Offsets o = offsets(layout);
+    if (layout->head_dim != kD)
+        return compress_other_dims(layout, rot, o, K, V, n_tokens, stride_b, stride_h, stride_t, t_begin, out,
+                                   static_cast<cudaStream_t>(stream));
     if (o.nq) {
         if (!qjl_S || !out->qjl_signs || !out->qjl_norm) return TQ_ERR_ARG;
         if (layout->jl_dim != kJl) return TQ_ERR_UNSUPPORTED;
@@ -888,6 +1052,10 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
         }
         return e == cudaSuccess ? TQ_OK : cuda_fail(e);
     }
+    if (o.nq == 0 && o.nv == 0) {  // no sketches: one thread per vector, a launch per width
+        const cudaError_t e = launch_rows(p, layout, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    }
     const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
@@ -901,11 +1069,13 @@ tq_status tq_dequantize(const tq_segment_layout *layout, const tq_packed_bufs *b
     if (t_begin < 0 || n_tokens < 0) return TQ_ERR_ARG;
     if (static_cast<int64_t>(t_begin) + n_tokens > layout->capacity) return TQ_ERR_SIZE;
     if ((k_orig || v_orig) && !rot) return TQ_ERR_ARG;
-    if (layout->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     if (rot && rot->head_dim != layout->head_dim) return TQ_ERR_ARG;
     if (!fits_u32(layout)) return TQ_ERR_UNSUPPORTED;
     if (n_tokens == 0) return TQ_OK;
     const Offsets o = offsets(layout);
+    if (layout->head_dim != kD)
+        return dequantize_other_dims(layout, bufs, rot, o, t_begin, n_tokens, k_rot, v_rot, k_orig, v_orig,
+                                     static_cast<cudaStream_t>(stream));
     DequantParams p;
     std::memset(&p, 0, sizeof(p));
     p.B = layout->batch;
@@ -1101,13 +1271,52 @@ tq_status tq_decode_attention(const tq_layer_view *layers, int n_layers, int bat
             std::memcpy(host + P.off_grp_part, P.grp_part.data(), sizeof(int) * P.grp_part.size());
             std::memcpy(host + P.off_grp_nparts, P.grp_nparts.data(), sizeof(int) * P.grp_nparts.size());
         }
-        std::memcpy(host + P.off_lbh_total, P.lbh_total.data(), sizeof(int) * P.lbh_total.size());
+        if (!P.lbh_total.empty())
+            std::memcpy(host + P.off_lbh_total, P.lbh_total.data(), sizeof(int) * P.lbh_total.size());
+        if (!P.signs.empty())
+            std::memcpy(host + P.off_signs, P.signs.data(), sizeof(uint32_t) * P.signs.size());
         if (!P.cta_item.empty())
             std::memcpy(host + P.off_cta_item, P.cta_item.data(), sizeof(int) * P.cta_item.size());
         e = cudaMemcpyAsync(ws, host, P.off_qrot, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e);
         e = cudaEventRecord(sl.ev, s);
         if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (P.generic) {  // head dims other than kD: one kernel, one CTA per (layer, batch, KV head)
+        GenDecodeParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        gp.L = n_layers;
+        gp.B = batch;
+        gp.H = n_heads;
+        gp.Hq = q_heads;
+        gp.gqa = P.dims.gqa;
+        gp.qk_scale = P.dims.qk_scale;
+        gp.inv_sqrt_d = P.dims.inv_sqrt_d;
+        gp.items = reinterpret_cast<const WorkItem *>(ws + P.off_items);
+        gp.layer = reinterpret_cast<const LayerPlan *>(ws + P.off_layer);
+        gp.signs = reinterpret_cast<const uint32_t *>(ws + P.off_signs);
+        gp.q = static_cast<const uint16_t *>(q);
+        gp.out = out;
+        {
+            std::lock_guard<std::mutex> lock(g_cb_mutex_tables());
+            for (const WorkItem &w : P.items)
+                if (w.kind == TQ_SEG_PACKED) {
+                    const FittedCodebook &cb = fit(w.vb, TQ_VALUE_LAW_GAUSS);
+                    for (int k = 0; k < (1 << w.vb); ++k) gp.centroid[cb_off(w.vb) + k] = static_cast<float>(cb.level[k]);
+                }
+        }
+        if (g_ev_start) {
+            e = cudaEventRecord(g_ev_start, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        e = launch_gen_decode(gp, head_dim, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (g_ev_stop) {
+            e = cudaEventRecord(g_ev_stop, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        g_last_launches.store(1);
+        return TQ_OK;
     }
     DecodeWorkspace W;
     W.items = reinterpret_cast<WorkItem *>(ws + P.off_items);

@@ -53,6 +53,24 @@ struct CompressParams {
     float cent[kCbTotal];        // value centroids, flat by bit width (value sketches)
 };
 
+// Keys or values of the heads of one bit width, one thread per vector
+// (tq_compress_rows.cu): launches of an SRHT compression without QJL sketches.
+struct RowsParams {
+    const uint16_t *X;           // K or V, element (b, h, t, i) at b*sb + h*sh + t*st + i
+    int64_t sb, sh, st;
+    int B, H, T, t_begin, capacity;
+    uint8_t *codes;              // kcodes or vcodes
+    float *scale;                // kscale or vscale
+    uint32_t block;              // bytes per batch element of the code buffer
+    uint32_t off[kMaxH];         // per-head byte offset inside a batch block
+    int n_heads;                 // heads of this launch (all of one width)
+    uint8_t head[kMaxH];         // their indices
+    uint32_t in_mask[kD / 2];    // word i: the input sign bits of coordinates 2i (bit 15), 2i + 1 (bit 31)
+    float out_scale[kD];         // coordinate i: -binary32(1/sqrt(d)) if D_i = -1, else +
+    float thr[255];              // values: the width's thresholds, ascending
+};
+cudaError_t launch_compress_rows(const RowsParams &p, int bits, bool values, cudaStream_t s);
+
 // ----------------------------------------------------------------- dequantize
 struct DequantParams {
     int B, H, t_begin, n, capacity;
@@ -159,9 +177,9 @@ struct DecodeWorkspace {
 };
 
 // Stage geometry of the split-K kernels: the fp16 kernel takes 64 tokens per
-// stage (16 per warp), the packed kernels 128 (32 per warp, two 16-token tiles).
+// stage (16 per warp); the packed kernels take 128 or 256 per stage (each warp
+// 32 tokens, two 16-token tiles, of every 128), see packed_stage_tokens.
 constexpr int kStageTokens = 64;
-constexpr int kPackedStageTokens = 128;
 constexpr int kDecodeWarps = 4;
 constexpr int kStages = 4;
 
@@ -176,12 +194,24 @@ struct ClassLaunch {
     int cta_off;       // this launch's per-CTA item table within DecodeWorkspace::cta_item
 };
 
-// Resident CTAs per SM of the packed split-K kernels (registers and shared
-// memory are sized for it).
-constexpr int kPackedCtasPerSm = 4;
-// QJL classes carry the sketch operands too: 3 CTAs per SM (more registers each)
-constexpr int kPackedCtasPerSmQjl = 3;
-__host__ __device__ constexpr int packed_ctas_per_sm(bool qjl) { return qjl ? kPackedCtasPerSmQjl : kPackedCtasPerSm; }
+// Stage geometry of a packed split-K class, chosen by the bytes a token-head
+// carries.  Light classes (<= 112 B: K3V3 and narrower) do little work per
+// token, so the per-stage costs (the CTA barrier, the copy issue, the cursor)
+// weigh more: they run 256-token stages (512 at <= 64 B: K2V1, K1V2, ...) at 3
+// resident CTAs per SM.  Heavier classes run 128-token stages at 4 CTAs per
+// SM, except with QJL sketches, whose operands take more registers (3 CTAs per
+// SM).  Registers and shared memory of each instantiation are sized for its
+// CTAs per SM.
+__host__ __device__ constexpr int packed_token_bytes(int kb, int vb, bool qjl) {
+    return 16 * (kb + vb) + 8 + (qjl ? 20 : 0);
+}
+__host__ __device__ constexpr bool packed_light(int kb, int vb, bool qjl) { return packed_token_bytes(kb, vb, qjl) <= 112; }
+__host__ __device__ constexpr int packed_stage_tokens(int kb, int vb, bool qjl) {
+    return packed_token_bytes(kb, vb, qjl) <= 64 ? 512 : (packed_light(kb, vb, qjl) ? 256 : 128);
+}
+__host__ __device__ constexpr int packed_ctas_per_sm(int kb, int vb, bool qjl) {
+    return (qjl || packed_light(kb, vb, qjl)) ? 3 : 4;
+}
 
 typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, const int *cta_item,
                                       int n_ctas, long long n_stages, const unsigned short *value_half,
@@ -195,6 +225,55 @@ PackedLauncher packed_launcher_kb5(int vb, bool qjl);
 PackedLauncher packed_launcher_kb6(int vb, bool qjl);
 PackedLauncher packed_launcher_kb7(int vb, bool qjl);
 PackedLauncher packed_launcher_kb8(int vb, bool qjl);
+
+// ----------------------------------------------------------------- other head dims
+// Compression, dequantization and decode attention for head dimensions other
+// than kD (powers of two 16..1024; tq_generic.cu).  No QJL sketches, dense
+// rotations or attention-mass outputs on this path.
+constexpr int kMaxD = TQ_MAX_HEAD_DIM;
+
+struct GenCompressParams {
+    const uint16_t *K, *V;
+    int64_t sb, sh, st;          // element strides of K and V
+    int B, H, T, t_begin, capacity;
+    uint8_t *kcodes, *vcodes;
+    float *kscale, *vscale;
+    uint32_t kblock, vblock;
+    uint32_t koff[kMaxH], voff[kMaxH];
+    uint8_t kbits[kMaxH], vbits[kMaxH];
+    uint32_t sign_bits[kMaxD / 32];
+    float inv_sqrt_d;
+    float thr[kCbTotal];         // value thresholds, flat by bit width
+};
+
+struct GenDequantParams {
+    int B, H, t_begin, n, capacity;
+    const uint8_t *kcodes, *vcodes;
+    const float *kscale, *vscale;
+    uint32_t kblock, vblock;
+    uint32_t koff[kMaxH], voff[kMaxH];
+    uint8_t kbits[kMaxH], vbits[kMaxH];
+    uint32_t sign_bits[kMaxD / 32];
+    float inv_sqrt_d;
+    float *k_rot, *v_rot, *k_orig, *v_orig;
+    float centroid[kCbTotal];
+};
+
+struct GenDecodeParams {
+    int L, B, H, Hq, gqa;
+    float qk_scale;              // log2(e) / sqrt(d)
+    float inv_sqrt_d;
+    const WorkItem *items;       // one per (layer, segment, KV head) with tokens
+    const LayerPlan *layer;      // each (layer, KV head)'s items
+    const uint32_t *signs;       // [L][kMaxD / 32] sign bits of each layer's rotation
+    const uint16_t *q;           // fp16 [L][B][Hq][d]
+    float *out;                  // [L][B][Hq][d]
+    float centroid[kCbTotal];    // value centroids, flat by bit width
+};
+
+cudaError_t launch_gen_compress(const GenCompressParams &p, int d, cudaStream_t s);
+cudaError_t launch_gen_dequant(const GenDequantParams &p, int d, cudaStream_t s);
+cudaError_t launch_gen_decode(const GenDecodeParams &p, int d, cudaStream_t s);
 
 // Records a CUDA error for tq_last_cuda_error() and returns TQ_ERR_CUDA.
 tq_status record_cuda_error(cudaError_t e);

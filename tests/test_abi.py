@@ -138,11 +138,12 @@ def test_host_side_argument_errors(tq):
     st = lib.tq_compress(ctypes.byref(L), ctypes.byref(rot), None, ctypes.c_void_p(18), ctypes.c_void_p(16),
                          8, 0, 0, 128, 0, ctypes.byref(fake), None)
     assert st == -3
-    # head_dim the kernels do not implement
-    L64 = tq.make_layout(1, 8, 64, 64, 3, 3)
+    # a feature the head dims other than 128 do not take (QJL sketches)
+    L64 = tq.make_layout(1, 8, 64, 64, 3, 3, qjl=[1] + [0] * 7)
     rot64 = tq.tq_make_rotation(64, 42)
-    st = lib.tq_compress(ctypes.byref(L64), ctypes.byref(rot64), None, ctypes.c_void_p(16), ctypes.c_void_p(16),
-                         8, 0, 0, 64, 0, ctypes.byref(fake), None)
+    st = lib.tq_compress(ctypes.byref(L64), ctypes.byref(rot64), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                         ctypes.c_void_p(16), 8, ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(64),
+                         0, ctypes.byref(tq.tq_packed_bufs(16, 16, 16, 16, 16, 16)), None)
     assert st == -2
     # decode: GQA 8 unsupported, bad head counts rejected
     seg = tq.Fp16Segment(1, 2, 128, 16, device="cpu", n_tokens=4)

@@ -163,6 +163,10 @@ def _groups(L, B, H):
     ("w4", None, None),
     ("w5", 32, 65536),
     ("w5", 1, 4096),
+    ("w5", 8, 16384),
+    ("w5", 32, 4096),
+    ("w3", 8, None),   # the age tiers at 1.05M cached tokens per layer
+    ("w4", 32, None),  # per-head widths and QJL at 1.05M cached tokens per layer
 ])
 def test_static_workload_full_size(lib, name, batch, context):
     T, MC = lib
