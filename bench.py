@@ -50,7 +50,7 @@ from rotated_quantized_kv_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attn HBM GB/s (% of ~8 TB/s) over packed KV; KV compress Mtok/s"
 NOMINAL_HBM_GBS = 8000.0
-DECODE_SRCS = ("tq_decode_packed.cuh", "tq_decode_common.cuh", "tq_decode.cu", "tq_internal.h")
+DECODE_SRCS = ("tq_decode_packed.cuh", "tq_decode_common.cuh", "tq_decode.cu", "tq_decode_geometry.h")
 
 
 def measured_tensor_peak():

@@ -35,7 +35,7 @@ def nvcc() -> str:
 def _sources():
     return [os.path.join(CSRC, s) for s in CUDA_SOURCES + HOST_SOURCES] + [
         os.path.join(CSRC, h) for h in ("tq_internal.h", "tq_decode_common.cuh", "tq_decode_packed.cuh",
-                                        "tq_mass.h")] + [
+                                        "tq_mass.h", "tq_decode_geometry.h")] + [
         os.path.join(ROOT, "include", "tq.h")]
 
 

@@ -66,6 +66,25 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return r;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// max(a, b, c) in one instruction (order-free: the absmax needs no fixed order)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
@@ -93,15 +112,35 @@ __device__ __forceinline__ void put(uint32_t (&w)[4 * B], int i, uint32_t k) {
     if (sh + B > 32) w[wi + 1] += k >> (32 - sh);
 }
 
+// Key codes are put as kKeyLo + code (a float bit pattern, see the key
+// quantizer); word j of the record then holds the sum of the kKeyLo parts of
+// its codes on top of the codes, modulo 2^32.  kKeyLo + code carries nothing
+// out of its low 10 bits (code < 512), so the parts shifted out of a word
+// (sh + B > 32, a right shift by less than B <= 8) are kKeyLo >> s exactly.
+constexpr uint32_t kKeyLo = 0x4B000000u + 512u;
+template <int B>
+__host__ __device__ constexpr uint32_t key_offset_word(int j) {
+    uint32_t c = 0;
+    for (int i = 0; i < 128; i++) {
+        const int bit = i * B, wi = bit >> 5, sh = bit & 31;
+        if (wi == j) c += kKeyLo << sh;
+        if (sh + B > 32 && wi + 1 == j) c += kKeyLo >> (32 - sh);
+    }
+    return c;
+}
+
 template <int BITS, bool VAL>
 __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid_constant__ RowsParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + kWarps * 2 * kWarpBuf);  // [64]
-    float *out_scale = reinterpret_cast<float *>(in_mask + 64);                      // [128]
-    float *thr = out_scale + kD;                                                     // [255]
+    float *out_pair = reinterpret_cast<float *>(in_mask + 64);                       // [64][2]
+    float *thr = out_pair + kD;                                                      // [255]
+    uint2 *vtab = reinterpret_cast<uint2 *>(thr + 256);                             // [1024] (values, <= 3 bits)
     for (int i = threadIdx.x; i < 64; i += kThreads) in_mask[i] = p.in_mask[i];
-    for (int i = threadIdx.x; i < kD; i += kThreads) out_scale[i] = p.out_scale[i];
+    for (int i = threadIdx.x; i < kD; i += kThreads) out_pair[i] = p.out_scale[(i >> 1) + 64 * (i & 1)];
     for (int i = threadIdx.x; i < 255; i += kThreads) thr[i] = p.thr[i];
+    if constexpr (VAL && BITS <= 3)
+        for (int i = threadIdx.x; i < kRowsBuckets; i += kThreads) vtab[i] = make_uint2(p.bucket[i].t, p.bucket[i].k);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,28 +162,24 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
         const int t = tb * 32 + lane;
         const uint8_t *row = bufs + (it & 1) * kWarpBuf + lane * kRowBytes;
 
-        // ---- load, input sign flip on the fp16 bits, widen
+        // ---- load, input sign flip on the fp16 bits, widen: chunks c and
+        // c + 8 (coordinates 8c.. and 64 + 8c..) are permuted into half2 pairs
+        // (m, m + 64) that widen straight into the register pairs
         float2 a[64];
 #pragma unroll
-        for (int c = 0; c < 16; c++) {
-            uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (c ^ (lane & 7)));
-            const uint4 mk = *reinterpret_cast<const uint4 *>(in_mask + 4 * c);
-            v.x ^= mk.x;
-            v.y ^= mk.y;
-            v.z ^= mk.z;
-            v.w ^= mk.w;
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int c = 0; c < 8; c++) {
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(row + 16 * (c ^ (lane & 7)));
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(row + 16 * ((c + 8) ^ (lane & 7)));
+            const uint4 m0 = *reinterpret_cast<const uint4 *>(in_mask + 4 * c);
+            const uint4 m1 = *reinterpret_cast<const uint4 *>(in_mask + 4 * (c + 8));
+            const uint32_t w0[4] = {v0.x ^ m0.x, v0.y ^ m0.y, v0.z ^ m0.z, v0.w ^ m0.w};
+            const uint32_t w1[4] = {v1.x ^ m1.x, v1.y ^ m1.y, v1.z ^ m1.z, v1.w ^ m1.w};
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&wv[e]));
-                const int i = 8 * c + 2 * e;  // coordinates i, i + 1
-                if (c < 8) {
-                    a[i].x = f.x;
-                    a[i + 1].x = f.y;
-                } else {
-                    a[i - 64].y = f.x;
-                    a[i - 63].y = f.y;
-                }
+                const int i = 8 * c + 2 * e;  // pairs (i, i + 64) and (i + 1, i + 65)
+                const uint32_t lo = prmt(w0[e], w1[e], 0x5410u), hi = prmt(w0[e], w1[e], 0x7632u);
+                a[i] = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+                a[i + 1] = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
             }
         }
         __syncwarp();  // every lane has read its row: the buffer may be restaged
@@ -168,8 +203,13 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
             a[m].y = __fsub_rn(u, v);
         }
         // output sign flip and binary32(1/sqrt(d)): one rounded multiply each
+        // (out_pair[m] = the scales of coordinates m and m + 64)
 #pragma unroll
-        for (int m = 0; m < 64; m++) a[m] = fmul2(a[m], make_float2(out_scale[m], out_scale[m + 64]));
+        for (int m = 0; m < 64; m += 2) {
+            const float4 sc = *reinterpret_cast<const float4 *>(out_pair + 2 * m);
+            a[m] = fmul2(a[m], make_float2(sc.x, sc.y));
+            a[m + 1] = fmul2(a[m + 1], make_float2(sc.z, sc.w));
+        }
 
         uint32_t w[4 * BITS];
 #pragma unroll
@@ -180,14 +220,17 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
             // code = clamp(floor(u), 0, 2^b - 1)
             float mx = 0.0f;
 #pragma unroll
-            for (int m = 0; m < 64; m++) mx = fmaxf(mx, fmaxf(fabsf(a[m].x), fabsf(a[m].y)));
+            for (int m = 0; m < 64; m++) mx = fmax3(mx, fabsf(a[m].x), fabsf(a[m].y));
             scale = mx;
             const float r = mx > 0.0f ? __frcp_rn(mx) : 0.0f;
             constexpr float hc = static_cast<float>(1 << (BITS - 1));
-            // floor(u) for u in [-1, 2^b]: round-down of u + 2^23 + 512 has the
-            // exponent of 2^23, so its low bits are 512 + floor(u)
+            // v = y r lies in [-1, 1]: r = binary32(1/m) is within 2^-24 of 1/m
+            // and |y| <= m, so |y r| <= 1 + 2^-24 rounds to at most 1.  Hence
+            // u = round(v + 1) 2^(b-1) >= 0 and only the top clamp can act (at
+            // v = 1).  floor(u): the round-down of u + 2^23 + 512 has the exponent
+            // of 2^23, so its bit pattern is kLo + floor(u).
             constexpr float kMagic = 8388608.0f + 512.0f;
-            constexpr int kLo = 0x4B000000 + 512, kHi = kLo + (1 << BITS) - 1;
+            constexpr uint32_t kHi = kKeyLo + (1u << BITS) - 1u;
 #pragma unroll
             for (int m = 0; m < 64; m++) {
                 const float2 v = fmul2(a[m], make_float2(r, r));
@@ -195,11 +238,12 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                 // power of two commutes with the rounding
                 const float2 u = ffma2(v, make_float2(hc, hc), make_float2(hc, hc));
                 const float2 f = fadd2_rm(u, make_float2(kMagic, kMagic));
-                const int k0 = min(max(__float_as_int(f.x), kLo), kHi) - kLo;
-                const int k1 = min(max(__float_as_int(f.y), kLo), kHi) - kLo;
-                put<BITS>(w, m, static_cast<uint32_t>(k0));
-                put<BITS>(w, m + 64, static_cast<uint32_t>(k1));
+                // kLo + code, placed as is: the words take off the kLo parts below
+                put<BITS>(w, m, min(__float_as_uint(f.x), kHi));
+                put<BITS>(w, m + 64, min(__float_as_uint(f.y), kHi));
             }
+#pragma unroll
+            for (int j = 0; j < 4 * BITS; j++) w[j] -= key_offset_word<BITS>(j);
         } else {
             // ---- values: sigma = sqrt(pairwise-tree sum of y^2 in index order / d),
             // u = y * binary32(1/sigma), code = #{k : thr_k < u}
@@ -222,7 +266,21 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
             scale = sigma;
             const float r = sigma > 0.0f ? __frcp_rn(sigma) : 0.0f;
             constexpr int NT = (1 << BITS) - 1;
-            if constexpr (BITS <= 4) {
+            if constexpr (BITS <= 3) {
+                // #{k : thr_k < u} from the bucket of u's top ten bits (sign,
+                // exponent, one mantissa bit): every u in a bucket exceeds the
+                // same k_base thresholds, and at most one threshold t_c lies in
+                // the bucket (the host checks), so the count is k_base + [t_c < u]
+                const uint32_t tab = static_cast<uint32_t>(__cvta_generic_to_shared(vtab));
+#pragma unroll
+                for (int m = 0; m < 64; m++) {
+                    const float2 u = fmul2(a[m], make_float2(r, r));
+                    const uint2 e0 = lds64(tab + ((__float_as_uint(u.x) >> 22) << 3));
+                    const uint2 e1 = lds64(tab + ((__float_as_uint(u.y) >> 22) << 3));
+                    put<BITS>(w, m, e0.y + (__uint_as_float(e0.x) < u.x ? 1u : 0u));
+                    put<BITS>(w, m + 64, e1.y + (__uint_as_float(e1.x) < u.y ? 1u : 0u));
+                }
+            } else if constexpr (BITS == 4) {
                 float th[NT];
 #pragma unroll
                 for (int j = 0; j < NT; j++) th[j] = thr[j];
@@ -274,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
 
 template <int BITS, bool VAL>
 cudaError_t rows_launch(const RowsParams &p, cudaStream_t s) {
-    constexpr size_t smem = kWarps * 2 * kWarpBuf + 64 * 4 + kD * 4 + 255 * 4;
+    constexpr size_t smem = kWarps * 2 * kWarpBuf + 64 * 4 + kD * 4 + 256 * 4 + ((VAL && BITS <= 3) ? kRowsBuckets * 8 : 0);
     static bool configured = false;
     if (!configured) {
         const cudaError_t e = cudaFuncSetAttribute(compress_rows_kernel<BITS, VAL>,

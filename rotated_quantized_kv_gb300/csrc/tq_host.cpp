@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstring>
 #include <atomic>
+#include <limits>
 #include <mutex>
 #include <vector>
 
@@ -315,10 +316,64 @@ int sm_count() {
 
 float inv_sqrt_f32(int d) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))); }
 
+// Bucket table of a value width <= 3 (RowsParams::bucket): bucket i holds the
+// bit patterns [i << 22, (i + 1) << 22), i.e. sign, exponent and one mantissa
+// bit of the quotient u; k = the thresholds below every u of the bucket, t = the
+// one threshold inside it (+inf if none).  False if a bucket holds two.
+bool value_buckets(const float *thr, int nt, RowsParams::Bucket *out) {
+    auto as_float = [](uint32_t b) {
+        float f;
+        std::memcpy(&f, &b, 4);
+        return f;
+    };
+    const float inf = std::numeric_limits<float>::infinity();
+    uint32_t inf_bits;
+    std::memcpy(&inf_bits, &inf, 4);
+    for (int i = 0; i < kRowsBuckets; ++i) {
+        const uint32_t m = static_cast<uint32_t>(i & 511);
+        if (m >= 510) {  // exponent 255: infinities and NaNs, never a quotient of finite inputs
+            out[i].t = inf_bits;
+            out[i].k = i < 512 ? static_cast<uint32_t>(nt) : 0u;
+            continue;
+        }
+        const float lo = as_float(m << 22);                                   // magnitude range [lo, hi)
+        const float hi = (m + 1) << 22 >= 0x7F800000u ? inf : as_float((m + 1) << 22);
+        int k = 0, inside = 0;
+        float t_c = inf;
+        for (int j = 0; j < nt; ++j) {
+            const float t = thr[j];
+            if (i < 512) {  // u in [lo, hi)
+                if (t < lo) ++k;
+                else if (t < hi) { ++inside; t_c = t; }
+            } else {  // u in (-hi, -lo]
+                if (t <= -hi) ++k;
+                else if (t <= -lo) { ++inside; t_c = t; }
+            }
+        }
+        if (inside > 1) return false;
+        uint32_t tb;
+        std::memcpy(&tb, &t_c, 4);
+        out[i].t = tb;
+        out[i].k = static_cast<uint32_t>(k);
+    }
+    return true;
+}
+
 // Launches of the one-thread-per-vector kernels for a compression without
 // sketches: the keys of each distinct key width, then the values of each
-// distinct value width (one launch each; uniform layouts take two).
+// distinct value width (one launch each; uniform layouts take two).  Returns
+// cudaErrorNotSupported, before launching anything, if a value width's bucket
+// table does not separate its thresholds (the caller then takes the
+// four-lanes-per-vector kernel).
 cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout, cudaStream_t s) {
+    for (int h = 0; h < c.H; ++h) {
+        if (c.vbits[h] > 3) continue;
+        const FittedCodebook &cb = fit(c.vbits[h], layout->value_law);
+        float thr[7];
+        for (int k = 0; k + 1 < (1 << c.vbits[h]); ++k) thr[k] = static_cast<float>(cb.bound[k]);
+        static thread_local RowsParams::Bucket scratch[kRowsBuckets];
+        if (!value_buckets(thr, (1 << c.vbits[h]) - 1, scratch)) return cudaErrorNotSupported;
+    }
     RowsParams p;
     std::memset(&p, 0, sizeof(p));
     p.sb = c.sb;
@@ -350,6 +405,7 @@ cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout
             if (values) {
                 const FittedCodebook &cb = fit(bits, layout->value_law);
                 for (int k = 0; k + 1 < (1 << bits); ++k) p.thr[k] = static_cast<float>(cb.bound[k]);
+                if (bits <= 3 && !value_buckets(p.thr, (1 << bits) - 1, p.bucket)) return cudaErrorNotSupported;
             }
             const cudaError_t e = launch_compress_rows(p, bits, values != 0, s);
             if (e != cudaSuccess) return e;
@@ -1054,7 +1110,7 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
     }
     if (o.nq == 0 && o.nv == 0) {  // no sketches: one thread per vector, a launch per width
         const cudaError_t e = launch_rows(p, layout, static_cast<cudaStream_t>(stream));
-        return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+        if (e != cudaErrorNotSupported) return e == cudaSuccess ? TQ_OK : cuda_fail(e);
     }
     const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/tq.h"
+#include "tq_decode_geometry.h"
 
 namespace tqk {
 
@@ -53,6 +54,8 @@ struct CompressParams {
     float cent[kCbTotal];        // value centroids, flat by bit width (value sketches)
 };
 
+constexpr int kRowsBuckets = 1024;  // buckets of a value quotient: sign, exponent, one mantissa bit
+
 // Keys or values of the heads of one bit width, one thread per vector
 // (tq_compress_rows.cu): launches of an SRHT compression without QJL sketches.
 struct RowsParams {
@@ -68,6 +71,9 @@ struct RowsParams {
     uint32_t in_mask[kD / 2];    // word i: the input sign bits of coordinates 2i (bit 15), 2i + 1 (bit 31)
     float out_scale[kD];         // coordinate i: -binary32(1/sqrt(d)) if D_i = -1, else +
     float thr[255];              // values: the width's thresholds, ascending
+    // values of <= 3 bits: bucket b = (bit pattern of u) >> 22 holds k_base and
+    // the bucket's one threshold t_c (+inf if none) as bits: code = k_base + [t_c < u]
+    struct Bucket { uint32_t t, k; } bucket[kRowsBuckets];
 };
 cudaError_t launch_compress_rows(const RowsParams &p, int bits, bool values, cudaStream_t s);
 
@@ -193,25 +199,6 @@ struct ClassLaunch {
     long long n_stages;
     int cta_off;       // this launch's per-CTA item table within DecodeWorkspace::cta_item
 };
-
-// Stage geometry of a packed split-K class, chosen by the bytes a token-head
-// carries.  Light classes (<= 112 B: K3V3 and narrower) do little work per
-// token, so the per-stage costs (the CTA barrier, the copy issue, the cursor)
-// weigh more: they run 256-token stages (512 at <= 64 B: K2V1, K1V2, ...) at 3
-// resident CTAs per SM.  Heavier classes run 128-token stages at 4 CTAs per
-// SM, except with QJL sketches, whose operands take more registers (3 CTAs per
-// SM).  Registers and shared memory of each instantiation are sized for its
-// CTAs per SM.
-__host__ __device__ constexpr int packed_token_bytes(int kb, int vb, bool qjl) {
-    return 16 * (kb + vb) + 8 + (qjl ? 20 : 0);
-}
-__host__ __device__ constexpr bool packed_light(int kb, int vb, bool qjl) { return packed_token_bytes(kb, vb, qjl) <= 112; }
-__host__ __device__ constexpr int packed_stage_tokens(int kb, int vb, bool qjl) {
-    return packed_token_bytes(kb, vb, qjl) <= 64 ? 512 : (packed_light(kb, vb, qjl) ? 256 : 128);
-}
-__host__ __device__ constexpr int packed_ctas_per_sm(int kb, int vb, bool qjl) {
-    return (qjl || packed_light(kb, vb, qjl)) ? 3 : 4;
-}
 
 typedef cudaError_t (*PackedLauncher)(const DecodeDims &, const DecodeWorkspace &, const int *cta_item,
                                       int n_ctas, long long n_stages, const unsigned short *value_half,
