@@ -31,6 +31,7 @@ workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -260,7 +261,8 @@ def result_line(args, world, m, t, e2e, comp, config, workload):
         "config": config,
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "tokens_per_s": round(world * m.B * K / (t["ms"] * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "decode_packed_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_packed_kernel" if m.d == 128 else "gen_decode_kernel",
+                     "achieved": round(achieved, 1),
                      "timing": "CUDA events around the packed launches of K further steps",
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic_for(workload, int(np.mean(t["packed_bytes"]))),
@@ -358,6 +360,8 @@ def run_static(args, rank, world, tq):
     from rotated_quantized_kv_gb300.model_cache import StaticCache
     dev = torch.cuda.current_device()
     w = W.WORKLOADS[args.workload]
+    if args.head_dim:
+        w = dataclasses.replace(w, head_dim=args.head_dim)
     seed = 1000 + int(args.workload[1:])
     m = StaticCache(w, batch=args.batch, context=args.context, seed=seed, rotation=args.rotation)
     K, Wm = args.steps, args.warmup
@@ -516,14 +520,18 @@ def run_static(args, rank, world, tq):
     return res
 
 
-EXTRA_POINTS = (("w2", None, None), ("w3", 8, None), ("w4", 32, None))
+# (workload, batch, context, head_dim): w2, the mixed-tier points of >= 1M cached
+# tokens per layer, and the w5 shape at head_dim 256 (the other head dims' kernels)
+EXTRA_POINTS = (("w2", None, None, None), ("w3", 8, None, None), ("w4", 32, None, None), ("w5", 8, 16384, 256))
 
 
-def decode_point(tq, name, batch, context, K, Wm, world, dev):
+def decode_point(tq, name, batch, context, K, Wm, world, dev, head_dim=None):
     """Decode figures of one more workload (compact): whole-step GB/s over K
-    steps and the packed split-K kernel alone (CUDA events on its stream)."""
+    steps and the split-K kernel alone (CUDA events on its stream)."""
     from rotated_quantized_kv_gb300.model_cache import ChunkedDecodeCache, StaticCache
     w = W.WORKLOADS[name]
+    if head_dim:
+        w = dataclasses.replace(w, head_dim=head_dim)
     if name == "w2":
         m = ChunkedDecodeCache()
         step = m.step
@@ -546,12 +554,34 @@ def decode_point(tq, name, batch, context, K, Wm, world, dev):
     value = whole_job_gbs(world, t["total_bytes"], t["ms"])
     kern_ms = float(np.mean(t["kern_ms"]))
     achieved = float(np.mean(t["packed_bytes"])) / (kern_ms * 1e-3) / 1e9
-    res = {"workload": w.name, "batch": B, "context": T, "tokens": B * T, "layers": w.layers,
+    res = {"workload": w.name, "batch": B, "context": T, "tokens": B * T, "layers": w.layers, "head_dim": w.head_dim,
+           "kernel": "decode_packed_kernel" if w.head_dim == 128 else "gen_decode_kernel",
            "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(t["ms"] / K, 5),
            "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
            "kernel_gbs": round(achieved, 1), "kernel_frac": round(achieved / peak, 4), "peak": peak,
            "peak_kind": peak_kind, "kernel_ms": round(kern_ms, 5),
            "bytes_per_step": int(t["total_bytes"] / K), "gpu_launches": t["launches"]}
+    if head_dim and head_dim != 128:
+        # compression at this head_dim: every layer's packed prompt again, from
+        # one fresh fp16 input per layer position (the generic kernels)
+        src = W.kv_block(w, 0, m.B, m.T, 1007, device="cuda")
+        calls, scr = [], {}
+        for l in range(m.L):
+            for si in m.layers[l]:
+                if si.packed:
+                    key = (tuple(si.seg.layout.kbits), tuple(si.seg.layout.vbits), si.pos0)
+                    if key not in scr:
+                        scr[key] = tq.PackedSegment(si.seg.layout)
+                    calls.append(lambda si=si, sg=scr[key], rot=m.rots[l]: tq.tq_compress(
+                        sg, rot, src[0][:, :, si.pos0:si.pos0 + si.n], src[1][:, :, si.pos0:si.pos0 + si.n]))
+        cms = time_compress(tq, calls) / m.L
+        ctok = sum(si.n for si in m.layers[0] if si.packed) * m.B
+        cbytes = sum(m.B * si.n * (m.H * m.d * 4 + si.bytes_per_token(m.d)) for si in m.layers[0] if si.packed)
+        res["compress"] = {"value": round(ctok / (cms * 1e-3) / 1e6, 1), "unit": "Mtok/s",
+                           "ms_per_layer": round(cms, 4), "achieved_gbs": round(cbytes / (cms * 1e-3) / 1e9, 1),
+                           "frac_of_peak": round(cbytes / (cms * 1e-3) / 1e9 / peak, 4),
+                           "kernel": "gen_compress_kernel"}
+        del src, calls, scr
     del m
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -572,10 +602,11 @@ def run_ours(args, rank, world):
         wl = W.WORKLOADS[args.workload]
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    if not args.no_extra and args.workload == "w5" and args.batch is None and args.context is None:
+    if (not args.no_extra and args.workload == "w5" and args.batch is None and args.context is None
+            and args.head_dim is None):
         dev = torch.cuda.current_device()
-        res["also"] = [decode_point(tq, n, b, c, args.steps, args.warmup, world, dev)
-                       for n, b, c in EXTRA_POINTS]
+        res["also"] = [decode_point(tq, n, b, c, args.steps, args.warmup, world, dev, head_dim=hd)
+                       for n, b, c, hd in EXTRA_POINTS]
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
     return res
@@ -734,6 +765,8 @@ def main():
     ap.add_argument("--rotation", default="srht", choices=["srht", "haar"],
                     help="haar: a dense Haar rotation per layer (tensor-core compressor; w1, w3, w5)")
     ap.add_argument("--context", type=int, default=None, help="override the workload's context (w1, w3-w5)")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="override the workload's head_dim (w1, w3-w5; a power of two 16..1024)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
