@@ -261,7 +261,7 @@ def result_line(args, world, m, t, e2e, comp, config, workload):
         "config": config,
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "tokens_per_s": round(world * m.B * K / (t["ms"] * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "decode_packed_kernel" if m.d == 128 else "gen_decode_kernel",
+        "roofline": {"bound": "hbm", "kernel": decode_kernel_name(m.d, m.Hq // m.H),
                      "achieved": round(achieved, 1),
                      "timing": "CUDA events around the packed launches of K further steps",
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -520,6 +520,12 @@ def run_static(args, rank, world, tq):
     return res
 
 
+def decode_kernel_name(d, gqa):
+    """The split-K kernel runs head_dim 128, and 256 / 512 at GQA 1, 2 or 4 (on
+    128-dim sub-records); other shapes run the generic kernel."""
+    return "decode_packed_kernel" if d == 128 or (d in (256, 512) and gqa in (1, 2, 4)) else "gen_decode_kernel"
+
+
 # (workload, batch, context, head_dim): w2, the mixed-tier points of >= 1M cached
 # tokens per layer, and the w5 shape at head_dim 256 (the other head dims' kernels)
 EXTRA_POINTS = (("w2", None, None, None), ("w3", 8, None, None), ("w4", 32, None, None), ("w5", 8, 16384, 256))
@@ -555,7 +561,7 @@ def decode_point(tq, name, batch, context, K, Wm, world, dev, head_dim=None):
     kern_ms = float(np.mean(t["kern_ms"]))
     achieved = float(np.mean(t["packed_bytes"])) / (kern_ms * 1e-3) / 1e9
     res = {"workload": w.name, "batch": B, "context": T, "tokens": B * T, "layers": w.layers, "head_dim": w.head_dim,
-           "kernel": "decode_packed_kernel" if w.head_dim == 128 else "gen_decode_kernel",
+           "kernel": decode_kernel_name(w.head_dim, w.q_heads // w.kv_heads),
            "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(t["ms"] / K, 5),
            "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
            "kernel_gbs": round(achieved, 1), "kernel_frac": round(achieved / peak, 4), "peak": peak,

@@ -23,6 +23,14 @@ namespace {
 // -------------------------------------------------------------- fp16 kernel
 constexpr int kRow16 = 272;  // padded row of 128 fp16 (conflict-free ldmatrix)
 constexpr int kStage16Bytes = 2 * kStageTokens * kRow16;  // one 64-token chunk of K and V
+// head_dim 128 nh: padded rows of 128 nh fp16, a 64-token chunk of K and V, then
+// the cross-warp merge scratch (write_partial) and the flag
+__host__ __device__ constexpr int row16(int nh) { return 256 * nh + 16; }
+__host__ __device__ constexpr int stage16_bytes(int nh) { return 2 * kStageTokens * row16(nh); }
+constexpr int kMergeScratchBytes = (32 + kDecodeWarps * kMaxGqa * kD) * 4;
+__host__ __device__ constexpr int fp16_smem_bytes(int nh) {
+    return nh == 1 ? kStage16Bytes + 16 : stage16_bytes(nh) + kMergeScratchBytes + 16;
+}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(p));
@@ -42,8 +50,14 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *
 // fragment of Q.K and V rows transposed as the A fragment of P.V.  One CTA per
 // (item, batch element, 64-token chunk): a single staged chunk, so that many
 // small CTAs (six per SM) cover the memory latency together.
-__global__ void __launch_bounds__(kThreads, 6)
+//
+// NH > 1 (head_dim 128 NH): the scores run over all NH 128-dim blocks, then
+// each block's P.V is merged across the warps and written as record
+// chunk NH + j of the group (block j), all with the chunk's m and l.
+template <int NH>
+__global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
     decode_fp16_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item) {
+    constexpr int kDh = NH * kD, kRow = row16(NH);
     extern __shared__ __align__(16) uint8_t smem[];
     const int idx = cta_item[blockIdx.x];
     const WorkItem &it = ws.items[idx];
@@ -51,13 +65,14 @@ __global__ void __launch_bounds__(kThreads, 6)
     const int b = local / it.n_chunks, chunk = local - b * it.n_chunks;
     const int tok0 = chunk * it.chunk;
     const int ntok = min(it.chunk, it.n_tokens - tok0);  // <= kStageTokens
-    const uint8_t *K = it.kc + b * it.kstride + static_cast<size_t>(tok0) * (kD * 2);
-    const uint8_t *V = it.vc + b * it.vstride + static_cast<size_t>(tok0) * (kD * 2);
-    for (int i = threadIdx.x; i < 2 * kStageTokens * 16; i += kThreads) {
-        const int which = i / (kStageTokens * 16), r = (i >> 4) % kStageTokens, ch = i & 15;
-        const uint8_t *src = (which ? V : K) + static_cast<size_t>(r) * (kD * 2) + ch * 16;
+    const uint8_t *K = it.kc + b * it.kstride + static_cast<size_t>(tok0) * (kDh * 2);
+    const uint8_t *V = it.vc + b * it.vstride + static_cast<size_t>(tok0) * (kDh * 2);
+    constexpr int kCh = 16 * NH;  // 16-byte pieces of a row
+    for (int i = threadIdx.x; i < 2 * kStageTokens * kCh; i += kThreads) {
+        const int which = i / (kStageTokens * kCh), r = (i / kCh) % kStageTokens, ch = i % kCh;
+        const uint8_t *src = (which ? V : K) + static_cast<size_t>(r) * (kDh * 2) + ch * 16;
         const bool ok = r < ntok;
-        cp_async16_zfill(smem + (which * kStageTokens + r) * kRow16 + ch * 16, ok ? src : K, ok ? 16 : 0);
+        cp_async16_zfill(smem + (which * kStageTokens + r) * kRow + ch * 16, ok ? src : K, ok ? 16 : 0);
     }
     cp_async_commit();
 
@@ -67,14 +82,14 @@ __global__ void __launch_bounds__(kThreads, 6)
     pdl_launch_dependents();
     // B fragments of the (fp16, hence exact) queries: column g holds head g/2;
     // the lo columns (g odd) are zero.
-    uint32_t bq[8][2];
+    uint32_t bq[8 * NH][2];
     {
         const int head = g >> 1;
         const size_t qidx = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + j0 + head;
         const bool ok = head < gqa && (g & 1) == 0;
-        const uint32_t *qw = reinterpret_cast<const uint32_t *>(ws.q + qidx * kD);
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(ws.q + qidx * kDh);
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
+        for (int kk = 0; kk < 8 * NH; kk++) {
             bq[kk][0] = ok ? qw[8 * kk + c] : 0u;
             bq[kk][1] = ok ? qw[8 * kk + c + 4] : 0u;
         }
@@ -84,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 6)
     cp_async_wait<0>();
     __syncthreads();
     const int tile0 = warp * 16;
+    if constexpr (NH == 1) {
     if (tile0 < ntok) {
         const uint8_t *Ks = smem, *Vs = smem + kStageTokens * kRow16;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -113,6 +129,47 @@ __global__ void __launch_bounds__(kThreads, 6)
                   [g](int mt, int r) { return 16 * mt + g + 8 * r; });
     pdl_wait();  // this grid's completion implies the completion of the earlier ones
     finish_and_combine(dims, ws, it.layer, b, it.head, reinterpret_cast<int *>(smem + kStage16Bytes));
+    } else {
+    const uint8_t *Ks = smem, *Vs = smem + kStageTokens * kRow;
+    uint32_t b0 = 0u, b1 = 0u;
+    if (tile0 < ntok) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 8 * NH; kk++) {
+            uint32_t a[4];
+            const int row = tile0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            ldmatrix_x4(a, Ks + row * kRow + kk * 32 + (lane >> 4) * 16);
+            mma16816(acc, a[0], a[1], a[2], a[3], bq[kk][0], bq[kk][1]);
+        }
+        softmax_tile(st, (acc[0] + acc[1]) * dims.qk_scale, (acc[2] + acc[3]) * dims.qk_scale, tile0 + g < ntok,
+                     tile0 + g + 8 < ntok, 1.f, 1.f, g, c, c < gqa, b0, b1);
+    }
+    float *scratch = reinterpret_cast<float *>(smem + stage16_bytes(NH));
+    const int slot0 = ws.grp_part[static_cast<size_t>(idx) * dims.B + b] + chunk * NH;
+#pragma unroll 1
+    for (int j = 0; j < NH; j++) {
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) st.acc[mt][q] = 0.f;
+        if (tile0 < ntok) {
+#pragma unroll
+            for (int mt = 0; mt < 8; mt++) {
+                uint32_t a[4];
+                const int mat = lane >> 3;
+                const int row = tile0 + (lane & 7) + (mat >> 1) * 8;
+                ldmatrix_x4_trans(a, Vs + row * kRow + (kD * j + 16 * mt + (mat & 1) * 8) * 2);
+                mma16816(st.acc[mt], a[0], a[1], a[2], a[3], b0, b1);
+            }
+        }
+        if (j > 0) __syncthreads();  // the previous block's merge is done with the scratch
+        float *part = ws.part + static_cast<size_t>(slot0 + j) * (kMaxGqa * kPartStride);
+        write_partial(st, scratch, part, gqa, [g](int mt, int r) { return 16 * mt + g + 8 * r; });
+    }
+    pdl_wait();
+    finish_and_combine<NH>(dims, ws, it.layer, b, it.head,
+                           reinterpret_cast<int *>(smem + stage16_bytes(NH) + kMergeScratchBytes));
+    }
 }
 
 // -------------------------------------------------------------- prep kernel
@@ -121,6 +178,11 @@ __global__ void __launch_bounds__(kThreads, 6)
 // SRHT or dense Q) and, for QJL layers, t = S q' (fp16 hi/lo words), with
 // sum q', sum t and the power of two, for the split-K kernels, which read them
 // after griddepcontrol.wait.
+//
+// NH > 1 (head_dim 128 NH, SRHT layers only): the same for a vector of NH
+// 128-dim blocks; hi words at [64 j, 64 j + 64) for block j, lo words after
+// all NH blocks' hi words.
+template <int NH>
 __global__ void __launch_bounds__(kThreads)
     decode_prep_kernel(const DecodeDims dims, const DecodeWorkspace ws, const float *S) {
     __shared__ float qsh[kThreads / 32][kD];
@@ -130,6 +192,30 @@ __global__ void __launch_bounds__(kThreads)
     if (wid >= dims.L * dims.B * dims.Hq) return;
     const int l = wid / (dims.B * dims.Hq);
     const LayerPlan &lp = ws.layer[l];
+    if constexpr (NH > 1) {
+        float y[NH][4];
+#pragma unroll
+        for (int j = 0; j < NH; j++) load_q4(ws.q + static_cast<size_t>(wid) * (NH * kD) + kD * j, lane, y[j]);
+        warp_rotate_wide<NH>(y, lp.sign_bits, dims.inv_sqrt_d, lane);
+        const float f = warp_pow2_norm_wide<NH>(y);
+        uint32_t *hi = ws.qrot + static_cast<size_t>(wid) * (NH * kD);
+        float qs = 0.f;
+#pragma unroll
+        for (int j = 0; j < NH; j++) {
+            float yn[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) yn[e] = y[j][e] * f;
+            qs += store_hilo_block(hi, hi + NH * kD / 2, yn, j, lane);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
+        if (lane == 0) {
+            ws.qsum[static_cast<size_t>(wid) * 4] = qs / f;
+            ws.qsum[static_cast<size_t>(wid) * 4 + 1] = 0.f;
+            ws.qsum[static_cast<size_t>(wid) * 4 + 2] = 1.0f / f;
+        }
+        return;
+    }
     float x[4];
     load_q4(ws.q + static_cast<size_t>(wid) * kD, lane, x);
     if (lp.dense) warp_rotate_dense(x, lp.dense, false, lane);
@@ -175,6 +261,32 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+PackedLauncher packed_launcher_wide(int kb, int vb, int nh) {
+    switch (kb) {
+        case 1: return packed_launcher_wide_kb1(vb, nh);
+        case 2: return packed_launcher_wide_kb2(vb, nh);
+        case 3: return packed_launcher_wide_kb3(vb, nh);
+        case 4: return packed_launcher_wide_kb4(vb, nh);
+        case 5: return packed_launcher_wide_kb5(vb, nh);
+        case 6: return packed_launcher_wide_kb6(vb, nh);
+        case 7: return packed_launcher_wide_kb7(vb, nh);
+        case 8: return packed_launcher_wide_kb8(vb, nh);
+        default: return nullptr;
+    }
+}
+
+template <int NH>
+cudaError_t configure_fp16() {
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(decode_fp16_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   fp16_smem_bytes(NH));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return cudaSuccess;
+}
+
 PackedLauncher packed_launcher(int kb, int vb, bool qjl) {
     switch (kb) {
         case 1: return packed_launcher_kb1(vb, qjl);
@@ -197,15 +309,14 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
                                   const float *value_c1,
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop, int *n_launched) {
     *n_launched = 0;
-    static bool configured = false;
-    const size_t smem16 = static_cast<size_t>(dec::kStage16Bytes) + 16;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(dec::decode_fp16_kernel,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem16));
+    const int nh = dims.nh;
+    if (nh != 1 && nh != 2 && nh != 4) return cudaErrorInvalidValue;
+    {
+        const cudaError_t e = nh == 1 ? dec::configure_fp16<1>() : nh == 2 ? dec::configure_fp16<2>()
+                                                                            : dec::configure_fp16<4>();
         if (e != cudaSuccess) return e;
-        configured = true;
     }
+    const size_t smem16 = static_cast<size_t>(dec::fp16_smem_bytes(nh));
     // Order: [prep] -> packed classes -> fp16 segments.  Every kernel after the
     // first may start early (programmatic dependent launch); each grid waits
     // for its predecessor before its final merges, the QJL classes also wait
@@ -219,7 +330,10 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (dims.any_prep) {
         const int n_warps = dims.L * dims.B * dims.Hq;
-        dec::decode_prep_kernel<<<(n_warps + 3) / 4, dec::kThreads, 0, s>>>(dims, ws, S);
+        const unsigned grid = static_cast<unsigned>((n_warps + 3) / 4);
+        if (nh == 1) dec::decode_prep_kernel<1><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
+        else if (nh == 2) dec::decode_prep_kernel<2><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
+        else dec::decode_prep_kernel<4><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
         first = false;
         ++*n_launched;
     }
@@ -232,7 +346,8 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
     for (int i = 0; i < n_classes; i++) {
         const ClassLaunch &c = classes[i];
         if (c.n_ctas <= 0 || c.kb == 16) continue;
-        const PackedLauncher fn = dec::packed_launcher(c.kb, c.vb, c.qjl != 0);
+        const PackedLauncher fn = nh == 1 ? dec::packed_launcher(c.kb, c.vb, c.qjl != 0)
+                                          : (c.qjl ? nullptr : dec::packed_launcher_wide(c.kb, c.vb, nh));
         if (!fn) return cudaErrorInvalidValue;
         const cudaError_t e =
             fn(dims, ws, ws.cta_item + c.cta_off, c.n_ctas, c.n_stages, value_half[i], value_c1[i], s, !first);
@@ -254,7 +369,10 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = first ? 0 : 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel, dims, ws, ws.cta_item + c.cta_off);
+        const cudaError_t e =
+            nh == 1   ? cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<1>, dims, ws, ws.cta_item + c.cta_off)
+            : nh == 2 ? cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<2>, dims, ws, ws.cta_item + c.cta_off)
+                      : cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<4>, dims, ws, ws.cta_item + c.cta_off);
         if (e != cudaSuccess) return e;
         ++*n_launched;
         first = false;

@@ -437,6 +437,80 @@ __device__ __forceinline__ float store_hilo(uint32_t *dst, const float (&x)[4], 
     return s;
 }
 
+// ------------------------------------------------------------ head_dim 128 nh
+// A warp-held vector of nh 128-dim blocks: x[j][e] is dimension 128 j + 4 lane + e.
+
+// y = R x with R = binary32(1/sqrt(d)) D H D, d = 128 nh: the Walsh-Hadamard
+// transform of each block, then the butterflies between blocks (widths 128,
+// 256, ...) in registers; block j's signs are words 4 j .. 4 j + 3.
+template <int NH>
+__device__ __forceinline__ void warp_rotate_wide(float (&x)[NH][4], const uint32_t *sign_bits, float inv_sqrt_d,
+                                                 int lane) {
+#pragma unroll
+    for (int j = 0; j < NH; j++) {
+        apply_signs(x[j], sign_bits + 4 * j, lane);
+        warp_wht(x[j], lane);
+    }
+#pragma unroll
+    for (int w = 1; w < NH; w <<= 1) {
+#pragma unroll
+        for (int j = 0; j < NH; j++) {
+            if (j & w) continue;
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const float a = x[j][e], b = x[j + w][e];
+                x[j][e] = a + b;
+                x[j + w][e] = a - b;
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NH; j++) {
+        apply_signs(x[j], sign_bits + 4 * j, lane);
+#pragma unroll
+        for (int e = 0; e < 4; e++) x[j][e] *= inv_sqrt_d;
+    }
+}
+
+// warp_pow2_norm over all blocks.
+template <int NH>
+__device__ __forceinline__ float warp_pow2_norm_wide(const float (&x)[NH][4]) {
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < NH; j++)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(x[j][0]), fabsf(x[j][1])), fmaxf(fabsf(x[j][2]), fabsf(x[j][3]))));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (!(m > 0.f) || !(m < __builtin_huge_valf())) return 1.f;
+    int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+    e = max(-100, min(100, e));
+    return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+// fp16 hi and lo = x - hi of block j as half2 words: hi at hi[64 j + 2 lane, +1],
+// lo at lo[64 j + 2 lane, +1]; returns this lane's sum of hi + lo.
+__device__ __forceinline__ float store_hilo_block(uint32_t *hi_w, uint32_t *lo_w, const float (&x)[4], int j,
+                                                  int lane) {
+    __half hi[4], lo[4];
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        hi[e] = __float2half_rn(x[e]);
+        lo[e] = __float2half_rn(x[e] - __half2float(hi[e]));
+        s += __half2float(hi[e]) + __half2float(lo[e]);
+    }
+    hi_w[64 * j + 2 * lane] = pack_half2(hi[0], hi[1]);
+    hi_w[64 * j + 2 * lane + 1] = pack_half2(hi[2], hi[3]);
+    lo_w[64 * j + 2 * lane] = pack_half2(lo[0], lo[1]);
+    lo_w[64 * j + 2 * lane + 1] = pack_half2(lo[2], lo[3]);
+    return s;
+}
+
+// Named barrier over `threads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ------------------------------------------------------------ dependent launches
 // Let the next kernel of the call start launching CTAs into free SM slots.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -451,6 +525,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // rotation of the packed sum (R is its own inverse), normalisation, store.
 // Called by all threads; returns with all threads synchronised.  `flag` is one
 // int of shared memory.
+//
+// With NH > 1 (head_dim 128 NH) record r of a group holds 128-dim block r mod
+// NH of its query head's sum; the NH records of one warp group (or fp16
+// chunk) carry the same m and l, counted once.
+template <int NH>
+__device__ __forceinline__ void combine_wide(const DecodeDims &dims, const DecodeWorkspace &ws, int layer, int b,
+                                             int h, int warp, int lane);
+
+template <int NH = 1>
 __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const DecodeWorkspace &ws, int layer,
                                                    int b, int h, int *flag) {
     __threadfence();
@@ -462,7 +545,12 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (*flag && warp < dims.gqa) {
+    if constexpr (NH > 1) {
+        if (*flag && warp < dims.gqa) {
+            __threadfence();
+            combine_wide<NH>(dims, ws, layer, b, h, warp, lane);
+        }
+    } else if (*flag && warp < dims.gqa) {
         __threadfence();
         const LayerPlan &lp = ws.layer[layer];
         const int n_items = lp.n_items[h];
@@ -536,6 +624,85 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
         }
     }
     __syncthreads();
+}
+
+template <int NH>
+__device__ __forceinline__ void combine_wide(const DecodeDims &dims, const DecodeWorkspace &ws, int layer, int b,
+                                             int h, int warp, int lane) {
+    static_assert(NH == 2 || NH == 4, "records are read eight at a time, NH | 8");
+    const LayerPlan &lp = ws.layer[layer];
+    const int n_items = lp.n_items[h];
+    const size_t rec_stride = kMaxGqa * kPartStride;
+    float M = kNegInf, L = 0.f;
+    float ar[NH][4], ao[NH][4];
+#pragma unroll
+    for (int j = 0; j < NH; j++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) ar[j][e] = ao[j][e] = 0.f;
+    for (int ii = 0; ii < n_items; ii++) {
+        const int item = lp.item[h][ii];
+        const size_t gr = static_cast<size_t>(item) * dims.B + b;
+        const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
+        const bool rot = ws.items[item].kind == TQ_SEG_PACKED;
+        const float *base = ws.part + static_cast<size_t>(p0) * rec_stride + warp * kPartStride;
+        for (int c0 = 0; c0 < np; c0 += 8) {  // record c0 + u holds block u mod NH
+            float m[8], l[8];
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int c = min(c0 + u, np - 1);
+                const float *rec = base + static_cast<size_t>(c) * rec_stride;
+                m[u] = c0 + u < np ? __ldcg(rec) : kNegInf;
+                l[u] = __ldcg(rec + 1);
+                v[u] = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
+            }
+            float mc = m[0];
+#pragma unroll
+            for (int u = 1; u < 8; u++) mc = fmaxf(mc, m[u]);
+            if (mc > M) {
+                const float sc = ex2(M - mc);
+                L *= sc;
+#pragma unroll
+                for (int j = 0; j < NH; j++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        ar[j][e] *= sc;
+                        ao[j][e] *= sc;
+                    }
+                M = mc;
+            }
+            float a[NH][4];
+#pragma unroll
+            for (int j = 0; j < NH; j++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) a[j][e] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                if (m[u] == kNegInf) continue;
+                const float f = ex2(m[u] - M);
+                if (u % NH == 0) L += f * l[u];
+                a[u % NH][0] += f * v[u].x;
+                a[u % NH][1] += f * v[u].y;
+                a[u % NH][2] += f * v[u].z;
+                a[u % NH][3] += f * v[u].w;
+            }
+#pragma unroll
+            for (int j = 0; j < NH; j++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    ar[j][e] += rot ? a[j][e] : 0.f;
+                    ao[j][e] += rot ? 0.f : a[j][e];
+                }
+        }
+    }
+    warp_rotate_wide<NH>(ar, lp.sign_bits, dims.inv_sqrt_d, lane);
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    const size_t qrow = (static_cast<size_t>(layer) * dims.B + b) * dims.Hq + h * dims.gqa + warp;
+    float4 *dst = reinterpret_cast<float4 *>(ws.out + qrow * (NH * kD));
+#pragma unroll
+    for (int j = 0; j < NH; j++)
+        dst[32 * j + lane] = make_float4((ar[j][0] + ao[j][0]) * inv, (ar[j][1] + ao[j][1]) * inv,
+                                         (ar[j][2] + ao[j][2]) * inv, (ar[j][3] + ao[j][3]) * inv);
 }
 
 // Write one warp's state as a partial record (no cross-warp merge): for each

@@ -7,22 +7,33 @@
 namespace tqk {
 
 // Stage geometry of a packed split-K class, chosen by the bytes a token-head
-// carries.  Light classes (<= 112 B: K3V3 and narrower) do little work per
-// token, so the per-stage costs (the CTA barrier, the copy issue, the cursor)
-// weigh more: they run 256-token stages (512 at <= 64 B: K2V1, K1V2, ...) at 3
-// resident CTAs per SM.  Heavier classes run 128-token stages at 4 CTAs per
-// SM, except with QJL sketches, whose operands take more registers (3 CTAs per
-// SM).  Registers and shared memory of each instantiation are sized for its
-// CTAs per SM.
-__host__ __device__ constexpr int packed_token_bytes(int kb, int vb, bool qjl) {
-    return 16 * (kb + vb) + 8 + (qjl ? 20 : 0);
+// carries.  Light classes (<= 112 B: K3V3 and narrower at head_dim 128) do
+// little work per token, so the per-stage costs (the CTA barrier, the copy
+// issue, the cursor) weigh more: they run 256-token stages (512 at <= 64 B:
+// K2V1, K1V2, ...) at 3 resident CTAs per SM.  Heavier classes run 128-token
+// stages at 4 CTAs per SM, except with QJL sketches, whose operands take more
+// registers (3 CTAs per SM).  Registers and shared memory of each
+// instantiation are sized for its CTAs per SM.
+//
+// nh: 128-dim sub-records per record (head_dim = 128 nh).  With nh > 1 the
+// warps of a CTA split each 32-token block by sub-record, so a warp holds the
+// registers of one 128-dim slice and the class runs at 3 CTAs per SM; token
+// records above 284 B (8-bit keys and values at head_dim 256) take 64-token
+// stages so that two stages still fit.
+__host__ __device__ constexpr int packed_token_bytes(int kb, int vb, bool qjl, int nh = 1) {
+    return 16 * nh * (kb + vb) + 8 + (qjl ? 20 : 0);
 }
-__host__ __device__ constexpr bool packed_light(int kb, int vb, bool qjl) { return packed_token_bytes(kb, vb, qjl) <= 112; }
-__host__ __device__ constexpr int packed_stage_tokens(int kb, int vb, bool qjl) {
-    return packed_token_bytes(kb, vb, qjl) <= 64 ? 512 : (packed_light(kb, vb, qjl) ? 256 : 128);
+__host__ __device__ constexpr bool packed_light(int kb, int vb, bool qjl, int nh = 1) {
+    return packed_token_bytes(kb, vb, qjl, nh) <= 112;
 }
-__host__ __device__ constexpr int packed_ctas_per_sm(int kb, int vb, bool qjl) {
-    return (qjl || packed_light(kb, vb, qjl)) ? 3 : 4;
+__host__ __device__ constexpr int packed_stage_tokens(int kb, int vb, bool qjl, int nh = 1) {
+    return packed_token_bytes(kb, vb, qjl, nh) <= 64    ? 512
+           : packed_light(kb, vb, qjl, nh)              ? 256
+           : packed_token_bytes(kb, vb, qjl, nh) <= 284 ? 128
+                                                        : 64;
+}
+__host__ __device__ constexpr int packed_ctas_per_sm(int kb, int vb, bool qjl, int nh = 1) {
+    return (nh > 1 || qjl || packed_light(kb, vb, qjl, nh)) ? 3 : 4;
 }
 
 }  // namespace tqk

@@ -424,11 +424,11 @@ struct ValueTable {
     float c1;                  // binary32 centroid 1 of a 1-bit codebook (= -centroid 0)
 };
 
-template <int KB, int VB, bool QJL>
+template <int KB, int VB, bool QJL, int NH = 1>
 struct PackedGeom {
-    static constexpr int PT = packed_stage_tokens(KB, VB, QJL);  // tokens per stage, a multiple of 128
-    static constexpr int CTAS = packed_ctas_per_sm(KB, VB, QJL);
-    static constexpr int RK = 16 * KB, RV = 16 * VB;
+    static constexpr int PT = packed_stage_tokens(KB, VB, QJL, NH);  // tokens per stage, a multiple of 64
+    static constexpr int CTAS = packed_ctas_per_sm(KB, VB, QJL, NH);
+    static constexpr int RK = 16 * KB * NH, RV = 16 * VB * NH;  // bytes of a token's key / value record
     static constexpr int offV = PT * RK;
     static constexpr int offKS = offV + PT * RV;
     static constexpr int offVS = offKS + PT * 4;
@@ -436,7 +436,10 @@ struct PackedGeom {
     static constexpr int offQN = offQS + PT * 16;
     static constexpr int stage = QJL ? offQN + PT * 4 : offQS;
     static constexpr int budget = 227 * 1024 / CTAS - 1024;
-    static constexpr int qbytes = 16 + 64;  // flag, barriers (the rotated queries come from the prep kernel)
+    // flag, barriers (the rotated queries come from the prep kernel); NH > 1:
+    // the raw-score exchange, two buffers of a float4 per thread
+    static constexpr int xbytes = NH > 1 ? 2 * kThreads * 16 : 0;
+    static constexpr int qbytes = 16 + 64 + xbytes;
     static constexpr int pair_entries = (VB == 2 || VB == 3) ? (1 << (2 * VB)) : 0;
     // pair table: one column per lane (32 copies) if that still leaves 3
     // stages in flight at the class's CTAs per SM, or as many as 16 copies
@@ -455,7 +458,8 @@ struct PackedGeom {
     static constexpr int qoff = ptab + tab_bytes;             // end of the tables
     static constexpr int flag = qoff;
     static constexpr int bar = flag + 16;                     // one mbarrier per stage buffer
-    static constexpr int smem = bar + 8 * stages;
+    static constexpr int xch = (bar + 8 * stages + 15) & ~15;  // NH > 1: the exchange buffers
+    static constexpr int smem = NH > 1 ? xch + xbytes : bar + 8 * stages;
 };
 
 // Position of a stage in the class's stage sequence (item, batch element,
@@ -506,17 +510,27 @@ struct StageCursor {
 // pipeline that never drains at group boundaries.  Each warp writes one
 // partial per (item, batch) group its CTA touches; the CTA completing a
 // (layer, batch, KV head) merges the partials (finish_and_combine).
-template <int KB, int VB, bool QJL>
-__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
+//
+// NH > 1 (head_dim 128 NH): a token's key (value) record is NH consecutive
+// 128-dim sub-records of 16 KB (16 VB) bytes, the LSB-first code stream cut at
+// dims 128 j.  NH warps share each 32-token block: warp w scores and sums
+// sub-record w mod NH with the 128-dim machinery, the NH warps add their raw
+// Q.K partials through shared memory (a named barrier per block, the same
+// order on every warp, so that all take identical softmax decisions), and
+// each writes its sub-record's partial (record w mod NH of its group).
+template <int KB, int VB, bool QJL, int NH = 1>
+__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
     decode_packed_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item,
                          const long long S, const __grid_constant__ ValueTable vt) {
-    using G = PackedGeom<KB, VB, QJL>;
+    static_assert(NH == 1 || (!QJL && (NH == 2 || NH == 4)), "QJL sketches at head_dim 128 only");
+    using G = PackedGeom<KB, VB, QJL, NH>;
     using KU = KUnpack<KB>;
     using VD = VDec<VB, G::TS>;
     constexpr int NS = G::stages;
     constexpr int kPT = G::PT;
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int sub = NH > 1 ? warp % NH : 0;  // the warp's 128-dim sub-record
     const int gqa = dims.gqa, B = dims.B;
     const long long s_begin = range_begin(blockIdx.x, S, gridDim.x);
     const int n_st = static_cast<int>(range_begin(blockIdx.x + 1, S, gridDim.x) - s_begin);
@@ -527,13 +541,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
     vx.ctab = reinterpret_cast<const unsigned short *>(smem + G::ctab);
     vx.tab = smem_u32(smem + G::ptab) + 4 * (lane & (G::copies - 1));
     if constexpr (VB == 1) {
-        vx.off = 2 * c * G::RV + 4 * (g >> 1);
+        vx.off = 2 * c * G::RV + 16 * VB * sub + 4 * (g >> 1);
         vx.sh = (g & 1) ? 0x7632 : 0x5410;  // PRMT: x's halfword g | y's halfword g
     } else if constexpr (VB == 3) {
-        vx.off = 2 * c * G::RV + 4 * ((3 * g) >> 1);
+        vx.off = 2 * c * G::RV + 16 * VB * sub + 4 * ((3 * g) >> 1);
         vx.sh = (g & 1) * 16;
     } else {
-        vx.off = 2 * c * G::RV + ((2 * VB * g) & ~3);
+        vx.off = 2 * c * G::RV + 16 * VB * sub + ((2 * VB * g) & ~3);
         vx.sh = ((2 * VB * g) & 3) * 8;
     }
     if constexpr (VB >= 5) {
@@ -615,9 +629,11 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
     constexpr float beta = 1.0f / static_cast<float>(1 << KB) - 1.0f;
     const float qk_scale = dims.qk_scale;
     const float c1 = vt.c1;
-    // byte offset of the thread's key window: codes [32c, 32c+32) of token row g
-    const int koff = g * G::RK + 4 * KB * c;
+    // byte offset of the thread's key window: codes [32c, 32c+32) of token row
+    // g's sub-record
+    const int koff = g * G::RK + 16 * KB * sub + 4 * KB * c;
 
+    int xpar = 0;  // exchange buffer of the warp's next block (NH > 1)
     // each warp writes its own partial of the current group; then the group's
     // CTA-level count (and possibly the merge)
     auto flush = [&]() {
@@ -631,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
                 if constexpr (VD::kLinear) return c1 * (2.0f * acc * VDec<1, 7>::unscale(mt, r) - W);
                 else return acc;
             });
-        finish_and_combine(dims, ws, g_layer, g_b, g_head, flag);
+        finish_and_combine<NH>(dims, ws, g_layer, g_b, g_head, flag);
     };
     // a new group: its identity and the B fragments of its rotated queries
     // (column g: head g/2, part g&1), each head divided by a power of two 2^e
@@ -660,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
             tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
             aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
         } else {  // the prep kernel rotated the queries
-            const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 2) + 16 * c;
+            const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (NH * kD / 2) + 64 * sub + 16 * c;
 #pragma unroll
             for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
             gather_b<KU>(q, bq);
@@ -673,6 +689,33 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
         constexpr bool FULL = decltype(full_tag)::value;
         float sc[4];
         const float *kss = reinterpret_cast<const float *>(buf + G::offKS);
+        if constexpr (NH > 1) {
+            // this sub-record's raw Q.K of tokens g, g+8 of both tiles, summed
+            // over the NH sub-records in the order 0..NH-1 by every warp
+            float r[4];
+            qk_raw<KU, KB>(buf + tA * G::RK + koff, buf + (tA + 8) * G::RK + koff, bq, r[0], r[1]);
+            qk_raw<KU, KB>(buf + (tA + 16) * G::RK + koff, buf + (tA + 24) * G::RK + koff, bq, r[2], r[3]);
+            float4 *xb = reinterpret_cast<float4 *>(smem + G::xch) + xpar * kThreads + (warp - sub) * 32 + lane;
+            xb[sub * 32] = make_float4(r[0], r[1], r[2], r[3]);
+            named_barrier(1 + warp / NH, 32 * NH);
+            float4 a = xb[0];
+#pragma unroll
+            for (int j = 1; j < NH; j++) {
+                const float4 o = xb[32 * j];
+                a.x += o.x;
+                a.y += o.y;
+                a.z += o.z;
+                a.w += o.w;
+            }
+            xpar ^= 1;
+            const float raw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int t = 0; t < 2; t++) {
+                const int t0 = tA + 16 * t;
+                sc[2 * t] = kss[t0 + g] * (aq * raw[2 * t] + beta * qsum) * qk_scale;
+                sc[2 * t + 1] = kss[t0 + g + 8] * (aq * raw[2 * t + 1] + beta * qsum) * qk_scale;
+            }
+        } else {
 #pragma unroll
         for (int t = 0; t < 2; t++) {
             const int t0 = tA + 16 * t;
@@ -691,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
             }
             sc[2 * t] = s0 * qk_scale;
             sc[2 * t + 1] = s1 * qk_scale;
+        }
         }
         const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
         bool okv[4];
@@ -745,7 +789,8 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
         const int n = min(kPT, cc.n_tokens - cc.st * kPT);
         new_group = cc.advance(ws.items, B, k + 1 < n_st);
         // warp w takes tokens [32 w, 32 w + 32) of every 128 of the stage
-        for (int tA = warp * 32; tA < n; tA += 32 * kDecodeWarps) {
+        // (NH > 1: block w / NH of every 128 / NH, sub-record w mod NH)
+        for (int tA = (warp / NH) * 32; tA < n; tA += 32 * (kDecodeWarps / NH)) {
             if (tA + 32 <= n) tiles(buf, tA, n, std::true_type{});
             else tiles(buf, tA, n, std::false_type{});
         }
@@ -756,15 +801,15 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL))
     flush();
 }
 
-template <int KB, int VB, bool QJL>
+template <int KB, int VB, bool QJL, int NH = 1>
 cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, const int *cta_item, int n_ctas,
                           long long n_stages, const unsigned short *value_half, float value_c1, cudaStream_t s,
                           bool pdl) {
-    using G = PackedGeom<KB, VB, QJL>;
+    using G = PackedGeom<KB, VB, QJL, NH>;
     static bool configured = false;
     if (!configured) {
         if (G::smem > 48 * 1024) {
-            const cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<KB, VB, QJL>,
+            const cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<KB, VB, QJL, NH>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, G::smem);
             if (e != cudaSuccess) return e;
         }
@@ -783,7 +828,7 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL>, dims, ws, cta_item, n_stages, vt);
+    return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL, NH>, dims, ws, cta_item, n_stages, vt);
 }
 
 }  // namespace dec
@@ -811,6 +856,33 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, con
             case 15: return dec::launch_packed<KB, 7, true>;                                                   \
             case 16: return dec::launch_packed<KB, 8, false>;                                                  \
             case 17: return dec::launch_packed<KB, 8, true>;                                                   \
+            default: return nullptr;                                                                           \
+        }                                                                                                      \
+    }                                                                                                          \
+    }
+
+// head_dim 128 nh (nh = 2, 4; no QJL): one translation unit per key width
+// instantiates every value width.
+#define TQ_INSTANTIATE_WIDE_KB(KB)                                                                            \
+    namespace tqk {                                                                                            \
+    PackedLauncher packed_launcher_wide_kb##KB(int vb, int nh) {                                               \
+        switch (vb * 8 + nh) {                                                                                 \
+            case 10: return dec::launch_packed<KB, 1, false, 2>;                                               \
+            case 12: return dec::launch_packed<KB, 1, false, 4>;                                               \
+            case 18: return dec::launch_packed<KB, 2, false, 2>;                                               \
+            case 20: return dec::launch_packed<KB, 2, false, 4>;                                               \
+            case 26: return dec::launch_packed<KB, 3, false, 2>;                                               \
+            case 28: return dec::launch_packed<KB, 3, false, 4>;                                               \
+            case 34: return dec::launch_packed<KB, 4, false, 2>;                                               \
+            case 36: return dec::launch_packed<KB, 4, false, 4>;                                               \
+            case 42: return dec::launch_packed<KB, 5, false, 2>;                                               \
+            case 44: return dec::launch_packed<KB, 5, false, 4>;                                               \
+            case 50: return dec::launch_packed<KB, 6, false, 2>;                                               \
+            case 52: return dec::launch_packed<KB, 6, false, 4>;                                               \
+            case 58: return dec::launch_packed<KB, 7, false, 2>;                                               \
+            case 60: return dec::launch_packed<KB, 7, false, 4>;                                               \
+            case 66: return dec::launch_packed<KB, 8, false, 2>;                                               \
+            case 68: return dec::launch_packed<KB, 8, false, 4>;                                               \
             default: return nullptr;                                                                           \
         }                                                                                                      \
     }                                                                                                          \

@@ -544,15 +544,22 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     if (!layers || n_layers < 1 || B < 1 || H < 1 || H > TQ_MAX_HEADS || Hq < H || Hq % H) return TQ_ERR_ARG;
     if (!pow2(d) || d < 16 || d > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     const int gqa = Hq / H;
-    const bool generic = d != kD;  // other head dims: the generic kernel (GQA up to 4, no QJL, SRHT)
-    if (!generic && gqa != 1 && gqa != 2 && gqa != 4) return TQ_ERR_UNSUPPORTED;
+    // head_dim 256 and 512 with GQA 1, 2 or 4 run the split-K kernels on 128-dim
+    // sub-records; other head dims the generic kernel (GQA up to 4); neither
+    // takes QJL sketches, dense rotations or attention-mass outputs
+    const bool mma_gqa = gqa == 1 || gqa == 2 || gqa == 4;
+    const bool wide = (d == 2 * kD || d == 4 * kD) && mma_gqa;
+    const bool generic = d != kD && !wide;
+    const bool other_dim = d != kD;
+    if (!generic && !mma_gqa) return TQ_ERR_UNSUPPORTED;
     if (generic && gqa > kMaxGqa) return TQ_ERR_UNSUPPORTED;
+    const int nh = wide ? d / kD : 1;
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
         if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
         if (lv.qjl_estimator != TQ_QJL_UNBIASED && lv.qjl_estimator != TQ_QJL_SIGN_PAIR) return TQ_ERR_ARG;
         if (check_ptrs && lv.rot.dense && !aligned16(lv.rot.dense)) return TQ_ERR_ALIGN;
-        if (generic && lv.rot.dense) return TQ_ERR_UNSUPPORTED;
+        if (other_dim && lv.rot.dense) return TQ_ERR_UNSUPPORTED;
         for (int s = 0; s < lv.n_segments; ++s) {
             const tq_segment &sg = lv.seg[s];
             const tq_segment_layout &L = sg.layout;
@@ -562,7 +569,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
             if (st != TQ_OK) return st;
             if (L.batch != B || L.n_heads != H || L.head_dim != d) return TQ_ERR_ARG;
             if (sg.n_tokens < 0 || sg.n_tokens > L.capacity) return TQ_ERR_SIZE;
-            if (generic && sg.attn_mass) return TQ_ERR_UNSUPPORTED;
+            if (other_dim && sg.attn_mass) return TQ_ERR_UNSUPPORTED;
             if (sg.kind == TQ_SEG_PACKED) {
                 if (L.capacity % 16) return TQ_ERR_ALIGN;
                 if (!fits_u32(&L)) return TQ_ERR_UNSUPPORTED;
@@ -587,7 +594,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                     }
                 }
                 if ((q || qv) && (jl != kJl || L.jl_dim != kJl)) return TQ_ERR_UNSUPPORTED;
-                if (generic && (q || qv || L.value_law != TQ_VALUE_LAW_GAUSS)) return TQ_ERR_UNSUPPORTED;
+                if (other_dim && (q || qv || L.value_law != TQ_VALUE_LAW_GAUSS)) return TQ_ERR_UNSUPPORTED;
             } else {
                 if (check_ptrs) {
                     if (!sg.k16 || !sg.v16) return TQ_ERR_ARG;
@@ -730,13 +737,13 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         ClassLaunch &c = P.classes.back();
         c.item_hi = static_cast<int>(i) + 1;
         if (w.kind == TQ_SEG_PACKED) {
-            const int pt = packed_stage_tokens(w.kb, w.vb, w.qjl != 0);
+            const int pt = packed_stage_tokens(w.kb, w.vb, w.qjl != 0, nh);
             w.n_stages = (w.n_tokens + pt - 1) / pt;
             w.stage_begin = stages;
             stages += static_cast<long long>(B) * w.n_stages;
             c.n_stages = stages;
-            c.n_ctas = static_cast<int>(std::min<long long>(stages, static_cast<long long>(sms) *
-                                                                         packed_ctas_per_sm(w.kb, w.vb, w.qjl != 0)));
+            c.n_ctas = static_cast<int>(std::min<long long>(
+                stages, static_cast<long long>(sms) * packed_ctas_per_sm(w.kb, w.vb, w.qjl != 0, nh)));
         } else {
             w.cta_begin = static_cast<int>(cta);
             cta += static_cast<long long>(B) * w.n_chunks;
@@ -764,7 +771,8 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
                                             dec_cta_of_stage(gs, c.n_stages, c.n_ctas) + 1);
                 np = kDecodeWarps * portions;
             } else {
-                portions = np = w.n_chunks;  // one CTA-merged record per chunk
+                portions = w.n_chunks;  // one CTA-merged record per chunk and 128-dim block
+                np = w.n_chunks * nh;
             }
             P.grp_part[i * B + b] = static_cast<int>(part);
             P.grp_nparts[i * B + b] = np;
@@ -853,6 +861,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.inv_sqrt_d = inv_sqrt_f32(d);
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     D.wait_polls = g_wait_polls.load();
+    D.nh = nh;
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
     // offset 0: the error flag (kept in its own 256 bytes so that it has a
     // fixed place), then the work items

@@ -136,7 +136,7 @@ struct alignas(16) WorkItem {
 };
 
 struct LayerPlan {
-    uint32_t sign_bits[kD / 32];
+    uint32_t sign_bits[TQ_MAX_HEAD_DIM / 32];  // the SRHT's sign bits (head_dim / 32 words used)
     const float *dense;                    // dense rotation (d x d, y = Q x) or nullptr: the SRHT
     int has_qjl;
     int has_vqjl;                          // some packed item of the layer sketches its values
@@ -152,6 +152,7 @@ struct DecodeDims {
     float qk_scale;      // log2(e) / sqrt(d)
     float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
     int wait_polls;      // polls of a split-K CTA's wait for its own copies before it gives up
+    int nh;              // 128-dim sub-records per head vector (head_dim / 128: 1, 2 or 4)
 };
 
 // Workspace: [WorkItem x n][LayerPlan x L][group tables][counters][q prep]
@@ -212,6 +213,15 @@ PackedLauncher packed_launcher_kb5(int vb, bool qjl);
 PackedLauncher packed_launcher_kb6(int vb, bool qjl);
 PackedLauncher packed_launcher_kb7(int vb, bool qjl);
 PackedLauncher packed_launcher_kb8(int vb, bool qjl);
+// head_dim 128 nh (nh = 2, 4), no QJL: one launcher table per key width
+PackedLauncher packed_launcher_wide_kb1(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb2(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb3(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb4(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb5(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb6(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb7(int vb, int nh);
+PackedLauncher packed_launcher_wide_kb8(int vb, int nh);
 
 // ----------------------------------------------------------------- other head dims
 // Compression, dequantization and decode attention for head dimensions other

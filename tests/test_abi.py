@@ -170,6 +170,21 @@ def test_host_side_argument_errors(tq):
     assert e.value.status == -3
     with pytest.raises(tq.TQError):
         tq.tq_age_tiers(10, [5, 3])
+    # head_dim 256 / 512: GQA 1-4 plan (1, 2, 4 on the split-K kernels, 3 on
+    # the generic one); QJL keys and attention-mass outputs stay at 128
+    for d in (256, 512):
+        rotd = tq.tq_make_rotation(d, 42)
+        Pd = tq.PackedSegment(tq.make_layout(1, 2, d, 48, 3, 3), device="cpu", n_tokens=40)
+        for hq in (2, 4, 6, 8):
+            assert tq.tq_decode_workspace_size([tq.layer_view(rotd, [Pd])], 1, 2, hq, d) > 0
+        Pq = tq.PackedSegment(tq.make_layout(1, 2, d, 48, 2, 3, qjl=[1, 0]), device="cpu", n_tokens=40)
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_decode_workspace_size([tq.layer_view(rotd, [Pq])], 1, 2, 8, d)
+        assert e.value.status == -2
+        Pd.attn_mass = torch.zeros(1, 2, 48)
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_decode_workspace_size([tq.layer_view(rotd, [Pd])], 1, 2, 8, d)
+        assert e.value.status == -2
 
 
 def test_requantize_argument_errors(tq):

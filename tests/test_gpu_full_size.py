@@ -14,6 +14,8 @@ The oracle cannot redo a whole workload in seconds, so it checks samples:
                with the oracle's fp64 attention over that group's packed and
                fp16 segments copied back from the device.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -43,7 +45,7 @@ def _u16(t):
     return t.contiguous().cpu().numpy().view(np.uint16)
 
 
-def _head_segments(si_list, b, h, buf_kv=None):
+def _head_segments(si_list, b, h, buf_kv=None, d=128):
     """Oracle segments (batch 1, one KV head) holding (b, h) of each device segment."""
     out = []
     for si in si_list:
@@ -52,18 +54,18 @@ def _head_segments(si_list, b, h, buf_kv=None):
                 k, v = buf_kv
             else:
                 k, v = si.seg.k[b, h, :si.n], si.seg.v[b, h, :si.n]
-            o = O.Fp16Segment(1, 1, 128, max(si.n, 1), n_tokens=si.n)
-            o.k16[:si.n * 128] = _u16(k).ravel()
-            o.v16[:si.n * 128] = _u16(v).ravel()
+            o = O.Fp16Segment(1, 1, d, max(si.n, 1), n_tokens=si.n)
+            o.k16[:si.n * d] = _u16(k).ravel()
+            o.v16[:si.n * d] = _u16(v).ravel()
             out.append(o)
             continue
         g = si.seg
         L = g.layout
         H, cap = L.n_heads, L.capacity
-        rk = [128 * L.kbits[i] // 8 for i in range(H)]
-        rv = [128 * L.vbits[i] // 8 for i in range(H)]
+        rk = [d * L.kbits[i] // 8 for i in range(H)]
+        rv = [d * L.vbits[i] // 8 for i in range(H)]
         qj = [L.qjl[i] for i in range(H)]
-        o = O.PackedSegment(1, 1, 128, cap, [L.kbits[h]], [L.vbits[h]], [qj[h]], jl=128, n_tokens=si.n)
+        o = O.PackedSegment(1, 1, d, cap, [L.kbits[h]], [L.vbits[h]], [qj[h]], jl=128, n_tokens=si.n)
         k0 = b * cap * sum(rk) + cap * sum(rk[:h])
         v0 = b * cap * sum(rv) + cap * sum(rv[:h])
         o.kcodes[:] = g.kcodes[k0:k0 + cap * rk[h]].cpu().numpy()
@@ -87,7 +89,7 @@ def _check_decode(out, q, groups, segs_of, sign_of, S):
         osegs = segs_of(l, b, h)
         ref = O.decode_attention(osegs, qn[l, b:b + 1, 4 * h:4 * h + 4], sign_of(l), 1, S=S)
         g = got[l, b, 4 * h:4 * h + 4]
-        r = ref.reshape(4, 128)
+        r = ref.reshape(4, g.shape[-1])
         rel = (np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)).max()
         worst = max(worst, rel)
     assert worst <= ATTN_TOL, worst
@@ -104,10 +106,11 @@ def _check_records(si, b, pos, kin, vin, sign, S):
     kb = [L.kbits[i] for i in range(H)]
     vb = [L.vbits[i] for i in range(H)]
     qj = [L.qjl[i] for i in range(H)]
-    o = O.PackedSegment(1, H, 128, _cap16(n), kb, vb, qj, jl=128)
+    d = kin.shape[-1]
+    o = O.PackedSegment(1, H, d, _cap16(n), kb, vb, qj, jl=128)
     O.compress(o, kin[None].view(np.uint16), vin[None].view(np.uint16), sign, S)
-    rk = [16 * x for x in kb]
-    rv = [16 * x for x in vb]
+    rk = [d * x // 8 for x in kb]
+    rv = [d * x // 8 for x in vb]
     pos = np.asarray(pos, np.int64)
     near = 0
     for h in range(H):
@@ -157,20 +160,25 @@ def _groups(L, B, H):
     return sorted(g)
 
 
-@pytest.mark.parametrize("name,batch,context", [
-    ("w1", None, None),
-    ("w3", None, None),
-    ("w4", None, None),
-    ("w5", 32, 65536),
-    ("w5", 1, 4096),
-    ("w5", 8, 16384),
-    ("w5", 32, 4096),
-    ("w3", 8, None),   # the age tiers at 1.05M cached tokens per layer
-    ("w4", 32, None),  # per-head widths and QJL at 1.05M cached tokens per layer
+@pytest.mark.parametrize("name,batch,context,head_dim", [
+    ("w1", None, None, None),
+    ("w3", None, None, None),
+    ("w4", None, None, None),
+    ("w5", 32, 65536, None),
+    ("w5", 1, 4096, None),
+    ("w5", 8, 16384, None),
+    ("w5", 32, 4096, None),
+    ("w3", 8, None, None),   # the age tiers at 1.05M cached tokens per layer
+    ("w4", 32, None, None),  # per-head widths and QJL at 1.05M cached tokens per layer
+    ("w5", 8, 16384, 256),   # the w5 shape at head_dim 256, as the benchmark runs it
+    ("w3", None, None, 256),  # the age tiers and fp16 segments at head_dim 256
 ])
-def test_static_workload_full_size(lib, name, batch, context):
+def test_static_workload_full_size(lib, name, batch, context, head_dim):
     T, MC = lib
     w = W.WORKLOADS[name]
+    if head_dim:
+        w = dataclasses.replace(w, head_dim=head_dim)
+    d = w.head_dim
     seed = 1000 + int(name[1:])
     B = batch or w.batch
     L = w.layers
@@ -192,7 +200,7 @@ def test_static_workload_full_size(lib, name, batch, context):
     # compression of sampled positions, every packed segment of the checked layers
     near = total = 0
     for l in sorted(check_layers):
-        sign = O.signs(128, W.ROTATION_SEED + l)
+        sign = O.signs(d, W.ROTATION_SEED + l)
         for b in check_b:
             K, V = samples[l][b]
             for i, si in enumerate(m.layers[l]):
@@ -205,13 +213,13 @@ def test_static_workload_full_size(lib, name, batch, context):
                 kin = K[:, tp].numpy()
                 vin = V[:, tp].numpy()
                 near += _check_records(si, b, pos, kin, vin, sign, S)
-                total += len(pos) * m.H * 128
+                total += len(pos) * m.H * d
     assert near <= 1e-5 * total
 
     # decode outputs of sampled groups
     _check_decode(m.out, q, _groups(L, m.B, m.H),
-                  lambda l, b, h: _head_segments(m.layers[l], b, h),
-                  lambda l: O.signs(128, W.ROTATION_SEED + l), S)
+                  lambda l, b, h: _head_segments(m.layers[l], b, h, d=d),
+                  lambda l: O.signs(d, W.ROTATION_SEED + l), S)
     del m, samples
     torch.cuda.empty_cache()
 

@@ -177,6 +177,16 @@ ATTN_CASES = [
     (512, 1, 1, 2, 8, [("fp16", 20), ("packed", 150, [2, 6], [5, 2])]),
     (1024, 1, 1, 1, 4, [("packed", 60, [4], [4]), ("fp16", 18)]),
     (64, 1, 1, 4, 12, [("packed", 0, [3] * 4, [3] * 4), ("fp16", 0)]),  # GQA 3, empty cache
+    # head_dim 256 / 512 on the split-K kernels (GQA 1, 2, 4): every key and
+    # value width, several stages per group, ragged tails, multi-chunk fp16
+    (256, 1, 3, 8, 8, [("packed", 333, [1, 2, 3, 4, 5, 6, 7, 8], [8, 7, 6, 5, 4, 3, 2, 1]), ("fp16", 150)]),
+    (256, 2, 2, 4, 8, [("fp16", 64), ("packed", 1000, [2, 3, 4, 5], [5, 4, 3, 2]),
+                       ("packed", 77, [8, 8, 1, 1], [1, 8, 1, 8])]),
+    (512, 1, 2, 2, 8, [("packed", 640, [3, 5], [4, 3]), ("fp16", 70)]),
+    (512, 1, 1, 4, 4, [("packed", 129, [1, 2, 7, 8], [8, 7, 2, 1])]),
+    (256, 2, 1, 2, 8, [("packed", 0, [3, 3], [3, 3]), ("fp16", 5)]),  # fp16 tokens only
+    (256, 1, 1, 2, 8, [("packed", 0, [3, 3], [3, 3]), ("fp16", 0)]),  # empty cache
+    (256, 1, 1, 2, 6, [("packed", 100, [3, 3], [3, 3]), ("fp16", 9)]),  # GQA 3: the generic kernel
 ]
 
 
