@@ -134,13 +134,15 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
 
 
-def traffic_for(workload: str, packed_bytes: int):
+def traffic_for(workload: str, packed_bytes: int, head_dim: int = 128):
     """DRAM bytes per launch of the packed kernel from an ncu capture taken on
     the current kernel sources (null otherwise): the captured bytes when the
     capture had this launch's size, else the captured traffic per algorithmic
     byte times this launch's algorithmic bytes (captures of the large
-    workloads are taken at a smaller batch)."""
-    path = os.path.join(ROOT, "profiles", f"decode_packed_{workload}_traffic.json")
+    workloads are taken at a smaller batch).  Captures at another head_dim
+    carry a _d<head_dim> suffix."""
+    suffix = "" if head_dim == 128 else f"_d{head_dim}"
+    path = os.path.join(ROOT, "profiles", f"decode_packed_{workload}{suffix}_traffic.json")
     if not os.path.exists(path):
         return None
     t = json.load(open(path))
@@ -265,7 +267,7 @@ def result_line(args, world, m, t, e2e, comp, config, workload):
                      "achieved": round(achieved, 1),
                      "timing": "CUDA events around the packed launches of K further steps",
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic_for(workload, int(np.mean(t["packed_bytes"]))),
+                     "traffic": traffic_for(workload, int(np.mean(t["packed_bytes"])), m.d),
                      "bytes_per_launch": int(np.mean(t["packed_bytes"])),
                      "avg_launch_ms": round(kern_avg_ms, 5)},
         "compress": {"value": round(comp["mtok"], 1), "unit": "Mtok/s", "ms_per_layer": round(comp["ms"], 4),

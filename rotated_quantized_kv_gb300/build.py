@@ -21,7 +21,8 @@ LIB = os.path.join(PKG, "_lib", "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_SOURCES = ["tq_compress.cu", "tq_compress_dense.cu", "tq_decode.cu", "tq_mass.cu", "tq_static.cu",
-                "tq_generic.cu", "tq_compress_rows.cu"] + [f"tq_decode_kb{k}.cu" for k in range(1, 9)] + [
+                "tq_generic.cu", "tq_compress_rows.cu", "tq_compress_rows_nh2.cu", "tq_compress_rows_nh4.cu"] + [
+                f"tq_decode_kb{k}.cu" for k in range(1, 9)] + [
                 f"tq_decode_wide_kb{k}.cu" for k in range(1, 9)]
 HOST_SOURCES = ["tq_host.cpp"]
 
@@ -36,7 +37,7 @@ def nvcc() -> str:
 def _sources():
     return [os.path.join(CSRC, s) for s in CUDA_SOURCES + HOST_SOURCES] + [
         os.path.join(CSRC, h) for h in ("tq_internal.h", "tq_decode_common.cuh", "tq_decode_packed.cuh",
-                                        "tq_mass.h", "tq_decode_geometry.h")] + [
+                                        "tq_mass.h", "tq_decode_geometry.h", "tq_compress_rows.cuh")] + [
         os.path.join(ROOT, "include", "tq.h")]
 
 

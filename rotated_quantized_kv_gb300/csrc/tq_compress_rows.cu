@@ -1,373 +1,14 @@
-// tq_compress_rows.cu -- compression of 128-dimension key or value vectors
-// with one thread per vector, for launches without QJL sketches.
-//
-// Method and format: as compress_kernel (tq_compress.cu): "turboquant-mlx"
-// (TurboQuant-MLX v2.0 README), "Walsh-Hadamard Rotation" (SRHT D H D / sqrt(d));
-// "TurboMOQ", "Architecture" (keys: symmetric grid, values: Gaussian Lloyd-Max
-// codebook, 1-8 bits per head) and "Project Structure" (bit packing).  Every
-// rounding step is the format's IEEE binary32 operation, so the codes are the
-// same bits as the oracle's.
-//
-// Design (GB300): a thread holds its whole vector in 64 float2 registers, pair
-// m = (coordinate m, coordinate m + 64).  Butterfly stages h = 1..32 pair
-// registers m and m + h, so one packed f32x2 add and one packed f32x2
-// subtract (Blackwell's add/sub.rn.f32x2: two independent IEEE operations)
-// do two butterflies each; stage 64 pairs the two halves of each register.
-// The output scale, the key grid arithmetic and the value quotient y / sigma
-// are packed f32x2 operations too, and the pairwise sum of squares runs as
-// two index-order trees of 64 (packed) joined at the root.  No exchanges
-// between lanes.  A warp compresses 32 consecutive tokens of one (batch,
-// head): their fp16 rows are staged in shared memory with 16-byte cp.async
-// copies (chunk c of row r at 16 (c ^ (r & 7)), so that the eight rows one
-// 16-byte load phase reads fall in eight bank groups), double-buffered per
-// warp, and each thread stores its record with 16-byte stores (16 b bytes per
-// vector).  Kernels are specialised by the width of the heads they carry
-// (keys and values launched separately), so each holds one quantizer.
-#include <algorithm>
-
-#include <cuda_fp16.h>
-
-#include "tq_internal.h"
+// tq_compress_rows.cu -- the one-thread-per-slice compressor at head_dim 128
+// and the dispatch over the slice counts (tq_compress_rows.cuh).
+#include "tq_compress_rows.cuh"
 
 namespace tqk {
-namespace {
-
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kRowBytes = 256;            // 128 fp16 coordinates
-constexpr int kWarpBuf = 32 * kRowBytes;  // one staged block of 32 rows
-
-// Packed binary32 pairs: two independent IEEE operations per instruction.
-// A packed product that feeds a packed sum can still be fused into one packed
-// multiply-add by the compiler (measured: the explicit rounding modifier does
-// not prevent it), so no product below ever feeds a sum directly: every chain
-// is add/sub only, or multiply then multiply / fma / compare.
-#define TQ_F32X2_BINARY(NAME, OP)                                                              \
-    __device__ __forceinline__ float2 NAME(float2 a, float2 b) {                               \
-        float2 r;                                                                              \
-        asm("{.reg .b64 ra, rb, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n" OP \
-            " rr, ra, rb;\n mov.b64 {%0, %1}, rr;}"                                          \
-            : "=f"(r.x), "=f"(r.y)                                                             \
-            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                         \
-        return r;                                                                              \
-    }
-TQ_F32X2_BINARY(fadd2, " add.rn.f32x2")
-TQ_F32X2_BINARY(fsub2, " sub.rn.f32x2")
-TQ_F32X2_BINARY(fmul2, " mul.rn.f32x2")
-TQ_F32X2_BINARY(fadd2_rm, " add.rm.f32x2")
-#undef TQ_F32X2_BINARY
-
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 r;
-    asm("{.reg .b64 ra, rb, rc, rr;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-        " fma.rn.f32x2 rr, ra, rb, rc;\n mov.b64 {%0, %1}, rr;}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
-// max(a, b, c) in one instruction (order-free: the absmax needs no fixed order)
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
-}
-
-// Stage the fp16 rows of block `blk` ((b, head of the list, 32-token block),
-// token block fastest) into this warp's buffer.
-__device__ __forceinline__ void stage_rows(const RowsParams &p, int n_tblk, int blk, uint8_t *buf, int lane) {
-    const int tb = blk % n_tblk, rest = blk / n_tblk;
-    const int h = p.head[rest % p.n_heads], b = rest / p.n_heads;
-    const int t0 = tb * 32, nt = min(32, p.T - t0);
-    const uint16_t *src = p.X + b * p.sb + h * p.sh + static_cast<int64_t>(t0) * p.st;
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const int idx = lane + 32 * i, r = idx >> 4, c = idx & 15;
-        if (r < nt) cp_async16(buf + r * kRowBytes + 16 * (c ^ (r & 7)), src + static_cast<int64_t>(r) * p.st + 8 * c);
-    }
-}
-
-// Code i (0..127) at bits [B i, B i + B) of the record's 4 B words.
-template <int B>
-__device__ __forceinline__ void put(uint32_t (&w)[4 * B], int i, uint32_t k) {
-    const int bit = i * B, wi = bit >> 5, sh = bit & 31;
-    w[wi] += k << sh;  // codes never overlap: an add (one shift-and-add instruction) is the or
-    if (sh + B > 32) w[wi + 1] += k >> (32 - sh);
-}
-
-// Key codes are put as kKeyLo + code (a float bit pattern, see the key
-// quantizer); word j of the record then holds the sum of the kKeyLo parts of
-// its codes on top of the codes, modulo 2^32.  kKeyLo + code carries nothing
-// out of its low 10 bits (code < 512), so the parts shifted out of a word
-// (sh + B > 32, a right shift by less than B <= 8) are kKeyLo >> s exactly.
-constexpr uint32_t kKeyLo = 0x4B000000u + 512u;
-template <int B>
-__host__ __device__ constexpr uint32_t key_offset_word(int j) {
-    uint32_t c = 0;
-    for (int i = 0; i < 128; i++) {
-        const int bit = i * B, wi = bit >> 5, sh = bit & 31;
-        if (wi == j) c += kKeyLo << sh;
-        if (sh + B > 32 && wi + 1 == j) c += kKeyLo >> (32 - sh);
-    }
-    return c;
-}
-
-template <int BITS, bool VAL>
-__global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid_constant__ RowsParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + kWarps * 2 * kWarpBuf);  // [64]
-    float *out_pair = reinterpret_cast<float *>(in_mask + 64);                       // [64][2]
-    float *thr = out_pair + kD;                                                      // [255]
-    uint2 *vtab = reinterpret_cast<uint2 *>(thr + 256);                             // [1024] (values, <= 3 bits)
-    for (int i = threadIdx.x; i < 64; i += kThreads) in_mask[i] = p.in_mask[i];
-    for (int i = threadIdx.x; i < kD; i += kThreads) out_pair[i] = p.out_scale[(i >> 1) + 64 * (i & 1)];
-    for (int i = threadIdx.x; i < 255; i += kThreads) thr[i] = p.thr[i];
-    if constexpr (VAL && BITS <= 3)
-        for (int i = threadIdx.x; i < kRowsBuckets; i += kThreads) vtab[i] = make_uint2(p.bucket[i].t, p.bucket[i].k);
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *bufs = smem + warp * 2 * kWarpBuf;
-    const int n_tblk = (p.T + 31) / 32;
-    const int n_blk = n_tblk * p.n_heads * p.B;
-    const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
-    if (gw < n_blk) stage_rows(p, n_tblk, gw, bufs, lane);
-    asm volatile("cp.async.commit_group;\n" ::);
-
-    for (int blk = gw, it = 0; blk < n_blk; blk += nw, it++) {
-        const int next = blk + nw;
-        if (next < n_blk) stage_rows(p, n_tblk, next, bufs + ((it + 1) & 1) * kWarpBuf, lane);
-        asm volatile("cp.async.commit_group;\n" ::);
-        asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-        __syncwarp();
-        const int tb = blk % n_tblk, rest = blk / n_tblk;
-        const int h = p.head[rest % p.n_heads], b = rest / p.n_heads;
-        const int t = tb * 32 + lane;
-        const uint8_t *row = bufs + (it & 1) * kWarpBuf + lane * kRowBytes;
-
-        // ---- load, input sign flip on the fp16 bits, widen: chunks c and
-        // c + 8 (coordinates 8c.. and 64 + 8c..) are permuted into half2 pairs
-        // (m, m + 64) that widen straight into the register pairs
-        float2 a[64];
-#pragma unroll
-        for (int c = 0; c < 8; c++) {
-            const uint4 v0 = *reinterpret_cast<const uint4 *>(row + 16 * (c ^ (lane & 7)));
-            const uint4 v1 = *reinterpret_cast<const uint4 *>(row + 16 * ((c + 8) ^ (lane & 7)));
-            const uint4 m0 = *reinterpret_cast<const uint4 *>(in_mask + 4 * c);
-            const uint4 m1 = *reinterpret_cast<const uint4 *>(in_mask + 4 * (c + 8));
-            const uint32_t w0[4] = {v0.x ^ m0.x, v0.y ^ m0.y, v0.z ^ m0.z, v0.w ^ m0.w};
-            const uint32_t w1[4] = {v1.x ^ m1.x, v1.y ^ m1.y, v1.z ^ m1.z, v1.w ^ m1.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int i = 8 * c + 2 * e;  // pairs (i, i + 64) and (i + 1, i + 65)
-                const uint32_t lo = prmt(w0[e], w1[e], 0x5410u), hi = prmt(w0[e], w1[e], 0x7632u);
-                a[i] = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
-                a[i + 1] = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-            }
-        }
-        __syncwarp();  // every lane has read its row: the buffer may be restaged
-
-        // ---- butterflies h = 1..32 on register pairs (packed), then h = 64
-#pragma unroll
-        for (int hh = 1; hh < 64; hh <<= 1) {
-#pragma unroll
-            for (int m = 0; m < 64; m++) {
-                if ((m & hh) == 0) {
-                    const float2 u = a[m], v = a[m + hh];
-                    a[m] = fadd2(u, v);
-                    a[m + hh] = fsub2(u, v);
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < 64; m++) {
-            const float u = a[m].x, v = a[m].y;
-            a[m].x = __fadd_rn(u, v);
-            a[m].y = __fsub_rn(u, v);
-        }
-        // output sign flip and binary32(1/sqrt(d)): one rounded multiply each
-        // (out_pair[m] = the scales of coordinates m and m + 64)
-#pragma unroll
-        for (int m = 0; m < 64; m += 2) {
-            const float4 sc = *reinterpret_cast<const float4 *>(out_pair + 2 * m);
-            a[m] = fmul2(a[m], make_float2(sc.x, sc.y));
-            a[m + 1] = fmul2(a[m + 1], make_float2(sc.z, sc.w));
-        }
-
-        uint32_t w[4 * BITS];
-#pragma unroll
-        for (int j = 0; j < 4 * BITS; j++) w[j] = 0u;
-        float scale;
-        if constexpr (!VAL) {
-            // ---- keys: m = max |y|, v = y * binary32(1/m), u = round(v + 1) 2^(b-1),
-            // code = clamp(floor(u), 0, 2^b - 1)
-            float mx = 0.0f;
-#pragma unroll
-            for (int m = 0; m < 64; m++) mx = fmax3(mx, fabsf(a[m].x), fabsf(a[m].y));
-            scale = mx;
-            const float r = mx > 0.0f ? __frcp_rn(mx) : 0.0f;
-            constexpr float hc = static_cast<float>(1 << (BITS - 1));
-            // v = y r lies in [-1, 1]: r = binary32(1/m) is within 2^-24 of 1/m
-            // and |y| <= m, so |y r| <= 1 + 2^-24 rounds to at most 1.  Hence
-            // u = round(v + 1) 2^(b-1) >= 0 and only the top clamp can act (at
-            // v = 1).  floor(u): the round-down of u + 2^23 + 512 has the exponent
-            // of 2^23, so its bit pattern is kLo + floor(u).
-            constexpr float kMagic = 8388608.0f + 512.0f;
-            constexpr uint32_t kHi = kKeyLo + (1u << BITS) - 1u;
-#pragma unroll
-            for (int m = 0; m < 64; m++) {
-                const float2 v = fmul2(a[m], make_float2(r, r));
-                // fma(v, 2^(b-1), 2^(b-1)) is round(v + 1) 2^(b-1): scaling by a
-                // power of two commutes with the rounding
-                const float2 u = ffma2(v, make_float2(hc, hc), make_float2(hc, hc));
-                const float2 f = fadd2_rm(u, make_float2(kMagic, kMagic));
-                // kLo + code, placed as is: the words take off the kLo parts below
-                put<BITS>(w, m, min(__float_as_uint(f.x), kHi));
-                put<BITS>(w, m + 64, min(__float_as_uint(f.y), kHi));
-            }
-#pragma unroll
-            for (int j = 0; j < 4 * BITS; j++) w[j] -= key_offset_word<BITS>(j);
-        } else {
-            // ---- values: sigma = sqrt(pairwise-tree sum of y^2 in index order / d),
-            // u = y * binary32(1/sigma), code = #{k : thr_k < u}
-            // first level scalar: the compiler fuses a packed multiply into a
-            // packed add (one rounding instead of two), which the scalar _rn
-            // intrinsics rule out; the later levels are additions only
-            float2 s[32];
-#pragma unroll
-            for (int j = 0; j < 32; j++) {
-                s[j].x = __fadd_rn(__fmul_rn(a[2 * j].x, a[2 * j].x), __fmul_rn(a[2 * j + 1].x, a[2 * j + 1].x));
-                s[j].y = __fadd_rn(__fmul_rn(a[2 * j].y, a[2 * j].y), __fmul_rn(a[2 * j + 1].y, a[2 * j + 1].y));
-            }
-#pragma unroll
-            for (int len = 32; len > 1; len >>= 1) {
-#pragma unroll
-                for (int j = 0; j < len / 2; j++) s[j] = fadd2(s[2 * j], s[2 * j + 1]);
-            }
-            const float tot = __fadd_rn(s[0].x, s[0].y);
-            const float sigma = __fsqrt_rn(__fmul_rn(tot, 1.0f / kD));  // / d exact (a power of two)
-            scale = sigma;
-            const float r = sigma > 0.0f ? __frcp_rn(sigma) : 0.0f;
-            constexpr int NT = (1 << BITS) - 1;
-            if constexpr (BITS <= 3) {
-                // #{k : thr_k < u} from the bucket of u's top ten bits (sign,
-                // exponent, one mantissa bit): every u in a bucket exceeds the
-                // same k_base thresholds, and at most one threshold t_c lies in
-                // the bucket (the host checks), so the count is k_base + [t_c < u]
-                const uint32_t tab = static_cast<uint32_t>(__cvta_generic_to_shared(vtab));
-#pragma unroll
-                for (int m = 0; m < 64; m++) {
-                    const float2 u = fmul2(a[m], make_float2(r, r));
-                    const uint2 e0 = lds64(tab + ((__float_as_uint(u.x) >> 22) << 3));
-                    const uint2 e1 = lds64(tab + ((__float_as_uint(u.y) >> 22) << 3));
-                    put<BITS>(w, m, e0.y + (__uint_as_float(e0.x) < u.x ? 1u : 0u));
-                    put<BITS>(w, m + 64, e1.y + (__uint_as_float(e1.x) < u.y ? 1u : 0u));
-                }
-            } else if constexpr (BITS == 4) {
-                float th[NT];
-#pragma unroll
-                for (int j = 0; j < NT; j++) th[j] = thr[j];
-#pragma unroll
-                for (int m = 0; m < 64; m++) {
-                    const float2 u = fmul2(a[m], make_float2(r, r));
-                    uint32_t k0 = 0, k1 = 0;
-#pragma unroll
-                    for (int st = 1 << (BITS - 1); st >= 1; st >>= 1) {
-                        // threshold k + st - 1 for the current prefix k: a select
-                        // tree over the candidates of this level
-                        float t0 = th[st - 1], t1 = th[st - 1];
-#pragma unroll
-                        for (int c = 2 * st; c < (1 << BITS); c += 2 * st) {
-                            t0 = (k0 >= static_cast<uint32_t>(c)) ? th[c + st - 1] : t0;
-                            t1 = (k1 >= static_cast<uint32_t>(c)) ? th[c + st - 1] : t1;
-                        }
-                        k0 += (t0 < u.x) ? st : 0;
-                        k1 += (t1 < u.y) ? st : 0;
-                    }
-                    put<BITS>(w, m, k0);
-                    put<BITS>(w, m + 64, k1);
-                }
-            } else {
-#pragma unroll
-                for (int m = 0; m < 64; m++) {
-                    const float2 u = fmul2(a[m], make_float2(r, r));
-                    uint32_t k0 = 0, k1 = 0;
-#pragma unroll
-                    for (int st = 1 << (BITS - 1); st >= 1; st >>= 1) {
-                        if (thr[k0 + st - 1] < u.x) k0 += st;
-                        if (thr[k1 + st - 1] < u.y) k1 += st;
-                    }
-                    put<BITS>(w, m, k0);
-                    put<BITS>(w, m + 64, k1);
-                }
-            }
-        }
-        if (t < p.T) {
-            const int pos = p.t_begin + t;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.codes + static_cast<size_t>(b) * p.block + p.off[h] +
-                                                   static_cast<size_t>(pos) * (16 * BITS));
-#pragma unroll
-            for (int j = 0; j < BITS; j++) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-            p.scale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = scale;
-        }
-    }
-}
-
-template <int BITS, bool VAL>
-cudaError_t rows_launch(const RowsParams &p, cudaStream_t s) {
-    constexpr size_t smem = kWarps * 2 * kWarpBuf + 64 * 4 + kD * 4 + 256 * 4 + ((VAL && BITS <= 3) ? kRowsBuckets * 8 : 0);
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(compress_rows_kernel<BITS, VAL>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    int sms = 148, dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long blocks = (static_cast<long long>((p.T + 31) / 32) * p.n_heads * p.B + kWarps - 1) / kWarps;
-    const long long grid = std::min<long long>(blocks, static_cast<long long>(sms) * 3);
-    compress_rows_kernel<BITS, VAL><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
-    return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t launch_compress_rows(const RowsParams &p, int bits, bool values, cudaStream_t s) {
-    switch (bits * 2 + (values ? 1 : 0)) {
-        case 2: return rows_launch<1, false>(p, s);
-        case 3: return rows_launch<1, true>(p, s);
-        case 4: return rows_launch<2, false>(p, s);
-        case 5: return rows_launch<2, true>(p, s);
-        case 6: return rows_launch<3, false>(p, s);
-        case 7: return rows_launch<3, true>(p, s);
-        case 8: return rows_launch<4, false>(p, s);
-        case 9: return rows_launch<4, true>(p, s);
-        case 10: return rows_launch<5, false>(p, s);
-        case 11: return rows_launch<5, true>(p, s);
-        case 12: return rows_launch<6, false>(p, s);
-        case 13: return rows_launch<6, true>(p, s);
-        case 14: return rows_launch<7, false>(p, s);
-        case 15: return rows_launch<7, true>(p, s);
-        case 16: return rows_launch<8, false>(p, s);
-        case 17: return rows_launch<8, true>(p, s);
+    switch (p.nh) {
+        case 1: return rows_dispatch<1>(p, bits, values, s);
+        case 2: return launch_compress_rows_nh2(p, bits, values, s);
+        case 4: return launch_compress_rows_nh4(p, bits, values, s);
         default: return cudaErrorInvalidValue;
     }
 }

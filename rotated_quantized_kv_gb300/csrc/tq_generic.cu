@@ -60,18 +60,30 @@ __device__ __forceinline__ int coord(int lt, int e) {
     return Team<D>::STAGE ? lt + 32 * e : lt * Team<D>::E + e;
 }
 
+// The signs a team lane applies, as bit masks over its E slots: in_neg bit e
+// for coordinate lt * E + e (the input), out_neg bit e for coord<D>(lt, e).
+template <int D>
+__device__ __forceinline__ void lane_sign_masks(const uint32_t *sb, int lt, uint32_t &in_neg, uint32_t &out_neg) {
+    in_neg = out_neg = 0u;
+#pragma unroll
+    for (int e = 0; e < Team<D>::E; e++) {
+        in_neg |= static_cast<uint32_t>(neg_coord(sb, lt * Team<D>::E + e)) << e;
+        out_neg |= static_cast<uint32_t>(neg_coord(sb, coord<D>(lt, e))) << e;
+    }
+}
+
 // y = c * D H D x in the format's binary32 order: input sign flip (exact),
 // butterfly widths h = 1, 2, ..., D/2 ascending with each pair (i, i + h) ->
 // (a + b, a - b), output sign flip (exact), one rounded multiply by c.  On
 // entry a[e] is coordinate lt * E + e; on return slot e holds coord<D>(lt, e).
 // stage: D floats of this warp's shared memory (d >= 256).
 template <int D>
-__device__ __forceinline__ void rotate_exact(float (&a)[Team<D>::E], int lt, const uint32_t *sb, float c,
-                                             float *stage) {
+__device__ __forceinline__ void rotate_exact(float (&a)[Team<D>::E], int lt, uint32_t in_neg, uint32_t out_neg,
+                                             float c, float *stage) {
     constexpr int E = Team<D>::E;
 #pragma unroll
     for (int e = 0; e < E; e++)
-        if (neg_coord(sb, lt * E + e)) a[e] = -a[e];
+        if ((in_neg >> e) & 1u) a[e] = -a[e];
 #pragma unroll
     for (int h = 1; h < E; h <<= 1) {
 #pragma unroll
@@ -128,40 +140,44 @@ __device__ __forceinline__ void rotate_exact(float (&a)[Team<D>::E], int lt, con
         }
     }
 #pragma unroll
-    for (int e = 0; e < E; e++) a[e] = __fmul_rn(c, neg_coord(sb, coord<D>(lt, e)) ? -a[e] : a[e]);
+    for (int e = 0; e < E; e++) a[e] = __fmul_rn(c, ((out_neg >> e) & 1u) ? -a[e] : a[e]);
 }
 
 // sum_i y_i^2 as a pairwise binary tree in index order, each square and sum
-// rounded once; every lane of the team returns the root.
+// rounded once; every lane of the team returns the root.  The lane's squares
+// of E consecutive indices lt * E + e (for d >= 256 the rotated vector is
+// strided, so the squares go through the warp's stage first) sum in-lane for
+// the blocks up to E, then across lanes (partner lt ^ x: the two add the same
+// pair, and IEEE addition commutes).
 template <int D>
-__device__ __forceinline__ float tree_sum_squares(const float (&a)[Team<D>::E]) {
+__device__ __forceinline__ float tree_sum_squares(const float (&a)[Team<D>::E], int lt, float *stage) {
     constexpr int E = Team<D>::E, T = Team<D>::T;
     float p[E];
+    if constexpr (!Team<D>::STAGE) {
 #pragma unroll
-    for (int e = 0; e < E; e++) p[e] = __fmul_rn(a[e], a[e]);
-    if constexpr (!Team<D>::STAGE) {  // contiguous blocks of E, then blocks across the team
+        for (int e = 0; e < E; e++) p[e] = __fmul_rn(a[e], a[e]);
+    } else {
 #pragma unroll
-        for (int len = E; len > 1; len >>= 1) {
+        for (int j = 0; j < E; j++) stage[lt + 32 * j] = __fmul_rn(a[j], a[j]);
+        __syncwarp();
 #pragma unroll
-            for (int j = 0; j < len / 2; j++) p[j] = __fadd_rn(p[2 * j], p[2 * j + 1]);
+        for (int e = 0; e < E; e += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(stage + lt * E + e);
+            p[e] = v.x;
+            p[e + 1] = v.y;
+            p[e + 2] = v.z;
+            p[e + 3] = v.w;
         }
-        float s = p[0];
-#pragma unroll
-        for (int x = 1; x < T; x <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, x));
-        return s;
-    } else {  // blocks of up to 32 indices are across lanes, larger ones in-lane over j
-#pragma unroll
-        for (int x = 1; x < 32; x <<= 1) {
-#pragma unroll
-            for (int j = 0; j < E; j++) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xffffffffu, p[j], x));
-        }
-#pragma unroll
-        for (int len = E; len > 1; len >>= 1) {
-#pragma unroll
-            for (int j = 0; j < len / 2; j++) p[j] = __fadd_rn(p[2 * j], p[2 * j + 1]);
-        }
-        return p[0];
     }
+#pragma unroll
+    for (int len = E; len > 1; len >>= 1) {
+#pragma unroll
+        for (int j = 0; j < len / 2; j++) p[j] = __fadd_rn(p[2 * j], p[2 * j + 1]);
+    }
+    float s = p[0];
+#pragma unroll
+    for (int x = 1; x < T; x <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, x));
+    return s;
 }
 
 // Bits [32 w, 32 w + 32) of a record from its code bytes (LSB-first stream).
@@ -176,20 +192,14 @@ __device__ __forceinline__ uint32_t record_word(const uint8_t *cw, int bits, int
     return x;
 }
 
-// Store the d*bits/8-byte record built from the code bytes, with the widest
-// stores its size allows (16-byte stores for d >= 128).
+// Store the d*bits/8-byte record built from the code bytes: each team lane
+// assembles whole 32-bit words (coalesced 4-byte stores); records of d = 16 at
+// an odd width in 2-byte halves.
 template <int D>
 __device__ __forceinline__ void store_record(const uint8_t *cw, int bits, uint8_t *dst, int lt) {
     constexpr int T = Team<D>::T;
     const int rk = D * bits / 8;
-    if (rk % 16 == 0) {
-        for (int c = lt; c < rk / 16; c += T)
-            reinterpret_cast<uint4 *>(dst)[c] = make_uint4(record_word(cw, bits, D, 4 * c), record_word(cw, bits, D, 4 * c + 1),
-                                                           record_word(cw, bits, D, 4 * c + 2), record_word(cw, bits, D, 4 * c + 3));
-    } else if (rk % 8 == 0) {
-        for (int c = lt; c < rk / 8; c += T)
-            reinterpret_cast<uint2 *>(dst)[c] = make_uint2(record_word(cw, bits, D, 2 * c), record_word(cw, bits, D, 2 * c + 1));
-    } else if (rk % 4 == 0) {
+    if (rk % 4 == 0) {
         for (int c = lt; c < rk / 4; c += T) reinterpret_cast<uint32_t *>(dst)[c] = record_word(cw, bits, D, c);
     } else {  // d = 16 and an odd width: 2-byte halves
         for (int c = lt; c < rk / 2; c += T) {
@@ -227,8 +237,9 @@ __device__ __forceinline__ void load_coords(const uint16_t *src, float (&a)[E]) 
 }
 
 // ------------------------------------------------------------------ compress
-// Vectors (K and V of every (b, h, t)) in the order kv, b, h, t (t fastest);
-// warp teams take consecutive vectors.
+// Rows (kv, b, h) of T vectors: blockIdx.y strides over the 2 B H rows (kv
+// slowest), blockIdx.x over each row's tokens; warp teams take consecutive
+// tokens of a row.
 template <int D>
 __global__ void __launch_bounds__(kGenThreads) gen_compress_kernel(const __grid_constant__ GenCompressParams p) {
     using TM = Team<D>;
@@ -240,19 +251,16 @@ __global__ void __launch_bounds__(kGenThreads) gen_compress_kernel(const __grid_
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int v = lane / T, lt = lane % T;
-    const long long NV = 2LL * p.B * p.H * p.T;
-    const long long nwarps = static_cast<long long>(gridDim.x) * kGenWarps;
-    for (long long base = (static_cast<long long>(blockIdx.x) * kGenWarps + warp) * VPW; base < NV;
-         base += nwarps * VPW) {
-        const long long f = base + v;
-        const bool valid = f < NV;
-        long long r = valid ? f : 0;
-        const int t = static_cast<int>(r % p.T);
-        r /= p.T;
-        const int h = static_cast<int>(r % p.H);
-        r /= p.H;
-        const int b = static_cast<int>(r % p.B);
-        const int kv = static_cast<int>(r / p.B);
+    uint32_t in_neg, out_neg;
+    lane_sign_masks<D>(p.sign_bits, lt, in_neg, out_neg);
+    const int rows = 2 * p.B * p.H;
+    for (int row = blockIdx.y; row < rows; row += gridDim.y)
+    for (int t0 = (blockIdx.x * kGenWarps + warp) * VPW; t0 < p.T; t0 += gridDim.x * kGenWarps * VPW) {
+        const int t = t0 + v;
+        const bool valid = t < p.T;
+        const int h = row % p.H;
+        const int b = (row / p.H) % p.B;
+        const int kv = row / (p.H * p.B);
         float a[E];
         if (valid) {
             load_coords<E>((kv ? p.V : p.K) + b * p.sb + h * p.sh + static_cast<int64_t>(t) * p.st + lt * E, a);
@@ -260,14 +268,14 @@ __global__ void __launch_bounds__(kGenThreads) gen_compress_kernel(const __grid_
 #pragma unroll
             for (int e = 0; e < E; e++) a[e] = 0.0f;
         }
-        rotate_exact<D>(a, lt, p.sign_bits, p.inv_sqrt_d, stage + (TM::STAGE ? warp * D : 0));
+        rotate_exact<D>(a, lt, in_neg, out_neg, p.inv_sqrt_d, stage + (TM::STAGE ? warp * D : 0));
         // both per-vector statistics for every team, so that the exchanges stay uniform
         float m = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; e++) m = fmaxf(m, fabsf(a[e]));
 #pragma unroll
         for (int x = 1; x < T; x <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, x));
-        const float S = tree_sum_squares<D>(a);
+        const float S = tree_sum_squares<D>(a, lt, stage + (TM::STAGE ? warp * D : 0));
         const int bits = kv ? p.vbits[h] : p.kbits[h];
         uint8_t *cw = codes[warp] + v * D;
         float scale;
@@ -328,6 +336,8 @@ __global__ void __launch_bounds__(kGenThreads) gen_dequant_kernel(const __grid_c
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int v = lane / T, lt = lane % T;
+    uint32_t in_neg, out_neg;
+    lane_sign_masks<D>(p.sign_bits, lt, in_neg, out_neg);
     const long long NV = 2LL * p.B * p.H * p.n;
     const long long nwarps = static_cast<long long>(gridDim.x) * kGenWarps;
     for (long long base = (static_cast<long long>(blockIdx.x) * kGenWarps + warp) * VPW; base < NV;
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kGenThreads) gen_dequant_kernel(const __grid_c
         }
         float *orig_out = kv ? p.v_orig : p.k_orig;
         if (p.k_orig || p.v_orig) {  // uniform across the warp: every team rotates
-            rotate_exact<D>(a, lt, p.sign_bits, p.inv_sqrt_d, stage + (TM::STAGE ? warp * D : 0));
+            rotate_exact<D>(a, lt, in_neg, out_neg, p.inv_sqrt_d, stage + (TM::STAGE ? warp * D : 0));
             if (valid && orig_out) {
 #pragma unroll
                 for (int e = 0; e < E; e++) orig_out[row + coord<D>(lt, e)] = a[e];
@@ -662,12 +672,15 @@ __global__ void __launch_bounds__(kGenThreads) gen_decode_kernel(const __grid_co
 
 template <int D>
 cudaError_t gen_compress_launch(const GenCompressParams &p, cudaStream_t s) {
-    const long long vecs = 2LL * p.B * p.H * p.T;
+    const int rows = 2 * p.B * p.H;
     const long long per_block = static_cast<long long>(kGenWarps) * Team<D>::VPW;
     int sms = 148, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long blocks = std::min<long long>((vecs + per_block - 1) / per_block, static_cast<long long>(sms) * 8);
-    gen_compress_kernel<D><<<static_cast<unsigned>(blocks), kGenThreads, 0, s>>>(p);
+    // about 8 resident blocks per SM in all, each block a strided share of one row
+    const long long want_x = std::max<long long>(1, static_cast<long long>(sms) * 8 / std::max(rows, 1));
+    const long long bx = std::min<long long>((p.T + per_block - 1) / per_block, want_x);
+    const int by = std::min(rows, 65535);
+    gen_compress_kernel<D><<<dim3(static_cast<unsigned>(bx), static_cast<unsigned>(by)), kGenThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

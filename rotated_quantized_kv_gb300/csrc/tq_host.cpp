@@ -359,13 +359,16 @@ bool value_buckets(const float *thr, int nt, RowsParams::Bucket *out) {
     return true;
 }
 
-// Launches of the one-thread-per-vector kernels for a compression without
-// sketches: the keys of each distinct key width, then the values of each
-// distinct value width (one launch each; uniform layouts take two).  Returns
-// cudaErrorNotSupported, before launching anything, if a value width's bucket
-// table does not separate its thresholds (the caller then takes the
-// four-lanes-per-vector kernel).
-cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout, cudaStream_t s) {
+// Launches of the one-thread-per-slice kernels for a compression without
+// sketches at head_dim d = 128, 256 or 512 (sign_bits: the rotation's d bits;
+// c supplies the pointers, strides and widths): the keys of each distinct key
+// width, then the values of each distinct value width (one launch each;
+// uniform layouts take two).  Returns cudaErrorNotSupported, before launching
+// anything, if a value width's bucket table does not separate its thresholds
+// (the caller then takes another kernel).
+cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout, const uint32_t *sign_bits, int d,
+                        cudaStream_t s) {
+    if (d != kD && d != 2 * kD && d != 4 * kD) return cudaErrorNotSupported;
     for (int h = 0; h < c.H; ++h) {
         if (c.vbits[h] > 3) continue;
         const FittedCodebook &cb = fit(c.vbits[h], layout->value_law);
@@ -384,13 +387,14 @@ cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout
     p.T = c.T;
     p.t_begin = c.t_begin;
     p.capacity = c.capacity;
-    for (int i = 0; i < kD / 2; ++i) {
-        const uint32_t s0 = (c.sign_bits[(2 * i) >> 5] >> ((2 * i) & 31)) & 1u;
-        const uint32_t s1 = (c.sign_bits[(2 * i + 1) >> 5] >> ((2 * i + 1) & 31)) & 1u;
+    p.nh = d / kD;
+    const float c_d = inv_sqrt_f32(d);
+    for (int i = 0; i < d / 2; ++i) {
+        const uint32_t s0 = (sign_bits[(2 * i) >> 5] >> ((2 * i) & 31)) & 1u;
+        const uint32_t s1 = (sign_bits[(2 * i + 1) >> 5] >> ((2 * i + 1) & 31)) & 1u;
         p.in_mask[i] = (s0 << 15) | (s1 << 31);
     }
-    for (int i = 0; i < kD; ++i)
-        p.out_scale[i] = ((c.sign_bits[i >> 5] >> (i & 31)) & 1u) ? -c.inv_sqrt_d : c.inv_sqrt_d;
+    for (int i = 0; i < d; ++i) p.out_scale[i] = ((sign_bits[i >> 5] >> (i & 31)) & 1u) ? -c_d : c_d;
     for (int values = 0; values < 2; ++values) {
         p.X = values ? c.V : c.K;
         p.codes = values ? c.vcodes : c.kcodes;
@@ -428,6 +432,34 @@ tq_status compress_other_dims(const tq_segment_layout *layout, const tq_rotation
     if (stride_t < d || stride_h < 0 || stride_b < 0 || (stride_t % 8) || (stride_h % 8) || (stride_b % 8))
         return TQ_ERR_ALIGN;
     if (n_tokens == 0) return TQ_OK;
+    if (d == 2 * kD || d == 4 * kD) {  // one thread per 128-dim slice
+        CompressParams c;
+        std::memset(&c, 0, sizeof(c));
+        c.K = static_cast<const uint16_t *>(K);
+        c.V = static_cast<const uint16_t *>(V);
+        c.sb = stride_b;
+        c.sh = stride_h;
+        c.st = stride_t;
+        c.B = layout->batch;
+        c.H = layout->n_heads;
+        c.T = n_tokens;
+        c.t_begin = t_begin;
+        c.capacity = layout->capacity;
+        c.kcodes = static_cast<uint8_t *>(out->kcodes);
+        c.vcodes = static_cast<uint8_t *>(out->vcodes);
+        c.kscale = out->kscale;
+        c.vscale = out->vscale;
+        c.kblock = o.kblock;
+        c.vblock = o.vblock;
+        for (int h = 0; h < c.H; ++h) {
+            c.koff[h] = o.koff[h];
+            c.voff[h] = o.voff[h];
+            c.kbits[h] = layout->kbits[h];
+            c.vbits[h] = layout->vbits[h];
+        }
+        const cudaError_t e = launch_rows(c, layout, rot->sign_bits, d, s);
+        if (e != cudaErrorNotSupported) return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    }
     GenCompressParams p;
     std::memset(&p, 0, sizeof(p));
     p.K = static_cast<const uint16_t *>(K);
@@ -1118,7 +1150,7 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
         return e == cudaSuccess ? TQ_OK : cuda_fail(e);
     }
     if (o.nq == 0 && o.nv == 0) {  // no sketches: one thread per vector, a launch per width
-        const cudaError_t e = launch_rows(p, layout, static_cast<cudaStream_t>(stream));
+        const cudaError_t e = launch_rows(p, layout, rot->sign_bits, kD, static_cast<cudaStream_t>(stream));
         if (e != cudaErrorNotSupported) return e == cudaSuccess ? TQ_OK : cuda_fail(e);
     }
     const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));

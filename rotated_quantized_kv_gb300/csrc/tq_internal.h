@@ -55,9 +55,11 @@ struct CompressParams {
 };
 
 constexpr int kRowsBuckets = 1024;  // buckets of a value quotient: sign, exponent, one mantissa bit
+constexpr int kRowsMaxD = 512;      // head_dim up to which the one-thread-per-slice compressor runs
 
-// Keys or values of the heads of one bit width, one thread per vector
-// (tq_compress_rows.cu): launches of an SRHT compression without QJL sketches.
+// Keys or values of the heads of one bit width, one thread per 128-dim slice
+// (tq_compress_rows*.cu): launches of an SRHT compression without QJL sketches
+// at head_dim 128, 256 or 512.
 struct RowsParams {
     const uint16_t *X;           // K or V, element (b, h, t, i) at b*sb + h*sh + t*st + i
     int64_t sb, sh, st;
@@ -68,14 +70,17 @@ struct RowsParams {
     uint32_t off[kMaxH];         // per-head byte offset inside a batch block
     int n_heads;                 // heads of this launch (all of one width)
     uint8_t head[kMaxH];         // their indices
-    uint32_t in_mask[kD / 2];    // word i: the input sign bits of coordinates 2i (bit 15), 2i + 1 (bit 31)
-    float out_scale[kD];         // coordinate i: -binary32(1/sqrt(d)) if D_i = -1, else +
+    int nh;                      // 128-dim slices per vector (head_dim / 128: 1, 2 or 4)
+    uint32_t in_mask[kRowsMaxD / 2];  // word i: the input sign bits of coordinates 2i (bit 15), 2i + 1 (bit 31)
+    float out_scale[kRowsMaxD];  // coordinate i: -binary32(1/sqrt(d)) if D_i = -1, else +
     float thr[255];              // values: the width's thresholds, ascending
     // values of <= 3 bits: bucket b = (bit pattern of u) >> 22 holds k_base and
     // the bucket's one threshold t_c (+inf if none) as bits: code = k_base + [t_c < u]
     struct Bucket { uint32_t t, k; } bucket[kRowsBuckets];
 };
 cudaError_t launch_compress_rows(const RowsParams &p, int bits, bool values, cudaStream_t s);
+cudaError_t launch_compress_rows_nh2(const RowsParams &p, int bits, bool values, cudaStream_t s);
+cudaError_t launch_compress_rows_nh4(const RowsParams &p, int bits, bool values, cudaStream_t s);
 
 // ----------------------------------------------------------------- dequantize
 struct DequantParams {
