@@ -13,7 +13,9 @@
 // reduction (absmax, the pairwise sum of squares) finishes with exchanges in the
 // same fixed order.  A CTA of 8 warps runs two independent groups: warps 0-3
 // compress key vectors, warps 4-7 value vectors, 32 vectors per pass.  Each
-// group loops over 32-token blocks of (batch, head) on its own (persistent
+// group loops over 32-token blocks of (batch, head) on its own, over the heads
+// the launch selects (the host sends heads without sketches to the
+// one-thread-per-vector kernels) (persistent
 // CTAs, three per SM), double-buffers its rows with coalesced 16-byte cp.async
 // copies and synchronises on its own named barrier, so the lighter key path
 // never waits for the value path.  Shared rows are laid out as four 80-byte
@@ -159,75 +161,129 @@ __device__ __forceinline__ uint32_t search_smem(float u, const float *t) {
     return k;
 }
 
-// The projection matrix S (jl x d binary32) in shared memory: row j holds
-// 32 16-byte chunks, quarter qq's chunk i4 (coordinates 32 qq + 4 i4 ..) at
-// chunk 8 qq + (i4 ^ qq), so that the four quarters a warp reads together
-// (same row and i4, one per lane q) fall in four different bank groups.
-constexpr int kSketchSmem = kJl * kD * 4;
+// ------------------------------------------------------------------ QJL sketch
+// Residuals of a 32-token block in shared memory, [32 rows][kRStride] binary32:
+// 16 floats of pad per row put the eight rows a quarter-warp reads with one
+// 16-byte load (rows g and g + 1 of a lane pair, four chunks each) in eight
+// different bank groups.
+constexpr int kRStride = kD + 16;
+constexpr int kRSmem = kTok * kRStride * 4;
 
-__device__ __forceinline__ float4 lds128(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void stage_sketch_matrix(const float *S, uint8_t *dst) {
-    for (int idx = threadIdx.x; idx < kJl * kD / 4; idx += blockDim.x) {
-        const int j = idx >> 5, c = idx & 31, qq = c >> 3, i4 = c & 7;
-        reinterpret_cast<float4 *>(dst)[j * 32 + qq * 8 + (i4 ^ qq)] = __ldg(reinterpret_cast<const float4 *>(S) + idx);
-    }
-}
-
-// Sketch of a residual held by four lanes (this lane's coordinates [32 q,
-// 32 q + 32) in r): p_j = sum_i S[j][i] r_i in binary32 (any order: the only
-// decision is the sign); bit j = (p_j >= 0); rho = ||r||_2.  Each lane forms
-// the partial sum over its 32 coordinates, the four lanes add them, and lane q
-// keeps the signs of projections [32 q, 32 q + 32).  S_sm: the shared address
-// of the staged matrix.
-__device__ __forceinline__ void qjl_sketch(uint32_t S_sm, const float (&y)[kQ], int q, bool store, uint8_t *rec,
-                                           float *norm) {
-    {
-        float ss = 0.0f;
+// This lane's quarter of a residual into row `row` of the block buffer, and
+// the residual's squared norm (binary32, any order) for rho = ||r||_2.
+__device__ __forceinline__ float residual_to_smem(float *R, const float (&y)[kQ], int row, int q) {
+    float ss = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kQ; i++) ss = fmaf(y[i], y[i], ss);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        uint32_t mine = 0;
+    for (int i = 0; i < kQ; i++) ss = fmaf(y[i], y[i], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    float *dst = R + row * kRStride + kQ * q;
+#pragma unroll
+    for (int i = 0; i < kQ; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(y[i], y[i + 1], y[i + 2], y[i + 3]);
+    return ss;
+}
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// x = hi + lo to 2^-22 relative: hi = tf32(x), lo = tf32(x - hi) (x - hi is exact)
+__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float f4at(const float4 &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+// Signs of P = R S^T for the block's 32 residual rows, projections [32 wq,
+// 32 wq + 32) on this warp (wq: the warp within its group), on the tensor
+// cores: mma.m16n8k8 in tf32 with every operand split as hi + lo and the
+// products hi hi + hi lo + lo hi accumulated in binary32.  Each dropped or
+// rounded part is below 2^-22 of |S_ji r_i|, so |P - S r| stays below
+// 7.2e-7 ||S_j|| ||r|| besides the accumulation rounding (the plain binary32
+// sum has the same kind of bound); only the sign of P is kept, bit j = (P_j >=
+// 0).  Within a pair of k-steps lane c takes dims 16 kp + 4 c .. + 3 of both
+// operands (any dim order is the same sum).  Row t's 16-byte record at rec0 +
+// 16 t receives word wq, for t < n_valid.
+__device__ __noinline__ void block_sketch(const float *R, const float *S, int wq, int lane, uint8_t *rec0,
+                                          int n_valid) {
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t word[2][2] = {{0u, 0u}, {0u, 0u}};  // [m-tile][row g | g + 8]
 #pragma unroll 1
-        for (int jc = 0; jc < 4; jc++) {  // projections 32 jc .. 32 jc + 31
-            uint32_t word = 0;
-#pragma unroll 4  // eight projections' shared loads in flight
-            for (int jj = 0; jj < 32; jj += 2) {  // two projections, four partial sums each
-                const uint32_t S0 = S_sm + static_cast<uint32_t>((32 * jc + jj) * kD * 4 + q * kQ * 4);
-                float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int nh = 0; nh < 2; nh++) {  // n-tiles 2 nh, 2 nh + 1
+        float acc[2][2][4];
 #pragma unroll
-                for (int i4 = 0; i4 < kQ / 4; i4++) {
-                    const uint32_t o = static_cast<uint32_t>((i4 ^ q) * 16);
-                    const float4 s = lds128(S0 + o), t = lds128(S0 + kD * 4 + o);
-                    const int e = i4 & 3;
-                    a0[e] = fmaf(s.x, y[4 * i4], a0[e]);
-                    a0[e] = fmaf(s.y, y[4 * i4 + 1], a0[e]);
-                    a0[e] = fmaf(s.z, y[4 * i4 + 2], a0[e]);
-                    a0[e] = fmaf(s.w, y[4 * i4 + 3], a0[e]);
-                    a1[e] = fmaf(t.x, y[4 * i4], a1[e]);
-                    a1[e] = fmaf(t.y, y[4 * i4 + 1], a1[e]);
-                    a1[e] = fmaf(t.z, y[4 * i4 + 2], a1[e]);
-                    a1[e] = fmaf(t.w, y[4 * i4 + 3], a1[e]);
+        for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) acc[mt][nt][e] = 0.0f;
+#pragma unroll 2
+        for (int kp = 0; kp < kD / 16; kp++) {
+            float4 ra[2][2], sb[2];
+#pragma unroll
+            for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+                for (int hf = 0; hf < 2; hf++)
+                    ra[mt][hf] = *reinterpret_cast<const float4 *>(R + (16 * mt + 8 * hf + g) * kRStride + 16 * kp + 4 * c);
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+                sb[nt] = __ldg(reinterpret_cast<const float4 *>(S + (32 * wq + 8 * (2 * nh + nt) + g) * kD + 16 * kp + 4 * c));
+#pragma unroll
+            for (int ks = 0; ks < 2; ks++) {
+                uint32_t ah[2][4], al[2][4], bh[2][2], bl[2][2];
+#pragma unroll
+                for (int mt = 0; mt < 2; mt++) {
+                    // a0: (row g, k c), a1: (row g + 8, k c), a2: (row g, k c + 4), a3: (row g + 8, k c + 4)
+                    tf32_split(f4at(ra[mt][0], 2 * ks), ah[mt][0], al[mt][0]);
+                    tf32_split(f4at(ra[mt][1], 2 * ks), ah[mt][1], al[mt][1]);
+                    tf32_split(f4at(ra[mt][0], 2 * ks + 1), ah[mt][2], al[mt][2]);
+                    tf32_split(f4at(ra[mt][1], 2 * ks + 1), ah[mt][3], al[mt][3]);
                 }
-                float p0 = (a0[0] + a0[1]) + (a0[2] + a0[3]), p1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
-                p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-                p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-                p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-                word |= ((p0 >= 0.0f ? 1u : 0u) << jj) | ((p1 >= 0.0f ? 1u : 0u) << (jj + 1));
+#pragma unroll
+                for (int nt = 0; nt < 2; nt++) {  // b0: (k c, n g), b1: (k c + 4, n g)
+                    tf32_split(f4at(sb[nt], 2 * ks), bh[nt][0], bl[nt][0]);
+                    tf32_split(f4at(sb[nt], 2 * ks + 1), bh[nt][1], bl[nt][1]);
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+                    for (int nt = 0; nt < 2; nt++) {
+                        mma_tf32(acc[mt][nt], al[mt], bh[nt][0], bh[nt][1]);
+                        mma_tf32(acc[mt][nt], ah[mt], bl[nt][0], bl[nt][1]);
+                        mma_tf32(acc[mt][nt], ah[mt], bh[nt][0], bh[nt][1]);
+                    }
             }
-            if (jc == q) mine = word;
         }
-        if (store) {
-            reinterpret_cast<uint32_t *>(rec)[q] = mine;
-            if (q == 0) *norm = sqrtf(ss);
-        }
+        // accumulator e of (mt, nt): row g (+8 for e >= 2), projection 8 (2 nh + nt) + 2 c + (e & 1)
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    word[mt][e >> 1] |= (acc[mt][nt][e] >= 0.0f ? 1u : 0u) << (8 * (2 * nh + nt) + 2 * c + (e & 1));
     }
+    // the four lanes of a quad hold disjoint bits of the same rows
+#pragma unroll
+    for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+            word[mt][hf] |= __shfl_xor_sync(0xffffffffu, word[mt][hf], 1);
+            word[mt][hf] |= __shfl_xor_sync(0xffffffffu, word[mt][hf], 2);
+        }
+    const int mt = c >> 1, hf = c & 1, row = 16 * mt + 8 * hf + g;
+    const uint32_t w = c == 0 ? word[0][0] : c == 1 ? word[0][1] : c == 2 ? word[1][0] : word[1][1];
+    if (row < n_valid) reinterpret_cast<uint32_t *>(rec0 + static_cast<size_t>(row) * (kJl / 8))[wq] = w;
 }
 
 // Quantize and store one key vector held by four lanes (this lane's rotated
@@ -235,7 +291,7 @@ __device__ __forceinline__ void qjl_sketch(uint32_t S_sm, const float (&y)[kQ], 
 // block's end (the lanes still run so that their exchanges stay warp-uniform).
 template <int KB, bool QJL>
 __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ], int q, int b, int h, int pos,
-                                         bool store, uint32_t S_sm = 0) {
+                                         bool store, float *Rsm = nullptr, int row = 0) {
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < kQ; i++) m = fmaxf(m, fabsf(y[i]));
@@ -269,13 +325,9 @@ __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ]
                                      static_cast<size_t>(pos) * (16 * KB) + q * (4 * KB), w);
         if (q == 0) p.kscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = m;
     }
-    if constexpr (QJL) {
-        if (store) {
-            const size_t qi = (static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos;
-            qjl_sketch(S_sm, y, q, true, p.qjl_signs + qi * (kJl / 8), p.qjl_norm + qi);
-        } else {
-            qjl_sketch(S_sm, y, q, false, nullptr, nullptr);
-        }
+    if constexpr (QJL) {  // the residual for the block's sketch (block_sketch), and rho
+        const float ss = residual_to_smem(Rsm, y, row, q);
+        if (store && q == 0) p.qjl_norm[(static_cast<size_t>(b) * p.nq + p.qrank[h]) * p.capacity + pos] = sqrtf(ss);
     }
 }
 
@@ -285,7 +337,7 @@ __device__ __forceinline__ void key_tail(const CompressParams &p, float (&y)[kQ]
 template <int VB, bool QJLV = false>
 __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[kQ], const float *thr_smem, int q,
                                            int b, int h, int pos, bool store, const float *cent_smem = nullptr,
-                                           uint32_t S_sm = 0) {
+                                           float *Rsm = nullptr, int row = 0) {
     // pairwise tree of squares in index order: this lane's 32 give one of the
     // four subtrees two levels under the root; the root adds
     // (q0 + q1) + (q2 + q3)
@@ -335,12 +387,8 @@ __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[k
         if (q == 0) p.vscale[(static_cast<size_t>(b) * p.H + h) * p.capacity + pos] = sigma;
     }
     if constexpr (QJLV) {
-        if (store) {
-            const size_t qi = (static_cast<size_t>(b) * p.nv + p.vrank[h]) * p.capacity + pos;
-            qjl_sketch(S_sm, y, q, true, p.vqjl_signs + qi * (kJl / 8), p.vqjl_norm + qi);
-        } else {
-            qjl_sketch(S_sm, y, q, false, nullptr, nullptr);
-        }
+        const float ss = residual_to_smem(Rsm, y, row, q);
+        if (store && q == 0) p.vqjl_norm[(static_cast<size_t>(b) * p.nv + p.vrank[h]) * p.capacity + pos] = sqrtf(ss);
     }
 }
 
@@ -348,27 +396,27 @@ __device__ __forceinline__ void value_tail(const CompressParams &p, float (&y)[k
 template <int KB, bool QJL>
 __device__ __noinline__ void key_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
                                         const float *out_scale, int q, int b, int h, int pos, bool store,
-                                        uint32_t S_sm) {
+                                        float *Rsm, int row) {
     float y[kQ];
     load_rotate(qrow, in_mask, out_scale, q, y);
-    key_tail<KB, QJL>(p, y, q, b, h, pos, store, S_sm);
+    key_tail<KB, QJL>(p, y, q, b, h, pos, store, Rsm, row);
 }
 
 template <int VB, bool QJLV>
 __device__ __noinline__ void value_vector(const CompressParams &p, const uint8_t *qrow, const uint32_t *in_mask,
                                           const float *out_scale, const float *thr_smem, const float *cent_smem,
-                                          int q, int b, int h, int pos, bool store, uint32_t S_sm) {
+                                          int q, int b, int h, int pos, bool store, float *Rsm, int row) {
     float y[kQ];
     load_rotate(qrow, in_mask, out_scale, q, y);
-    value_tail<VB, QJLV>(p, y, thr_smem, q, b, h, pos, store, cent_smem, S_sm);
+    value_tail<VB, QJLV>(p, y, thr_smem, q, b, h, pos, store, cent_smem, Rsm, row);
 }
 
-// Stage the rows of block `blk` (t-block fastest, then head, then batch) of
-// one group (0: K, 1: V) into `dst`, by the group's 128 threads.
+// Stage the rows of block `blk` (t-block fastest, then selected head, then
+// batch) of one group (0: K, 1: V) into `dst`, by the group's 128 threads.
 __device__ __forceinline__ void stage_block(const CompressParams &p, int n_tblk, int blk, int group, int gtid,
                                             uint8_t *dst) {
     const int tb = blk % n_tblk, rest = blk / n_tblk;
-    const int h = rest % p.H, b = rest / p.H;
+    const int h = p.sel[rest % p.n_sel], b = rest / p.n_sel;
     const int t0 = tb * kTok, nt = min(kTok, p.T - t0);
     const uint16_t *src = (group ? p.V : p.K) + b * p.sb + h * p.sh;
 #pragma unroll
@@ -389,11 +437,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     float *out_scale = reinterpret_cast<float *>(in_mask + kD / 2);          // [128]
     float *thr = out_scale + kD;                                             // [kCbTotal]
     float *cent = thr + kCbTotal;                                            // [kCbTotal]
-    uint8_t *S_stage = reinterpret_cast<uint8_t *>(cent + kCbTotal);         // [jl][d] when sketching
-    const uint32_t S_sm = static_cast<uint32_t>(__cvta_generic_to_shared(S_stage));
+    // residual rows of the current block, keys then values, when the launch sketches them
+    float *R_key = cent + kCbTotal;
+    float *R_val = R_key + (p.nq > 0 ? kTok * kRStride : 0);
 
     const int n_tblk = (p.T + kTok - 1) / kTok;
-    const int n_blk = n_tblk * p.H * p.B;
+    const int n_blk = n_tblk * p.n_sel * p.B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int group = warp >> 2, gtid = threadIdx.x & 127, q = lane & 3;
     const int r = (warp & 3) * 8 + (lane >> 2);  // this vector's row in the block
@@ -417,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 3)
         thr[j] = p.thr[j];
         cent[j] = p.cent[j];
     }
-    if (p.nq > 0 || p.nv > 0) stage_sketch_matrix(p.S, S_stage);
     __syncthreads();  // tables written
 
     for (int it = 0; blk < n_blk; blk += gridDim.x, it++) {
@@ -428,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         group_sync(group);  // block `blk` staged and visible to the group
 
         const int tb = blk % n_tblk, rest = blk / n_tblk;
-        const int h = rest % p.H, b = rest / p.H;
+        const int h = p.sel[rest % p.n_sel], b = rest / p.n_sel;
         const int t0 = tb * kTok, nt = min(kTok, p.T - t0);
         const bool store = r < nt;
         const int pos = p.t_begin + t0 + r;
@@ -437,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             const bool qj = p.qrank[h] >= 0;
             switch (p.kbits[h] * 2 + (qj ? 1 : 0)) {
 #define TQ_KEY_CASE(KB)                                                                                 \
-    case 2 * KB: key_vector<KB, false>(p, qrow, in_mask, out_scale, q, b, h, pos, store, S_sm); break;   \
-    case 2 * KB + 1: key_vector<KB, true>(p, qrow, in_mask, out_scale, q, b, h, pos, store, S_sm); break;
+    case 2 * KB: key_vector<KB, false>(p, qrow, in_mask, out_scale, q, b, h, pos, store, R_key, r); break;   \
+    case 2 * KB + 1: key_vector<KB, true>(p, qrow, in_mask, out_scale, q, b, h, pos, store, R_key, r); break;
                 TQ_KEY_CASE(1) TQ_KEY_CASE(2) TQ_KEY_CASE(3) TQ_KEY_CASE(4)
                 TQ_KEY_CASE(5) TQ_KEY_CASE(6) TQ_KEY_CASE(7) TQ_KEY_CASE(8)
 #undef TQ_KEY_CASE
@@ -450,15 +498,25 @@ __global__ void __launch_bounds__(kThreads, 3)
             const bool qv = p.vrank[h] >= 0;
             switch (vb * 2 + (qv ? 1 : 0)) {
 #define TQ_VAL_CASE(VB)                                                                                         \
-    case 2 * VB: value_vector<VB, false>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store, S_sm); break;   \
-    case 2 * VB + 1: value_vector<VB, true>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store, S_sm); break;
+    case 2 * VB: value_vector<VB, false>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store, R_val, r); break;   \
+    case 2 * VB + 1: value_vector<VB, true>(p, qrow, in_mask, out_scale, t, c, q, b, h, pos, store, R_val, r); break;
                 TQ_VAL_CASE(1) TQ_VAL_CASE(2) TQ_VAL_CASE(3) TQ_VAL_CASE(4)
                 TQ_VAL_CASE(5) TQ_VAL_CASE(6) TQ_VAL_CASE(7) TQ_VAL_CASE(8)
 #undef TQ_VAL_CASE
                 default: break;
             }
         }
-        group_sync(group);  // the group is done with this buffer before it is restaged
+        // sketched heads: the group's four warps project the block's 32
+        // residuals (rows in R_key / R_val), 32 projections each
+        const int rank = group == 0 ? p.qrank[h] : p.vrank[h];
+        if (rank >= 0) {
+            group_sync(group);  // every residual row written
+            const size_t rec = (static_cast<size_t>(b) * (group == 0 ? p.nq : p.nv) + rank) * p.capacity +
+                               p.t_begin + t0;
+            block_sketch(group == 0 ? R_key : R_val, p.S, warp & 3, lane,
+                         (group == 0 ? p.qjl_signs : p.vqjl_signs) + rec * (kJl / 8), nt);
+        }
+        group_sync(group);  // the group is done with this buffer (and its residual rows) before they are restaged
     }
 }
 
@@ -628,12 +686,13 @@ __global__ void dequant_kernel(const __grid_constant__ DequantParams p) {
 
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t s) {
     static bool configured = false;
-    // launches with sketched heads also stage S (two CTAs per SM instead of three)
-    const bool sketch = p.nq > 0 || p.nv > 0;
-    const size_t smem = compress_smem() + (sketch ? kSketchSmem : 0);
+    // launches with sketched keys (values) also hold the block's key (value)
+    // residuals: three CTAs per SM with one of the two, two with both
+    const size_t smem = compress_smem() + (p.nq > 0 ? kRSmem : 0) + (p.nv > 0 ? kRSmem : 0);
+    const bool sketch = p.nq > 0 && p.nv > 0;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(compress_smem() + kSketchSmem));
+                                             static_cast<int>(compress_smem() + 2 * kRSmem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -642,7 +701,7 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const long long n_blk = static_cast<long long>((p.T + kTok - 1) / kTok) * p.H * p.B;
+    const long long n_blk = static_cast<long long>((p.T + kTok - 1) / kTok) * p.n_sel * p.B;
     if (n_blk == 0) return cudaSuccess;
     const int grid = static_cast<int>(std::min<long long>(n_blk, (sketch ? 2LL : 3LL) * sms));
     compress_kernel<<<grid, kThreads, smem, s>>>(p);

@@ -359,18 +359,20 @@ bool value_buckets(const float *thr, int nt, RowsParams::Bucket *out) {
     return true;
 }
 
-// Launches of the one-thread-per-slice kernels for a compression without
-// sketches at head_dim d = 128, 256 or 512 (sign_bits: the rotation's d bits;
-// c supplies the pointers, strides and widths): the keys of each distinct key
-// width, then the values of each distinct value width (one launch each;
-// uniform layouts take two).  Returns cudaErrorNotSupported, before launching
-// anything, if a value width's bucket table does not separate its thresholds
-// (the caller then takes another kernel).
+// Launches of the one-thread-per-slice kernels for the heads c.sel[0..n_sel)
+// (none of them sketched) at head_dim d = 128, 256 or 512 (sign_bits: the
+// rotation's d bits; c supplies the pointers, strides and widths): the keys of
+// each distinct key width, then the values of each distinct value width (one
+// launch each; uniform layouts take two).  Returns cudaErrorNotSupported,
+// before launching anything, if a value width's bucket table does not separate
+// its thresholds (the caller then takes another kernel).
 cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout, const uint32_t *sign_bits, int d,
                         cudaStream_t s) {
     if (d != kD && d != 2 * kD && d != 4 * kD) return cudaErrorNotSupported;
+    bool in_sel[kMaxH] = {};
+    for (int i = 0; i < c.n_sel; ++i) in_sel[c.sel[i]] = true;
     for (int h = 0; h < c.H; ++h) {
-        if (c.vbits[h] > 3) continue;
+        if (!in_sel[h] || c.vbits[h] > 3) continue;
         const FittedCodebook &cb = fit(c.vbits[h], layout->value_law);
         float thr[7];
         for (int k = 0; k + 1 < (1 << c.vbits[h]); ++k) thr[k] = static_cast<float>(cb.bound[k]);
@@ -404,7 +406,7 @@ cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout
         for (int bits = 1; bits <= 8; ++bits) {
             p.n_heads = 0;
             for (int h = 0; h < c.H; ++h)
-                if ((values ? c.vbits[h] : c.kbits[h]) == bits) p.head[p.n_heads++] = static_cast<uint8_t>(h);
+                if (in_sel[h] && (values ? c.vbits[h] : c.kbits[h]) == bits) p.head[p.n_heads++] = static_cast<uint8_t>(h);
             if (p.n_heads == 0) continue;
             if (values) {
                 const FittedCodebook &cb = fit(bits, layout->value_law);
@@ -456,6 +458,7 @@ tq_status compress_other_dims(const tq_segment_layout *layout, const tq_rotation
             c.voff[h] = o.voff[h];
             c.kbits[h] = layout->kbits[h];
             c.vbits[h] = layout->vbits[h];
+            c.sel[c.n_sel++] = static_cast<uint8_t>(h);
         }
         const cudaError_t e = launch_rows(c, layout, rot->sign_bits, d, s);
         if (e != cudaErrorNotSupported) return e == cudaSuccess ? TQ_OK : cuda_fail(e);
@@ -1133,7 +1136,9 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
         p.vbits[h] = layout->vbits[h];
         p.qrank[h] = o.qrank[h];
         p.vrank[h] = o.vrank[h];
+        p.sel[h] = static_cast<uint8_t>(h);
     }
+    p.n_sel = p.H;
     std::memcpy(p.sign_bits, rot->sign_bits, sizeof(p.sign_bits));
     p.inv_sqrt_d = inv_sqrt_f32(kD);
     p.Q = rot->dense;
@@ -1149,9 +1154,25 @@ tq_status tq_compress(const tq_segment_layout *layout, const tq_rotation *rot, c
         }
         return e == cudaSuccess ? TQ_OK : cuda_fail(e);
     }
-    if (o.nq == 0 && o.nv == 0) {  // no sketches: one thread per vector, a launch per width
-        const cudaError_t e = launch_rows(p, layout, rot->sign_bits, kD, static_cast<cudaStream_t>(stream));
-        if (e != cudaErrorNotSupported) return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+    // heads without sketches: one thread per vector, a launch per width; the
+    // sketched heads (all heads if a value width's bucket table does not
+    // separate its thresholds): four lanes per vector
+    {
+        CompressParams plain = p;
+        plain.n_sel = 0;
+        for (int h = 0; h < p.H; ++h)
+            if (p.qrank[h] < 0 && p.vrank[h] < 0) plain.sel[plain.n_sel++] = static_cast<uint8_t>(h);
+        if (plain.n_sel > 0) {
+            const cudaError_t e = launch_rows(plain, layout, rot->sign_bits, kD, static_cast<cudaStream_t>(stream));
+            if (e == cudaSuccess) {
+                p.n_sel = 0;
+                for (int h = 0; h < p.H; ++h)
+                    if (p.qrank[h] >= 0 || p.vrank[h] >= 0) p.sel[p.n_sel++] = static_cast<uint8_t>(h);
+                if (p.n_sel == 0) return TQ_OK;
+            } else if (e != cudaErrorNotSupported) {
+                return cuda_fail(e);
+            }
+        }
     }
     const cudaError_t e = launch_compress(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);

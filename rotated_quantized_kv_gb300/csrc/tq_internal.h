@@ -52,6 +52,8 @@ struct CompressParams {
     int8_t vrank[kMaxH];         // -1: no value sketch
     float thr[kCbTotal];         // value thresholds, flat by bit width
     float cent[kCbTotal];        // value centroids, flat by bit width (value sketches)
+    int n_sel;                   // compress_kernel: the heads it compresses, sel[0..n_sel)
+    uint8_t sel[kMaxH];
 };
 
 constexpr int kRowsBuckets = 1024;  // buckets of a value quotient: sign, exponent, one mantissa bit

@@ -92,6 +92,7 @@ COMPRESS_CASES = [
     (3, 4, 77, 32, [1, 2, 2, 3], [1, 3, 2, 4], [1, 1, 0, 0], 0),
     (1, 8, 130, 0, [8, 3, 2, 1, 5, 7, 6, 4], [3, 1, 8, 2, 6, 4, 5, 7], [0, 0, 1, 1, 0, 0, 0, 1], 0),
     (2, 8, 150, 16, [4, 4, 3, 3, 2, 2, 1, 8], [1, 2, 3, 4, 5, 6, 7, 8], [0, 0, 0, 0, 1, 0, 0, 0], 1),
+    (1, 4, 90, 0, [1, 2, 1, 2], [3, 2, 3, 5], [1, 1, 1, 1], 0),  # every head sketched
     # no sketches: the one-thread-per-vector kernels, every width, both codebook laws
     (2, 8, 150, 16, [2, 4, 6, 8, 1, 3, 5, 7], [1, 2, 3, 4, 5, 6, 7, 8], None, 1),
     (3, 2, 33, 7, [3, 3], [3, 3], None, 0),
