@@ -26,29 +26,30 @@ def tq():
     return T
 
 
-def _packed_cache(tq, L, B, H, T, seed):
-    w = W.Workload("t", layers=L, batch=B, context=T, kv_heads=H, law="outliers")
+def _packed_cache(tq, L, B, H, T, seed, d=128):
+    w = W.Workload("t", layers=L, batch=B, context=T, kv_heads=H, head_dim=d, law="outliers")
     keep, views = [], []
     for l in range(L):
-        rot = tq.tq_make_rotation(128, 42 + l)
+        rot = tq.tq_make_rotation(d, 42 + l)
         K, V = W.kv_block(w, l, B, T, seed)
-        seg = tq.PackedSegment(tq.make_layout(B, H, 128, T, [3] * H, [3] * H))
+        seg = tq.PackedSegment(tq.make_layout(B, H, d, T, [3] * H, [3] * H))
         tq.tq_compress(seg, rot, K.cuda(), V.cuda())
         keep.append(seg)
         views.append(tq.layer_view(rot, [seg]))
     return keep, tq.views_array(views)
 
 
-def test_decode_wait_timeout_sets_flag_and_clears(tq):
+@pytest.mark.parametrize("d", [128, 256])  # 256: the split-K kernels on 128-dim sub-records
+def test_decode_wait_timeout_sets_flag_and_clears(tq, d):
     L, B, H, Hq, T = 2, 2, 4, 16, 1024
-    keep, arr = _packed_cache(tq, L, B, H, T, seed=5)
-    ws = torch.empty(tq.tq_decode_workspace_size(list(arr), B, H, Hq, 128), dtype=torch.uint8, device="cuda")
-    q = torch.randn(L, B, Hq, 128, generator=torch.Generator().manual_seed(3)).half().cuda()
-    ref = torch.empty(L, B, Hq, 128, device="cuda")
+    keep, arr = _packed_cache(tq, L, B, H, T, seed=5, d=d)
+    ws = torch.empty(tq.tq_decode_workspace_size(list(arr), B, H, Hq, d), dtype=torch.uint8, device="cuda")
+    q = torch.randn(L, B, Hq, d, generator=torch.Generator().manual_seed(3)).half().cuda()
+    ref = torch.empty(L, B, Hq, d, device="cuda")
     tq.tq_decode_attention(None, q, ref, ws, H, views=arr)
     assert tq.tq_decode_error_flag(ws) == 0
 
-    out = torch.full((L, B, Hq, 128), float("nan"), device="cuda")
+    out = torch.full((L, B, Hq, d), float("nan"), device="cuda")
     try:
         tq.tq_set_decode_wait_polls(0)
         tq.tq_decode_attention(None, q, out, ws, H, views=arr)
