@@ -523,14 +523,15 @@ def run_static(args, rank, world, tq):
 
 
 def decode_kernel_name(d, gqa):
-    """The split-K kernel runs head_dim 128, and 256 / 512 at GQA 1, 2 or 4 (on
-    128-dim sub-records); other shapes run the generic kernel."""
-    return "decode_packed_kernel" if d == 128 or (d in (256, 512) and gqa in (1, 2, 4)) else "gen_decode_kernel"
+    """The split-K kernel runs head_dim 128, and 64 / 256 / 512 at GQA 1, 2 or 4
+    (token pairs / 128-dim sub-records); other shapes run the generic kernel."""
+    return "decode_packed_kernel" if d == 128 or (d in (64, 256, 512) and gqa in (1, 2, 4)) else "gen_decode_kernel"
 
 
 # (workload, batch, context, head_dim): w2, the mixed-tier points of >= 1M cached
-# tokens per layer, and the w5 shape at head_dim 256 (the other head dims' kernels)
-EXTRA_POINTS = (("w2", None, None, None), ("w3", 8, None, None), ("w4", 32, None, None), ("w5", 8, 16384, 256))
+# tokens per layer, and the w5 shape at head_dim 256 and 64 (the other head dims' kernels)
+EXTRA_POINTS = (("w2", None, None, None), ("w3", 8, None, None), ("w4", 32, None, None), ("w5", 8, 16384, 256),
+                ("w5", 8, 16384, 64))
 
 
 def decode_point(tq, name, batch, context, K, Wm, world, dev, head_dim=None):

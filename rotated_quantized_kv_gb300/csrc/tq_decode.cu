@@ -25,11 +25,12 @@ constexpr int kRow16 = 272;  // padded row of 128 fp16 (conflict-free ldmatrix)
 constexpr int kStage16Bytes = 2 * kStageTokens * kRow16;  // one 64-token chunk of K and V
 // head_dim 128 nh: padded rows of 128 nh fp16, a 64-token chunk of K and V, then
 // the cross-warp merge scratch (write_partial) and the flag
-__host__ __device__ constexpr int row16(int nh) { return 256 * nh + 16; }
-__host__ __device__ constexpr int stage16_bytes(int nh) { return 2 * kStageTokens * row16(nh); }
+// (head_dim 64: np = 2, rows of 64 fp16)
+__host__ __device__ constexpr int row16(int nh, int np = 1) { return 256 * nh / np + 16; }
+__host__ __device__ constexpr int stage16_bytes(int nh, int np = 1) { return 2 * kStageTokens * row16(nh, np); }
 constexpr int kMergeScratchBytes = (32 + kDecodeWarps * kMaxGqa * kD) * 4;
-__host__ __device__ constexpr int fp16_smem_bytes(int nh) {
-    return nh == 1 ? kStage16Bytes + 16 : stage16_bytes(nh) + kMergeScratchBytes + 16;
+__host__ __device__ constexpr int fp16_smem_bytes(int nh, int np = 1) {
+    return nh == 1 && np == 1 ? kStage16Bytes + 16 : stage16_bytes(nh, np) + kMergeScratchBytes + 16;
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void *p) {
@@ -54,10 +55,12 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *
 // NH > 1 (head_dim 128 NH): the scores run over all NH 128-dim blocks, then
 // each block's P.V is merged across the warps and written as record
 // chunk NH + j of the group (block j), all with the chunk's m and l.
-template <int NH>
-__global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
+// NP = 2 (head_dim 64): rows of 64 dims; the record's virtual dims 64..127
+// stay zero (the merge adds the two halves).
+template <int NH, int NP = 1>
+__global__ void __launch_bounds__(kThreads, NH == 1 && NP == 1 ? 6 : 1)
     decode_fp16_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item) {
-    constexpr int kDh = NH * kD, kRow = row16(NH);
+    constexpr int kDh = NH * kD / NP, kRow = row16(NH, NP);
     extern __shared__ __align__(16) uint8_t smem[];
     const int idx = cta_item[blockIdx.x];
     const WorkItem &it = ws.items[idx];
@@ -67,7 +70,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
     const int ntok = min(it.chunk, it.n_tokens - tok0);  // <= kStageTokens
     const uint8_t *K = it.kc + b * it.kstride + static_cast<size_t>(tok0) * (kDh * 2);
     const uint8_t *V = it.vc + b * it.vstride + static_cast<size_t>(tok0) * (kDh * 2);
-    constexpr int kCh = 16 * NH;  // 16-byte pieces of a row
+    constexpr int kCh = 16 * NH / NP;  // 16-byte pieces of a row
     for (int i = threadIdx.x; i < 2 * kStageTokens * kCh; i += kThreads) {
         const int which = i / (kStageTokens * kCh), r = (i / kCh) % kStageTokens, ch = i % kCh;
         const uint8_t *src = (which ? V : K) + static_cast<size_t>(r) * (kDh * 2) + ch * 16;
@@ -82,14 +85,14 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
     pdl_launch_dependents();
     // B fragments of the (fp16, hence exact) queries: column g holds head g/2;
     // the lo columns (g odd) are zero.
-    uint32_t bq[8 * NH][2];
+    uint32_t bq[8 * NH / NP][2];
     {
         const int head = g >> 1;
         const size_t qidx = (static_cast<size_t>(it.layer) * dims.B + b) * dims.Hq + j0 + head;
         const bool ok = head < gqa && (g & 1) == 0;
         const uint32_t *qw = reinterpret_cast<const uint32_t *>(ws.q + qidx * kDh);
 #pragma unroll
-        for (int kk = 0; kk < 8 * NH; kk++) {
+        for (int kk = 0; kk < 8 * NH / NP; kk++) {
             bq[kk][0] = ok ? qw[8 * kk + c] : 0u;
             bq[kk][1] = ok ? qw[8 * kk + c + 4] : 0u;
         }
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
     cp_async_wait<0>();
     __syncthreads();
     const int tile0 = warp * 16;
-    if constexpr (NH == 1) {
+    if constexpr (NH == 1 && NP == 1) {
     if (tile0 < ntok) {
         const uint8_t *Ks = smem, *Vs = smem + kStageTokens * kRow16;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
     if (tile0 < ntok) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < 8 * NH; kk++) {
+        for (int kk = 0; kk < 8 * NH / NP; kk++) {
             uint32_t a[4];
             const int row = tile0 + (lane & 7) + ((lane >> 3) & 1) * 8;
             ldmatrix_x4(a, Ks + row * kRow + kk * 32 + (lane >> 4) * 16);
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
         softmax_tile(st, (acc[0] + acc[1]) * dims.qk_scale, (acc[2] + acc[3]) * dims.qk_scale, tile0 + g < ntok,
                      tile0 + g + 8 < ntok, 1.f, 1.f, g, c, c < gqa, b0, b1);
     }
-    float *scratch = reinterpret_cast<float *>(smem + stage16_bytes(NH));
+    float *scratch = reinterpret_cast<float *>(smem + stage16_bytes(NH, NP));
     const int slot0 = ws.grp_part[static_cast<size_t>(idx) * dims.B + b] + chunk * NH;
 #pragma unroll 1
     for (int j = 0; j < NH; j++) {
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
             for (int q = 0; q < 4; q++) st.acc[mt][q] = 0.f;
         if (tile0 < ntok) {
 #pragma unroll
-            for (int mt = 0; mt < 8; mt++) {
+            for (int mt = 0; mt < 8 / NP; mt++) {
                 uint32_t a[4];
                 const int mat = lane >> 3;
                 const int row = tile0 + (lane & 7) + (mat >> 1) * 8;
@@ -167,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
         write_partial(st, scratch, part, gqa, [g](int mt, int r) { return 16 * mt + g + 8 * r; });
     }
     pdl_wait();
-    finish_and_combine<NH>(dims, ws, it.layer, b, it.head,
-                           reinterpret_cast<int *>(smem + stage16_bytes(NH) + kMergeScratchBytes));
+    finish_and_combine<NH, NP>(dims, ws, it.layer, b, it.head,
+                               reinterpret_cast<int *>(smem + stage16_bytes(NH, NP) + kMergeScratchBytes));
     }
 }
 
@@ -182,7 +185,10 @@ __global__ void __launch_bounds__(kThreads, NH == 1 ? 6 : 1)
 // NH > 1 (head_dim 128 NH, SRHT layers only): the same for a vector of NH
 // 128-dim blocks; hi words at [64 j, 64 j + 64) for block j, lo words after
 // all NH blocks' hi words.
-template <int NH>
+//
+// NP = 2 (head_dim 64): lanes 0..15 hold dims 4 l .. 4 l + 3; hi words
+// [0, 32), lo words [32, 64).
+template <int NH, int NP = 1>
 __global__ void __launch_bounds__(kThreads)
     decode_prep_kernel(const DecodeDims dims, const DecodeWorkspace ws, const float *S) {
     __shared__ float qsh[kThreads / 32][kD];
@@ -192,6 +198,27 @@ __global__ void __launch_bounds__(kThreads)
     if (wid >= dims.L * dims.B * dims.Hq) return;
     const int l = wid / (dims.B * dims.Hq);
     const LayerPlan &lp = ws.layer[l];
+    if constexpr (NP == 2) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (lane < 16) load_q4(ws.q + static_cast<size_t>(wid) * (kD / 2), lane, x);
+        warp_rotate_64(x, lp.sign_bits, dims.inv_sqrt_d, lane);
+        if (lane >= 16) x[0] = x[1] = x[2] = x[3] = 0.f;
+        const float f = warp_pow2_norm(x);
+        float xn[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) xn[e] = x[e] * f;
+        uint32_t *hi = ws.qrot + static_cast<size_t>(wid) * (kD / 2);
+        float qs = 0.f;
+        if (lane < 16) qs = store_hilo_block(hi, hi + kD / 4, xn, 0, lane);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
+        if (lane == 0) {
+            ws.qsum[static_cast<size_t>(wid) * 4] = qs / f;
+            ws.qsum[static_cast<size_t>(wid) * 4 + 1] = 0.f;
+            ws.qsum[static_cast<size_t>(wid) * 4 + 2] = 1.0f / f;
+        }
+        return;
+    }
     if constexpr (NH > 1) {
         float y[NH][4];
 #pragma unroll
@@ -261,6 +288,20 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+PackedLauncher packed_launcher_narrow(int kb, int vb) {
+    switch (kb) {
+        case 1: return packed_launcher_narrow_kb1(vb);
+        case 2: return packed_launcher_narrow_kb2(vb);
+        case 3: return packed_launcher_narrow_kb3(vb);
+        case 4: return packed_launcher_narrow_kb4(vb);
+        case 5: return packed_launcher_narrow_kb5(vb);
+        case 6: return packed_launcher_narrow_kb6(vb);
+        case 7: return packed_launcher_narrow_kb7(vb);
+        case 8: return packed_launcher_narrow_kb8(vb);
+        default: return nullptr;
+    }
+}
+
 PackedLauncher packed_launcher_wide(int kb, int vb, int nh) {
     switch (kb) {
         case 1: return packed_launcher_wide_kb1(vb, nh);
@@ -275,12 +316,12 @@ PackedLauncher packed_launcher_wide(int kb, int vb, int nh) {
     }
 }
 
-template <int NH>
+template <int NH, int NP = 1>
 cudaError_t configure_fp16() {
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(decode_fp16_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   fp16_smem_bytes(NH));
+        const cudaError_t e = cudaFuncSetAttribute(decode_fp16_kernel<NH, NP>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, fp16_smem_bytes(NH, NP));
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -309,14 +350,16 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
                                   const float *value_c1,
                                   cudaStream_t s, cudaEvent_t ev_start, cudaEvent_t ev_stop, int *n_launched) {
     *n_launched = 0;
-    const int nh = dims.nh;
-    if (nh != 1 && nh != 2 && nh != 4) return cudaErrorInvalidValue;
+    const int nh = dims.nh, np = dims.np;
+    if ((nh != 1 && nh != 2 && nh != 4) || (np != 1 && np != 2) || (np == 2 && nh != 1)) return cudaErrorInvalidValue;
     {
-        const cudaError_t e = nh == 1 ? dec::configure_fp16<1>() : nh == 2 ? dec::configure_fp16<2>()
-                                                                            : dec::configure_fp16<4>();
+        const cudaError_t e = np == 2    ? dec::configure_fp16<1, 2>()
+                              : nh == 1 ? dec::configure_fp16<1>()
+                              : nh == 2 ? dec::configure_fp16<2>()
+                                        : dec::configure_fp16<4>();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem16 = static_cast<size_t>(dec::fp16_smem_bytes(nh));
+    const size_t smem16 = static_cast<size_t>(dec::fp16_smem_bytes(nh, np));
     // Order: [prep] -> packed classes -> fp16 segments.  Every kernel after the
     // first may start early (programmatic dependent launch); each grid waits
     // for its predecessor before its final merges, the QJL classes also wait
@@ -331,7 +374,8 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
     if (dims.any_prep) {
         const int n_warps = dims.L * dims.B * dims.Hq;
         const unsigned grid = static_cast<unsigned>((n_warps + 3) / 4);
-        if (nh == 1) dec::decode_prep_kernel<1><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
+        if (np == 2) dec::decode_prep_kernel<1, 2><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
+        else if (nh == 1) dec::decode_prep_kernel<1><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
         else if (nh == 2) dec::decode_prep_kernel<2><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
         else dec::decode_prep_kernel<4><<<grid, dec::kThreads, 0, s>>>(dims, ws, S);
         first = false;
@@ -346,8 +390,10 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
     for (int i = 0; i < n_classes; i++) {
         const ClassLaunch &c = classes[i];
         if (c.n_ctas <= 0 || c.kb == 16) continue;
-        const PackedLauncher fn = nh == 1 ? dec::packed_launcher(c.kb, c.vb, c.qjl != 0)
-                                          : (c.qjl ? nullptr : dec::packed_launcher_wide(c.kb, c.vb, nh));
+        const PackedLauncher fn = c.qjl && (nh != 1 || np != 1) ? nullptr
+                                  : np == 2                   ? dec::packed_launcher_narrow(c.kb, c.vb)
+                                  : nh == 1                   ? dec::packed_launcher(c.kb, c.vb, c.qjl != 0)
+                                                              : dec::packed_launcher_wide(c.kb, c.vb, nh);
         if (!fn) return cudaErrorInvalidValue;
         const cudaError_t e =
             fn(dims, ws, ws.cta_item + c.cta_off, c.n_ctas, c.n_stages, value_half[i], value_c1[i], s, !first);
@@ -370,7 +416,8 @@ cudaError_t launch_decode_kernels(const DecodeDims &dims, const DecodeWorkspace 
         cfg.attrs = attr;
         cfg.numAttrs = first ? 0 : 1;
         const cudaError_t e =
-            nh == 1   ? cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<1>, dims, ws, ws.cta_item + c.cta_off)
+            np == 2   ? cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<1, 2>, dims, ws, ws.cta_item + c.cta_off)
+            : nh == 1 ? cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<1>, dims, ws, ws.cta_item + c.cta_off)
             : nh == 2 ? cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<2>, dims, ws, ws.cta_item + c.cta_off)
                       : cudaLaunchKernelEx(&cfg, dec::decode_fp16_kernel<4>, dims, ws, ws.cta_item + c.cta_off);
         if (e != cudaSuccess) return e;

@@ -110,7 +110,8 @@ __device__ __forceinline__ float warp_sum_g(float v) {
 // group; acc holds the P.V accumulator fragment (8 m-tiles x 4).
 struct WarpState {
     float m, l;
-    float wsum;  // sum of the weights p * value scale (linear value decodes only)
+    float wsum;      // sum of the weights p * value scale (linear value decodes only)
+    float wsum_odd;  // the same over the odd tokens of token pairs (head_dim 64)
     float acc[8][4];
 };
 
@@ -118,6 +119,7 @@ __device__ __forceinline__ void init_state(WarpState &st) {
     st.m = kNegInf;
     st.l = 0.f;
     st.wsum = 0.f;
+    st.wsum_odd = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; mt++)
 #pragma unroll
@@ -267,6 +269,111 @@ __device__ __forceinline__ void write_warp_partial_pair(WarpState &st, float *re
     for (int e = 0; e < 2; e++) {
         const int h = 2 * c + e;
         const float Wh = e ? W1 : W0;
+        if (h < gqa) {
+            float *rec = rec_base + h * kPartStride + 4;
+#pragma unroll
+            for (int mt = 0; mt < 8; mt++) {
+                rec[dim_of(mt, 0)] = fin(mt, 0, st.acc[mt][e], Wh);
+                rec[dim_of(mt, 1)] = fin(mt, 1, st.acc[mt][2 + e], Wh);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ head_dim 64
+// The packed kernel reads two consecutive tokens (2 v, 2 v + 1) as one 128-dim
+// "virtual" record (their two 64-dim records are adjacent).  Scores come per
+// (virtual row, parity); the P.V B fragment's eight columns are (head n & 3,
+// parity n >> 2), so accumulator row (dim) of thread group g is meaningful for
+// the columns whose parity is that of its half (g < 4: even tokens, dims
+// 0..63; g >= 4: odd tokens, virtual dims 64..127); the merge adds the halves.
+
+// softmax_pair for token pairs: s[4 t + 2 r + p] = tile t, virtual row g + 8 r,
+// parity p; the B fragment column g (head g & 3, parity g >> 2) of virtual
+// tokens 2c, 2c+1 (b[2t]) and 2c+8, 2c+9 (b[2t+1]).
+template <bool FULL, bool WSUM>
+__device__ __forceinline__ void softmax_pair2(WarpState &st, const float (&s)[8], const bool (&ok)[8],
+                                              const float (&vs)[8], int g, int c, uint32_t (&b)[4]) {
+    const int lane = threadIdx.x & 31;
+    float smax = kNegInf, vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        smax = fmaxf(smax, (FULL || ok[i]) ? s[i] : kNegInf);
+        vmax = fmaxf(vmax, (FULL || ok[i]) ? vs[i] : 0.f);
+    }
+    if (__any_sync(0xffffffffu, smax > st.m + 8.0f || (smax > st.m && vmax > 255.0f))) {
+        const float mnew = fmaxf(st.m, warp_max_g(smax));
+        const float corr = (mnew == kNegInf) ? 1.f : ex2(st.m - mnew);
+        st.l *= corr;
+        if constexpr (WSUM) {
+            st.wsum *= corr;
+            st.wsum_odd *= corr;
+        }
+        const float c0 = __shfl_sync(0xffffffffu, corr, (lane & ~3) | ((2 * c) & 3));
+        const float c1 = __shfl_sync(0xffffffffu, corr, (lane & ~3) | ((2 * c + 1) & 3));
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) {
+            st.acc[mt][0] *= c0;
+            st.acc[mt][1] *= c1;
+            st.acc[mt][2] *= c0;
+            st.acc[mt][3] *= c1;
+        }
+        st.m = mnew;
+    }
+    float w[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const float p = (FULL || ok[i]) ? ex2(s[i] - st.m) : 0.f;
+        st.l += p;
+        w[i] = (FULL || ok[i]) ? p * vs[i] : 0.f;  // a select: masked scales may be stale bytes
+    }
+    if constexpr (WSUM) {
+        st.wsum += (w[0] + w[2]) + (w[4] + w[6]);
+        st.wsum_odd += (w[1] + w[3]) + (w[5] + w[7]);
+    }
+    const int src0 = 8 * c + (g & 3), src1 = src0 + 4;
+    const bool odd = (g >> 2) != 0;
+#pragma unroll
+    for (int t = 0; t < 2; t++) {
+        float x[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {  // (row g_s, source): (0, src0), (0, src1), (1, src0), (1, src1)
+            const int r = k >> 1;
+            const int src = (k & 1) ? src1 : src0;
+            const float xe = __shfl_sync(0xffffffffu, w[4 * t + 2 * r], src);
+            const float xo = __shfl_sync(0xffffffffu, w[4 * t + 2 * r + 1], src);
+            x[k] = odd ? xo : xe;
+        }
+        const __half2 h01 = __floats2half2_rn(x[0], x[1]), h23 = __floats2half2_rn(x[2], x[3]);
+        b[2 * t] = *reinterpret_cast<const uint32_t *>(&h01);
+        b[2 * t + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+    }
+}
+
+// write_warp_partial_pair for token pairs: lane (g, c) holds columns 2c, 2c+1 =
+// (heads (2c) & 3, (2c+1) & 3; parity c >> 1) and writes the rows of its half
+// (g < 4 with even columns, g >= 4 with odd ones) as virtual dims 0..127 of
+// its heads' records.
+template <typename DimOf, typename Fin>
+__device__ __forceinline__ void write_warp_partial_pair2(WarpState &st, float *rec_base, int gqa, DimOf dim_of,
+                                                         Fin fin) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const float l = warp_sum_g(st.l);
+    const float We = warp_sum_g(st.wsum), Wo = warp_sum_g(st.wsum_odd);
+    const bool odd = (c >> 1) != 0;
+    const float W0e = __shfl_sync(0xffffffffu, We, (lane & ~3) | ((2 * c) & 3));
+    const float W0o = __shfl_sync(0xffffffffu, Wo, (lane & ~3) | ((2 * c) & 3));
+    const float W1e = __shfl_sync(0xffffffffu, We, (lane & ~3) | ((2 * c + 1) & 3));
+    const float W1o = __shfl_sync(0xffffffffu, Wo, (lane & ~3) | ((2 * c + 1) & 3));
+    if (c < gqa && g == 0) {
+        rec_base[c * kPartStride] = st.m;
+        rec_base[c * kPartStride + 1] = l;
+    }
+    if ((g >= 4) != odd) return;
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int h = (2 * c + e) & 3;
+        const float Wh = e ? (odd ? W1o : W1e) : (odd ? W0o : W0e);
         if (h < gqa) {
             float *rec = rec_base + h * kPartStride + 4;
 #pragma unroll
@@ -472,6 +579,31 @@ __device__ __forceinline__ void warp_rotate_wide(float (&x)[NH][4], const uint32
     }
 }
 
+// y = R x for a 64-vector on lanes 0..15 (lane l: dims 4 l .. 4 l + 3); lanes
+// 16..31 run the same steps on their own copy (shuffles stay within each half).
+__device__ __forceinline__ void warp_rotate_64(float (&x)[4], const uint32_t *sign_bits, float inv_sqrt_d,
+                                               int lane) {
+    const int l = lane & 15;
+    apply_signs(x, sign_bits, l);
+    const float t0 = x[0] + x[1], t1 = x[0] - x[1], t2 = x[2] + x[3], t3 = x[2] - x[3];
+    x[0] = t0 + t2;
+    x[2] = t0 - t2;
+    x[1] = t1 + t3;
+    x[3] = t1 - t3;
+#pragma unroll
+    for (int hl = 1; hl < 16; hl <<= 1) {
+        const bool upper = lane & hl;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[e], hl);
+            x[e] = upper ? (o - x[e]) : (x[e] + o);
+        }
+    }
+    apply_signs(x, sign_bits, l);
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] *= inv_sqrt_d;
+}
+
 // warp_pow2_norm over all blocks.
 template <int NH>
 __device__ __forceinline__ float warp_pow2_norm_wide(const float (&x)[NH][4]) {
@@ -532,8 +664,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 template <int NH>
 __device__ __forceinline__ void combine_wide(const DecodeDims &dims, const DecodeWorkspace &ws, int layer, int b,
                                              int h, int warp, int lane);
+// NP = 2 (head_dim 64): records hold 128 virtual dims, the sum over even
+// tokens in dims 0..63 and over odd tokens in 64..127; the merge adds them.
+__device__ __forceinline__ void combine_np2(const DecodeDims &dims, const DecodeWorkspace &ws, int layer, int b,
+                                            int h, int warp, int lane);
 
-template <int NH = 1>
+template <int NH = 1, int NP = 1>
 __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const DecodeWorkspace &ws, int layer,
                                                    int b, int h, int *flag) {
     __threadfence();
@@ -549,6 +685,11 @@ __device__ __forceinline__ void finish_and_combine(const DecodeDims &dims, const
         if (*flag && warp < dims.gqa) {
             __threadfence();
             combine_wide<NH>(dims, ws, layer, b, h, warp, lane);
+        }
+    } else if constexpr (NP == 2) {
+        if (*flag && warp < dims.gqa) {
+            __threadfence();
+            combine_np2(dims, ws, layer, b, h, warp, lane);
         }
     } else if (*flag && warp < dims.gqa) {
         __threadfence();
@@ -703,6 +844,75 @@ __device__ __forceinline__ void combine_wide(const DecodeDims &dims, const Decod
     for (int j = 0; j < NH; j++)
         dst[32 * j + lane] = make_float4((ar[j][0] + ao[j][0]) * inv, (ar[j][1] + ao[j][1]) * inv,
                                          (ar[j][2] + ao[j][2]) * inv, (ar[j][3] + ao[j][3]) * inv);
+}
+
+__device__ __forceinline__ void combine_np2(const DecodeDims &dims, const DecodeWorkspace &ws, int layer, int b,
+                                            int h, int warp, int lane) {
+    const LayerPlan &lp = ws.layer[layer];
+    const int n_items = lp.n_items[h];
+    const size_t rec_stride = kMaxGqa * kPartStride;
+    float M = kNegInf, L = 0.f;
+    float ar[4] = {0.f, 0.f, 0.f, 0.f}, ao[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ii = 0; ii < n_items; ii++) {
+        const int item = lp.item[h][ii];
+        const size_t gr = static_cast<size_t>(item) * dims.B + b;
+        const int p0 = ws.grp_part[gr], np = ws.grp_nparts[gr];
+        const bool rot = ws.items[item].kind == TQ_SEG_PACKED;
+        const float *base = ws.part + static_cast<size_t>(p0) * rec_stride + warp * kPartStride;
+        for (int c0 = 0; c0 < np; c0 += 8) {
+            float m[8], l[8];
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int c = min(c0 + u, np - 1);
+                const float *rec = base + static_cast<size_t>(c) * rec_stride;
+                m[u] = c0 + u < np ? __ldcg(rec) : kNegInf;
+                l[u] = __ldcg(rec + 1);
+                v[u] = __ldcg(reinterpret_cast<const float4 *>(rec + 4) + lane);
+            }
+            float mc = m[0];
+#pragma unroll
+            for (int u = 1; u < 8; u++) mc = fmaxf(mc, m[u]);
+            if (mc > M) {
+                const float sc = ex2(M - mc);
+                L *= sc;
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    ar[e] *= sc;
+                    ao[e] *= sc;
+                }
+                M = mc;
+            }
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                if (m[u] == kNegInf) continue;
+                const float f = ex2(m[u] - M);
+                L += f * l[u];
+                a[0] += f * v[u].x;
+                a[1] += f * v[u].y;
+                a[2] += f * v[u].z;
+                a[3] += f * v[u].w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                ar[e] += rot ? a[e] : 0.f;
+                ao[e] += rot ? 0.f : a[e];
+            }
+        }
+    }
+    // virtual dims 4 lane + e: lanes 16..31 hold the odd tokens' dims 4 (lane - 16) + e
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        ar[e] += __shfl_xor_sync(0xffffffffu, ar[e], 16);
+        ao[e] += __shfl_xor_sync(0xffffffffu, ao[e], 16);
+    }
+    warp_rotate_64(ar, lp.sign_bits, dims.inv_sqrt_d, lane);
+    const float inv = L > 0.f ? 1.0f / L : 0.f;
+    const size_t qrow = (static_cast<size_t>(layer) * dims.B + b) * dims.Hq + h * dims.gqa + warp;
+    if (lane < 16)
+        reinterpret_cast<float4 *>(ws.out + qrow * (kD / 2))[lane] =
+            make_float4((ar[0] + ao[0]) * inv, (ar[1] + ao[1]) * inv, (ar[2] + ao[2]) * inv, (ar[3] + ao[3]) * inv);
 }
 
 // Write one warp's state as a partial record (no cross-warp merge): for each

@@ -26,14 +26,19 @@ __host__ __device__ constexpr int packed_token_bytes(int kb, int vb, bool qjl, i
 __host__ __device__ constexpr bool packed_light(int kb, int vb, bool qjl, int nh = 1) {
     return packed_token_bytes(kb, vb, qjl, nh) <= 112;
 }
-__host__ __device__ constexpr int packed_stage_tokens(int kb, int vb, bool qjl, int nh = 1) {
-    return packed_token_bytes(kb, vb, qjl, nh) <= 64    ? 512
+//
+// np = 2 (head_dim 64): a tile row is a pair of tokens read as one 128-dim
+// record, so a stage holds twice the tokens of the 128-dim class of the same
+// widths (the same bytes), at 3 CTAs per SM.
+__host__ __device__ constexpr int packed_stage_tokens(int kb, int vb, bool qjl, int nh = 1, int np = 1) {
+    return np > 1                                       ? np * packed_stage_tokens(kb, vb, qjl, 1, 1)
+           : packed_token_bytes(kb, vb, qjl, nh) <= 64  ? 512
            : packed_light(kb, vb, qjl, nh)              ? 256
            : packed_token_bytes(kb, vb, qjl, nh) <= 284 ? 128
                                                         : 64;
 }
-__host__ __device__ constexpr int packed_ctas_per_sm(int kb, int vb, bool qjl, int nh = 1) {
-    return (nh > 1 || qjl || packed_light(kb, vb, qjl, nh)) ? 3 : 4;
+__host__ __device__ constexpr int packed_ctas_per_sm(int kb, int vb, bool qjl, int nh = 1, int np = 1) {
+    return (np > 1 || nh > 1 || qjl || packed_light(kb, vb, qjl, nh)) ? 3 : 4;
 }
 
 }  // namespace tqk

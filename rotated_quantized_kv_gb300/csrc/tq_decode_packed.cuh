@@ -208,6 +208,31 @@ __device__ __forceinline__ void qk_raw(const uint8_t *rec0, const uint8_t *rec1,
     raw1 = (e[2] + e[3]) + (o[2] + o[3]);
 }
 
+// Token pairs (head_dim 64): rows g, g+8 are virtual records (2 v, 2 v + 1);
+// the E columns take q against all 128 virtual dims, the O columns q with the
+// odd half negated (nmask = 0x80008000 on the lanes c >= 2 holding it), so
+// that E + O and E - O are twice the even and odd tokens' raw Q.K.
+template <typename KU, int NW>
+__device__ __forceinline__ void qk_raw2(const uint8_t *rec0, const uint8_t *rec1, const uint32_t (&bq)[16],
+                                        uint32_t nmask, float (&raw)[4]) {
+    uint32_t w0[NW], w1[NW], a0[16], a1[16];
+    lds_words(w0, rec0);
+    lds_words(w1, rec1);
+    KU::run(w0, a0);
+    KU::run(w1, a1);
+    float e[4] = {0.f, 0.f, 0.f, 0.f}, o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+        mma16816(e, a0[2 * kk], a1[2 * kk], a0[2 * kk + 1], a1[2 * kk + 1], bq[2 * kk], bq[2 * kk + 1]);
+        mma16816(o, a0[2 * kk], a1[2 * kk], a0[2 * kk + 1], a1[2 * kk + 1], bq[2 * kk] ^ nmask,
+                 bq[2 * kk + 1] ^ nmask);
+    }
+    raw[0] = e[0] + e[1];  // row g: E
+    raw[1] = o[0] + o[1];  // row g: O
+    raw[2] = e[2] + e[3];  // row g + 8: E
+    raw[3] = o[2] + o[3];  // row g + 8: O
+}
+
 // B fragment (16 registers) of a natural-order fp16 vector slice: words q[0..15]
 // hold dims 2i, 2i+1 of the thread's 32-dim slice; register r pairs dims
 // KU::dim(r, 0) and KU::dim(r, 1), each scaled by 2^(kA - shift) (exact).
@@ -424,11 +449,12 @@ struct ValueTable {
     float c1;                  // binary32 centroid 1 of a 1-bit codebook (= -centroid 0)
 };
 
-template <int KB, int VB, bool QJL, int NH = 1>
+template <int KB, int VB, bool QJL, int NH = 1, int NP = 1>
 struct PackedGeom {
-    static constexpr int PT = packed_stage_tokens(KB, VB, QJL, NH);  // tokens per stage, a multiple of 64
-    static constexpr int CTAS = packed_ctas_per_sm(KB, VB, QJL, NH);
-    static constexpr int RK = 16 * KB * NH, RV = 16 * VB * NH;  // bytes of a token's key / value record
+    static constexpr int PT = packed_stage_tokens(KB, VB, QJL, NH, NP);  // tokens per stage, a multiple of 64
+    static constexpr int CTAS = packed_ctas_per_sm(KB, VB, QJL, NH, NP);
+    static constexpr int RK = 16 * KB * NH / NP, RV = 16 * VB * NH / NP;  // bytes of a token's key / value record
+    static constexpr int RKR = RK * NP, RVR = RV * NP;  // bytes of a tile row (NP tokens)
     static constexpr int offV = PT * RK;
     static constexpr int offKS = offV + PT * RV;
     static constexpr int offVS = offKS + PT * 4;
@@ -518,12 +544,16 @@ struct StageCursor {
 // Q.K partials through shared memory (a named barrier per block, the same
 // order on every warp, so that all take identical softmax decisions), and
 // each writes its sub-record's partial (record w mod NH of its group).
-template <int KB, int VB, bool QJL, int NH = 1>
-__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
+//
+// NP = 2 (head_dim 64): a tile row is a token pair, read as one 128-dim
+// record (qk_raw2, softmax_pair2, write_warp_partial_pair2, combine_np2).
+template <int KB, int VB, bool QJL, int NH = 1, int NP = 1>
+__global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, NP))
     decode_packed_kernel(const DecodeDims dims, const DecodeWorkspace ws, const int *__restrict__ cta_item,
                          const long long S, const __grid_constant__ ValueTable vt) {
     static_assert(NH == 1 || (!QJL && (NH == 2 || NH == 4)), "QJL sketches at head_dim 128 only");
-    using G = PackedGeom<KB, VB, QJL, NH>;
+    static_assert(NP == 1 || (!QJL && NH == 1 && NP == 2), "token pairs: head_dim 64, no QJL");
+    using G = PackedGeom<KB, VB, QJL, NH, NP>;
     using KU = KUnpack<KB>;
     using VD = VDec<VB, G::TS>;
     constexpr int NS = G::stages;
@@ -541,13 +571,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
     vx.ctab = reinterpret_cast<const unsigned short *>(smem + G::ctab);
     vx.tab = smem_u32(smem + G::ptab) + 4 * (lane & (G::copies - 1));
     if constexpr (VB == 1) {
-        vx.off = 2 * c * G::RV + 16 * VB * sub + 4 * (g >> 1);
+        vx.off = 2 * c * G::RVR + 16 * VB * sub + 4 * (g >> 1);
         vx.sh = (g & 1) ? 0x7632 : 0x5410;  // PRMT: x's halfword g | y's halfword g
     } else if constexpr (VB == 3) {
-        vx.off = 2 * c * G::RV + 16 * VB * sub + 4 * ((3 * g) >> 1);
+        vx.off = 2 * c * G::RVR + 16 * VB * sub + 4 * ((3 * g) >> 1);
         vx.sh = (g & 1) * 16;
     } else {
-        vx.off = 2 * c * G::RV + 16 * VB * sub + ((2 * VB * g) & ~3);
+        vx.off = 2 * c * G::RVR + 16 * VB * sub + ((2 * VB * g) & ~3);
         vx.sh = ((2 * VB * g) & 3) * 8;
     }
     if constexpr (VB >= 5) {
@@ -595,7 +625,10 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
         const int t0 = lc.st * kPT;
         const int n = min(kPT, lc.n_tokens - t0);
         // scale runs are rounded up to 16 bytes: rows hold a multiple of 16 tokens
-        const unsigned nk = n * G::RK, nv = n * G::RV, ns = (n * 4 + 15) & ~15u;
+        // token pairs: an odd count rounds up to 16 bytes inside the row
+        const unsigned nk = NP == 1 ? n * G::RK : (n * G::RK + 15) & ~15u;
+        const unsigned nv = NP == 1 ? n * G::RV : (n * G::RV + 15) & ~15u;
+        const unsigned ns = (n * 4 + 15) & ~15u;
         const unsigned total = nk + nv + 2 * ns + (QJL ? n * 16 + ns : 0);
         fence_proxy_async();
         mbar_expect_tx(bar, total);
@@ -631,7 +664,8 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
     const float c1 = vt.c1;
     // byte offset of the thread's key window: codes [32c, 32c+32) of token row
     // g's sub-record
-    const int koff = g * G::RK + 16 * KB * sub + 4 * KB * c;
+    const int koff = g * G::RKR + 16 * KB * sub + 4 * KB * c;
+    const uint32_t nmask = (NP == 2 && c >= 2) ? 0x80008000u : 0u;  // token pairs: the odd half's sign
 
     int xpar = 0;  // exchange buffer of the warp's next block (NH > 1)
     // each warp writes its own partial of the current group; then the group's
@@ -640,14 +674,15 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
         const long long gr = static_cast<long long>(g_item) * B + g_b;
         const int slot = ws.grp_part[gr] +
                          kDecodeWarps * static_cast<int>(blockIdx.x - cta_of_stage(g_stage0, S, gridDim.x)) + warp;
-        write_warp_partial_pair(
-            st, ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride), gqa,
-            [g](int mt, int r) { return 16 * g + VD::dim(mt, r); },
-            [c1](int mt, int r, float acc, float W) {
-                if constexpr (VD::kLinear) return c1 * (2.0f * acc * VDec<1, 7>::unscale(mt, r) - W);
-                else return acc;
-            });
-        finish_and_combine<NH>(dims, ws, g_layer, g_b, g_head, flag);
+        auto dim_of = [g](int mt, int r) { return 16 * g + VD::dim(mt, r); };
+        auto fin = [c1](int mt, int r, float acc, float W) {
+            if constexpr (VD::kLinear) return c1 * (2.0f * acc * VDec<1, 7>::unscale(mt, r) - W);
+            else return acc;
+        };
+        float *rec = ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride);
+        if constexpr (NP == 2) write_warp_partial_pair2(st, rec, gqa, dim_of, fin);
+        else write_warp_partial_pair(st, rec, gqa, dim_of, fin);
+        finish_and_combine<NH, NP>(dims, ws, g_layer, g_b, g_head, flag);
     };
     // a new group: its identity and the B fragments of its rotated queries
     // (column g: head g/2, part g&1), each head divided by a power of two 2^e
@@ -675,6 +710,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
             qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             tsum = c < gqa ? ws.qsum[(qbase + c) * 4 + 1] : 0.f;
             aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
+        } else if constexpr (NP == 2) {  // 64 dims: lanes c and c + 2 take the same 32
+            const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (kD / 4) + 16 * (c & 1);
+#pragma unroll
+            for (int i = 0; i < 16; i++) q[i] = head < gqa ? qw[i] : 0u;
+            gather_b<KU>(q, bq);
+            qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
+            aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
         } else {  // the prep kernel rotated the queries
             const uint32_t *qw = ws.qrot + ((qbase + head) * 2 + part) * (NH * kD / 2) + 64 * sub + 16 * c;
 #pragma unroll
@@ -687,8 +729,35 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
     // the warp's two 16-token tiles: tokens [tA, tA + 32) of the stage buffer
     auto tiles = [&](const uint8_t *buf, int tA, int n, auto full_tag) {
         constexpr bool FULL = decltype(full_tag)::value;
-        float sc[4];
         const float *kss = reinterpret_cast<const float *>(buf + G::offKS);
+        const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
+        uint32_t bp[4];
+        if constexpr (NP == 2) {
+            // virtual rows tA + 16 t + g (+ 8): tokens 2 row, 2 row + 1
+            float s8[8], vs8[8];
+            bool ok8[8];
+            const float ha = 0.5f * aq;
+#pragma unroll
+            for (int t = 0; t < 2; t++) {
+                const int t0 = tA + 16 * t, r0 = t0 + g;
+                float raw[4];
+                qk_raw2<KU, KB>(buf + t0 * G::RKR + koff, buf + (t0 + 8) * G::RKR + koff, bq, nmask, raw);
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    const float E = raw[2 * r], O = raw[2 * r + 1];
+#pragma unroll
+                    for (int par = 0; par < 2; par++) {
+                        const int tok = 2 * (r0 + 8 * r) + par;
+                        const int i = 4 * t + 2 * r + par;
+                        s8[i] = kss[tok] * (ha * (par ? E - O : E + O) + beta * qsum) * qk_scale;
+                        ok8[i] = FULL || tok < n;
+                        vs8[i] = vss[tok];
+                    }
+                }
+            }
+            softmax_pair2<FULL, VD::kLinear>(st, s8, ok8, vs8, g, c, bp);
+        } else {
+        float sc[4];
         if constexpr (NH > 1) {
             // this sub-record's raw Q.K of tokens g, g+8 of both tiles, summed
             // over the NH sub-records in the order 0..NH-1 by every warp
@@ -736,7 +805,6 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
             sc[2 * t + 1] = s1 * qk_scale;
         }
         }
-        const float *vss = reinterpret_cast<const float *>(buf + G::offVS);
         bool okv[4];
         if constexpr (FULL) {
             okv[0] = okv[1] = okv[2] = okv[3] = true;
@@ -747,17 +815,18 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
             okv[3] = tA + 24 + g < n;
         }
         const float vsv[4] = {vss[tA + g], vss[tA + g + 8], vss[tA + 16 + g], vss[tA + 24 + g]};
-        uint32_t bp[4];
         softmax_pair<FULL, VD::kLinear>(st, sc, okv, vsv, g, c, bp);
-        // ---- values of both tiles
+        }
+        // ---- values of both tiles (rows: tokens, or token pairs for NP = 2)
         const uint8_t *vst = buf + G::offV;
+        const int nrows = NP == 1 ? n : (n + 1) / 2;
 #pragma unroll
         for (int t = 0; t < 2; t++) {
-            if (!FULL && t == 1 && tA + 16 >= n) break;
-            const uint8_t *vrow = vst + (tA + 16 * t) * G::RV;
+            if (!FULL && t == 1 && tA + 16 >= nrows) break;
+            const uint8_t *vrow = vst + (tA + 16 * t) * G::RVR;
             uint32_t ra[8], rb[8], rc[8], rd[8];
-            VD::pair(vrow, G::RV, vx, ra, rb);              // tokens 2c, 2c+1
-            VD::pair(vrow + 8 * G::RV, G::RV, vx, rc, rd);  // tokens 2c+8, 2c+9
+            VD::pair(vrow, G::RVR, vx, ra, rb);               // rows 2c, 2c+1
+            VD::pair(vrow + 8 * G::RVR, G::RVR, vx, rc, rd);  // rows 2c+8, 2c+9
 #pragma unroll
             for (int mt = 0; mt < 8; mt++)
                 mma16816(st.acc[mt], ra[mt], rb[mt], rc[mt], rd[mt], bp[2 * t], bp[2 * t + 1]);
@@ -789,9 +858,11 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
         const int n = min(kPT, cc.n_tokens - cc.st * kPT);
         new_group = cc.advance(ws.items, B, k + 1 < n_st);
         // warp w takes tokens [32 w, 32 w + 32) of every 128 of the stage
-        // (NH > 1: block w / NH of every 128 / NH, sub-record w mod NH)
-        for (int tA = (warp / NH) * 32; tA < n; tA += 32 * (kDecodeWarps / NH)) {
-            if (tA + 32 <= n) tiles(buf, tA, n, std::true_type{});
+        // (NH > 1: block w / NH of every 128 / NH, sub-record w mod NH; NP = 2:
+        // rows of token pairs)
+        const int nrows = NP == 1 ? n : (n + 1) / 2;
+        for (int tA = (warp / NH) * 32; tA < nrows; tA += 32 * (kDecodeWarps / NH)) {
+            if (NP * (tA + 32) <= n) tiles(buf, tA, n, std::true_type{});
             else tiles(buf, tA, n, std::false_type{});
         }
     }
@@ -801,15 +872,15 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH))
     flush();
 }
 
-template <int KB, int VB, bool QJL, int NH = 1>
+template <int KB, int VB, bool QJL, int NH = 1, int NP = 1>
 cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, const int *cta_item, int n_ctas,
                           long long n_stages, const unsigned short *value_half, float value_c1, cudaStream_t s,
                           bool pdl) {
-    using G = PackedGeom<KB, VB, QJL, NH>;
+    using G = PackedGeom<KB, VB, QJL, NH, NP>;
     static bool configured = false;
     if (!configured) {
         if (G::smem > 48 * 1024) {
-            const cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<KB, VB, QJL, NH>,
+            const cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<KB, VB, QJL, NH, NP>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, G::smem);
             if (e != cudaSuccess) return e;
         }
@@ -828,7 +899,7 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL, NH>, dims, ws, cta_item, n_stages, vt);
+    return cudaLaunchKernelEx(&cfg, decode_packed_kernel<KB, VB, QJL, NH, NP>, dims, ws, cta_item, n_stages, vt);
 }
 
 }  // namespace dec
@@ -861,8 +932,8 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, con
     }                                                                                                          \
     }
 
-// head_dim 128 nh (nh = 2, 4; no QJL): one translation unit per key width
-// instantiates every value width.
+// head_dim 128 nh (nh = 2, 4) and head_dim 64 (token pairs), no QJL: one
+// translation unit per key width instantiates every value width.
 #define TQ_INSTANTIATE_WIDE_KB(KB)                                                                            \
     namespace tqk {                                                                                            \
     PackedLauncher packed_launcher_wide_kb##KB(int vb, int nh) {                                               \
@@ -883,6 +954,19 @@ cudaError_t launch_packed(const DecodeDims &dims, const DecodeWorkspace &ws, con
             case 60: return dec::launch_packed<KB, 7, false, 4>;                                               \
             case 66: return dec::launch_packed<KB, 8, false, 2>;                                               \
             case 68: return dec::launch_packed<KB, 8, false, 4>;                                               \
+            default: return nullptr;                                                                           \
+        }                                                                                                      \
+    }                                                                                                          \
+    PackedLauncher packed_launcher_narrow_kb##KB(int vb) {                                                     \
+        switch (vb) {                                                                                          \
+            case 1: return dec::launch_packed<KB, 1, false, 1, 2>;                                             \
+            case 2: return dec::launch_packed<KB, 2, false, 1, 2>;                                             \
+            case 3: return dec::launch_packed<KB, 3, false, 1, 2>;                                             \
+            case 4: return dec::launch_packed<KB, 4, false, 1, 2>;                                             \
+            case 5: return dec::launch_packed<KB, 5, false, 1, 2>;                                             \
+            case 6: return dec::launch_packed<KB, 6, false, 1, 2>;                                             \
+            case 7: return dec::launch_packed<KB, 7, false, 1, 2>;                                             \
+            case 8: return dec::launch_packed<KB, 8, false, 1, 2>;                                             \
             default: return nullptr;                                                                           \
         }                                                                                                      \
     }                                                                                                          \

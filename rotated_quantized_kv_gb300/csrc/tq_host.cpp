@@ -580,15 +580,18 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     if (!pow2(d) || d < 16 || d > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     const int gqa = Hq / H;
     // head_dim 256 and 512 with GQA 1, 2 or 4 run the split-K kernels on 128-dim
-    // sub-records; other head dims the generic kernel (GQA up to 4); neither
-    // takes QJL sketches, dense rotations or attention-mass outputs
+    // sub-records, head_dim 64 on token pairs read as 128-dim records; other
+    // head dims the generic kernel (GQA up to 4); none of them takes QJL
+    // sketches, dense rotations or attention-mass outputs
     const bool mma_gqa = gqa == 1 || gqa == 2 || gqa == 4;
     const bool wide = (d == 2 * kD || d == 4 * kD) && mma_gqa;
-    const bool generic = d != kD && !wide;
+    const bool narrow = d == kD / 2 && mma_gqa;
+    const bool generic = d != kD && !wide && !narrow;
     const bool other_dim = d != kD;
     if (!generic && !mma_gqa) return TQ_ERR_UNSUPPORTED;
     if (generic && gqa > kMaxGqa) return TQ_ERR_UNSUPPORTED;
     const int nh = wide ? d / kD : 1;
+    const int np = narrow ? 2 : 1;
     for (int l = 0; l < n_layers; ++l) {
         const tq_layer_view &lv = layers[l];
         if (lv.n_segments < 0 || lv.n_segments > TQ_MAX_SEGMENTS || lv.rot.head_dim != d) return TQ_ERR_ARG;
@@ -772,13 +775,13 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
         ClassLaunch &c = P.classes.back();
         c.item_hi = static_cast<int>(i) + 1;
         if (w.kind == TQ_SEG_PACKED) {
-            const int pt = packed_stage_tokens(w.kb, w.vb, w.qjl != 0, nh);
+            const int pt = packed_stage_tokens(w.kb, w.vb, w.qjl != 0, nh, np);
             w.n_stages = (w.n_tokens + pt - 1) / pt;
             w.stage_begin = stages;
             stages += static_cast<long long>(B) * w.n_stages;
             c.n_stages = stages;
             c.n_ctas = static_cast<int>(std::min<long long>(
-                stages, static_cast<long long>(sms) * packed_ctas_per_sm(w.kb, w.vb, w.qjl != 0, nh)));
+                stages, static_cast<long long>(sms) * packed_ctas_per_sm(w.kb, w.vb, w.qjl != 0, nh, np)));
         } else {
             w.cta_begin = static_cast<int>(cta);
             cta += static_cast<long long>(B) * w.n_chunks;
@@ -897,6 +900,7 @@ tq_status build_plan(const tq_layer_view *layers, int n_layers, int B, int H, in
     D.qk_scale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     D.wait_polls = g_wait_polls.load();
     D.nh = nh;
+    D.np = np;
     const size_t nq = static_cast<size_t>(n_layers) * B * Hq;
     // offset 0: the error flag (kept in its own 256 bytes so that it has a
     // fixed place), then the work items

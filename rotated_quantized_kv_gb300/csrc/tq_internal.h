@@ -160,6 +160,7 @@ struct DecodeDims {
     float inv_sqrt_d;    // binary32(1/sqrt(d)) used by the rotations
     int wait_polls;      // polls of a split-K CTA's wait for its own copies before it gives up
     int nh;              // 128-dim sub-records per head vector (head_dim / 128: 1, 2 or 4)
+    int np;              // tokens per 128-dim tile row (2 at head_dim 64, else 1)
 };
 
 // Workspace: [WorkItem x n][LayerPlan x L][group tables][counters][q prep]
@@ -229,6 +230,15 @@ PackedLauncher packed_launcher_wide_kb5(int vb, int nh);
 PackedLauncher packed_launcher_wide_kb6(int vb, int nh);
 PackedLauncher packed_launcher_wide_kb7(int vb, int nh);
 PackedLauncher packed_launcher_wide_kb8(int vb, int nh);
+// head_dim 64 (token pairs), no QJL
+PackedLauncher packed_launcher_narrow_kb1(int vb);
+PackedLauncher packed_launcher_narrow_kb2(int vb);
+PackedLauncher packed_launcher_narrow_kb3(int vb);
+PackedLauncher packed_launcher_narrow_kb4(int vb);
+PackedLauncher packed_launcher_narrow_kb5(int vb);
+PackedLauncher packed_launcher_narrow_kb6(int vb);
+PackedLauncher packed_launcher_narrow_kb7(int vb);
+PackedLauncher packed_launcher_narrow_kb8(int vb);
 
 // ----------------------------------------------------------------- other head dims
 // Compression, dequantization and decode attention for head dimensions other

@@ -170,9 +170,9 @@ def test_host_side_argument_errors(tq):
     assert e.value.status == -3
     with pytest.raises(tq.TQError):
         tq.tq_age_tiers(10, [5, 3])
-    # head_dim 256 / 512: GQA 1-4 plan (1, 2, 4 on the split-K kernels, 3 on
-    # the generic one); QJL keys and attention-mass outputs stay at 128
-    for d in (256, 512):
+    # head_dim 64 / 256 / 512: GQA 1-4 plan (1, 2, 4 on the split-K kernels, 3
+    # on the generic one); QJL keys and attention-mass outputs stay at 128
+    for d in (64, 256, 512):
         rotd = tq.tq_make_rotation(d, 42)
         Pd = tq.PackedSegment(tq.make_layout(1, 2, d, 48, 3, 3), device="cpu", n_tokens=40)
         for hq in (2, 4, 6, 8):

@@ -172,6 +172,7 @@ def _groups(L, B, H):
     ("w4", 32, None, None),  # per-head widths and QJL at 1.05M cached tokens per layer
     ("w5", 8, 16384, 256),   # the w5 shape at head_dim 256, as the benchmark runs it
     ("w3", None, None, 256),  # the age tiers and fp16 segments at head_dim 256
+    ("w5", 8, 16384, 64),    # the w5 shape at head_dim 64, as the benchmark runs it
 ])
 def test_static_workload_full_size(lib, name, batch, context, head_dim):
     T, MC = lib

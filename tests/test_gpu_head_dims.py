@@ -187,6 +187,13 @@ ATTN_CASES = [
     (256, 2, 1, 2, 8, [("packed", 0, [3, 3], [3, 3]), ("fp16", 5)]),  # fp16 tokens only
     (256, 1, 1, 2, 8, [("packed", 0, [3, 3], [3, 3]), ("fp16", 0)]),  # empty cache
     (256, 1, 1, 2, 6, [("packed", 100, [3, 3], [3, 3]), ("fp16", 9)]),  # GQA 3: the generic kernel
+    # head_dim 64 on the split-K kernels (token pairs read as 128-dim records):
+    # every width, odd token counts (an unpaired last token), GQA 1, 2, 4
+    (64, 1, 3, 8, 8, [("packed", 333, [1, 2, 3, 4, 5, 6, 7, 8], [8, 7, 6, 5, 4, 3, 2, 1]), ("fp16", 151)]),
+    (64, 2, 2, 4, 8, [("fp16", 64), ("packed", 2049, [2, 3, 4, 5], [5, 4, 3, 2]),
+                      ("packed", 77, [8, 8, 1, 1], [1, 8, 1, 8])]),
+    (64, 1, 1, 2, 8, [("packed", 1, [3, 3], [3, 3]), ("fp16", 0)]),  # a single (unpaired) token
+    (64, 1, 2, 2, 8, [("packed", 0, [3, 3], [3, 3]), ("fp16", 33)]),  # fp16 tokens only
 ]
 
 

@@ -39,7 +39,7 @@ def _packed_cache(tq, L, B, H, T, seed, d=128):
     return keep, tq.views_array(views)
 
 
-@pytest.mark.parametrize("d", [128, 256])  # 256: the split-K kernels on 128-dim sub-records
+@pytest.mark.parametrize("d", [128, 256, 64])  # 256: 128-dim sub-records; 64: token pairs
 def test_decode_wait_timeout_sets_flag_and_clears(tq, d):
     L, B, H, Hq, T = 2, 2, 4, 16, 1024
     keep, arr = _packed_cache(tq, L, B, H, T, seed=5, d=d)
