@@ -21,7 +21,8 @@ LIB = os.path.join(PKG, "_lib", "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_SOURCES = ["tq_compress.cu", "tq_compress_dense.cu", "tq_decode.cu", "tq_mass.cu", "tq_static.cu",
-                "tq_generic.cu", "tq_compress_rows.cu", "tq_compress_rows_nh2.cu", "tq_compress_rows_nh4.cu"] + [
+                "tq_generic.cu", "tq_compress_rows.cu", "tq_compress_rows_nh2.cu", "tq_compress_rows_nh4.cu",
+                "tq_compress_rows_np2.cu"] + [
                 f"tq_decode_kb{k}.cu" for k in range(1, 9)] + [
                 f"tq_decode_wide_kb{k}.cu" for k in range(1, 9)]
 HOST_SOURCES = ["tq_host.cpp"]

@@ -38,6 +38,15 @@
 // the same order on both sides.  A d-dim record is the NH 128-dim records of
 // the slices one after another (the LSB-first stream cut at dims 128 j falls on
 // a byte boundary), so each thread stores its slice's 16 b bytes.
+//
+// Head_dim 64 (NP = 2): a thread takes two consecutive tokens, the first in
+// the low halves of its 64 register pairs and the second in the high halves
+// (the staged row is the two tokens' 64-dim vectors one after the other).  The
+// stages h = 1..32 run as at 128 dims on both at once; stage 64 and the root of
+// the sum-of-squares tree, which would join the halves, are left out, and each
+// half gets its own absmax or sigma.  The two 64-dim records are adjacent in
+// the segment, so the thread's 128 codes are both records in order (one
+// 16 b-byte store when both tokens exist and the first position is even).
 #pragma once
 
 #include <algorithm>
@@ -109,12 +118,12 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
 }
 
-// Stage the fp16 rows of block `blk` ((b, head of the list, block of 32 / NH
-// tokens), token block fastest) into this warp's buffer: row r is slice
-// r / (32 / NH) of token r mod (32 / NH) of the block.
-template <int NH>
+// Stage the fp16 rows of block `blk` ((b, head of the list, block of tokens),
+// token block fastest) into this warp's buffer: row r is slice r / (32 / NH)
+// of token r mod (32 / NH) of the block (NP = 2: tokens 2 r, 2 r + 1).
+template <int NH, int NP>
 __device__ __forceinline__ void stage_rows(const RowsParams &p, int n_tblk, int blk, uint8_t *buf, int lane) {
-    constexpr int TPW = 32 / NH;
+    constexpr int TPW = 32 * NP / NH;
     const int tb = blk % n_tblk, rest = blk / n_tblk;
     const int h = p.head[rest % p.n_heads], b = rest / p.n_heads;
     const int t0 = tb * TPW, nt = min(TPW, p.T - t0);
@@ -122,10 +131,17 @@ __device__ __forceinline__ void stage_rows(const RowsParams &p, int n_tblk, int 
 #pragma unroll
     for (int i = 0; i < 16; i++) {
         const int idx = lane + 32 * i, r = idx >> 4, c = idx & 15;
-        const int tok = r % TPW, sl = r / TPW;
-        if (tok < nt)
-            cp_async16(buf + r * kRowBytes + 16 * (c ^ (r & 7)),
-                       src + static_cast<int64_t>(tok) * p.st + kD * sl + 8 * c);
+        if constexpr (NP == 2) {
+            const int tok = 2 * r + (c >> 3);
+            if (tok < nt)
+                cp_async16(buf + r * kRowBytes + 16 * (c ^ (r & 7)),
+                           src + static_cast<int64_t>(tok) * p.st + 8 * (c & 7));
+        } else {
+            const int tok = r % TPW, sl = r / TPW;
+            if (tok < nt)
+                cp_async16(buf + r * kRowBytes + 16 * (c ^ (r & 7)),
+                           src + static_cast<int64_t>(tok) * p.st + kD * sl + 8 * c);
+        }
     }
 }
 
@@ -160,9 +176,10 @@ __host__ __device__ constexpr size_t rows_smem_bytes(bool val_table) {
            (val_table ? kRowsBuckets * 8 : 0);
 }
 
-template <int BITS, bool VAL, int NH>
+template <int BITS, bool VAL, int NH, int NP = 1>
 __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid_constant__ RowsParams p) {
-    constexpr int TPW = 32 / NH;  // tokens of a warp block
+    static_assert(NP == 1 || NH == 1, "token pairs: head_dim 64");
+    constexpr int TPW = 32 * NP / NH;  // tokens of a warp block
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t *in_mask = reinterpret_cast<uint32_t *>(smem + kWarps * 2 * kWarpBuf);  // [NH][kMaskStride]
     float *out_pair = reinterpret_cast<float *>(in_mask + NH * kMaskStride);         // [NH][kPairStride]
@@ -186,18 +203,18 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
     const int n_tblk = (p.T + TPW - 1) / TPW;
     const int n_blk = n_tblk * p.n_heads * p.B;
     const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
-    if (gw < n_blk) stage_rows<NH>(p, n_tblk, gw, bufs, lane);
+    if (gw < n_blk) stage_rows<NH, NP>(p, n_tblk, gw, bufs, lane);
     asm volatile("cp.async.commit_group;\n" ::);
 
     for (int blk = gw, it = 0; blk < n_blk; blk += nw, it++) {
         const int next = blk + nw;
-        if (next < n_blk) stage_rows<NH>(p, n_tblk, next, bufs + ((it + 1) & 1) * kWarpBuf, lane);
+        if (next < n_blk) stage_rows<NH, NP>(p, n_tblk, next, bufs + ((it + 1) & 1) * kWarpBuf, lane);
         asm volatile("cp.async.commit_group;\n" ::);
         asm volatile("cp.async.wait_group 1;\n" ::: "memory");
         __syncwarp();
         const int tb = blk % n_tblk, rest = blk / n_tblk;
         const int h = p.head[rest % p.n_heads], b = rest / p.n_heads;
-        const int t = tb * TPW + lane % TPW;
+        const int t = NP == 2 ? tb * TPW + 2 * lane : tb * TPW + lane % TPW;  // (the first token of the pair)
         const uint8_t *row = bufs + (it & 1) * kWarpBuf + lane * kRowBytes;
 
         // ---- load, input sign flip on the fp16 bits, widen: chunks c and
@@ -234,11 +251,13 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                 }
             }
         }
+        if constexpr (NP == 1) {
 #pragma unroll
-        for (int m = 0; m < 64; m++) {
-            const float u = a[m].x, v = a[m].y;
-            a[m].x = __fadd_rn(u, v);
-            a[m].y = __fsub_rn(u, v);
+            for (int m = 0; m < 64; m++) {
+                const float u = a[m].x, v = a[m].y;
+                a[m].x = __fadd_rn(u, v);
+                a[m].y = __fsub_rn(u, v);
+            }
         }
         // h = 128 (256): the same register of slice sl ^ x, x = 1 (2), from
         // lane ^ x TPW; fma(+-1, own, other) rounds the exact sum once
@@ -264,17 +283,27 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
         uint32_t w[4 * BITS];
 #pragma unroll
         for (int j = 0; j < 4 * BITS; j++) w[j] = 0u;
-        float scale;
+        float scale, scale_b = 0.0f;  // scale_b: the pair's second token (NP = 2)
         if constexpr (!VAL) {
             // ---- keys: m = max |y|, v = y * binary32(1/m), u = round(v + 1) 2^(b-1),
             // code = clamp(floor(u), 0, 2^b - 1)
-            float mx = 0.0f;
+            float mx = 0.0f, mxb = 0.0f;
+            if constexpr (NP == 2) {
 #pragma unroll
-            for (int m = 0; m < 64; m++) mx = fmax3(mx, fabsf(a[m].x), fabsf(a[m].y));
+                for (int m = 0; m < 64; m += 2) {
+                    mx = fmax3(mx, fabsf(a[m].x), fabsf(a[m + 1].x));
+                    mxb = fmax3(mxb, fabsf(a[m].y), fabsf(a[m + 1].y));
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < 64; m++) mx = fmax3(mx, fabsf(a[m].x), fabsf(a[m].y));
+            }
 #pragma unroll
             for (int x = 1; x < NH; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x * TPW));
             scale = mx;
+            scale_b = mxb;
             const float r = mx > 0.0f ? __frcp_rn(mx) : 0.0f;
+            const float rb = NP == 2 ? (mxb > 0.0f ? __frcp_rn(mxb) : 0.0f) : r;
             constexpr float hc = static_cast<float>(1 << (BITS - 1));
             // v = y r lies in [-1, 1]: r = binary32(1/m) is within 2^-24 of 1/m
             // and |y| <= m, so |y r| <= 1 + 2^-24 rounds to at most 1.  Hence
@@ -285,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
             constexpr uint32_t kHi = kKeyLo + (1u << BITS) - 1u;
 #pragma unroll
             for (int m = 0; m < 64; m++) {
-                const float2 v = fmul2(a[m], make_float2(r, r));
+                const float2 v = fmul2(a[m], make_float2(r, rb));
                 // fma(v, 2^(b-1), 2^(b-1)) is round(v + 1) 2^(b-1): scaling by a
                 // power of two commutes with the rounding
                 const float2 u = ffma2(v, make_float2(hc, hc), make_float2(hc, hc));
@@ -313,13 +342,18 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
 #pragma unroll
                 for (int j = 0; j < len / 2; j++) s[j] = fadd2(s[2 * j], s[2 * j + 1]);
             }
-            float tot = __fadd_rn(s[0].x, s[0].y);
+            // NP = 2: the two halves' trees are the two tokens' sums (no root join)
+            float tot = NP == 2 ? s[0].x : __fadd_rn(s[0].x, s[0].y);
             // blocks of 256 (512) coordinates: slices (2i, 2i + 1), then (4i, 4i + 2)
 #pragma unroll
             for (int x = 1; x < NH; x <<= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, x * TPW));
-            const float sigma = __fsqrt_rn(__fmul_rn(tot, 1.0f / (kD * NH)));  // / d exact (a power of two)
+            constexpr float inv_d = 1.0f / (kD * NH / NP);  // exact (a power of two)
+            const float sigma = __fsqrt_rn(__fmul_rn(tot, inv_d));
+            const float sigma_b = NP == 2 ? __fsqrt_rn(__fmul_rn(s[0].y, inv_d)) : sigma;
             scale = sigma;
+            scale_b = sigma_b;
             const float r = sigma > 0.0f ? __frcp_rn(sigma) : 0.0f;
+            const float rb = NP == 2 ? (sigma_b > 0.0f ? __frcp_rn(sigma_b) : 0.0f) : r;
             constexpr int NT = (1 << BITS) - 1;
             if constexpr (BITS <= 3) {
                 // #{k : thr_k < u} from the bucket of u's top ten bits (sign,
@@ -329,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                 const uint32_t tab = static_cast<uint32_t>(__cvta_generic_to_shared(vtab));
 #pragma unroll
                 for (int m = 0; m < 64; m++) {
-                    const float2 u = fmul2(a[m], make_float2(r, r));
+                    const float2 u = fmul2(a[m], make_float2(r, rb));
                     const uint2 e0 = lds64(tab + ((__float_as_uint(u.x) >> 22) << 3));
                     const uint2 e1 = lds64(tab + ((__float_as_uint(u.y) >> 22) << 3));
                     put<BITS>(w, m, e0.y + (__uint_as_float(e0.x) < u.x ? 1u : 0u));
@@ -341,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                 for (int j = 0; j < NT; j++) th[j] = thr[j];
 #pragma unroll
                 for (int m = 0; m < 64; m++) {
-                    const float2 u = fmul2(a[m], make_float2(r, r));
+                    const float2 u = fmul2(a[m], make_float2(r, rb));
                     uint32_t k0 = 0, k1 = 0;
 #pragma unroll
                     for (int st = 1 << (BITS - 1); st >= 1; st >>= 1) {
@@ -362,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
             } else {
 #pragma unroll
                 for (int m = 0; m < 64; m++) {
-                    const float2 u = fmul2(a[m], make_float2(r, r));
+                    const float2 u = fmul2(a[m], make_float2(r, rb));
                     uint32_t k0 = 0, k1 = 0;
 #pragma unroll
                     for (int st = 1 << (BITS - 1); st >= 1; st >>= 1) {
@@ -374,7 +408,23 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                 }
             }
         }
-        if (t < p.T) {
+        if constexpr (NP == 2) {
+            // the pair's two 8 b-byte records (t_begin even: 16-byte aligned)
+            const int pos = p.t_begin + t;
+            uint8_t *dst = p.codes + static_cast<size_t>(b) * p.block + p.off[h] + static_cast<size_t>(pos) * (8 * BITS);
+            float *sc = p.scale + (static_cast<size_t>(b) * p.H + h) * p.capacity + pos;
+            if (t + 1 < p.T) {
+#pragma unroll
+                for (int j = 0; j < BITS; j++)
+                    reinterpret_cast<uint4 *>(dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                sc[0] = scale;
+                sc[1] = scale_b;
+            } else if (t < p.T) {  // an unpaired last token
+#pragma unroll
+                for (int j = 0; j < BITS; j++) reinterpret_cast<uint2 *>(dst)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
+                sc[0] = scale;
+            }
+        } else if (t < p.T) {
             const int pos = p.t_begin + t;
             uint4 *dst = reinterpret_cast<uint4 *>(p.codes + static_cast<size_t>(b) * p.block + p.off[h] +
                                                    static_cast<size_t>(pos) * (16 * BITS * NH) + 16 * BITS * sl);
@@ -385,45 +435,45 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
     }
 }
 
-template <int BITS, bool VAL, int NH>
+template <int BITS, bool VAL, int NH, int NP = 1>
 cudaError_t rows_launch(const RowsParams &p, cudaStream_t s) {
     constexpr size_t smem = rows_smem_bytes<NH>(VAL && BITS <= 3);
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(compress_rows_kernel<BITS, VAL, NH>,
+        const cudaError_t e = cudaFuncSetAttribute(compress_rows_kernel<BITS, VAL, NH, NP>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
     int sms = 148, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    constexpr int TPW = 32 / NH;
+    constexpr int TPW = 32 * NP / NH;
     const long long blocks = (static_cast<long long>((p.T + TPW - 1) / TPW) * p.n_heads * p.B + kWarps - 1) / kWarps;
     const long long grid = std::min<long long>(blocks, static_cast<long long>(sms) * 3);
-    compress_rows_kernel<BITS, VAL, NH><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
+    compress_rows_kernel<BITS, VAL, NH, NP><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 // The launch of one width, keys or values.
-template <int NH>
+template <int NH, int NP = 1>
 cudaError_t rows_dispatch(const RowsParams &p, int bits, bool values, cudaStream_t s) {
     switch (bits * 2 + (values ? 1 : 0)) {
-        case 2: return rows_launch<1, false, NH>(p, s);
-        case 3: return rows_launch<1, true, NH>(p, s);
-        case 4: return rows_launch<2, false, NH>(p, s);
-        case 5: return rows_launch<2, true, NH>(p, s);
-        case 6: return rows_launch<3, false, NH>(p, s);
-        case 7: return rows_launch<3, true, NH>(p, s);
-        case 8: return rows_launch<4, false, NH>(p, s);
-        case 9: return rows_launch<4, true, NH>(p, s);
-        case 10: return rows_launch<5, false, NH>(p, s);
-        case 11: return rows_launch<5, true, NH>(p, s);
-        case 12: return rows_launch<6, false, NH>(p, s);
-        case 13: return rows_launch<6, true, NH>(p, s);
-        case 14: return rows_launch<7, false, NH>(p, s);
-        case 15: return rows_launch<7, true, NH>(p, s);
-        case 16: return rows_launch<8, false, NH>(p, s);
-        case 17: return rows_launch<8, true, NH>(p, s);
+        case 2: return rows_launch<1, false, NH, NP>(p, s);
+        case 3: return rows_launch<1, true, NH, NP>(p, s);
+        case 4: return rows_launch<2, false, NH, NP>(p, s);
+        case 5: return rows_launch<2, true, NH, NP>(p, s);
+        case 6: return rows_launch<3, false, NH, NP>(p, s);
+        case 7: return rows_launch<3, true, NH, NP>(p, s);
+        case 8: return rows_launch<4, false, NH, NP>(p, s);
+        case 9: return rows_launch<4, true, NH, NP>(p, s);
+        case 10: return rows_launch<5, false, NH, NP>(p, s);
+        case 11: return rows_launch<5, true, NH, NP>(p, s);
+        case 12: return rows_launch<6, false, NH, NP>(p, s);
+        case 13: return rows_launch<6, true, NH, NP>(p, s);
+        case 14: return rows_launch<7, false, NH, NP>(p, s);
+        case 15: return rows_launch<7, true, NH, NP>(p, s);
+        case 16: return rows_launch<8, false, NH, NP>(p, s);
+        case 17: return rows_launch<8, true, NH, NP>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -368,7 +368,8 @@ bool value_buckets(const float *thr, int nt, RowsParams::Bucket *out) {
 // its thresholds (the caller then takes another kernel).
 cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout, const uint32_t *sign_bits, int d,
                         cudaStream_t s) {
-    if (d != kD && d != 2 * kD && d != 4 * kD) return cudaErrorNotSupported;
+    // head_dim 64: token pairs starting at even positions (whole 16-byte stores)
+    if (d != kD && d != 2 * kD && d != 4 * kD && !(d == kD / 2 && c.t_begin % 2 == 0)) return cudaErrorNotSupported;
     bool in_sel[kMaxH] = {};
     for (int i = 0; i < c.n_sel; ++i) in_sel[c.sel[i]] = true;
     for (int h = 0; h < c.H; ++h) {
@@ -389,14 +390,19 @@ cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout
     p.T = c.T;
     p.t_begin = c.t_begin;
     p.capacity = c.capacity;
-    p.nh = d / kD;
+    p.nh = d >= kD ? d / kD : 1;
+    p.np = d >= kD ? 1 : kD / d;  // head_dim 64: two tokens per thread, the same signs for both
     const float c_d = inv_sqrt_f32(d);
-    for (int i = 0; i < d / 2; ++i) {
-        const uint32_t s0 = (sign_bits[(2 * i) >> 5] >> ((2 * i) & 31)) & 1u;
-        const uint32_t s1 = (sign_bits[(2 * i + 1) >> 5] >> ((2 * i + 1) & 31)) & 1u;
+    for (int i = 0; i < p.nh * kD / 2; ++i) {
+        const int j = i % (d / 2);
+        const uint32_t s0 = (sign_bits[(2 * j) >> 5] >> ((2 * j) & 31)) & 1u;
+        const uint32_t s1 = (sign_bits[(2 * j + 1) >> 5] >> ((2 * j + 1) & 31)) & 1u;
         p.in_mask[i] = (s0 << 15) | (s1 << 31);
     }
-    for (int i = 0; i < d; ++i) p.out_scale[i] = ((sign_bits[i >> 5] >> (i & 31)) & 1u) ? -c_d : c_d;
+    for (int i = 0; i < p.nh * kD; ++i) {
+        const int j = i % d;
+        p.out_scale[i] = ((sign_bits[j >> 5] >> (j & 31)) & 1u) ? -c_d : c_d;
+    }
     for (int values = 0; values < 2; ++values) {
         p.X = values ? c.V : c.K;
         p.codes = values ? c.vcodes : c.kcodes;
@@ -434,7 +440,7 @@ tq_status compress_other_dims(const tq_segment_layout *layout, const tq_rotation
     if (stride_t < d || stride_h < 0 || stride_b < 0 || (stride_t % 8) || (stride_h % 8) || (stride_b % 8))
         return TQ_ERR_ALIGN;
     if (n_tokens == 0) return TQ_OK;
-    if (d == 2 * kD || d == 4 * kD) {  // one thread per 128-dim slice
+    if (d == kD / 2 || d == 2 * kD || d == 4 * kD) {  // one thread per 128-dim slice (or per token pair)
         CompressParams c;
         std::memset(&c, 0, sizeof(c));
         c.K = static_cast<const uint16_t *>(K);

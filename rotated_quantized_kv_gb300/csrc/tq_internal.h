@@ -73,6 +73,7 @@ struct RowsParams {
     int n_heads;                 // heads of this launch (all of one width)
     uint8_t head[kMaxH];         // their indices
     int nh;                      // 128-dim slices per vector (head_dim / 128: 1, 2 or 4)
+    int np;                      // tokens per thread (2 at head_dim 64, else 1)
     uint32_t in_mask[kRowsMaxD / 2];  // word i: the input sign bits of coordinates 2i (bit 15), 2i + 1 (bit 31)
     float out_scale[kRowsMaxD];  // coordinate i: -binary32(1/sqrt(d)) if D_i = -1, else +
     float thr[255];              // values: the width's thresholds, ascending
@@ -83,6 +84,7 @@ struct RowsParams {
 cudaError_t launch_compress_rows(const RowsParams &p, int bits, bool values, cudaStream_t s);
 cudaError_t launch_compress_rows_nh2(const RowsParams &p, int bits, bool values, cudaStream_t s);
 cudaError_t launch_compress_rows_nh4(const RowsParams &p, int bits, bool values, cudaStream_t s);
+cudaError_t launch_compress_rows_np2(const RowsParams &p, int bits, bool values, cudaStream_t s);
 
 // ----------------------------------------------------------------- dequantize
 struct DequantParams {

@@ -58,6 +58,26 @@ def test_compress_bit_exact_other_dims(tq, d):
     assert np.array_equal(g.vscale.cpu().numpy().view(np.uint32), oseg.vscale.view(np.uint32))
 
 
+@pytest.mark.parametrize("t_begin,T", [(0, 45), (4, 46), (2, 1), (0, 600)])
+def test_compress_bit_exact_token_pairs(tq, t_begin, T):
+    # head_dim 64 from an even position: two tokens per thread (an odd count
+    # leaves the last token unpaired); odd positions take the team kernel
+    d, B, H = 64, 2, 4
+    cap = ((t_begin + T + 15) // 16) * 16
+    kb, vb = [1, 3, 4, 8], [2, 3, 5, 7]
+    K, V = _kv(B, H, T, d, seed=T + t_begin)
+    sign = O.signs(d, 44)
+    oseg = O.PackedSegment(B, H, d, cap, kb, vb)
+    O.compress(oseg, K.numpy().view(np.uint16), V.numpy().view(np.uint16), sign, t_begin=t_begin)
+    g = tq.PackedSegment(tq.make_layout(B, H, d, cap, kb, vb))
+    tq.tq_compress(g, tq.tq_make_rotation(d, 44), K.cuda(), V.cuda(), t_begin=t_begin)
+    torch.cuda.synchronize()
+    assert np.array_equal(g.kcodes.cpu().numpy(), oseg.kcodes)
+    assert np.array_equal(g.vcodes.cpu().numpy(), oseg.vcodes)
+    assert np.array_equal(g.kscale.cpu().numpy().view(np.uint32), oseg.kscale.view(np.uint32))
+    assert np.array_equal(g.vscale.cpu().numpy().view(np.uint32), oseg.vscale.view(np.uint32))
+
+
 @pytest.mark.parametrize("d", [16, 64, 256, 1024])
 def test_compress_edge_vectors_other_dims(tq, d):
     # zeros, one-hot and fp16 extremes: the scale-0 and clamp paths
