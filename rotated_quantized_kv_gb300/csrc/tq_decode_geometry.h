@@ -7,7 +7,7 @@
 namespace tqk {
 
 // Stage geometry of a packed split-K class, chosen by the bytes a token-head
-// carries.  Light classes (<= 112 B: K3V3 and narrower at head_dim 128) do
+// carries.  Light classes (<= 144 B: K4V4 and narrower at head_dim 128) do
 // little work per token, so the per-stage costs (the CTA barrier, the copy
 // issue, the cursor) weigh more: they run 256-token stages (512 at <= 64 B:
 // K2V1, K1V2, ...) at 3 resident CTAs per SM.  Heavier classes run 128-token
@@ -24,7 +24,7 @@ __host__ __device__ constexpr int packed_token_bytes(int kb, int vb, bool qjl, i
     return 16 * nh * (kb + vb) + 8 + (qjl ? 20 : 0);
 }
 __host__ __device__ constexpr bool packed_light(int kb, int vb, bool qjl, int nh = 1) {
-    return packed_token_bytes(kb, vb, qjl, nh) <= 112;
+    return packed_token_bytes(kb, vb, qjl, nh) <= 144;
 }
 //
 // np = 2 (head_dim 64): a tile row is a pair of tokens read as one 128-dim
