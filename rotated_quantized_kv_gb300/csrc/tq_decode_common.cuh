@@ -2,6 +2,8 @@
 // kernels (split-K over packed and fp16 segments, prep, combine).
 #pragma once
 
+#include <utility>
+
 #include <cuda_fp16.h>
 
 #include "tq_internal.h"
@@ -55,6 +57,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// The same copy with an L2 eviction policy (policy_evict_first: read once,
+// streamed), so that a stream much larger than L2 does not push out the small
+// working set that is read again (partial records, queries).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, unsigned bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
@@ -383,6 +401,147 @@ __device__ __forceinline__ void write_warp_partial_pair2(WarpState &st, float *r
             }
         }
     }
+}
+
+// Spills.  A warp's running state (m, l, sums) is folded into its partial
+// record every few dozen tiles and restarted from zero sums, so that no sum the
+// tensor cores accumulate runs long: mma.sync adds its products to the fp32
+// accumulator with truncation, which over ~1000 tiles of one warp drifts by
+// ~1e-3 of the result, while the folds below round to nearest.  The first
+// spill of a group writes the record (write_warp_partial_pair*), whose max
+// m_ref then stays: later spills add the state times f = 2^(m - m_ref) >= 1
+// (m never decreases within a group) with fire-and-forget vector atomic adds
+// (fold_warp_partial).  Should m outgrow m_ref by more than 2^64 (a score
+// range that could overflow the scaled sums), merge_warp_partial rescales the
+// record to the state's max instead.  Both follow the column ownership of
+// write_warp_partial_pair (NP = 1) and write_warp_partial_pair2 (NP = 2): the
+// 16 accumulator rows of lane (g, c) are, for every value decoder VD, the dims
+// [16 g, 16 g + 16) of its heads' records in the order VD::dim, so each head
+// takes four 16-byte accesses.  fin is linear in (acc, W).
+template <int NP>
+struct PairColumns {
+    int h[2];     // heads of the lane's accumulator columns 2c, 2c+1
+    bool wr[2];   // whether the lane writes them
+    bool odd;     // token pairs: the columns hold the odd half
+    __device__ __forceinline__ PairColumns(int gqa) {
+        const int g = (threadIdx.x & 31) >> 2, c = threadIdx.x & 3;
+        odd = NP == 2 && (c >> 1) != 0;
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            h[e] = NP == 2 ? (2 * c + e) & 3 : 2 * c + e;
+            wr[e] = h[e] < gqa && (NP == 1 || (g >= 4) == odd);
+        }
+    }
+};
+
+// 2 mt + r of the accumulator row that holds dim d of the lane's 16
+template <typename VD>
+__host__ __device__ constexpr int acc_row_of_dim(int d) {
+    for (int mt = 0; mt < 8; mt++)
+        for (int r = 0; r < 2; r++)
+            if (VD::dim(mt, r) == d) return 2 * mt + r;
+    return -1;
+}
+template <typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F &&f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+    static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
+// the lane's 16 finished sums of column e, in dim order
+template <typename VD, typename Fin>
+__device__ __forceinline__ void lane_rows(const WarpState &st, int e, float Wh, Fin fin, float (&v)[16]) {
+    static_for<16>([&](auto D) {
+        constexpr int s = acc_row_of_dim<VD>(decltype(D)::value);
+        static_assert(s >= 0, "VD::dim: a permutation of 0..15");
+        v[decltype(D)::value] = fin(s >> 1, s & 1, st.acc[s >> 1][2 * (s & 1) + e], Wh);
+    });
+}
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// f: head c's factor on lane c
+template <int NP, typename VD, typename Fin>
+__device__ __forceinline__ void fold_warp_partial(WarpState &st, float *rec_base, int gqa, Fin fin, float f) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const PairColumns<NP> pc(gqa);
+    const float l = warp_sum_g(st.l);
+    const float We = warp_sum_g(st.wsum);
+    const float Wo = NP == 2 ? warp_sum_g(st.wsum_odd) : 0.f;
+    if (c < gqa && g == 0) atomicAdd(rec_base + c * kPartStride + 1, l * f);
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int src = (lane & ~3) | ((2 * c + e) & 3);
+        const float fh = __shfl_sync(0xffffffffu, f, src);
+        const float Wse = __shfl_sync(0xffffffffu, We, src), Wso = __shfl_sync(0xffffffffu, Wo, src);
+        const float Wh = pc.odd ? Wso : Wse;
+        if (pc.wr[e]) {
+            float v[16];
+            lane_rows<VD>(st, e, Wh, fin, v);
+            float *row = rec_base + pc.h[e] * kPartStride + 4 + 16 * g;
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                red_add_v4(row + 4 * j, v[4 * j] * fh, v[4 * j + 1] * fh, v[4 * j + 2] * fh, v[4 * j + 3] * fh);
+        }
+    }
+}
+
+// With M = max(m of the record, m of the state): record = record 2^(m_rec -
+// M) + state 2^(m - M), for m, l and every summed dimension.  The record is
+// read as it stands in L2 (earlier folds were atomic adds there).
+template <int NP, typename VD, typename Fin>
+__device__ __forceinline__ void merge_warp_partial(WarpState &st, float *rec_base, int gqa, Fin fin) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const PairColumns<NP> pc(gqa);
+    float mp = kNegInf, lp = 0.f;
+    if (c < gqa) {
+        mp = __ldcg(rec_base + c * kPartStride);
+        lp = __ldcg(rec_base + c * kPartStride + 1);
+    }
+    const float l = warp_sum_g(st.l);
+    const float We = warp_sum_g(st.wsum);
+    const float Wo = NP == 2 ? warp_sum_g(st.wsum_odd) : 0.f;
+    const float M = fmaxf(mp, st.m);
+    const float fp = M == kNegInf ? 0.f : ex2(mp - M), fn = M == kNegInf ? 0.f : ex2(st.m - M);
+    __syncwarp();  // every lane has read the record's m and l before they are rewritten
+    if (c < gqa && g == 0) {
+        rec_base[c * kPartStride] = M;
+        rec_base[c * kPartStride + 1] = lp * fp + l * fn;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int src = (lane & ~3) | ((2 * c + e) & 3);
+        const float fph = __shfl_sync(0xffffffffu, fp, src), fnh = __shfl_sync(0xffffffffu, fn, src);
+        const float Wse = __shfl_sync(0xffffffffu, We, src), Wso = __shfl_sync(0xffffffffu, Wo, src);
+        const float Wh = pc.odd ? Wso : Wse;
+        if (pc.wr[e]) {
+            float4 *row = reinterpret_cast<float4 *>(rec_base + pc.h[e] * kPartStride + 4 + 16 * g);
+            float4 o[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) o[j] = __ldcg(row + j);
+            float v[16];
+            lane_rows<VD>(st, e, Wh, fin, v);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                row[j] = make_float4(o[j].x * fph + v[4 * j] * fnh, o[j].y * fph + v[4 * j + 1] * fnh,
+                                     o[j].z * fph + v[4 * j + 2] * fnh, o[j].w * fph + v[4 * j + 3] * fnh);
+        }
+    }
+}
+
+// After a spill the state restarts from zero sums, keeping its reference max.
+__device__ __forceinline__ void restart_sums(WarpState &st) {
+    st.l = 0.f;
+    st.wsum = 0.f;
+    st.wsum_odd = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+        for (int q = 0; q < 4; q++) st.acc[mt][q] = 0.f;
 }
 
 // Merge the four warps' states through shared memory and write the CTA's

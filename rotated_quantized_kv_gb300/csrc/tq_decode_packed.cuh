@@ -632,13 +632,15 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
         const unsigned total = nk + nv + 2 * ns + (QJL ? n * 16 + ns : 0);
         fence_proxy_async();
         mbar_expect_tx(bar, total);
-        bulk_g2s(dst, lc.kc + static_cast<size_t>(t0) * G::RK, nk, bar);
-        bulk_g2s(dst + G::offV, lc.vc + static_cast<size_t>(t0) * G::RV, nv, bar);
-        bulk_g2s(dst + G::offKS, lc.ks + t0, ns, bar);
-        bulk_g2s(dst + G::offVS, lc.vs + t0, ns, bar);
+        // the cache streams through L2 once: evict it first
+        const uint64_t pol = policy_evict_first();
+        bulk_g2s_hint(dst, lc.kc + static_cast<size_t>(t0) * G::RK, nk, bar, pol);
+        bulk_g2s_hint(dst + G::offV, lc.vc + static_cast<size_t>(t0) * G::RV, nv, bar, pol);
+        bulk_g2s_hint(dst + G::offKS, lc.ks + t0, ns, bar, pol);
+        bulk_g2s_hint(dst + G::offVS, lc.vs + t0, ns, bar, pol);
         if constexpr (QJL) {
-            bulk_g2s(dst + G::offQS, lc.qs + static_cast<size_t>(t0) * 16, n * 16, bar);
-            bulk_g2s(dst + G::offQN, lc.qn + t0, ns, bar);
+            bulk_g2s_hint(dst + G::offQS, lc.qs + static_cast<size_t>(t0) * 16, n * 16, bar, pol);
+            bulk_g2s_hint(dst + G::offQN, lc.qn + t0, ns, bar, pol);
         }
         // rebind only if another stage follows in this CTA's range
         lc.advance(ws.items, B, --loads_left > 0);
@@ -651,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
     // ---- consumer
     StageCursor<QJL, false> cc;
     cc.locate(ws.items, cta_item[blockIdx.x], s_begin);
-    int g_layer = 0, g_head = 0, g_b = 0, g_item = 0;
-    long long g_stage0 = 0;  // class stage index of the group's first stage
+    int g_layer = 0, g_head = 0, g_b = 0;
+    int g_slot = 0;  // the warp's partial-record slot of the group
     uint32_t bq[16], bt[16];
     float qsum = 0.f, tsum = 0.f, aq = 0.f;
     WarpState st;
@@ -668,33 +670,45 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
     const uint32_t nmask = (NP == 2 && c >= 2) ? 0x80008000u : 0u;  // token pairs: the odd half's sign
 
     int xpar = 0;  // exchange buffer of the warp's next block (NH > 1)
-    // each warp writes its own partial of the current group; then the group's
-    // CTA-level count (and possibly the merge)
-    auto flush = [&]() {
-        const long long gr = static_cast<long long>(g_item) * B + g_b;
-        const int slot = ws.grp_part[gr] +
-                         kDecodeWarps * static_cast<int>(blockIdx.x - cta_of_stage(g_stage0, S, gridDim.x)) + warp;
+    // spilled: the warp's record of the current group holds an earlier part of
+    // it, relative to the max m_ref (of head c, on lane c)
+    bool spilled = false;
+    float m_ref = 0.f;
+    // the warp's state into its record slot of the current group: written at
+    // the group's first spill or flush, folded in at later ones
+    auto write_record = [&]() {
         auto dim_of = [g](int mt, int r) { return 16 * g + VD::dim(mt, r); };
         auto fin = [c1](int mt, int r, float acc, float W) {
             if constexpr (VD::kLinear) return c1 * (2.0f * acc * VDec<1, 7>::unscale(mt, r) - W);
             else return acc;
         };
-        float *rec = ws.part + static_cast<size_t>(slot) * (kMaxGqa * kPartStride);
-        if constexpr (NP == 2) write_warp_partial_pair2(st, rec, gqa, dim_of, fin);
-        else write_warp_partial_pair(st, rec, gqa, dim_of, fin);
-        finish_and_combine<NH, NP>(dims, ws, g_layer, g_b, g_head, flag);
+        float *rec = ws.part + static_cast<size_t>(g_slot) * (kMaxGqa * kPartStride);
+        const float dm = st.m - m_ref;
+        if (!spilled) {
+            if constexpr (NP == 2) write_warp_partial_pair2(st, rec, gqa, dim_of, fin);
+            else write_warp_partial_pair(st, rec, gqa, dim_of, fin);
+        } else if (__any_sync(0xffffffffu, c < gqa && !(dm <= 64.f))) {
+            merge_warp_partial<NP, VD>(st, rec, gqa, fin);
+        } else {
+            fold_warp_partial<NP, VD>(st, rec, gqa, fin, ex2(dm));
+            return;
+        }
+        m_ref = st.m;
     };
     // a new group: its identity and the B fragments of its rotated queries
     // (column g: head g/2, part g&1), each head divided by a power of two 2^e
     // that brings its largest coordinate into [0.5, 1)
     auto start_group = [&]() {
         const WorkItem &it = ws.items[cc.item];
-        g_item = cc.item;
         g_b = cc.b;
         g_layer = it.layer;
         g_head = it.head;
-        g_stage0 = it.stage_begin + static_cast<long long>(cc.b) * it.n_stages;
+        // the group's CTAs write consecutive slots of kDecodeWarps, by CTA
+        const long long stage0 = it.stage_begin + static_cast<long long>(cc.b) * it.n_stages;
+        g_slot = ws.grp_part[static_cast<long long>(cc.item) * B + cc.b] +
+                 kDecodeWarps * static_cast<int>(blockIdx.x - cta_of_stage(stage0, S, gridDim.x)) + warp;
         init_state(st);
+        spilled = false;
         const size_t qbase = (static_cast<size_t>(g_layer) * B + g_b) * dims.Hq + g_head * gqa;
         const int head = g >> 1, part = g & 1;
         uint32_t q[16];
@@ -835,24 +849,50 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
     __syncthreads();  // codebook and pair table written
     start_group();
     bool new_group = false;
+    // stages between spills (a power of two): a warp accumulates 16-token
+    // tiles at kPT NH / (16 NP kDecodeWarps) per stage, 64 between spills
+    constexpr int kSpill = (64 * 16 * NP * kDecodeWarps) / (kPT * NH) > 0 ? (64 * 16 * NP * kDecodeWarps) / (kPT * NH) : 1;
+    static_assert((kSpill & (kSpill - 1)) == 0, "spill cadence: a power of two");
 
-    for (int k = 0; k < n_st; k++) {
-        const bool arrived = mbar_wait(&full[k % NS], (k / NS) & 1, dims.wait_polls);
-        // all warps are past stage k-1 (its buffer is free) and agree on errors
-        if (__syncthreads_or(!arrived)) {
-            if (threadIdx.x == 0) {
-                atomicExch(ws.error, 1);
-                // let the copies still in flight land before the CTA's shared
-                // memory goes away (always with the full bound)
-                for (int j = k; j < n_st && j < k + NS - 1; j++) mbar_wait(&full[j % NS], (j / NS) & 1);
+    // one pass per stage, and a last one (k = n_st) for the final merge
+    for (int k = 0;; k++) {
+        const bool last = k == n_st;
+        if (!last) {
+            const bool arrived = mbar_wait(&full[k % NS], (k / NS) & 1, dims.wait_polls);
+            // all warps are past stage k-1 (its buffer is free) and agree on errors
+            if (__syncthreads_or(!arrived)) {
+                if (threadIdx.x == 0) {
+                    atomicExch(ws.error, 1);
+                    // let the copies still in flight land before the CTA's shared
+                    // memory goes away (always with the full bound)
+                    for (int j = k; j < n_st && j < k + NS - 1; j++) mbar_wait(&full[j % NS], (j / NS) & 1);
+                }
+                __syncthreads();
+                return;
             }
-            __syncthreads();
-            return;
+            if (threadIdx.x == 0 && k + NS - 1 < n_st) load_next(k + NS - 1);
+        } else {
+            // every thread waits for the previous grid of the call before its
+            // last merge, so that this grid's completion implies that of all
+            // earlier ones
+            pdl_wait();
         }
-        if (threadIdx.x == 0 && k + NS - 1 < n_st) load_next(k + NS - 1);
-        if (new_group) {
-            flush();
-            start_group();
+        // the one place where the warps' states leave their registers: at the
+        // end of a group or of the range (flush), and every kSpill stages of
+        // the range (~64 tiles of each warp) for the group in progress (spill).
+        // CTAs spill at staggered stages, so that the folds of all CTAs do not
+        // meet in L2 at once.
+        const bool spill_due = k > 0 && ((k - 1 + static_cast<int>(blockIdx.x)) & (kSpill - 1)) == kSpill - 1;
+        if (new_group || last || spill_due) {
+            write_record();
+            if (new_group || last) {
+                finish_and_combine<NH, NP>(dims, ws, g_layer, g_b, g_head, flag);
+                if (last) break;
+                start_group();
+            } else {
+                restart_sums(st);
+                spilled = true;
+            }
         }
         const uint8_t *buf = smem + (k % NS) * G::stage;
         const int n = min(kPT, cc.n_tokens - cc.st * kPT);
@@ -866,10 +906,6 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
             else tiles(buf, tA, n, std::false_type{});
         }
     }
-    // every thread waits for the previous grid of the call before its last
-    // merge, so that this grid's completion implies that of all earlier ones
-    pdl_wait();
-    flush();
 }
 
 template <int KB, int VB, bool QJL, int NH = 1, int NP = 1>

@@ -156,7 +156,10 @@ def _sample_positions(n, k=48, seed=0):
 
 
 def _groups(L, B, H):
-    g = {(0, 0, 0), (L - 1, B - 1, H - 1), (L // 2, B // 2, H // 2), (L - 1, 0, 1 % H)}
+    """Sampled (layer, batch element, KV head) groups: the corners and middles
+    of each axis (up to 18), plus two interior points."""
+    g = {(l, b, h) for l in (0, L // 2, L - 1) for b in (0, B - 1) for h in (0, H // 2, H - 1)}
+    g |= {(L // 3, B // 2, 1 % H), ((2 * L) // 3, (B - 1) // 3, (3 * H) // 4)}
     return sorted(g)
 
 
@@ -284,4 +287,55 @@ def test_dense_rotation_workload(lib):
         worst = max(worst, (np.abs(g - ref).max(axis=1) / np.abs(ref).max(axis=1)).max())
     assert worst <= ATTN_TOL, worst
     del m
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("d,T", [(128, 32768), (64, 65536), (256, 16384)])
+def test_decode_scores_growing_along_context(lib, d, T):
+    """Keys whose scores grow by ~560 nats along the context, at 4.2M (d 128,
+    256: 2.1M) cached token-heads of K3V3, enough that every CTA of the
+    split-K decode runs two or more of its fold intervals (64 tiles of each
+    warp) inside one group.  Across one interval (an eighth of the context)
+    the running max grows by ~70 nats, more than the 2^64 that the folds by
+    atomic adds allow, so the folds after a group's first take the rescaling
+    path.  Each group's query heads share one direction u; the keys are
+    N(0, 1) plus 560 (t / T) sqrt(d) u / |u|^2, so the score of token t is
+    ~560 t / T.  Checked like the workloads: sampled records bit-exact, the
+    outputs of sampled groups against the oracle."""
+    import types
+    tq, _ = lib
+    L, B, H, gqa = 2, 8, 8, 4
+    Hq = H * gqa
+    gen = torch.Generator().manual_seed(700 + d)
+    u = torch.randn(L, B, H, d, generator=gen)
+    q = (u.repeat_interleave(gqa, dim=2) + 0.05 * torch.randn(L, B, Hq, d, generator=gen)).half()
+    ramp = 560.0 * torch.arange(T, dtype=torch.float32) / T
+    keep, views, segs = [], [], []
+    for l in range(L):
+        rot = tq.tq_make_rotation(d, 42 + l)
+        dirn = (d ** 0.5) * u[l] / (u[l] * u[l]).sum(-1, keepdim=True)  # [B][H][d]
+        K = (torch.randn(B, H, T, d, generator=gen) + ramp[None, None, :, None] * dirn[:, :, None, :]).half()
+        V = torch.randn(B, H, T, d, generator=gen).half()
+        seg = tq.PackedSegment(tq.make_layout(B, H, d, T, [3] * H, [3] * H))
+        tq.tq_compress(seg, rot, K.cuda(), V.cuda())
+        keep.append(seg)
+        views.append(tq.layer_view(rot, [seg]))
+        si = types.SimpleNamespace(packed=True, seg=seg, n=T, pos0=0)
+        segs.append([si])
+        sign = O.signs(d, 42 + l)
+        for b in (0, B - 1):
+            pos = _sample_positions(T, seed=l * 17 + b)
+            tp = torch.from_numpy(pos)
+            _check_records(si, b, pos, K[b][:, tp].numpy(), V[b][:, tp].numpy(), sign, None)
+        del K, V
+    arr = tq.views_array(views)
+    ws = torch.empty(tq.tq_decode_workspace_size(list(arr), B, H, Hq, d), dtype=torch.uint8, device="cuda")
+    out = torch.empty(L, B, Hq, d, device="cuda")
+    qd = q.cuda()
+    tq.tq_decode_attention(None, qd, out, ws, H, views=arr)
+    assert tq.tq_decode_error_flag(ws) == 0
+    torch.cuda.synchronize()
+    _check_decode(out, qd, _groups(L, B, H), lambda l, b, h: _head_segments(segs[l], b, h, d=d),
+                  lambda l: O.signs(d, 42 + l), None)
+    del keep, views, arr, ws, out
     torch.cuda.empty_cache()
