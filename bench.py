@@ -573,7 +573,7 @@ def decode_point(tq, name, batch, context, K, Wm, world, dev, head_dim=None):
            "bytes_per_step": int(t["total_bytes"] / K), "gpu_launches": t["launches"]}
     if head_dim and head_dim != 128:
         # compression at this head_dim: every layer's packed prompt again, from
-        # one fresh fp16 input per layer position (the generic kernels)
+        # one fresh fp16 input per layer position
         src = W.kv_block(w, 0, m.B, m.T, 1007, device="cuda")
         calls, scr = [], {}
         for l in range(m.L):
@@ -590,7 +590,7 @@ def decode_point(tq, name, batch, context, K, Wm, world, dev, head_dim=None):
         res["compress"] = {"value": round(ctok / (cms * 1e-3) / 1e6, 1), "unit": "Mtok/s",
                            "ms_per_layer": round(cms, 4), "achieved_gbs": round(cbytes / (cms * 1e-3) / 1e9, 1),
                            "frac_of_peak": round(cbytes / (cms * 1e-3) / 1e9 / peak, 4),
-                           "kernel": "gen_compress_kernel"}
+                           "kernel": "compress_rows_kernel" if m.d in (64, 256, 512) else "gen_compress_kernel"}
         del src, calls, scr
     del m
     torch.cuda.synchronize()
