@@ -191,7 +191,6 @@ __global__ void __launch_bounds__(kThreads, NH == 1 && NP == 1 ? 6 : 1)
 template <int NH, int NP = 1>
 __global__ void __launch_bounds__(kThreads)
     decode_prep_kernel(const DecodeDims dims, const DecodeWorkspace ws, const float *S) {
-    __shared__ float qsh[kThreads / 32][kD];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wid = blockIdx.x * (kThreads / 32) + warp;
     pdl_launch_dependents();
@@ -256,17 +255,9 @@ __global__ void __launch_bounds__(kThreads)
     const float qs = store_hilo(ws.qrot + static_cast<size_t>(wid) * kD, xn, lane) / f;
     float ts = 0.f;
     if (lp.has_qjl) {
-#pragma unroll
-        for (int e = 0; e < 4; e++) qsh[warp][4 * lane + e] = x[e];
-        __syncwarp();
+        // t_j = (S q')_j for j = 4 lane + e (coalesced rows of S)
         float t[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const float *row = S + static_cast<size_t>(4 * lane + e) * kD;
-            float acc = 0.f;
-            for (int i = 0; i < kD; i++) acc = fmaf(row[i], qsh[warp][i], acc);
-            t[e] = acc;
-        }
+        warp_matvec(S, x, t, lane);
         if (lp.qjl_mode == TQ_QJL_SIGN_PAIR) {
             // sign-pair estimator: t_j = sqrt(pi/2) ||q'|| sign((S q')_j), so that
             // the kernels' sqrt(pi/2)/jl * rho * <t, s> is (pi/2)/jl ||q'|| rho <sign(S q'), s>

@@ -635,6 +635,37 @@ __device__ __forceinline__ void warp_rotate(float (&x)[4], const uint32_t *sign_
 // Dense rotation of a warp-held vector (lane holds coordinates 4 lane + e):
 // y = Q x (transpose = false) or y = Q^T x, Q row-major d x d.  Each step
 // reads one row of Q with one coalesced 16-byte load per lane.
+// y_e = M[4 lane + e] . x for a 128 x 128 binary32 row-major M (16-byte
+// aligned), x and y held as coordinates 4 lane .. 4 lane + 3 of each lane.
+// Each row is read whole by the warp (a float4 per lane against the lane's
+// four coordinates), so every load is one coalesced 512-byte row; the 32 rows
+// {4 r + e} of block e are then summed across the lanes by recursive halving
+// (step h: a lane keeps the half of its rows selected by its bit h and adds
+// its partner's partials of them), which leaves row 4 L + e on lane L: 31
+// shuffles per 32 rows instead of 5 per row.
+__device__ __forceinline__ void warp_matvec(const float *M, const float (&x)[4], float (&y)[4], int lane) {
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        float pr[32];
+#pragma unroll
+        for (int r = 0; r < 32; r++) {
+            const float4 m = __ldg(reinterpret_cast<const float4 *>(M + static_cast<size_t>(4 * r + e) * kD) + lane);
+            pr[r] = fmaf(m.w, x[3], fmaf(m.z, x[2], fmaf(m.y, x[1], m.x * x[0])));
+        }
+#pragma unroll
+        for (int h = 16; h >= 1; h >>= 1) {
+            const bool up = (lane & h) != 0;
+#pragma unroll
+            for (int r = 0; r < h; r++) {
+                const float send = up ? pr[r] : pr[r + h];
+                const float keep = up ? pr[r + h] : pr[r];
+                pr[r] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+            }
+        }
+        y[e] = pr[0];
+    }
+}
+
 __device__ __forceinline__ void warp_rotate_dense(float (&x)[4], const float *Q, bool transpose, int lane) {
     float y[4] = {0.f, 0.f, 0.f, 0.f};
     if (transpose) {  // y_j = sum_i Q[i][j] x_i
@@ -647,15 +678,8 @@ __device__ __forceinline__ void warp_rotate_dense(float (&x)[4], const float *Q,
             y[2] = fmaf(r.z, xi, y[2]);
             y[3] = fmaf(r.w, xi, y[3]);
         }
-    } else {  // y_j = sum_i Q[j][i] x_i: a warp sum per row
-#pragma unroll 4
-        for (int j = 0; j < kD; j++) {
-            const float4 r = __ldg(reinterpret_cast<const float4 *>(Q + static_cast<size_t>(j) * kD) + lane);
-            float s = fmaf(r.x, x[0], fmaf(r.y, x[1], fmaf(r.z, x[2], r.w * x[3])));
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if ((j >> 2) == lane) y[j & 3] = s;
-        }
+    } else {  // y_j = sum_i Q[j][i] x_i
+        warp_matvec(Q, x, y, lane);
     }
 #pragma unroll
     for (int e = 0; e < 4; e++) x[e] = y[e];
