@@ -107,6 +107,18 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
+__device__ __forceinline__ uint32_t lds32r(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+// #{k : thr_k < u} from the 4-bit table (RowsParams::bucket4)
+__device__ __forceinline__ uint32_t bucket4_code(uint32_t tab, float u) {
+    const uint32_t ub = __float_as_uint(u);
+    const uint32_t e = lds32r(tab + ((ub >> 21) << 2));
+    const uint32_t x = (ub ^ static_cast<uint32_t>(static_cast<int32_t>(ub) >> 31)) & 0x1FFFFFu;
+    return (e >> 21) + ((e & 0x1FFFFFu) < x ? 1u : 0u);
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -193,6 +205,10 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
     for (int i = threadIdx.x; i < 255; i += kThreads) thr[i] = p.thr[i];
     if constexpr (VAL && BITS <= 3)
         for (int i = threadIdx.x; i < kRowsBuckets; i += kThreads) vtab[i] = make_uint2(p.bucket[i].t, p.bucket[i].k);
+    if constexpr (VAL && BITS == 4)
+        if (p.bucket4_ok)
+            for (int i = threadIdx.x; i < kRowsBuckets; i += kThreads)
+                vtab[i] = make_uint2(p.bucket4[2 * i], p.bucket4[2 * i + 1]);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -370,6 +386,15 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                     put<BITS>(w, m + 64, e1.y + (__uint_as_float(e1.x) < u.y ? 1u : 0u));
                 }
             } else if constexpr (BITS == 4) {
+              if (p.bucket4_ok) {
+                const uint32_t tab = static_cast<uint32_t>(__cvta_generic_to_shared(vtab));
+#pragma unroll
+                for (int m = 0; m < 64; m++) {
+                    const float2 u = fmul2(a[m], make_float2(r, rb));
+                    put<BITS>(w, m, bucket4_code(tab, u.x));
+                    put<BITS>(w, m + 64, bucket4_code(tab, u.y));
+                }
+              } else {
                 float th[NT];
 #pragma unroll
                 for (int j = 0; j < NT; j++) th[j] = thr[j];
@@ -393,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
                     put<BITS>(w, m, k0);
                     put<BITS>(w, m + 64, k1);
                 }
+              }
             } else {
 #pragma unroll
                 for (int m = 0; m < 64; m++) {
@@ -437,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 3) compress_rows_kernel(const __grid
 
 template <int BITS, bool VAL, int NH, int NP = 1>
 cudaError_t rows_launch(const RowsParams &p, cudaStream_t s) {
-    constexpr size_t smem = rows_smem_bytes<NH>(VAL && BITS <= 3);
+    constexpr size_t smem = rows_smem_bytes<NH>(VAL && BITS <= 4);
     static bool configured = false;
     if (!configured) {
         const cudaError_t e = cudaFuncSetAttribute(compress_rows_kernel<BITS, VAL, NH, NP>,

@@ -359,6 +359,53 @@ bool value_buckets(const float *thr, int nt, RowsParams::Bucket *out) {
     return true;
 }
 
+// The 4-bit table of compress_rows_kernel (RowsParams::bucket4): buckets of
+// the 11 top bits of u, each holding at most one threshold; false if some
+// bucket holds two (the kernel then searches the thresholds).
+bool value_buckets4(const float *thr, int nt, uint32_t *out) {
+    auto as_float = [](uint32_t b) {
+        float f;
+        std::memcpy(&f, &b, 4);
+        return f;
+    };
+    constexpr uint32_t kLow = (1u << 21) - 1u;
+    const float inf = std::numeric_limits<float>::infinity();
+    for (int i = 0; i < 2 * kRowsBuckets; ++i) {
+        const uint32_t m = static_cast<uint32_t>(i & 1023);
+        const bool neg = i >= 1024;
+        if (m >= 1020) {  // exponent 255: infinities and NaNs, never a quotient of finite inputs
+            out[i] = (static_cast<uint32_t>(neg ? 0 : nt) << 21) | kLow;
+            continue;
+        }
+        const float lo = as_float(m << 21);  // magnitude range [lo, hi)
+        const float hi = (m + 1) << 21 >= 0x7F800000u ? inf : as_float((m + 1) << 21);
+        int k = 0, inside = 0;
+        uint32_t tl = kLow;  // no threshold: [t' < x] never holds
+        for (int j = 0; j < nt; ++j) {
+            const float t = thr[j];
+            bool in;
+            if (!neg) {  // u in [lo, hi)
+                in = !(t < lo) && t < hi;
+                if (t < lo) ++k;
+            } else {  // u in (-hi, -lo]
+                in = !(t <= -hi) && t <= -lo;
+                if (t <= -hi) ++k;
+            }
+            if (in) {
+                // t shares u's top 11 bits, or t = +-0 at lo = 0, whose low bits
+                // (0) give [t < u] all the same
+                uint32_t tb;
+                std::memcpy(&tb, &t, 4);
+                tl = (tb & kLow) ^ (neg ? kLow : 0u);
+                ++inside;
+            }
+        }
+        if (inside > 1) return false;
+        out[i] = (static_cast<uint32_t>(k) << 21) | tl;
+    }
+    return true;
+}
+
 // Launches of the one-thread-per-slice kernels for the heads c.sel[0..n_sel)
 // (none of them sketched) at head_dim d = 128, 256 or 512 (sign_bits: the
 // rotation's d bits; c supplies the pointers, strides and widths): the keys of
@@ -418,6 +465,7 @@ cudaError_t launch_rows(const CompressParams &c, const tq_segment_layout *layout
                 const FittedCodebook &cb = fit(bits, layout->value_law);
                 for (int k = 0; k + 1 < (1 << bits); ++k) p.thr[k] = static_cast<float>(cb.bound[k]);
                 if (bits <= 3 && !value_buckets(p.thr, (1 << bits) - 1, p.bucket)) return cudaErrorNotSupported;
+                p.bucket4_ok = bits == 4 && value_buckets4(p.thr, 15, p.bucket4) ? 1 : 0;
             }
             const cudaError_t e = launch_compress_rows(p, bits, values != 0, s);
             if (e != cudaSuccess) return e;

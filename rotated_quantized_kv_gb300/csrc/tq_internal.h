@@ -78,8 +78,18 @@ struct RowsParams {
     float out_scale[kRowsMaxD];  // coordinate i: -binary32(1/sqrt(d)) if D_i = -1, else +
     float thr[255];              // values: the width's thresholds, ascending
     // values of <= 3 bits: bucket b = (bit pattern of u) >> 22 holds k_base and
-    // the bucket's one threshold t_c (+inf if none) as bits: code = k_base + [t_c < u]
-    struct Bucket { uint32_t t, k; } bucket[kRowsBuckets];
+    // the bucket's one threshold t_c (+inf if none) as bits: code = k_base + [t_c < u].
+    // 4 bits (bucket4_ok): bucket b = (bit pattern of u) >> 21 (sign, exponent,
+    // two mantissa bits) holds k_base << 21 | t', t' the low 21 bits of the
+    // bucket's one threshold, complemented in negative buckets (2^21 - 1 if
+    // none): code = k_base + [t' < x], x the low 21 bits of u, complemented if
+    // u < 0 (both share u's top 11 bits, so that this is [t_c < u])
+    struct Bucket { uint32_t t, k; };
+    union {
+        Bucket bucket[kRowsBuckets];
+        uint32_t bucket4[2 * kRowsBuckets];
+    };
+    int bucket4_ok;
 };
 cudaError_t launch_compress_rows(const RowsParams &p, int bits, bool values, cudaStream_t s);
 cudaError_t launch_compress_rows_nh2(const RowsParams &p, int bits, bool values, cudaStream_t s);
