@@ -290,12 +290,12 @@ def test_dense_rotation_workload(lib):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("d,T", [(128, 32768), (64, 65536), (256, 16384)])
+@pytest.mark.parametrize("d,T", [(128, 32768), (64, 65536), (256, 16384), (512, 8192)])
 def test_decode_scores_growing_along_context(lib, d, T):
-    """Keys whose scores grow by ~560 nats along the context, at 4.2M (d 128,
-    256: 2.1M) cached token-heads of K3V3, enough that every CTA of the
-    split-K decode runs two or more of its fold intervals (64 tiles of each
-    warp) inside one group.  Across one interval (an eighth of the context)
+    """Keys whose scores grow by ~560 nats along the context, at 4.2M (d 128),
+    8.4M (d 64), 2.1M (d 256) or 1.05M (d 512) cached token-heads of K3V3, enough
+    that every CTA of the split-K decode runs two or more of its fold
+    intervals (64 tiles of each warp) inside one group.  Across one interval (an eighth of the context)
     the running max grows by ~70 nats, more than the 2^64 that the folds by
     atomic adds allow, so the folds after a group's first take the rescaling
     path.  Each group's query heads share one direction u; the keys are
