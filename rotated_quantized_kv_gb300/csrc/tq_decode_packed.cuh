@@ -657,6 +657,11 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
     int g_slot = 0;  // the warp's partial-record slot of the group
     uint32_t bq[16], bt[16];
     float qsum = 0.f, tsum = 0.f, aq = 0.f;
+    // classes with the 168-register budget (3 CTAs per SM) fold the score
+    // scale into the group's constants (aq and beta qsum times the scale), one
+    // multiply less per score; the 128-register classes keep it apart
+    constexpr bool kFoldScale = G::CTAS == 3;
+    float aqs = 0.f, bqs = 0.f;
     WarpState st;
     int *flag = reinterpret_cast<int *>(smem + G::flag);
     // raw = (q / 2^e) . code * 2^(kA - 24) and q . yhat = m (alpha q.code + beta sum q)
@@ -739,6 +744,10 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
             qsum = c < gqa ? ws.qsum[(qbase + c) * 4] : 0.f;
             aq = c < gqa ? alphaA * ws.qsum[(qbase + c) * 4 + 2] : 0.f;
         }
+        if constexpr (kFoldScale) {
+            aqs = aq * qk_scale;
+            bqs = beta * qsum * qk_scale;
+        }
     };
     // the warp's two 16-token tiles: tokens [tA, tA + 32) of the stage buffer
     auto tiles = [&](const uint8_t *buf, int tA, int n, auto full_tag) {
@@ -795,8 +804,13 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
 #pragma unroll
             for (int t = 0; t < 2; t++) {
                 const int t0 = tA + 16 * t;
-                sc[2 * t] = kss[t0 + g] * (aq * raw[2 * t] + beta * qsum) * qk_scale;
-                sc[2 * t + 1] = kss[t0 + g + 8] * (aq * raw[2 * t + 1] + beta * qsum) * qk_scale;
+                if constexpr (kFoldScale) {
+                    sc[2 * t] = kss[t0 + g] * (aqs * raw[2 * t] + bqs);
+                    sc[2 * t + 1] = kss[t0 + g + 8] * (aqs * raw[2 * t + 1] + bqs);
+                } else {
+                    sc[2 * t] = kss[t0 + g] * (aq * raw[2 * t] + beta * qsum) * qk_scale;
+                    sc[2 * t + 1] = kss[t0 + g + 8] * (aq * raw[2 * t + 1] + beta * qsum) * qk_scale;
+                }
             }
         } else {
 #pragma unroll
@@ -804,19 +818,26 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
             const int t0 = tA + 16 * t;
             float raw0, raw1;
             qk_raw<KU, KB>(buf + t0 * G::RK + koff, buf + (t0 + 8) * G::RK + koff, bq, raw0, raw1);
-            float s0 = kss[t0 + g] * (aq * raw0 + beta * qsum);
-            float s1 = kss[t0 + g + 8] * (aq * raw1 + beta * qsum);
+            float s0, s1;
+            if constexpr (kFoldScale) {
+                s0 = kss[t0 + g] * (aqs * raw0 + bqs);
+                s1 = kss[t0 + g + 8] * (aqs * raw1 + bqs);
+            } else {
+                s0 = kss[t0 + g] * (aq * raw0 + beta * qsum);
+                s1 = kss[t0 + g + 8] * (aq * raw1 + beta * qsum);
+            }
             if constexpr (QJL) {
                 const float *qns = reinterpret_cast<const float *>(buf + G::offQN);
                 float r0, r1;
                 qk_raw<SignUnpack, 1>(buf + G::offQS + (t0 + g) * 16 + 4 * c,
                                       buf + G::offQS + (t0 + g + 8) * 16 + 4 * c, bt, r0, r1);
                 constexpr float gam = 1.2533141373155003f / kJl;  // sqrt(pi/2) / jl
-                s0 += gam * qns[t0 + g] * (33554432.0f * r0 - tsum);
-                s1 += gam * qns[t0 + g + 8] * (33554432.0f * r1 - tsum);
+                const float gqs = kFoldScale ? gam * qk_scale : gam;
+                s0 += gqs * qns[t0 + g] * (33554432.0f * r0 - tsum);
+                s1 += gqs * qns[t0 + g + 8] * (33554432.0f * r1 - tsum);
             }
-            sc[2 * t] = s0 * qk_scale;
-            sc[2 * t + 1] = s1 * qk_scale;
+            sc[2 * t] = kFoldScale ? s0 : s0 * qk_scale;
+            sc[2 * t + 1] = kFoldScale ? s1 : s1 * qk_scale;
         }
         }
         bool okv[4];
@@ -881,9 +902,10 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
         // end of a group or of the range (flush), and every kSpill stages of
         // the range (~64 tiles of each warp) for the group in progress (spill).
         // CTAs spill at staggered stages, so that the folds of all CTAs do not
-        // meet in L2 at once.
+        // meet in L2 at once.  (Rare: marked unlikely, so that this code stays
+        // off the loop's straight path.)
         const bool spill_due = k > 0 && ((k - 1 + static_cast<int>(blockIdx.x)) & (kSpill - 1)) == kSpill - 1;
-        if (new_group || last || spill_due) {
+        if (__builtin_expect(new_group || last || spill_due, 0)) {
             write_record();
             if (new_group || last) {
                 finish_and_combine<NH, NP>(dims, ws, g_layer, g_b, g_head, flag);
