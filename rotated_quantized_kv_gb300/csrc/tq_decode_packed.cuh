@@ -189,7 +189,7 @@ __device__ __forceinline__ void lds_words(uint32_t (&w)[NW], const uint8_t *p) {
 }
 
 // Raw Q.K of tokens g and g+8 for head c (units of 2^(KU::kA - 24) code units).
-template <typename KU, int NW>
+template <typename KU, int NW, bool TWO = true>
 __device__ __forceinline__ void qk_raw(const uint8_t *rec0, const uint8_t *rec1, const uint32_t (&bq)[16],
                                        float &raw0, float &raw1) {
     uint32_t w0[NW], w1[NW], a0[16], a1[16];
@@ -197,15 +197,24 @@ __device__ __forceinline__ void qk_raw(const uint8_t *rec0, const uint8_t *rec1,
     lds_words(w1, rec1);
     KU::run(w0, a0);
     KU::run(w1, a1);
-    float e[4] = {0.f, 0.f, 0.f, 0.f}, o[4] = {0.f, 0.f, 0.f, 0.f};  // two chains for ILP
+    if constexpr (TWO) {  // two chains for ILP
+        float e[4] = {0.f, 0.f, 0.f, 0.f}, o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int kk = 0; kk < 8; kk += 2) {
-        mma16816(e, a0[2 * kk], a1[2 * kk], a0[2 * kk + 1], a1[2 * kk + 1], bq[2 * kk], bq[2 * kk + 1]);
-        mma16816(o, a0[2 * kk + 2], a1[2 * kk + 2], a0[2 * kk + 3], a1[2 * kk + 3], bq[2 * kk + 2],
-                 bq[2 * kk + 3]);
+        for (int kk = 0; kk < 8; kk += 2) {
+            mma16816(e, a0[2 * kk], a1[2 * kk], a0[2 * kk + 1], a1[2 * kk + 1], bq[2 * kk], bq[2 * kk + 1]);
+            mma16816(o, a0[2 * kk + 2], a1[2 * kk + 2], a0[2 * kk + 3], a1[2 * kk + 3], bq[2 * kk + 2],
+                     bq[2 * kk + 3]);
+        }
+        raw0 = (e[0] + e[1]) + (o[0] + o[1]);
+        raw1 = (e[2] + e[3]) + (o[2] + o[3]);
+    } else {  // one chain: two adds less per tile row pair
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+            mma16816(e, a0[2 * kk], a1[2 * kk], a0[2 * kk + 1], a1[2 * kk + 1], bq[2 * kk], bq[2 * kk + 1]);
+        raw0 = e[0] + e[1];
+        raw1 = e[2] + e[3];
     }
-    raw0 = (e[0] + e[1]) + (o[0] + o[1]);
-    raw1 = (e[2] + e[3]) + (o[2] + o[3]);
 }
 
 // Token pairs (head_dim 64): rows g, g+8 are virtual records (2 v, 2 v + 1);
@@ -659,7 +668,9 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
     float qsum = 0.f, tsum = 0.f, aq = 0.f;
     // classes with the 168-register budget (3 CTAs per SM) fold the score
     // scale into the group's constants (aq and beta qsum times the scale), one
-    // multiply less per score; the 128-register classes keep it apart
+    // multiply less per score, and sum Q.K in one mma chain (two adds less per
+    // pair of tile rows); the 128-register classes keep both apart (their
+    // registers spill otherwise)
     constexpr bool kFoldScale = G::CTAS == 3;
     float aqs = 0.f, bqs = 0.f;
     WarpState st;
@@ -785,8 +796,9 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
             // this sub-record's raw Q.K of tokens g, g+8 of both tiles, summed
             // over the NH sub-records in the order 0..NH-1 by every warp
             float r[4];
-            qk_raw<KU, KB>(buf + tA * G::RK + koff, buf + (tA + 8) * G::RK + koff, bq, r[0], r[1]);
-            qk_raw<KU, KB>(buf + (tA + 16) * G::RK + koff, buf + (tA + 24) * G::RK + koff, bq, r[2], r[3]);
+            qk_raw<KU, KB, !kFoldScale>(buf + tA * G::RK + koff, buf + (tA + 8) * G::RK + koff, bq, r[0], r[1]);
+            qk_raw<KU, KB, !kFoldScale>(buf + (tA + 16) * G::RK + koff, buf + (tA + 24) * G::RK + koff, bq, r[2],
+                                        r[3]);
             float4 *xb = reinterpret_cast<float4 *>(smem + G::xch) + xpar * kThreads + (warp - sub) * 32 + lane;
             xb[sub * 32] = make_float4(r[0], r[1], r[2], r[3]);
             named_barrier(1 + warp / NH, 32 * NH);
@@ -817,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, packed_ctas_per_sm(KB, VB, QJL, NH, 
         for (int t = 0; t < 2; t++) {
             const int t0 = tA + 16 * t;
             float raw0, raw1;
-            qk_raw<KU, KB>(buf + t0 * G::RK + koff, buf + (t0 + 8) * G::RK + koff, bq, raw0, raw1);
+            qk_raw<KU, KB, !kFoldScale>(buf + t0 * G::RK + koff, buf + (t0 + 8) * G::RK + koff, bq, raw0, raw1);
             float s0, s1;
             if constexpr (kFoldScale) {
                 s0 = kss[t0 + g] * (aqs * raw0 + bqs);
