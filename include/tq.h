@@ -120,6 +120,23 @@ tq_status tq_fit_codebook(int bits, float *centroids, float *thresholds);
  * (head_dim 128 fits are kept for the process). */
 tq_status tq_fit_codebook_sphere(int bits, int head_dim, float *centroids, float *thresholds);
 
+/* The value-code lookup table that the one-thread-per-vector compressor uses
+ * for a width of 1-4 bits and an ascending threshold set (host; for
+ * inspection and tests).  The code of a quotient u is #{j : thresholds[j] < u};
+ * the table gives it from u's binary32 bit pattern p:
+ *   bits 1-3: entry i = (table[2i], table[2i + 1]) = (t, k) for p >> 22 = i
+ *     (sign, exponent, one mantissa bit): k thresholds lie below every u of
+ *     the bucket and t is the bit pattern of the bucket's one threshold (+inf
+ *     if none): code = k + [t < u];
+ *   bits 4: entry i = table[i] = k << 21 | t' for p >> 21 = i (two mantissa
+ *     bits): t' the low 21 bits of the bucket's threshold, complemented in
+ *     buckets of negative u (2^21 - 1 if none): code = k + [t' < x], x the low
+ *     21 bits of p, complemented if u < 0.
+ * table: 2048 uint32 (host).  TQ_ERR_ARG for bits outside 1..4 or NULL
+ * pointers; TQ_ERR_UNSUPPORTED when a bucket holds two thresholds (the
+ * compressor then searches the thresholds instead). */
+tq_status tq_value_code_table(int bits, const float *thresholds, uint32_t *table);
+
 /* ------------------------------------------------------------------------ */
 /* QJL projection ("TurboMOQ", "QJL residual correction (sub-2-bit)":          */
 /* QJLConfig(head_dim, jl_dim); "turboquant-mlx", "RaBitQ vs QJL correction").  */

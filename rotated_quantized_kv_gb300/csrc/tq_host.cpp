@@ -1048,6 +1048,19 @@ tq_status tq_fit_codebook_sphere(int bits, int head_dim, float *centroids, float
     return TQ_OK;
 }
 
+tq_status tq_value_code_table(int bits, const float *thresholds, uint32_t *table) {
+    if (bits < 1 || bits > 4 || !thresholds || !table) return TQ_ERR_ARG;
+    const int nt = (1 << bits) - 1;
+    if (bits == 4) return value_buckets4(thresholds, nt, table) ? TQ_OK : TQ_ERR_UNSUPPORTED;
+    std::vector<RowsParams::Bucket> b(kRowsBuckets);
+    if (!value_buckets(thresholds, nt, b.data())) return TQ_ERR_UNSUPPORTED;
+    for (int i = 0; i < kRowsBuckets; ++i) {
+        table[2 * i] = b[i].t;
+        table[2 * i + 1] = b[i].k;
+    }
+    return TQ_OK;
+}
+
 tq_status tq_make_haar_rotation(int head_dim, uint64_t seed, float *Q) {
     if (!Q || !pow2(head_dim) || head_dim < 16 || head_dim > TQ_MAX_HEAD_DIM) return TQ_ERR_ARG;
     const int d = head_dim;

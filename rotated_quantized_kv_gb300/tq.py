@@ -15,6 +15,8 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
+
 import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libtq.so")
@@ -49,7 +51,7 @@ EXPORTED = ["tq_status_string", "tq_last_cuda_error", "tq_version", "tq_make_rot
             "tq_age_tiers", "tq_decode_workspace_size", "tq_decode_attention",
             "tq_set_decode_kernel_events", "tq_decode_attention_static", "tq_decode_error_flag",
             "tq_requantize", "tq_fit_codebook_sphere", "tq_make_haar_rotation", "tq_compress_error_flag", "tq_decode_last_launches",
-            "tq_set_decode_wait_polls"]
+            "tq_set_decode_wait_polls", "tq_value_code_table"]
 
 
 class TQError(RuntimeError):
@@ -107,6 +109,7 @@ _lib.tq_decode_last_launches.argtypes = []
 _lib.tq_make_rotation.argtypes = [_I, ctypes.c_uint64, ctypes.POINTER(tq_rotation)]
 _lib.tq_fit_codebook.argtypes = [_I, _P, _P]
 _lib.tq_fit_codebook_sphere.argtypes = [_I, _I, _P, _P]
+_lib.tq_value_code_table.argtypes = [_I, _P, _P]
 _lib.tq_make_haar_rotation.argtypes = [_I, ctypes.c_uint64, _P]
 _lib.tq_compress_error_flag.argtypes = [ctypes.POINTER(ctypes.c_int), _I]
 _lib.tq_make_qjl.argtypes = [_I, _I, ctypes.c_uint64, _P]
@@ -170,6 +173,15 @@ def tq_fit_codebook(bits: int):
     t = torch.zeros(max((1 << bits) - 1, 1), dtype=torch.float32)
     _check(_lib.tq_fit_codebook(bits, c.data_ptr(), t.data_ptr()), "tq_fit_codebook")
     return c, t[: (1 << bits) - 1]
+
+
+def tq_value_code_table(bits: int, thresholds) -> np.ndarray:
+    """The compressor's value-code lookup table (2048 uint32) for 1-4 bits and
+    an ascending binary32 threshold set (see include/tq.h)."""
+    t = np.ascontiguousarray(np.asarray(thresholds, dtype=np.float32))
+    out = np.zeros(2048, dtype=np.uint32)
+    _check(_lib.tq_value_code_table(bits, t.ctypes.data, out.ctypes.data), "tq_value_code_table")
+    return out
 
 
 def tq_fit_codebook_sphere(bits: int, head_dim: int = 128):
