@@ -62,8 +62,12 @@ def test_traffic_follows_the_kernel_sources(monkeypatch):
     assert bench.traffic_for("no_such_workload", 1) is None
 
 
+TRAFFIC_FILES = ("decode_packed_w2_traffic.json", "decode_packed_w5_traffic.json",
+                 "decode_packed_w5_d256_traffic.json", "decode_packed_w5_d64_traffic.json")
+
+
 def test_committed_traffic_files_are_consistent():
-    for name in ("decode_packed_w2_traffic.json", "decode_packed_w5_traffic.json"):
+    for name in TRAFFIC_FILES:
         t = json.load(open(os.path.join(ROOT, "profiles", name)))
         assert tuple(t["source_files"]) == tuple(bench.DECODE_SRCS)
         assert len(t["source_sha256"]) == 64
@@ -75,3 +79,15 @@ def test_committed_traffic_files_are_consistent():
         # DRAM traffic within 2% of the algorithmic bytes: no re-reads
         assert 1.0 <= t["traffic_ratio"] < 1.02
         assert t["command"].startswith("ncu ") and "--clock-control none" in t["command"]
+
+
+def test_committed_traffic_files_match_the_committed_kernel():
+    """Every committed capture was taken on the decode sources as committed, so
+    the benchmark's roofline carries a traffic figure; a change to those
+    sources needs a new capture (and this fails until it is taken)."""
+    sha = bench.kernel_sha()
+    for name in TRAFFIC_FILES:
+        t = json.load(open(os.path.join(ROOT, "profiles", name)))
+        assert t["source_sha256"] == sha, name
+    assert bench.traffic_for("w5", 69656903680) is not None
+    assert bench.traffic_for("w5", 8674344960, 256) is not None
